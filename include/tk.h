@@ -1,0 +1,217 @@
+/*
+ * tk.h -- C ABI of the GB300 persistent training-step kernel (libtk.so).
+ *
+ * One functional training step (forward addmm/relu, loss, explicit backward
+ * mm/threshold_backward, bias column sums, in-place parameter update) is given
+ * as a static op list in topological order.  tk_program_create plans it once
+ * (op order, inlining of single-use pointwise values, GEMM epilogue chains,
+ * workspace arena, grid-barrier placement) and uploads a device op table;
+ * tk_run launches ONE cooperative persistent kernel that walks the op table
+ * stage by stage with a grid-wide barrier between dependent stages.
+ *
+ * The statement of the problem follows trainkernel (pages "trainkernel 0.1.0 --
+ * trainkernel/codegen.py" and "trainkernel/runtime.py"):
+ *   - tensors are TensorSpec views (buffer, shape, element strides, element
+ *     offset, dtype) -- codegen.py, `_Generator.read` / `coords`;
+ *   - the op set is the pointwise set {add, sub, mul, div, neg, relu, pow,
+ *     threshold_backward, full, cast}, mm/addmm and sum/mean -- codegen.py
+ *     `_POINTWISE`, `emit_mm`, `emit_reduction`;
+ *   - every op computes in float32 and rounds its result to its output dtype
+ *     (round to nearest even) -- codegen.py `_round`, `store`;
+ *   - `allocate` sizes a float32 workspace and binds in-place outputs to their
+ *     inputs; `run_into` checks buffers and launches -- runtime.py
+ *     `CompiledProgram.allocate` / `run_into` / `ExecutionBuffers`;
+ *   - in-place outputs map an output slot to the input it overwrites --
+ *     codegen.py `generate(..., inplace_outputs=...)`.
+ *
+ * Conventions for every entry point:
+ *   - Device memory is owned by the caller (inputs, outputs, workspace).  The
+ *     library owns the plan and its device op table.
+ *   - Every pointer argument documented as "device" must be a device address on
+ *     the program's device, 16-byte aligned when non-NULL.
+ *   - `stream` is a cudaStream_t (CUstream) handle passed as void*; NULL means
+ *     the legacy default stream.  Calls that take a stream are asynchronous.
+ *   - A non-zero tk_status means nothing was launched; tk_last_error() then
+ *     returns a "tk: ..." message (thread-local, valid until the next call).
+ */
+#ifndef TK_H
+#define TK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TK_MAX_RANK 4
+#define TK_MAX_OPERANDS 3
+#define TK_MAX_IO 256
+
+typedef enum {
+  TK_OK = 0,
+  TK_ERR_INVALID = 1,          /* malformed program, argument or buffer */
+  TK_ERR_UNSUPPORTED = 2,      /* well-formed but outside the supported subset */
+  TK_ERR_WORKSPACE = 3,        /* workspace missing or smaller than tk_allocate says */
+  TK_ERR_ALIAS = 4,            /* outputs/workspace overlap inputs or each other */
+  TK_ERR_CUDA = 5,             /* a CUDA runtime call failed */
+  TK_ERR_DEVICE = 6,           /* no usable device (or a plan-only program was run) */
+  TK_ERR_BARRIER_TIMEOUT = 7,  /* device status: a grid barrier wait ran out */
+  TK_ERR_PIPELINE_TIMEOUT = 8  /* device status: a tensor-core pipeline wait ran out */
+} tk_status;
+
+typedef enum { TK_F32 = 0, TK_F16 = 1, TK_BF16 = 2 } tk_dtype;
+
+typedef enum {
+  TK_OP_ADD = 0,                /* in0 + alpha*in1            (codegen.py point_expr) */
+  TK_OP_SUB = 1,                /* in0 - alpha*in1 */
+  TK_OP_MUL = 2,                /* in0 * in1 */
+  TK_OP_DIV = 3,                /* in0 / in1 (IEEE) */
+  TK_OP_NEG = 4,                /* -in0 */
+  TK_OP_RELU = 5,               /* in0 < 0 ? 0 : in0 */
+  TK_OP_POW = 6,                /* in0 ^ exponent (exponent: scalar in1, else attr) */
+  TK_OP_THRESHOLD_BACKWARD = 7, /* in1 <= threshold ? 0 : in0 */
+  TK_OP_FULL = 8,               /* value (scalar in0, else attr) */
+  TK_OP_CAST = 9,               /* in0, rounded to the output dtype */
+  TK_OP_MM = 10,                /* in0[m,k] @ in1[k,n]        (codegen.py emit_mm) */
+  TK_OP_ADDMM = 11,             /* alpha*(in1 @ in2) + beta*in0 (bias broadcast) */
+  TK_OP_SUM = 12,               /* sum of in0 over dims       (codegen.py emit_reduction) */
+  TK_OP_MEAN = 13               /* sum / float32(size); empty -> NaN */
+} tk_op_kind;
+
+/* A strided view of a buffer.  buffer_id names the buffer: a program input
+ * defines one, an op output defines one.  shape/strides/offset count elements;
+ * only the first `rank` entries are read.  An op's output view must be
+ * contiguous with offset 0 (it is the buffer). */
+typedef struct {
+  int32_t buffer_id;
+  int32_t rank;
+  int64_t shape[TK_MAX_RANK];
+  int64_t strides[TK_MAX_RANK];
+  int64_t offset;
+  int32_t dtype;               /* tk_dtype */
+  int32_t reserved;
+} tk_tensor_spec;
+
+/* One operation.  Operand i is scalars[i] (a float32 literal once rounded) when
+ * bit i of scalar_mask is set, else the view inputs[i].  Attributes the op does
+ * not use are ignored.  Reductions: n_dims == -1 reduces every dim, otherwise
+ * dims[0..n_dims) (negative dims count from the end). */
+typedef struct {
+  int32_t kind;                /* tk_op_kind */
+  int32_t n_inputs;
+  tk_tensor_spec inputs[TK_MAX_OPERANDS];
+  double scalars[TK_MAX_OPERANDS];
+  uint32_t scalar_mask;
+  int32_t n_dims;
+  int32_t dims[TK_MAX_RANK];
+  tk_tensor_spec output;
+  double alpha, beta, threshold, exponent, value;
+} tk_op;
+
+/* A whole program.  inplace holds n_inplace pairs {output_slot, input_index}:
+ * that output overwrites that input's storage (transactionally: every read of
+ * the old value happens first). */
+typedef struct {
+  int32_t n_inputs;
+  const tk_tensor_spec* inputs;
+  int32_t n_outputs;
+  const tk_tensor_spec* outputs;
+  int32_t n_ops;
+  const tk_op* ops;
+  int32_t n_inplace;
+  const int32_t* inplace;
+} tk_program_desc;
+
+/* Planner and launch options (codegen.py `generate` keyword knobs). */
+typedef struct {
+  int32_t blocks_per_sm;       /* upper bound on resident blocks per SM, 1..8 (default 1) */
+  int32_t max_blocks;          /* cap on the grid; <= 0: none */
+  int32_t fuse_pointwise;      /* inline single-use pointwise values (default 1) */
+  int32_t fuse_epilogues;      /* fuse pointwise chains into GEMM epilogues (default 1) */
+  int32_t inline_input_casts;  /* inline casts of program inputs (default 1) */
+  int32_t tensor_cores;        /* 1: tcgen05 path for eligible bf16/fp16 GEMMs (default 1) */
+  int32_t sm_count;            /* 0: query the device; > 0: SM count for a plan-only program */
+  int32_t reserved;
+  double barrier_timeout_s;    /* limit of every in-kernel wait (default 2.0) */
+} tk_options;
+
+/* What the planner decided (codegen.py `GeneratedKernel` counters). */
+typedef struct {
+  int32_t materialized_ops;    /* scheduled ops (a fused GEMM+chain counts once) */
+  int32_t inlined_ops;         /* pointwise values evaluated at their consumer */
+  int32_t fused_epilogues;     /* GEMMs carrying a pointwise chain */
+  int32_t tensor_core_ops;     /* GEMMs on the tcgen05 path */
+  int32_t stages;              /* barrier-separated stages */
+  int32_t grid_barriers;       /* = stages - 1 */
+  int32_t direct_outputs;      /* outputs written in place by their producer */
+  int32_t direct_state_commits;/* in-place outputs written directly (no commit copy) */
+  int32_t max_work_items;      /* largest stage, in work items */
+  int32_t grid_blocks;         /* blocks tk_run launches */
+  int32_t output_copies;       /* end-of-kernel copies and transactional commits */
+  int32_t split_reductions;    /* reductions done as partials + a final pass */
+  int64_t workspace_elements;  /* float32 elements tk_allocate reports */
+  int64_t arena_elements;      /* of which: intermediate-value arena */
+} tk_plan_stats;
+
+typedef struct tk_program tk_program;
+
+/* Fill *opt with the defaults above. */
+void tk_options_default(tk_options* opt);
+
+/* Validate and plan `desc` for `device` (a CUDA ordinal; -1 = plan only: no
+ * CUDA call is made and tk_run refuses the program).  `opt` may be NULL.  The
+ * descriptor is copied; the caller may free it on return.  On success *out owns
+ * the plan and must be released with tk_program_destroy. */
+tk_status tk_program_create(const tk_program_desc* desc, const tk_options* opt, int device,
+                            tk_program** out);
+
+/* Free a program and its device op table (NULL is ignored).  No run using it
+ * may still be pending. */
+void tk_program_destroy(tk_program* program);
+
+/* Size of the float32 workspace tk_run needs, in elements (>= 1).  Sizing
+ * only: the caller allocates (runtime.py `allocate`). */
+tk_status tk_allocate(const tk_program* program, size_t* workspace_elements);
+
+/* Zero the workspace header (barrier counter and status word) on `stream`.
+ * Required once for each new workspace and again after a run whose device
+ * status was not TK_OK; every successful run leaves the header ready for the
+ * next one. */
+tk_status tk_workspace_init(const tk_program* program, float* workspace, size_t workspace_elements,
+                            void* stream);
+
+/* Launch one step on `stream`.  inputs[i] / outputs[j] are device base
+ * addresses of the program's inputs / outputs (element (c) of a view lives at
+ * base + offset + sum(c*stride)).  An in-place output must be given exactly its
+ * input's pointer; otherwise outputs must not overlap each other, the
+ * workspace or any input, and the workspace must not overlap an input
+ * (runtime.py `run_into`).  workspace: device, >= tk_allocate elements,
+ * header initialised by tk_workspace_init.  Asynchronous; errors found on the
+ * host return before anything is launched. */
+tk_status tk_run(tk_program* program, const void* const* inputs, int32_t n_inputs,
+                 void* const* outputs, int32_t n_outputs, float* workspace,
+                 size_t workspace_elements, void* stream);
+
+/* Synchronise `stream` and read the device status word a run left in the
+ * workspace header: TK_OK, TK_ERR_BARRIER_TIMEOUT or TK_ERR_PIPELINE_TIMEOUT,
+ * with the stage where the wait gave up in *stage (may be NULL). */
+tk_status tk_run_status(const tk_program* program, const float* workspace, void* stream,
+                        int32_t* device_status, int32_t* stage);
+
+/* Kernel resources (codegen.py `resource_usage`): out[0] registers per thread,
+ * out[1] local bytes per thread, out[2] shared bytes per block (static +
+ * dynamic), out[3] resident blocks per SM. */
+tk_status tk_resource_usage(const tk_program* program, int64_t out[4]);
+
+/* Planner decisions for tests and reports. */
+tk_status tk_plan_stats_get(const tk_program* program, tk_plan_stats* stats);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char* tk_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TK_H */

@@ -1,0 +1,1224 @@
+// Host planner for the persistent training-step kernel.
+//
+// The planning rules follow trainkernel's generator (page "trainkernel 0.1.0
+// -- trainkernel/codegen.py", class `_Generator`): operations run in the given
+// topological order; a GEMM whose result feeds a chain of single-user,
+// shape-preserving pointwise ops writes the chain's last value from its tile
+// (`__init__`, epilogue detection); a pointwise value with one consumer is
+// recomputed at that consumer (`self.inline`); an in-place output is written
+// straight into its input when no later op reads that input (`direct_aliases`),
+// otherwise it is committed after the last read (`generate`, transactional
+// commit); intermediates live in a best-fit arena that recycles a slot after
+// its last reader (`_plan_workspace`); and a grid barrier is placed only where
+// a read-after-write, write-after-write or write-after-read overlap -- arena
+// reuse included -- would otherwise occur inside a stage (`generate`).
+//
+// What differs, and why (GB300 build):
+//   * one hand-written kernel interprets a device op table instead of a
+//     generated kernel per program, so every expression is lowered to a small
+//     register program (Instr) evaluated per element;
+//   * low-precision intermediates are stored packed in their own dtype inside
+//     the float32-sized workspace (half the bytes; values are already rounded);
+//   * a value consumed as a GEMM A/B operand is never inlined (TMA and the
+//     shared-memory staging read memory), and an expression needing more than
+//     kVmRegs registers keeps its operands materialised;
+//   * a split reduction keeps its own partial-sum slots and costs one barrier
+//     between its partial and final passes; the pass after it joins the normal
+//     hazard analysis.
+#include "planner.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <set>
+#include <unordered_map>
+
+namespace tkp {
+namespace {
+
+using tkd::Instr;
+using tkd::Ref;
+using tkd::Stage;
+using tkd::Task;
+using Shape = std::vector<int64_t>;
+
+bool is_pointwise(int k) { return k >= TK_OP_ADD && k <= TK_OP_CAST; }
+bool is_mm(int k) { return k == TK_OP_MM || k == TK_OP_ADDMM; }
+bool is_red(int k) { return k == TK_OP_SUM || k == TK_OP_MEAN; }
+int64_t esize(int dt) { return dt == TK_F32 ? 4 : 2; }
+
+Shape shape_of(const tk_tensor_spec& s) { return Shape(s.shape, s.shape + s.rank); }
+Shape strides_of(const tk_tensor_spec& s) { return Shape(s.strides, s.strides + s.rank); }
+int64_t numel_of(const Shape& sh) {
+  int64_t n = 1;
+  for (auto v : sh) n *= v;
+  return n;
+}
+int64_t numel(const tk_tensor_spec& s) { return numel_of(shape_of(s)); }
+Shape contig(const Shape& sh) {
+  Shape st(sh.size());
+  int64_t a = 1;
+  for (int d = int(sh.size()) - 1; d >= 0; --d) {
+    st[d] = a;
+    a *= sh[d];
+  }
+  return st;
+}
+bool exact_contig(const tk_tensor_spec& s) { return s.offset == 0 && strides_of(s) == contig(shape_of(s)); }
+bool relaxed_contig(const tk_tensor_spec& s) {
+  Shape c = contig(shape_of(s));
+  for (int d = 0; d < s.rank; ++d)
+    if (s.shape[d] > 1 && s.strides[d] != c[d]) return false;
+  return s.offset == 0;
+}
+// Elements a view can address: max index + 1 (0 for an empty view).
+int64_t extent_of(const tk_tensor_spec& s) {
+  if (numel(s) == 0) return 0;
+  int64_t m = s.offset;
+  for (int d = 0; d < s.rank; ++d) m += (s.shape[d] - 1) * s.strides[d];
+  return m + 1;
+}
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Operand {
+  bool scalar = false;
+  double value = 0.0;
+  tk_tensor_spec t{};
+};
+
+struct OpInfo {
+  int index = 0;
+  int kind = 0;
+  std::vector<Operand> in;
+  tk_tensor_spec out{};
+  double alpha = 1, beta = 1, threshold = 0, exponent = 2, value = 0;
+  int n_dims = -1;
+  int dims[TK_MAX_RANK] = {0, 0, 0, 0};
+};
+
+struct Buf {
+  int dtype = 0;
+  Shape shape;
+  int64_t extent = 0;
+  int producer = -1;  // op index
+  int input = -1;     // program input index
+  std::vector<int> users;
+};
+
+struct Region {
+  int space, slot;
+  int64_t lo, hi;
+};
+bool overlap(const Region& a, const Region& b) {
+  return a.space == b.space && a.slot == b.slot && a.lo < b.hi && b.lo < a.hi;
+}
+
+// Raised while lowering when an expression needs too many registers; the
+// named inlined value is materialised instead and planning restarts.
+struct RegisterOverflow {
+  int buffer;
+};
+
+float f32(double v) { return static_cast<float>(v); }
+
+class Planner {
+ public:
+  Planner(const tk_program_desc& d, const tk_options& o, int sms) : opt_(o), sms_(std::max(sms, 1)) {
+    read_desc(d);
+  }
+
+  Plan run() {
+    for (int attempt = 0;; ++attempt) {
+      try {
+        return plan_once();
+      } catch (const RegisterOverflow& r) {
+        if (attempt > 256) throw Error(TK_ERR_UNSUPPORTED, "expression too deep to evaluate inline");
+        no_inline_.insert(r.buffer);
+      }
+    }
+  }
+
+ private:
+  tk_options opt_;
+  int sms_;
+  std::vector<OpInfo> ops_;
+  std::vector<tk_tensor_spec> inputs_, outputs_;
+  std::map<int, int> inplace_;  // output slot -> input index
+  std::unordered_map<int, Buf> bufs_;
+  std::set<int> output_buffers_;
+  std::set<int> no_inline_;
+
+  // per-attempt decisions
+  struct Fused {
+    std::vector<int> chain;
+    int final_buf;
+  };
+  std::map<int, Fused> fused_;          // mm op index -> chain
+  std::set<int> fused_skip_;            // buffers a fused GEMM makes unnecessary
+  std::set<int> inline_;                // buffers evaluated at their consumer
+  std::vector<int> schedule_;           // op indices (a fused mm stands for its chain)
+  std::map<int, int> writer_;           // buffer -> scheduled op that stores it
+  std::map<int, int> direct_;           // output slot -> input index, written directly
+  std::map<int, int> binding_;          // buffer -> output slot it is written into
+  std::map<int, int64_t> arena_off_;    // buffer -> arena offset (float units)
+  std::map<int, int64_t> arena_units_;  // buffer -> units used
+  int64_t arena_total_ = 0;
+
+  // ---------------------------------------------------------------- input
+
+  static void check_spec(const tk_tensor_spec& s) {
+    if (s.rank < 0 || s.rank > TK_MAX_RANK) throw Error(TK_ERR_UNSUPPORTED, "tensor rank must be 0..4");
+    for (int d = 0; d < s.rank; ++d)
+      if (s.shape[d] < 0 || s.strides[d] < 0) throw Error(TK_ERR_INVALID, "invalid static shape or stride");
+    if (s.offset < 0) throw Error(TK_ERR_INVALID, "invalid static offset");
+    if (s.dtype < TK_F32 || s.dtype > TK_BF16) throw Error(TK_ERR_UNSUPPORTED, "unsupported dtype");
+  }
+
+  void check_view(const tk_tensor_spec& v) {
+    check_spec(v);
+    auto it = bufs_.find(v.buffer_id);
+    if (it == bufs_.end())
+      throw Error(TK_ERR_INVALID, "operation reads buffer " + std::to_string(v.buffer_id) +
+                                      " before it is defined (ops must be in topological order)");
+    if (v.dtype != it->second.dtype) throw Error(TK_ERR_INVALID, "a view must have its buffer's dtype");
+    if (extent_of(v) > it->second.extent) throw Error(TK_ERR_INVALID, "view reads past the end of its buffer");
+  }
+
+  static void check_scalar(double v) {
+    if (!std::isfinite(v)) throw Error(TK_ERR_UNSUPPORTED, "non-finite scalar constants are unsupported");
+  }
+
+  static void check_broadcast(const tk_tensor_spec& operand, const Shape& out) {
+    if (operand.rank > int(out.size())) throw Error(TK_ERR_INVALID, "invalid broadcast rank");
+    for (int d = 0; d < operand.rank; ++d) {
+      int64_t want = out[d + out.size() - operand.rank];
+      if (operand.shape[d] != 1 && operand.shape[d] != want)
+        throw Error(TK_ERR_INVALID, "incompatible broadcast dimensions");
+    }
+  }
+
+  void read_desc(const tk_program_desc& d) {
+    if (d.n_inputs < 0 || d.n_outputs < 0 || d.n_ops < 0 || d.n_inplace < 0)
+      throw Error(TK_ERR_INVALID, "negative count in program descriptor");
+    if (d.n_inputs > tkd::kMaxIO || d.n_outputs > tkd::kMaxIO)
+      throw Error(TK_ERR_UNSUPPORTED, "at most 256 inputs and 256 outputs");
+    if ((d.n_inputs && !d.inputs) || (d.n_outputs && !d.outputs) || (d.n_ops && !d.ops) ||
+        (d.n_inplace && !d.inplace))
+      throw Error(TK_ERR_INVALID, "NULL array in program descriptor");
+    for (int i = 0; i < d.n_inputs; ++i) {
+      const auto& s = d.inputs[i];
+      check_spec(s);
+      if (bufs_.count(s.buffer_id)) throw Error(TK_ERR_INVALID, "buffer defined twice");
+      Buf b;
+      b.dtype = s.dtype;
+      b.shape = shape_of(s);
+      b.extent = extent_of(s);
+      b.input = i;
+      bufs_[s.buffer_id] = b;
+      inputs_.push_back(s);
+    }
+    for (int i = 0; i < d.n_ops; ++i) {
+      const tk_op& src = d.ops[i];
+      OpInfo op;
+      op.index = i;
+      op.kind = src.kind;
+      if (op.kind < TK_OP_ADD || op.kind > TK_OP_MEAN) throw Error(TK_ERR_UNSUPPORTED, "unsupported operation");
+      if (src.n_inputs < 0 || src.n_inputs > TK_MAX_OPERANDS) throw Error(TK_ERR_INVALID, "bad operand count");
+      op.alpha = src.alpha;
+      op.beta = src.beta;
+      op.threshold = src.threshold;
+      op.exponent = src.exponent;
+      op.value = src.value;
+      op.n_dims = src.n_dims;
+      for (int j = 0; j < TK_MAX_RANK; ++j) op.dims[j] = src.dims[j];
+      for (int j = 0; j < src.n_inputs; ++j) {
+        Operand o;
+        if (src.scalar_mask & (1u << j)) {
+          o.scalar = true;
+          o.value = src.scalars[j];
+          check_scalar(o.value);
+        } else {
+          o.t = src.inputs[j];
+          check_view(o.t);
+        }
+        op.in.push_back(o);
+      }
+      op.out = src.output;
+      check_spec(op.out);
+      if (bufs_.count(op.out.buffer_id)) throw Error(TK_ERR_INVALID, "buffer defined twice");
+      if (!relaxed_contig(op.out))
+        throw Error(TK_ERR_INVALID, "materialized output must be contiguous: op " + std::to_string(i));
+      check_op(op);
+      Buf b;
+      b.dtype = op.out.dtype;
+      b.shape = shape_of(op.out);
+      b.extent = numel(op.out);
+      b.producer = i;
+      bufs_[op.out.buffer_id] = b;
+      for (const auto& o : op.in)
+        if (!o.scalar) bufs_[o.t.buffer_id].users.push_back(i);
+      ops_.push_back(op);
+    }
+    for (int j = 0; j < d.n_outputs; ++j) {
+      const auto& s = d.outputs[j];
+      check_view(s);
+      outputs_.push_back(s);
+      output_buffers_.insert(s.buffer_id);
+    }
+    std::set<int> targets;
+    for (int k = 0; k < d.n_inplace; ++k) {
+      int slot = d.inplace[2 * k], idx = d.inplace[2 * k + 1];
+      if (slot < 0 || slot >= d.n_outputs || idx < 0 || idx >= d.n_inputs || inplace_.count(slot))
+        throw Error(TK_ERR_INVALID, "invalid inplace output/input index");
+      if (!targets.insert(idx).second) throw Error(TK_ERR_INVALID, "inplace outputs must target distinct inputs");
+      const auto &o = outputs_[slot], &in = inputs_[idx];
+      if (shape_of(o) != shape_of(in) || o.dtype != in.dtype || !exact_contig(in))
+        throw Error(TK_ERR_INVALID, "inplace output must match a contiguous input shape and dtype");
+      if (bufs_[o.buffer_id].producer < 0)
+        throw Error(TK_ERR_INVALID, "inplace outputs must be computed values, not input views");
+      inplace_[slot] = idx;
+    }
+  }
+
+  void check_op(OpInfo& op) {
+    const Shape out = shape_of(op.out);
+    auto need = [&](size_t lo, size_t hi) {
+      if (op.in.size() < lo || op.in.size() > hi) throw Error(TK_ERR_INVALID, "wrong operand count");
+    };
+    switch (op.kind) {
+      case TK_OP_ADD:
+      case TK_OP_SUB:
+        need(2, 2);
+        check_scalar(op.alpha);
+        break;
+      case TK_OP_MUL:
+      case TK_OP_DIV:
+        need(2, 2);
+        break;
+      case TK_OP_THRESHOLD_BACKWARD:
+        need(2, 2);
+        check_scalar(op.threshold);
+        break;
+      case TK_OP_NEG:
+      case TK_OP_RELU:
+      case TK_OP_CAST:
+        need(1, 1);
+        break;
+      case TK_OP_POW:
+        need(1, 2);
+        if (op.in.size() == 2 && !op.in[1].scalar) throw Error(TK_ERR_UNSUPPORTED, "pow exponent must be a scalar");
+        if (op.in.size() == 1) check_scalar(op.exponent);
+        if (op.in[0].scalar) throw Error(TK_ERR_UNSUPPORTED, "pow base must be a tensor");
+        break;
+      case TK_OP_FULL:
+        need(0, 1);
+        if (op.in.size() == 1 && !op.in[0].scalar) throw Error(TK_ERR_INVALID, "full takes a scalar value");
+        if (op.in.empty()) check_scalar(op.value);
+        break;
+      case TK_OP_MM:
+      case TK_OP_ADDMM: {
+        size_t base = op.kind == TK_OP_ADDMM ? 1 : 0;
+        need(base + 2, base + 2);
+        const Operand &a = op.in[base], &b = op.in[base + 1];
+        if (a.scalar || b.scalar || a.t.rank != 2 || b.t.rank != 2 || a.t.shape[1] != b.t.shape[0])
+          throw Error(TK_ERR_INVALID, "mm requires compatible rank-two tensors");
+        if (op.out.rank != 2 || op.out.shape[0] != a.t.shape[0] || op.out.shape[1] != b.t.shape[1])
+          throw Error(TK_ERR_INVALID, "matrix output shape does not match its inputs");
+        if (op.kind == TK_OP_ADDMM) {
+          check_scalar(op.alpha);
+          check_scalar(op.beta);
+          if (!op.in[0].scalar) check_broadcast(op.in[0].t, out);
+        }
+        return;
+      }
+      case TK_OP_SUM:
+      case TK_OP_MEAN: {
+        need(1, 1);
+        if (op.in[0].scalar) throw Error(TK_ERR_INVALID, "reduction requires a tensor");
+        const auto& s = op.in[0].t;
+        if (op.n_dims > TK_MAX_RANK || op.n_dims < -1) throw Error(TK_ERR_INVALID, "bad reduction dims");
+        if (op.n_dims > 0 && s.rank == 0) throw Error(TK_ERR_INVALID, "bad reduction dims");
+        for (int j = 0; j < op.n_dims; ++j)
+          if (op.dims[j] >= s.rank || op.dims[j] < -s.rank) throw Error(TK_ERR_INVALID, "bad reduction dims");
+        int64_t kept = 1;
+        std::vector<bool> red = reduced_mask(op);
+        for (int d = 0; d < s.rank; ++d)
+          if (!red[d]) kept *= s.shape[d];
+        if (kept != numel(op.out))
+          throw Error(TK_ERR_INVALID, "reduction output shape does not match its axes");
+        return;
+      }
+      default:
+        throw Error(TK_ERR_UNSUPPORTED, "unsupported operation");
+    }
+    for (const auto& o : op.in)
+      if (!o.scalar) check_broadcast(o.t, out);
+  }
+
+  static std::vector<bool> reduced_mask(const OpInfo& op) {
+    const auto& s = op.in[0].t;
+    std::vector<bool> red(s.rank, op.n_dims < 0);
+    for (int j = 0; j < op.n_dims; ++j) red[((op.dims[j] % s.rank) + s.rank) % s.rank] = true;
+    return red;
+  }
+
+  // ------------------------------------------------------------ decisions
+
+  // Is a view of an op's contiguous output an affine, per-dimension read of it?
+  // Returns, for each producer dim, the view dim that drives it (-1: index 0).
+  static bool compose_dims(const tk_tensor_spec& v, const Shape& prod_shape, std::vector<int>* view_dim_of) {
+    Shape c = contig(prod_shape);
+    std::vector<int> of(prod_shape.size(), -1);
+    if (v.offset != 0) return false;
+    for (int d = 0; d < v.rank; ++d) {
+      if (v.shape[d] <= 1) continue;
+      int found = -1;
+      for (int e = 0; e < int(prod_shape.size()); ++e)
+        if (prod_shape[e] > 1 && c[e] == v.strides[d]) found = e;
+      if (found < 0 || of[found] >= 0 || v.shape[d] > prod_shape[found]) return false;
+      of[found] = d;
+    }
+    if (view_dim_of) *view_dim_of = of;
+    return true;
+  }
+
+  bool reads_as_gemm_operand(int buffer) const {
+    for (int u : bufs_.at(buffer).users) {
+      const OpInfo& op = ops_[u];
+      if (!is_mm(op.kind)) continue;
+      size_t base = op.kind == TK_OP_ADDMM ? 1 : 0;
+      for (size_t j = base; j < base + 2; ++j)
+        if (!op.in[j].scalar && op.in[j].t.buffer_id == buffer) return true;
+    }
+    return false;
+  }
+
+  void detect_epilogues() {
+    if (!opt_.fuse_epilogues) return;
+    for (const OpInfo& mm : ops_) {
+      if (!is_mm(mm.kind) || output_buffers_.count(mm.out.buffer_id)) continue;
+      std::vector<int> chain, skipped;
+      int current = mm.out.buffer_id;
+      while (bufs_[current].users.size() == 1) {
+        const OpInfo& nxt = ops_[bufs_[current].users[0]];
+        if (!is_pointwise(nxt.kind) || output_buffers_.count(nxt.out.buffer_id)) break;
+        // The GEMM root must be read with its own logical layout.
+        bool any = false, ok = true;
+        for (const auto& o : nxt.in) {
+          if (o.scalar || o.t.buffer_id != current) continue;
+          any = true;
+          if (shape_of(o.t) != bufs_[current].shape || !exact_contig(o.t)) ok = false;
+        }
+        if (!any || !ok) break;
+        chain.push_back(nxt.index);
+        skipped.push_back(current);
+        current = nxt.out.buffer_id;
+        if (bufs_[current].users.size() != 1) break;
+      }
+      if (chain.empty()) continue;
+      bool safe = true;
+      std::set<int> chain_bufs = {mm.out.buffer_id};
+      for (int ci : chain) {
+        const auto& c = ops_[ci];
+        if (shape_of(c.out) != shape_of(mm.out) || !exact_contig(c.out)) safe = false;
+        chain_bufs.insert(c.out.buffer_id);
+      }
+      for (int ci : chain)
+        for (const auto& o : ops_[ci].in) {
+          if (o.scalar || chain_bufs.count(o.t.buffer_id)) continue;
+          if (!exact_contig(o.t)) safe = false;
+          int p = bufs_[o.t.buffer_id].producer;
+          if (p >= 0 && p >= mm.index) safe = false;
+        }
+      if (!safe) continue;
+      Fused f;
+      f.chain = chain;
+      f.final_buf = current;
+      fused_[mm.index] = f;
+      for (int b : skipped) fused_skip_.insert(b);
+      fused_skip_.insert(current);
+    }
+  }
+
+  bool is_chain_final(int buffer) const {
+    for (const auto& kv : fused_)
+      if (kv.second.final_buf == buffer) return true;
+    return false;
+  }
+
+  void choose_inline() {
+    if (!opt_.fuse_pointwise) return;
+    for (const OpInfo& op : ops_) {
+      int b = op.out.buffer_id;
+      if (!is_pointwise(op.kind) || output_buffers_.count(b) || is_chain_final(b) || no_inline_.count(b)) continue;
+      const Buf& buf = bufs_[b];
+      bool input_cast = opt_.inline_input_casts && op.kind == TK_OP_CAST && !op.in[0].scalar &&
+                        bufs_[op.in[0].t.buffer_id].input >= 0;
+      if (!(buf.users.size() == 1 || input_cast)) continue;
+      if (reads_as_gemm_operand(b)) continue;
+      bool composable = true;
+      for (int u : buf.users)
+        for (const auto& o : ops_[u].in)
+          if (!o.scalar && o.t.buffer_id == b && !compose_dims(o.t, buf.shape, nullptr)) composable = false;
+      if (!composable) continue;
+      inline_.insert(b);
+    }
+  }
+
+  int out_buffer_of(int op_index) const {
+    auto it = fused_.find(op_index);
+    return it != fused_.end() ? it->second.final_buf : ops_[op_index].out.buffer_id;
+  }
+
+  void build_schedule() {
+    for (const OpInfo& op : ops_) {
+      if (fused_.count(op.index)) {
+        schedule_.push_back(op.index);
+      } else if (!fused_skip_.count(op.out.buffer_id) && !inline_.count(op.out.buffer_id)) {
+        schedule_.push_back(op.index);
+      }
+    }
+    for (int s : schedule_) writer_[out_buffer_of(s)] = s;
+  }
+
+  // Every tensor operand a scheduled op reads (GEMM + chain externals).
+  std::vector<tk_tensor_spec> reads_of(int op_index) const {
+    std::vector<tk_tensor_spec> r;
+    for (const auto& o : ops_[op_index].in)
+      if (!o.scalar) r.push_back(o.t);
+    auto it = fused_.find(op_index);
+    if (it != fused_.end()) {
+      std::set<int> chain_bufs = {ops_[op_index].out.buffer_id};
+      for (int ci : it->second.chain) chain_bufs.insert(ops_[ci].out.buffer_id);
+      for (int ci : it->second.chain)
+        for (const auto& o : ops_[ci].in)
+          if (!o.scalar && !chain_bufs.count(o.t.buffer_id)) r.push_back(o.t);
+    }
+    return r;
+  }
+
+  std::set<int> raw_inputs(int buffer) const {
+    const Buf& b = bufs_.at(buffer);
+    if (b.input >= 0) return {buffer};
+    std::set<int> r;
+    if (inline_.count(buffer))
+      for (const auto& o : ops_[b.producer].in)
+        if (!o.scalar) {
+          auto s = raw_inputs(o.t.buffer_id);
+          r.insert(s.begin(), s.end());
+        }
+    return r;
+  }
+
+  bool identity_access(const tk_tensor_spec& spec, int target, const Shape& shape) const {
+    if (!raw_inputs(spec.buffer_id).count(target)) return true;
+    if (shape_of(spec) != shape || !exact_contig(spec)) return false;
+    if (spec.buffer_id == target) return true;
+    for (const auto& o : ops_[bufs_.at(spec.buffer_id).producer].in)
+      if (!o.scalar && !identity_access(o.t, target, shape)) return false;
+    return true;
+  }
+
+  void choose_direct_aliases() {
+    std::map<int, int> out_count;
+    for (const auto& o : outputs_) out_count[o.buffer_id]++;
+    for (const auto& kv : inplace_) {
+      int slot = kv.first, idx = kv.second;
+      const auto& out = outputs_[slot];
+      int target = inputs_[idx].buffer_id;
+      int pos = -1;
+      for (size_t i = 0; i < schedule_.size(); ++i)
+        if (out_buffer_of(schedule_[i]) == out.buffer_id) pos = int(i);
+      if (pos < 0 || !is_pointwise(ops_[schedule_[pos]].kind) || fused_.count(schedule_[pos]) ||
+          out_count[out.buffer_id] != 1)
+        continue;
+      if (!exact_contig(out)) continue;
+      bool target_is_output = false;
+      for (const auto& o : outputs_)
+        if (o.buffer_id == target) target_is_output = true;
+      if (target_is_output) continue;
+      bool later_read = false;
+      for (size_t i = pos + 1; i < schedule_.size() && !later_read; ++i)
+        for (const auto& v : reads_of(schedule_[i]))
+          if (raw_inputs(v.buffer_id).count(target)) later_read = true;
+      if (later_read) continue;
+      bool ident = true;
+      for (const auto& v : reads_of(schedule_[pos]))
+        if (!identity_access(v, target, shape_of(out))) ident = false;
+      if (!ident) continue;
+      direct_[slot] = idx;
+    }
+  }
+
+  void choose_bindings() {
+    for (size_t j = 0; j < outputs_.size(); ++j) {
+      if (inplace_.count(int(j)) && !direct_.count(int(j))) continue;
+      const auto& spec = outputs_[j];
+      auto w = writer_.find(spec.buffer_id);
+      if (w == writer_.end()) continue;  // an input view: copied at the end
+      const Buf& b = bufs_[spec.buffer_id];
+      if (b.dtype == spec.dtype && relaxed_contig(spec) && numel(spec) == numel_of(b.shape))
+        binding_.emplace(spec.buffer_id, int(j));
+    }
+  }
+
+  int64_t units_of(int buffer) const {
+    const Buf& b = bufs_.at(buffer);
+    return ceil_div(numel_of(b.shape) * esize(b.dtype), 4);
+  }
+
+  std::set<int> roots(int buffer) const {
+    if (!inline_.count(buffer)) return {buffer};
+    std::set<int> r;
+    for (const auto& o : ops_[bufs_.at(buffer).producer].in)
+      if (!o.scalar) {
+        auto s = roots(o.t.buffer_id);
+        r.insert(s.begin(), s.end());
+      }
+    return r;
+  }
+
+  void plan_arena() {
+    std::map<int, int> last;
+    for (size_t i = 0; i < schedule_.size(); ++i)
+      for (const auto& v : reads_of(schedule_[i]))
+        for (int r : roots(v.buffer_id)) last[r] = int(i);
+    for (const auto& o : outputs_)
+      for (int r : roots(o.buffer_id)) last[r] = int(schedule_.size());
+    struct Slot {
+      int buf;
+      int64_t start, size;
+    };
+    std::vector<Slot> active;
+    std::vector<std::pair<int64_t, int64_t>> free_list;  // (start, size)
+    int64_t total = 0;
+    for (size_t i = 0; i < schedule_.size(); ++i) {
+      int b = out_buffer_of(schedule_[i]);
+      if (binding_.count(b)) continue;
+      std::vector<Slot> keep;
+      for (const auto& s : active) {
+        auto it = last.find(s.buf);
+        if ((it == last.end() ? -1 : it->second) < int(i))
+          free_list.push_back({s.start, s.size});
+        else
+          keep.push_back(s);
+      }
+      active = keep;
+      int64_t size = std::max<int64_t>(64, round_up(units_of(b), 64));
+      int best = -1;
+      for (size_t j = 0; j < free_list.size(); ++j) {
+        if (free_list[j].second < size) continue;
+        // smallest sufficient slot; on a tie the one freed first
+        if (best < 0 || free_list[j].second < free_list[best].second) best = int(j);
+      }
+      int64_t start;
+      if (best >= 0) {
+        start = free_list[best].first;
+        int64_t n = free_list[best].second;
+        free_list.erase(free_list.begin() + best);
+        if (n > size) free_list.push_back({start + size, n - size});
+      } else {
+        start = total;
+        total += size;
+      }
+      arena_off_[b] = start;
+      arena_units_[b] = units_of(b);
+      active.push_back({b, start, size});
+    }
+    arena_total_ = total;
+  }
+
+  // ------------------------------------------------------------ locations
+
+  // Where buffer b is stored: (space, slot, element base).
+  void location(int b, int* space, int* slot, int64_t* base) const {
+    const Buf& buf = bufs_.at(b);
+    if (buf.input >= 0) {
+      *space = tkd::SP_IN;
+      *slot = buf.input;
+      *base = 0;
+      return;
+    }
+    auto bind = binding_.find(b);
+    if (bind != binding_.end()) {
+      *space = tkd::SP_OUT;
+      *slot = bind->second;
+      *base = 0;
+      return;
+    }
+    auto it = arena_off_.find(b);
+    if (it == arena_off_.end()) throw Error(TK_ERR_INVALID, "internal: value has no storage");
+    *space = tkd::SP_WS;
+    *slot = 0;
+    *base = (tkd::kHeaderUnits + it->second) * 4 / esize(buf.dtype);
+  }
+
+  Region storage_region(int b) const {
+    const Buf& buf = bufs_.at(b);
+    if (buf.input >= 0) return {tkd::SP_IN, buf.input, 0, buf.extent};
+    auto bind = binding_.find(b);
+    if (bind != binding_.end()) {
+      auto d = direct_.find(bind->second);
+      if (d != direct_.end()) return {tkd::SP_IN, d->second, 0, bufs_.at(inputs_[d->second].buffer_id).extent};
+      return {tkd::SP_OUT, bind->second, 0, numel(outputs_[bind->second])};
+    }
+    int64_t off = arena_off_.at(b);
+    return {tkd::SP_WS, 0, off, off + arena_units_.at(b)};
+  }
+
+  void read_regions(const tk_tensor_spec& v, std::vector<Region>& out) const {
+    if (inline_.count(v.buffer_id)) {
+      for (const auto& o : ops_[bufs_.at(v.buffer_id).producer].in)
+        if (!o.scalar) read_regions(o.t, out);
+      return;
+    }
+    const Buf& b = bufs_.at(v.buffer_id);
+    if (b.input >= 0) {
+      if (!direct_.empty()) out.push_back({tkd::SP_IN, b.input, 0, b.extent});
+      return;
+    }
+    out.push_back(storage_region(v.buffer_id));
+  }
+
+  // ------------------------------------------------------------ lowering
+
+  struct Emit {
+    Plan* plan;
+    const Planner* P;
+    int task_ref_begin;
+    Shape space;
+    int root_buf = -1;
+    int max_reg = 0;
+
+    void push(uint8_t op, int dst, int a, int b, int round, float imm = 0.f, int ref = -1) {
+      if (dst >= tkd::kVmRegs || a >= tkd::kVmRegs || b >= tkd::kVmRegs) throw RegisterOverflow{-1};
+      Instr in{};
+      in.op = op;
+      in.dst = uint8_t(dst);
+      in.a = uint8_t(a);
+      in.b = uint8_t(b);
+      in.round = uint8_t(round);
+      in.imm = imm;
+      in.ref = ref;
+      plan->code.push_back(in);
+      max_reg = std::max(max_reg, std::max(dst, std::max(a, b)));
+    }
+
+    int add_ref(const tk_tensor_spec& v, const std::vector<int>& dimmap) {
+      Ref r{};
+      int64_t base;
+      P->location(v.buffer_id, &r.space, &r.slot, &base);
+      r.dtype = v.dtype;
+      r.base = base + v.offset;
+      for (int d = 0; d < v.rank; ++d)
+        if (v.shape[d] > 1 && dimmap[d] >= 0) r.stride[dimmap[d]] += v.strides[d];
+      plan->refs.push_back(r);
+      return int(plan->refs.size()) - 1 - task_ref_begin;
+    }
+
+    // Value of view v into register r; dimmap[d] = index dim driving view dim d.
+    void value(const tk_tensor_spec& v, const std::vector<int>& dimmap, int r) {
+      if (v.buffer_id == root_buf) {
+        if (r != 0) push(tkd::OP_MOV, r, 0, 0, TK_F32);
+        return;
+      }
+      if (P->inline_.count(v.buffer_id)) {
+        const Buf& b = P->bufs_.at(v.buffer_id);
+        std::vector<int> of;
+        if (!compose_dims(v, b.shape, &of)) throw Error(TK_ERR_INVALID, "internal: non-affine inline view");
+        std::vector<int> pmap(b.shape.size(), -1);
+        for (size_t e = 0; e < of.size(); ++e) pmap[e] = of[e] >= 0 ? dimmap[of[e]] : -1;
+        try {
+          op_value(P->ops_[b.producer], pmap, r);
+        } catch (const RegisterOverflow&) {
+          throw RegisterOverflow{v.buffer_id};
+        }
+        return;
+      }
+      push(tkd::OP_LOAD, r, 0, 0, TK_F32, 0.f, add_ref(v, dimmap));
+    }
+
+    // Value of pointwise op `op` into register r (temporaries above r);
+    // outmap[d] = index dim driving output dim d.
+    void op_value(const OpInfo& op, const std::vector<int>& outmap, int r) {
+      int rank = op.out.rank;
+      auto operand = [&](int j, int reg) {
+        const Operand& o = op.in[j];
+        if (o.scalar) {
+          push(tkd::OP_CONST, reg, 0, 0, TK_F32, f32(o.value));
+          return;
+        }
+        std::vector<int> m(o.t.rank, -1);
+        for (int d = 0; d < o.t.rank; ++d)
+          m[d] = o.t.shape[d] == 1 ? -1 : outmap[d + rank - o.t.rank];
+        value(o.t, m, reg);
+      };
+      int rd = op.out.dtype;
+      switch (op.kind) {
+        case TK_OP_ADD:
+        case TK_OP_SUB:
+        case TK_OP_MUL:
+        case TK_OP_DIV:
+        case TK_OP_THRESHOLD_BACKWARD: {
+          operand(0, r);
+          operand(1, r + 1);
+          uint8_t code = op.kind == TK_OP_ADD ? tkd::OP_ADD
+                         : op.kind == TK_OP_SUB ? tkd::OP_SUB
+                         : op.kind == TK_OP_MUL ? tkd::OP_MUL
+                         : op.kind == TK_OP_DIV ? tkd::OP_DIV
+                                                : tkd::OP_THRESH;
+          float imm = (op.kind == TK_OP_ADD || op.kind == TK_OP_SUB) ? f32(op.alpha)
+                      : op.kind == TK_OP_THRESHOLD_BACKWARD        ? f32(op.threshold)
+                                                                   : 0.f;
+          push(code, r, r, r + 1, rd, imm);
+          return;
+        }
+        case TK_OP_NEG:
+          operand(0, r);
+          push(tkd::OP_NEG, r, r, r, rd);
+          return;
+        case TK_OP_RELU:
+          operand(0, r);
+          push(tkd::OP_RELU, r, r, r, rd);
+          return;
+        case TK_OP_CAST:
+          operand(0, r);
+          push(tkd::OP_MOV, r, r, r, rd);
+          return;
+        case TK_OP_POW: {
+          double e = op.in.size() > 1 ? op.in[1].value : op.exponent;
+          operand(0, r);
+          if (e == 2.0)
+            push(tkd::OP_SQUARE, r, r, r, rd);
+          else
+            push(tkd::OP_POW, r, r, r, rd, f32(e));
+          return;
+        }
+        case TK_OP_FULL:
+          push(tkd::OP_CONST, r, 0, 0, rd, f32(op.in.empty() ? op.value : op.in[0].value));
+          return;
+        default:
+          throw Error(TK_ERR_INVALID, "internal: not a pointwise op");
+      }
+    }
+  };
+
+  static std::vector<int> identity_map(int rank) {
+    std::vector<int> m(rank);
+    for (int d = 0; d < rank; ++d) m[d] = d;
+    return m;
+  }
+
+  Task new_task(int kind, const Shape& space) const {
+    Task t{};
+    t.kind = kind;
+    t.rank = int(space.size());
+    for (int d = 0; d < t.rank; ++d) t.shape[d] = space[d];
+    t.numel = numel_of(space);
+    t.vec = (t.rank >= 1 && t.shape[t.rank - 1] % 8 == 0 && t.numel > 0) ? 8 : 1;
+    t.tma_a = t.tma_b = -1;
+    return t;
+  }
+
+  Ref out_ref(int buffer) const {
+    Ref r{};
+    int64_t base;
+    location(buffer, &r.space, &r.slot, &base);
+    r.dtype = bufs_.at(buffer).dtype;
+    r.base = base;
+    r.vmode = tkd::VM_CONTIG;
+    return r;
+  }
+
+  // Fill vector modes once the task's vector width is known.
+  void finish_refs(Plan& plan, Task& t) const {
+    for (int i = 0; i < t.n_refs; ++i) {
+      Ref& r = plan.refs[t.ref_begin + i];
+      r.vmode = tkd::VM_GATHER;
+      if (t.vec != 8 || t.rank == 0) continue;
+      int64_t s = r.stride[t.rank - 1];
+      if (s == 0) {
+        r.vmode = tkd::VM_BCAST;
+      } else if (s == 1 && r.base % 8 == 0) {
+        bool ok = true;
+        for (int d = 0; d < t.rank - 1; ++d)
+          if (r.stride[d] % 8) ok = false;
+        if (ok) r.vmode = tkd::VM_CONTIG;
+      }
+    }
+  }
+
+  int items_pointwise(const Task& t) const { return int(ceil_div(t.numel, int64_t(tkd::kThreads) * t.vec)); }
+
+  // A pointwise task computing `op` (or copying a view when op == nullptr).
+  Task lower_pointwise(Plan& plan, const OpInfo* op, const tk_tensor_spec* copy_src, const Shape& space,
+                       Ref out, int round) {
+    Task t = new_task(tkd::T_POINTWISE, space);
+    t.code_begin = int(plan.code.size());
+    t.ref_begin = int(plan.refs.size());
+    Emit e{&plan, this, t.ref_begin, space};
+    if (op) {
+      e.op_value(*op, identity_map(int(space.size())), 0);
+    } else {
+      e.value(*copy_src, identity_map(copy_src->rank), 0);
+      e.push(tkd::OP_MOV, 0, 0, 0, round);
+    }
+    t.code_len = int(plan.code.size()) - t.code_begin;
+    t.n_refs = int(plan.refs.size()) - t.ref_begin;
+    t.out = out;
+    finish_refs(plan, t);
+    t.n_items = items_pointwise(t);
+    return t;
+  }
+
+  Task lower_gemm(Plan& plan, const OpInfo& mm) {
+    size_t base = mm.kind == TK_OP_ADDMM ? 1 : 0;
+    const tk_tensor_spec &A = mm.in[base].t, &B = mm.in[base + 1].t;
+    int64_t M = A.shape[0], K = A.shape[1], N = B.shape[1];
+    Shape space = {M, N};
+    Task t = new_task(tkd::T_GEMM_SIMT, space);
+    t.m = int(M);
+    t.n = int(N);
+    t.k = int(K);
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) throw Error(TK_ERR_UNSUPPORTED, "GEMM too large");
+    auto operand_ref = [&](const tk_tensor_spec& v) {
+      Ref r{};
+      int64_t b;
+      location(v.buffer_id, &r.space, &r.slot, &b);
+      r.dtype = v.dtype;
+      r.base = b + v.offset;
+      r.stride[0] = v.strides[0];
+      r.stride[1] = v.strides[1];
+      return r;
+    };
+    t.a = operand_ref(A);
+    t.b = operand_ref(B);
+    t.a_kcontig = A.strides[1] == 1 || A.shape[0] <= 1;
+    t.b_ncontig = B.strides[1] == 1 || B.shape[0] <= 1;
+    // tile: the largest of 64/32/16 that still gives every SM a tile
+    int tile = 16;
+    for (int cand : {64, 32}) {
+      if (ceil_div(M, cand) * ceil_div(N, cand) >= sms_) {
+        tile = cand;
+        break;
+      }
+    }
+    t.tile_m = t.tile_n = tile;
+    t.tiles_n = int(ceil_div(N, tile));
+    t.n_items = int(ceil_div(M, tile) * ceil_div(N, tile));
+    if (M == 0 || N == 0) t.n_items = 0;
+
+    // epilogue: addmm formula, rounding to the GEMM dtype, then the chain
+    t.code_begin = int(plan.code.size());
+    t.ref_begin = int(plan.refs.size());
+    Emit e{&plan, this, t.ref_begin, space};
+    std::vector<int> idmap = identity_map(2);
+    int rd = mm.out.dtype;
+    if (mm.kind == TK_OP_MM) {
+      e.push(tkd::OP_ACC, 0, 0, 0, rd);
+    } else {
+      auto bias = [&](int reg) {
+        const Operand& o = mm.in[0];
+        if (o.scalar) {
+          e.push(tkd::OP_CONST, reg, 0, 0, TK_F32, f32(o.value));
+        } else {
+          std::vector<int> m(o.t.rank, -1);
+          for (int d = 0; d < o.t.rank; ++d) m[d] = o.t.shape[d] == 1 ? -1 : d + 2 - o.t.rank;
+          e.value(o.t, m, reg);
+        }
+      };
+      if (mm.alpha == 0.0 && mm.beta == 0.0) {
+        e.push(tkd::OP_CONST, 0, 0, 0, rd, 0.f);
+      } else if (mm.beta == 0.0) {
+        e.push(tkd::OP_ACC, 0, 0, 0, TK_F32);
+        e.push(tkd::OP_CONST, 1, 0, 0, TK_F32, f32(mm.alpha));
+        e.push(tkd::OP_MUL, 0, 0, 1, rd);
+      } else if (mm.alpha == 0.0) {
+        bias(0);
+        e.push(tkd::OP_CONST, 1, 0, 0, TK_F32, f32(mm.beta));
+        e.push(tkd::OP_MUL, 0, 0, 1, rd);
+      } else {
+        e.push(tkd::OP_ACC, 0, 0, 0, TK_F32);
+        if (mm.alpha != 1.0) {
+          e.push(tkd::OP_CONST, 1, 0, 0, TK_F32, f32(mm.alpha));
+          e.push(tkd::OP_MUL, 0, 0, 1, TK_F32);
+        }
+        bias(1);
+        if (mm.beta != 1.0) {
+          e.push(tkd::OP_CONST, 2, 0, 0, TK_F32, f32(mm.beta));
+          e.push(tkd::OP_MUL, 1, 1, 2, TK_F32);
+        }
+        e.push(tkd::OP_ADD, 0, 0, 1, rd, 1.0f);
+      }
+    }
+    int out_buf = mm.out.buffer_id;
+    auto it = fused_.find(mm.index);
+    if (it != fused_.end()) {
+      for (int ci : it->second.chain) {
+        const OpInfo& c = ops_[ci];
+        e.root_buf = out_buf;
+        // operands go to registers 1.., the running root stays in register 0
+        e.op_value(c, idmap, 1);
+        e.push(tkd::OP_MOV, 0, 1, 1, TK_F32);
+        out_buf = c.out.buffer_id;
+      }
+      e.root_buf = -1;
+    }
+    t.code_len = int(plan.code.size()) - t.code_begin;
+    t.n_refs = int(plan.refs.size()) - t.ref_begin;
+    t.out = out_ref(out_buf);
+    finish_refs(plan, t);
+    return t;
+  }
+
+  // Reduction as one task (parts == 1) or partials + a final task.
+  std::vector<Task> lower_reduction(Plan& plan, const OpInfo& op, int64_t* scratch_cursor) {
+    const tk_tensor_spec& src = op.in[0].t;
+    std::vector<bool> red = reduced_mask(op);
+    std::vector<int> kept, reduced;
+    for (int d = 0; d < src.rank; ++d) (red[d] ? reduced : kept).push_back(d);
+    bool row = src.rank == 0 || red[src.rank - 1];
+    std::vector<int> perm;
+    if (row) {
+      perm = kept;
+      perm.insert(perm.end(), reduced.begin(), reduced.end());
+    } else {
+      perm = reduced;
+      perm.insert(perm.end(), kept.begin(), kept.end());
+    }
+    Shape space;
+    for (int d : perm) space.push_back(src.shape[d]);
+    std::vector<int> dimmap(src.rank);
+    for (size_t j = 0; j < perm.size(); ++j) dimmap[perm[j]] = int(j);
+    int64_t n_out = 1, n_red = 1;
+    for (int d : kept) n_out *= src.shape[d];
+    for (int d : reduced) n_red *= src.shape[d];
+
+    Task t = new_task(row ? tkd::T_REDUCE_ROW : tkd::T_REDUCE_COL, space);
+    t.code_begin = int(plan.code.size());
+    t.ref_begin = int(plan.refs.size());
+    Emit e{&plan, this, t.ref_begin, space};
+    e.value(src, dimmap, 0);
+    t.code_len = int(plan.code.size()) - t.code_begin;
+    t.n_refs = int(plan.refs.size()) - t.ref_begin;
+    t.out = out_ref(op.out.buffer_id);
+    t.red_mean = op.kind == TK_OP_MEAN;
+    t.size_f = float(double(n_red));
+    if (row) {
+      // vectors run along the reduced dims: the innermost index dim is reduced
+      t.vec = (!reduced.empty() && src.shape[src.rank - 1] % 8 == 0 && n_red > 0) ? 8 : 1;
+      t.red_outer = n_out;
+      t.red_inner = n_red;
+      int64_t parts = 1;
+      if (n_out < sms_ && n_red > 16384) {
+        parts = std::min<int64_t>(ceil_div(n_red, 8192), std::max<int64_t>(1, ceil_div(2 * sms_, n_out)));
+        parts = std::min<int64_t>(parts, 1024);
+      }
+      int64_t step = int64_t(tkd::kThreads) * t.vec;
+      t.part_len = round_up(ceil_div(std::max<int64_t>(n_red, 1), parts), step);
+      t.parts = int(ceil_div(std::max<int64_t>(n_red, 1), t.part_len));
+      t.n_items = int(n_out * t.parts);
+    } else {
+      t.red_outer = n_red;
+      t.red_inner = n_out;
+      int64_t cw = 32 * t.vec;
+      int64_t chunks = ceil_div(n_out, cw);
+      int64_t parts = 1;
+      if (chunks < sms_ / 2 && n_red > 512)
+        parts = std::min<int64_t>(ceil_div(n_red, 128), std::max<int64_t>(1, ceil_div(2 * sms_, chunks)));
+      t.part_len = ceil_div(std::max<int64_t>(n_red, 1), parts);
+      t.parts = int(ceil_div(std::max<int64_t>(n_red, 1), t.part_len));
+      t.n_items = int(chunks * t.parts);
+    }
+    finish_refs(plan, t);
+    if (n_out == 0) t.n_items = 0;
+    if (t.parts <= 1) {
+      t.parts = 1;
+      return {t};
+    }
+    t.scratch = tkd::kHeaderUnits + arena_total_ + *scratch_cursor;
+    *scratch_cursor += round_up(n_out * t.parts, 64);
+    Task f = new_task(tkd::T_REDUCE_FINAL, Shape{n_out});
+    f.out = t.out;
+    f.red_mean = t.red_mean;
+    f.size_f = t.size_f;
+    f.parts = t.parts;
+    f.scratch = t.scratch;
+    f.red_outer = n_out;
+    f.final_block = n_out < 64;
+    f.n_items = int(f.final_block ? n_out : ceil_div(n_out, tkd::kThreads));
+    f.code_begin = int(plan.code.size());
+    f.ref_begin = int(plan.refs.size());
+    return {t, f};
+  }
+
+  // ------------------------------------------------------------ the plan
+
+  Plan plan_once() {
+    fused_.clear();
+    fused_skip_.clear();
+    inline_.clear();
+    schedule_.clear();
+    writer_.clear();
+    direct_.clear();
+    binding_.clear();
+    arena_off_.clear();
+    arena_units_.clear();
+    arena_total_ = 0;
+
+    detect_epilogues();
+    choose_inline();
+    build_schedule();
+    choose_direct_aliases();
+    choose_bindings();
+    plan_arena();
+
+    Plan plan;
+    std::vector<std::vector<Task>> stages(1);
+    std::vector<Region> stage_reads, stage_writes;
+    int64_t scratch = 0;
+    int split = 0;
+    auto barrier = [&]() {
+      stages.emplace_back();
+      stage_reads.clear();
+      stage_writes.clear();
+    };
+    auto hazard = [&](const std::vector<Region>& reads, const std::vector<Region>& writes) {
+      for (const auto& w : stage_writes) {
+        for (const auto& r : reads)
+          if (overlap(w, r)) return true;
+        for (const auto& r : writes)
+          if (overlap(w, r)) return true;
+      }
+      for (const auto& r : stage_reads)
+        for (const auto& w : writes)
+          if (overlap(r, w)) return true;
+      return false;
+    };
+
+    for (int s : schedule_) {
+      const OpInfo& op = ops_[s];
+      std::vector<Region> reads, writes;
+      for (const auto& v : reads_of(s)) read_regions(v, reads);
+      writes.push_back(storage_region(out_buffer_of(s)));
+      if (is_red(op.kind)) {
+        std::vector<Task> ts = lower_reduction(plan, op, &scratch);
+        if (ts.size() == 2) {
+          ++split;
+          if (hazard(reads, {})) barrier();
+          stages.back().push_back(ts[0]);
+          stage_reads.insert(stage_reads.end(), reads.begin(), reads.end());
+          barrier();
+          stages.back().push_back(ts[1]);
+          stage_writes.insert(stage_writes.end(), writes.begin(), writes.end());
+          continue;
+        }
+        if (hazard(reads, writes)) barrier();
+        stages.back().push_back(ts[0]);
+      } else {
+        Task t = is_mm(op.kind) ? lower_gemm(plan, op)
+                                : lower_pointwise(plan, &op, nullptr, shape_of(op.out), out_ref(op.out.buffer_id),
+                                                  op.out.dtype);
+        if (hazard(reads, writes)) barrier();
+        stages.back().push_back(t);
+      }
+      stage_reads.insert(stage_reads.end(), reads.begin(), reads.end());
+      stage_writes.insert(stage_writes.end(), writes.begin(), writes.end());
+    }
+
+    // End-of-kernel output copies, then transactional commits of in-place outputs.
+    int copies = 0;
+    bool needs_copy = false;
+    for (size_t j = 0; j < outputs_.size(); ++j) {
+      auto b = binding_.find(outputs_[j].buffer_id);
+      if (b == binding_.end() || b->second != int(j)) needs_copy = true;
+    }
+    if (!stage_writes.empty() && needs_copy) barrier();
+    bool copied = false;
+    for (size_t j = 0; j < outputs_.size(); ++j) {
+      if (inplace_.count(int(j))) continue;
+      auto b = binding_.find(outputs_[j].buffer_id);
+      if (b != binding_.end() && b->second == int(j)) continue;
+      Ref out{};
+      out.space = tkd::SP_OUT;
+      out.slot = int(j);
+      out.dtype = outputs_[j].dtype;
+      stages.back().push_back(
+          lower_pointwise(plan, nullptr, &outputs_[j], shape_of(outputs_[j]), out, outputs_[j].dtype));
+      copied = true;
+      ++copies;
+    }
+    if (!inplace_.empty()) {
+      bool any_commit = false;
+      for (const auto& kv : inplace_)
+        if (!direct_.count(kv.first)) any_commit = true;
+      if (any_commit && copied) barrier();
+      for (const auto& kv : inplace_) {
+        if (direct_.count(kv.first)) continue;
+        const auto& spec = outputs_[kv.first];
+        Ref out{};
+        out.space = tkd::SP_OUT;
+        out.slot = kv.first;
+        out.dtype = spec.dtype;
+        stages.back().push_back(lower_pointwise(plan, nullptr, &spec, shape_of(spec), out, spec.dtype));
+        ++copies;
+      }
+    }
+    while (stages.size() > 1 && stages.back().empty()) stages.pop_back();
+
+    // Flatten: tensor-core tasks first inside each stage.
+    int tc_ops = 0;
+    for (auto& st : stages) {
+      std::stable_sort(st.begin(), st.end(), [](const Task& a, const Task& b) {
+        return (a.kind == tkd::T_GEMM_TC) > (b.kind == tkd::T_GEMM_TC);
+      });
+      Stage S{};
+      S.task_begin = int(plan.tasks.size());
+      for (auto& t : st) {
+        S.n_items += t.n_items;
+        if (t.kind == tkd::T_GEMM_TC) {
+          S.n_tc_items += t.n_items;
+          ++tc_ops;
+        }
+        plan.tasks.push_back(t);
+      }
+      S.task_end = int(plan.tasks.size());
+      plan.stages.push_back(S);
+      plan.max_items = std::max(plan.max_items, S.n_items);
+    }
+
+    plan.arena_units = arena_total_;
+    plan.workspace_units = tkd::kHeaderUnits + arena_total_ + scratch;
+    plan.uses_tc = tc_ops > 0;
+    for (const auto& s : inputs_) plan.input_bytes.push_back(extent_of(s) * esize(s.dtype));
+    for (const auto& s : outputs_) plan.output_bytes.push_back(numel(s) * esize(s.dtype));
+    for (const auto& kv : inplace_) plan.inplace.push_back({kv.first, kv.second});
+
+    tk_plan_stats& st = plan.stats;
+    st.materialized_ops = int(schedule_.size());
+    st.inlined_ops = int(inline_.size());
+    st.fused_epilogues = int(fused_.size());
+    st.tensor_core_ops = tc_ops;
+    st.stages = int(plan.stages.size());
+    st.grid_barriers = st.stages - 1;
+    st.direct_outputs = int(binding_.size());
+    st.direct_state_commits = int(direct_.size());
+    st.max_work_items = plan.max_items;
+    st.output_copies = copies;
+    st.split_reductions = split;
+    st.workspace_elements = plan.workspace_units;
+    st.arena_elements = arena_total_;
+    return plan;
+  }
+};
+
+}  // namespace
+
+Plan build_plan(const tk_program_desc& desc, const tk_options& opt, int sm_count) {
+  Planner p(desc, opt, sm_count);
+  return p.run();
+}
+
+}  // namespace tkp

@@ -1,0 +1,49 @@
+// Host planner: turns a tk_program_desc into the device op table.
+#pragma once
+
+#include <stdexcept>
+#include <string>
+#include <vector>
+
+#include "../../include/tk.h"
+#include "tk_device.h"
+
+namespace tkp {
+
+struct Error : std::runtime_error {
+  tk_status status;
+  Error(tk_status s, const std::string& m) : std::runtime_error("tk: " + m), status(s) {}
+};
+
+// One GEMM operand the tensor-core path loads with TMA.
+struct TmaOperand {
+  int32_t space, slot;      // where the matrix lives (Space / slot)
+  int64_t base_elems;       // element offset of the view from the space's base
+  int32_t dtype;
+  int64_t inner, outer;     // extents: contiguous dim, strided dim
+  int64_t outer_stride;     // elements between consecutive outer rows
+  int32_t box_inner, box_outer;
+};
+
+struct Plan {
+  std::vector<tkd::Stage> stages;
+  std::vector<tkd::Task> tasks;
+  std::vector<tkd::Instr> code;
+  std::vector<tkd::Ref> refs;
+  std::vector<TmaOperand> tma;
+  int64_t workspace_units = 0;
+  int64_t arena_units = 0;
+  int32_t max_items = 1;
+  size_t smem_bytes = 0;
+  bool uses_tc = false;
+  tk_plan_stats stats{};
+  // what tk_run checks
+  std::vector<int64_t> input_bytes;
+  std::vector<int64_t> output_bytes;
+  std::vector<std::pair<int, int>> inplace;  // {output slot, input index}
+};
+
+// Throws Error for an invalid or unsupported program.
+Plan build_plan(const tk_program_desc& desc, const tk_options& opt, int sm_count);
+
+}  // namespace tkp

@@ -1,0 +1,324 @@
+// C ABI of libtk: program creation (plan + device op table), workspace
+// sizing, the checked launch boundary and status/resource queries.
+//
+// The boundary checks mirror trainkernel's runtime (page "trainkernel 0.1.0
+// -- trainkernel/runtime.py", `CompiledProgram.run_into`): buffer counts,
+// workspace size, in-place outputs bound to exactly their declared input, an
+// in-place target not shared with another input, and no overlap between
+// outputs, the workspace and inputs.  With raw pointers the check is on byte
+// ranges instead of torch storages.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/tk.h"
+#include "planner.h"
+#include "tk_device.h"
+#include "tk_kernel.h"
+
+struct tk_program {
+  tkp::Plan plan;
+  tk_options opt{};
+  int device = -1;
+  int sm_count = 0;
+  int grid = 1;
+  size_t dyn_smem = 0;
+  void* d_table = nullptr;
+  const tkd::Program* d_prog = nullptr;
+};
+
+namespace {
+
+thread_local std::string g_error;
+
+tk_status fail(tk_status s, const std::string& msg) {
+  g_error = msg.rfind("tk: ", 0) == 0 ? msg : "tk: " + msg;
+  return s;
+}
+
+tk_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(TK_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Copy the plan's tables into one device allocation and patch the pointers.
+tk_status upload(tk_program* p) {
+  const tkp::Plan& pl = p->plan;
+  size_t off_prog = 0;
+  size_t off_stages = align_up(sizeof(tkd::Program), 64);
+  size_t off_tasks = align_up(off_stages + pl.stages.size() * sizeof(tkd::Stage), 64);
+  size_t off_code = align_up(off_tasks + pl.tasks.size() * sizeof(tkd::Task), 64);
+  size_t off_refs = align_up(off_code + pl.code.size() * sizeof(tkd::Instr), 64);
+  size_t total = align_up(off_refs + pl.refs.size() * sizeof(tkd::Ref), 64);
+  std::vector<unsigned char> host(total, 0);
+  void* dev = nullptr;
+  cudaError_t e = cudaMalloc(&dev, total);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(op table)");
+  auto* base = static_cast<unsigned char*>(dev);
+  tkd::Program prog{};
+  prog.n_stages = int32_t(pl.stages.size());
+  prog.n_tasks = int32_t(pl.tasks.size());
+  prog.n_code = int32_t(pl.code.size());
+  prog.n_refs = int32_t(pl.refs.size());
+  prog.stages = reinterpret_cast<const tkd::Stage*>(base + off_stages);
+  prog.tasks = reinterpret_cast<const tkd::Task*>(base + off_tasks);
+  prog.code = reinterpret_cast<const tkd::Instr*>(base + off_code);
+  prog.refs = reinterpret_cast<const tkd::Ref*>(base + off_refs);
+  std::memcpy(host.data() + off_prog, &prog, sizeof(prog));
+  if (!pl.stages.empty()) std::memcpy(host.data() + off_stages, pl.stages.data(), pl.stages.size() * sizeof(tkd::Stage));
+  if (!pl.tasks.empty()) std::memcpy(host.data() + off_tasks, pl.tasks.data(), pl.tasks.size() * sizeof(tkd::Task));
+  if (!pl.code.empty()) std::memcpy(host.data() + off_code, pl.code.data(), pl.code.size() * sizeof(tkd::Instr));
+  if (!pl.refs.empty()) std::memcpy(host.data() + off_refs, pl.refs.data(), pl.refs.size() * sizeof(tkd::Ref));
+  e = cudaMemcpy(dev, host.data(), total, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(dev);
+    return cuda_fail(e, "cudaMemcpy(op table)");
+  }
+  p->d_table = dev;
+  p->d_prog = reinterpret_cast<const tkd::Program*>(base + off_prog);
+  return TK_OK;
+}
+
+struct Range {
+  uintptr_t lo, hi;
+};
+bool overlaps(const Range& a, const Range& b) { return a.lo < b.hi && b.lo < a.hi; }
+Range range_of(const void* p, int64_t bytes) {
+  uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return {lo, lo + uintptr_t(bytes > 0 ? bytes : 0)};
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tk_last_error(void) { return g_error.c_str(); }
+
+void tk_options_default(tk_options* opt) {
+  if (!opt) return;
+  std::memset(opt, 0, sizeof(*opt));
+  opt->blocks_per_sm = 1;
+  opt->max_blocks = 0;
+  opt->fuse_pointwise = 1;
+  opt->fuse_epilogues = 1;
+  opt->inline_input_casts = 1;
+  opt->tensor_cores = 1;
+  opt->sm_count = 0;
+  opt->barrier_timeout_s = 2.0;
+}
+
+tk_status tk_program_create(const tk_program_desc* desc, const tk_options* opt_in, int device, tk_program** out) {
+  if (!out) return fail(TK_ERR_INVALID, "out must not be NULL");
+  *out = nullptr;
+  if (!desc) return fail(TK_ERR_INVALID, "desc must not be NULL");
+  tk_options opt;
+  tk_options_default(&opt);
+  if (opt_in) opt = *opt_in;
+  if (opt.blocks_per_sm < 1 || opt.blocks_per_sm > 8) return fail(TK_ERR_INVALID, "blocks_per_sm must be between 1 and 8");
+  if (!(opt.barrier_timeout_s > 0.0) || opt.barrier_timeout_s > 3600.0)
+    return fail(TK_ERR_INVALID, "barrier_timeout_s must be in (0, 3600]");
+  if (opt.sm_count < 0) return fail(TK_ERR_INVALID, "sm_count must be >= 0");
+
+  int sms = opt.sm_count > 0 ? opt.sm_count : 152;
+  if (device >= 0) {
+    DeviceGuard g(device);
+    if (!g.ok) return fail(TK_ERR_DEVICE, "cannot select CUDA device " + std::to_string(device));
+    cudaDeviceProp prop;
+    cudaError_t e = cudaGetDeviceProperties(&prop, device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+    if (prop.major != 10 || prop.minor != 3)
+      return fail(TK_ERR_DEVICE, "this build targets sm_103a (GB300); device is sm_" + std::to_string(prop.major) +
+                                     std::to_string(prop.minor));
+    if (!prop.cooperativeLaunch) return fail(TK_ERR_DEVICE, "device does not support cooperative launch");
+    if (opt.sm_count == 0) sms = prop.multiProcessorCount;
+  } else if (device != -1) {
+    return fail(TK_ERR_INVALID, "device must be a CUDA ordinal or -1");
+  }
+
+  auto* p = new (std::nothrow) tk_program();
+  if (!p) return fail(TK_ERR_INVALID, "out of host memory");
+  try {
+    p->plan = tkp::build_plan(*desc, opt, sms);
+  } catch (const tkp::Error& e) {
+    delete p;
+    return fail(e.status, e.what());
+  } catch (const std::exception& e) {
+    delete p;
+    return fail(TK_ERR_INVALID, e.what());
+  }
+  p->opt = opt;
+  p->device = device;
+  p->sm_count = sms;
+  p->dyn_smem = p->plan.smem_bytes;
+  int occupancy = 1;
+  if (device >= 0) {
+    DeviceGuard g(device);
+    cudaError_t e = tk_kernel_occupancy(&occupancy, p->dyn_smem);
+    if (e != cudaSuccess) {
+      delete p;
+      return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    }
+    if (occupancy < 1) {
+      delete p;
+      return fail(TK_ERR_DEVICE, "kernel has no resident blocks");
+    }
+    tk_status s = upload(p);
+    if (s != TK_OK) {
+      delete p;
+      return s;
+    }
+  }
+  int64_t grid = int64_t(sms) * std::min(occupancy, opt.blocks_per_sm);
+  grid = std::min<int64_t>(grid, p->plan.max_items);
+  if (opt.max_blocks > 0) grid = std::min<int64_t>(grid, opt.max_blocks);
+  p->grid = int(std::max<int64_t>(grid, 1));
+  p->plan.stats.grid_blocks = p->grid;
+  *out = p;
+  return TK_OK;
+}
+
+void tk_program_destroy(tk_program* p) {
+  if (!p) return;
+  if (p->d_table) {
+    DeviceGuard g(p->device);
+    cudaFree(p->d_table);
+  }
+  delete p;
+}
+
+tk_status tk_allocate(const tk_program* p, size_t* n) {
+  if (!p || !n) return fail(TK_ERR_INVALID, "program and workspace_elements must not be NULL");
+  *n = size_t(std::max<int64_t>(p->plan.workspace_units, 1));
+  return TK_OK;
+}
+
+tk_status tk_workspace_init(const tk_program* p, float* ws, size_t n, void* stream) {
+  if (!p) return fail(TK_ERR_INVALID, "program must not be NULL");
+  if (p->device < 0) return fail(TK_ERR_DEVICE, "plan-only program (created with device -1)");
+  if (!ws || n < size_t(p->plan.workspace_units))
+    return fail(TK_ERR_WORKSPACE, "workspace does not match compiled requirements");
+  DeviceGuard g(p->device);
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(tkd::Header), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace header)");
+  return TK_OK;
+}
+
+tk_status tk_run(tk_program* p, const void* const* inputs, int32_t n_inputs, void* const* outputs, int32_t n_outputs,
+                 float* ws, size_t ws_elems, void* stream) {
+  if (!p) return fail(TK_ERR_INVALID, "program must not be NULL");
+  if (p->device < 0) return fail(TK_ERR_DEVICE, "plan-only program (created with device -1)");
+  const tkp::Plan& pl = p->plan;
+  if (n_inputs != int32_t(pl.input_bytes.size()))
+    return fail(TK_ERR_INVALID, "expected " + std::to_string(pl.input_bytes.size()) + " inputs, got " +
+                                    std::to_string(n_inputs));
+  if (n_outputs != int32_t(pl.output_bytes.size())) return fail(TK_ERR_INVALID, "incorrect output buffer count");
+  if ((n_inputs && !inputs) || (n_outputs && !outputs)) return fail(TK_ERR_INVALID, "NULL buffer array");
+  if (!ws || ws_elems < size_t(pl.workspace_units))
+    return fail(TK_ERR_WORKSPACE, "workspace does not match compiled requirements");
+  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return fail(TK_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  for (int i = 0; i < n_inputs; ++i) {
+    if (pl.input_bytes[i] > 0 && !inputs[i]) return fail(TK_ERR_INVALID, "input " + std::to_string(i) + " is NULL");
+    if (reinterpret_cast<uintptr_t>(inputs[i]) % 16) return fail(TK_ERR_INVALID, "input pointers must be 16-byte aligned");
+  }
+  for (int j = 0; j < n_outputs; ++j) {
+    if (pl.output_bytes[j] > 0 && !outputs[j]) return fail(TK_ERR_INVALID, "output " + std::to_string(j) + " is NULL");
+    if (reinterpret_cast<uintptr_t>(outputs[j]) % 16) return fail(TK_ERR_INVALID, "output pointers must be 16-byte aligned");
+  }
+  // In-place outputs bind exactly their declared input; nothing else may overlap.
+  std::vector<bool> is_inplace(n_outputs, false), is_target(n_inputs, false);
+  for (const auto& kv : pl.inplace) {
+    if (outputs[kv.first] != inputs[kv.second])
+      return fail(TK_ERR_ALIAS, "inplace output must bind its declared input");
+    is_inplace[kv.first] = true;
+    is_target[kv.second] = true;
+  }
+  for (int i = 0; i < n_inputs; ++i) {
+    if (!is_target[i] || pl.input_bytes[i] == 0) continue;
+    Range t = range_of(inputs[i], pl.input_bytes[i]);
+    for (int k = 0; k < n_inputs; ++k)
+      if (k != i && overlaps(t, range_of(inputs[k], pl.input_bytes[k])))
+        return fail(TK_ERR_ALIAS, "inplace target must not alias another input");
+  }
+  Range wsr = range_of(ws, int64_t(pl.workspace_units) * 4);
+  std::vector<Range> written = {wsr};
+  for (int j = 0; j < n_outputs; ++j)
+    if (!is_inplace[j]) written.push_back(range_of(outputs[j], pl.output_bytes[j]));
+  for (size_t a = 0; a < written.size(); ++a) {
+    for (size_t b = a + 1; b < written.size(); ++b)
+      if (overlaps(written[a], written[b])) return fail(TK_ERR_ALIAS, "execution buffers must not alias inputs or each other");
+    for (int i = 0; i < n_inputs; ++i)
+      if (overlaps(written[a], range_of(inputs[i], pl.input_bytes[i])))
+        return fail(TK_ERR_ALIAS, "execution buffers must not alias inputs or each other");
+  }
+
+  tkd::Params prm{};
+  prm.prog = p->d_prog;
+  prm.ws = reinterpret_cast<char*>(ws);
+  prm.timeout_ns = static_cast<long long>(p->opt.barrier_timeout_s * 1e9);
+  prm.n_in = n_inputs;
+  prm.n_out = n_outputs;
+  for (int i = 0; i < n_inputs; ++i) prm.io[i] = const_cast<void*>(inputs[i]);
+  for (int j = 0; j < n_outputs; ++j) prm.io[tkd::kMaxIO + j] = outputs[j];
+  DeviceGuard g(p->device);
+  cudaError_t e = tk_kernel_launch(prm, p->grid, p->dyn_smem, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cooperative launch");
+  return TK_OK;
+}
+
+tk_status tk_run_status(const tk_program* p, const float* ws, void* stream, int32_t* device_status, int32_t* stage) {
+  if (!p || !ws || !device_status) return fail(TK_ERR_INVALID, "program, workspace and device_status must not be NULL");
+  if (p->device < 0) return fail(TK_ERR_DEVICE, "plan-only program (created with device -1)");
+  DeviceGuard g(p->device);
+  int32_t h[4] = {0, 0, 0, 0};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(h, ws, sizeof(h), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the workspace header");
+  *device_status = h[2];
+  if (stage) *stage = h[3];
+  return TK_OK;
+}
+
+tk_status tk_resource_usage(const tk_program* p, int64_t out[4]) {
+  if (!p || !out) return fail(TK_ERR_INVALID, "program and out must not be NULL");
+  if (p->device < 0) return fail(TK_ERR_DEVICE, "plan-only program (created with device -1)");
+  DeviceGuard g(p->device);
+  cudaFuncAttributes a;
+  cudaError_t e = tk_kernel_attributes(&a);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes");
+  int occ = 0;
+  e = tk_kernel_occupancy(&occ, p->dyn_smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  out[0] = a.numRegs;
+  out[1] = int64_t(a.localSizeBytes);
+  out[2] = int64_t(a.sharedSizeBytes) + int64_t(p->dyn_smem);
+  out[3] = occ;
+  return TK_OK;
+}
+
+tk_status tk_plan_stats_get(const tk_program* p, tk_plan_stats* s) {
+  if (!p || !s) return fail(TK_ERR_INVALID, "program and stats must not be NULL");
+  *s = p->plan.stats;
+  return TK_OK;
+}
+
+}  // extern "C"

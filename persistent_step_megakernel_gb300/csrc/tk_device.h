@@ -1,0 +1,138 @@
+// Device op table: the plan as the persistent kernel reads it.
+//
+// The host planner lowers every scheduled operation into a Task (a kind, an
+// index space, a small expression program and operand references) and groups
+// tasks into Stages; a grid barrier separates consecutive stages.  Each task
+// is cut into independent work items that blocks take round-robin.
+//
+// This header is plain data shared by planner.cpp and megakernel.cu.
+#pragma once
+
+#include <stdint.h>
+
+namespace tkd {
+
+constexpr int kThreads = 256;      // threads per block (8 warps)
+constexpr int kMaxRank = 4;
+constexpr int kVmRegs = 6;         // expression registers per element
+constexpr int kHeaderUnits = 64;   // workspace header: 64 floats = 256 bytes
+constexpr int kMaxIO = 256;        // program inputs (and outputs) per launch
+
+// Where a referenced tensor lives.
+enum Space : int32_t { SP_IN = 0, SP_OUT = 1, SP_WS = 2 };
+
+// How V consecutive index-space elements map to memory.
+enum VMode : int32_t {
+  VM_GATHER = 0,   // per-element address
+  VM_CONTIG = 1,   // unit stride along the innermost index dim, vector-aligned
+  VM_BCAST = 2     // stride 0 along the innermost index dim
+};
+
+// A tensor operand seen from a task's index space: element (c) is at
+// base + sum_d c[d] * stride[d] in units of its dtype.
+struct Ref {
+  int32_t space, slot, dtype, vmode;
+  int64_t base;
+  int64_t stride[kMaxRank];
+};
+
+// Expression instructions; every result is rounded to `round` (a tk_dtype).
+enum Opcode : uint8_t {
+  OP_LOAD = 0,    // dst <- ref[ref]
+  OP_CONST = 1,   // dst <- imm
+  OP_ACC = 2,     // dst <- value supplied by the task (GEMM accumulator)
+  OP_MOV = 3,     // dst <- a
+  OP_ADD = 4,     // dst <- a + fl(imm * b)
+  OP_SUB = 5,     // dst <- a - fl(imm * b)
+  OP_MUL = 6,     // dst <- a * b
+  OP_DIV = 7,     // dst <- a / b
+  OP_NEG = 8,     // dst <- -a
+  OP_RELU = 9,    // dst <- a < 0 ? 0 : a
+  OP_SQUARE = 10, // dst <- a * a
+  OP_POW = 11,    // dst <- powf(a, imm)
+  OP_THRESH = 12  // dst <- b <= imm ? 0 : a
+};
+
+struct Instr {
+  uint8_t op, dst, a, b;
+  uint8_t round;
+  uint8_t pad[3];
+  float imm;
+  int32_t ref;
+};
+
+enum TaskKind : int32_t {
+  T_POINTWISE = 0,     // out[i] = expr(i)
+  T_REDUCE_ROW = 1,    // reduce the innermost index dims; item = (output, part)
+  T_REDUCE_COL = 2,    // reduce the outer index dims; item = (column chunk, part)
+  T_REDUCE_FINAL = 3,  // sum the partials of a split reduction
+  T_GEMM_SIMT = 4,     // CUDA-core tiled GEMM + epilogue expression
+  T_GEMM_TC = 5        // tcgen05 GEMM + epilogue expression
+};
+
+struct Task {
+  int32_t kind;
+  int32_t n_items;
+  int32_t rank;              // index-space rank (0..4)
+  int32_t vec;               // elements per thread-vector: 8 or 1
+  int64_t shape[kMaxRank];   // index space
+  int64_t numel;
+  int32_t code_begin, code_len;
+  int32_t ref_begin, n_refs;
+  Ref out;                   // contiguous output, addressed by flat output index
+  // reductions
+  int32_t red_mean;          // 1: divide by size_f
+  int32_t parts;             // > 1: partials then a T_REDUCE_FINAL task
+  int64_t red_outer;         // ROW: outputs;      COL: reduced rows
+  int64_t red_inner;         // ROW: reduced size; COL: outputs (columns)
+  int64_t part_len;          // ROW: elements per part; COL: rows per part
+  int64_t scratch;           // float offset of the partials in the workspace
+  float size_f;              // float32(reduced size)
+  int32_t final_block;       // FINAL: 1 block per output (else 1 thread per output)
+  // GEMM (A[m,k] strides: a.stride[0], a.stride[1]; B[k,n]: b.stride[0], b.stride[1])
+  int32_t m, n, k;
+  int32_t tile_m, tile_n, tiles_n;
+  int32_t a_kcontig, b_ncontig;
+  Ref a, b;
+  // tcgen05 path
+  int32_t tma_a, tma_b;
+  uint32_t idesc;
+  int32_t a_mn_major, b_mn_major;
+  int32_t k_blocks;
+};
+
+struct Stage {
+  int32_t task_begin, task_end;
+  int32_t n_items;           // all items of the stage (tensor-core tiles first)
+  int32_t n_tc_items;
+};
+
+struct Program {
+  int32_t n_stages, n_tasks, n_code, n_refs;
+  const Stage* stages;
+  const Task* tasks;
+  const Instr* code;
+  const Ref* refs;
+};
+
+// Workspace header (offset 0, 256 bytes).  `count` returns to 0 after every
+// barrier, so a run that completes leaves the header ready for the next run.
+struct Header {
+  unsigned int count;   // arrivals at the current barrier
+  unsigned int gen;     // barrier generation
+  int status;           // 0, or the tk_status of the first failure
+  int stage;            // stage of the first failure
+  int abort;            // nonzero once any block gives up
+  int pad[59];
+};
+
+// Kernel arguments: io[i] is input i, io[kMaxIO + j] is output j.
+struct Params {
+  const Program* prog;
+  char* ws;
+  long long timeout_ns;
+  int n_in, n_out;
+  void* io[2 * kMaxIO];
+};
+
+}  // namespace tkd

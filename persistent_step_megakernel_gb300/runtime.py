@@ -1,0 +1,87 @@
+"""Torch-facing wrapper over the C ABI: device memory, streams and checks.
+
+PyTorch provides the allocations and the stream; the step itself runs in the
+kernel behind ``tk_run``.  The checks mirror trainkernel's runtime boundary
+(page "trainkernel 0.1.0 -- trainkernel/runtime.py", `_validate_inputs`,
+`allocate`, `run_into`): inputs must match the program's device, shape,
+strides and dtype; outputs are fresh contiguous tensors except in-place slots,
+which bind their declared input; the workspace is float32.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+from .ir import Program
+
+TORCH_DTYPE = {"float32": torch.float32, "float16": torch.float16, "bfloat16": torch.bfloat16}
+
+
+class TrainStep:
+    """One planned program on one CUDA device."""
+
+    def __init__(self, program: Program, device: int = 0, **options):
+        self.program = program
+        self.device = torch.device("cuda", device)
+        self.options = B.options(**options)
+        self.handle = B.tk_program_create(program, self.options, device)
+        self.workspace_elements = B.tk_allocate(self.handle)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h:
+            B.tk_program_destroy(h)
+            self.handle = None
+
+    @property
+    def stats(self) -> dict:
+        return B.tk_plan_stats_get(self.handle)
+
+    def resource_usage(self) -> dict:
+        return B.tk_resource_usage(self.handle)
+
+    def _stream(self, stream) -> int:
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        return int(s.cuda_stream)
+
+    def validate_inputs(self, inputs) -> None:
+        if len(inputs) != len(self.program.inputs):
+            raise ValueError(f"tk: expected {len(self.program.inputs)} inputs, got {len(inputs)}")
+        for i, (t, spec) in enumerate(zip(inputs, self.program.inputs)):
+            if not isinstance(t, torch.Tensor):
+                raise TypeError(f"tk: input {i} must be a tensor")
+            if (t.device != self.device or tuple(t.shape) != tuple(spec.shape)
+                    or tuple(t.stride()) != tuple(spec.strides) or t.dtype != TORCH_DTYPE[spec.dtype]):
+                raise ValueError(f"tk: input {i} does not match compiled device, shape, stride, or dtype")
+
+    def allocate(self, inputs, stream=None):
+        """Output tensors (in-place slots bind their input) and an initialised workspace."""
+        self.validate_inputs(inputs)
+        outs = []
+        for j, spec in enumerate(self.program.outputs):
+            if j in self.program.inplace:
+                outs.append(inputs[self.program.inplace[j]])
+            else:
+                outs.append(torch.empty(spec.shape, dtype=TORCH_DTYPE[spec.dtype], device=self.device))
+        ws = torch.empty(self.workspace_elements, dtype=torch.float32, device=self.device)
+        B.tk_workspace_init(self.handle, ws.data_ptr(), ws.numel(), self._stream(stream))
+        return outs, ws
+
+    def run(self, inputs, outputs, workspace, stream=None):
+        self.validate_inputs(inputs)
+        for j, (o, spec) in enumerate(zip(outputs, self.program.outputs)):
+            if (o.device != self.device or tuple(o.shape) != tuple(spec.shape)
+                    or o.dtype != TORCH_DTYPE[spec.dtype] or not o.is_contiguous()):
+                raise ValueError(f"tk: output {j} does not match compiled requirements")
+        if workspace.dtype != torch.float32 or not workspace.is_contiguous() or workspace.device != self.device:
+            raise ValueError("tk: workspace does not match compiled requirements")
+        B.tk_run(self.handle, [t.data_ptr() for t in inputs], [o.data_ptr() for o in outputs],
+                 workspace.data_ptr(), workspace.numel(), self._stream(stream))
+        return outputs
+
+    def status(self, workspace, stream=None):
+        return B.tk_run_status(self.handle, workspace.data_ptr(), self._stream(stream))
+
+    def __call__(self, *inputs):
+        outs, ws = self.allocate(inputs)
+        return self.run(inputs, outs, ws)

@@ -1,0 +1,260 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Checks, on seeded synthetic inputs:
+  * per op, teacher-forced: every materialised op output of an unfused plan is
+    recomputed by the oracle from the GPU's own operand values; pointwise ops
+    must be bit-exact, float32 ops within abs 1e-5 + rel 1e-4, bfloat16/float16
+    GEMMs and reductions within 2 ulp of the output dtype -- or, where the
+    float32 accumulation cannot reach that (heavy cancellation), within the
+    rigorous float32 summation bound K * 2^-24 * sum|terms| plus one ulp;
+  * the fused production plan gives bit-identical results to the unfused plan;
+  * results do not depend on the grid size;
+  * whole steps track the oracle end to end.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from persistent_step_megakernel_gb300 import binding as B
+from persistent_step_megakernel_gb300 import synthetic as S
+from persistent_step_megakernel_gb300.build import build
+from persistent_step_megakernel_gb300.ir import Operation, Program, TensorSpec
+from persistent_step_megakernel_gb300.runtime import TrainStep
+from tests._util import to_f64, to_torch, ulp_distance, ulp_of, values
+
+pytestmark = pytest.mark.gpu
+U32 = 2.0 ** -24
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build()
+
+
+def run_step(program, arrays, steps=1, **opts):
+    step = TrainStep(program, 0, **opts)
+    ins = [to_torch(a, s.dtype, "cuda") for a, s in zip(arrays, program.inputs)]
+    outs, ws = step.allocate(ins)
+    for _ in range(steps):
+        step.run(ins, outs, ws)
+    torch.cuda.synchronize()
+    status, stage = step.status(ws)
+    assert status == 0, f"device status {status} at stage {stage}"
+    return [to_f64(o) for o in outs], step
+
+
+def check_op(op, got, want, bound):
+    dt = op.output.dtype
+    got, want = np.asarray(got), np.asarray(want)
+    if op.op in ("mm", "addmm"):
+        k = op.inputs[-1].shape[0]
+    elif op.op in ("sum", "mean"):
+        src = op.inputs[0]
+        k = max(1, int(np.prod(src.shape)) // max(1, int(np.prod(op.output.shape)) if op.output.shape else 1))
+    else:
+        bad = ulp_distance(got, want, dt) != 0
+        assert not bad.any(), (op.name, got[bad][:5], want[bad][:5])
+        return 0
+    err = np.abs(got - want)
+    accum = 1.01 * k * U32 * np.asarray(bound)
+    if op.op == "mean":
+        accum = accum / max(k, 1)
+    if dt == "float32":
+        ok = (err <= 1e-5 + 1e-4 * np.abs(want)) | (err <= accum + ulp_of(want, dt))
+    else:
+        ok = (ulp_distance(got, want, dt) <= 2) | (err <= accum + ulp_of(want, dt))
+    nan_ok = np.isnan(got) & np.isnan(want)
+    ok = ok | nan_ok
+    assert ok.all(), (op.name, got[~ok][:5], want[~ok][:5], accum[~ok][:5])
+    return int(ulp_distance(got, want, dt).max()) if dt != "float32" else 0
+
+
+def teacher_forced(program, arrays, gpu_outs, sample=4096, seed=0):
+    """Every op of an all-outputs program against the oracle on GPU operands."""
+    rng = np.random.default_rng(seed)
+    o = oracle.Oracle(program)
+    for s, v in zip(program.inputs, values(arrays, program)):
+        o.set(s.buffer, v)
+    got_by_buf = {}
+    for s, v in zip(program.outputs, gpu_outs):
+        got_by_buf.setdefault(s.buffer, v)
+        o.set(s.buffer, v)
+    worst = 0
+    for i, op in enumerate(program.operations):
+        g = got_by_buf[op.output.buffer].reshape(-1)
+        idx = np.arange(g.size) if g.size <= 2 * sample else np.sort(rng.choice(g.size, sample, replace=False))
+        want, bound = o.eval_op_sampled(i, idx)
+        worst = max(worst, check_op(op, g[idx], want, bound))
+    return worst
+
+
+SMALL = {
+    "c1": S.CONFIGS["c1"],
+    "c2": S.CONFIGS["c2"],
+    "c3s": S.scaled(S.CONFIGS["c3"], batch=64, dims=(256, 1024, 256)),
+    "c4": S.CONFIGS["c4"],
+    "c5s": S.scaled(S.CONFIGS["c5"], batch=256, dims=(512,) * 5),
+    "ragged_f32": S.scaled(S.CONFIGS["c1"], batch=3, dims=(13, 7, 5)),
+    "ragged_bf16": S.scaled(S.CONFIGS["c2"], batch=5, dims=(37, 19, 11)),
+    "ragged_f16_mom": S.scaled(S.CONFIGS["c3"], batch=9, dims=(24, 40, 24)),
+}
+
+
+@pytest.mark.parametrize("key", list(SMALL))
+def test_each_op_matches_oracle_teacher_forced(key):
+    cfg = SMALL[key]
+    prog = S.mlp_step_program(cfg, export="all")
+    arrays = S.mlp_inputs(cfg, prog)
+    outs, step = run_step(prog, arrays)
+    assert step.stats["fused_epilogues"] == 0 and step.stats["inlined_ops"] == 0
+    teacher_forced(prog, arrays, outs)
+
+
+@pytest.mark.parametrize("key", list(SMALL))
+def test_fused_plan_bit_identical_to_unfused(key):
+    cfg = SMALL[key]
+    fused = S.mlp_step_program(cfg, export="grads")
+    unfused = S.mlp_step_program(cfg, export="all")
+    arrays = S.mlp_inputs(cfg, fused)
+    a, sa = run_step(fused, arrays)
+    b, _ = run_step(unfused, arrays)
+    assert sa.stats["fused_epilogues"] > 0
+    names_b = {s.buffer: v for s, v in zip(unfused.outputs, b)}
+    for s, v in zip(fused.outputs, a):
+        np.testing.assert_array_equal(v, names_b[s.buffer], err_msg=s.buffer)
+
+
+@pytest.mark.parametrize("key", ["c1", "c2", "c4", "ragged_bf16"])
+def test_results_do_not_depend_on_grid_size(key):
+    cfg = SMALL[key]
+    prog = S.mlp_step_program(cfg, export="grads")
+    arrays = S.mlp_inputs(cfg, prog)
+    ref, _ = run_step(prog, arrays)
+    for mb in (1, 3, 17):
+        got, st = run_step(prog, arrays, max_blocks=mb)
+        assert st.stats["grid_blocks"] <= mb
+        for x, y in zip(ref, got):
+            np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("key", ["c1", "c2", "c3s", "c4", "ragged_f32", "ragged_f16_mom"])
+def test_whole_step_tracks_oracle(key):
+    cfg = SMALL[key]
+    prog = S.mlp_step_program(cfg, export="grads")
+    arrays = S.mlp_inputs(cfg, prog)
+    gpu, _ = run_step(prog, arrays)
+    want = oracle.run_program(prog, values(arrays, prog))
+    dt = cfg.dtype
+    if dt == "float32":
+        for s, g, w in zip(prog.outputs, gpu, want):
+            np.testing.assert_allclose(g, w, rtol=1e-4, atol=1e-5, err_msg=s.buffer)
+        return
+    assert abs(gpu[0] - want[0]) <= 2e-2 * abs(want[0]) + 1e-6      # loss
+    for slot, idx in prog.inplace.items():                            # updated state
+        assert ulp_distance(gpu[slot], want[slot], dt).max() <= 2, prog.outputs[slot].buffer
+
+
+def test_three_steps_feed_state_back():
+    cfg = S.CONFIGS["c2"]
+    prog = S.mlp_step_program(cfg, export="state")
+    arrays = S.mlp_inputs(cfg, prog)
+    gpu, _ = run_step(prog, arrays, steps=3)
+    vals = values(arrays, prog)
+    for _ in range(3):
+        outs = oracle.run_program(prog, vals)
+        for slot, idx in prog.inplace.items():
+            vals[idx] = outs[slot]
+    for slot, idx in prog.inplace.items():
+        assert ulp_distance(gpu[slot], outs[slot], cfg.dtype).max() <= 3
+
+
+def test_empty_batch():
+    cfg = S.scaled(S.CONFIGS["c1"], batch=0)
+    prog = S.mlp_step_program(cfg, export="grads")
+    arrays = S.mlp_inputs(cfg, prog)
+    gpu, _ = run_step(prog, arrays)
+    want = oracle.run_program(prog, values(arrays, prog))
+    assert np.isnan(gpu[0]) and np.isnan(want[0])
+    for g, w in zip(gpu[1:], want[1:]):
+        np.testing.assert_array_equal(g, w)
+
+
+def _mixed_program():
+    """Broadcasts, scalars, transposed and negative-dim reductions, rank 0."""
+    T = TensorSpec.contiguous
+    x, r, c = T("x", (6, 40), "bfloat16"), T("r", (40,), "bfloat16"), T("c", (6, 1), "bfloat16")
+    ops = [
+        Operation("a", "add", (x, r), T("a", (6, 40), "bfloat16"), {"alpha": -0.5}),
+        Operation("m", "mul", (T("a", (6, 40), "bfloat16"), c), T("m", (6, 40), "bfloat16")),
+        Operation("q", "div", (T("m", (6, 40), "bfloat16"), 3.0), T("q", (6, 40), "bfloat16")),
+        Operation("n", "neg", (T("q", (6, 40), "bfloat16"),), T("n", (6, 40), "bfloat16")),
+        Operation("s1", "sum", (T("n", (6, 40), "bfloat16"),), T("s1", (6,), "bfloat16"), {"dims": (-1,)}),
+        Operation("s2", "sum", (T("q", (6, 40), "bfloat16").T,), T("s2", (6,), "bfloat16"), {"dims": (0,)}),
+        Operation("f", "full", (), T("f", (3, 8), "float32"), {"value": 0.1}),
+        Operation("k", "cast", (x,), T("k", (6, 40), "float16")),
+        Operation("p", "pow", (T("k", (6, 40), "float16"), 2), T("p", (6, 40), "float16")),
+        Operation("mu", "mean", (T("p", (6, 40), "float16"),), T("mu", (), "float16")),
+        Operation("t", "threshold_backward", (x, T("a", (6, 40), "bfloat16")), T("t", (6, 40), "bfloat16"),
+                  {"threshold": 0.25}),
+        Operation("rl", "relu", (T("t", (6, 40), "bfloat16"),), T("rl", (6, 40), "bfloat16")),
+    ]
+    outs = [T("s1", (6,), "bfloat16"), T("s2", (6,), "bfloat16"), T("f", (3, 8), "float32"),
+            T("mu", (), "float16"), T("rl", (6, 40), "bfloat16"), T("a", (6, 40), "bfloat16")]
+    return Program([x, r, c], outs, ops)
+
+
+@pytest.mark.parametrize("fuse", [0, 1])
+def test_mixed_pointwise_and_reduction_program(fuse):
+    prog = _mixed_program()
+    arrays = [S.to_storage(S.normal(S.stream_seed(3, i), int(np.prod(s.shape))), s.dtype).reshape(s.shape)
+              for i, s in enumerate(prog.inputs)]
+    gpu, _ = run_step(prog, arrays, fuse_pointwise=fuse, fuse_epilogues=fuse)
+    want = oracle.run_program(prog, values(arrays, prog))
+    for s, g, w in zip(prog.outputs, gpu, want):
+        if s.buffer in ("s1", "s2", "mu"):
+            assert ulp_distance(g, w, s.dtype).max() <= 2, s.buffer
+        else:
+            assert ulp_distance(g, w, s.dtype).max() == 0, s.buffer
+
+
+def test_barrier_timeout_is_reported_and_recoverable():
+    """A barrier that can never complete gives up after its limit (no hang)."""
+    cfg = S.CONFIGS["c1"]
+    prog = S.mlp_step_program(cfg, export="state")
+    arrays = S.mlp_inputs(cfg, prog)
+    step = TrainStep(prog, 0, max_blocks=1, barrier_timeout_s=1e-3)
+    ins = [to_torch(a, s.dtype, "cuda") for a, s in zip(arrays, prog.inputs)]
+    outs, ws = step.allocate(ins)
+    ws.view(torch.int32)[0] = 7          # pretend 7 arrivals that never complete
+    step.run(ins, outs, ws)
+    status, stage = step.status(ws)
+    assert status == 7 and stage == 0    # TK_ERR_BARRIER_TIMEOUT in the first barrier
+    ins = [to_torch(a, s.dtype, "cuda") for a, s in zip(arrays, prog.inputs)]
+    outs, ws = step.allocate(ins)        # re-initialised header
+    step.run(ins, outs, ws)
+    assert step.status(ws) == (0, 0)
+
+
+def test_boundary_rejects_bad_buffers():
+    cfg = S.CONFIGS["c1"]
+    prog = S.mlp_step_program(cfg, export="state")
+    arrays = S.mlp_inputs(cfg, prog)
+    step = TrainStep(prog, 0)
+    ins = [to_torch(a, s.dtype, "cuda") for a, s in zip(arrays, prog.inputs)]
+    outs, ws = step.allocate(ins)
+    h, ip, op = step.handle, [t.data_ptr() for t in ins], [o.data_ptr() for o in outs]
+    with pytest.raises(B.TkError, match="inputs"):
+        B.tk_run(h, ip[:-1], op, ws.data_ptr(), ws.numel())
+    with pytest.raises(B.TkError, match="TK_ERR_WORKSPACE"):
+        B.tk_run(h, ip, op, ws.data_ptr(), ws.numel() - 1)
+    bad = list(op)
+    bad[1] = ip[0]                       # an in-place slot bound to the wrong input
+    with pytest.raises(B.TkError, match="TK_ERR_ALIAS"):
+        B.tk_run(h, ip, bad, ws.data_ptr(), ws.numel())
+    bad = list(op)
+    bad[0] = ip[0]                       # the loss written over an input
+    with pytest.raises(B.TkError, match="TK_ERR_ALIAS"):
+        B.tk_run(h, ip, bad, ws.data_ptr(), ws.numel())
+    with pytest.raises(B.TkError, match="TK_ERR_ALIAS"):
+        B.tk_run(h, ip, op, ip[0] - (ip[0] % 256), ws.numel())

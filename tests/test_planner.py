@@ -1,0 +1,167 @@
+"""Golden planner tests (no GPU): hand-built programs whose inlining, epilogue
+fusion, arena reuse and barrier placement follow from the planning rules of
+trainkernel/codegen.py (`_Generator`), and the boundary's error cases."""
+import pytest
+
+from persistent_step_megakernel_gb300 import binding as B
+from persistent_step_megakernel_gb300 import synthetic as S
+from persistent_step_megakernel_gb300.build import build
+from persistent_step_megakernel_gb300.ir import Operation, Program, TensorSpec
+
+T = TensorSpec.contiguous
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build()
+
+
+def plan(prog, **opts):
+    h = B.tk_program_create(prog, B.options(sm_count=152, **opts), device=-1)
+    try:
+        return B.tk_plan_stats_get(h)
+    finally:
+        B.tk_program_destroy(h)
+
+
+def f32(name, shape):
+    return T(name, shape, "float32")
+
+
+def test_independent_ops_share_one_stage():
+    x, y = f32("x", (4, 8)), f32("y", (4, 8))
+    prog = Program([x, y], [f32("a", (4, 8)), f32("b", (4, 8))],
+                   [Operation("a", "add", (x, y), f32("a", (4, 8))),
+                    Operation("b", "mul", (x, y), f32("b", (4, 8)))])
+    s = plan(prog)
+    assert (s["materialized_ops"], s["inlined_ops"], s["stages"], s["direct_outputs"], s["output_copies"]) == (2, 0, 1, 2, 0)
+
+
+def test_single_use_pointwise_is_inlined():
+    x, y = f32("x", (4, 8)), f32("y", (4, 8))
+    prog = Program([x, y], [f32("b", (4, 8))],
+                   [Operation("a", "add", (x, y), f32("a", (4, 8))),
+                    Operation("b", "mul", (f32("a", (4, 8)), 2.0), f32("b", (4, 8)))])
+    s = plan(prog)
+    assert (s["materialized_ops"], s["inlined_ops"], s["stages"]) == (1, 1, 1)
+    s = plan(prog, fuse_pointwise=0)
+    assert (s["materialized_ops"], s["inlined_ops"], s["stages"]) == (2, 0, 2)
+
+
+def _gemm_relu_sum(relu_is_output):
+    x, w = f32("x", (4, 8)), f32("W", (16, 8))
+    ops = [Operation("t", "mm", (x, w.T), f32("t", (4, 16))),
+           Operation("u", "relu", (f32("t", (4, 16)),), f32("u", (4, 16))),
+           Operation("s", "sum", (f32("u", (4, 16)),), f32("s", ()))]
+    outs = [f32("s", ())] + ([f32("u", (4, 16))] if relu_is_output else [])
+    return Program([x, w], outs, ops)
+
+
+def test_gemm_epilogue_chain_fusion():
+    s = plan(_gemm_relu_sum(False))
+    assert (s["fused_epilogues"], s["materialized_ops"], s["inlined_ops"], s["stages"]) == (1, 2, 0, 2)
+    s = plan(_gemm_relu_sum(False), fuse_epilogues=0)           # relu then inlines into the sum
+    assert (s["fused_epilogues"], s["materialized_ops"], s["inlined_ops"], s["stages"]) == (0, 2, 1, 2)
+
+
+def test_chain_stops_at_program_outputs():
+    s = plan(_gemm_relu_sum(True))
+    assert (s["fused_epilogues"], s["materialized_ops"], s["inlined_ops"], s["stages"]) == (0, 3, 0, 3)
+
+
+def _update(read_after):
+    w, g = f32("W", (8,)), f32("g", (8,))
+    upd = Operation("Wn", "sub", (w, g), f32("Wn", (8,)), {"alpha": 0.5})
+    use = Operation("c", "mul", (w, 2.0), f32("c", (8,)))
+    ops = [upd, use] if read_after else [use, upd]
+    return Program([w, g], [f32("Wn", (8,)), f32("c", (8,))], ops, {0: 0})
+
+
+def test_inplace_update_direct_when_no_later_reader():
+    s = plan(_update(read_after=False))
+    assert (s["direct_state_commits"], s["output_copies"], s["stages"], s["direct_outputs"]) == (1, 0, 2, 2)
+
+
+def test_inplace_update_committed_after_a_later_reader():
+    s = plan(_update(read_after=True))
+    assert (s["direct_state_commits"], s["output_copies"], s["stages"], s["direct_outputs"]) == (0, 1, 2, 1)
+
+
+def test_arena_reuse_adds_a_write_after_read_barrier():
+    x = f32("x", (64,))
+    v = lambda n: f32(n, (64,))
+    ops = [Operation("a", "neg", (x,), v("a")),
+           Operation("b", "mul", (v("a"), 2.0), v("b")),
+           Operation("c", "add", (v("a"), 1.0), v("c")),
+           Operation("d", "mul", (x, 3.0), v("d")),
+           Operation("e", "add", (v("d"), v("d")), v("e"))]
+    s = plan(Program([x], [v("b"), v("c"), v("e")], ops))
+    assert (s["materialized_ops"], s["stages"], s["arena_elements"]) == (5, 4, 64)
+
+
+def test_large_mean_is_split():
+    x = f32("x", (1024, 1024))
+    s = plan(Program([x], [f32("m", ())], [Operation("m", "mean", (x,), f32("m", ()))]))
+    assert (s["split_reductions"], s["stages"], s["max_work_items"]) == (1, 2, 128)
+
+
+def test_mlp_step_plan_counts():
+    s = plan(S.mlp_step_program(S.CONFIGS["c2"], export="state"))
+    # fused: 3 forward addmm(+relu/+sub) and 2 input-grad mm(+threshold_backward); inlined: pow
+    assert (s["fused_epilogues"], s["inlined_ops"], s["materialized_ops"]) == (5, 1, 19)
+    assert (s["direct_state_commits"], s["direct_outputs"], s["output_copies"]) == (6, 7, 0)
+
+
+# ------------------------------------------------------------ errors
+
+def _err(prog, match, status=None, **opts):
+    with pytest.raises(B.TkError, match=match) as e:
+        plan(prog, **opts)
+    if status is not None:
+        assert e.value.status == status
+
+
+def test_rejects_malformed_programs():
+    x, w = f32("x", (4, 8)), f32("W", (16, 8))
+    _err(Program([x, w], [f32("t", (4, 16))], [Operation("t", "mm", (x, w), f32("t", (4, 16)))]),
+         "compatible rank-two")
+    _err(Program([x, f32("r", (3,))], [f32("a", (4, 8))],
+                 [Operation("a", "add", (x, f32("r", (3,))), f32("a", (4, 8)))]), "incompatible broadcast")
+    _err(Program([x], [f32("a", (4, 8))], [Operation("a", "mul", (x, float("inf")), f32("a", (4, 8)))]),
+         "non-finite", 2)
+    _err(Program([x], [f32("a", (4, 8))],
+                 [Operation("a", "neg", (x,), TensorSpec("a", (4, 8), (1, 4), 0, "float32"))]), "contiguous")
+    _err(Program([x], [f32("b", (4, 8))],
+                 [Operation("b", "neg", (f32("a", (4, 8)),), f32("b", (4, 8))),
+                  Operation("a", "neg", (x,), f32("a", (4, 8)))]), "topological")
+    _err(Program([T("x", (4, 8), "float64")], [], []), "unsupported dtype", 2)
+    _err(Program([TensorSpec("x", (-1, 8), (8, 1), 0, "float32")], [], []), "invalid static shape")
+    _err(Program([x], [f32("s", (4,))], [Operation("s", "sum", (x,), f32("s", (4,)), {"dims": (2,)})]),
+         "reduction dims")
+    _err(Program([x], [f32("s", (3,))], [Operation("s", "sum", (x,), f32("s", (3,)), {"dims": (1,)})]),
+         "reduction output shape")
+    _err(Program([x], [f32("p", (4, 8))], [Operation("p", "pow", (x, x), f32("p", (4, 8)))]), "exponent")
+    _err(Program([x], [f32("a", (4, 8))], [Operation("a", "neg", (x,), f32("a", (4, 8)))]), "blocks_per_sm",
+         blocks_per_sm=9)
+
+
+def test_rejects_bad_inplace_mappings():
+    x, y = f32("x", (4, 8)), f32("y", (4, 4))
+    neg = Operation("a", "neg", (x,), f32("a", (4, 8)))
+    _err(Program([x, y], [f32("a", (4, 8))], [neg], {0: 1}), "match a contiguous input")
+    _err(Program([x], [x], [], {0: 0}), "computed values")
+    _err(Program([x, f32("z", (4, 8))], [f32("a", (4, 8)), f32("b", (4, 8))],
+                 [neg, Operation("b", "neg", (x,), f32("b", (4, 8)))], {0: 0, 1: 0}), "distinct inputs")
+    _err(Program([x], [f32("a", (4, 8))], [neg], {0: 5}), "invalid inplace")
+
+
+def test_plan_only_program_cannot_run():
+    prog = S.mlp_step_program(S.CONFIGS["c1"])
+    h = B.tk_program_create(prog, B.options(sm_count=8), device=-1)
+    try:
+        assert B.tk_allocate(h) >= 64
+        with pytest.raises(B.TkError, match="plan-only") as e:
+            B.tk_run(h, [16] * len(prog.inputs), [16] * len(prog.outputs), 256, 1 << 20)
+        assert e.value.status == 6
+    finally:
+        B.tk_program_destroy(h)

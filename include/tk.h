@@ -132,7 +132,7 @@ typedef struct {
   int32_t inline_input_casts;  /* inline casts of program inputs (default 1) */
   int32_t tensor_cores;        /* 1: tcgen05 path for eligible bf16/fp16 GEMMs (default 1) */
   int32_t sm_count;            /* 0: query the device; > 0: SM count for a plan-only program */
-  int32_t reserved;
+  int32_t profile;             /* 1: record per-stage globaltimer stamps (see tk_profile_read) */
   double barrier_timeout_s;    /* limit of every in-kernel wait (default 2.0) */
 } tk_options;
 
@@ -203,6 +203,17 @@ tk_status tk_run_status(const tk_program* program, const float* workspace, void*
  * out[1] local bytes per thread, out[2] shared bytes per block (static +
  * dynamic), out[3] resident blocks per SM. */
 tk_status tk_resource_usage(const tk_program* program, int64_t out[4]);
+
+/* Per-stage timing of the last run of a program created with profile = 1.
+ * Synchronises `stream`, then copies stages * grid_blocks groups of 8
+ * %globaltimer stamps (ns) into stamps[(s*grid+b)*8 + i]: i = 0 block b starts
+ * stage s, 1 it reaches the barrier after it, 2 its TMA producer is done,
+ * 3 its first operand tile has landed, 4 its MMA issue is done, 5 its first
+ * accumulator is ready, 6 its epilogue is done (2-6 are 0 when the block has
+ * no tensor-core tile in that stage), 7 kernel entry (stage 0 only).
+ * n_stamps must be >= 8 * stages * grid_blocks (see tk_plan_stats). */
+tk_status tk_profile_read(const tk_program* program, const float* workspace, void* stream, int64_t* stamps,
+                          size_t n_stamps);
 
 /* Planner decisions for tests and reports. */
 tk_status tk_plan_stats_get(const tk_program* program, tk_plan_stats* stats);

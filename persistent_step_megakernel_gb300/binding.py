@@ -51,7 +51,7 @@ class tk_options(ctypes.Structure):
     _fields_ = [("blocks_per_sm", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
                 ("fuse_pointwise", ctypes.c_int32), ("fuse_epilogues", ctypes.c_int32),
                 ("inline_input_casts", ctypes.c_int32), ("tensor_cores", ctypes.c_int32),
-                ("sm_count", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("sm_count", ctypes.c_int32), ("profile", ctypes.c_int32),
                 ("barrier_timeout_s", ctypes.c_double)]
 
 
@@ -76,6 +76,8 @@ SIGNATURES = [
     ("tk_run_status", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                      ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]),
     ("tk_resource_usage", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64 * 4]),
+    ("tk_profile_read", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.POINTER(ctypes.c_int64), ctypes.c_size_t]),
     ("tk_plan_stats_get", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(tk_plan_stats)]),
     ("tk_last_error", ctypes.c_char_p, []),
 ]
@@ -224,6 +226,18 @@ def tk_resource_usage(handle) -> dict:
     check(lib().tk_resource_usage(handle, out))
     return dict(zip(("registers_per_thread", "local_bytes_per_thread", "shared_bytes_per_block",
                      "resident_blocks_per_sm"), list(out)))
+
+
+PROFILE_STAMPS = 8
+
+
+def tk_profile_read(handle, workspace_ptr: int, stages: int, grid: int, stream: int = 0):
+    """Stamps as a list [stage][block] of 8-tuples (see tk_profile_read in tk.h)."""
+    n = PROFILE_STAMPS * stages * grid
+    buf = (ctypes.c_int64 * n)()
+    check(lib().tk_profile_read(handle, ctypes.c_void_p(workspace_ptr), ctypes.c_void_p(stream), buf, n))
+    k = PROFILE_STAMPS
+    return [[tuple(buf[(s * grid + b) * k:(s * grid + b + 1) * k]) for b in range(grid)] for s in range(stages)]
 
 
 def tk_plan_stats_get(handle) -> dict:

@@ -17,6 +17,7 @@
 // program's timeout records TK_ERR_BARRIER_TIMEOUT and the stage in the
 // workspace header, raises an abort flag and returns; blocks that see the
 // flag return too.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -29,8 +30,12 @@ namespace tkk {
 
 using namespace tkd;
 
+// Descriptor pointers are indexed with global task/instruction/ref indices;
+// for the current stage they usually point into shared memory.
 struct Ctx {
-  const Program* prog;
+  const Task* tasks;
+  const Instr* code;
+  const Ref* refs;
   char* ws;
   Header* hdr;
   void* const* io;  // shared-memory copy of Params::io
@@ -124,13 +129,17 @@ __device__ __forceinline__ void store_out(const Ctx& c, const Ref& o, int64_t fl
 
 // ------------------------------------------------------ expression machine
 
+// Index-space coordinates of flat index f (the planner keeps every index
+// space below 2^31 elements, so 32-bit division suffices).
 __device__ __forceinline__ void unravel(const Task& t, int64_t f, int64_t* crd) {
+  uint32_t g = uint32_t(f);
 #pragma unroll
   for (int d = kMaxRank - 1; d >= 0; --d) {
     if (d < t.rank) {
-      int64_t n = t.shape[d];
-      crd[d] = f % n;
-      f /= n;
+      const uint32_t n = uint32_t(t.shape[d]);
+      const uint32_t q = g / n;
+      crd[d] = int64_t(g - q * n);
+      g = q;
     } else {
       crd[d] = 0;
     }
@@ -171,7 +180,7 @@ struct Regs {
   case k:                                                \
     _Pragma("unroll") for (int j = 0; j < V; ++j) out[j] = r[k][j]; \
     break;
-      TK_GET(0) TK_GET(1) TK_GET(2) TK_GET(3) TK_GET(4) TK_GET(5)
+      TK_GET(0) TK_GET(1) TK_GET(2) TK_GET(3)
 #undef TK_GET
     }
   }
@@ -181,7 +190,7 @@ struct Regs {
   case k:                                                \
     _Pragma("unroll") for (int j = 0; j < V; ++j) r[k][j] = in[j]; \
     break;
-      TK_SET(0) TK_SET(1) TK_SET(2) TK_SET(3) TK_SET(4) TK_SET(5)
+      TK_SET(0) TK_SET(1) TK_SET(2) TK_SET(3)
 #undef TK_SET
     }
   }
@@ -193,8 +202,8 @@ template <int V>
 __device__ __forceinline__ void vm_eval(const Ctx& c, const Task& t, const int64_t* crd, const float* acc,
                                         float (&res)[V]) {
   Regs<V> R;
-  const Instr* code = c.prog->code + t.code_begin;
-  const Ref* refs = c.prog->refs + t.ref_begin;
+  const Instr* code = c.code + t.code_begin;
+  const Ref* refs = c.refs + t.ref_begin;
   for (int pc = 0; pc < t.code_len; ++pc) {
     const Instr in = code[pc];
     float a[V], b[V], r[V];
@@ -269,6 +278,154 @@ __device__ __forceinline__ void vm_eval(const Ctx& c, const Task& t, const int64
   R.get(0, res);
 }
 
+// ------------------------------------------------------------- chains
+
+template <int V>
+__device__ __forceinline__ void chain_load(const Ctx& c, const Task& t, const int64_t* crd, float (&L)[2][V]) {
+  const Chain& ch = t.chain;
+  const Ref* refs = c.refs + t.ref_begin;
+  if (ch.n_loads > 0) load_ref<V>(c, t, refs[ch.load_ref[0]], crd, L[0]);
+  if (ch.n_loads > 1) load_ref<V>(c, t, refs[ch.load_ref[1]], crd, L[1]);
+}
+
+template <int V>
+__device__ __forceinline__ void round_vec(float (&x)[V], int dt) {
+  if (dt == TK_BF16) {
+#pragma unroll
+    for (int j = 0; j < V; ++j) x[j] = __bfloat162float(__float2bfloat16_rn(x[j]));
+  } else if (dt == TK_F16) {
+#pragma unroll
+    for (int j = 0; j < V; ++j) x[j] = __half2float(__float2half_rn(x[j]));
+  }
+}
+
+// The chain's value for V elements from their loaded operands (and the GEMM
+// accumulator for CH_ACC): same arithmetic, operation by operation, as the
+// instruction form.  Every branch is uniform across the block.
+template <int V>
+__device__ __forceinline__ void chain_compute(const Task& t, const float (&L)[2][V], const float* acc, float (&x)[V]) {
+  const Chain& ch = t.chain;
+  if (ch.start == CH_LOAD) {
+#pragma unroll
+    for (int j = 0; j < V; ++j) x[j] = L[0][j];
+  } else if (ch.start == CH_CONST) {
+#pragma unroll
+    for (int j = 0; j < V; ++j) x[j] = ch.start_const;
+  } else {
+    float b[V];
+    if (ch.bias == 0) {
+#pragma unroll
+      for (int j = 0; j < V; ++j) b[j] = L[0][j];
+    } else if (ch.bias == 1) {
+#pragma unroll
+      for (int j = 0; j < V; ++j) b[j] = L[1][j];
+    } else {
+#pragma unroll
+      for (int j = 0; j < V; ++j) b[j] = ch.bias_const;
+    }
+    switch (ch.addmm_mode) {
+      case AM_ACC:
+#pragma unroll
+        for (int j = 0; j < V; ++j) x[j] = acc[j];
+        break;
+      case AM_SUM:
+#pragma unroll
+        for (int j = 0; j < V; ++j) x[j] = __fadd_rn(acc[j], b[j]);
+        break;
+      case AM_ZERO:
+#pragma unroll
+        for (int j = 0; j < V; ++j) x[j] = 0.0f;
+        break;
+      case AM_ALPHA:
+#pragma unroll
+        for (int j = 0; j < V; ++j) x[j] = __fmul_rn(ch.alpha, acc[j]);
+        break;
+      case AM_BETA:
+#pragma unroll
+        for (int j = 0; j < V; ++j) x[j] = __fmul_rn(ch.beta, b[j]);
+        break;
+      default:
+#pragma unroll
+        for (int j = 0; j < V; ++j) x[j] = __fadd_rn(__fmul_rn(ch.alpha, acc[j]), __fmul_rn(ch.beta, b[j]));
+        break;
+    }
+    round_vec<V>(x, ch.round0);
+  }
+  for (int s = 0; s < ch.n_steps; ++s) {
+    const ChainStep st = ch.steps[s];
+    float e[V];
+    if (st.ext == EXT_LOAD0) {
+#pragma unroll
+      for (int j = 0; j < V; ++j) e[j] = L[0][j];
+    } else if (st.ext == EXT_LOAD1) {
+#pragma unroll
+      for (int j = 0; j < V; ++j) e[j] = L[1][j];
+    } else {
+#pragma unroll
+      for (int j = 0; j < V; ++j) e[j] = st.cval;
+    }
+    if (st.second) {  // running value is the second operand: swap roles
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        const float tmp = e[j];
+        e[j] = x[j];
+        x[j] = tmp;
+      }
+    }
+    // now x holds operand a, e holds operand b
+    switch (st.op) {
+      case OP_ADD:
+#pragma unroll
+        for (int j = 0; j < V; ++j) x[j] = __fadd_rn(x[j], __fmul_rn(st.imm, e[j]));
+        break;
+      case OP_SUB:
+#pragma unroll
+        for (int j = 0; j < V; ++j) x[j] = __fsub_rn(x[j], __fmul_rn(st.imm, e[j]));
+        break;
+      case OP_MUL:
+#pragma unroll
+        for (int j = 0; j < V; ++j) x[j] = __fmul_rn(x[j], e[j]);
+        break;
+      case OP_DIV:
+#pragma unroll
+        for (int j = 0; j < V; ++j) x[j] = __fdiv_rn(x[j], e[j]);
+        break;
+      case OP_NEG:
+#pragma unroll
+        for (int j = 0; j < V; ++j) x[j] = -x[j];
+        break;
+      case OP_RELU:
+#pragma unroll
+        for (int j = 0; j < V; ++j) x[j] = x[j] < 0.0f ? 0.0f : x[j];
+        break;
+      case OP_SQUARE:
+#pragma unroll
+        for (int j = 0; j < V; ++j) x[j] = __fmul_rn(x[j], x[j]);
+        break;
+      case OP_THRESH:
+#pragma unroll
+        for (int j = 0; j < V; ++j) x[j] = e[j] <= st.imm ? 0.0f : x[j];
+        break;
+      default:
+        break;
+    }
+    round_vec<V>(x, st.round);
+  }
+}
+
+// One vector of a task's expression, whichever form the planner chose.
+template <int V>
+__device__ __forceinline__ void eval_expr(const Ctx& c, const Task& t, const int64_t* crd, const float* acc,
+                                          float (&out)[V]) {
+  if (t.chain.valid) {
+    float L[2][V];
+    chain_load<V>(c, t, crd, L);
+    chain_compute<V>(t, L, acc, out);
+  } else {
+    vm_eval<V>(c, t, crd, acc, out);
+  }
+}
+
 // ------------------------------------------------------------- barriers
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -295,38 +452,34 @@ __device__ void record_failure(const Ctx& c, int status, int stage) {
   atomicExch(&c.hdr->abort, 1);
 }
 
-// All blocks meet here; returns false if the kernel must stop.
-__device__ bool grid_barrier(const Ctx& c, int stage, int* s_flag) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int ok = 1;
-    Header* h = c.hdr;
-    unsigned gen = ld_acquire(&h->gen);
-    unsigned arrived = atom_add_acq_rel(&h->count, 1u) + 1u;
-    if (arrived == gridDim.x) {
-      atomicExch(&h->count, 0u);
-      st_release(&h->gen, gen + 1u);
-    } else {
-      long long t0 = global_ns();
-      unsigned spins = 0;
-      while (ld_acquire(&h->gen) == gen) {
-        if ((++spins & 31u) == 0u) {
-          if (*reinterpret_cast<volatile int*>(&h->abort)) {
-            ok = 0;
-            break;
-          }
-          if (global_ns() - t0 > c.timeout_ns) {
-            record_failure(c, TK_ERR_BARRIER_TIMEOUT, stage);
-            ok = 0;
-            break;
-          }
-        }
+// Grid barrier, in two halves so the block can stage the next stage's
+// descriptors while thread 0 waits.  Thread 0 only.
+__device__ __forceinline__ unsigned barrier_arrive(const Ctx& c) {
+  Header* h = c.hdr;
+  unsigned gen = ld_acquire(&h->gen);
+  unsigned arrived = atom_add_acq_rel(&h->count, 1u) + 1u;
+  if (arrived == gridDim.x) {
+    atomicExch(&h->count, 0u);
+    st_release(&h->gen, gen + 1u);
+  }
+  return gen;
+}
+
+// Thread 0 only; false when the wait timed out or another block gave up.
+__device__ __forceinline__ bool barrier_wait(const Ctx& c, unsigned gen, int stage) {
+  Header* h = c.hdr;
+  const long long t0 = global_ns();
+  unsigned spins = 0;
+  while (ld_acquire(&h->gen) == gen) {
+    if ((++spins & 31u) == 0u) {
+      if (*reinterpret_cast<volatile int*>(&h->abort)) return false;
+      if (global_ns() - t0 > c.timeout_ns) {
+        record_failure(c, TK_ERR_BARRIER_TIMEOUT, stage);
+        return false;
       }
     }
-    *s_flag = ok;
   }
-  __syncthreads();
-  return *s_flag != 0;
+  return true;
 }
 
 // ------------------------------------------------------------ block sums
@@ -354,23 +507,95 @@ __device__ __forceinline__ void finish_reduction(const Ctx& c, const Task& t, in
 
 // ------------------------------------------------------------- work items
 
+// Elements per pointwise work item: kThreads threads x V elements x U vectors.
 template <int V>
-__device__ void run_pointwise(const Ctx& c, const Task& t, int item) {
-  int64_t i0 = (int64_t(item) * kThreads + threadIdx.x) * V;
-  if (i0 >= t.numel) return;
+__device__ __forceinline__ constexpr int pointwise_unroll() { return V == 8 ? kPointwiseUnroll : 1; }
+
+// Vectors u = 0..U-1 of the item, software-pipelined: the loads of vector
+// u+1 are in flight while vector u is computed and stored.
+template <int V>
+__device__ __noinline__ void pointwise_chain(const Ctx& c, const Task& t, int item) {
+  constexpr int U = pointwise_unroll<V>();
+  const int64_t base = int64_t(item) * kThreads * V * U + int64_t(threadIdx.x) * V;
+  constexpr int64_t step = int64_t(kThreads) * V;
+  float cur[2][V], nxt[2][V];
   int64_t crd[kMaxRank];
-  unravel(t, i0, crd);
-  float v[V];
-  vm_eval<V>(c, t, crd, nullptr, v);
-  store_out<V>(c, t.out, i0, v);
+  if (base >= t.numel) return;
+  unravel(t, base, crd);
+  chain_load<V>(c, t, crd, cur);
+#pragma unroll 1
+  for (int u = 0; u < U; ++u) {
+    const int64_t i0 = base + u * step;
+    const bool more = u + 1 < U && i0 + step < t.numel;
+    if (more) {
+      unravel(t, i0 + step, crd);
+      chain_load<V>(c, t, crd, nxt);
+    }
+    float v[V];
+    chain_compute<V>(t, cur, nullptr, v);
+    store_out<V>(c, t.out, i0, v);
+    if (!more) break;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      cur[0][j] = nxt[0][j];
+      cur[1][j] = nxt[1][j];
+    }
+  }
 }
 
 template <int V>
-__device__ void run_reduce_row(const Ctx& c, const Task& t, int item, float* red) {
-  const int64_t o = item / t.parts;
-  const int p = item % t.parts;
-  const int64_t r0 = int64_t(p) * t.part_len;
-  const int64_t r1 = min(t.red_inner, r0 + t.part_len);
+__device__ __noinline__ void pointwise_vm(const Ctx& c, const Task& t, int item) {
+  constexpr int U = pointwise_unroll<V>();
+  const int64_t base = int64_t(item) * kThreads * V * U;
+  for (int u = 0; u < U; ++u) {
+    const int64_t i0 = base + (int64_t(u) * kThreads + threadIdx.x) * V;
+    if (i0 >= t.numel) return;
+    int64_t crd[kMaxRank];
+    unravel(t, i0, crd);
+    float v[V];
+    vm_eval<V>(c, t, crd, nullptr, v);
+    store_out<V>(c, t.out, i0, v);
+  }
+}
+
+template <int V>
+__device__ __forceinline__ void run_pointwise(const Ctx& c, const Task& t, int item) {
+  if (t.chain.valid)
+    pointwise_chain<V>(c, t, item);
+  else
+    pointwise_vm<V>(c, t, item);
+}
+
+// This thread's share of one output row of a row reduction, in element order.
+template <int V>
+__device__ __noinline__ float row_sum_chain(const Ctx& c, const Task& t, int64_t o, int64_t r0, int64_t r1) {
+  constexpr int64_t step = int64_t(kThreads) * V;
+  float acc = 0.0f;
+  for (int64_t r = r0 + int64_t(threadIdx.x) * V; r < r1; r += 2 * step) {
+    // two vectors in flight: the second one's loads overlap the first
+    const bool second = r + step < r1;
+    float L0[2][V], L1[2][V], v[V];
+    int64_t crd[kMaxRank];
+    unravel(t, o * t.red_inner + r, crd);
+    chain_load<V>(c, t, crd, L0);
+    if (second) {
+      unravel(t, o * t.red_inner + r + step, crd);
+      chain_load<V>(c, t, crd, L1);
+    }
+    chain_compute<V>(t, L0, nullptr, v);
+#pragma unroll
+    for (int j = 0; j < V; ++j) acc = __fadd_rn(acc, v[j]);
+    if (second) {
+      chain_compute<V>(t, L1, nullptr, v);
+#pragma unroll
+      for (int j = 0; j < V; ++j) acc = __fadd_rn(acc, v[j]);
+    }
+  }
+  return acc;
+}
+
+template <int V>
+__device__ __noinline__ float row_sum_vm(const Ctx& c, const Task& t, int64_t o, int64_t r0, int64_t r1) {
   float acc = 0.0f;
   for (int64_t r = r0 + int64_t(threadIdx.x) * V; r < r1; r += int64_t(kThreads) * V) {
     int64_t crd[kMaxRank];
@@ -380,6 +605,16 @@ __device__ void run_reduce_row(const Ctx& c, const Task& t, int item, float* red
 #pragma unroll
     for (int j = 0; j < V; ++j) acc = __fadd_rn(acc, v[j]);
   }
+  return acc;
+}
+
+template <int V>
+__device__ __noinline__ void run_reduce_row(const Ctx& c, const Task& t, int item, float* red) {
+  const int64_t o = item / t.parts;
+  const int p = item % t.parts;
+  const int64_t r0 = int64_t(p) * t.part_len;
+  const int64_t r1 = min(t.red_inner, r0 + t.part_len);
+  float acc = t.chain.valid ? row_sum_chain<V>(c, t, o, r0, r1) : row_sum_vm<V>(c, t, o, r0, r1);
   acc = block_sum(acc, red);
   if (threadIdx.x == 0) {
     if (t.parts == 1)
@@ -390,7 +625,7 @@ __device__ void run_reduce_row(const Ctx& c, const Task& t, int item, float* red
 }
 
 template <int V>
-__device__ void run_reduce_col(const Ctx& c, const Task& t, int item, float* red) {
+__device__ __noinline__ void run_reduce_col(const Ctx& c, const Task& t, int item, float* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t ch = item / t.parts;
   const int p = item % t.parts;
@@ -406,7 +641,7 @@ __device__ void run_reduce_col(const Ctx& c, const Task& t, int item, float* red
       int64_t crd[kMaxRank];
       unravel(t, r * Q + col0, crd);
       float v[V];
-      vm_eval<V>(c, t, crd, nullptr, v);
+      eval_expr<V>(c, t, crd, nullptr, v);
 #pragma unroll
       for (int j = 0; j < V; ++j) acc[j] = __fadd_rn(acc[j], v[j]);
     }
@@ -429,7 +664,7 @@ __device__ void run_reduce_col(const Ctx& c, const Task& t, int item, float* red
   __syncthreads();
 }
 
-__device__ void run_reduce_final(const Ctx& c, const Task& t, int item, float* red) {
+__device__ __noinline__ void run_reduce_final(const Ctx& c, const Task& t, int item, float* red) {
   const float* part = reinterpret_cast<const float*>(c.ws) + t.scratch;
   if (t.final_block) {
     const int64_t o = item;
@@ -449,7 +684,7 @@ __device__ void run_reduce_final(const Ctx& c, const Task& t, int item, float* r
 // CUDA-core GEMM tile: TM x TM outputs, 16 x 16 threads, (TM/16)^2 each;
 // float32 fmaf accumulation in k order, then the epilogue expression.
 template <int TM>
-__device__ void run_gemm_simt(const Ctx& c, const Task& t, int item, float* smem) {
+__device__ __noinline__ void run_gemm_simt(const Ctx& c, const Task& t, int item, float* smem) {
   constexpr int KT = 16, P = TM + 4, R = TM / 16;
   float* As = smem;           // [KT][P]
   float* Bs = smem + KT * P;  // [KT][P]
@@ -514,11 +749,323 @@ __device__ void run_gemm_simt(const Ctx& c, const Task& t, int item, float* smem
         int64_t crd[kMaxRank] = {row, col, 0, 0};
         float v[1];
         const float a1[1] = {acc[i][j]};
-        vm_eval<1>(c, t, crd, a1, v);
+        eval_expr<1>(c, t, crd, a1, v);
         store_out<1>(c, t.out, row * t.n + col, v);
       }
     }
   }
+}
+
+// ---------------------------------------------------- tcgen05 tile path
+//
+// Warp roles while a stage's tensor-core tiles run (8 warps):
+//   warp 0, lane 0: TMA producer -- waits for a free ring slot, arms its
+//                   "full" mbarrier with the byte count and issues the A/B
+//                   tile loads;
+//   warp 1, lane 0: MMA issuer -- waits for a full slot, issues four
+//                   tcgen05.mma (K = 16 each) into the TMEM accumulator and
+//                   commits the slot back to "empty"; after the last K block
+//                   it commits the accumulator to "acc_full";
+//   warps 4..7:     epilogue -- each reads its 32 TMEM lanes (tile rows) with
+//                   tcgen05.ld, runs the task's epilogue expression on 8
+//                   columns at a time and stores; then frees the accumulator.
+// Two accumulators (2 x 256 TMEM columns) let the epilogue of one tile
+// overlap the MMAs of the next.  Ring and accumulator counters live in the
+// role's registers for the whole kernel, so every stage continues the same
+// phase sequence.
+
+struct TcState {
+  uint32_t ring;                  // shared address of the 1024-aligned ring
+  uint32_t full, empty;           // shared addresses of kStages mbarriers each
+  uint32_t acc_full, acc_empty;   // 2 mbarriers each
+  uint32_t tmem;                  // TMEM base address
+  uint32_t p_it, m_it, m_tile, e_tile;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long timeout_ns) {
+  for (int i = 0; i < 256; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > timeout_ns) return false;
+  return true;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle: start, leading and
+// stride byte offsets in 16-byte units, descriptor version 1 (bit 46),
+// layout SWIZZLE_128B (2 in bits 61-63).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return uint64_t((addr >> 4) & 0x3FFF) | (uint64_t((lbo >> 4) & 0x3FFF) << 16) |
+         (uint64_t((sbo >> 4) & 0x3FFF) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]),
+               "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+               "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+               "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]),
+               "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])::"memory");
+}
+
+// Walk this block's tensor-core tiles of a stage in order (all roles use the
+// same sequence).  fn(task, m0, n0) returns false to stop.
+template <typename F>
+__device__ __forceinline__ void for_my_tiles(const Ctx& c, const Stage& st, F&& fn) {
+  int ti = st.task_begin, base = 0;
+  for (int g = blockIdx.x; g < st.n_tc_items; g += gridDim.x) {
+    while (g >= base + c.tasks[ti].n_items) {
+      base += c.tasks[ti].n_items;
+      ++ti;
+    }
+    const Task& t = c.tasks[ti];
+    const int item = g - base;
+    if (!fn(t, int64_t(item / t.tiles_n) * kTileM, int64_t(item % t.tiles_n) * t.tile_n)) return;
+  }
+}
+
+__device__ __noinline__ void tc_epilogue_tile_chain(const Ctx& c, const Task& t, int64_t m0, int64_t n0,
+                                                    uint32_t taddr) {
+  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
+  const int64_t row = m0 + q * 32 + lane;
+  const bool live = row < t.m;
+  for (int cc = 0; cc < t.tile_n; cc += 32) {
+    uint32_t r[32];
+    __syncwarp();
+    tmem_ld32(taddr + (uint32_t(q * 32) << 16) + uint32_t(cc), r);
+    if (!live) continue;
+    const int64_t col0 = n0 + cc;
+    float cur[2][8], nxt[2][8];
+    int64_t crd[kMaxRank] = {row, col0, 0, 0};
+    if (col0 < t.n) chain_load<8>(c, t, crd, cur);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int64_t col = col0 + 8 * v;
+      if (col >= t.n) break;
+      const bool more = v < 3 && col + 8 < t.n;
+      if (more) {
+        crd[1] = col + 8;
+        chain_load<8>(c, t, crd, nxt);
+      }
+      float a8[8], out[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) a8[j] = __uint_as_float(r[8 * v + j]);
+      chain_compute<8>(t, cur, a8, out);
+      store_out<8>(c, t.out, row * t.n + col, out);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        cur[0][j] = nxt[0][j];
+        cur[1][j] = nxt[1][j];
+      }
+    }
+  }
+}
+
+__device__ __noinline__ void tc_epilogue_tile_any(const Ctx& c, const Task& t, int64_t m0, int64_t n0,
+                                                  uint32_t taddr) {
+  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
+  const int64_t row = m0 + q * 32 + lane;
+  for (int cc = 0; cc < t.tile_n; cc += 32) {
+    uint32_t r[32];
+    __syncwarp();
+    tmem_ld32(taddr + (uint32_t(q * 32) << 16) + uint32_t(cc), r);
+    if (row >= t.m) continue;
+    if (t.vec == 8) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const int64_t col = n0 + cc + 8 * v;
+        if (col < t.n) {
+          float a8[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) a8[j] = __uint_as_float(r[8 * v + j]);
+          int64_t crd[kMaxRank] = {row, col, 0, 0};
+          float out[8];
+          vm_eval<8>(c, t, crd, a8, out);
+          store_out<8>(c, t.out, row * t.n + col, out);
+        }
+      }
+    } else {
+      for (int j = 0; j < 32; ++j) {
+        const int64_t col = n0 + cc + j;
+        if (col < t.n) {
+          const float a1[1] = {__uint_as_float(r[j])};
+          int64_t crd[kMaxRank] = {row, col, 0, 0};
+          float out[1];
+          eval_expr<1>(c, t, crd, a1, out);
+          store_out<1>(c, t.out, row * t.n + col, out);
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tc_epilogue_tile(const Ctx& c, const Task& t, int64_t m0, int64_t n0, uint32_t taddr) {
+  if (t.vec == 8 && t.chain.valid)
+    tc_epilogue_tile_chain(c, t, m0, n0, taddr);
+  else
+    tc_epilogue_tile_any(c, t, m0, n0, taddr);
+}
+
+__device__ __noinline__ bool tc_producer(const Ctx& c, const Stage& st, const CUtensorMap* maps, TcState& ts) {
+  bool ok = true;
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  for_my_tiles(c, st, [&](const Task& t, int64_t m0, int64_t n0) {
+    const uint32_t bytes = uint32_t(kStageBytesA + t.tile_n * kTileK * 2);
+    for (int kb = 0; kb < t.k_blocks; ++kb) {
+      const uint32_t slot = ts.p_it % kStages, ph = ((ts.p_it / kStages) & 1u) ^ 1u;
+      if (!mbar_wait(ts.empty + 8 * slot, ph, c.timeout_ns)) return ok = false;
+      const uint32_t full = ts.full + 8 * slot;
+      mbar_expect_tx(full, bytes);
+      const uint32_t a_dst = ts.ring + slot * (kStageBytesA + kStageBytesB), b_dst = a_dst + kStageBytesA;
+      const int k0 = kb * kTileK;
+      if (!t.a_mn_major) {
+        tma_load_2d(a_dst, &maps[t.tma_a], k0, int(m0), full);
+      } else {
+        tma_load_2d(a_dst, &maps[t.tma_a], int(m0), k0, full);
+        tma_load_2d(a_dst + 8192, &maps[t.tma_a], int(m0) + 64, k0, full);
+      }
+      if (!t.b_mn_major) {
+        tma_load_2d(b_dst, &maps[t.tma_b], k0, int(n0), full);
+      } else {
+        for (int j = 0; j < t.tile_n / 64; ++j) tma_load_2d(b_dst + 8192 * j, &maps[t.tma_b], int(n0) + 64 * j, k0, full);
+      }
+      ++ts.p_it;
+    }
+    return true;
+  });
+  return ok;
+}
+
+__device__ __noinline__ bool tc_mma(const Ctx& c, const Stage& st, TcState& ts, long long* prof) {
+  bool ok = true;
+  bool first = true;
+  for_my_tiles(c, st, [&](const Task& t, int64_t, int64_t) {
+    const uint32_t acc = ts.m_tile & 1u, ph = ((ts.m_tile >> 1) & 1u) ^ 1u;
+    if (!mbar_wait(ts.acc_empty + 8 * acc, ph, c.timeout_ns)) return ok = false;
+    tc_fence_after();
+    const uint32_t d_tmem = ts.tmem + acc * kMaxTileN;
+    for (int kb = 0; kb < t.k_blocks; ++kb) {
+      const uint32_t slot = ts.m_it % kStages, fph = (ts.m_it / kStages) & 1u;
+      if (!mbar_wait(ts.full + 8 * slot, fph, c.timeout_ns)) return ok = false;
+      if (prof && first) prof[3] = global_ns();
+      first = false;
+      tc_fence_after();
+      const uint32_t a_base = ts.ring + slot * (kStageBytesA + kStageBytesB), b_base = a_base + kStageBytesA;
+#pragma unroll
+      for (int k = 0; k < kTileK / 16; ++k) {
+        const uint64_t ad = t.a_mn_major ? smem_desc(a_base + 2048 * k, 8192, 1024) : smem_desc(a_base + 32 * k, 16, 1024);
+        const uint64_t bd = t.b_mn_major ? smem_desc(b_base + 2048 * k, 8192, 1024) : smem_desc(b_base + 32 * k, 16, 1024);
+        umma_f16(d_tmem, ad, bd, t.idesc, uint32_t(kb | k));
+      }
+      umma_commit(ts.empty + 8 * slot);
+      ++ts.m_it;
+    }
+    umma_commit(ts.acc_full + 8 * acc);
+    ++ts.m_tile;
+    return true;
+  });
+  return ok;
+}
+
+__device__ __noinline__ bool tc_epilogue(const Ctx& c, const Stage& st, TcState& ts, long long* prof) {
+  bool ok = true;
+  bool first = true;
+  const int lane = threadIdx.x & 31;
+  for_my_tiles(c, st, [&](const Task& t, int64_t m0, int64_t n0) {
+    const uint32_t acc = ts.e_tile & 1u, ph = (ts.e_tile >> 1) & 1u;
+    if (!mbar_wait(ts.acc_full + 8 * acc, ph, c.timeout_ns)) return ok = false;
+    if (prof && first && threadIdx.x == 128) prof[5] = global_ns();
+    first = false;
+    tc_fence_after();
+    tc_epilogue_tile(c, t, m0, n0, ts.tmem + acc * kMaxTileN);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(ts.acc_empty + 8 * acc);
+    ++ts.e_tile;
+    return true;
+  });
+  return ok;
+}
+
+// Run this block's tensor-core tiles of one stage; false after a wait timed out.
+__device__ bool run_tc_phase(const Ctx& c, const Stage& st, const CUtensorMap* maps, TcState& ts, int stage,
+                             int* s_flag, long long* prof) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  bool ok = true;
+  if (warp == 0 && lane == 0) {
+    ok = tc_producer(c, st, maps, ts);
+    if (prof) prof[2] = global_ns();
+  } else if (warp == 1 && lane == 0) {
+    ok = tc_mma(c, st, ts, prof);
+    if (prof) prof[4] = global_ns();
+  } else if (warp >= 4) {
+    ok = tc_epilogue(c, st, ts, prof);
+    if (prof && threadIdx.x == 128) prof[6] = global_ns();
+  }
+  if (!ok) record_failure(c, TK_ERR_PIPELINE_TIMEOUT, stage);
+  if (threadIdx.x == 0) *s_flag = 1;
+  __syncthreads();
+  if (!ok) *s_flag = 0;
+  __syncthreads();
+  return *s_flag != 0;
 }
 
 __device__ void run_item(const Ctx& c, const Task& t, int item, float* smem) {
@@ -559,34 +1106,159 @@ __device__ void run_item(const Ctx& c, const Task& t, int item, float* smem) {
 
 constexpr int kSmemFloats = 2 * 16 * (64 + 4) > 8 * 256 ? 2 * 16 * (64 + 4) : 8 * 256;
 
-__global__ void __launch_bounds__(kThreads, 1) tk_persistent(const __grid_constant__ Params p) {
+__device__ __forceinline__ void copy_words(void* dst, const void* src, int bytes, int tid, int n) {
+  uint64_t* d = static_cast<uint64_t*>(dst);
+  const uint64_t* q = static_cast<const uint64_t*>(src);
+  for (int i = tid; i < bytes / 8; i += n) d[i] = q[i];
+}
+
+// Copy stage s's tasks, instructions and refs into shared memory (threads
+// first..kThreads-1 take part); ranges that do not fit stay in global memory.
+__device__ __forceinline__ void stage_in(const Program* prog, int s, Stage* s_stage, Task* s_tasks, Instr* s_code,
+                                         Ref* s_refs, int first) {
+  if (int(threadIdx.x) < first) return;
+  const int tid = threadIdx.x - first, n = kThreads - first;
+  const Stage st = prog->stages[s];
+  if (tid == 0) *s_stage = st;
+  if (st.task_end - st.task_begin <= kStageTasks)
+    copy_words(s_tasks, prog->tasks + st.task_begin, (st.task_end - st.task_begin) * int(sizeof(Task)), tid, n);
+  if (st.code_hi - st.code_lo <= kStageCode)
+    copy_words(s_code, prog->code + st.code_lo, (st.code_hi - st.code_lo) * int(sizeof(Instr)), tid, n);
+  if (st.ref_hi - st.ref_lo <= kStageRefs)
+    copy_words(s_refs, prog->refs + st.ref_lo, (st.ref_hi - st.ref_lo) * int(sizeof(Ref)), tid, n);
+}
+
+__device__ __forceinline__ void persistent_body(const Params& p, const CUtensorMap* maps) {
   __shared__ void* s_io[2 * kMaxIO];
   __shared__ __align__(16) float s_work[kSmemFloats];
+  __shared__ Task s_tasks[kStageTasks];
+  __shared__ __align__(16) Instr s_code[kStageCode];
+  __shared__ __align__(16) Ref s_refs[kStageRefs];
+  __shared__ Stage s_stage;
+  __shared__ __align__(8) uint64_t s_bar[2 * kStages + 4];
+  __shared__ uint32_t s_tmem;
   __shared__ int s_flag;
-  for (int i = threadIdx.x; i < 2 * kMaxIO; i += kThreads) s_io[i] = p.io[i];
-  __syncthreads();
-  Ctx c{p.prog, p.ws, reinterpret_cast<Header*>(p.ws), s_io, p.timeout_ns};
+  extern __shared__ __align__(1024) unsigned char s_ring[];
+  const bool tc = maps != nullptr;
+  const int warp = threadIdx.x >> 5;
   const Program* prog = p.prog;
+  const long long entry_ns = global_ns();
+  for (int i = threadIdx.x; i < p.n_in; i += kThreads) s_io[i] = p.io[i];
+  for (int i = threadIdx.x; i < p.n_out; i += kThreads) s_io[kMaxIO + i] = p.io[kMaxIO + i];
+  stage_in(prog, 0, &s_stage, s_tasks, s_code, s_refs, 0);
+  TcState ts{};
+  if (tc) {
+    ts.ring = (smem_u32(s_ring) + 1023u) & ~1023u;
+    ts.full = smem_u32(&s_bar[0]);
+    ts.empty = smem_u32(&s_bar[kStages]);
+    ts.acc_full = smem_u32(&s_bar[2 * kStages]);
+    ts.acc_empty = smem_u32(&s_bar[2 * kStages + 2]);
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < kStages; ++i) {
+        mbar_init(ts.full + 8 * i, 1);
+        mbar_init(ts.empty + 8 * i, 1);
+      }
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(ts.acc_full + 8 * i, 1);
+        mbar_init(ts.acc_empty + 8 * i, 4);
+      }
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (threadIdx.x == 0)
+      for (int i = 0; i < p.n_maps; ++i)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps[i])) : "memory");
+    if (warp == 1) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                   "r"(kTmemCols));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (tc) {
+    tc_fence_after();
+    ts.tmem = s_tmem;
+  }
+  Ctx c{nullptr, nullptr, nullptr, p.ws, reinterpret_cast<Header*>(p.ws), s_io, p.timeout_ns};
+  long long* prof = p.prof ? p.prof + kProfStamps * int64_t(blockIdx.x) : nullptr;
+  const int64_t prof_step = kProfStamps * int64_t(gridDim.x);
+  if (prof && threadIdx.x == 0) prof[7] = entry_ns;
   const int n_stages = prog->n_stages;
   for (int s = 0; s < n_stages; ++s) {
-    const Stage st = prog->stages[s];
+    const Stage st = s_stage;
+    if (prof && threadIdx.x == 0) prof[s * prof_step] = global_ns();
+    c.tasks = st.task_end - st.task_begin <= kStageTasks ? s_tasks - st.task_begin : prog->tasks;
+    c.code = st.code_hi - st.code_lo <= kStageCode ? s_code - st.code_lo : prog->code;
+    c.refs = st.ref_hi - st.ref_lo <= kStageRefs ? s_refs - st.ref_lo : prog->refs;
+    if (tc && st.n_tc_items > 0 && !run_tc_phase(c, st, maps, ts, s, &s_flag, prof ? prof + s * prof_step : nullptr))
+      break;
     int ti = st.task_begin, base = 0;
     for (int g = blockIdx.x; g < st.n_items; g += gridDim.x) {
-      while (ti < st.task_end && g >= base + prog->tasks[ti].n_items) {
-        base += prog->tasks[ti].n_items;
+      if (g < st.n_tc_items) continue;  // handled by the tensor-core phase
+      while (ti < st.task_end && g >= base + c.tasks[ti].n_items) {
+        base += c.tasks[ti].n_items;
         ++ti;
       }
-      run_item(c, prog->tasks[ti], g - base, s_work);
+      run_item(c, c.tasks[ti], g - base, s_work);
     }
-    if (s + 1 < n_stages && !grid_barrier(c, s, &s_flag)) return;
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncthreads();
+    if (prof && threadIdx.x == 0) prof[s * prof_step + 1] = global_ns();
+    if (s + 1 == n_stages) break;
+    unsigned gen = 0;
+    if (threadIdx.x == 0) gen = barrier_arrive(c);
+    stage_in(prog, s + 1, &s_stage, s_tasks, s_code, s_refs, 32);
+    if (threadIdx.x == 0) s_flag = barrier_wait(c, gen, s) ? 1 : 0;
+    __syncthreads();
+    if (!s_flag) break;
   }
+  if (tc) {
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(ts.tmem), "r"(kTmemCols));
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) tk_persistent(const __grid_constant__ Params p) {
+  persistent_body(p, nullptr);
+}
+
+template <int NM>
+struct ParamsTc {
+  Params p;
+  CUtensorMap maps[NM];
+};
+
+template <int NM>
+__global__ void __launch_bounds__(kThreads, 1) tk_persistent_tc(const __grid_constant__ ParamsTc<NM> p) {
+  persistent_body(p.p, p.maps);
 }
 
 }  // namespace tkk
 
 // ------------------------------------------------------------ host side
+//
+// The tensor-core variant passes the TMA descriptors by value as
+// __grid_constant__ parameters; two capacities keep the parameter block small
+// for programs with few GEMMs.
 
-cudaError_t tk_kernel_launch(const tkd::Params& params, int grid, size_t dyn_smem, cudaStream_t stream) {
+namespace {
+constexpr int kSmallMaps = 32;
+
+template <int NM>
+cudaError_t launch_tc(cudaLaunchConfig_t* cfg, const tkd::Params& params, const void* maps, int n_maps) {
+  static thread_local tkk::ParamsTc<NM> big;
+  big.p = params;
+  memcpy(big.maps, maps, size_t(n_maps) * sizeof(CUtensorMap));
+  return cudaLaunchKernelEx(cfg, tkk::tk_persistent_tc<NM>, big);
+}
+}  // namespace
+
+cudaError_t tk_kernel_launch(const tkd::Params& params, const void* maps, int n_maps, int grid, size_t dyn_smem,
+                             cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(tkd::kThreads);
@@ -597,13 +1269,29 @@ cudaError_t tk_kernel_launch(const tkd::Params& params, int grid, size_t dyn_sme
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tkk::tk_persistent, params);
+  if (!maps) return cudaLaunchKernelEx(&cfg, tkk::tk_persistent, params);
+  if (n_maps > tkd::kMaxMaps) return cudaErrorInvalidValue;
+  if (n_maps <= kSmallMaps) return launch_tc<kSmallMaps>(&cfg, params, maps, n_maps);
+  return launch_tc<tkd::kMaxMaps>(&cfg, params, maps, n_maps);
 }
 
-cudaError_t tk_kernel_occupancy(int* blocks_per_sm, size_t dyn_smem) {
+cudaError_t tk_kernel_prepare(bool tc, size_t dyn_smem) {
+  if (!tc) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(tkk::tk_persistent_tc<kSmallMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(dyn_smem));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(tkk::tk_persistent_tc<tkd::kMaxMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(dyn_smem));
+}
+
+cudaError_t tk_kernel_occupancy(int* blocks_per_sm, bool tc, size_t dyn_smem) {
+  if (tc)
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, tkk::tk_persistent_tc<tkd::kMaxMaps>,
+                                                         tkd::kThreads, dyn_smem);
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, tkk::tk_persistent, tkd::kThreads, dyn_smem);
 }
 
-cudaError_t tk_kernel_attributes(cudaFuncAttributes* attr) {
+cudaError_t tk_kernel_attributes(cudaFuncAttributes* attr, bool tc) {
+  if (tc) return cudaFuncGetAttributes(attr, tkk::tk_persistent_tc<tkd::kMaxMaps>);
   return cudaFuncGetAttributes(attr, tkk::tk_persistent);
 }

@@ -805,6 +805,163 @@ class Planner {
     }
   };
 
+  // Builds the linear-chain form of an expression (see tkd::Chain); `fail`
+  // is set when the expression is not a chain with at most two loads.
+  struct ChainBuild {
+    Plan* plan;
+    const Planner* P;
+    int task_ref_begin;
+    tkd::Chain ch{};
+    int root_buf = -1;
+    bool fail = false;
+    bool started = false;
+
+    int add_ref(const tk_tensor_spec& v, const std::vector<int>& dimmap) {
+      Emit e{plan, P, task_ref_begin, {}};
+      return e.add_ref(v, dimmap);
+    }
+    int load_slot(const tk_tensor_spec& v, const std::vector<int>& dimmap) {
+      if (ch.n_loads >= 2) {
+        fail = true;
+        return 0;
+      }
+      ch.load_ref[ch.n_loads] = add_ref(v, dimmap);
+      return ch.n_loads++;
+    }
+    void step(int op, int round, int ext, int second, float imm, float cval) {
+      if (ch.n_steps >= tkd::kChainSteps) {
+        fail = true;
+        return;
+      }
+      tkd::ChainStep& st = ch.steps[ch.n_steps++];
+      st.op = uint8_t(op);
+      st.round = uint8_t(round);
+      st.ext = uint8_t(ext);
+      st.second = uint8_t(second);
+      st.imm = imm;
+      st.cval = cval;
+    }
+    bool is_tree(const Operand& o) const {
+      return !o.scalar && (o.t.buffer_id == root_buf || P->inline_.count(o.t.buffer_id));
+    }
+    // The running value becomes view v.
+    void spine(const tk_tensor_spec& v, const std::vector<int>& dimmap) {
+      if (fail) return;
+      if (v.buffer_id == root_buf) return;
+      if (P->inline_.count(v.buffer_id)) {
+        const Buf& b = P->bufs_.at(v.buffer_id);
+        std::vector<int> of;
+        if (!compose_dims(v, b.shape, &of)) {
+          fail = true;
+          return;
+        }
+        std::vector<int> pmap(b.shape.size(), -1);
+        for (size_t e = 0; e < of.size(); ++e) pmap[e] = of[e] >= 0 ? dimmap[of[e]] : -1;
+        spine_op(P->ops_[b.producer], pmap);
+        return;
+      }
+      if (started || ch.n_loads) {
+        fail = true;
+        return;
+      }
+      ch.start = tkd::CH_LOAD;
+      load_slot(v, dimmap);
+      started = true;
+    }
+    std::vector<int> operand_map(const OpInfo& op, const Operand& o, const std::vector<int>& outmap) const {
+      std::vector<int> m(o.t.rank, -1);
+      for (int d = 0; d < o.t.rank; ++d) m[d] = o.t.shape[d] == 1 ? -1 : outmap[d + op.out.rank - o.t.rank];
+      return m;
+    }
+    void spine_op(const OpInfo& op, const std::vector<int>& outmap) {
+      if (fail) return;
+      const int rd = op.out.dtype;
+      auto start_const = [&](double v) {
+        if (started) {
+          fail = true;
+          return;
+        }
+        ch.start = tkd::CH_CONST;
+        ch.start_const = f32(v);
+        started = true;
+      };
+      auto unary_spine = [&](const Operand& o) {
+        if (o.scalar)
+          start_const(o.value);
+        else
+          spine(o.t, operand_map(op, o, outmap));
+      };
+      switch (op.kind) {
+        case TK_OP_NEG:
+        case TK_OP_RELU:
+        case TK_OP_CAST:
+          unary_spine(op.in[0]);
+          step(op.kind == TK_OP_NEG ? tkd::OP_NEG : op.kind == TK_OP_RELU ? tkd::OP_RELU : tkd::OP_MOV, rd, 0, 0, 0.f,
+               0.f);
+          return;
+        case TK_OP_POW: {
+          double e = op.in.size() > 1 ? op.in[1].value : op.exponent;
+          if (e != 2.0) {  // general powf stays in the instruction form
+            fail = true;
+            return;
+          }
+          unary_spine(op.in[0]);
+          step(tkd::OP_SQUARE, rd, 0, 0, f32(e), 0.f);
+          return;
+        }
+        case TK_OP_FULL:
+          start_const(op.in.empty() ? op.value : op.in[0].value);
+          step(tkd::OP_MOV, rd, 0, 0, 0.f, 0.f);
+          return;
+        default:
+          break;
+      }
+      const Operand &o0 = op.in[0], &o1 = op.in[1];
+      const bool t0 = is_tree(o0), t1 = is_tree(o1);
+      if (t0 && t1) {
+        fail = true;
+        return;
+      }
+      const int side = t0 ? 0 : t1 ? 1 : (o0.scalar ? 1 : 0);
+      const Operand& sp = side == 0 ? o0 : o1;
+      const Operand& other = side == 0 ? o1 : o0;
+      unary_spine(sp);
+      int ext;
+      float cval = 0.f;
+      if (other.scalar) {
+        ext = tkd::EXT_CONST;
+        cval = f32(other.value);
+      } else {
+        ext = load_slot(other.t, operand_map(op, other, outmap)) == 0 ? tkd::EXT_LOAD0 : tkd::EXT_LOAD1;
+      }
+      const int code = op.kind == TK_OP_ADD ? tkd::OP_ADD
+                       : op.kind == TK_OP_SUB ? tkd::OP_SUB
+                       : op.kind == TK_OP_MUL ? tkd::OP_MUL
+                       : op.kind == TK_OP_DIV ? tkd::OP_DIV
+                                              : tkd::OP_THRESH;
+      const float imm = (op.kind == TK_OP_ADD || op.kind == TK_OP_SUB) ? f32(op.alpha)
+                        : op.kind == TK_OP_THRESHOLD_BACKWARD        ? f32(op.threshold)
+                                                                     : 0.f;
+      step(code, rd, ext, side, imm, cval);
+    }
+  };
+
+  // Chain form of task t's expression into t.chain; false leaves no trace.
+  template <typename F>
+  bool try_chain(Plan& plan, Task& t, F&& build) const {
+    ChainBuild cb{&plan, this, t.ref_begin};
+    build(cb);
+    if (cb.fail) {
+      plan.refs.resize(t.ref_begin);
+      return false;
+    }
+    cb.ch.valid = 1;
+    t.chain = cb.ch;
+    t.code_len = 0;
+    t.n_refs = int(plan.refs.size()) - t.ref_begin;
+    return true;
+  }
+
   static std::vector<int> identity_map(int rank) {
     std::vector<int> m(rank);
     for (int d = 0; d < rank; ++d) m[d] = d;
@@ -817,6 +974,7 @@ class Planner {
     t.rank = int(space.size());
     for (int d = 0; d < t.rank; ++d) t.shape[d] = space[d];
     t.numel = numel_of(space);
+    if (t.numel >= (int64_t(1) << 31)) throw Error(TK_ERR_UNSUPPORTED, "tensors of 2^31 or more elements");
     t.vec = (t.rank >= 1 && t.shape[t.rank - 1] % 8 == 0 && t.numel > 0) ? 8 : 1;
     t.tma_a = t.tma_b = -1;
     return t;
@@ -850,7 +1008,10 @@ class Planner {
     }
   }
 
-  int items_pointwise(const Task& t) const { return int(ceil_div(t.numel, int64_t(tkd::kThreads) * t.vec)); }
+  int items_pointwise(const Task& t) const {
+    const int64_t per = int64_t(tkd::kThreads) * t.vec * (t.vec == 8 ? tkd::kPointwiseUnroll : 1);
+    return int(ceil_div(t.numel, per));
+  }
 
   // A pointwise task computing `op` (or copying a view when op == nullptr).
   Task lower_pointwise(Plan& plan, const OpInfo* op, const tk_tensor_spec* copy_src, const Shape& space,
@@ -858,19 +1019,102 @@ class Planner {
     Task t = new_task(tkd::T_POINTWISE, space);
     t.code_begin = int(plan.code.size());
     t.ref_begin = int(plan.refs.size());
-    Emit e{&plan, this, t.ref_begin, space};
-    if (op) {
-      e.op_value(*op, identity_map(int(space.size())), 0);
-    } else {
-      e.value(*copy_src, identity_map(copy_src->rank), 0);
-      e.push(tkd::OP_MOV, 0, 0, 0, round);
+    bool chained = try_chain(plan, t, [&](ChainBuild& cb) {
+      if (op) {
+        cb.spine_op(*op, identity_map(int(space.size())));
+      } else {
+        cb.spine(*copy_src, identity_map(copy_src->rank));
+        cb.step(tkd::OP_MOV, round, 0, 0, 0.f, 0.f);
+      }
+    });
+    if (!chained) {
+      Emit e{&plan, this, t.ref_begin, space};
+      if (op) {
+        e.op_value(*op, identity_map(int(space.size())), 0);
+      } else {
+        e.value(*copy_src, identity_map(copy_src->rank), 0);
+        e.push(tkd::OP_MOV, 0, 0, 0, round);
+      }
+      t.code_len = int(plan.code.size()) - t.code_begin;
+      t.n_refs = int(plan.refs.size()) - t.ref_begin;
     }
-    t.code_len = int(plan.code.size()) - t.code_begin;
-    t.n_refs = int(plan.refs.size()) - t.ref_begin;
     t.out = out;
     finish_refs(plan, t);
     t.n_items = items_pointwise(t);
     return t;
+  }
+
+  // TMA view of one GEMM operand: the contiguous dim is the box's inner dim.
+  // A is [M,K], B is [K,N]; "K-major" means K is the contiguous dim.
+  bool tma_operand(const tk_tensor_spec& v, bool is_a, int box_rows, TmaOperand* out, bool* mn_major) const {
+    int64_t base;
+    int space, slot;
+    location(v.buffer_id, &space, &slot, &base);
+    base += v.offset;
+    const int k_dim = is_a ? 1 : 0, mn_dim = is_a ? 0 : 1;
+    TmaOperand o{};
+    o.space = space;
+    o.slot = slot;
+    o.base_elems = base;
+    o.dtype = v.dtype;
+    o.box_inner = tkd::kTileK;
+    if (v.strides[k_dim] == 1 && v.shape[k_dim] >= 1) {
+      *mn_major = false;
+      o.inner = v.shape[k_dim];
+      o.outer = v.shape[mn_dim];
+      o.outer_stride = v.strides[mn_dim];
+      o.box_outer = box_rows;
+    } else if (v.strides[mn_dim] == 1) {
+      *mn_major = true;
+      o.inner = v.shape[mn_dim];
+      o.outer = v.shape[k_dim];
+      o.outer_stride = v.strides[k_dim];
+      o.box_outer = tkd::kTileK;
+    } else {
+      return false;
+    }
+    if (o.outer <= 1) o.outer_stride = round_up(std::max<int64_t>(o.inner, 8), 8);
+    // TMA: 16-byte aligned start and row pitch, at least 16 bytes per row
+    if (base % 8 || o.outer_stride % 8 || o.inner < 8 || o.outer_stride < o.inner) return false;
+    if (o.inner >= (int64_t(1) << 32) || o.outer >= (int64_t(1) << 32)) return false;
+    *out = o;
+    return true;
+  }
+
+  bool try_tensor_core(Plan& plan, Task& t, const tk_tensor_spec& A, const tk_tensor_spec& B) const {
+    if (!opt_.tensor_cores || A.dtype != B.dtype || (A.dtype != TK_BF16 && A.dtype != TK_F16)) return false;
+    const int64_t M = t.m, N = t.n, K = t.k;
+    if (M < 1 || N < 1 || K < 1) return false;
+    if (plan.tma.size() + 2 > size_t(tkd::kMaxMaps)) return false;
+    // widest N tile that still spreads the tiles over the SMs
+    int bn = 64;
+    for (int cand : {256, 128}) {
+      if (ceil_div(M, tkd::kTileM) * ceil_div(N, cand) >= (cand == 256 ? sms_ : sms_ / 2)) {
+        bn = cand;
+        break;
+      }
+    }
+    TmaOperand ta, tb;
+    bool a_mn = false, b_mn = false;
+    if (!tma_operand(A, true, tkd::kTileM, &ta, &a_mn) || !tma_operand(B, false, bn, &tb, &b_mn)) return false;
+    t.kind = tkd::T_GEMM_TC;
+    t.tile_m = tkd::kTileM;
+    t.tile_n = bn;
+    t.tiles_n = int(ceil_div(N, bn));
+    t.k_blocks = int(ceil_div(K, tkd::kTileK));
+    t.n_items = int(ceil_div(M, tkd::kTileM) * t.tiles_n);
+    t.a_mn_major = a_mn;
+    t.b_mn_major = b_mn;
+    t.tma_a = int(plan.tma.size());
+    plan.tma.push_back(ta);
+    t.tma_b = int(plan.tma.size());
+    plan.tma.push_back(tb);
+    // instruction descriptor, kind::f16: D f32 (bits 4-5), A/B type (7-9, 10-12:
+    // 0 f16, 1 bf16), A/B MN-major (15, 16), N >> 3 (17-22), M >> 4 (24-28)
+    uint32_t ab = A.dtype == TK_BF16 ? 1u : 0u;
+    t.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) |
+              (uint32_t(bn >> 3) << 17) | (uint32_t(tkd::kTileM >> 4) << 24);
+    return true;
   }
 
   Task lower_gemm(Plan& plan, const OpInfo& mm) {
@@ -897,22 +1141,69 @@ class Planner {
     t.b = operand_ref(B);
     t.a_kcontig = A.strides[1] == 1 || A.shape[0] <= 1;
     t.b_ncontig = B.strides[1] == 1 || B.shape[0] <= 1;
-    // tile: the largest of 64/32/16 that still gives every SM a tile
-    int tile = 16;
-    for (int cand : {64, 32}) {
-      if (ceil_div(M, cand) * ceil_div(N, cand) >= sms_) {
-        tile = cand;
-        break;
+    if (!try_tensor_core(plan, t, A, B)) {
+      // CUDA-core tile: the largest of 64/32/16 that still gives every SM a tile
+      int tile = 16;
+      for (int cand : {64, 32}) {
+        if (ceil_div(M, cand) * ceil_div(N, cand) >= sms_) {
+          tile = cand;
+          break;
+        }
       }
+      t.tile_m = t.tile_n = tile;
+      t.tiles_n = int(ceil_div(N, tile));
+      t.n_items = int(ceil_div(M, tile) * ceil_div(N, tile));
     }
-    t.tile_m = t.tile_n = tile;
-    t.tiles_n = int(ceil_div(N, tile));
-    t.n_items = int(ceil_div(M, tile) * ceil_div(N, tile));
     if (M == 0 || N == 0) t.n_items = 0;
 
     // epilogue: addmm formula, rounding to the GEMM dtype, then the chain
     t.code_begin = int(plan.code.size());
     t.ref_begin = int(plan.refs.size());
+    auto fused_it = fused_.find(mm.index);
+    bool chained = try_chain(plan, t, [&](ChainBuild& cb) {
+      tkd::Chain& ch = cb.ch;
+      ch.start = tkd::CH_ACC;
+      ch.round0 = mm.out.dtype;
+      ch.alpha = f32(mm.alpha);
+      ch.beta = f32(mm.beta);
+      ch.bias = -1;
+      cb.started = true;
+      if (mm.kind == TK_OP_MM) {
+        ch.addmm_mode = tkd::AM_ACC;
+      } else {
+        ch.addmm_mode = (mm.alpha == 0.0 && mm.beta == 0.0) ? tkd::AM_ZERO
+                        : mm.beta == 0.0                   ? tkd::AM_ALPHA
+                        : mm.alpha == 0.0                  ? tkd::AM_BETA
+                        : (mm.alpha == 1.0 && mm.beta == 1.0) ? tkd::AM_SUM
+                                                             : tkd::AM_FULL;
+        const Operand& o = mm.in[0];
+        if (ch.addmm_mode != tkd::AM_ZERO && ch.addmm_mode != tkd::AM_ALPHA) {
+          if (o.scalar) {
+            ch.bias = 2;
+            ch.bias_const = f32(o.value);
+          } else if (inline_.count(o.t.buffer_id)) {
+            cb.fail = true;
+          } else {
+            std::vector<int> m(o.t.rank, -1);
+            for (int d = 0; d < o.t.rank; ++d) m[d] = o.t.shape[d] == 1 ? -1 : d + 2 - o.t.rank;
+            ch.bias = cb.load_slot(o.t, m);
+          }
+        }
+      }
+      int root = mm.out.buffer_id;
+      if (fused_it != fused_.end())
+        for (int ci : fused_it->second.chain) {
+          cb.root_buf = root;
+          cb.spine_op(ops_[ci], identity_map(2));
+          root = ops_[ci].out.buffer_id;
+        }
+    });
+    if (chained) {
+      int out_buf = fused_it != fused_.end() ? fused_it->second.final_buf : mm.out.buffer_id;
+      t.out = out_ref(out_buf);
+      finish_refs(plan, t);
+      return t;
+    }
     Emit e{&plan, this, t.ref_begin, space};
     std::vector<int> idmap = identity_map(2);
     int rd = mm.out.dtype;
@@ -999,10 +1290,12 @@ class Planner {
     Task t = new_task(row ? tkd::T_REDUCE_ROW : tkd::T_REDUCE_COL, space);
     t.code_begin = int(plan.code.size());
     t.ref_begin = int(plan.refs.size());
-    Emit e{&plan, this, t.ref_begin, space};
-    e.value(src, dimmap, 0);
-    t.code_len = int(plan.code.size()) - t.code_begin;
-    t.n_refs = int(plan.refs.size()) - t.ref_begin;
+    if (!try_chain(plan, t, [&](ChainBuild& cb) { cb.spine(src, dimmap); })) {
+      Emit e{&plan, this, t.ref_begin, space};
+      e.value(src, dimmap, 0);
+      t.code_len = int(plan.code.size()) - t.code_begin;
+      t.n_refs = int(plan.refs.size()) - t.ref_begin;
+    }
     t.out = out_ref(op.out.buffer_id);
     t.red_mean = op.kind == TK_OP_MEAN;
     t.size_f = float(double(n_red));
@@ -1176,7 +1469,17 @@ class Planner {
       });
       Stage S{};
       S.task_begin = int(plan.tasks.size());
+      S.code_lo = S.ref_lo = INT32_MAX;
+      S.code_hi = S.ref_hi = 0;
       for (auto& t : st) {
+        if (t.code_len) {
+          S.code_lo = std::min(S.code_lo, t.code_begin);
+          S.code_hi = std::max(S.code_hi, t.code_begin + t.code_len);
+        }
+        if (t.n_refs) {
+          S.ref_lo = std::min(S.ref_lo, t.ref_begin);
+          S.ref_hi = std::max(S.ref_hi, t.ref_begin + t.n_refs);
+        }
         S.n_items += t.n_items;
         if (t.kind == tkd::T_GEMM_TC) {
           S.n_tc_items += t.n_items;
@@ -1185,6 +1488,8 @@ class Planner {
         plan.tasks.push_back(t);
       }
       S.task_end = int(plan.tasks.size());
+      if (S.code_lo > S.code_hi) S.code_lo = S.code_hi = 0;
+      if (S.ref_lo > S.ref_hi) S.ref_lo = S.ref_hi = 0;
       plan.stages.push_back(S);
       plan.max_items = std::max(plan.max_items, S.n_items);
     }
@@ -1192,6 +1497,7 @@ class Planner {
     plan.arena_units = arena_total_;
     plan.workspace_units = tkd::kHeaderUnits + arena_total_ + scratch;
     plan.uses_tc = tc_ops > 0;
+    plan.smem_bytes = plan.uses_tc ? size_t(tkd::kTcSmemBytes) : 0;
     for (const auto& s : inputs_) plan.input_bytes.push_back(extent_of(s) * esize(s.dtype));
     for (const auto& s : outputs_) plan.output_bytes.push_back(numel(s) * esize(s.dtype));
     for (const auto& kv : inplace_) plan.inplace.push_back({kv.first, kv.second});

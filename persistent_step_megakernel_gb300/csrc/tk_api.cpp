@@ -7,9 +7,11 @@
 // in-place target not shared with another input, and no overlap between
 // outputs, the workspace and inputs.  With raw pointers the check is on byte
 // ranges instead of torch storages.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <mutex>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -30,6 +32,11 @@ struct tk_program {
   size_t dyn_smem = 0;
   void* d_table = nullptr;
   const tkd::Program* d_prog = nullptr;
+  // TMA descriptors of the last run and the base pointers they encode
+  std::vector<CUtensorMap> maps;
+  std::vector<const void*> map_bases;
+  // optional per-stage stamps at the end of the workspace (float units)
+  int64_t prof_offset = -1;
 };
 
 namespace {
@@ -95,6 +102,53 @@ tk_status upload(tk_program* p) {
   }
   p->d_table = dev;
   p->d_prog = reinterpret_cast<const tkd::Program*>(base + off_prog);
+  return TK_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, through the runtime's entry-point query.
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Encode every TMA operand of the plan for these base pointers (cached).
+tk_status encode_maps(tk_program* p, const void* const* inputs, void* const* outputs, float* ws) {
+  const auto& ops = p->plan.tma;
+  std::vector<const void*> bases(ops.size());
+  for (size_t i = 0; i < ops.size(); ++i) {
+    const auto& o = ops[i];
+    bases[i] = o.space == tkd::SP_IN ? inputs[o.slot] : o.space == tkd::SP_OUT ? outputs[o.slot] : ws;
+  }
+  if (bases == p->map_bases && p->maps.size() == ops.size()) return TK_OK;
+  EncodeTiledFn fn = encoder();
+  if (!fn) return fail(TK_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  std::vector<CUtensorMap> maps(ops.size());
+  for (size_t i = 0; i < ops.size(); ++i) {
+    const auto& o = ops[i];
+    char* addr = static_cast<char*>(const_cast<void*>(bases[i])) + o.base_elems * 2;
+    cuuint64_t dims[2] = {cuuint64_t(o.inner), cuuint64_t(o.outer)};
+    cuuint64_t strides[1] = {cuuint64_t(o.outer_stride) * 2};
+    cuuint32_t box[2] = {cuuint32_t(o.box_inner), cuuint32_t(o.box_outer)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(&maps[i], o.dtype == TK_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    2, addr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(TK_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string(int(r)) + ")");
+  }
+  p->maps.swap(maps);
+  p->map_bases.swap(bases);
   return TK_OK;
 }
 
@@ -172,7 +226,8 @@ tk_status tk_program_create(const tk_program_desc* desc, const tk_options* opt_i
   int occupancy = 1;
   if (device >= 0) {
     DeviceGuard g(device);
-    cudaError_t e = tk_kernel_occupancy(&occupancy, p->dyn_smem);
+    cudaError_t e = tk_kernel_prepare(p->plan.uses_tc, p->dyn_smem);
+    if (e == cudaSuccess) e = tk_kernel_occupancy(&occupancy, p->plan.uses_tc, p->dyn_smem);
     if (e != cudaSuccess) {
       delete p;
       return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
@@ -192,6 +247,12 @@ tk_status tk_program_create(const tk_program_desc* desc, const tk_options* opt_i
   if (opt.max_blocks > 0) grid = std::min<int64_t>(grid, opt.max_blocks);
   p->grid = int(std::max<int64_t>(grid, 1));
   p->plan.stats.grid_blocks = p->grid;
+  if (opt.profile) {
+    p->prof_offset = p->plan.workspace_units;
+    int64_t units = int64_t(p->plan.stages.size()) * p->grid * 2 * tkd::kProfStamps;  // int64 stamps
+    p->plan.workspace_units += (units + 63) / 64 * 64;
+    p->plan.stats.workspace_elements = p->plan.workspace_units;
+  }
   *out = p;
   return TK_OK;
 }
@@ -274,12 +335,21 @@ tk_status tk_run(tk_program* p, const void* const* inputs, int32_t n_inputs, voi
   prm.prog = p->d_prog;
   prm.ws = reinterpret_cast<char*>(ws);
   prm.timeout_ns = static_cast<long long>(p->opt.barrier_timeout_s * 1e9);
+  prm.prof = p->prof_offset >= 0 ? reinterpret_cast<long long*>(ws + p->prof_offset) : nullptr;
   prm.n_in = n_inputs;
   prm.n_out = n_outputs;
   for (int i = 0; i < n_inputs; ++i) prm.io[i] = const_cast<void*>(inputs[i]);
   for (int j = 0; j < n_outputs; ++j) prm.io[tkd::kMaxIO + j] = outputs[j];
   DeviceGuard g(p->device);
-  cudaError_t e = tk_kernel_launch(prm, p->grid, p->dyn_smem, static_cast<cudaStream_t>(stream));
+  const void* maps = nullptr;
+  if (p->plan.uses_tc) {
+    tk_status s = encode_maps(p, inputs, outputs, ws);
+    if (s != TK_OK) return s;
+    maps = p->maps.data();
+    prm.n_maps = int(p->maps.size());
+  }
+  cudaError_t e = tk_kernel_launch(prm, maps, int(p->maps.size()), p->grid, p->dyn_smem,
+                                   static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cooperative launch");
   return TK_OK;
 }
@@ -303,15 +373,29 @@ tk_status tk_resource_usage(const tk_program* p, int64_t out[4]) {
   if (p->device < 0) return fail(TK_ERR_DEVICE, "plan-only program (created with device -1)");
   DeviceGuard g(p->device);
   cudaFuncAttributes a;
-  cudaError_t e = tk_kernel_attributes(&a);
+  cudaError_t e = tk_kernel_attributes(&a, p->plan.uses_tc);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes");
   int occ = 0;
-  e = tk_kernel_occupancy(&occ, p->dyn_smem);
+  e = tk_kernel_occupancy(&occ, p->plan.uses_tc, p->dyn_smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
   out[0] = a.numRegs;
   out[1] = int64_t(a.localSizeBytes);
   out[2] = int64_t(a.sharedSizeBytes) + int64_t(p->dyn_smem);
   out[3] = occ;
+  return TK_OK;
+}
+
+tk_status tk_profile_read(const tk_program* p, const float* ws, void* stream, int64_t* stamps, size_t n) {
+  if (!p || !ws || !stamps) return fail(TK_ERR_INVALID, "program, workspace and stamps must not be NULL");
+  if (p->device < 0) return fail(TK_ERR_DEVICE, "plan-only program (created with device -1)");
+  if (p->prof_offset < 0) return fail(TK_ERR_INVALID, "program was created without profile = 1");
+  size_t need = size_t(tkd::kProfStamps) * p->plan.stages.size() * size_t(p->grid);
+  if (n < need) return fail(TK_ERR_INVALID, "stamps array too small: need " + std::to_string(need));
+  DeviceGuard g(p->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(stamps, ws + p->prof_offset, need * sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading profile stamps");
   return TK_OK;
 }
 

@@ -14,9 +14,23 @@ namespace tkd {
 
 constexpr int kThreads = 256;      // threads per block (8 warps)
 constexpr int kMaxRank = 4;
-constexpr int kVmRegs = 6;         // expression registers per element
+constexpr int kVmRegs = 4;         // expression registers per element
+constexpr int kPointwiseUnroll = 4; // 8-element vectors per thread in a pointwise item
 constexpr int kHeaderUnits = 64;   // workspace header: 64 floats = 256 bytes
 constexpr int kMaxIO = 256;        // program inputs (and outputs) per launch
+
+// tcgen05 tile path: a 128 x BN output tile (BN = 64, 128 or 256) accumulates
+// in TMEM over K blocks of 64 bf16/fp16 elements (one 128-byte swizzle row)
+// staged by TMA through a kStages-deep shared-memory ring.
+constexpr int kTileM = 128;
+constexpr int kTileK = 64;
+constexpr int kMaxTileN = 256;
+constexpr int kStages = 4;
+constexpr int kStageBytesA = kTileM * kTileK * 2;       // 16 KB
+constexpr int kStageBytesB = kMaxTileN * kTileK * 2;    // 32 KB
+constexpr int kTcSmemBytes = kStages * (kStageBytesA + kStageBytesB) + 1024;
+constexpr int kTmemCols = 2 * kMaxTileN;                // double-buffered accumulator
+constexpr int kMaxMaps = 192;                           // TMA descriptors per launch
 
 // Where a referenced tensor lives.
 enum Space : int32_t { SP_IN = 0, SP_OUT = 1, SP_WS = 2 };
@@ -61,6 +75,41 @@ struct Instr {
   int32_t ref;
 };
 
+// Linear-chain form of an expression, evaluated by compiled code instead of
+// the instruction loop: a start value (the GEMM accumulator through the addmm
+// formula, a load, or a constant), then up to kChainSteps ops, each combining
+// the running value with nothing, a loaded operand or a constant.  At most two
+// operand loads per element, which the kernel issues before any arithmetic.
+constexpr int kChainSteps = 4;
+
+enum ChainStart : int32_t { CH_ACC = 0, CH_LOAD = 1, CH_CONST = 2 };
+enum ChainExt : uint8_t { EXT_NONE = 0, EXT_LOAD0 = 1, EXT_LOAD1 = 2, EXT_CONST = 3 };
+enum AddmmMode : int32_t { AM_ACC = 0, AM_FULL = 1, AM_ZERO = 2, AM_ALPHA = 3, AM_BETA = 4, AM_SUM = 5 };
+
+struct ChainStep {
+  uint8_t op;       // Opcode (OP_ADD ... OP_THRESH, OP_MOV for a cast)
+  uint8_t round;    // tk_dtype of the result
+  uint8_t ext;      // ChainExt
+  uint8_t second;   // 1: the running value is the op's second operand
+  float imm;        // alpha (add/sub), threshold, exponent
+  float cval;       // constant operand (EXT_CONST)
+};
+
+struct Chain {
+  int32_t valid;
+  int32_t n_loads;
+  int32_t load_ref[2];   // task-relative refs of the two load slots
+  int32_t start;         // ChainStart; CH_LOAD reads slot 0
+  float start_const;
+  int32_t bias;          // addmm bias: -1 none, 0/1 load slot, 2 constant
+  float bias_const;
+  float alpha, beta;
+  int32_t addmm_mode;    // AddmmMode
+  int32_t round0;        // dtype of the start value
+  int32_t n_steps;
+  ChainStep steps[kChainSteps];
+};
+
 enum TaskKind : int32_t {
   T_POINTWISE = 0,     // out[i] = expr(i)
   T_REDUCE_ROW = 1,    // reduce the innermost index dims; item = (output, part)
@@ -70,7 +119,7 @@ enum TaskKind : int32_t {
   T_GEMM_TC = 5        // tcgen05 GEMM + epilogue expression
 };
 
-struct Task {
+struct alignas(16) Task {
   int32_t kind;
   int32_t n_items;
   int32_t rank;              // index-space rank (0..4)
@@ -79,6 +128,7 @@ struct Task {
   int64_t numel;
   int32_t code_begin, code_len;
   int32_t ref_begin, n_refs;
+  Chain chain;               // used instead of the instructions when valid
   Ref out;                   // contiguous output, addressed by flat output index
   // reductions
   int32_t red_mean;          // 1: divide by size_f
@@ -105,7 +155,15 @@ struct Stage {
   int32_t task_begin, task_end;
   int32_t n_items;           // all items of the stage (tensor-core tiles first)
   int32_t n_tc_items;
+  int32_t code_lo, code_hi;  // instructions the stage's tasks use
+  int32_t ref_lo, ref_hi;    // operand refs the stage's tasks use
 };
+
+// A stage whose descriptors fit these bounds is copied into shared memory
+// while the previous grid barrier completes.
+constexpr int kStageTasks = 16;
+constexpr int kStageCode = 128;
+constexpr int kStageRefs = 64;
 
 struct Program {
   int32_t n_stages, n_tasks, n_code, n_refs;
@@ -127,11 +185,17 @@ struct Header {
 };
 
 // Kernel arguments: io[i] is input i, io[kMaxIO + j] is output j.
+// Profile stamps per (stage, block): 0 stage begin, 1 barrier arrival,
+// 2 producer done, 3 first operand tile ready, 4 MMA issue done, 5 first
+// accumulator ready, 6 epilogue done, 7 kernel entry (stage 0 only).
+constexpr int kProfStamps = 8;
+
 struct Params {
   const Program* prog;
   char* ws;
   long long timeout_ns;
-  int n_in, n_out;
+  long long* prof;      // optional stamps, [stage][block][kProfStamps]
+  int n_in, n_out, n_maps;
   void* io[2 * kMaxIO];
 };
 

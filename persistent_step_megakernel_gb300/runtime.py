@@ -79,6 +79,24 @@ class TrainStep:
                  workspace.data_ptr(), workspace.numel(), self._stream(stream))
         return outputs
 
+    def profile(self, workspace, stream=None) -> dict:
+        """Per-stage timing of the last run (program created with profile=1).
+
+        work_us[s]: first block starting stage s -> last block reaching the
+        barrier after it; barrier_us[s]: last arrival at barrier s -> first
+        block starting stage s+1.
+        """
+        st = self.stats
+        stamps = B.tk_profile_read(self.handle, workspace.data_ptr(), st["stages"], st["grid_blocks"],
+                                   self._stream(stream))
+        begin = [min(r[0] for r in row) for row in stamps]
+        arrive = [max(r[1] for r in row) for row in stamps]
+        work = [(a - b) / 1e3 for b, a in zip(begin, arrive)]
+        barrier = [(begin[s + 1] - arrive[s]) / 1e3 for s in range(len(stamps) - 1)]
+        entry = min(r[7] for r in stamps[0])
+        return {"work_us": work, "barrier_us": barrier, "total_us": (arrive[-1] - begin[0]) / 1e3,
+                "prologue_us": (begin[0] - entry) / 1e3, "stamps": stamps}
+
     def status(self, workspace, stream=None):
         return B.tk_run_status(self.handle, workspace.data_ptr(), self._stream(stream))
 

@@ -195,12 +195,12 @@ def mlp_step_program(cfg: MLPConfig, export: str = "state", dtype: str | None = 
         d = emit("d", "sub", (out, y), (B, dims[-1]))
         sq = emit("sq", "pow", (d, 2), (B, dims[-1]))
         loss = emit("loss", "mean", (sq,), ())
-        g = emit(f"g{L}", "mul", (d, 2.0 / n_out), (B, dims[-1]))
+        g = emit(f"g{L}", "mul", (d, 2.0 / n_out if n_out else 0.0), (B, dims[-1]))
     elif cfg.loss == "mean_square_residual":
         r = emit("out", "add", (out, x), (B, dims[-1]))
         sq = emit("sq", "pow", (r, 2), (B, dims[-1]))
         loss = emit("loss", "mean", (sq,), ())
-        g = emit(f"g{L}", "mul", (r, 2.0 / n_out), (B, dims[-1]))
+        g = emit(f"g{L}", "mul", (r, 2.0 / n_out if n_out else 0.0), (B, dims[-1]))
     else:
         raise ValueError(cfg.loss)
 

@@ -428,18 +428,10 @@ __device__ __forceinline__ void eval_expr(const Ctx& c, const Task& t, const int
 
 // ------------------------------------------------------------- barriers
 
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
   unsigned old;
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
-}
-__device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ long long global_ns() {
   long long t;
@@ -453,33 +445,47 @@ __device__ void record_failure(const Ctx& c, int status, int stage) {
 }
 
 // Grid barrier, in two halves so the block can stage the next stage's
-// descriptors while thread 0 waits.  Thread 0 only.
-__device__ __forceinline__ unsigned barrier_arrive(const Ctx& c) {
-  Header* h = c.hdr;
-  unsigned gen = ld_acquire(&h->gen);
-  unsigned arrived = atom_add_acq_rel(&h->count, 1u) + 1u;
-  if (arrived == gridDim.x) {
-    atomicExch(&h->count, 0u);
-    st_release(&h->gen, gen + 1u);
-  }
-  return gen;
+// descriptors while thread 0 waits.  Barrier j of a run completes when the
+// arrival counter reaches (j + 1) * gridDim.x: arriving is one fire-and-forget
+// release reduction, waiting is a relaxed poll followed by one acquire fence.
+// Thread 0 only.
+__device__ __forceinline__ void barrier_arrive(const Ctx& c) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&c.hdr->count) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // Thread 0 only; false when the wait timed out or another block gave up.
-__device__ __forceinline__ bool barrier_wait(const Ctx& c, unsigned gen, int stage) {
+__device__ __forceinline__ bool barrier_wait(const Ctx& c, unsigned target, int stage) {
   Header* h = c.hdr;
-  const long long t0 = global_ns();
   unsigned spins = 0;
-  while (ld_acquire(&h->gen) == gen) {
+  long long t0 = 0;
+  while (int(ld_relaxed(&h->count) - target) < 0) {
     if ((++spins & 31u) == 0u) {
       if (*reinterpret_cast<volatile int*>(&h->abort)) return false;
-      if (global_ns() - t0 > c.timeout_ns) {
+      const long long now = global_ns();
+      if (t0 == 0) t0 = now;
+      if (now - t0 > c.timeout_ns) {
         record_failure(c, TK_ERR_BARRIER_TIMEOUT, stage);
         return false;
       }
     }
   }
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
   return true;
+}
+
+// Last block out resets the counters for the next run.  Thread 0 only.
+__device__ __forceinline__ void kernel_exit(const Ctx& c) {
+  Header* h = c.hdr;
+  if (atom_add_acq_rel(&h->exits, 1u) + 1u == gridDim.x) {
+    atomicExch(&h->count, 0u);
+    atomicExch(&h->exits, 0u);
+  }
 }
 
 // ------------------------------------------------------------ block sums
@@ -1206,13 +1212,14 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     __syncthreads();
     if (prof && threadIdx.x == 0) prof[s * prof_step + 1] = global_ns();
     if (s + 1 == n_stages) break;
-    unsigned gen = 0;
-    if (threadIdx.x == 0) gen = barrier_arrive(c);
+    if (threadIdx.x == 0) barrier_arrive(c);
     stage_in(prog, s + 1, &s_stage, s_tasks, s_code, s_refs, 32);
-    if (threadIdx.x == 0) s_flag = barrier_wait(c, gen, s) ? 1 : 0;
+    if (threadIdx.x == 0) s_flag = barrier_wait(c, unsigned(s + 1) * gridDim.x, s) ? 1 : 0;
     __syncthreads();
     if (!s_flag) break;
   }
+  __syncthreads();
+  if (threadIdx.x == 0) kernel_exit(c);
   if (tc) {
     tc_fence_before();
     __syncthreads();

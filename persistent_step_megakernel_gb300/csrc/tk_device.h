@@ -173,11 +173,13 @@ struct Program {
   const Ref* refs;
 };
 
-// Workspace header (offset 0, 256 bytes).  `count` returns to 0 after every
-// barrier, so a run that completes leaves the header ready for the next run.
+// Workspace header (offset 0, 256 bytes).  `count` only grows during a run
+// (barrier j completes when it reaches (j+1) * gridDim.x); the last block to
+// leave the kernel sets `count` and `exits` back to 0, so a run that
+// completes leaves the header ready for the next run.
 struct Header {
-  unsigned int count;   // arrivals at the current barrier
-  unsigned int gen;     // barrier generation
+  unsigned int count;   // barrier arrivals in this run
+  unsigned int exits;   // blocks that have left the kernel
   int status;           // 0, or the tk_status of the first failure
   int stage;            // stage of the first failure
   int abort;            // nonzero once any block gives up

@@ -230,7 +230,7 @@ def test_barrier_timeout_is_reported_and_recoverable():
     step = TrainStep(prog, 0, max_blocks=1, barrier_timeout_s=1e-3)
     ins = [to_torch(a, s.dtype, "cuda") for a, s in zip(arrays, prog.inputs)]
     outs, ws = step.allocate(ins)
-    ws.view(torch.int32)[0] = 7          # pretend 7 arrivals that never complete
+    ws.view(torch.int32)[0] = -8         # arrival counter far behind: the first barrier can never complete
     step.run(ins, outs, ws)
     status, stage = step.status(ws)
     assert status == 7 and stage == 0    # TK_ERR_BARRIER_TIMEOUT in the first barrier

@@ -218,6 +218,42 @@ tk_status tk_profile_read(const tk_program* program, const float* workspace, voi
 /* Planner decisions for tests and reports. */
 tk_status tk_plan_stats_get(const tk_program* program, tk_plan_stats* stats);
 
+/* ---- Built-in workspace (no allocation) ---------------------------------
+ * The pages this library follows have no counterpart for this entry point.
+ *
+ * tk_run_static runs one step exactly like tk_run, but its workspace is an
+ * array compiled into this library instead of memory the caller allocates.
+ * It is for callers that cannot allocate device memory where they run a step:
+ * code inside a CUDA stream capture that must not add allocation calls,
+ * runtimes whose device memory is entirely reserved by another allocator, and
+ * embedders that only receive input/output pointers from a framework that
+ * owns every allocation.  The caller still passes inputs and outputs (same
+ * rules as tk_run, including in-place outputs bound to their inputs).
+ *
+ * Limits and behaviour:
+ *   - the array holds TK_STATIC_WORKSPACE_ELEMENTS float32 elements (8 MiB);
+ *     a program whose tk_allocate size is larger is rejected with
+ *     TK_ERR_WORKSPACE and a message naming both sizes -- use tk_run then;
+ *   - every GPU on which this library's device code is loaded keeps the 8 MiB
+ *     array until the process exits;
+ *   - the first call for a program's device performs set-up: it looks up the
+ *     array's device address with that device current (which also makes the
+ *     CUDA runtime load this library's device code there).  Make that first
+ *     call before any stream capture;
+ *   - every call shares the one array, which keeps the previous call's
+ *     contents; each call clears the header (barrier counter, status word)
+ *     with an asynchronous memset on `stream` before launching;
+ *   - calls that can overlap on the GPU (different streams, or different
+ *     programs on the same device without ordering) race on the array: order
+ *     them on one stream;
+ *   - nothing is allocated: no cudaMalloc/cudaFree or allocating library call;
+ *   - tk_run_status and tk_profile_read do not apply (no workspace pointer is
+ *     exposed to the caller). */
+#define TK_STATIC_WORKSPACE_ELEMENTS 2097152
+
+tk_status tk_run_static(tk_program* program, const void* const* inputs, int32_t n_inputs,
+                        void* const* outputs, int32_t n_outputs, void* stream);
+
 /* Message of the last failing call on this thread ("" if none). */
 const char* tk_last_error(void);
 

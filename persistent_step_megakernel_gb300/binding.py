@@ -79,8 +79,12 @@ SIGNATURES = [
     ("tk_profile_read", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.POINTER(ctypes.c_int64), ctypes.c_size_t]),
     ("tk_plan_stats_get", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(tk_plan_stats)]),
+    ("tk_run_static", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32,
+                                     ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32, ctypes.c_void_p]),
     ("tk_last_error", ctypes.c_char_p, []),
 ]
+
+STATIC_WORKSPACE_ELEMENTS = 2097152
 
 
 class TkError(RuntimeError):
@@ -244,6 +248,19 @@ def tk_plan_stats_get(handle) -> dict:
     s = tk_plan_stats()
     check(lib().tk_plan_stats_get(handle, ctypes.byref(s)))
     return {name: getattr(s, name) for name, _ in tk_plan_stats._fields_}
+
+
+def tk_run_static(handle, input_ptrs, output_ptrs, stream: int = 0) -> None:
+    """tk_run with the library's built-in 8 MiB workspace: allocates nothing.
+
+    For callers that cannot allocate device memory where they run a step (see
+    tk_run_static in include/tk.h).  The first call per device does set-up and
+    should happen before any stream capture; calls share one array, so order
+    them on one stream.
+    """
+    ins = (ctypes.c_void_p * max(1, len(input_ptrs)))(*input_ptrs)
+    outs = (ctypes.c_void_p * max(1, len(output_ptrs)))(*output_ptrs)
+    check(lib().tk_run_static(handle, ins, len(input_ptrs), outs, len(output_ptrs), ctypes.c_void_p(stream)))
 
 
 def tk_last_error() -> str:

@@ -163,6 +163,10 @@ Range range_of(const void* p, int64_t bytes) {
 
 }  // namespace
 
+// Internal helpers for the built-in-workspace entry point (tk_static.cu).
+tk_status tkapi_fail(tk_status s, const std::string& msg) { return fail(s, msg); }
+int tkapi_device(const tk_program* p) { return p ? p->device : -1; }
+
 extern "C" {
 
 const char* tk_last_error(void) { return g_error.c_str(); }

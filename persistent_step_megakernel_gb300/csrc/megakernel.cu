@@ -288,6 +288,104 @@ __device__ __forceinline__ void chain_load(const Ctx& c, const Task& t, const in
   if (ch.n_loads > 1) load_ref<V>(c, t, refs[ch.load_ref[1]], crd, L[1]);
 }
 
+// A chain with its operands resolved to byte pointers and 32-bit byte strides,
+// copied into registers once per work item: the hot loops then read no
+// descriptor memory.  (Index spaces are below 2^31 elements and the planner
+// keeps chain operand strides below 2^31 bytes.)
+struct PLoad {
+  const char* p;            // operand element (0,...,0)
+  int32_t sb[kMaxRank];     // byte stride per index dim
+  int32_t dtype, vmode, inner_b;
+};
+
+struct Prep {
+  Chain ch;
+  PLoad ld[2];
+  char* out;                // output element 0
+  int32_t out_dtype;
+};
+
+__device__ __forceinline__ int esize_of(int dt) { return dt == TK_F32 ? 4 : 2; }
+
+__device__ __forceinline__ void prepare(const Ctx& c, const Task& t, Prep& P) {
+  P.ch = t.chain;
+  const Ref* refs = c.refs + t.ref_begin;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    if (i < P.ch.n_loads) {
+      const Ref& r = refs[P.ch.load_ref[i]];
+      const int es = esize_of(r.dtype);
+      P.ld[i].p = space_ptr(c, r.space, r.slot) + r.base * es;
+#pragma unroll
+      for (int d = 0; d < kMaxRank; ++d) P.ld[i].sb[d] = int32_t(r.stride[d] * es);
+      P.ld[i].dtype = r.dtype;
+      P.ld[i].vmode = r.vmode;
+      P.ld[i].inner_b = t.rank ? int32_t(r.stride[t.rank - 1] * es) : 0;
+    }
+  }
+  P.out = space_ptr(c, t.out.space, t.out.slot) + t.out.base * esize_of(t.out.dtype);
+  P.out_dtype = t.out.dtype;
+}
+
+__device__ __forceinline__ float ld1b(const char* a, int dt) {
+  if (dt == TK_F32) return *reinterpret_cast<const float*>(a);
+  if (dt == TK_BF16) return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(a));
+  return __half2float(*reinterpret_cast<const __half*>(a));
+}
+
+template <int V>
+__device__ __forceinline__ void pload(const PLoad& l, const int32_t* crd, float (&out)[V]) {
+  int64_t off = 0;
+#pragma unroll
+  for (int d = 0; d < kMaxRank; ++d) off += int64_t(crd[d]) * l.sb[d];
+  const char* a = l.p + off;
+  if constexpr (V == 8) {
+    if (l.vmode == VM_CONTIG) {
+      load8(a, l.dtype, 0, out);
+    } else if (l.vmode == VM_BCAST) {
+      const float x = ld1b(a, l.dtype);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) out[j] = x;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) out[j] = ld1b(a + j * l.inner_b, l.dtype);
+    }
+  } else {
+    out[0] = ld1b(a, l.dtype);
+  }
+}
+
+template <int V>
+__device__ __forceinline__ void prep_load(const Prep& P, const int32_t* crd, float (&L)[2][V]) {
+  if (P.ch.n_loads > 0) pload<V>(P.ld[0], crd, L[0]);
+  if (P.ch.n_loads > 1) pload<V>(P.ld[1], crd, L[1]);
+}
+
+template <int V>
+__device__ __forceinline__ void prep_store(const Prep& P, int64_t flat, const float (&v)[V]) {
+  if constexpr (V == 8) {
+    store8(P.out, P.out_dtype, flat, v);
+  } else {
+#pragma unroll
+    for (int j = 0; j < V; ++j) store1(P.out, P.out_dtype, flat + j, v[j]);
+  }
+}
+
+// 32-bit index-space coordinates of flat index f.
+__device__ __forceinline__ void unravel32(const Task& t, uint32_t f, int32_t* crd) {
+#pragma unroll
+  for (int d = kMaxRank - 1; d >= 0; --d) {
+    if (d < t.rank) {
+      const uint32_t n = uint32_t(t.shape[d]);
+      const uint32_t q = f / n;
+      crd[d] = int32_t(f - q * n);
+      f = q;
+    } else {
+      crd[d] = 0;
+    }
+  }
+}
+
 template <int V>
 __device__ __forceinline__ void round_vec(float (&x)[V], int dt) {
   if (dt == TK_BF16) {
@@ -303,8 +401,7 @@ __device__ __forceinline__ void round_vec(float (&x)[V], int dt) {
 // accumulator for CH_ACC): same arithmetic, operation by operation, as the
 // instruction form.  Every branch is uniform across the block.
 template <int V>
-__device__ __forceinline__ void chain_compute(const Task& t, const float (&L)[2][V], const float* acc, float (&x)[V]) {
-  const Chain& ch = t.chain;
+__device__ __forceinline__ void chain_compute(const Chain& ch, const float (&L)[2][V], const float* acc, float (&x)[V]) {
   if (ch.start == CH_LOAD) {
 #pragma unroll
     for (int j = 0; j < V; ++j) x[j] = L[0][j];
@@ -351,7 +448,9 @@ __device__ __forceinline__ void chain_compute(const Task& t, const float (&L)[2]
     }
     round_vec<V>(x, ch.round0);
   }
-  for (int s = 0; s < ch.n_steps; ++s) {
+#pragma unroll
+  for (int s = 0; s < kChainSteps; ++s) {
+    if (s >= ch.n_steps) break;
     const ChainStep st = ch.steps[s];
     float e[V];
     if (st.ext == EXT_LOAD0) {
@@ -420,7 +519,7 @@ __device__ __forceinline__ void eval_expr(const Ctx& c, const Task& t, const int
   if (t.chain.valid) {
     float L[2][V];
     chain_load<V>(c, t, crd, L);
-    chain_compute<V>(t, L, acc, out);
+    chain_compute<V>(t.chain, L, acc, out);
   } else {
     vm_eval<V>(c, t, crd, acc, out);
   }
@@ -520,26 +619,29 @@ __device__ __forceinline__ constexpr int pointwise_unroll() { return V == 8 ? kP
 // Vectors u = 0..U-1 of the item, software-pipelined: the loads of vector
 // u+1 are in flight while vector u is computed and stored.
 template <int V>
-__device__ __noinline__ void pointwise_chain(const Ctx& c, const Task& t, int item) {
+__device__ __noinline__ void pointwise_chain(const Ctx c, const Task& t, int item) {
   constexpr int U = pointwise_unroll<V>();
   const int64_t base = int64_t(item) * kThreads * V * U + int64_t(threadIdx.x) * V;
   constexpr int64_t step = int64_t(kThreads) * V;
+  const int64_t numel = t.numel;
+  if (base >= numel) return;
+  Prep P;
+  prepare(c, t, P);
   float cur[2][V], nxt[2][V];
-  int64_t crd[kMaxRank];
-  if (base >= t.numel) return;
-  unravel(t, base, crd);
-  chain_load<V>(c, t, crd, cur);
+  int32_t crd[kMaxRank];
+  unravel32(t, uint32_t(base), crd);
+  prep_load<V>(P, crd, cur);
 #pragma unroll 1
   for (int u = 0; u < U; ++u) {
     const int64_t i0 = base + u * step;
-    const bool more = u + 1 < U && i0 + step < t.numel;
+    const bool more = u + 1 < U && i0 + step < numel;
     if (more) {
-      unravel(t, i0 + step, crd);
-      chain_load<V>(c, t, crd, nxt);
+      unravel32(t, uint32_t(i0 + step), crd);
+      prep_load<V>(P, crd, nxt);
     }
     float v[V];
-    chain_compute<V>(t, cur, nullptr, v);
-    store_out<V>(c, t.out, i0, v);
+    chain_compute<V>(P.ch, cur, nullptr, v);
+    prep_store<V>(P, i0, v);
     if (!more) break;
 #pragma unroll
     for (int j = 0; j < V; ++j) {
@@ -550,7 +652,7 @@ __device__ __noinline__ void pointwise_chain(const Ctx& c, const Task& t, int it
 }
 
 template <int V>
-__device__ __noinline__ void pointwise_vm(const Ctx& c, const Task& t, int item) {
+__device__ __noinline__ void pointwise_vm(const Ctx c, const Task& t, int item) {
   constexpr int U = pointwise_unroll<V>();
   const int64_t base = int64_t(item) * kThreads * V * U;
   for (int u = 0; u < U; ++u) {
@@ -574,25 +676,28 @@ __device__ __forceinline__ void run_pointwise(const Ctx& c, const Task& t, int i
 
 // This thread's share of one output row of a row reduction, in element order.
 template <int V>
-__device__ __noinline__ float row_sum_chain(const Ctx& c, const Task& t, int64_t o, int64_t r0, int64_t r1) {
+__device__ __noinline__ float row_sum_chain(const Ctx c, const Task& t, int64_t o, int64_t r0, int64_t r1) {
   constexpr int64_t step = int64_t(kThreads) * V;
+  Prep P;
+  prepare(c, t, P);
+  const int64_t row0 = o * t.red_inner;
   float acc = 0.0f;
   for (int64_t r = r0 + int64_t(threadIdx.x) * V; r < r1; r += 2 * step) {
     // two vectors in flight: the second one's loads overlap the first
     const bool second = r + step < r1;
     float L0[2][V], L1[2][V], v[V];
-    int64_t crd[kMaxRank];
-    unravel(t, o * t.red_inner + r, crd);
-    chain_load<V>(c, t, crd, L0);
+    int32_t crd[kMaxRank];
+    unravel32(t, uint32_t(row0 + r), crd);
+    prep_load<V>(P, crd, L0);
     if (second) {
-      unravel(t, o * t.red_inner + r + step, crd);
-      chain_load<V>(c, t, crd, L1);
+      unravel32(t, uint32_t(row0 + r + step), crd);
+      prep_load<V>(P, crd, L1);
     }
-    chain_compute<V>(t, L0, nullptr, v);
+    chain_compute<V>(P.ch, L0, nullptr, v);
 #pragma unroll
     for (int j = 0; j < V; ++j) acc = __fadd_rn(acc, v[j]);
     if (second) {
-      chain_compute<V>(t, L1, nullptr, v);
+      chain_compute<V>(P.ch, L1, nullptr, v);
 #pragma unroll
       for (int j = 0; j < V; ++j) acc = __fadd_rn(acc, v[j]);
     }
@@ -601,7 +706,7 @@ __device__ __noinline__ float row_sum_chain(const Ctx& c, const Task& t, int64_t
 }
 
 template <int V>
-__device__ __noinline__ float row_sum_vm(const Ctx& c, const Task& t, int64_t o, int64_t r0, int64_t r1) {
+__device__ __noinline__ float row_sum_vm(const Ctx c, const Task& t, int64_t o, int64_t r0, int64_t r1) {
   float acc = 0.0f;
   for (int64_t r = r0 + int64_t(threadIdx.x) * V; r < r1; r += int64_t(kThreads) * V) {
     int64_t crd[kMaxRank];
@@ -615,7 +720,7 @@ __device__ __noinline__ float row_sum_vm(const Ctx& c, const Task& t, int64_t o,
 }
 
 template <int V>
-__device__ __noinline__ void run_reduce_row(const Ctx& c, const Task& t, int item, float* red) {
+__device__ __noinline__ void run_reduce_row(const Ctx c, const Task& t, int item, float* red) {
   const int64_t o = item / t.parts;
   const int p = item % t.parts;
   const int64_t r0 = int64_t(p) * t.part_len;
@@ -631,7 +736,7 @@ __device__ __noinline__ void run_reduce_row(const Ctx& c, const Task& t, int ite
 }
 
 template <int V>
-__device__ __noinline__ void run_reduce_col(const Ctx& c, const Task& t, int item, float* red) {
+__device__ __noinline__ void run_reduce_col(const Ctx c, const Task& t, int item, float* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t ch = item / t.parts;
   const int p = item % t.parts;
@@ -670,7 +775,7 @@ __device__ __noinline__ void run_reduce_col(const Ctx& c, const Task& t, int ite
   __syncthreads();
 }
 
-__device__ __noinline__ void run_reduce_final(const Ctx& c, const Task& t, int item, float* red) {
+__device__ __noinline__ void run_reduce_final(const Ctx c, const Task& t, int item, float* red) {
   const float* part = reinterpret_cast<const float*>(c.ws) + t.scratch;
   if (t.final_block) {
     const int64_t o = item;
@@ -690,7 +795,7 @@ __device__ __noinline__ void run_reduce_final(const Ctx& c, const Task& t, int i
 // CUDA-core GEMM tile: TM x TM outputs, 16 x 16 threads, (TM/16)^2 each;
 // float32 fmaf accumulation in k order, then the epilogue expression.
 template <int TM>
-__device__ __noinline__ void run_gemm_simt(const Ctx& c, const Task& t, int item, float* smem) {
+__device__ __noinline__ void run_gemm_simt(const Ctx c, const Task& t, int item, float* smem) {
   constexpr int KT = 16, P = TM + 4, R = TM / 16;
   float* As = smem;           // [KT][P]
   float* Bs = smem + KT * P;  // [KT][P]
@@ -782,6 +887,7 @@ __device__ __noinline__ void run_gemm_simt(const Ctx& c, const Task& t, int item
 
 struct TcState {
   uint32_t ring;                  // shared address of the 1024-aligned ring
+  uint32_t slot_bytes;            // bytes per ring slot (A tile, then B tile)
   uint32_t full, empty;           // shared addresses of kStages mbarriers each
   uint32_t acc_full, acc_empty;   // 2 mbarriers each
   uint32_t tmem;                  // TMEM base address
@@ -888,34 +994,38 @@ __device__ __forceinline__ void for_my_tiles(const Ctx& c, const Stage& st, F&& 
   }
 }
 
-__device__ __noinline__ void tc_epilogue_tile_chain(const Ctx& c, const Task& t, int64_t m0, int64_t n0,
+__device__ __noinline__ void tc_epilogue_tile_chain(const Ctx c, const Task& t, int64_t m0, int64_t n0,
                                                     uint32_t taddr) {
   const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
   const int64_t row = m0 + q * 32 + lane;
-  const bool live = row < t.m;
-  for (int cc = 0; cc < t.tile_n; cc += 32) {
+  const int64_t M = t.m, N = t.n;
+  const int tile_n = t.tile_n;
+  const bool live = row < M;
+  Prep P;
+  prepare(c, t, P);
+  for (int cc = 0; cc < tile_n; cc += 32) {
     uint32_t r[32];
     __syncwarp();
     tmem_ld32(taddr + (uint32_t(q * 32) << 16) + uint32_t(cc), r);
     if (!live) continue;
     const int64_t col0 = n0 + cc;
     float cur[2][8], nxt[2][8];
-    int64_t crd[kMaxRank] = {row, col0, 0, 0};
-    if (col0 < t.n) chain_load<8>(c, t, crd, cur);
+    int32_t crd[kMaxRank] = {int32_t(row), int32_t(col0), 0, 0};
+    if (col0 < N) prep_load<8>(P, crd, cur);
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
       const int64_t col = col0 + 8 * v;
-      if (col >= t.n) break;
-      const bool more = v < 3 && col + 8 < t.n;
+      if (col >= N) break;
+      const bool more = v < 3 && col + 8 < N;
       if (more) {
-        crd[1] = col + 8;
-        chain_load<8>(c, t, crd, nxt);
+        crd[1] = int32_t(col + 8);
+        prep_load<8>(P, crd, nxt);
       }
       float a8[8], out[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) a8[j] = __uint_as_float(r[8 * v + j]);
-      chain_compute<8>(t, cur, a8, out);
-      store_out<8>(c, t.out, row * t.n + col, out);
+      chain_compute<8>(P.ch, cur, a8, out);
+      prep_store<8>(P, row * N + col, out);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         cur[0][j] = nxt[0][j];
@@ -925,7 +1035,7 @@ __device__ __noinline__ void tc_epilogue_tile_chain(const Ctx& c, const Task& t,
   }
 }
 
-__device__ __noinline__ void tc_epilogue_tile_any(const Ctx& c, const Task& t, int64_t m0, int64_t n0,
+__device__ __noinline__ void tc_epilogue_tile_any(const Ctx c, const Task& t, int64_t m0, int64_t n0,
                                                   uint32_t taddr) {
   const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
   const int64_t row = m0 + q * 32 + lane;
@@ -970,73 +1080,85 @@ __device__ __forceinline__ void tc_epilogue_tile(const Ctx& c, const Task& t, in
     tc_epilogue_tile_any(c, t, m0, n0, taddr);
 }
 
-__device__ __noinline__ bool tc_producer(const Ctx& c, const Stage& st, const CUtensorMap* maps, TcState& ts) {
+// Each role returns its updated ring/accumulator counter in the low 32 bits
+// and 1 << 32 if all its waits completed.
+__device__ __noinline__ uint64_t tc_producer(const Ctx c, const Stage st, const CUtensorMap* maps, const TcState ts,
+                                             uint32_t p_it) {
   bool ok = true;
   asm volatile("fence.proxy.async.global;" ::: "memory");
   for_my_tiles(c, st, [&](const Task& t, int64_t m0, int64_t n0) {
     const uint32_t bytes = uint32_t(kStageBytesA + t.tile_n * kTileK * 2);
-    for (int kb = 0; kb < t.k_blocks; ++kb) {
-      const uint32_t slot = ts.p_it % kStages, ph = ((ts.p_it / kStages) & 1u) ^ 1u;
+    const int kblocks = t.k_blocks, tile_n = t.tile_n, tma_a = t.tma_a, tma_b = t.tma_b;
+    const bool a_mn = t.a_mn_major, b_mn = t.b_mn_major;
+    for (int kb = 0; kb < kblocks; ++kb) {
+      const uint32_t slot = p_it % kStages, ph = ((p_it / kStages) & 1u) ^ 1u;
       if (!mbar_wait(ts.empty + 8 * slot, ph, c.timeout_ns)) return ok = false;
       const uint32_t full = ts.full + 8 * slot;
       mbar_expect_tx(full, bytes);
-      const uint32_t a_dst = ts.ring + slot * (kStageBytesA + kStageBytesB), b_dst = a_dst + kStageBytesA;
+      const uint32_t a_dst = ts.ring + slot * ts.slot_bytes, b_dst = a_dst + kStageBytesA;
       const int k0 = kb * kTileK;
-      if (!t.a_mn_major) {
-        tma_load_2d(a_dst, &maps[t.tma_a], k0, int(m0), full);
+      if (!a_mn) {
+        tma_load_2d(a_dst, &maps[tma_a], k0, int(m0), full);
       } else {
-        tma_load_2d(a_dst, &maps[t.tma_a], int(m0), k0, full);
-        tma_load_2d(a_dst + 8192, &maps[t.tma_a], int(m0) + 64, k0, full);
+        tma_load_2d(a_dst, &maps[tma_a], int(m0), k0, full);
+        tma_load_2d(a_dst + 8192, &maps[tma_a], int(m0) + 64, k0, full);
       }
-      if (!t.b_mn_major) {
-        tma_load_2d(b_dst, &maps[t.tma_b], k0, int(n0), full);
+      if (!b_mn) {
+        tma_load_2d(b_dst, &maps[tma_b], k0, int(n0), full);
       } else {
-        for (int j = 0; j < t.tile_n / 64; ++j) tma_load_2d(b_dst + 8192 * j, &maps[t.tma_b], int(n0) + 64 * j, k0, full);
+        for (int j = 0; j < tile_n / 64; ++j) tma_load_2d(b_dst + 8192 * j, &maps[tma_b], int(n0) + 64 * j, k0, full);
       }
-      ++ts.p_it;
+      ++p_it;
     }
     return true;
   });
-  return ok;
+  return (uint64_t(ok) << 32) | p_it;
 }
 
-__device__ __noinline__ bool tc_mma(const Ctx& c, const Stage& st, TcState& ts, long long* prof) {
+__device__ __noinline__ uint64_t tc_mma(const Ctx c, const Stage st, const TcState ts, uint32_t m_it,
+                                        uint32_t* m_tile_io, long long* prof) {
   bool ok = true;
   bool first = true;
+  uint32_t m_tile = *m_tile_io;
   for_my_tiles(c, st, [&](const Task& t, int64_t, int64_t) {
-    const uint32_t acc = ts.m_tile & 1u, ph = ((ts.m_tile >> 1) & 1u) ^ 1u;
+    const uint32_t acc = m_tile & 1u, ph = ((m_tile >> 1) & 1u) ^ 1u;
     if (!mbar_wait(ts.acc_empty + 8 * acc, ph, c.timeout_ns)) return ok = false;
     tc_fence_after();
     const uint32_t d_tmem = ts.tmem + acc * kMaxTileN;
-    for (int kb = 0; kb < t.k_blocks; ++kb) {
-      const uint32_t slot = ts.m_it % kStages, fph = (ts.m_it / kStages) & 1u;
+    const int kblocks = t.k_blocks;
+    const uint32_t idesc = t.idesc;
+    const bool a_mn = t.a_mn_major, b_mn = t.b_mn_major;
+    for (int kb = 0; kb < kblocks; ++kb) {
+      const uint32_t slot = m_it % kStages, fph = (m_it / kStages) & 1u;
       if (!mbar_wait(ts.full + 8 * slot, fph, c.timeout_ns)) return ok = false;
       if (prof && first) prof[3] = global_ns();
       first = false;
       tc_fence_after();
-      const uint32_t a_base = ts.ring + slot * (kStageBytesA + kStageBytesB), b_base = a_base + kStageBytesA;
+      const uint32_t a_base = ts.ring + slot * ts.slot_bytes, b_base = a_base + kStageBytesA;
 #pragma unroll
       for (int k = 0; k < kTileK / 16; ++k) {
-        const uint64_t ad = t.a_mn_major ? smem_desc(a_base + 2048 * k, 8192, 1024) : smem_desc(a_base + 32 * k, 16, 1024);
-        const uint64_t bd = t.b_mn_major ? smem_desc(b_base + 2048 * k, 8192, 1024) : smem_desc(b_base + 32 * k, 16, 1024);
-        umma_f16(d_tmem, ad, bd, t.idesc, uint32_t(kb | k));
+        const uint64_t ad = a_mn ? smem_desc(a_base + 2048 * k, 8192, 1024) : smem_desc(a_base + 32 * k, 16, 1024);
+        const uint64_t bd = b_mn ? smem_desc(b_base + 2048 * k, 8192, 1024) : smem_desc(b_base + 32 * k, 16, 1024);
+        umma_f16(d_tmem, ad, bd, idesc, uint32_t(kb | k));
       }
       umma_commit(ts.empty + 8 * slot);
-      ++ts.m_it;
+      ++m_it;
     }
     umma_commit(ts.acc_full + 8 * acc);
-    ++ts.m_tile;
+    ++m_tile;
     return true;
   });
-  return ok;
+  *m_tile_io = m_tile;
+  return (uint64_t(ok) << 32) | m_it;
 }
 
-__device__ __noinline__ bool tc_epilogue(const Ctx& c, const Stage& st, TcState& ts, long long* prof) {
+__device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const TcState ts, uint32_t e_tile,
+                                             long long* prof) {
   bool ok = true;
   bool first = true;
   const int lane = threadIdx.x & 31;
   for_my_tiles(c, st, [&](const Task& t, int64_t m0, int64_t n0) {
-    const uint32_t acc = ts.e_tile & 1u, ph = (ts.e_tile >> 1) & 1u;
+    const uint32_t acc = e_tile & 1u, ph = (e_tile >> 1) & 1u;
     if (!mbar_wait(ts.acc_full + 8 * acc, ph, c.timeout_ns)) return ok = false;
     if (prof && first && threadIdx.x == 128) prof[5] = global_ns();
     first = false;
@@ -1045,10 +1167,10 @@ __device__ __noinline__ bool tc_epilogue(const Ctx& c, const Stage& st, TcState&
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(ts.acc_empty + 8 * acc);
-    ++ts.e_tile;
+    ++e_tile;
     return true;
   });
-  return ok;
+  return (uint64_t(ok) << 32) | e_tile;
 }
 
 // Run this block's tensor-core tiles of one stage; false after a wait timed out.
@@ -1057,13 +1179,21 @@ __device__ bool run_tc_phase(const Ctx& c, const Stage& st, const CUtensorMap* m
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   bool ok = true;
   if (warp == 0 && lane == 0) {
-    ok = tc_producer(c, st, maps, ts);
+    const uint64_t r = tc_producer(c, st, maps, ts, ts.p_it);
+    ts.p_it = uint32_t(r);
+    ok = (r >> 32) != 0;
     if (prof) prof[2] = global_ns();
   } else if (warp == 1 && lane == 0) {
-    ok = tc_mma(c, st, ts, prof);
+    uint32_t m_tile = ts.m_tile;
+    const uint64_t r = tc_mma(c, st, ts, ts.m_it, &m_tile, prof);
+    ts.m_it = uint32_t(r);
+    ts.m_tile = m_tile;
+    ok = (r >> 32) != 0;
     if (prof) prof[4] = global_ns();
   } else if (warp >= 4) {
-    ok = tc_epilogue(c, st, ts, prof);
+    const uint64_t r = tc_epilogue(c, st, ts, ts.e_tile, prof);
+    ts.e_tile = uint32_t(r);
+    ok = (r >> 32) != 0;
     if (prof && threadIdx.x == 128) prof[6] = global_ns();
   }
   if (!ok) record_failure(c, TK_ERR_PIPELINE_TIMEOUT, stage);
@@ -1155,6 +1285,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   TcState ts{};
   if (tc) {
     ts.ring = (smem_u32(s_ring) + 1023u) & ~1023u;
+    ts.slot_bytes = uint32_t(p.ring_stage_bytes);
     ts.full = smem_u32(&s_bar[0]);
     ts.empty = smem_u32(&s_bar[kStages]);
     ts.acc_full = smem_u32(&s_bar[2 * kStages]);

@@ -951,6 +951,11 @@ class Planner {
   bool try_chain(Plan& plan, Task& t, F&& build) const {
     ChainBuild cb{&plan, this, t.ref_begin};
     build(cb);
+    for (size_t i = t.ref_begin; i < plan.refs.size() && !cb.fail; ++i) {
+      const int64_t es = plan.refs[i].dtype == TK_F32 ? 4 : 2;
+      for (int d = 0; d < tkd::kMaxRank; ++d)
+        if (plan.refs[i].stride[d] * es >= (int64_t(1) << 31)) cb.fail = true;
+    }
     if (cb.fail) {
       plan.refs.resize(t.ref_begin);
       return false;
@@ -1497,7 +1502,13 @@ class Planner {
     plan.arena_units = arena_total_;
     plan.workspace_units = tkd::kHeaderUnits + arena_total_ + scratch;
     plan.uses_tc = tc_ops > 0;
-    plan.smem_bytes = plan.uses_tc ? size_t(tkd::kTcSmemBytes) : 0;
+    int max_bn = 0;
+    for (const auto& t : plan.tasks)
+      if (t.kind == tkd::T_GEMM_TC) max_bn = std::max(max_bn, t.tile_n);
+    // Ring slots sized for the widest tile: smaller rings leave more of the
+    // SM's unified L1/shared memory to the L1 cache.
+    plan.ring_stage_bytes = tkd::kStageBytesA + max_bn * tkd::kTileK * 2;
+    plan.smem_bytes = plan.uses_tc ? size_t(tkd::kStages) * plan.ring_stage_bytes + 1024 : 0;
     for (const auto& s : inputs_) plan.input_bytes.push_back(extent_of(s) * esize(s.dtype));
     for (const auto& s : outputs_) plan.output_bytes.push_back(numel(s) * esize(s.dtype));
     for (const auto& kv : inplace_) plan.inplace.push_back({kv.first, kv.second});

@@ -35,6 +35,7 @@ struct Plan {
   int64_t arena_units = 0;
   int32_t max_items = 1;
   size_t smem_bytes = 0;
+  int ring_stage_bytes = 0;  // TMA ring slot size for the widest tensor-core tile
   bool uses_tc = false;
   tk_plan_stats stats{};
   // what tk_run checks

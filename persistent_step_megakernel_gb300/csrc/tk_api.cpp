@@ -340,6 +340,7 @@ tk_status tk_run(tk_program* p, const void* const* inputs, int32_t n_inputs, voi
   prm.ws = reinterpret_cast<char*>(ws);
   prm.timeout_ns = static_cast<long long>(p->opt.barrier_timeout_s * 1e9);
   prm.prof = p->prof_offset >= 0 ? reinterpret_cast<long long*>(ws + p->prof_offset) : nullptr;
+  prm.ring_stage_bytes = pl.ring_stage_bytes;
   prm.n_in = n_inputs;
   prm.n_out = n_outputs;
   for (int i = 0; i < n_inputs; ++i) prm.io[i] = const_cast<void*>(inputs[i]);

@@ -198,6 +198,7 @@ struct Params {
   long long timeout_ns;
   long long* prof;      // optional stamps, [stage][block][kProfStamps]
   int n_in, n_out, n_maps;
+  int ring_stage_bytes; // bytes per TMA ring slot (A tile + widest B tile)
   void* io[2 * kMaxIO];
 };
 

@@ -30,6 +30,8 @@ namespace tkk {
 
 using namespace tkd;
 
+struct Prep;
+
 // Descriptor pointers are indexed with global task/instruction/ref indices;
 // for the current stage they usually point into shared memory.
 struct Ctx {
@@ -40,6 +42,7 @@ struct Ctx {
   Header* hdr;
   void* const* io;  // shared-memory copy of Params::io
   long long timeout_ns;
+  Prep* prep;       // shared memory: one prepared chain per warp
 };
 
 // ------------------------------------------------------------------ memory
@@ -289,8 +292,9 @@ __device__ __forceinline__ void chain_load(const Ctx& c, const Task& t, const in
 }
 
 // A chain with its operands resolved to byte pointers and 32-bit byte strides,
-// copied into registers once per work item: the hot loops then read no
-// descriptor memory.  (Index spaces are below 2^31 elements and the planner
+// prepared once per work item into the warp's slot in shared memory: the hot
+// loops read it with shared-memory loads instead of holding ~60 values in
+// registers (which spilled to local memory, i.e. to L2 behind a small L1).  (Index spaces are below 2^31 elements and the planner
 // keeps chain operand strides below 2^31 bytes.)
 struct PLoad {
   const char* p;            // operand element (0,...,0)
@@ -625,7 +629,7 @@ __device__ __noinline__ void pointwise_chain(const Ctx c, const Task& t, int ite
   constexpr int64_t step = int64_t(kThreads) * V;
   const int64_t numel = t.numel;
   if (base >= numel) return;
-  Prep P;
+  Prep& P = c.prep[threadIdx.x >> 5];
   prepare(c, t, P);
   float cur[2][V], nxt[2][V];
   int32_t crd[kMaxRank];
@@ -678,7 +682,7 @@ __device__ __forceinline__ void run_pointwise(const Ctx& c, const Task& t, int i
 template <int V>
 __device__ __noinline__ float row_sum_chain(const Ctx c, const Task& t, int64_t o, int64_t r0, int64_t r1) {
   constexpr int64_t step = int64_t(kThreads) * V;
-  Prep P;
+  Prep& P = c.prep[threadIdx.x >> 5];
   prepare(c, t, P);
   const int64_t row0 = o * t.red_inner;
   float acc = 0.0f;
@@ -1001,7 +1005,7 @@ __device__ __noinline__ void tc_epilogue_tile_chain(const Ctx c, const Task& t, 
   const int64_t M = t.m, N = t.n;
   const int tile_n = t.tile_n;
   const bool live = row < M;
-  Prep P;
+  Prep& P = c.prep[threadIdx.x >> 5];
   prepare(c, t, P);
   for (int cc = 0; cc < tile_n; cc += 32) {
     uint32_t r[32];
@@ -1009,27 +1013,25 @@ __device__ __noinline__ void tc_epilogue_tile_chain(const Ctx c, const Task& t, 
     tmem_ld32(taddr + (uint32_t(q * 32) << 16) + uint32_t(cc), r);
     if (!live) continue;
     const int64_t col0 = n0 + cc;
-    float cur[2][8], nxt[2][8];
-    int32_t crd[kMaxRank] = {int32_t(row), int32_t(col0), 0, 0};
-    if (col0 < N) prep_load<8>(P, crd, cur);
+    // operand loads two vectors at a time, issued before their arithmetic
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const int64_t col = col0 + 8 * v;
-      if (col >= N) break;
-      const bool more = v < 3 && col + 8 < N;
-      if (more) {
-        crd[1] = int32_t(col + 8);
-        prep_load<8>(P, crd, nxt);
+    for (int v = 0; v < 4; v += 2) {
+      float L[2][2][8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int32_t crd[kMaxRank] = {int32_t(row), int32_t(col0 + 8 * (v + h)), 0, 0};
+        if (col0 + 8 * (v + h) < N) prep_load<8>(P, crd, L[h]);
       }
-      float a8[8], out[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) a8[j] = __uint_as_float(r[8 * v + j]);
-      chain_compute<8>(P.ch, cur, a8, out);
-      prep_store<8>(P, row * N + col, out);
+      for (int h = 0; h < 2; ++h) {
+        const int64_t col = col0 + 8 * (v + h);
+        if (col < N) {
+          float a8[8], out[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        cur[0][j] = nxt[0][j];
-        cur[1][j] = nxt[1][j];
+          for (int j = 0; j < 8; ++j) a8[j] = __uint_as_float(r[8 * (v + h) + j]);
+          chain_compute<8>(P.ch, L[h], a8, out);
+          prep_store<8>(P, row * N + col, out);
+        }
       }
     }
   }
@@ -1271,6 +1273,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   __shared__ __align__(16) Instr s_code[kStageCode];
   __shared__ __align__(16) Ref s_refs[kStageRefs];
   __shared__ Stage s_stage;
+  __shared__ Prep s_prep[kThreads / 32];
   __shared__ __align__(8) uint64_t s_bar[2 * kStages + 4];
   __shared__ uint32_t s_tmem;
   __shared__ int s_flag;
@@ -1317,7 +1320,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     tc_fence_after();
     ts.tmem = s_tmem;
   }
-  Ctx c{nullptr, nullptr, nullptr, p.ws, reinterpret_cast<Header*>(p.ws), s_io, p.timeout_ns};
+  Ctx c{nullptr, nullptr, nullptr, p.ws, reinterpret_cast<Header*>(p.ws), s_io, p.timeout_ns, s_prep};
   long long* prof = p.prof ? p.prof + kProfStamps * int64_t(blockIdx.x) : nullptr;
   const int64_t prof_step = kProfStamps * int64_t(gridDim.x);
   if (prof && threadIdx.x == 0) prof[7] = entry_ns;
@@ -1395,8 +1398,26 @@ cudaError_t launch_tc(cudaLaunchConfig_t* cfg, const tkd::Params& params, const 
 }
 }  // namespace
 
+// Shared-memory carveout: ask for just the shared memory a launch needs so the
+// rest of the SM's unified L1/shared array stays L1 cache (spilled registers
+// and operand loads hit it).  Applied only when it changes for a kernel.
+template <typename K>
+cudaError_t set_carveout(K kernel, size_t dyn_smem, int* last) {
+  cudaFuncAttributes a;
+  cudaError_t e = cudaFuncGetAttributes(&a, kernel);
+  if (e != cudaSuccess) return e;
+  const size_t need = dyn_smem + a.sharedSizeBytes + 1024;
+  int pct = int((need * 100 + 233471) / 233472) + 1;  // of the largest carveout (228 KB)
+  pct = pct > 100 ? 100 : pct;
+  if (pct == *last) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, pct);
+  if (e == cudaSuccess) *last = pct;
+  return e;
+}
+
 cudaError_t tk_kernel_launch(const tkd::Params& params, const void* maps, int n_maps, int grid, size_t dyn_smem,
                              cudaStream_t stream) {
+  static int last_plain = -1, last_small = -1, last_big = -1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(tkd::kThreads);
@@ -1407,19 +1428,29 @@ cudaError_t tk_kernel_launch(const tkd::Params& params, const void* maps, int n_
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (!maps) return cudaLaunchKernelEx(&cfg, tkk::tk_persistent, params);
+  cudaError_t e;
+  if (!maps) {
+    e = set_carveout(tkk::tk_persistent, dyn_smem, &last_plain);
+    return e != cudaSuccess ? e : cudaLaunchKernelEx(&cfg, tkk::tk_persistent, params);
+  }
   if (n_maps > tkd::kMaxMaps) return cudaErrorInvalidValue;
-  if (n_maps <= kSmallMaps) return launch_tc<kSmallMaps>(&cfg, params, maps, n_maps);
-  return launch_tc<tkd::kMaxMaps>(&cfg, params, maps, n_maps);
+  if (n_maps <= kSmallMaps) {
+    e = set_carveout(tkk::tk_persistent_tc<kSmallMaps>, dyn_smem, &last_small);
+    return e != cudaSuccess ? e : launch_tc<kSmallMaps>(&cfg, params, maps, n_maps);
+  }
+  e = set_carveout(tkk::tk_persistent_tc<tkd::kMaxMaps>, dyn_smem, &last_big);
+  return e != cudaSuccess ? e : launch_tc<tkd::kMaxMaps>(&cfg, params, maps, n_maps);
 }
 
-cudaError_t tk_kernel_prepare(bool tc, size_t dyn_smem) {
+// The dynamic shared-memory limit is raised once to the largest any program
+// uses, so programs of different sizes can be launched in any order.
+cudaError_t tk_kernel_prepare(bool tc, size_t) {
   if (!tc) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(tkk::tk_persistent_tc<kSmallMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(dyn_smem));
+                                       tkd::kTcSmemBytes);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(tkk::tk_persistent_tc<tkd::kMaxMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(dyn_smem));
+                              tkd::kTcSmemBytes);
 }
 
 cudaError_t tk_kernel_occupancy(int* blocks_per_sm, bool tc, size_t dyn_smem) {

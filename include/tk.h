@@ -152,6 +152,8 @@ typedef struct {
   int32_t split_reductions;    /* reductions done as partials + a final pass */
   int64_t workspace_elements;  /* float32 elements tk_allocate reports */
   int64_t arena_elements;      /* of which: intermediate-value arena */
+  int32_t compiled_tasks;      /* tasks whose expression runs as a compiled loop of a fixed shape */
+  int32_t chain_tasks;         /* tasks evaluating a generic linear chain (the rest use instructions) */
 } tk_plan_stats;
 
 typedef struct tk_program tk_program;

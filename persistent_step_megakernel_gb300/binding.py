@@ -59,7 +59,8 @@ class tk_plan_stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "materialized_ops", "inlined_ops", "fused_epilogues", "tensor_core_ops", "stages", "grid_barriers",
         "direct_outputs", "direct_state_commits", "max_work_items", "grid_blocks", "output_copies",
-        "split_reductions")] + [("workspace_elements", ctypes.c_int64), ("arena_elements", ctypes.c_int64)]
+        "split_reductions")] + [("workspace_elements", ctypes.c_int64), ("arena_elements", ctypes.c_int64),
+        ("compiled_tasks", ctypes.c_int32), ("chain_tasks", ctypes.c_int32)]
 
 
 # (name, restype, argtypes) for every entry point of include/tk.h

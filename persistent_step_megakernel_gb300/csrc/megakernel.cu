@@ -516,6 +516,134 @@ __device__ __forceinline__ void chain_compute(const Chain& ch, const float (&L)[
   }
 }
 
+// ------------------------------------------------- compiled chain shapes
+//
+// Parameters of a FastKind chain, read once per work item into registers.
+struct Fast {
+  const char* p0;
+  const char* p1;
+  int32_t rs0, rs1;   // byte stride per index-space row (GEMM epilogues)
+  int32_t dt0, dt1;   // operand dtypes
+  int32_t r0, r1, r2; // rounding: start value, step 0, step 1
+  float a0, a1, c0;   // step 0 / step 1 alpha or threshold; step 0 constant
+  int32_t sub0, sub1; // the add/sub step subtracts
+  char* out;
+  int32_t out_dt;
+};
+
+__device__ __forceinline__ Fast fast_params(const Ctx& c, const Task& t) {
+  const Chain& ch = t.chain;
+  const Ref* refs = c.refs + t.ref_begin;
+  Fast F;
+  F.p0 = F.p1 = nullptr;
+  F.rs0 = F.rs1 = 0;
+  F.dt0 = F.dt1 = TK_F32;
+  if (ch.n_loads > 0) {
+    const Ref& r = refs[ch.load_ref[0]];
+    const int es = esize_of(r.dtype);
+    F.p0 = space_ptr(c, r.space, r.slot) + r.base * es;
+    F.rs0 = int32_t(r.stride[0] * es);
+    F.dt0 = r.dtype;
+  }
+  if (ch.n_loads > 1) {
+    const Ref& r = refs[ch.load_ref[1]];
+    const int es = esize_of(r.dtype);
+    F.p1 = space_ptr(c, r.space, r.slot) + r.base * es;
+    F.rs1 = int32_t(r.stride[0] * es);
+    F.dt1 = r.dtype;
+  }
+  F.r0 = ch.round0;
+  F.r1 = ch.steps[0].round;
+  F.r2 = ch.steps[1].round;
+  F.a0 = ch.steps[0].imm;
+  F.a1 = ch.steps[1].imm;
+  F.c0 = ch.steps[0].cval;
+  F.sub0 = ch.steps[0].op == OP_SUB;
+  F.sub1 = ch.steps[1].op == OP_SUB;
+  F.out = space_ptr(c, t.out.space, t.out.slot) + t.out.base * esize_of(t.out.dtype);
+  F.out_dt = t.out.dtype;
+  return F;
+}
+
+template <int K>
+struct FastTraits {
+  static constexpr bool load0 = K != FK_E_ACC;
+  static constexpr bool load1 = K == FK_E_BIAS_AXPY || K == FK_L_AXPY || K == FK_L_SCALE_AXPY;
+};
+
+// The same operations, in the same order and with the same roundings, as the
+// chain the kind stands for.
+template <int K>
+__device__ __forceinline__ void fast_apply(const Fast& F, const float (&l0)[8], const float (&l1)[8],
+                                           const float (&acc)[8], float (&x)[8]) {
+  if constexpr (K >= FK_E_ACC && K <= FK_E_ACC_THRESH) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = (K == FK_E_ACC || K == FK_E_ACC_THRESH) ? acc[j] : __fadd_rn(acc[j], l0[j]);
+    round_vec<8>(x, F.r0);
+    if constexpr (K == FK_E_BIAS_RELU) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = x[j] < 0.0f ? 0.0f : x[j];
+      round_vec<8>(x, F.r1);
+    } else if constexpr (K == FK_E_BIAS_AXPY) {
+      if (F.sub0) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = __fsub_rn(x[j], __fmul_rn(F.a0, l1[j]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = __fadd_rn(x[j], __fmul_rn(F.a0, l1[j]));
+      }
+      round_vec<8>(x, F.r1);
+    } else if constexpr (K == FK_E_ACC_THRESH) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = l0[j] <= F.a0 ? 0.0f : x[j];
+      round_vec<8>(x, F.r1);
+    }
+  } else if constexpr (K == FK_L) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = l0[j];
+  } else if constexpr (K == FK_L_MOV) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = l0[j];
+    round_vec<8>(x, F.r1);
+  } else if constexpr (K == FK_L_SQUARE) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = __fmul_rn(l0[j], l0[j]);
+    round_vec<8>(x, F.r1);
+  } else if constexpr (K == FK_L_SCALE || K == FK_L_SCALE_AXPY) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = __fmul_rn(l0[j], F.c0);
+    round_vec<8>(x, F.r1);
+    if constexpr (K == FK_L_SCALE_AXPY) {
+      if (F.sub1) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = __fsub_rn(x[j], __fmul_rn(F.a1, l1[j]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = __fadd_rn(x[j], __fmul_rn(F.a1, l1[j]));
+      }
+      round_vec<8>(x, F.r2);
+    }
+  } else if constexpr (K == FK_L_AXPY) {
+    if (F.sub0) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = __fsub_rn(l0[j], __fmul_rn(F.a0, l1[j]));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = __fadd_rn(l0[j], __fmul_rn(F.a0, l1[j]));
+    }
+    round_vec<8>(x, F.r1);
+  }
+}
+
+// Dispatch a FastKind to a template taking the kind as its parameter.
+#define TK_FAST_L_CASES(CALL)                 \
+  case FK_L: CALL(FK_L); break;               \
+  case FK_L_MOV: CALL(FK_L_MOV); break;       \
+  case FK_L_SQUARE: CALL(FK_L_SQUARE); break; \
+  case FK_L_SCALE: CALL(FK_L_SCALE); break;   \
+  case FK_L_AXPY: CALL(FK_L_AXPY); break;     \
+  case FK_L_SCALE_AXPY: CALL(FK_L_SCALE_AXPY); break;
+
 // One vector of a task's expression, whichever form the planner chose.
 template <int V>
 __device__ __forceinline__ void eval_expr(const Ctx& c, const Task& t, const int64_t* crd, const float* acc,
@@ -670,8 +798,46 @@ __device__ __noinline__ void pointwise_vm(const Ctx c, const Task& t, int item) 
   }
 }
 
+// A FastKind pointwise item: operands and output at the flat index, all U
+// vectors' loads issued before the first store.
+template <int K>
+__device__ __noinline__ void pointwise_fast(const Ctx c, const Task& t, int item) {
+  constexpr int U = kPointwiseUnroll;
+  constexpr int64_t step = int64_t(kThreads) * 8;
+  const int64_t base = int64_t(item) * kThreads * 8 * U + int64_t(threadIdx.x) * 8;
+  const int64_t numel = t.numel;
+  const Fast F = fast_params(c, t);
+  float l0[U][8], l1[U][8], none[8];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int64_t i = base + u * step;
+    if (i < numel) {
+      load8(F.p0, F.dt0, i, l0[u]);
+      if constexpr (FastTraits<K>::load1) load8(F.p1, F.dt1, i, l1[u]);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int64_t i = base + u * step;
+    if (i < numel) {
+      float x[8];
+      fast_apply<K>(F, l0[u], l1[u], none, x);
+      store8(F.out, F.out_dt, i, x);
+    }
+  }
+}
+
 template <int V>
 __device__ __forceinline__ void run_pointwise(const Ctx& c, const Task& t, int item) {
+  if constexpr (V == 8) {
+#define TK_CALL(k) pointwise_fast<k>(c, t, item)
+    switch (t.chain.fast) {
+      TK_FAST_L_CASES(TK_CALL)
+      default: break;
+    }
+#undef TK_CALL
+    if (t.chain.fast != FK_NONE) return;
+  }
   if (t.chain.valid)
     pointwise_chain<V>(c, t, item);
   else
@@ -709,6 +875,34 @@ __device__ __noinline__ float row_sum_chain(const Ctx c, const Task& t, int64_t 
   return acc;
 }
 
+// row_sum_chain for a FastKind chain over flat-addressed operands.
+template <int K>
+__device__ __noinline__ float row_sum_fast(const Ctx c, const Task& t, int64_t o, int64_t r0, int64_t r1) {
+  constexpr int64_t step = int64_t(kThreads) * 8;
+  const Fast F = fast_params(c, t);
+  const int64_t row0 = o * t.red_inner;
+  float acc = 0.0f, none[8];
+  for (int64_t r = r0 + int64_t(threadIdx.x) * 8; r < r1; r += 2 * step) {
+    const bool second = r + step < r1;
+    float a0[8], a1[8], b0[8], b1[8], x[8];
+    load8(F.p0, F.dt0, row0 + r, a0);
+    if constexpr (FastTraits<K>::load1) load8(F.p1, F.dt1, row0 + r, a1);
+    if (second) {
+      load8(F.p0, F.dt0, row0 + r + step, b0);
+      if constexpr (FastTraits<K>::load1) load8(F.p1, F.dt1, row0 + r + step, b1);
+    }
+    fast_apply<K>(F, a0, a1, none, x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc = __fadd_rn(acc, x[j]);
+    if (second) {
+      fast_apply<K>(F, b0, b1, none, x);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc = __fadd_rn(acc, x[j]);
+    }
+  }
+  return acc;
+}
+
 template <int V>
 __device__ __noinline__ float row_sum_vm(const Ctx c, const Task& t, int64_t o, int64_t r0, int64_t r1) {
   float acc = 0.0f;
@@ -729,7 +923,18 @@ __device__ __noinline__ void run_reduce_row(const Ctx c, const Task& t, int item
   const int p = item % t.parts;
   const int64_t r0 = int64_t(p) * t.part_len;
   const int64_t r1 = min(t.red_inner, r0 + t.part_len);
-  float acc = t.chain.valid ? row_sum_chain<V>(c, t, o, r0, r1) : row_sum_vm<V>(c, t, o, r0, r1);
+  float acc;
+  bool done = false;
+  if constexpr (V == 8) {
+    done = true;
+#define TK_CALL(k) acc = row_sum_fast<k>(c, t, o, r0, r1)
+    switch (t.chain.fast) {
+      TK_FAST_L_CASES(TK_CALL)
+      default: done = false; break;
+    }
+#undef TK_CALL
+  }
+  if (!done) acc = t.chain.valid ? row_sum_chain<V>(c, t, o, r0, r1) : row_sum_vm<V>(c, t, o, r0, r1);
   acc = block_sum(acc, red);
   if (threadIdx.x == 0) {
     if (t.parts == 1)
@@ -737,6 +942,69 @@ __device__ __noinline__ void run_reduce_row(const Ctx c, const Task& t, int item
     else
       reinterpret_cast<float*>(c.ws)[t.scratch + o * t.parts + p] = acc;
   }
+}
+
+// Column reductions: warp w sums rows r0+w, r0+w+8, ... of 8*32 columns
+// (lane l: columns 8l..8l+7), then the 8 warps' partial sums are added in warp
+// order.
+template <int V>
+__device__ __forceinline__ void col_combine(const Ctx& c, const Task& t, int64_t ch, int p, const float (&acc)[V],
+                                            float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t Q = t.red_inner;
+#pragma unroll
+  for (int j = 0; j < V; ++j) red[warp * 32 * V + lane * V + j] = acc[j];
+  __syncthreads();
+  if (threadIdx.x < 32 * V) {
+    float s = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) s = __fadd_rn(s, red[w * 32 * V + threadIdx.x]);
+    const int64_t col = ch * 32 * V + threadIdx.x;
+    if (col < Q) {
+      if (t.parts == 1)
+        finish_reduction(c, t, col, s);
+      else
+        reinterpret_cast<float*>(c.ws)[t.scratch + col * t.parts + p] = s;
+    }
+  }
+  __syncthreads();
+}
+
+template <int K>
+__device__ __noinline__ void run_reduce_col_fast(const Ctx c, const Task& t, int item, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int64_t rstep = kThreads / 32;
+  const int64_t ch = item / t.parts;
+  const int p = item % t.parts;
+  const int64_t Q = t.red_inner;
+  const int64_t col0 = ch * 256 + lane * 8;
+  const int64_t r0 = int64_t(p) * t.part_len;
+  const int64_t r1 = min(t.red_outer, r0 + t.part_len);
+  const Fast F = fast_params(c, t);
+  float acc[8], none[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+  if (col0 < Q) {
+    for (int64_t r = r0 + warp; r < r1; r += 2 * rstep) {
+      const bool second = r + rstep < r1;
+      float a0[8], a1[8], b0[8], b1[8], x[8];
+      load8(F.p0, F.dt0, r * Q + col0, a0);
+      if constexpr (FastTraits<K>::load1) load8(F.p1, F.dt1, r * Q + col0, a1);
+      if (second) {
+        load8(F.p0, F.dt0, (r + rstep) * Q + col0, b0);
+        if constexpr (FastTraits<K>::load1) load8(F.p1, F.dt1, (r + rstep) * Q + col0, b1);
+      }
+      fast_apply<K>(F, a0, a1, none, x);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], x[j]);
+      if (second) {
+        fast_apply<K>(F, b0, b1, none, x);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], x[j]);
+      }
+    }
+  }
+  col_combine<8>(c, t, ch, p, acc, red);
 }
 
 template <int V>
@@ -761,22 +1029,7 @@ __device__ __noinline__ void run_reduce_col(const Ctx c, const Task& t, int item
       for (int j = 0; j < V; ++j) acc[j] = __fadd_rn(acc[j], v[j]);
     }
   }
-#pragma unroll
-  for (int j = 0; j < V; ++j) red[warp * 32 * V + lane * V + j] = acc[j];
-  __syncthreads();
-  if (threadIdx.x < 32 * V) {
-    float s = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) s = __fadd_rn(s, red[w * 32 * V + threadIdx.x]);
-    const int64_t col = ch * 32 * V + threadIdx.x;
-    if (col < Q) {
-      if (t.parts == 1)
-        finish_reduction(c, t, col, s);
-      else
-        reinterpret_cast<float*>(c.ws)[t.scratch + col * t.parts + p] = s;
-    }
-  }
-  __syncthreads();
+  col_combine<V>(c, t, ch, p, acc, red);
 }
 
 __device__ __noinline__ void run_reduce_final(const Ctx c, const Task& t, int item, float* red) {
@@ -1037,6 +1290,49 @@ __device__ __noinline__ void tc_epilogue_tile_chain(const Ctx c, const Task& t, 
   }
 }
 
+// A FastKind epilogue: thread (q, lane) owns tile row q*32+lane; per 32-column
+// chunk it reads its accumulator slice from TMEM, issues all operand loads,
+// then computes and stores 4 vectors of 8.
+template <int K>
+__device__ __noinline__ void tc_epilogue_fast(const Ctx c, const Task& t, int64_t m0, int64_t n0, uint32_t taddr) {
+  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
+  const int64_t row = m0 + q * 32 + lane;
+  const int64_t N = t.n;
+  const int tile_n = t.tile_n;
+  const bool live = row < t.m;
+  const Fast F = fast_params(c, t);
+  const char* p0 = FastTraits<K>::load0 ? F.p0 + row * F.rs0 : nullptr;
+  const char* p1 = FastTraits<K>::load1 ? F.p1 + row * F.rs1 : nullptr;
+  const int64_t orow = row * N;
+  for (int cc = 0; cc < tile_n; cc += 32) {
+    uint32_t r[32];
+    __syncwarp();
+    tmem_ld32(taddr + (uint32_t(q * 32) << 16) + uint32_t(cc), r);
+    if (!live) continue;
+    const int64_t col0 = n0 + cc;
+    float l0[4][8], l1[4][8];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int64_t col = col0 + 8 * v;
+      if (col < N) {
+        if constexpr (FastTraits<K>::load0) load8(p0, F.dt0, col, l0[v]);
+        if constexpr (FastTraits<K>::load1) load8(p1, F.dt1, col, l1[v]);
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int64_t col = col0 + 8 * v;
+      if (col < N) {
+        float a8[8], x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a8[j] = __uint_as_float(r[8 * v + j]);
+        fast_apply<K>(F, l0[v], l1[v], a8, x);
+        store8(F.out, F.out_dt, orow + col, x);
+      }
+    }
+  }
+}
+
 __device__ __noinline__ void tc_epilogue_tile_any(const Ctx c, const Task& t, int64_t m0, int64_t n0,
                                                   uint32_t taddr) {
   const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
@@ -1076,6 +1372,14 @@ __device__ __noinline__ void tc_epilogue_tile_any(const Ctx c, const Task& t, in
 }
 
 __device__ __forceinline__ void tc_epilogue_tile(const Ctx& c, const Task& t, int64_t m0, int64_t n0, uint32_t taddr) {
+  switch (t.chain.fast) {
+    case FK_E_ACC: tc_epilogue_fast<FK_E_ACC>(c, t, m0, n0, taddr); return;
+    case FK_E_BIAS: tc_epilogue_fast<FK_E_BIAS>(c, t, m0, n0, taddr); return;
+    case FK_E_BIAS_RELU: tc_epilogue_fast<FK_E_BIAS_RELU>(c, t, m0, n0, taddr); return;
+    case FK_E_BIAS_AXPY: tc_epilogue_fast<FK_E_BIAS_AXPY>(c, t, m0, n0, taddr); return;
+    case FK_E_ACC_THRESH: tc_epilogue_fast<FK_E_ACC_THRESH>(c, t, m0, n0, taddr); return;
+    default: break;
+  }
   if (t.vec == 8 && t.chain.valid)
     tc_epilogue_tile_chain(c, t, m0, n0, taddr);
   else
@@ -1222,7 +1526,12 @@ __device__ void run_item(const Ctx& c, const Task& t, int item, float* smem) {
       break;
     case T_REDUCE_COL:
       if (t.vec == 8)
-        run_reduce_col<8>(c, t, item, smem);
+        switch (t.chain.fast) {
+#define TK_CALL(k) run_reduce_col_fast<k>(c, t, item, smem)
+          TK_FAST_L_CASES(TK_CALL)
+#undef TK_CALL
+          default: run_reduce_col<8>(c, t, item, smem); break;
+        }
       else
         run_reduce_col<1>(c, t, item, smem);
       break;

@@ -1013,6 +1013,58 @@ class Planner {
     }
   }
 
+  // Recognise the chain shapes the kernel runs as compiled loops (FastKind).
+  // Called once the task's refs have their vector modes.
+  void classify_fast(Plan& plan, Task& t) const {
+    tkd::Chain& ch = t.chain;
+    ch.fast = tkd::FK_NONE;
+    if (!ch.valid || t.vec != 8) return;
+    auto ref = [&](int slot) -> const Ref& { return plan.refs[t.ref_begin + ch.load_ref[slot]]; };
+    auto contig = [&](int slot) { return slot < ch.n_loads && ref(slot).vmode == tkd::VM_CONTIG; };
+    Shape sp(t.shape, t.shape + t.rank);
+    Shape cs = contig_strides_of(sp);
+    auto flat = [&](int slot) {
+      if (slot >= ch.n_loads) return false;
+      const Ref& r = ref(slot);
+      for (int d = 0; d < t.rank; ++d)
+        if (t.shape[d] > 1 && r.stride[d] != cs[d]) return false;
+      return r.base % 8 == 0;
+    };
+    const tkd::ChainStep& s0 = ch.steps[0];
+    const tkd::ChainStep& s1 = ch.steps[1];
+    auto axpy = [](const tkd::ChainStep& st, int ext) {
+      return (st.op == tkd::OP_ADD || st.op == tkd::OP_SUB) && st.ext == ext && !st.second;
+    };
+    if (t.kind == tkd::T_GEMM_TC) {
+      if (ch.start != tkd::CH_ACC) return;
+      if (ch.addmm_mode == tkd::AM_ACC && ch.bias == -1) {
+        if (ch.n_steps == 0 && ch.n_loads == 0) ch.fast = tkd::FK_E_ACC;
+        if (ch.n_steps == 1 && ch.n_loads == 1 && s0.op == tkd::OP_THRESH && s0.ext == tkd::EXT_LOAD0 &&
+            !s0.second && contig(0))
+          ch.fast = tkd::FK_E_ACC_THRESH;
+      } else if (ch.addmm_mode == tkd::AM_SUM && ch.bias == 0 && contig(0)) {
+        if (ch.n_steps == 0 && ch.n_loads == 1) ch.fast = tkd::FK_E_BIAS;
+        if (ch.n_steps == 1 && ch.n_loads == 1 && s0.op == tkd::OP_RELU) ch.fast = tkd::FK_E_BIAS_RELU;
+        if (ch.n_steps == 1 && ch.n_loads == 2 && axpy(s0, tkd::EXT_LOAD1) && contig(1)) ch.fast = tkd::FK_E_BIAS_AXPY;
+      }
+      return;
+    }
+    if (t.kind != tkd::T_POINTWISE && t.kind != tkd::T_REDUCE_ROW && t.kind != tkd::T_REDUCE_COL) return;
+    if (ch.start != tkd::CH_LOAD || !flat(0)) return;
+    if (ch.n_steps == 0 && ch.n_loads == 1) ch.fast = tkd::FK_L;
+    if (ch.n_steps == 1 && ch.n_loads == 1) {
+      if (s0.op == tkd::OP_MOV) ch.fast = tkd::FK_L_MOV;
+      if (s0.op == tkd::OP_SQUARE) ch.fast = tkd::FK_L_SQUARE;
+      if (s0.op == tkd::OP_MUL && s0.ext == tkd::EXT_CONST) ch.fast = tkd::FK_L_SCALE;
+    }
+    if (ch.n_steps == 1 && ch.n_loads == 2 && axpy(s0, tkd::EXT_LOAD1) && flat(1)) ch.fast = tkd::FK_L_AXPY;
+    if (ch.n_steps == 2 && ch.n_loads == 2 && s0.op == tkd::OP_MUL && s0.ext == tkd::EXT_CONST &&
+        axpy(s1, tkd::EXT_LOAD1) && flat(1))
+      ch.fast = tkd::FK_L_SCALE_AXPY;
+  }
+
+  static Shape contig_strides_of(const Shape& sh) { return contig(sh); }
+
   int items_pointwise(const Task& t) const {
     const int64_t per = int64_t(tkd::kThreads) * t.vec * (t.vec == 8 ? tkd::kPointwiseUnroll : 1);
     return int(ceil_div(t.numel, per));
@@ -1045,6 +1097,7 @@ class Planner {
     }
     t.out = out;
     finish_refs(plan, t);
+    classify_fast(plan, t);
     t.n_items = items_pointwise(t);
     return t;
   }
@@ -1207,6 +1260,7 @@ class Planner {
       int out_buf = fused_it != fused_.end() ? fused_it->second.final_buf : mm.out.buffer_id;
       t.out = out_ref(out_buf);
       finish_refs(plan, t);
+    classify_fast(plan, t);
       return t;
     }
     Emit e{&plan, this, t.ref_begin, space};
@@ -1266,6 +1320,7 @@ class Planner {
     t.n_refs = int(plan.refs.size()) - t.ref_begin;
     t.out = out_ref(out_buf);
     finish_refs(plan, t);
+    classify_fast(plan, t);
     return t;
   }
 
@@ -1331,6 +1386,7 @@ class Planner {
       t.n_items = int(chunks * t.parts);
     }
     finish_refs(plan, t);
+    classify_fast(plan, t);
     if (n_out == 0) t.n_items = 0;
     if (t.parts <= 1) {
       t.parts = 1;
@@ -1527,6 +1583,10 @@ class Planner {
     st.split_reductions = split;
     st.workspace_elements = plan.workspace_units;
     st.arena_elements = arena_total_;
+    for (const auto& t : plan.tasks) {
+      if (t.chain.valid && t.chain.fast != tkd::FK_NONE) ++st.compiled_tasks;
+      else if (t.chain.valid) ++st.chain_tasks;
+    }
     return plan;
   }
 };

@@ -95,8 +95,28 @@ struct ChainStep {
   float cval;       // constant operand (EXT_CONST)
 };
 
+// Chains of these shapes run as compiled loops with their parameters hoisted
+// out of the element loop (no per-element decoding).  E_*: GEMM epilogues on
+// a [M,N] tile, operands contiguous along N; L_*: a load of operand slot 0
+// addressed by the flat index, then the listed steps.
+enum FastKind : int32_t {
+  FK_NONE = 0,
+  FK_E_ACC = 1,          // round(acc)
+  FK_E_BIAS = 2,         // round(acc + l0)
+  FK_E_BIAS_RELU = 3,    // round(relu(round(acc + l0)))
+  FK_E_BIAS_AXPY = 4,    // round(round(acc + l0) +/- a*l1)
+  FK_E_ACC_THRESH = 5,   // round(l0 <= a ? 0 : round(acc))
+  FK_L = 6,              // l0
+  FK_L_MOV = 7,          // round(l0)
+  FK_L_SQUARE = 8,       // round(l0 * l0)
+  FK_L_SCALE = 9,        // round(l0 * c)
+  FK_L_AXPY = 10,        // round(l0 +/- a*l1)
+  FK_L_SCALE_AXPY = 11   // round(round(l0 * c) +/- a*l1)
+};
+
 struct Chain {
   int32_t valid;
+  int32_t fast;          // FastKind
   int32_t n_loads;
   int32_t load_ref[2];   // task-relative refs of the two load slots
   int32_t start;         // ChainStart; CH_LOAD reads slot 0

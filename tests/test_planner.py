@@ -165,3 +165,22 @@ def test_plan_only_program_cannot_run():
         assert e.value.status == 6
     finally:
         B.tk_program_destroy(h)
+
+
+@pytest.mark.parametrize("name", ["c2", "c3", "c5"])
+def test_mlp_step_tasks_take_compiled_loops(name):
+    # Every expression of the bf16 MLP step has one of the fixed shapes: bias
+    # (+ReLU) and bias-minus-target GEMM epilogues, the ReLU-mask epilogue,
+    # squares and scaled sums, SGD and momentum updates.
+    s = plan(S.mlp_step_program(S.CONFIGS[name], export="state"))
+    assert s["compiled_tasks"] == s["materialized_ops"] and s["chain_tasks"] == 0
+
+
+def test_strided_operand_falls_back_to_generic_chain():
+    x = f32("x", (8, 16))
+    xt = TensorSpec("x", (16, 8), (1, 16), 0, "float32")
+    prog = Program([x], [f32("y", (16, 8))], [Operation("y", "mul", (xt, 3.0), f32("y", (16, 8)))])
+    s = plan(prog)
+    assert (s["compiled_tasks"], s["chain_tasks"]) == (0, 1)
+    s = plan(Program([x], [f32("y", (8, 16))], [Operation("y", "mul", (x, 3.0), f32("y", (8, 16)))]))
+    assert (s["compiled_tasks"], s["chain_tasks"]) == (1, 0)

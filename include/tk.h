@@ -134,6 +134,10 @@ typedef struct {
   int32_t sm_count;            /* 0: query the device; > 0: SM count for a plan-only program */
   int32_t profile;             /* 1: record per-stage globaltimer stamps (see tk_profile_read) */
   double barrier_timeout_s;    /* limit of every in-kernel wait (default 2.0) */
+  int32_t expr_forms;          /* expression evaluators the planner may pick: 0 all (compiled
+                                  loops of fixed shapes, else generic chains, else instructions;
+                                  default), 1 no compiled loops, 2 instructions only.  All give
+                                  bit-identical results; 1 and 2 exist for testing. */
 } tk_options;
 
 /* What the planner decided (codegen.py `GeneratedKernel` counters). */
@@ -154,7 +158,26 @@ typedef struct {
   int64_t arena_elements;      /* of which: intermediate-value arena */
   int32_t compiled_tasks;      /* tasks whose expression runs as a compiled loop of a fixed shape */
   int32_t chain_tasks;         /* tasks evaluating a generic linear chain (the rest use instructions) */
+  int32_t tasks;               /* device tasks (see tk_plan_task) */
+  int32_t reserved0;           /* 0 */
 } tk_plan_stats;
+
+/* One device task of a plan: a scheduled op (with whatever the planner fused
+ * into its expression), one half of a split reduction, or an end-of-kernel
+ * output copy.  Tasks are listed stage by stage. */
+typedef struct {
+  int32_t stage;               /* barrier-separated stage the task runs in */
+  int32_t kind;                /* 0 pointwise, 1 row reduction, 2 column reduction, 3 partials sum,
+                                  4 CUDA-core GEMM, 5 tensor-core GEMM */
+  int32_t op_index;            /* index into tk_program_desc.ops; -1 for an output copy or commit */
+  int32_t n_items;             /* work items (GEMM tiles, element blocks, reduction outputs x parts) */
+  int32_t form;                /* expression evaluator: 0 instructions, 1 generic chain, 2 compiled loop */
+  int32_t compiled_shape;      /* which compiled loop (1..11) when form == 2, else 0 */
+  int32_t m, n, k;             /* GEMM extents (0 otherwise) */
+  int32_t tile_m, tile_n;      /* GEMM tile (0 otherwise) */
+  int32_t parts;               /* reduction parts (1 = not split) */
+  int64_t numel;               /* elements of the task's index space */
+} tk_task_info;
 
 typedef struct tk_program tk_program;
 
@@ -219,6 +242,10 @@ tk_status tk_profile_read(const tk_program* program, const float* workspace, voi
 
 /* Planner decisions for tests and reports. */
 tk_status tk_plan_stats_get(const tk_program* program, tk_plan_stats* stats);
+
+/* Task `index` (0 <= index < stats.tasks) of the plan; TK_ERR_INVALID if out of
+ * range.  Plan-only programs (device -1) answer too. */
+tk_status tk_plan_task(const tk_program* program, int32_t index, tk_task_info* info);
 
 /* ---- Built-in workspace (no allocation) ---------------------------------
  * The pages this library follows have no counterpart for this entry point.

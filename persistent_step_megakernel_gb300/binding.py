@@ -52,7 +52,7 @@ class tk_options(ctypes.Structure):
                 ("fuse_pointwise", ctypes.c_int32), ("fuse_epilogues", ctypes.c_int32),
                 ("inline_input_casts", ctypes.c_int32), ("tensor_cores", ctypes.c_int32),
                 ("sm_count", ctypes.c_int32), ("profile", ctypes.c_int32),
-                ("barrier_timeout_s", ctypes.c_double)]
+                ("barrier_timeout_s", ctypes.c_double), ("expr_forms", ctypes.c_int32)]
 
 
 class tk_plan_stats(ctypes.Structure):
@@ -60,7 +60,14 @@ class tk_plan_stats(ctypes.Structure):
         "materialized_ops", "inlined_ops", "fused_epilogues", "tensor_core_ops", "stages", "grid_barriers",
         "direct_outputs", "direct_state_commits", "max_work_items", "grid_blocks", "output_copies",
         "split_reductions")] + [("workspace_elements", ctypes.c_int64), ("arena_elements", ctypes.c_int64),
-        ("compiled_tasks", ctypes.c_int32), ("chain_tasks", ctypes.c_int32)]
+        ("compiled_tasks", ctypes.c_int32), ("chain_tasks", ctypes.c_int32), ("tasks", ctypes.c_int32),
+        ("reserved0", ctypes.c_int32)]
+
+
+class tk_task_info(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "stage", "kind", "op_index", "n_items", "form", "compiled_shape", "m", "n", "k", "tile_m", "tile_n",
+        "parts")] + [("numel", ctypes.c_int64)]
 
 
 # (name, restype, argtypes) for every entry point of include/tk.h
@@ -80,6 +87,7 @@ SIGNATURES = [
     ("tk_profile_read", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.POINTER(ctypes.c_int64), ctypes.c_size_t]),
     ("tk_plan_stats_get", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(tk_plan_stats)]),
+    ("tk_plan_task", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(tk_task_info)]),
     ("tk_run_static", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32,
                                      ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32, ctypes.c_void_p]),
     ("tk_last_error", ctypes.c_char_p, []),
@@ -249,6 +257,19 @@ def tk_plan_stats_get(handle) -> dict:
     s = tk_plan_stats()
     check(lib().tk_plan_stats_get(handle, ctypes.byref(s)))
     return {name: getattr(s, name) for name, _ in tk_plan_stats._fields_}
+
+
+TASK_KINDS = ("pointwise", "reduce_row", "reduce_col", "reduce_final", "gemm_simt", "gemm_tc")
+EXPR_FORMS = ("instructions", "chain", "compiled")
+
+
+def tk_plan_task(handle, index: int) -> dict:
+    t = tk_task_info()
+    check(lib().tk_plan_task(handle, index, ctypes.byref(t)))
+    d = {name: getattr(t, name) for name, _ in tk_task_info._fields_}
+    d["kind"] = TASK_KINDS[d["kind"]]
+    d["form"] = EXPR_FORMS[d["form"]]
+    return d
 
 
 def tk_run_static(handle, input_ptrs, output_ptrs, stream: int = 0) -> None:

@@ -576,7 +576,19 @@ struct FastTraits {
 template <int K>
 __device__ __forceinline__ void fast_apply(const Fast& F, const float (&l0)[8], const float (&l1)[8],
                                            const float (&acc)[8], float (&x)[8]) {
-  if constexpr (K >= FK_E_ACC && K <= FK_E_ACC_THRESH) {
+  if constexpr (K == FK_E_UPDATE) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = acc[j];
+    round_vec<8>(x, F.r0);
+    if (F.sub0) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = __fsub_rn(l0[j], __fmul_rn(F.a0, x[j]));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = __fadd_rn(l0[j], __fmul_rn(F.a0, x[j]));
+    }
+    round_vec<8>(x, F.r1);
+  } else if constexpr (K >= FK_E_ACC && K <= FK_E_ACC_THRESH) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) x[j] = (K == FK_E_ACC || K == FK_E_ACC_THRESH) ? acc[j] : __fadd_rn(acc[j], l0[j]);
     round_vec<8>(x, F.r0);
@@ -1378,6 +1390,7 @@ __device__ __forceinline__ void tc_epilogue_tile(const Ctx& c, const Task& t, in
     case FK_E_BIAS_RELU: tc_epilogue_fast<FK_E_BIAS_RELU>(c, t, m0, n0, taddr); return;
     case FK_E_BIAS_AXPY: tc_epilogue_fast<FK_E_BIAS_AXPY>(c, t, m0, n0, taddr); return;
     case FK_E_ACC_THRESH: tc_epilogue_fast<FK_E_ACC_THRESH>(c, t, m0, n0, taddr); return;
+    case FK_E_UPDATE: tc_epilogue_fast<FK_E_UPDATE>(c, t, m0, n0, taddr); return;
     default: break;
   }
   if (t.vec == 8 && t.chain.valid)
@@ -1632,8 +1645,16 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   Ctx c{nullptr, nullptr, nullptr, p.ws, reinterpret_cast<Header*>(p.ws), s_io, p.timeout_ns, s_prep};
   long long* prof = p.prof ? p.prof + kProfStamps * int64_t(blockIdx.x) : nullptr;
   const int64_t prof_step = kProfStamps * int64_t(gridDim.x);
-  if (prof && threadIdx.x == 0) prof[7] = entry_ns;
   const int n_stages = prog->n_stages;
+  if (prof) {
+    // stamps a stage may leave unwritten read as 0
+    if (threadIdx.x == 0) {
+      for (int s = 0; s < n_stages; ++s)
+        for (int k = 2; k < kProfStamps; ++k) prof[s * prof_step + k] = 0;
+      prof[7] = entry_ns;
+    }
+    __syncthreads();
+  }
   for (int s = 0; s < n_stages; ++s) {
     const Stage st = s_stage;
     if (prof && threadIdx.x == 0) prof[s * prof_step] = global_ns();

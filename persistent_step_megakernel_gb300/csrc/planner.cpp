@@ -403,7 +403,10 @@ class Planner {
       int current = mm.out.buffer_id;
       while (bufs_[current].users.size() == 1) {
         const OpInfo& nxt = ops_[bufs_[current].users[0]];
-        if (!is_pointwise(nxt.kind) || output_buffers_.count(nxt.out.buffer_id)) break;
+        // A chain may end at a program output (its value is then stored
+        // straight from the tile) but not pass through one.
+        const bool ends_at_output = output_buffers_.count(nxt.out.buffer_id) > 0;
+        if (!is_pointwise(nxt.kind)) break;
         // The GEMM root must be read with its own logical layout.
         bool any = false, ok = true;
         for (const auto& o : nxt.in) {
@@ -415,7 +418,7 @@ class Planner {
         chain.push_back(nxt.index);
         skipped.push_back(current);
         current = nxt.out.buffer_id;
-        if (bufs_[current].users.size() != 1) break;
+        if (ends_at_output || bufs_[current].users.size() != 1) break;
       }
       if (chain.empty()) continue;
       bool safe = true;
@@ -480,7 +483,45 @@ class Planner {
         schedule_.push_back(op.index);
       }
     }
+    defer_inplace_epilogues();
     for (int s : schedule_) writer_[out_buffer_of(s)] = s;
+  }
+
+  // Input buffer an in-place output overwrites (-1: not in place).
+  int inplace_target(int buffer) const {
+    for (const auto& kv : inplace_)
+      if (outputs_[kv.first].buffer_id == buffer) return inputs_[kv.second].buffer_id;
+    return -1;
+  }
+
+  // A fused GEMM whose chain ends in an in-place output (e.g. a weight
+  // gradient GEMM ending in the SGD update of that weight) moves after the
+  // last scheduled op that still reads the old value (the input-gradient GEMM
+  // of the same layer), so that it can write the new value directly.  Moving
+  // it later is legal: only program outputs depend on it.
+  void defer_inplace_epilogues() {
+    for (size_t i = 0; i < schedule_.size(); ++i) {
+      const int f = schedule_[i];
+      auto fu = fused_.find(f);
+      if (fu == fused_.end()) continue;
+      const int target = inplace_target(fu->second.final_buf);
+      if (target < 0) continue;
+      size_t last = i;
+      bool blocked = false;
+      for (size_t j = i + 1; j < schedule_.size(); ++j) {
+        bool reads_target = false;
+        for (const auto& v : reads_of(schedule_[j])) {
+          if (raw_inputs(v.buffer_id).count(target)) reads_target = true;
+          if (roots(v.buffer_id).count(fu->second.final_buf)) blocked = true;
+        }
+        if (blocked) break;
+        if (reads_target) last = j;
+      }
+      if (blocked || last == i) continue;
+      schedule_.erase(schedule_.begin() + i);
+      schedule_.insert(schedule_.begin() + last, f);
+      --i;  // the op now at position i has not been examined
+    }
   }
 
   // Every tensor operand a scheduled op reads (GEMM + chain externals).
@@ -531,9 +572,9 @@ class Planner {
       int pos = -1;
       for (size_t i = 0; i < schedule_.size(); ++i)
         if (out_buffer_of(schedule_[i]) == out.buffer_id) pos = int(i);
-      if (pos < 0 || !is_pointwise(ops_[schedule_[pos]].kind) || fused_.count(schedule_[pos]) ||
-          out_count[out.buffer_id] != 1)
-        continue;
+      if (pos < 0 || out_count[out.buffer_id] != 1) continue;
+      const bool fused_gemm = fused_.count(schedule_[pos]) > 0;
+      if (!fused_gemm && !is_pointwise(ops_[schedule_[pos]].kind)) continue;
       if (!exact_contig(out)) continue;
       bool target_is_output = false;
       for (const auto& o : outputs_)
@@ -580,7 +621,11 @@ class Planner {
     return r;
   }
 
-  void plan_arena() {
+  // Arena offsets of the stored intermediate values in schedule order.  With
+  // `reuse`, a value takes the smallest sufficient freed slot (on a tie the
+  // one freed first) whose previous occupant was last accessed in an earlier
+  // stage (stage_of_ from a first pass); without it every value has its own.
+  void plan_arena(bool reuse) {
     std::map<int, int> last;
     for (size_t i = 0; i < schedule_.size(); ++i)
       for (const auto& v : reads_of(schedule_[i]))
@@ -590,9 +635,14 @@ class Planner {
     struct Slot {
       int buf;
       int64_t start, size;
+      int pos;  // schedule position of the writer
+    };
+    struct Free {
+      int64_t start, size;
+      int stage;  // stage of the last access to the previous occupant
     };
     std::vector<Slot> active;
-    std::vector<std::pair<int64_t, int64_t>> free_list;  // (start, size)
+    std::vector<Free> free_list;
     int64_t total = 0;
     for (size_t i = 0; i < schedule_.size(); ++i) {
       int b = out_buffer_of(schedule_[i]);
@@ -600,32 +650,33 @@ class Planner {
       std::vector<Slot> keep;
       for (const auto& s : active) {
         auto it = last.find(s.buf);
-        if ((it == last.end() ? -1 : it->second) < int(i))
-          free_list.push_back({s.start, s.size});
+        const int l = it == last.end() ? -1 : it->second;
+        if (l < int(i))
+          free_list.push_back({s.start, s.size, reuse ? stage_of_[size_t(std::max(l, s.pos))] : 0});
         else
           keep.push_back(s);
       }
       active = keep;
       int64_t size = std::max<int64_t>(64, round_up(units_of(b), 64));
       int best = -1;
-      for (size_t j = 0; j < free_list.size(); ++j) {
-        if (free_list[j].second < size) continue;
-        // smallest sufficient slot; on a tie the one freed first
-        if (best < 0 || free_list[j].second < free_list[best].second) best = int(j);
+      for (size_t j = 0; j < free_list.size() && reuse; ++j) {
+        if (free_list[j].size < size || free_list[j].stage >= stage_of_[i]) continue;
+        if (best < 0 || free_list[j].size < free_list[best].size) best = int(j);
       }
       int64_t start;
       if (best >= 0) {
-        start = free_list[best].first;
-        int64_t n = free_list[best].second;
+        start = free_list[best].start;
+        const int64_t n = free_list[best].size;
+        const int st = free_list[best].stage;
         free_list.erase(free_list.begin() + best);
-        if (n > size) free_list.push_back({start + size, n - size});
+        if (n > size) free_list.push_back({start + size, n - size, st});
       } else {
         start = total;
         total += size;
       }
       arena_off_[b] = start;
       arena_units_[b] = units_of(b);
-      active.push_back({b, start, size});
+      active.push_back({b, start, size, int(i)});
     }
     arena_total_ = total;
   }
@@ -949,6 +1000,7 @@ class Planner {
   // Chain form of task t's expression into t.chain; false leaves no trace.
   template <typename F>
   bool try_chain(Plan& plan, Task& t, F&& build) const {
+    if (opt_.expr_forms >= 2) return false;
     ChainBuild cb{&plan, this, t.ref_begin};
     build(cb);
     for (size_t i = t.ref_begin; i < plan.refs.size() && !cb.fail; ++i) {
@@ -982,6 +1034,7 @@ class Planner {
     if (t.numel >= (int64_t(1) << 31)) throw Error(TK_ERR_UNSUPPORTED, "tensors of 2^31 or more elements");
     t.vec = (t.rank >= 1 && t.shape[t.rank - 1] % 8 == 0 && t.numel > 0) ? 8 : 1;
     t.tma_a = t.tma_b = -1;
+    t.op_index = -1;
     return t;
   }
 
@@ -1018,7 +1071,7 @@ class Planner {
   void classify_fast(Plan& plan, Task& t) const {
     tkd::Chain& ch = t.chain;
     ch.fast = tkd::FK_NONE;
-    if (!ch.valid || t.vec != 8) return;
+    if (!ch.valid || t.vec != 8 || opt_.expr_forms >= 1) return;
     auto ref = [&](int slot) -> const Ref& { return plan.refs[t.ref_begin + ch.load_ref[slot]]; };
     auto contig = [&](int slot) { return slot < ch.n_loads && ref(slot).vmode == tkd::VM_CONTIG; };
     Shape sp(t.shape, t.shape + t.rank);
@@ -1042,6 +1095,9 @@ class Planner {
         if (ch.n_steps == 1 && ch.n_loads == 1 && s0.op == tkd::OP_THRESH && s0.ext == tkd::EXT_LOAD0 &&
             !s0.second && contig(0))
           ch.fast = tkd::FK_E_ACC_THRESH;
+        if (ch.n_steps == 1 && ch.n_loads == 1 && (s0.op == tkd::OP_ADD || s0.op == tkd::OP_SUB) &&
+            s0.ext == tkd::EXT_LOAD0 && s0.second && contig(0))
+          ch.fast = tkd::FK_E_UPDATE;
       } else if (ch.addmm_mode == tkd::AM_SUM && ch.bias == 0 && contig(0)) {
         if (ch.n_steps == 0 && ch.n_loads == 1) ch.fast = tkd::FK_E_BIAS;
         if (ch.n_steps == 1 && ch.n_loads == 1 && s0.op == tkd::OP_RELU) ch.fast = tkd::FK_E_BIAS_RELU;
@@ -1427,8 +1483,21 @@ class Planner {
     build_schedule();
     choose_direct_aliases();
     choose_bindings();
-    plan_arena();
+    // Stages first with a private slot per intermediate value, then the arena
+    // reuses a slot only for a value written in a later stage than the last
+    // read of its previous occupant: slot reuse never adds a barrier.
+    plan_arena(false);
+    lower_and_stage();
+    arena_off_.clear();
+    arena_units_.clear();
+    plan_arena(true);
+    return lower_and_stage();
+  }
 
+  std::vector<int> stage_of_;  // stage of each schedule position (last stage for split reductions)
+
+  Plan lower_and_stage() {
+    stage_of_.assign(schedule_.size(), 0);
     Plan plan;
     std::vector<std::vector<Task>> stages(1);
     std::vector<Region> stage_reads, stage_writes;
@@ -1452,13 +1521,15 @@ class Planner {
       return false;
     };
 
-    for (int s : schedule_) {
+    for (size_t pos = 0; pos < schedule_.size(); ++pos) {
+      const int s = schedule_[pos];
       const OpInfo& op = ops_[s];
       std::vector<Region> reads, writes;
       for (const auto& v : reads_of(s)) read_regions(v, reads);
       writes.push_back(storage_region(out_buffer_of(s)));
       if (is_red(op.kind)) {
         std::vector<Task> ts = lower_reduction(plan, op, &scratch);
+        for (auto& t : ts) t.op_index = op.index;
         if (ts.size() == 2) {
           ++split;
           if (hazard(reads, {})) barrier();
@@ -1467,6 +1538,7 @@ class Planner {
           barrier();
           stages.back().push_back(ts[1]);
           stage_writes.insert(stage_writes.end(), writes.begin(), writes.end());
+          stage_of_[pos] = int(stages.size()) - 1;
           continue;
         }
         if (hazard(reads, writes)) barrier();
@@ -1475,9 +1547,11 @@ class Planner {
         Task t = is_mm(op.kind) ? lower_gemm(plan, op)
                                 : lower_pointwise(plan, &op, nullptr, shape_of(op.out), out_ref(op.out.buffer_id),
                                                   op.out.dtype);
+        t.op_index = op.index;
         if (hazard(reads, writes)) barrier();
         stages.back().push_back(t);
       }
+      stage_of_[pos] = int(stages.size()) - 1;
       stage_reads.insert(stage_reads.end(), reads.begin(), reads.end());
       stage_writes.insert(stage_writes.end(), writes.begin(), writes.end());
     }
@@ -1533,6 +1607,7 @@ class Planner {
       S.code_lo = S.ref_lo = INT32_MAX;
       S.code_hi = S.ref_hi = 0;
       for (auto& t : st) {
+        t.stage = int(plan.stages.size());
         if (t.code_len) {
           S.code_lo = std::min(S.code_lo, t.code_begin);
           S.code_hi = std::max(S.code_hi, t.code_begin + t.code_len);
@@ -1583,6 +1658,7 @@ class Planner {
     st.split_reductions = split;
     st.workspace_elements = plan.workspace_units;
     st.arena_elements = arena_total_;
+    st.tasks = int(plan.tasks.size());
     for (const auto& t : plan.tasks) {
       if (t.chain.valid && t.chain.fast != tkd::FK_NONE) ++st.compiled_tasks;
       else if (t.chain.valid) ++st.chain_tasks;

@@ -192,6 +192,7 @@ tk_status tk_program_create(const tk_program_desc* desc, const tk_options* opt_i
   tk_options_default(&opt);
   if (opt_in) opt = *opt_in;
   if (opt.blocks_per_sm < 1 || opt.blocks_per_sm > 8) return fail(TK_ERR_INVALID, "blocks_per_sm must be between 1 and 8");
+  if (opt.expr_forms < 0 || opt.expr_forms > 2) return fail(TK_ERR_INVALID, "expr_forms must be 0, 1 or 2");
   if (!(opt.barrier_timeout_s > 0.0) || opt.barrier_timeout_s > 3600.0)
     return fail(TK_ERR_INVALID, "barrier_timeout_s must be in (0, 3600]");
   if (opt.sm_count < 0) return fail(TK_ERR_INVALID, "sm_count must be >= 0");
@@ -407,6 +408,31 @@ tk_status tk_profile_read(const tk_program* p, const float* ws, void* stream, in
 tk_status tk_plan_stats_get(const tk_program* p, tk_plan_stats* s) {
   if (!p || !s) return fail(TK_ERR_INVALID, "program and stats must not be NULL");
   *s = p->plan.stats;
+  return TK_OK;
+}
+
+tk_status tk_plan_task(const tk_program* p, int32_t index, tk_task_info* info) {
+  if (!p || !info) return fail(TK_ERR_INVALID, "program and info must not be NULL");
+  if (index < 0 || size_t(index) >= p->plan.tasks.size()) return fail(TK_ERR_INVALID, "task index out of range");
+  const tkd::Task& t = p->plan.tasks[size_t(index)];
+  tk_task_info r{};
+  r.stage = t.stage;
+  r.kind = t.kind;
+  r.op_index = t.op_index;
+  r.n_items = t.n_items;
+  r.form = !t.chain.valid ? 0 : (t.chain.fast != tkd::FK_NONE ? 2 : 1);
+  r.compiled_shape = r.form == 2 ? t.chain.fast : 0;
+  const bool gemm = t.kind == tkd::T_GEMM_SIMT || t.kind == tkd::T_GEMM_TC;
+  if (gemm) {
+    r.m = t.m;
+    r.n = t.n;
+    r.k = t.k;
+    r.tile_m = t.tile_m;
+    r.tile_n = t.tile_n;
+  }
+  r.parts = t.parts > 0 ? t.parts : 1;
+  r.numel = t.numel;
+  *info = r;
   return TK_OK;
 }
 

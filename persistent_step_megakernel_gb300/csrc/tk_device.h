@@ -111,7 +111,8 @@ enum FastKind : int32_t {
   FK_L_SQUARE = 8,       // round(l0 * l0)
   FK_L_SCALE = 9,        // round(l0 * c)
   FK_L_AXPY = 10,        // round(l0 +/- a*l1)
-  FK_L_SCALE_AXPY = 11   // round(round(l0 * c) +/- a*l1)
+  FK_L_SCALE_AXPY = 11,  // round(round(l0 * c) +/- a*l1)
+  FK_E_UPDATE = 12       // round(l0 +/- a*round(acc))   (SGD step in a weight-gradient epilogue)
 };
 
 struct Chain {
@@ -142,6 +143,8 @@ enum TaskKind : int32_t {
 struct alignas(16) Task {
   int32_t kind;
   int32_t n_items;
+  int32_t op_index;          // program op this task computes (-1: an output copy or commit)
+  int32_t stage;             // stage the task runs in
   int32_t rank;              // index-space rank (0..4)
   int32_t vec;               // elements per thread-vector: 8 or 1
   int64_t shape[kMaxRank];   // index space

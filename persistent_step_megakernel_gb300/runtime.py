@@ -37,6 +37,15 @@ class TrainStep:
     def stats(self) -> dict:
         return B.tk_plan_stats_get(self.handle)
 
+    def tasks(self) -> list:
+        """The plan's device tasks in stage order, each with the op name it computes."""
+        out = []
+        for i in range(self.stats["tasks"]):
+            t = B.tk_plan_task(self.handle, i)
+            t["op"] = self.program.operations[t["op_index"]].name if t["op_index"] >= 0 else None
+            out.append(t)
+        return out
+
     def resource_usage(self) -> dict:
         return B.tk_resource_usage(self.handle)
 

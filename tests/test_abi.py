@@ -42,4 +42,4 @@ def test_options_defaults():
 def test_struct_sizes_match_the_header():
     assert ctypes.sizeof(B.tk_tensor_spec) == 88
     assert ctypes.sizeof(B.tk_op) == 448
-    assert ctypes.sizeof(B.tk_options) == 40
+    assert ctypes.sizeof(B.tk_options) == 48

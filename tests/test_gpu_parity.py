@@ -125,6 +125,21 @@ def test_fused_plan_bit_identical_to_unfused(key):
         np.testing.assert_array_equal(v, names_b[s.buffer], err_msg=s.buffer)
 
 
+@pytest.mark.parametrize("key", list(SMALL))
+def test_expression_forms_bit_identical(key):
+    # compiled fixed-shape loops, generic chains and the instruction form
+    # perform the same roundings in the same order
+    cfg = SMALL[key]
+    prog = S.mlp_step_program(cfg, export="grads")
+    arrays = S.mlp_inputs(cfg, prog)
+    ref, s0 = run_step(prog, arrays, expr_forms=0)
+    for forms in (1, 2):
+        got, st = run_step(prog, arrays, expr_forms=forms)
+        assert st.stats["compiled_tasks"] == 0
+        for spec, x, y in zip(prog.outputs, ref, got):
+            np.testing.assert_array_equal(x, y, err_msg=f"{spec.buffer} forms={forms}")
+
+
 @pytest.mark.parametrize("key", ["c1", "c2", "c4", "ragged_bf16"])
 def test_results_do_not_depend_on_grid_size(key):
     cfg = SMALL[key]
@@ -171,6 +186,21 @@ def test_three_steps_feed_state_back():
             vals[idx] = outs[slot]
     for slot, idx in prog.inplace.items():
         assert ulp_distance(gpu[slot], outs[slot], cfg.dtype).max() <= 3
+
+
+@pytest.mark.parametrize("key", list(SMALL))
+def test_state_program_fused_matches_unfused_over_steps(key):
+    # The timed program: weight-gradient GEMMs carry the in-place parameter
+    # update in their epilogue and run after the input-gradient GEMM that
+    # still reads the old weights; intermediate slots are reused across stages.
+    cfg = SMALL[key]
+    prog = S.mlp_step_program(cfg, export="state")
+    arrays = S.mlp_inputs(cfg, prog)
+    fused, sf = run_step(prog, arrays, steps=2)
+    plain, sp = run_step(prog, arrays, steps=2, fuse_epilogues=0, fuse_pointwise=0)
+    assert sf.stats["stages"] <= sp.stats["stages"]
+    for spec, x, y in zip(prog.outputs, fused, plain):
+        np.testing.assert_array_equal(x, y, err_msg=spec.buffer)
 
 
 def test_empty_batch():

@@ -64,9 +64,22 @@ def test_gemm_epilogue_chain_fusion():
     assert (s["fused_epilogues"], s["materialized_ops"], s["inlined_ops"], s["stages"]) == (0, 2, 1, 2)
 
 
-def test_chain_stops_at_program_outputs():
+def test_chain_ends_at_a_program_output():
+    # the relu output is returned: the epilogue stores it straight from the tile
     s = plan(_gemm_relu_sum(True))
-    assert (s["fused_epilogues"], s["materialized_ops"], s["inlined_ops"], s["stages"]) == (0, 3, 0, 3)
+    assert (s["fused_epilogues"], s["materialized_ops"], s["inlined_ops"], s["stages"]) == (1, 2, 0, 2)
+
+
+def test_chain_does_not_pass_through_a_program_output():
+    x, w = f32("x", (4, 8)), f32("W", (16, 8))
+    v = lambda n: f32(n, (4, 16))
+    ops = [Operation("t", "mm", (x, w.T), v("t")),
+           Operation("u", "relu", (v("t"),), v("u")),
+           Operation("n", "neg", (v("u"),), v("n")),
+           Operation("s", "sum", (v("n"),), f32("s", ()))]
+    s = plan(Program([x, w], [f32("s", ()), v("u")], ops))
+    # mm+relu fused (ends at the output u); neg inlines into the sum
+    assert (s["fused_epilogues"], s["materialized_ops"], s["inlined_ops"], s["stages"]) == (1, 2, 1, 2)
 
 
 def _update(read_after):
@@ -87,7 +100,7 @@ def test_inplace_update_committed_after_a_later_reader():
     assert (s["direct_state_commits"], s["output_copies"], s["stages"], s["direct_outputs"]) == (0, 1, 2, 1)
 
 
-def test_arena_reuse_adds_a_write_after_read_barrier():
+def test_arena_reuse_never_adds_a_barrier():
     x = f32("x", (64,))
     v = lambda n: f32(n, (64,))
     ops = [Operation("a", "neg", (x,), v("a")),
@@ -95,8 +108,21 @@ def test_arena_reuse_adds_a_write_after_read_barrier():
            Operation("c", "add", (v("a"), 1.0), v("c")),
            Operation("d", "mul", (x, 3.0), v("d")),
            Operation("e", "add", (v("d"), v("d")), v("e"))]
+    # d (stage 0) may not take a's slot while a is still read in stage 1
     s = plan(Program([x], [v("b"), v("c"), v("e")], ops))
-    assert (s["materialized_ops"], s["stages"], s["arena_elements"]) == (5, 4, 64)
+    assert (s["materialized_ops"], s["stages"], s["arena_elements"]) == (5, 3, 128)
+
+
+def test_arena_reuses_slots_across_stages():
+    x = f32("x", (64,))
+    v = lambda n: f32(n, (64,))
+    ops = [Operation("a", "neg", (x,), v("a")),
+           Operation("b", "mul", (v("a"), 2.0), v("b")),
+           Operation("c", "add", (v("b"), 1.0), v("c")),
+           Operation("e", "mul", (v("c"), 3.0), v("e"))]
+    # c (stage 2) takes a's slot: a was last read in stage 1
+    s = plan(Program([x], [v("e")], ops), fuse_pointwise=0)
+    assert (s["materialized_ops"], s["stages"], s["arena_elements"]) == (4, 4, 128)
 
 
 def test_large_mean_is_split():
@@ -107,9 +133,24 @@ def test_large_mean_is_split():
 
 def test_mlp_step_plan_counts():
     s = plan(S.mlp_step_program(S.CONFIGS["c2"], export="state"))
-    # fused: 3 forward addmm(+relu/+sub) and 2 input-grad mm(+threshold_backward); inlined: pow
-    assert (s["fused_epilogues"], s["inlined_ops"], s["materialized_ops"]) == (5, 1, 19)
+    # fused: 3 forward addmm(+relu/+sub), 2 input-grad mm(+threshold_backward) and
+    # 3 weight-grad mm(+SGD update, written in place); inlined: pow
+    assert (s["fused_epilogues"], s["inlined_ops"], s["materialized_ops"]) == (8, 1, 16)
     assert (s["direct_state_commits"], s["direct_outputs"], s["output_copies"]) == (6, 7, 0)
+    # forward 3, loss 1, then ga2 | gW3+update, ga1 | gW2+update, gW1+update | b1 update
+    assert s["stages"] == 8
+
+
+def test_weight_update_gemm_runs_after_the_input_grad_gemm_that_reads_w():
+    prog = S.mlp_step_program(S.CONFIGS["c2"], export="state")
+    h = B.tk_program_create(prog, B.options(sm_count=152), device=-1)
+    try:
+        tasks = [B.tk_plan_task(h, i) for i in range(B.tk_plan_stats_get(h)["tasks"])]
+    finally:
+        B.tk_program_destroy(h)
+    stage = {prog.operations[t["op_index"]].name: t["stage"] for t in tasks if t["op_index"] >= 0}
+    for i in (2, 3):  # gW_i (fused with W_i's update) after ga_{i-1}, which reads W_i
+        assert stage[f"gW{i}"] > stage[f"ga{i-1}"]
 
 
 # ------------------------------------------------------------ errors
@@ -184,3 +225,13 @@ def test_strided_operand_falls_back_to_generic_chain():
     assert (s["compiled_tasks"], s["chain_tasks"]) == (0, 1)
     s = plan(Program([x], [f32("y", (8, 16))], [Operation("y", "mul", (x, 3.0), f32("y", (8, 16)))]))
     assert (s["compiled_tasks"], s["chain_tasks"]) == (1, 0)
+
+
+def test_expr_forms_option_restricts_evaluators():
+    prog = S.mlp_step_program(S.CONFIGS["c2"], export="state")
+    s0, s1, s2 = (plan(prog, expr_forms=f) for f in (0, 1, 2))
+    assert s0["compiled_tasks"] > 0
+    assert s1["compiled_tasks"] == 0 and s1["chain_tasks"] == s0["compiled_tasks"] + s0["chain_tasks"]
+    assert s2["compiled_tasks"] == 0 and s2["chain_tasks"] == 0
+    with pytest.raises(B.TkError):
+        plan(prog, expr_forms=3)

@@ -176,6 +176,8 @@ typedef struct {
   int32_t m, n, k;             /* GEMM extents (0 otherwise) */
   int32_t tile_m, tile_n;      /* GEMM tile (0 otherwise) */
   int32_t parts;               /* reduction parts (1 = not split) */
+  int32_t staged_epilogue;     /* tensor-core GEMM whose epilogue moves tiles through shared memory */
+  int32_t reserved0;           /* 0 */
   int64_t numel;               /* elements of the task's index space */
 } tk_task_info;
 

@@ -73,6 +73,38 @@ __device__ __forceinline__ void store1(char* p, int dt, int64_t i, float v) {
     reinterpret_cast<__half*>(p)[i] = __float2half_rn(v);
 }
 
+// 8 bf16 or fp16 values packed in 16 bytes <-> floats.
+__device__ __forceinline__ void unpack8(uint4 raw, int dt, float (&v)[8]) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (dt == TK_BF16) {
+      __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[j]);
+      v[2 * j] = __low2float(h);
+      v[2 * j + 1] = __high2float(h);
+    } else {
+      __half2 h = *reinterpret_cast<const __half2*>(&w[j]);
+      v[2 * j] = __low2float(h);
+      v[2 * j + 1] = __high2float(h);
+    }
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&v)[8], int dt) {
+  uint32_t w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (dt == TK_BF16) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+      w[j] = *reinterpret_cast<uint32_t*>(&h);
+    } else {
+      __half2 h = __floats2half2_rn(v[2 * j], v[2 * j + 1]);
+      w[j] = *reinterpret_cast<uint32_t*>(&h);
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // 8 consecutive elements from a 16-byte aligned address.
 __device__ __forceinline__ void load8(const char* p, int dt, int64_t i, float (&v)[8]) {
   if (dt == TK_F32) {
@@ -81,20 +113,7 @@ __device__ __forceinline__ void load8(const char* p, int dt, int64_t i, float (&
     v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
     v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
   } else {
-    uint4 raw = *reinterpret_cast<const uint4*>(p + i * 2);
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (dt == TK_BF16) {
-        __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[j]);
-        v[2 * j] = __low2float(h);
-        v[2 * j + 1] = __high2float(h);
-      } else {
-        __half2 h = *reinterpret_cast<const __half2*>(&w[j]);
-        v[2 * j] = __low2float(h);
-        v[2 * j + 1] = __high2float(h);
-      }
-    }
+    unpack8(*reinterpret_cast<const uint4*>(p + i * 2), dt, v);
   }
 }
 
@@ -104,18 +123,7 @@ __device__ __forceinline__ void store8(char* p, int dt, int64_t i, const float (
     q[0] = make_float4(v[0], v[1], v[2], v[3]);
     q[1] = make_float4(v[4], v[5], v[6], v[7]);
   } else {
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (dt == TK_BF16) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-        w[j] = *reinterpret_cast<uint32_t*>(&h);
-      } else {
-        __half2 h = __floats2half2_rn(v[2 * j], v[2 * j + 1]);
-        w[j] = *reinterpret_cast<uint32_t*>(&h);
-      }
-    }
-    *reinterpret_cast<uint4*>(p + i * 2) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(p + i * 2) = pack8(v, dt);
   }
 }
 
@@ -392,12 +400,23 @@ __device__ __forceinline__ void unravel32(const Task& t, uint32_t f, int32_t* cr
 
 template <int V>
 __device__ __forceinline__ void round_vec(float (&x)[V], int dt) {
+  // pairs go through the packed conversions (each element rounded on its own)
   if (dt == TK_BF16) {
 #pragma unroll
-    for (int j = 0; j < V; ++j) x[j] = __bfloat162float(__float2bfloat16_rn(x[j]));
+    for (int j = 0; j + 1 < V; j += 2) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(x[j], x[j + 1]);
+      x[j] = __low2float(h);
+      x[j + 1] = __high2float(h);
+    }
+    if (V & 1) x[V - 1] = __bfloat162float(__float2bfloat16_rn(x[V - 1]));
   } else if (dt == TK_F16) {
 #pragma unroll
-    for (int j = 0; j < V; ++j) x[j] = __half2float(__float2half_rn(x[j]));
+    for (int j = 0; j + 1 < V; j += 2) {
+      const __half2 h = __floats2half2_rn(x[j], x[j + 1]);
+      x[j] = __low2float(h);
+      x[j + 1] = __high2float(h);
+    }
+    if (V & 1) x[V - 1] = __half2float(__float2half_rn(x[V - 1]));
   }
 }
 
@@ -573,7 +592,10 @@ struct FastTraits {
 
 // The same operations, in the same order and with the same roundings, as the
 // chain the kind stands for.
-template <int K>
+// kLast = false leaves out the final rounding, for a caller that converts the
+// result to the same 16-bit type right away (rounding twice to one format
+// equals rounding once).
+template <int K, bool kLast = true>
 __device__ __forceinline__ void fast_apply(const Fast& F, const float (&l0)[8], const float (&l1)[8],
                                            const float (&acc)[8], float (&x)[8]) {
   if constexpr (K == FK_E_UPDATE) {
@@ -587,15 +609,15 @@ __device__ __forceinline__ void fast_apply(const Fast& F, const float (&l0)[8], 
 #pragma unroll
       for (int j = 0; j < 8; ++j) x[j] = __fadd_rn(l0[j], __fmul_rn(F.a0, x[j]));
     }
-    round_vec<8>(x, F.r1);
+    if constexpr (kLast) round_vec<8>(x, F.r1);
   } else if constexpr (K >= FK_E_ACC && K <= FK_E_ACC_THRESH) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) x[j] = (K == FK_E_ACC || K == FK_E_ACC_THRESH) ? acc[j] : __fadd_rn(acc[j], l0[j]);
-    round_vec<8>(x, F.r0);
+    if (kLast || !(K == FK_E_ACC || K == FK_E_BIAS)) round_vec<8>(x, F.r0);  // r0 is the last rounding of these two
     if constexpr (K == FK_E_BIAS_RELU) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) x[j] = x[j] < 0.0f ? 0.0f : x[j];
-      round_vec<8>(x, F.r1);
+      if constexpr (kLast) round_vec<8>(x, F.r1);
     } else if constexpr (K == FK_E_BIAS_AXPY) {
       if (F.sub0) {
 #pragma unroll
@@ -604,11 +626,11 @@ __device__ __forceinline__ void fast_apply(const Fast& F, const float (&l0)[8], 
 #pragma unroll
         for (int j = 0; j < 8; ++j) x[j] = __fadd_rn(x[j], __fmul_rn(F.a0, l1[j]));
       }
-      round_vec<8>(x, F.r1);
+      if constexpr (kLast) round_vec<8>(x, F.r1);
     } else if constexpr (K == FK_E_ACC_THRESH) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) x[j] = l0[j] <= F.a0 ? 0.0f : x[j];
-      round_vec<8>(x, F.r1);
+      if constexpr (kLast) round_vec<8>(x, F.r1);
     }
   } else if constexpr (K == FK_L) {
 #pragma unroll
@@ -1160,6 +1182,8 @@ struct TcState {
   uint32_t full, empty;           // shared addresses of kStages mbarriers each
   uint32_t acc_full, acc_empty;   // 2 mbarriers each
   uint32_t tmem;                  // TMEM base address
+  uint32_t stg;                   // shared address of the epilogue staging area
+  uint32_t stg_warp_bytes;        // staging bytes per epilogue warp
   uint32_t p_it, m_it, m_tile, e_tile;
 };
 
@@ -1345,6 +1369,139 @@ __device__ __noinline__ void tc_epilogue_fast(const Ctx c, const Task& t, int64_
   }
 }
 
+// ---------------------------------------------- staged GEMM epilogue
+//
+// TMEM gives each epilogue thread one row of the tile, so direct global
+// accesses put 32 rows behind every warp instruction (32 L1 wavefronts).  The
+// staged epilogue moves each 32 x 32 chunk through shared memory instead:
+// per-row operands arrive by cp.async in row-contiguous order (issued a chunk
+// ahead, the first before the accumulator is ready), each thread reads its
+// row from shared memory, writes its results back there, and the warp stores
+// the chunk with 4 threads per 64-byte row.
+//
+// Piece j (16 bytes, 0..3) of row r in a 32 x 64-byte buffer sits at a
+// swizzled position so that both access patterns are free of bank conflicts.
+__device__ __forceinline__ uint32_t stg_off(int r, int j) {
+  return uint32_t(r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// Returns false if the accumulator wait timed out.  An operand with one row
+// for all tile rows (a bias) is staged once per tile: its tile_n values.
+template <int K>
+__device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int64_t m0, int64_t n0, uint32_t taddr,
+                                                uint32_t stg, uint32_t acc_bar, uint32_t phase, long long* stamp) {
+  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
+  const int64_t row0 = m0 + q * 32;
+  const int64_t M = t.m, N = t.n;
+  const int nch = t.tile_n / 32;
+  const int mask = t.epi_stage;
+  constexpr bool L0 = FastTraits<K>::load0, L1 = FastTraits<K>::load1;
+  const bool st0 = L0 && (mask & 1), st1 = L1 && (mask & 2);
+  const Fast F = fast_params(c, t);
+  // per warp: two chunk buffers per per-row slot (slot 0's first), then one
+  // kBcastBytes row per one-row slot, then (only without per-row slots) the
+  // output buffer; the output otherwise reuses the first per-row slot's
+  // current buffer
+  const uint32_t b0 = stg, b1 = b0 + (st0 ? 2 * kEpiBufBytes : 0);
+  const uint32_t r0 = b1 + (st1 ? 2 * kEpiBufBytes : 0);
+  const uint32_t r1 = r0 + (L0 && !st0 ? kBcastBytes : 0);
+  const uint32_t only = r1 + (L1 && !st1 ? kBcastBytes : 0);
+
+  auto prefetch = [&](int ch) {
+    const int64_t col0 = n0 + 32 * ch;
+    const uint32_t half = uint32_t(ch & 1) * kEpiBufBytes;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int p = 32 * i + lane, r = p >> 2, j = p & 3;
+      const int64_t row = row0 + r, col = col0 + 8 * j;
+      if (row < M && col < N) {
+        if (st0) cp_async16(b0 + half + stg_off(r, j), F.p0 + row * F.rs0 + col * 2);
+        if (st1) cp_async16(b1 + half + stg_off(r, j), F.p1 + row * F.rs1 + col * 2);
+      }
+    }
+  };
+
+  // one-row operands: 8 values per lane, with chunk 0
+  {
+    const int64_t col = n0 + 8 * lane;
+    if (8 * lane < t.tile_n && col < N) {
+      if (L0 && !st0) cp_async16(r0 + 16 * lane, F.p0 + col * 2);
+      if (L1 && !st1) cp_async16(r1 + 16 * lane, F.p1 + col * 2);
+    }
+  }
+  prefetch(0);
+  cp_async_commit();
+  if (!mbar_wait(acc_bar, phase, c.timeout_ns)) {
+    cp_async_wait<0>();
+    return false;
+  }
+  if (stamp) *stamp = global_ns();
+  tc_fence_after();
+  for (int ch = 0; ch < nch; ++ch) {
+    if (ch + 1 < nch) prefetch(ch + 1);
+    cp_async_commit();
+    uint32_t r[32];
+    tmem_ld32(taddr + (uint32_t(q * 32) << 16) + uint32_t(32 * ch), r);
+    cp_async_wait<1>();
+    __syncwarp();
+    const int64_t col0 = n0 + 32 * ch;
+    const uint32_t half = uint32_t(ch & 1) * kEpiBufBytes;
+    const uint32_t ob = st0 ? b0 + half : (st1 ? b1 + half : only);
+    // one 8-wide vector at a time: this thread's row, read and written in place
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      float l0[8], l1[8], a8[8], x[8];
+      if constexpr (L0) unpack8(lds128(st0 ? b0 + half + stg_off(lane, v) : r0 + 64 * ch + 16 * v), F.dt0, l0);
+      if constexpr (L1) unpack8(lds128(st1 ? b1 + half + stg_off(lane, v) : r1 + 64 * ch + 16 * v), F.dt1, l1);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) a8[j] = __uint_as_float(r[8 * v + j]);
+      fast_apply<K, false>(F, l0, l1, a8, x);
+      sts128(ob + stg_off(lane, v), pack8(x, F.out_dt));
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int p = 32 * i + lane, rr = p >> 2, j = p & 3;
+      const int64_t row = row0 + rr, col = col0 + 8 * j;
+      const uint4 val = lds128(ob + stg_off(rr, j));
+      if (row < M && col < N) *reinterpret_cast<uint4*>(F.out + (row * N + col) * 2) = val;
+    }
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+  return true;
+}
+
+__device__ __noinline__ bool tc_epilogue_staged_any(const Ctx c, const Task& t, int64_t m0, int64_t n0,
+                                                    uint32_t taddr, uint32_t stg, uint32_t acc_bar, uint32_t phase,
+                                                    long long* stamp) {
+  switch (t.chain.fast) {
+    case FK_E_ACC: return tc_epilogue_staged<FK_E_ACC>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp);
+    case FK_E_BIAS: return tc_epilogue_staged<FK_E_BIAS>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp);
+    case FK_E_BIAS_RELU: return tc_epilogue_staged<FK_E_BIAS_RELU>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp);
+    case FK_E_BIAS_AXPY: return tc_epilogue_staged<FK_E_BIAS_AXPY>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp);
+    case FK_E_ACC_THRESH: return tc_epilogue_staged<FK_E_ACC_THRESH>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp);
+    default: return tc_epilogue_staged<FK_E_UPDATE>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp);
+  }
+}
+
 __device__ __noinline__ void tc_epilogue_tile_any(const Ctx c, const Task& t, int64_t m0, int64_t n0,
                                                   uint32_t taddr) {
   const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
@@ -1476,13 +1633,20 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
   bool ok = true;
   bool first = true;
   const int lane = threadIdx.x & 31;
+  const uint32_t stg = ts.stg + uint32_t((threadIdx.x >> 5) - 4) * ts.stg_warp_bytes;
   for_my_tiles(c, st, [&](const Task& t, int64_t m0, int64_t n0) {
     const uint32_t acc = e_tile & 1u, ph = (e_tile >> 1) & 1u;
-    if (!mbar_wait(ts.acc_full + 8 * acc, ph, c.timeout_ns)) return ok = false;
-    if (prof && first && threadIdx.x == 128) prof[5] = global_ns();
+    long long* stamp = prof && first && threadIdx.x == 128 ? prof + 5 : nullptr;
     first = false;
-    tc_fence_after();
-    tc_epilogue_tile(c, t, m0, n0, ts.tmem + acc * kMaxTileN);
+    if (t.epi_stage) {
+      if (!tc_epilogue_staged_any(c, t, m0, n0, ts.tmem + acc * kMaxTileN, stg, ts.acc_full + 8 * acc, ph, stamp))
+        return ok = false;
+    } else {
+      if (!mbar_wait(ts.acc_full + 8 * acc, ph, c.timeout_ns)) return ok = false;
+      if (stamp) *stamp = global_ns();
+      tc_fence_after();
+      tc_epilogue_tile(c, t, m0, n0, ts.tmem + acc * kMaxTileN);
+    }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(ts.acc_empty + 8 * acc);
@@ -1564,7 +1728,6 @@ __device__ void run_item(const Ctx& c, const Task& t, int item, float* smem) {
   }
 }
 
-constexpr int kSmemFloats = 2 * 16 * (64 + 4) > 8 * 256 ? 2 * 16 * (64 + 4) : 8 * 256;
 
 __device__ __forceinline__ void copy_words(void* dst, const void* src, int bytes, int tid, int n) {
   uint64_t* d = static_cast<uint64_t*>(dst);
@@ -1590,7 +1753,6 @@ __device__ __forceinline__ void stage_in(const Program* prog, int s, Stage* s_st
 
 __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorMap* maps) {
   __shared__ void* s_io[2 * kMaxIO];
-  __shared__ __align__(16) float s_work[kSmemFloats];
   __shared__ Task s_tasks[kStageTasks];
   __shared__ __align__(16) Instr s_code[kStageCode];
   __shared__ __align__(16) Ref s_refs[kStageRefs];
@@ -1599,8 +1761,11 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   __shared__ __align__(8) uint64_t s_bar[2 * kStages + 4];
   __shared__ uint32_t s_tmem;
   __shared__ int s_flag;
-  extern __shared__ __align__(1024) unsigned char s_ring[];
+  extern __shared__ __align__(1024) unsigned char s_dyn[];
   const bool tc = maps != nullptr;
+  // scratch for reductions and CUDA-core GEMMs at the start of the dynamic
+  // region; in a tensor-core launch it overlays the (then idle) ring
+  float* s_work = reinterpret_cast<float*>(s_dyn + ((1024u - (smem_u32(s_dyn) & 1023u)) & 1023u));
   const int warp = threadIdx.x >> 5;
   const Program* prog = p.prog;
   const long long entry_ns = global_ns();
@@ -1609,8 +1774,10 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   stage_in(prog, 0, &s_stage, s_tasks, s_code, s_refs, 0);
   TcState ts{};
   if (tc) {
-    ts.ring = (smem_u32(s_ring) + 1023u) & ~1023u;
+    ts.ring = (smem_u32(s_dyn) + 1023u) & ~1023u;
     ts.slot_bytes = uint32_t(p.ring_stage_bytes);
+    ts.stg = ts.ring + uint32_t(kStages) * ts.slot_bytes;
+    ts.stg_warp_bytes = uint32_t(p.epi_warp_bytes);
     ts.full = smem_u32(&s_bar[0]);
     ts.empty = smem_u32(&s_bar[kStages]);
     ts.acc_full = smem_u32(&s_bar[2 * kStages]);
@@ -1641,6 +1808,17 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   if (tc) {
     tc_fence_after();
     ts.tmem = s_tmem;
+  }
+  if (warp == 2) {
+    // L2 prefetch of the op table and the inputs, spread over blocks and lanes
+    const int n_pf = prog->n_prefetch;
+    for (int g = blockIdx.x + gridDim.x * (threadIdx.x & 31); g < n_pf; g += 32 * gridDim.x) {
+      const Prefetch f = prog->prefetch[g];
+      const char* base = f.space == SP_TABLE ? reinterpret_cast<const char*>(prog)
+                                              : static_cast<const char*>(s_io[f.space == SP_IN ? f.slot : kMaxIO + f.slot]);
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + f.offset), "r"(uint32_t(f.bytes))
+                   : "memory");
+    }
   }
   Ctx c{nullptr, nullptr, nullptr, p.ws, reinterpret_cast<Header*>(p.ws), s_io, p.timeout_ns, s_prep};
   long long* prof = p.prof ? p.prof + kProfStamps * int64_t(blockIdx.x) : nullptr;
@@ -1777,10 +1955,10 @@ cudaError_t tk_kernel_launch(const tkd::Params& params, const void* maps, int n_
 cudaError_t tk_kernel_prepare(bool tc, size_t) {
   if (!tc) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(tkk::tk_persistent_tc<kSmallMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       tkd::kTcSmemBytes);
+                                       tkd::kDynSmemBudget);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(tkk::tk_persistent_tc<tkd::kMaxMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              tkd::kTcSmemBytes);
+                              tkd::kDynSmemBudget);
 }
 
 cudaError_t tk_kernel_occupancy(int* blocks_per_sm, bool tc, size_t dyn_smem) {

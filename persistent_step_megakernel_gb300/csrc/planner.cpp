@@ -1066,6 +1066,40 @@ class Planner {
     }
   }
 
+  // Staged epilogue of a compiled GEMM epilogue with a 16-bit output: which
+  // load slots are read per row (row stride != 0; 16-bit, 16-byte aligned
+  // rows) and go through shared memory.  -1: not eligible.
+  int epi_stage_mask(const Plan& plan, const Task& t) const {
+    const tkd::Chain& ch = t.chain;
+    if (t.kind != tkd::T_GEMM_TC || !ch.valid || ch.fast < tkd::FK_E_ACC ||
+        (ch.fast > tkd::FK_E_ACC_THRESH && ch.fast != tkd::FK_E_UPDATE))
+      return -1;
+    if (t.out.dtype == TK_F32 || t.out.base % 8 != 0 || t.n % 8 != 0) return -1;
+    // the last rounding is to the output type (the kernel folds it into the store)
+    const int last = ch.n_steps ? ch.steps[ch.n_steps - 1].round : ch.round0;
+    if (last != t.out.dtype) return -1;
+    int mask = 4;
+    for (int s = 0; s < ch.n_loads; ++s) {
+      const Ref& r = plan.refs[t.ref_begin + ch.load_ref[s]];
+      if (r.dtype == TK_F32 || r.base % 8 != 0) return -1;
+      if (r.stride[0] == 0) continue;  // one row for all tile rows: read directly
+      if ((r.stride[0] * 2) % 16 != 0) return -1;
+      mask |= 1 << s;
+    }
+    return mask;
+  }
+
+  // Staging bytes per epilogue warp: two chunk buffers per per-row operand
+  // (the output reuses the current one, else has its own buffer) and one
+  // tile row per one-row operand.
+  int epi_stage_plan(const Plan& plan, const Task& t) const {
+    const int mask = epi_stage_mask(plan, t);
+    if (mask < 0) return 0;
+    const int rows = (mask & 1) + ((mask >> 1) & 1);
+    const int bcast = t.chain.n_loads - rows;
+    return (rows ? 2 * rows : 1) * tkd::kEpiBufBytes + bcast * tkd::kBcastBytes;
+  }
+
   // Recognise the chain shapes the kernel runs as compiled loops (FastKind).
   // Called once the task's refs have their vector modes.
   void classify_fast(Plan& plan, Task& t) const {
@@ -1639,7 +1673,16 @@ class Planner {
     // Ring slots sized for the widest tile: smaller rings leave more of the
     // SM's unified L1/shared memory to the L1 cache.
     plan.ring_stage_bytes = tkd::kStageBytesA + max_bn * tkd::kTileK * 2;
-    plan.smem_bytes = plan.uses_tc ? size_t(tkd::kStages) * plan.ring_stage_bytes + 1024 : 0;
+    const size_t ring = 1024 + size_t(tkd::kStages) * plan.ring_stage_bytes;
+    for (auto& t : plan.tasks) {
+      t.epi_stage = 0;
+      const int need = epi_stage_plan(plan, t);
+      if (need > 0 && ring + 4 * size_t(std::max(need, plan.epi_warp_bytes)) <= size_t(tkd::kDynSmemBudget)) {
+        plan.epi_warp_bytes = std::max(plan.epi_warp_bytes, need);
+        t.epi_stage = epi_stage_mask(plan, t);
+      }
+    }
+    plan.smem_bytes = plan.uses_tc ? ring + 4 * size_t(plan.epi_warp_bytes) : 1024 + size_t(tkd::kWorkFloats) * 4;
     for (const auto& s : inputs_) plan.input_bytes.push_back(extent_of(s) * esize(s.dtype));
     for (const auto& s : outputs_) plan.output_bytes.push_back(numel(s) * esize(s.dtype));
     for (const auto& kv : inplace_) plan.inplace.push_back({kv.first, kv.second});

@@ -36,6 +36,7 @@ struct Plan {
   int32_t max_items = 1;
   size_t smem_bytes = 0;
   int ring_stage_bytes = 0;  // TMA ring slot size for the widest tensor-core tile
+  int epi_warp_bytes = 0;    // epilogue staging per epilogue warp
   bool uses_tc = false;
   tk_plan_stats stats{};
   // what tk_run checks

@@ -75,7 +75,26 @@ tk_status upload(tk_program* p) {
   size_t off_tasks = align_up(off_stages + pl.stages.size() * sizeof(tkd::Stage), 64);
   size_t off_code = align_up(off_tasks + pl.tasks.size() * sizeof(tkd::Task), 64);
   size_t off_refs = align_up(off_code + pl.code.size() * sizeof(tkd::Instr), 64);
-  size_t total = align_up(off_refs + pl.refs.size() * sizeof(tkd::Ref), 64);
+  size_t off_pf = align_up(off_refs + pl.refs.size() * sizeof(tkd::Ref), 64);
+  // L2 prefetch pieces: the op table, then the program inputs in order while
+  // their total stays within the budget.
+  std::vector<tkd::Prefetch> pf;
+  auto add_range = [&](int32_t space, int32_t slot, int64_t bytes) {
+    bytes &= ~int64_t(15);
+    for (int64_t o = 0; o < bytes; o += tkd::kPrefetchPiece)
+      pf.push_back({space, slot, o, std::min<int64_t>(tkd::kPrefetchPiece, bytes - o)});
+  };
+  int64_t in_total = 0;
+  for (int64_t b : pl.input_bytes) in_total += b;
+  const bool pf_inputs = in_total <= tkd::kPrefetchInputBudget;
+  // room for every piece: the table's (+1 for the piece list itself) and each input's
+  size_t max_pieces = size_t((off_pf + tkd::kPrefetchPiece - 1) / tkd::kPrefetchPiece) + 1;
+  if (pf_inputs) max_pieces += size_t(in_total / tkd::kPrefetchPiece) + pl.input_bytes.size();
+  size_t total = align_up(off_pf + max_pieces * sizeof(tkd::Prefetch), 64);
+  add_range(tkd::SP_TABLE, 0, int64_t(total));
+  if (pf_inputs)
+    for (size_t i = 0; i < pl.input_bytes.size(); ++i) add_range(tkd::SP_IN, int32_t(i), pl.input_bytes[i]);
+  if (pf.size() > max_pieces) return fail(TK_ERR_INVALID, "internal: prefetch list overflow");
   std::vector<unsigned char> host(total, 0);
   void* dev = nullptr;
   cudaError_t e = cudaMalloc(&dev, total);
@@ -90,7 +109,10 @@ tk_status upload(tk_program* p) {
   prog.tasks = reinterpret_cast<const tkd::Task*>(base + off_tasks);
   prog.code = reinterpret_cast<const tkd::Instr*>(base + off_code);
   prog.refs = reinterpret_cast<const tkd::Ref*>(base + off_refs);
+  prog.n_prefetch = int32_t(pf.size());
+  prog.prefetch = reinterpret_cast<const tkd::Prefetch*>(base + off_pf);
   std::memcpy(host.data() + off_prog, &prog, sizeof(prog));
+  if (!pf.empty()) std::memcpy(host.data() + off_pf, pf.data(), pf.size() * sizeof(tkd::Prefetch));
   if (!pl.stages.empty()) std::memcpy(host.data() + off_stages, pl.stages.data(), pl.stages.size() * sizeof(tkd::Stage));
   if (!pl.tasks.empty()) std::memcpy(host.data() + off_tasks, pl.tasks.data(), pl.tasks.size() * sizeof(tkd::Task));
   if (!pl.code.empty()) std::memcpy(host.data() + off_code, pl.code.data(), pl.code.size() * sizeof(tkd::Instr));
@@ -342,6 +364,7 @@ tk_status tk_run(tk_program* p, const void* const* inputs, int32_t n_inputs, voi
   prm.timeout_ns = static_cast<long long>(p->opt.barrier_timeout_s * 1e9);
   prm.prof = p->prof_offset >= 0 ? reinterpret_cast<long long*>(ws + p->prof_offset) : nullptr;
   prm.ring_stage_bytes = pl.ring_stage_bytes;
+  prm.epi_warp_bytes = pl.epi_warp_bytes;
   prm.n_in = n_inputs;
   prm.n_out = n_outputs;
   for (int i = 0; i < n_inputs; ++i) prm.io[i] = const_cast<void*>(inputs[i]);
@@ -431,6 +454,7 @@ tk_status tk_plan_task(const tk_program* p, int32_t index, tk_task_info* info) {
     r.tile_n = t.tile_n;
   }
   r.parts = t.parts > 0 ? t.parts : 1;
+  r.staged_epilogue = t.epi_stage != 0;
   r.numel = t.numel;
   *info = r;
   return TK_OK;

@@ -28,7 +28,18 @@ constexpr int kMaxTileN = 256;
 constexpr int kStages = 4;
 constexpr int kStageBytesA = kTileM * kTileK * 2;       // 16 KB
 constexpr int kStageBytesB = kMaxTileN * kTileK * 2;    // 32 KB
-constexpr int kTcSmemBytes = kStages * (kStageBytesA + kStageBytesB) + 1024;
+// Dynamic shared memory of a tensor-core launch: 1 KB alignment slack, the
+// TMA ring, then each epilogue warp's staging buffers.  The planner keeps the
+// total within kDynSmemBudget (the 227 KB per-block limit minus the kernel's
+// static shared memory, with margin).
+constexpr int kDynSmemBudget = 210 * 1024;
+// Scratch floats for reductions and CUDA-core GEMM tiles; at the start of the
+// dynamic region (in a tensor-core launch it overlays the ring, which is idle
+// outside the tensor-core phase of a stage).
+constexpr int kWorkFloats = 2 * 16 * (64 + 4) > 8 * 256 ? 2 * 16 * (64 + 4) : 8 * 256;
+// Epilogue staging: a 32-row x 32-column chunk of 16-bit values (64-byte rows).
+constexpr int kEpiBufBytes = 32 * 64;
+constexpr int kBcastBytes = kMaxTileN * 2;   // one 16-bit row of a tile
 constexpr int kTmemCols = 2 * kMaxTileN;                // double-buffered accumulator
 constexpr int kMaxMaps = 192;                           // TMA descriptors per launch
 
@@ -172,6 +183,10 @@ struct alignas(16) Task {
   uint32_t idesc;
   int32_t a_mn_major, b_mn_major;
   int32_t k_blocks;
+  // Staged epilogue (compiled GEMM epilogues with 16-bit output): bit s set =
+  // load slot s is read per row and copied through shared memory; bit 2 =
+  // the staged path is on.  0 = operands and output accessed directly.
+  int32_t epi_stage;
 };
 
 struct Stage {
@@ -184,9 +199,21 @@ struct Stage {
 
 // A stage whose descriptors fit these bounds is copied into shared memory
 // while the previous grid barrier completes.
-constexpr int kStageTasks = 16;
+constexpr int kStageTasks = 8;
 constexpr int kStageCode = 128;
 constexpr int kStageRefs = 64;
+
+// A byte range the kernel asks L2 to fetch at entry, so that the first reads
+// of program inputs and of the op table in later stages hit L2.  `space` is a
+// Space or SP_TABLE (the op table itself); offset and bytes are multiples of 16.
+constexpr int32_t SP_TABLE = 3;
+constexpr int64_t kPrefetchPiece = 64 * 1024;            // bytes per prefetch instruction
+constexpr int64_t kPrefetchInputBudget = 48ll << 20;     // inputs larger in total are not prefetched
+
+struct Prefetch {
+  int32_t space, slot;
+  int64_t offset, bytes;
+};
 
 struct Program {
   int32_t n_stages, n_tasks, n_code, n_refs;
@@ -194,6 +221,8 @@ struct Program {
   const Task* tasks;
   const Instr* code;
   const Ref* refs;
+  int32_t n_prefetch, pad;
+  const Prefetch* prefetch;
 };
 
 // Workspace header (offset 0, 256 bytes).  `count` only grows during a run
@@ -222,6 +251,7 @@ struct Params {
   long long* prof;      // optional stamps, [stage][block][kProfStamps]
   int n_in, n_out, n_maps;
   int ring_stage_bytes; // bytes per TMA ring slot (A tile + widest B tile)
+  int epi_warp_bytes;   // staging bytes per epilogue warp (after the ring)
   void* io[2 * kMaxIO];
 };
 

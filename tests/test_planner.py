@@ -235,3 +235,20 @@ def test_expr_forms_option_restricts_evaluators():
     assert s2["compiled_tasks"] == 0 and s2["chain_tasks"] == 0
     with pytest.raises(B.TkError):
         plan(prog, expr_forms=3)
+
+
+@pytest.mark.parametrize("name", ["c2", "c5"])
+def test_tensor_core_epilogues_are_staged(name):
+    # 16-bit GEMM epilogues move their tiles through shared memory.  With
+    # 256-wide tiles (C5) the ring leaves room for one per-row operand and no
+    # bias row besides it, so the output layer's bias-minus-target epilogue
+    # keeps direct accesses.
+    prog = S.mlp_step_program(S.CONFIGS[name], export="state")
+    h = B.tk_program_create(prog, B.options(sm_count=152), device=-1)
+    try:
+        tasks = [B.tk_plan_task(h, i) for i in range(B.tk_plan_stats_get(h)["tasks"])]
+    finally:
+        B.tk_program_destroy(h)
+    tc = [t for t in tasks if t["kind"] == "gemm_tc"]
+    direct = [prog.operations[t["op_index"]].name for t in tc if not t["staged_epilogue"]]
+    assert tc and direct == ([] if name == "c2" else ["z4"])

@@ -1271,6 +1271,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
                "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])::"memory");
 }
 
+// 8 consecutive accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])::"memory");
+}
+
 // Walk this block's tensor-core tiles of a stage in order (all roles use the
 // same sequence).  fn(task, m0, n0) returns false to stop.
 template <typename F>
@@ -1424,10 +1433,14 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
   const uint32_t r1 = r0 + (L0 && !st0 ? kBcastBytes : 0);
   const uint32_t only = r1 + (L1 && !st1 ? kBcastBytes : 0);
 
+  // The loops below stay rolled: the code is small enough to stay in the
+  // instruction cache, which matters more than loop overhead for the small
+  // tiles of latency-bound steps (the first chunk of a stage otherwise waits
+  // for its instructions).
   auto prefetch = [&](int ch) {
     const int64_t col0 = n0 + 32 * ch;
     const uint32_t half = uint32_t(ch & 1) * kEpiBufBytes;
-#pragma unroll
+#pragma unroll 1
     for (int i = 0; i < 4; ++i) {
       const int p = 32 * i + lane, r = p >> 2, j = p & 3;
       const int64_t row = row0 + r, col = col0 + 8 * j;
@@ -1454,29 +1467,31 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
   }
   if (stamp) *stamp = global_ns();
   tc_fence_after();
+  const uint32_t tlane = taddr + (uint32_t(q * 32) << 16);
+#pragma unroll 1
   for (int ch = 0; ch < nch; ++ch) {
     if (ch + 1 < nch) prefetch(ch + 1);
     cp_async_commit();
-    uint32_t r[32];
-    tmem_ld32(taddr + (uint32_t(q * 32) << 16) + uint32_t(32 * ch), r);
     cp_async_wait<1>();
     __syncwarp();
     const int64_t col0 = n0 + 32 * ch;
     const uint32_t half = uint32_t(ch & 1) * kEpiBufBytes;
     const uint32_t ob = st0 ? b0 + half : (st1 ? b1 + half : only);
     // one 8-wide vector at a time: this thread's row, read and written in place
-#pragma unroll
+#pragma unroll 1
     for (int v = 0; v < 4; ++v) {
+      uint32_t rv[8];
+      tmem_ld8(tlane + uint32_t(32 * ch + 8 * v), rv);
       float l0[8], l1[8], a8[8], x[8];
       if constexpr (L0) unpack8(lds128(st0 ? b0 + half + stg_off(lane, v) : r0 + 64 * ch + 16 * v), F.dt0, l0);
       if constexpr (L1) unpack8(lds128(st1 ? b1 + half + stg_off(lane, v) : r1 + 64 * ch + 16 * v), F.dt1, l1);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) a8[j] = __uint_as_float(r[8 * v + j]);
+      for (int j = 0; j < 8; ++j) a8[j] = __uint_as_float(rv[j]);
       fast_apply<K, false>(F, l0, l1, a8, x);
       sts128(ob + stg_off(lane, v), pack8(x, F.out_dt));
     }
     __syncwarp();
-#pragma unroll
+#pragma unroll 1
     for (int i = 0; i < 4; ++i) {
       const int p = 32 * i + lane, rr = p >> 2, j = p & 3;
       const int64_t row = row0 + rr, col = col0 + 8 * j;

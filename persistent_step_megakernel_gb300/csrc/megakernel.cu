@@ -771,8 +771,46 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return s;
 }
 
-__device__ __forceinline__ void finish_reduction(const Ctx& c, const Task& t, int64_t o, float acc) {
+// A reduction's epilogue chain at output o (coordinates over post_shape).
+__device__ __noinline__ float reduction_post(const Ctx c, const Task& t, int64_t o, float v) {
+  int64_t crd[kMaxRank];
+  int64_t f = o;
+#pragma unroll
+  for (int d = kMaxRank - 1; d >= 0; --d) {
+    if (d < t.post_rank) {
+      crd[d] = f % t.post_shape[d];
+      f /= t.post_shape[d];
+    } else {
+      crd[d] = 0;
+    }
+  }
+  const Ref* refs = c.refs + t.ref_begin;
+  float L[2][1] = {{0.0f}, {0.0f}};
+  if (t.post.n_loads > 0) load_ref<1>(c, t, refs[t.post.load_ref[0]], crd, L[0]);
+  if (t.post.n_loads > 1) load_ref<1>(c, t, refs[t.post.load_ref[1]], crd, L[1]);
+  const float a[1] = {v};
+  float x[1];
+  chain_compute<1>(t.post, L, a, x);
+  return x[0];
+}
+
+// The operand of a compiled reduction epilogue (the parameter being updated)
+// at output o, loaded before the reduction so its latency overlaps the sums.
+__device__ __forceinline__ float post_operand(const Ctx& c, const Task& t, int64_t o) {
+  if (t.post.fast != FK_E_UPDATE) return 0.0f;
+  const Ref& r = c.refs[t.ref_begin + t.post.load_ref[0]];
+  return load1(space_ptr(c, r.space, r.slot), r.dtype, r.base + o);
+}
+
+__device__ __forceinline__ void finish_reduction(const Ctx& c, const Task& t, int64_t o, float acc, float pre) {
   float v = t.red_mean ? __fdiv_rn(acc, t.size_f) : acc;
+  if (t.post.fast == FK_E_UPDATE) {  // p -/+ a * round(v)
+    const ChainStep st = t.post.steps[0];
+    const float r = round_to(v, t.post.round0);
+    v = round_to(st.op == OP_SUB ? __fsub_rn(pre, __fmul_rn(st.imm, r)) : __fadd_rn(pre, __fmul_rn(st.imm, r)), st.round);
+  } else if (t.post.valid) {
+    v = reduction_post(c, t, o, v);
+  }
   store1(space_ptr(c, t.out.space, t.out.slot), t.out.dtype, t.out.base + o, v);
 }
 
@@ -957,6 +995,7 @@ __device__ __noinline__ void run_reduce_row(const Ctx c, const Task& t, int item
   const int p = item % t.parts;
   const int64_t r0 = int64_t(p) * t.part_len;
   const int64_t r1 = min(t.red_inner, r0 + t.part_len);
+  const float pre = threadIdx.x == 0 && t.parts == 1 ? post_operand(c, t, o) : 0.0f;
   float acc;
   bool done = false;
   if constexpr (V == 8) {
@@ -972,7 +1011,7 @@ __device__ __noinline__ void run_reduce_row(const Ctx c, const Task& t, int item
   acc = block_sum(acc, red);
   if (threadIdx.x == 0) {
     if (t.parts == 1)
-      finish_reduction(c, t, o, acc);
+      finish_reduction(c, t, o, acc, pre);
     else
       reinterpret_cast<float*>(c.ws)[t.scratch + o * t.parts + p] = acc;
   }
@@ -983,7 +1022,7 @@ __device__ __noinline__ void run_reduce_row(const Ctx c, const Task& t, int item
 // order.
 template <int V>
 __device__ __forceinline__ void col_combine(const Ctx& c, const Task& t, int64_t ch, int p, const float (&acc)[V],
-                                            float* red) {
+                                            float* red, float pre) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t Q = t.red_inner;
 #pragma unroll
@@ -996,7 +1035,7 @@ __device__ __forceinline__ void col_combine(const Ctx& c, const Task& t, int64_t
     const int64_t col = ch * 32 * V + threadIdx.x;
     if (col < Q) {
       if (t.parts == 1)
-        finish_reduction(c, t, col, s);
+        finish_reduction(c, t, col, s, pre);
       else
         reinterpret_cast<float*>(c.ws)[t.scratch + col * t.parts + p] = s;
     }
@@ -1014,6 +1053,8 @@ __device__ __noinline__ void run_reduce_col_fast(const Ctx c, const Task& t, int
   const int64_t col0 = ch * 256 + lane * 8;
   const int64_t r0 = int64_t(p) * t.part_len;
   const int64_t r1 = min(t.red_outer, r0 + t.part_len);
+  const int64_t my_col = ch * 256 + threadIdx.x;
+  const float pre = t.parts == 1 && my_col < Q ? post_operand(c, t, my_col) : 0.0f;
   const Fast F = fast_params(c, t);
   float acc[8], none[8];
 #pragma unroll
@@ -1038,7 +1079,7 @@ __device__ __noinline__ void run_reduce_col_fast(const Ctx c, const Task& t, int
       }
     }
   }
-  col_combine<8>(c, t, ch, p, acc, red);
+  col_combine<8>(c, t, ch, p, acc, red, pre);
 }
 
 template <int V>
@@ -1050,6 +1091,8 @@ __device__ __noinline__ void run_reduce_col(const Ctx c, const Task& t, int item
   const int64_t col0 = ch * 32 * V + lane * V;
   const int64_t r0 = int64_t(p) * t.part_len;
   const int64_t r1 = min(t.red_outer, r0 + t.part_len);
+  const int64_t my_col = ch * 32 * V + threadIdx.x;
+  const float pre = t.parts == 1 && threadIdx.x < 32 * V && my_col < Q ? post_operand(c, t, my_col) : 0.0f;
   float acc[V];
 #pragma unroll
   for (int j = 0; j < V; ++j) acc[j] = 0.0f;
@@ -1063,23 +1106,25 @@ __device__ __noinline__ void run_reduce_col(const Ctx c, const Task& t, int item
       for (int j = 0; j < V; ++j) acc[j] = __fadd_rn(acc[j], v[j]);
     }
   }
-  col_combine<V>(c, t, ch, p, acc, red);
+  col_combine<V>(c, t, ch, p, acc, red, pre);
 }
 
 __device__ __noinline__ void run_reduce_final(const Ctx c, const Task& t, int item, float* red) {
   const float* part = reinterpret_cast<const float*>(c.ws) + t.scratch;
   if (t.final_block) {
     const int64_t o = item;
+    const float pre = threadIdx.x == 0 ? post_operand(c, t, o) : 0.0f;
     float acc = 0.0f;
     for (int q = threadIdx.x; q < t.parts; q += kThreads) acc = __fadd_rn(acc, part[o * t.parts + q]);
     acc = block_sum(acc, red);
-    if (threadIdx.x == 0) finish_reduction(c, t, o, acc);
+    if (threadIdx.x == 0) finish_reduction(c, t, o, acc, pre);
   } else {
     const int64_t o = int64_t(item) * kThreads + threadIdx.x;
     if (o >= t.red_outer) return;
+    const float pre = post_operand(c, t, o);
     float acc = 0.0f;
     for (int q = 0; q < t.parts; ++q) acc = __fadd_rn(acc, part[o * t.parts + q]);
-    finish_reduction(c, t, o, acc);
+    finish_reduction(c, t, o, acc, pre);
   }
 }
 

@@ -445,6 +445,55 @@ class Planner {
     }
   }
 
+  // Reduction epilogues (a GB300 addition): the single-user pointwise chain
+  // after a sum/mean whose output is not returned, e.g. gb = sum(g, 0) then the
+  // in-place b' = b - lr*gb.  Only chains the kernel evaluates in chain form
+  // are taken: every other operand is a scalar or a contiguous view (of the
+  // output's shape) of a program input or of a GEMM/reduction result, at most
+  // two loads and four steps.
+  void detect_reduction_epilogues() {
+    if (!opt_.fuse_epilogues || opt_.expr_forms >= 2) return;
+    for (const OpInfo& r : ops_) {
+      if (!is_red(r.kind) || output_buffers_.count(r.out.buffer_id) || fused_.count(r.index)) continue;
+      std::vector<int> chain;
+      int current = r.out.buffer_id, loads = 0;
+      bool ok = true;
+      while (ok && bufs_[current].users.size() == 1 && chain.size() < size_t(tkd::kChainSteps)) {
+        const OpInfo& nxt = ops_[bufs_[current].users[0]];
+        if (!is_pointwise(nxt.kind) || nxt.kind == TK_OP_FULL) break;
+        if (nxt.kind == TK_OP_POW && (nxt.in.size() > 1 ? nxt.in[1].value : nxt.exponent) != 2.0) break;
+        if (shape_of(nxt.out) != bufs_[current].shape || !exact_contig(nxt.out)) break;
+        int roots_seen = 0;
+        for (const auto& o : nxt.in) {
+          if (o.scalar) continue;
+          if (o.t.buffer_id == current) {
+            if (shape_of(o.t) != bufs_[current].shape || !exact_contig(o.t)) ok = false;
+            ++roots_seen;
+            continue;
+          }
+          const Buf& b = bufs_.at(o.t.buffer_id);
+          const bool materialised = b.input >= 0 || (b.producer >= 0 && !is_pointwise(ops_[b.producer].kind) &&
+                                                     b.producer < r.index);
+          if (!materialised || shape_of(o.t) != bufs_[current].shape || !exact_contig(o.t)) ok = false;
+          ++loads;
+        }
+        if (roots_seen != 1 || loads > 2) ok = false;
+        if (!ok) break;
+        chain.push_back(nxt.index);
+        current = nxt.out.buffer_id;
+        if (output_buffers_.count(current)) break;
+      }
+      if (!ok || chain.empty()) continue;
+      Fused f;
+      f.chain = chain;
+      f.final_buf = current;
+      fused_[r.index] = f;
+      fused_skip_.insert(r.out.buffer_id);
+      for (size_t i = 0; i + 1 < chain.size(); ++i) fused_skip_.insert(ops_[chain[i]].out.buffer_id);
+      fused_skip_.insert(current);
+    }
+  }
+
   bool is_chain_final(int buffer) const {
     for (const auto& kv : fused_)
       if (kv.second.final_buf == buffer) return true;
@@ -1446,7 +1495,8 @@ class Planner {
       t.code_len = int(plan.code.size()) - t.code_begin;
       t.n_refs = int(plan.refs.size()) - t.ref_begin;
     }
-    t.out = out_ref(op.out.buffer_id);
+    auto fused_it = fused_.find(op.index);
+    t.out = out_ref(fused_it != fused_.end() ? fused_it->second.final_buf : op.out.buffer_id);
     t.red_mean = op.kind == TK_OP_MEAN;
     t.size_f = float(double(n_red));
     if (row) {
@@ -1475,6 +1525,7 @@ class Planner {
       t.parts = int(ceil_div(std::max<int64_t>(n_red, 1), t.part_len));
       t.n_items = int(chunks * t.parts);
     }
+    if (t.parts <= 1 && fused_it != fused_.end()) lower_post_chain(plan, t, op, fused_it->second);
     finish_refs(plan, t);
     classify_fast(plan, t);
     if (n_out == 0) t.n_items = 0;
@@ -1495,7 +1546,45 @@ class Planner {
     f.n_items = int(f.final_block ? n_out : ceil_div(n_out, tkd::kThreads));
     f.code_begin = int(plan.code.size());
     f.ref_begin = int(plan.refs.size());
+    if (fused_it != fused_.end()) {
+      lower_post_chain(plan, f, op, fused_it->second);
+      finish_refs(plan, f);
+    }
     return {t, f};
+  }
+
+  // The chain after reduction r, evaluated per finished output of task t.
+  void lower_post_chain(Plan& plan, Task& t, const OpInfo& r, const Fused& fu) {
+    const Shape out_shape = shape_of(r.out);
+    t.post_rank = int(out_shape.size());
+    for (size_t d = 0; d < out_shape.size(); ++d) t.post_shape[d] = out_shape[d];
+    ChainBuild cb{&plan, this, t.ref_begin};
+    cb.ch.start = tkd::CH_ACC;
+    cb.ch.addmm_mode = tkd::AM_ACC;
+    cb.ch.bias = -1;
+    cb.ch.round0 = r.out.dtype;
+    cb.started = true;
+    int root = r.out.buffer_id;
+    for (int ci : fu.chain) {
+      cb.root_buf = root;
+      cb.spine_op(ops_[ci], identity_map(int(out_shape.size())));
+      root = ops_[ci].out.buffer_id;
+    }
+    if (cb.fail) throw Error(TK_ERR_INVALID, "internal: reduction epilogue is not a chain");
+    cb.ch.valid = 1;
+    // p -/+ a*round(v) with p contiguous over the outputs: the compiled update
+    const tkd::ChainStep& s0 = cb.ch.steps[0];
+    if (opt_.expr_forms == 0 && cb.ch.n_steps == 1 && cb.ch.n_loads == 1 && s0.ext == tkd::EXT_LOAD0 && s0.second &&
+        (s0.op == tkd::OP_ADD || s0.op == tkd::OP_SUB)) {
+      const Ref& r = plan.refs[t.ref_begin + cb.ch.load_ref[0]];
+      bool flat = true;
+      Shape cs = contig(out_shape);
+      for (int d = 0; d < t.post_rank; ++d)
+        if (out_shape[d] > 1 && r.stride[d] != cs[d]) flat = false;
+      if (flat) cb.ch.fast = tkd::FK_E_UPDATE;
+    }
+    t.post = cb.ch;
+    t.n_refs = int(plan.refs.size()) - t.ref_begin;
   }
 
   // ------------------------------------------------------------ the plan
@@ -1513,6 +1602,7 @@ class Planner {
     arena_total_ = 0;
 
     detect_epilogues();
+    detect_reduction_epilogues();
     choose_inline();
     build_schedule();
     choose_direct_aliases();
@@ -1571,6 +1661,8 @@ class Planner {
           stage_reads.insert(stage_reads.end(), reads.begin(), reads.end());
           barrier();
           stages.back().push_back(ts[1]);
+          // the final pass reads a reduction epilogue's operands
+          if (ts[1].post.valid) stage_reads.insert(stage_reads.end(), reads.begin(), reads.end());
           stage_writes.insert(stage_writes.end(), writes.begin(), writes.end());
           stage_of_[pos] = int(stages.size()) - 1;
           continue;

@@ -183,6 +183,13 @@ struct alignas(16) Task {
   uint32_t idesc;
   int32_t a_mn_major, b_mn_major;
   int32_t k_blocks;
+  // Reductions: a pointwise chain applied to each finished output (e.g. the
+  // SGD step of a bias right after its gradient's column sum).  Its start is
+  // the reduced value (after the mean division) rounded to round0; its loads
+  // are indexed by the output's coordinates in post_shape.
+  Chain post;
+  int64_t post_shape[kMaxRank];
+  int32_t post_rank;
   // Staged epilogue (compiled GEMM epilogues with 16-bit output): bit s set =
   // load slot s is read per row and copied through shared memory; bit 2 =
   // the staged path is on.  0 = operands and output accessed directly.

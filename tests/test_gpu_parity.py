@@ -203,6 +203,29 @@ def test_state_program_fused_matches_unfused_over_steps(key):
         np.testing.assert_array_equal(x, y, err_msg=spec.buffer)
 
 
+@pytest.mark.parametrize("rows,cols,dims,op", [(4096, 8, (0,), "sum"), (64, 24, (0,), "sum"),
+                                                  (3, 40000, (1,), "mean"), (8, 16, (1,), "mean")])
+def test_reduction_epilogue_matches_unfused_and_oracle(rows, cols, dims, op):
+    # A chain after a reduction runs on each finished output, also behind a
+    # split reduction's final pass.
+    g = TensorSpec.contiguous("g", (rows, cols), "float32")
+    n_out = cols if dims == (0,) else rows
+    b = TensorSpec.contiguous("b", (n_out,), "bfloat16")
+    red = TensorSpec.contiguous("r", (n_out,), "float32")
+    ops = [Operation("r", op, (g,), red, {"dims": dims}),
+           Operation("bn", "sub", (b, red), TensorSpec.contiguous("bn", (n_out,), "bfloat16"), {"alpha": 0.25})]
+    prog = Program([g, b], [TensorSpec.contiguous("bn", (n_out,), "bfloat16")], ops, {0: 1})
+    rng = np.random.default_rng(7)
+    arrays = [S.to_storage(rng.standard_normal((rows, cols)), "float32"),
+              S.to_storage(rng.standard_normal(n_out), "bfloat16")]
+    fused, sf = run_step(prog, arrays)
+    plain, sp = run_step(prog, arrays, fuse_epilogues=0)
+    assert sf.stats["fused_epilogues"] == 1 and sp.stats["fused_epilogues"] == 0
+    np.testing.assert_array_equal(fused[0], plain[0])
+    want = oracle.run_program(prog, values(arrays, prog))[0]
+    assert ulp_distance(fused[0], want, "bfloat16").max() <= 1
+
+
 def test_empty_batch():
     cfg = S.scaled(S.CONFIGS["c1"], batch=0)
     prog = S.mlp_step_program(cfg, export="grads")

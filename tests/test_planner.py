@@ -133,12 +133,14 @@ def test_large_mean_is_split():
 
 def test_mlp_step_plan_counts():
     s = plan(S.mlp_step_program(S.CONFIGS["c2"], export="state"))
-    # fused: 3 forward addmm(+relu/+sub), 2 input-grad mm(+threshold_backward) and
-    # 3 weight-grad mm(+SGD update, written in place); inlined: pow
-    assert (s["fused_epilogues"], s["inlined_ops"], s["materialized_ops"]) == (8, 1, 16)
+    # fused: 3 forward addmm(+relu/+sub), 2 input-grad mm(+threshold_backward),
+    # 3 weight-grad mm(+SGD update, written in place) and 3 bias-grad sums
+    # (+SGD update); inlined: pow
+    assert (s["fused_epilogues"], s["inlined_ops"], s["materialized_ops"]) == (11, 1, 13)
     assert (s["direct_state_commits"], s["direct_outputs"], s["output_copies"]) == (6, 7, 0)
-    # forward 3, loss 1, then ga2 | gW3+update, ga1 | gW2+update, gW1+update | b1 update
-    assert s["stages"] == 8
+    # forward 3, loss 1, then ga2, gb3+update | gW3+update, ga1, gb2+update |
+    # gW2+update, gW1+update, gb1+update
+    assert s["stages"] == 7
 
 
 def test_weight_update_gemm_runs_after_the_input_grad_gemm_that_reads_w():
@@ -252,3 +254,14 @@ def test_tensor_core_epilogues_are_staged(name):
     tc = [t for t in tasks if t["kind"] == "gemm_tc"]
     direct = [prog.operations[t["op_index"]].name for t in tc if not t["staged_epilogue"]]
     assert tc and direct == ([] if name == "c2" else ["z4"])
+
+
+def test_reduction_epilogue_fuses_the_bias_update():
+    g, b = f32("g", (16, 8)), f32("b", (8,))
+    ops = [Operation("gb", "sum", (g,), f32("gb", (8,)), {"dims": (0,)}),
+           Operation("bn", "sub", (b, f32("gb", (8,))), f32("bn", (8,)), {"alpha": 0.5})]
+    s = plan(Program([g, b], [f32("bn", (8,))], ops, {0: 1}))
+    assert (s["fused_epilogues"], s["materialized_ops"], s["stages"], s["direct_state_commits"]) == (1, 1, 1, 1)
+    # a returned gradient is not fused (the chain would have to pass through it)
+    s = plan(Program([g, b], [f32("bn", (8,)), f32("gb", (8,))], ops, {0: 1}))
+    assert (s["fused_epilogues"], s["materialized_ops"], s["stages"]) == (0, 2, 2)

@@ -535,6 +535,24 @@ __device__ __forceinline__ void chain_compute(const Chain& ch, const float (&L)[
   }
 }
 
+// A GEMM's side output: one op on the stored (rounded) final value x, the
+// same arithmetic as the chain step it stands for.
+// (The planner only makes sides of multiplications by a constant, negations
+// and casts.)
+__device__ __forceinline__ float side_value(const ChainStep& st, float x) {
+  const float y = st.op == OP_MUL ? __fmul_rn(x, st.cval) : st.op == OP_NEG ? -x : x;
+  return round_to(y, st.round);
+}
+
+// Out of line, so that the epilogues without a side output carry no code for it.
+template <int V>
+__device__ __noinline__ void store_side(const Ctx c, const Task& t, int64_t flat, const float (&x)[V]) {
+  float y[V];
+#pragma unroll 1
+  for (int j = 0; j < V; ++j) y[j] = side_value(t.side, x[j]);
+  store_out<V>(c, t.out2, flat, y);
+}
+
 // ------------------------------------------------- compiled chain shapes
 //
 // Parameters of a FastKind chain, read once per work item into registers.
@@ -1198,6 +1216,7 @@ __device__ __noinline__ void run_gemm_simt(const Ctx c, const Task& t, int item,
         const float a1[1] = {acc[i][j]};
         eval_expr<1>(c, t, crd, a1, v);
         store_out<1>(c, t.out, row * t.n + col, v);
+        if (t.has_side) store_side<1>(c, t, row * t.n + col, v);
       }
     }
   }
@@ -1374,6 +1393,7 @@ __device__ __noinline__ void tc_epilogue_tile_chain(const Ctx c, const Task& t, 
           for (int j = 0; j < 8; ++j) a8[j] = __uint_as_float(r[8 * (v + h) + j]);
           chain_compute<8>(P.ch, L[h], a8, out);
           prep_store<8>(P, row * N + col, out);
+          if (t.has_side) store_side<8>(c, t, row * N + col, out);
         }
       }
     }
@@ -1418,6 +1438,7 @@ __device__ __noinline__ void tc_epilogue_fast(const Ctx c, const Task& t, int64_
         for (int j = 0; j < 8; ++j) a8[j] = __uint_as_float(r[8 * v + j]);
         fast_apply<K>(F, l0[v], l1[v], a8, x);
         store8(F.out, F.out_dt, orow + col, x);
+        if (t.has_side) store_side<8>(c, t, orow + col, x);
       }
     }
   }
@@ -1456,6 +1477,43 @@ __device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+// Store a staged 32 x 32 chunk (16-bit values), four lanes per 64-byte row.
+__device__ __forceinline__ void stage_store(uint32_t buf, char* out, int64_t row0, int64_t col0, int64_t M,
+                                            int64_t N) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int i = 0; i < 4; ++i) {
+    const int p = 32 * i + lane, rr = p >> 2, j = p & 3;
+    const int64_t row = row0 + rr, col = col0 + 8 * j;
+    const uint4 val = lds128(buf + stg_off(rr, j));
+    if (row < M && col < N) *reinterpret_cast<uint4*>(out + (row * N + col) * 2) = val;
+  }
+}
+
+// A GEMM's side output from a staged chunk: each lane turns its row of the
+// stored (rounded) values into the side values in place, then the chunk goes
+// to out2.  Called after the chunk's own store (a __syncwarp apart).
+__device__ __noinline__ void stage_side(const Task& t, uint32_t buf, int64_t row0, int64_t col0, int64_t M,
+                                        int64_t N, int out_dt, char* out2) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+#pragma unroll 1
+  for (int v = 0; v < 4; ++v) {
+    float x[8];
+    unpack8(lds128(buf + stg_off(lane, v)), out_dt, x);
+    if (t.side.op == OP_MUL) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = __fmul_rn(x[j], t.side.cval);
+    } else if (t.side.op == OP_NEG) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = -x[j];
+    }
+    sts128(buf + stg_off(lane, v), pack8(x, t.out2.dtype));  // rounds to the side's type
+  }
+  __syncwarp();
+  stage_store(buf, out2, row0, col0, M, N);
+}
+
 // Returns false if the accumulator wait timed out.  An operand with one row
 // for all tile rows (a bias) is staged once per tile: its tile_n values.
 template <int K>
@@ -1477,6 +1535,7 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
   const uint32_t r0 = b1 + (st1 ? 2 * kEpiBufBytes : 0);
   const uint32_t r1 = r0 + (L0 && !st0 ? kBcastBytes : 0);
   const uint32_t only = r1 + (L1 && !st1 ? kBcastBytes : 0);
+  char* const out2 = t.has_side ? space_ptr(c, t.out2.space, t.out2.slot) + t.out2.base * 2 : nullptr;
 
   // The loops below stay rolled: the code is small enough to stay in the
   // instruction cache, which matters more than loop overhead for the small
@@ -1536,13 +1595,8 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
       sts128(ob + stg_off(lane, v), pack8(x, F.out_dt));
     }
     __syncwarp();
-#pragma unroll 1
-    for (int i = 0; i < 4; ++i) {
-      const int p = 32 * i + lane, rr = p >> 2, j = p & 3;
-      const int64_t row = row0 + rr, col = col0 + 8 * j;
-      const uint4 val = lds128(ob + stg_off(rr, j));
-      if (row < M && col < N) *reinterpret_cast<uint4*>(F.out + (row * N + col) * 2) = val;
-    }
+    stage_store(ob, F.out, row0, col0, M, N);
+    if (t.has_side) stage_side(t, ob, row0, col0, M, N, F.out_dt, out2);
     __syncwarp();
   }
   cp_async_wait<0>();
@@ -1583,6 +1637,7 @@ __device__ __noinline__ void tc_epilogue_tile_any(const Ctx c, const Task& t, in
           float out[8];
           vm_eval<8>(c, t, crd, a8, out);
           store_out<8>(c, t.out, row * t.n + col, out);
+          if (t.has_side) store_side<8>(c, t, row * t.n + col, out);
         }
       }
     } else {
@@ -1594,6 +1649,7 @@ __device__ __noinline__ void tc_epilogue_tile_any(const Ctx c, const Task& t, in
           float out[1];
           eval_expr<1>(c, t, crd, a1, out);
           store_out<1>(c, t.out, row * t.n + col, out);
+          if (t.has_side) store_side<1>(c, t, row * t.n + col, out);
         }
       }
     }

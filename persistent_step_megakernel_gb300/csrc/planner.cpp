@@ -156,6 +156,7 @@ class Planner {
     int final_buf;
   };
   std::map<int, Fused> fused_;          // mm op index -> chain
+  std::map<int, int> side_;             // fused mm op index -> pointwise op it also computes
   std::set<int> fused_skip_;            // buffers a fused GEMM makes unnecessary
   std::set<int> inline_;                // buffers evaluated at their consumer
   std::vector<int> schedule_;           // op indices (a fused mm stands for its chain)
@@ -494,6 +495,52 @@ class Planner {
     }
   }
 
+  // Side outputs (a GB300 addition in the spirit of the page's side
+  // epilogues): a fused GEMM whose final value has several users also writes
+  // one of them from the same tile when that user is a one-operand pointwise
+  // op of the final value (e.g. the loss gradient 2/N * d next to d) and would
+  // be stored anyway (a GEMM operand, a returned value or a value with several
+  // users).  Not for in-place outputs.
+  void detect_side_outputs() {
+    for (auto& kv : fused_) {
+      const OpInfo& mm = ops_[kv.first];
+      if (!is_mm(mm.kind)) continue;
+      const int fin = kv.second.final_buf;
+      const Buf& fb = bufs_.at(fin);
+      if (fb.users.size() < 2) continue;
+      for (int u : fb.users) {
+        const OpInfo& op = ops_[u];
+        if (!is_pointwise(op.kind) || op.kind == TK_OP_FULL || fused_skip_.count(op.out.buffer_id)) continue;
+        if (op.kind != TK_OP_MUL && op.kind != TK_OP_NEG && op.kind != TK_OP_CAST) continue;
+        if (inplace_target(op.out.buffer_id) >= 0) continue;
+        if (shape_of(op.out) != fb.shape || !exact_contig(op.out)) continue;
+        bool ok = true;
+        int roots_seen = 0;
+        for (const auto& o : op.in) {
+          if (o.scalar) continue;
+          if (o.t.buffer_id == fin && shape_of(o.t) == fb.shape && exact_contig(o.t)) ++roots_seen;
+          else ok = false;
+        }
+        if (!ok || roots_seen != 1) continue;
+        const Buf& ub = bufs_.at(op.out.buffer_id);
+        const bool stored = output_buffers_.count(op.out.buffer_id) || ub.users.size() != 1 ||
+                            reads_as_gemm_operand(op.out.buffer_id);
+        if (!stored) continue;
+        side_[kv.first] = u;
+        fused_skip_.insert(op.out.buffer_id);
+        break;
+      }
+    }
+  }
+
+  // Buffers scheduled op s stores: its (final) output and a side output.
+  std::vector<int> stored_buffers(int s) const {
+    std::vector<int> r = {out_buffer_of(s)};
+    auto it = side_.find(s);
+    if (it != side_.end()) r.push_back(ops_[it->second].out.buffer_id);
+    return r;
+  }
+
   bool is_chain_final(int buffer) const {
     for (const auto& kv : fused_)
       if (kv.second.final_buf == buffer) return true;
@@ -533,7 +580,8 @@ class Planner {
       }
     }
     defer_inplace_epilogues();
-    for (int s : schedule_) writer_[out_buffer_of(s)] = s;
+    for (int s : schedule_)
+      for (int b : stored_buffers(s)) writer_[b] = s;
   }
 
   // Input buffer an in-place output overwrites (-1: not in place).
@@ -552,7 +600,7 @@ class Planner {
     for (size_t i = 0; i < schedule_.size(); ++i) {
       const int f = schedule_[i];
       auto fu = fused_.find(f);
-      if (fu == fused_.end()) continue;
+      if (fu == fused_.end() || side_.count(f)) continue;
       const int target = inplace_target(fu->second.final_buf);
       if (target < 0) continue;
       size_t last = i;
@@ -693,8 +741,8 @@ class Planner {
     std::vector<Slot> active;
     std::vector<Free> free_list;
     int64_t total = 0;
-    for (size_t i = 0; i < schedule_.size(); ++i) {
-      int b = out_buffer_of(schedule_[i]);
+    for (size_t i = 0; i < schedule_.size(); ++i)
+     for (int b : stored_buffers(schedule_[i])) {
       if (binding_.count(b)) continue;
       std::vector<Slot> keep;
       for (const auto& s : active) {
@@ -1124,6 +1172,7 @@ class Planner {
         (ch.fast > tkd::FK_E_ACC_THRESH && ch.fast != tkd::FK_E_UPDATE))
       return -1;
     if (t.out.dtype == TK_F32 || t.out.base % 8 != 0 || t.n % 8 != 0) return -1;
+    if (t.has_side && (t.out2.dtype == TK_F32 || t.out2.base % 8 != 0)) return -1;
     // the last rounding is to the output type (the kernel folds it into the store)
     const int last = ch.n_steps ? ch.steps[ch.n_steps - 1].round : ch.round0;
     if (last != t.out.dtype) return -1;
@@ -1146,6 +1195,10 @@ class Planner {
     if (mask < 0) return 0;
     const int rows = (mask & 1) + ((mask >> 1) & 1);
     const int bcast = t.chain.n_loads - rows;
+    return main_stage_bytes(rows, bcast);
+  }
+
+  static int main_stage_bytes(int rows, int bcast) {
     return (rows ? 2 * rows : 1) * tkd::kEpiBufBytes + bcast * tkd::kBcastBytes;
   }
 
@@ -1314,6 +1367,29 @@ class Planner {
     return true;
   }
 
+  // The side output of fused GEMM mm (if any) as one chain step on the final value.
+  void attach_side(Task& t, const OpInfo& mm) const {
+    auto it = side_.find(mm.index);
+    if (it == side_.end()) return;
+    const OpInfo& op = ops_[it->second];
+    const int fin = fused_.at(mm.index).final_buf;
+    tkd::ChainStep st{};
+    st.round = uint8_t(op.out.dtype);
+    st.ext = tkd::EXT_NONE;
+    // x*c (= c*x), -x, or a cast
+    if (op.kind == TK_OP_MUL) {
+      const bool root_first = !op.in[0].scalar && op.in[0].t.buffer_id == fin;
+      st.op = tkd::OP_MUL;
+      st.ext = tkd::EXT_CONST;
+      st.cval = f32(root_first ? op.in[1].value : op.in[0].value);
+    } else {
+      st.op = op.kind == TK_OP_NEG ? tkd::OP_NEG : tkd::OP_MOV;
+    }
+    t.has_side = 1;
+    t.side = st;
+    t.out2 = out_ref(op.out.buffer_id);
+  }
+
   Task lower_gemm(Plan& plan, const OpInfo& mm) {
     size_t base = mm.kind == TK_OP_ADDMM ? 1 : 0;
     const tk_tensor_spec &A = mm.in[base].t, &B = mm.in[base + 1].t;
@@ -1395,11 +1471,12 @@ class Planner {
           root = ops_[ci].out.buffer_id;
         }
     });
+    attach_side(t, mm);
     if (chained) {
       int out_buf = fused_it != fused_.end() ? fused_it->second.final_buf : mm.out.buffer_id;
       t.out = out_ref(out_buf);
       finish_refs(plan, t);
-    classify_fast(plan, t);
+      classify_fast(plan, t);
       return t;
     }
     Emit e{&plan, this, t.ref_begin, space};
@@ -1591,6 +1668,7 @@ class Planner {
 
   Plan plan_once() {
     fused_.clear();
+    side_.clear();
     fused_skip_.clear();
     inline_.clear();
     schedule_.clear();
@@ -1603,6 +1681,7 @@ class Planner {
 
     detect_epilogues();
     detect_reduction_epilogues();
+    detect_side_outputs();
     choose_inline();
     build_schedule();
     choose_direct_aliases();
@@ -1650,7 +1729,7 @@ class Planner {
       const OpInfo& op = ops_[s];
       std::vector<Region> reads, writes;
       for (const auto& v : reads_of(s)) read_regions(v, reads);
-      writes.push_back(storage_region(out_buffer_of(s)));
+      for (int b : stored_buffers(s)) writes.push_back(storage_region(b));
       if (is_red(op.kind)) {
         std::vector<Task> ts = lower_reduction(plan, op, &scratch);
         for (auto& t : ts) t.op_index = op.index;

@@ -32,7 +32,7 @@ constexpr int kStageBytesB = kMaxTileN * kTileK * 2;    // 32 KB
 // TMA ring, then each epilogue warp's staging buffers.  The planner keeps the
 // total within kDynSmemBudget (the 227 KB per-block limit minus the kernel's
 // static shared memory, with margin).
-constexpr int kDynSmemBudget = 210 * 1024;
+constexpr int kDynSmemBudget = 211 * 1024;
 // Scratch floats for reductions and CUDA-core GEMM tiles; at the start of the
 // dynamic region (in a tensor-core launch it overlays the ring, which is idle
 // outside the tensor-core phase of a stage).
@@ -190,6 +190,11 @@ struct alignas(16) Task {
   Chain post;
   int64_t post_shape[kMaxRank];
   int32_t post_rank;
+  // GEMMs: a side output, one more pointwise op on the stored (rounded) final
+  // value, written to out2 (same shape, contiguous) from the same tile.
+  int32_t has_side;
+  ChainStep side;            // ext is EXT_CONST or EXT_NONE
+  Ref out2;
   // Staged epilogue (compiled GEMM epilogues with 16-bit output): bit s set =
   // load slot s is read per row and copied through shared memory; bit 2 =
   // the staged path is on.  0 = operands and output accessed directly.
@@ -206,9 +211,9 @@ struct Stage {
 
 // A stage whose descriptors fit these bounds is copied into shared memory
 // while the previous grid barrier completes.
-constexpr int kStageTasks = 8;
-constexpr int kStageCode = 128;
-constexpr int kStageRefs = 64;
+constexpr int kStageTasks = 6;
+constexpr int kStageCode = 96;
+constexpr int kStageRefs = 48;
 
 // A byte range the kernel asks L2 to fetch at entry, so that the first reads
 // of program inputs and of the op table in later stages hit L2.  `space` is a

@@ -105,6 +105,7 @@ class MLPConfig:
     loss: str = "mse"      # "mse" (targets y) | "mean_square_residual"
     momentum: float = 0.0  # > 0: SGD with a momentum buffer per parameter
     seed: int = 0
+    master: str | None = None  # e.g. "float32": parameters kept in this type, GEMMs in dtype
 
     @property
     def layers(self) -> int:
@@ -117,13 +118,15 @@ class MLPConfig:
 
     def compulsory_bytes(self) -> int:
         """Parameters read+written, x (+y) read, momentum read+written, loss written."""
-        e = {"float32": 4, "float16": 2, "bfloat16": 2}[self.dtype]
+        sizes = {"float32": 4, "float16": 2, "bfloat16": 2}
+        e = sizes[self.dtype]
+        pe = sizes[self.master or self.dtype]
         params = sum(a * b + b for a, b in zip(self.dims[:-1], self.dims[1:]))
-        total = 2 * params * e + self.batch * self.dims[0] * e + e
+        total = 2 * params * pe + self.batch * self.dims[0] * e + (4 if self.master else e)
         if self.loss == "mse":
             total += self.batch * self.dims[-1] * e
         if self.momentum:
-            total += 2 * params * e
+            total += 2 * params * pe
         return total
 
 
@@ -139,6 +142,10 @@ CONFIGS = {
                     "bfloat16", 32, (128,) * 17, 1e-3, "kaiming_uniform"),
     "c5": MLPConfig("c5", "GEMM-bound bf16 MLP step: batch 4096, 4 layers 4096->4096, ReLU, MSE, SGD lr=1e-4",
                     "bfloat16", 4096, (4096,) * 5, 1e-4, "normal002"),
+    # the mixed-precision method of the pages' harness on the C2 shapes
+    "c2m": MLPConfig("c2m", "mixed-precision MLP step: fp32 master weights, bf16 GEMMs, fp32 loss and SGD; "
+                     "batch 64, 256->512->512->128", "bfloat16", 64, (256, 512, 512, 128), 1e-3,
+                     "kaiming_uniform", master="float32"),
 }
 
 
@@ -160,6 +167,9 @@ def mlp_step_program(cfg: MLPConfig, export: str = "state", dtype: str | None = 
     finite-difference instantiation).
     """
     dt = dtype or cfg.dtype
+    # mixed precision (the pages' harness): parameters, momentum, loss and
+    # updates in the master type; GEMM operands and activations in dt
+    pt = (dtype or cfg.master) if cfg.master else dt
     B, dims, L = cfg.batch, cfg.dims, cfg.layers
     T = TensorSpec.contiguous
     x = T("x", (B, dims[0]), dt)
@@ -170,56 +180,62 @@ def mlp_step_program(cfg: MLPConfig, export: str = "state", dtype: str | None = 
         inputs.append(y)
     W, b, vW, vb = {}, {}, {}, {}
     for i in range(1, L + 1):
-        W[i] = T(f"W{i}", (dims[i], dims[i - 1]), dt)
-        b[i] = T(f"b{i}", (dims[i],), dt)
+        W[i] = T(f"W{i}", (dims[i], dims[i - 1]), pt)
+        b[i] = T(f"b{i}", (dims[i],), pt)
         inputs += [W[i], b[i]]
         if cfg.momentum:
-            vW[i] = T(f"vW{i}", (dims[i], dims[i - 1]), dt)
-            vb[i] = T(f"vb{i}", (dims[i],), dt)
+            vW[i] = T(f"vW{i}", (dims[i], dims[i - 1]), pt)
+            vb[i] = T(f"vb{i}", (dims[i],), pt)
             inputs += [vW[i], vb[i]]
     ops: list[Operation] = []
 
-    def emit(name, op, ins, shape, attrs=None):
-        out = T(name, shape, dt)
+    def emit(name, op, ins, shape, attrs=None, out_dtype=None):
+        out = T(name, shape, out_dtype or dt)
         ops.append(Operation(name, op, tuple(ins), out, dict(attrs or {})))
         return out
+
+    # GEMM copies of the master weights
+    Wc = dict(W)
+    if pt != dt:
+        for i in range(1, L + 1):
+            Wc[i] = emit(f"Wc{i}", "cast", (W[i],), W[i].shape)
 
     # forward: z_i = b_i + a_{i-1} W_i^T ; a_i = relu(z_i) between layers
     a = {0: x}
     for i in range(1, L + 1):
-        z = emit(f"z{i}", "addmm", (b[i], a[i - 1], W[i].T), (B, dims[i]))
+        z = emit(f"z{i}", "addmm", (b[i], a[i - 1], Wc[i].T), (B, dims[i]))
         a[i] = emit(f"a{i}", "relu", (z,), (B, dims[i])) if i < L else z
     out = a[L]
     n_out = B * dims[-1]
     if cfg.loss == "mse":
-        d = emit("d", "sub", (out, y), (B, dims[-1]))
-        sq = emit("sq", "pow", (d, 2), (B, dims[-1]))
-        loss = emit("loss", "mean", (sq,), ())
+        d = emit("d", "sub", (out, y), (B, dims[-1]), out_dtype=pt)
+        sq = emit("sq", "pow", (d, 2), (B, dims[-1]), out_dtype=pt)
+        loss = emit("loss", "mean", (sq,), (), out_dtype=pt)
         g = emit(f"g{L}", "mul", (d, 2.0 / n_out if n_out else 0.0), (B, dims[-1]))
     elif cfg.loss == "mean_square_residual":
-        r = emit("out", "add", (out, x), (B, dims[-1]))
-        sq = emit("sq", "pow", (r, 2), (B, dims[-1]))
-        loss = emit("loss", "mean", (sq,), ())
+        r = emit("out", "add", (out, x), (B, dims[-1]), out_dtype=pt)
+        sq = emit("sq", "pow", (r, 2), (B, dims[-1]), out_dtype=pt)
+        loss = emit("loss", "mean", (sq,), (), out_dtype=pt)
         g = emit(f"g{L}", "mul", (r, 2.0 / n_out if n_out else 0.0), (B, dims[-1]))
     else:
         raise ValueError(cfg.loss)
 
     grads_w, grads_b, new_state = {}, {}, []
     for i in range(L, 0, -1):
-        grads_w[i] = emit(f"gW{i}", "mm", (g.T, a[i - 1]), (dims[i], dims[i - 1]))
-        grads_b[i] = emit(f"gb{i}", "sum", (g,), (dims[i],), {"dims": (0,)})
+        grads_w[i] = emit(f"gW{i}", "mm", (g.T, a[i - 1]), (dims[i], dims[i - 1]), out_dtype=pt)
+        grads_b[i] = emit(f"gb{i}", "sum", (g,), (dims[i],), {"dims": (0,)}, out_dtype=pt)
         if i > 1:
-            ga = emit(f"ga{i - 1}", "mm", (g, W[i]), (B, dims[i - 1]))
+            ga = emit(f"ga{i - 1}", "mm", (g, Wc[i]), (B, dims[i - 1]))
             g_prev = emit(f"g{i - 1}", "threshold_backward", (ga, a[i - 1]), (B, dims[i - 1]),
                           {"threshold": 0.0})
         for p, gp, v, tag in ((W[i], grads_w[i], vW.get(i), "W"), (b[i], grads_b[i], vb.get(i), "b")):
             if cfg.momentum:
-                mv = emit(f"m{tag}{i}", "mul", (v, cfg.momentum), v.shape)
-                v_new = emit(f"v{tag}{i}_new", "add", (mv, gp), v.shape)
-                p_new = emit(f"{tag}{i}_new", "sub", (p, v_new), p.shape, {"alpha": cfg.lr})
+                mv = emit(f"m{tag}{i}", "mul", (v, cfg.momentum), v.shape, out_dtype=pt)
+                v_new = emit(f"v{tag}{i}_new", "add", (mv, gp), v.shape, out_dtype=pt)
+                p_new = emit(f"{tag}{i}_new", "sub", (p, v_new), p.shape, {"alpha": cfg.lr}, out_dtype=pt)
                 new_state += [(p_new, p), (v_new, v)]
             else:
-                p_new = emit(f"{tag}{i}_new", "sub", (p, gp), p.shape, {"alpha": cfg.lr})
+                p_new = emit(f"{tag}{i}_new", "sub", (p, gp), p.shape, {"alpha": cfg.lr}, out_dtype=pt)
                 new_state.append((p_new, p))
         if i > 1:
             g = g_prev

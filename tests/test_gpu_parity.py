@@ -98,6 +98,8 @@ SMALL = {
     "ragged_f32": S.scaled(S.CONFIGS["c1"], batch=3, dims=(13, 7, 5)),
     "ragged_bf16": S.scaled(S.CONFIGS["c2"], batch=5, dims=(37, 19, 11)),
     "ragged_f16_mom": S.scaled(S.CONFIGS["c3"], batch=9, dims=(24, 40, 24)),
+    "c2m": S.CONFIGS["c2m"],
+    "ragged_mixed_mom": S.scaled(S.CONFIGS["c2m"], batch=5, dims=(37, 19, 11), momentum=0.9),
 }
 
 
@@ -153,7 +155,7 @@ def test_results_do_not_depend_on_grid_size(key):
             np.testing.assert_array_equal(x, y)
 
 
-@pytest.mark.parametrize("key", ["c1", "c2", "c3s", "c4", "ragged_f32", "ragged_f16_mom"])
+@pytest.mark.parametrize("key", ["c1", "c2", "c3s", "c4", "ragged_f32", "ragged_f16_mom", "c2m", "ragged_mixed_mom"])
 def test_whole_step_tracks_oracle(key):
     cfg = SMALL[key]
     prog = S.mlp_step_program(cfg, export="grads")
@@ -170,7 +172,11 @@ def test_whole_step_tracks_oracle(key):
     # test_each_op_matches_oracle_teacher_forced.
     assert abs(gpu[0] - want[0]) <= 2e-2 * abs(want[0]) + 1e-6      # loss
     for slot, idx in prog.inplace.items():                            # updated state
-        u = ulp_distance(gpu[slot], want[slot], dt)
+        sdt = prog.outputs[slot].dtype
+        if sdt == "float32":  # mixed precision: fp32 master state, lr times a bf16-path gradient
+            np.testing.assert_allclose(gpu[slot], want[slot], rtol=1e-5, atol=1e-6, err_msg=prog.outputs[slot].buffer)
+            continue
+        u = ulp_distance(gpu[slot], want[slot], sdt)
         assert (u <= 2).mean() >= 0.99 and u.max() <= 64, (prog.outputs[slot].buffer, (u <= 2).mean(), u.max())
 
 
@@ -273,6 +279,29 @@ def test_mixed_pointwise_and_reduction_program(fuse):
             assert ulp_distance(g, w, s.dtype).max() <= 2, s.buffer
         else:
             assert ulp_distance(g, w, s.dtype).max() == 0, s.buffer
+
+
+def test_general_pow_and_middle_dim_reductions():
+    # powf stays in the instruction form; rank-3 reductions over a middle dim
+    # and over two dims go through the index permutation of the row/column paths
+    T = TensorSpec.contiguous
+    x = T("x", (4, 6, 40), "float32")
+    ops = [Operation("a", "pow", (x, 3.0), T("a", (4, 6, 40), "float32")),
+           Operation("b", "pow", (T("a", (4, 6, 40), "float32"), 1.0 / 3.0), T("b", (4, 6, 40), "bfloat16")),
+           Operation("m", "sum", (T("a", (4, 6, 40), "float32"),), T("m", (4, 40), "float32"), {"dims": (1,)}),
+           Operation("n", "mean", (x,), T("n", (6,), "float32"), {"dims": (0, 2)}),
+           Operation("o", "sum", (T("b", (4, 6, 40), "bfloat16"),), T("o", (4, 6), "bfloat16"), {"dims": (-1,)})]
+    prog = Program([x], [T("b", (4, 6, 40), "bfloat16"), T("m", (4, 40), "float32"), T("n", (6,), "float32"),
+                         T("o", (4, 6), "bfloat16")], ops)
+    arrays = [S.to_storage(np.abs(S.normal(S.stream_seed(5, 0), 960)) + 0.1, "float32").reshape(4, 6, 40)]
+    want = oracle.run_program(prog, values(arrays, prog))
+    for fuse in (0, 1):
+        gpu, _ = run_step(prog, arrays, fuse_pointwise=fuse)
+        # CUDA powf is within 2 ulp of float32 (not correctly rounded): 1 ulp of bf16
+        assert ulp_distance(gpu[0], want[0], "bfloat16").max() <= 1
+        np.testing.assert_allclose(gpu[1], want[1], rtol=1e-5)
+        np.testing.assert_allclose(gpu[2], want[2], rtol=1e-5)
+        assert ulp_distance(gpu[3], want[3], "bfloat16").max() <= 2
 
 
 def test_barrier_timeout_is_reported_and_recoverable():

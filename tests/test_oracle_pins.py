@@ -188,6 +188,16 @@ def test_pointwise_semantics_special_cases():
     np.testing.assert_array_equal(d, gv / 4)
     p = _run_single("pow", (g, 2), T("p", (6,), "float32"), {"g": gv})
     np.testing.assert_array_equal(p, gv ** 2)
+    # general exponents: exact cases of the real power function
+    p = _run_single("pow", (g, 3), T("p", (6,), "float32"), {"g": gv})
+    np.testing.assert_array_equal(p, gv ** 3)
+    sq = np.array([1.0, 4.0, 9.0, 16.0, 0.25, 2.0 ** 20])
+    p = _run_single("pow", (g, 0.5), T("p", (6,), "float32"), {"g": sq})
+    np.testing.assert_array_equal(p, np.sqrt(sq))
+    p = _run_single("pow", (g, -1), T("p", (6,), "float32"), {"g": np.array([1.0, 2.0, 4.0, 0.5, -8.0, 1024.0])})
+    np.testing.assert_array_equal(p, [1.0, 0.5, 0.25, 2.0, -0.125, 2.0 ** -10])
+    p = _run_single("pow", (g, 0), T("p", (6,), "float32"), {"g": np.array([0.0, -3.0, 7.5, 1e30, -0.0, 2.0])})
+    np.testing.assert_array_equal(p, np.ones(6))
     n = _run_single("neg", (g,), T("n", (6,), "float32"), {"g": gv})
     np.testing.assert_array_equal(n, -gv)
     f = _run_single("full", (), T("f", (2, 3), "bfloat16"), {}, {"value": 1 + 2 ** -8})

@@ -1706,10 +1706,41 @@ class Planner {
     std::vector<Region> stage_reads, stage_writes;
     int64_t scratch = 0;
     int split = 0;
+    // Final passes of split reductions wait here and join the next stage
+    // that starts for any reason (or the one a reader of their result forces),
+    // instead of forcing a barrier right after their partial sums.
+    struct Pending {
+      Task f;
+      size_t pos;
+      std::vector<Region> reads, writes;
+    };
+    std::vector<Pending> pending;
     auto barrier = [&]() {
       stages.emplace_back();
       stage_reads.clear();
       stage_writes.clear();
+      for (auto& p : pending) {
+        stages.back().push_back(p.f);
+        stage_of_[p.pos] = int(stages.size()) - 1;
+        if (p.f.post.valid) stage_reads.insert(stage_reads.end(), p.reads.begin(), p.reads.end());
+        stage_writes.insert(stage_writes.end(), p.writes.begin(), p.writes.end());
+      }
+      pending.clear();
+    };
+    auto conflicts_pending = [&](const std::vector<Region>& reads, const std::vector<Region>& writes) {
+      for (const auto& p : pending) {
+        for (const auto& w : p.writes) {
+          for (const auto& r : reads)
+            if (overlap(w, r)) return true;
+          for (const auto& r : writes)
+            if (overlap(w, r)) return true;
+        }
+        if (p.f.post.valid)
+          for (const auto& r : p.reads)
+            for (const auto& w : writes)
+              if (overlap(r, w)) return true;
+      }
+      return false;
     };
     auto hazard = [&](const std::vector<Region>& reads, const std::vector<Region>& writes) {
       for (const auto& w : stage_writes) {
@@ -1735,31 +1766,32 @@ class Planner {
         for (auto& t : ts) t.op_index = op.index;
         if (ts.size() == 2) {
           ++split;
-          if (hazard(reads, {})) barrier();
+          if (conflicts_pending(reads, {})) barrier();
+          while (hazard(reads, {})) barrier();
           stages.back().push_back(ts[0]);
           stage_reads.insert(stage_reads.end(), reads.begin(), reads.end());
-          barrier();
-          stages.back().push_back(ts[1]);
-          // the final pass reads a reduction epilogue's operands
-          if (ts[1].post.valid) stage_reads.insert(stage_reads.end(), reads.begin(), reads.end());
-          stage_writes.insert(stage_writes.end(), writes.begin(), writes.end());
-          stage_of_[pos] = int(stages.size()) - 1;
+          // the final pass also reads a reduction epilogue's operands
+          pending.push_back({ts[1], pos, reads, writes});
           continue;
         }
-        if (hazard(reads, writes)) barrier();
+        if (conflicts_pending(reads, writes)) barrier();
+        while (hazard(reads, writes)) barrier();
         stages.back().push_back(ts[0]);
       } else {
         Task t = is_mm(op.kind) ? lower_gemm(plan, op)
                                 : lower_pointwise(plan, &op, nullptr, shape_of(op.out), out_ref(op.out.buffer_id),
                                                   op.out.dtype);
         t.op_index = op.index;
-        if (hazard(reads, writes)) barrier();
+        if (conflicts_pending(reads, writes)) barrier();
+        while (hazard(reads, writes)) barrier();
         stages.back().push_back(t);
       }
       stage_of_[pos] = int(stages.size()) - 1;
       stage_reads.insert(stage_reads.end(), reads.begin(), reads.end());
       stage_writes.insert(stage_writes.end(), writes.begin(), writes.end());
     }
+
+    if (!pending.empty()) barrier();
 
     // End-of-kernel output copies, then transactional commits of in-place outputs.
     int copies = 0;

@@ -486,6 +486,11 @@ __device__ __forceinline__ void chain_compute(const Chain& ch, const float (&L)[
 #pragma unroll
       for (int j = 0; j < V; ++j) e[j] = st.cval;
     }
+    if (st.ext_mul) {  // an inlined c * input
+#pragma unroll
+      for (int j = 0; j < V; ++j) e[j] = __fmul_rn(e[j], st.cval);
+      round_vec<V>(e, st.ext_round);
+    }
     if (st.second) {  // running value is the second operand: swap roles
 #pragma unroll
       for (int j = 0; j < V; ++j) {
@@ -564,6 +569,7 @@ struct Fast {
   int32_t r0, r1, r2; // rounding: start value, step 0, step 1
   float a0, a1, c0;   // step 0 / step 1 alpha or threshold; step 0 constant
   int32_t sub0, sub1; // the add/sub step subtracts
+  int32_t er;         // rounding of a scaled operand (momentum)
   char* out;
   int32_t out_dt;
 };
@@ -597,6 +603,7 @@ __device__ __forceinline__ Fast fast_params(const Ctx& c, const Task& t) {
   F.c0 = ch.steps[0].cval;
   F.sub0 = ch.steps[0].op == OP_SUB;
   F.sub1 = ch.steps[1].op == OP_SUB;
+  F.er = ch.steps[0].ext_round;
   F.out = space_ptr(c, t.out.space, t.out.slot) + t.out.base * esize_of(t.out.dtype);
   F.out_dt = t.out.dtype;
   return F;
@@ -616,7 +623,20 @@ struct FastTraits {
 template <int K, bool kLast = true>
 __device__ __forceinline__ void fast_apply(const Fast& F, const float (&l0)[8], const float (&l1)[8],
                                            const float (&acc)[8], float (&x)[8]) {
-  if constexpr (K == FK_E_UPDATE) {
+  if constexpr (K == FK_E_MOMENTUM) {
+    // v' = round(round(v * mu) + a * round(acc))
+    float m[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      x[j] = acc[j];
+      m[j] = __fmul_rn(l0[j], F.c0);
+    }
+    round_vec<8>(x, F.r0);
+    round_vec<8>(m, F.er);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = __fadd_rn(m[j], __fmul_rn(F.a0, x[j]));
+    if constexpr (kLast) round_vec<8>(x, F.r1);
+  } else if constexpr (K == FK_E_UPDATE) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) x[j] = acc[j];
     round_vec<8>(x, F.r0);
@@ -1612,6 +1632,7 @@ __device__ __noinline__ bool tc_epilogue_staged_any(const Ctx c, const Task& t, 
     case FK_E_BIAS_RELU: return tc_epilogue_staged<FK_E_BIAS_RELU>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp);
     case FK_E_BIAS_AXPY: return tc_epilogue_staged<FK_E_BIAS_AXPY>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp);
     case FK_E_ACC_THRESH: return tc_epilogue_staged<FK_E_ACC_THRESH>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp);
+    case FK_E_MOMENTUM: return tc_epilogue_staged<FK_E_MOMENTUM>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp);
     default: return tc_epilogue_staged<FK_E_UPDATE>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp);
   }
 }
@@ -1664,6 +1685,7 @@ __device__ __forceinline__ void tc_epilogue_tile(const Ctx& c, const Task& t, in
     case FK_E_BIAS_AXPY: tc_epilogue_fast<FK_E_BIAS_AXPY>(c, t, m0, n0, taddr); return;
     case FK_E_ACC_THRESH: tc_epilogue_fast<FK_E_ACC_THRESH>(c, t, m0, n0, taddr); return;
     case FK_E_UPDATE: tc_epilogue_fast<FK_E_UPDATE>(c, t, m0, n0, taddr); return;
+    case FK_E_MOMENTUM: tc_epilogue_fast<FK_E_MOMENTUM>(c, t, m0, n0, taddr); return;
     default: break;
   }
   if (t.vec == 8 && t.chain.valid)

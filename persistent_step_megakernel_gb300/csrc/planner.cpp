@@ -434,7 +434,7 @@ class Planner {
           if (o.scalar || chain_bufs.count(o.t.buffer_id)) continue;
           if (!exact_contig(o.t)) safe = false;
           int p = bufs_[o.t.buffer_id].producer;
-          if (p >= 0 && p >= mm.index) safe = false;
+          if (p >= 0 && p >= mm.index && !scaled_input(o.t.buffer_id)) safe = false;
         }
       if (!safe) continue;
       Fused f;
@@ -473,8 +473,8 @@ class Planner {
             continue;
           }
           const Buf& b = bufs_.at(o.t.buffer_id);
-          const bool materialised = b.input >= 0 || (b.producer >= 0 && !is_pointwise(ops_[b.producer].kind) &&
-                                                     b.producer < r.index);
+          const bool materialised = b.input >= 0 || scaled_input(o.t.buffer_id) ||
+                                    (b.producer >= 0 && !is_pointwise(ops_[b.producer].kind) && b.producer < r.index);
           if (!materialised || shape_of(o.t) != bufs_[current].shape || !exact_contig(o.t)) ok = false;
           ++loads;
         }
@@ -539,6 +539,18 @@ class Planner {
     auto it = side_.find(s);
     if (it != side_.end()) r.push_back(ops_[it->second].out.buffer_id);
     return r;
+  }
+
+  // A single-use value c * (contiguous view of a program input): evaluated
+  // inside whatever consumes it, so it may be produced after a GEMM whose
+  // epilogue reads it (the momentum term mul(v, 0.9)).
+  bool scaled_input(int buffer) const {
+    const Buf& b = bufs_.at(buffer);
+    if (b.producer < 0 || b.users.size() != 1 || output_buffers_.count(buffer) || !opt_.fuse_pointwise) return false;
+    const OpInfo& op = ops_[b.producer];
+    if (op.kind != TK_OP_MUL || op.in.size() != 2 || op.in[0].scalar == op.in[1].scalar) return false;
+    const Operand& v = op.in[0].scalar ? op.in[1] : op.in[0];
+    return bufs_.at(v.t.buffer_id).input >= 0 && exact_contig(v.t) && shape_of(v.t) == b.shape;
   }
 
   bool is_chain_final(int buffer) const {
@@ -1065,7 +1077,18 @@ class Planner {
           break;
       }
       const Operand &o0 = op.in[0], &o1 = op.in[1];
-      const bool t0 = is_tree(o0), t1 = is_tree(o1);
+      bool t0 = is_tree(o0), t1 = is_tree(o1);
+      // an inlined c * input next to the running value is loaded and scaled
+      const OpInfo* scaled = nullptr;
+      if (t0 && t1 && root_buf >= 0) {
+        const int oi = o0.t.buffer_id == root_buf ? 1 : o1.t.buffer_id == root_buf ? 0 : -1;
+        const Operand& other = oi == 1 ? o1 : o0;
+        if (oi >= 0 && P->inline_.count(other.t.buffer_id) && P->scaled_input(other.t.buffer_id) &&
+            shape_of(other.t) == P->bufs_.at(other.t.buffer_id).shape && exact_contig(other.t)) {
+          scaled = &P->ops_[P->bufs_.at(other.t.buffer_id).producer];
+          (oi == 1 ? t1 : t0) = false;
+        }
+      }
       if (t0 && t1) {
         fail = true;
         return;
@@ -1076,9 +1099,17 @@ class Planner {
       unary_spine(sp);
       int ext;
       float cval = 0.f;
+      uint8_t ext_mul = 0, ext_round = 0;
       if (other.scalar) {
         ext = tkd::EXT_CONST;
         cval = f32(other.value);
+      } else if (scaled) {
+        const Operand& v = scaled->in[0].scalar ? scaled->in[1] : scaled->in[0];
+        const double c = scaled->in[0].scalar ? scaled->in[0].value : scaled->in[1].value;
+        ext = load_slot(v.t, operand_map(op, other, outmap)) == 0 ? tkd::EXT_LOAD0 : tkd::EXT_LOAD1;
+        cval = f32(c);
+        ext_mul = 1;
+        ext_round = uint8_t(scaled->out.dtype);
       } else {
         ext = load_slot(other.t, operand_map(op, other, outmap)) == 0 ? tkd::EXT_LOAD0 : tkd::EXT_LOAD1;
       }
@@ -1091,6 +1122,10 @@ class Planner {
                         : op.kind == TK_OP_THRESHOLD_BACKWARD        ? f32(op.threshold)
                                                                      : 0.f;
       step(code, rd, ext, side, imm, cval);
+      if (!fail) {
+        ch.steps[ch.n_steps - 1].ext_mul = ext_mul;
+        ch.steps[ch.n_steps - 1].ext_round = ext_round;
+      }
     }
   };
 
@@ -1169,7 +1204,7 @@ class Planner {
   int epi_stage_mask(const Plan& plan, const Task& t) const {
     const tkd::Chain& ch = t.chain;
     if (t.kind != tkd::T_GEMM_TC || !ch.valid || ch.fast < tkd::FK_E_ACC ||
-        (ch.fast > tkd::FK_E_ACC_THRESH && ch.fast != tkd::FK_E_UPDATE))
+        (ch.fast > tkd::FK_E_ACC_THRESH && ch.fast != tkd::FK_E_UPDATE && ch.fast != tkd::FK_E_MOMENTUM))
       return -1;
     if (t.out.dtype == TK_F32 || t.out.base % 8 != 0 || t.n % 8 != 0) return -1;
     if (t.has_side && (t.out2.dtype == TK_F32 || t.out2.base % 8 != 0)) return -1;
@@ -1221,8 +1256,10 @@ class Planner {
     };
     const tkd::ChainStep& s0 = ch.steps[0];
     const tkd::ChainStep& s1 = ch.steps[1];
+    for (int i = 0; i < ch.n_steps; ++i)
+      if (ch.steps[i].ext_mul && !(t.kind == tkd::T_GEMM_TC && i == 0)) return;
     auto axpy = [](const tkd::ChainStep& st, int ext) {
-      return (st.op == tkd::OP_ADD || st.op == tkd::OP_SUB) && st.ext == ext && !st.second;
+      return (st.op == tkd::OP_ADD || st.op == tkd::OP_SUB) && st.ext == ext && !st.second && !st.ext_mul;
     };
     if (t.kind == tkd::T_GEMM_TC) {
       if (ch.start != tkd::CH_ACC) return;
@@ -1233,7 +1270,11 @@ class Planner {
           ch.fast = tkd::FK_E_ACC_THRESH;
         if (ch.n_steps == 1 && ch.n_loads == 1 && (s0.op == tkd::OP_ADD || s0.op == tkd::OP_SUB) &&
             s0.ext == tkd::EXT_LOAD0 && s0.second && contig(0))
-          ch.fast = tkd::FK_E_UPDATE;
+          ch.fast = s0.ext_mul ? (s0.op == tkd::OP_ADD ? tkd::FK_E_MOMENTUM : tkd::FK_NONE) : tkd::FK_E_UPDATE;
+      }
+      for (int i = 0; i < ch.n_steps; ++i)
+        if (ch.steps[i].ext_mul && ch.fast != tkd::FK_E_MOMENTUM) ch.fast = tkd::FK_NONE;
+      if (ch.addmm_mode == tkd::AM_ACC && ch.bias == -1) {
       } else if (ch.addmm_mode == tkd::AM_SUM && ch.bias == 0 && contig(0)) {
         if (ch.n_steps == 0 && ch.n_loads == 1) ch.fast = tkd::FK_E_BIAS;
         if (ch.n_steps == 1 && ch.n_loads == 1 && s0.op == tkd::OP_RELU) ch.fast = tkd::FK_E_BIAS_RELU;
@@ -1652,7 +1693,7 @@ class Planner {
     // p -/+ a*round(v) with p contiguous over the outputs: the compiled update
     const tkd::ChainStep& s0 = cb.ch.steps[0];
     if (opt_.expr_forms == 0 && cb.ch.n_steps == 1 && cb.ch.n_loads == 1 && s0.ext == tkd::EXT_LOAD0 && s0.second &&
-        (s0.op == tkd::OP_ADD || s0.op == tkd::OP_SUB)) {
+        !s0.ext_mul && (s0.op == tkd::OP_ADD || s0.op == tkd::OP_SUB)) {
       const Ref& r = plan.refs[t.ref_begin + cb.ch.load_ref[0]];
       bool flat = true;
       Shape cs = contig(out_shape);

@@ -102,8 +102,11 @@ struct ChainStep {
   uint8_t round;    // tk_dtype of the result
   uint8_t ext;      // ChainExt
   uint8_t second;   // 1: the running value is the op's second operand
+  uint8_t ext_mul;  // 1: a loaded operand is first scaled: round(load * cval, ext_round)
+  uint8_t ext_round;
+  uint8_t pad[2];
   float imm;        // alpha (add/sub), threshold, exponent
-  float cval;       // constant operand (EXT_CONST)
+  float cval;       // constant operand (EXT_CONST), or the scale of a loaded one
 };
 
 // Chains of these shapes run as compiled loops with their parameters hoisted
@@ -123,7 +126,8 @@ enum FastKind : int32_t {
   FK_L_SCALE = 9,        // round(l0 * c)
   FK_L_AXPY = 10,        // round(l0 +/- a*l1)
   FK_L_SCALE_AXPY = 11,  // round(round(l0 * c) +/- a*l1)
-  FK_E_UPDATE = 12       // round(l0 +/- a*round(acc))   (SGD step in a weight-gradient epilogue)
+  FK_E_UPDATE = 12,      // round(l0 +/- a*round(acc))   (SGD step in a weight-gradient epilogue)
+  FK_E_MOMENTUM = 13     // round(round(l0*c) + a*round(acc))   (momentum buffer update)
 };
 
 struct Chain {

@@ -52,7 +52,7 @@ def test_static_workspace_matches_caller_workspace_on_two_calls(key):
 
 
 def test_static_workspace_rejects_programs_that_do_not_fit():
-    cfg = S.CONFIGS["c3"]                       # needs ~13.6 MB of workspace
+    cfg = S.scaled(S.CONFIGS["c3"], batch=1024)  # needs ~21 MB of workspace
     prog = S.mlp_step_program(cfg, export="state")
     step = TrainStep(prog, 0)
     assert step.workspace_elements > B.STATIC_WORKSPACE_ELEMENTS

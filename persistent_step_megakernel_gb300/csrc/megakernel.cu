@@ -910,6 +910,36 @@ __device__ __noinline__ void pointwise_vm(const Ctx c, const Task& t, int item) 
 
 // A FastKind pointwise item: operands and output at the flat index, all U
 // vectors' loads issued before the first store.
+// Operands and output all 16-bit: raw 16-byte vectors, twice as many in flight.
+template <int K>
+__device__ __noinline__ void pointwise_fast16(const Ctx c, const Task& t, int item) {
+  constexpr int U = kPointwiseUnroll16;
+  constexpr int64_t step = int64_t(kThreads) * 8;
+  const int64_t base = int64_t(item) * kThreads * 8 * U + int64_t(threadIdx.x) * 8;
+  const int64_t numel = t.numel;
+  const Fast F = fast_params(c, t);
+  uint4 q0[U], q1[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int64_t i = base + u * step;
+    if (i < numel) {
+      q0[u] = *reinterpret_cast<const uint4*>(F.p0 + i * 2);
+      if constexpr (FastTraits<K>::load1) q1[u] = *reinterpret_cast<const uint4*>(F.p1 + i * 2);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int64_t i = base + u * step;
+    if (i < numel) {
+      float l0[8], l1[8], none[8], x[8];
+      unpack8(q0[u], F.dt0, l0);
+      if constexpr (FastTraits<K>::load1) unpack8(q1[u], F.dt1, l1);
+      fast_apply<K>(F, l0, l1, none, x);
+      *reinterpret_cast<uint4*>(F.out + i * 2) = pack8(x, F.out_dt);
+    }
+  }
+}
+
 template <int K>
 __device__ __noinline__ void pointwise_fast(const Ctx c, const Task& t, int item) {
   constexpr int U = kPointwiseUnroll;
@@ -940,12 +970,21 @@ __device__ __noinline__ void pointwise_fast(const Ctx c, const Task& t, int item
 template <int V>
 __device__ __forceinline__ void run_pointwise(const Ctx& c, const Task& t, int item) {
   if constexpr (V == 8) {
-#define TK_CALL(k) pointwise_fast<k>(c, t, item)
-    switch (t.chain.fast) {
-      TK_FAST_L_CASES(TK_CALL)
-      default: break;
-    }
+    if (t.pw_unroll == kPointwiseUnroll16) {
+#define TK_CALL(k) pointwise_fast16<k>(c, t, item)
+      switch (t.chain.fast) {
+        TK_FAST_L_CASES(TK_CALL)
+        default: break;
+      }
 #undef TK_CALL
+    } else {
+#define TK_CALL(k) pointwise_fast<k>(c, t, item)
+      switch (t.chain.fast) {
+        TK_FAST_L_CASES(TK_CALL)
+        default: break;
+      }
+#undef TK_CALL
+    }
     if (t.chain.fast != FK_NONE) return;
   }
   if (t.chain.valid)

@@ -1298,8 +1298,19 @@ class Planner {
 
   static Shape contig_strides_of(const Shape& sh) { return contig(sh); }
 
+  // Compiled loops whose operands and output are all 16-bit keep twice as
+  // many loads in flight (their raw 16-byte vectors fit in registers).
+  int pointwise_unroll(const Plan& plan, const Task& t) const {
+    if (t.vec != 8) return 1;
+    if (t.chain.fast < tkd::FK_L || t.chain.fast > tkd::FK_L_SCALE_AXPY || t.out.dtype == TK_F32)
+      return tkd::kPointwiseUnroll;
+    for (int i = 0; i < t.chain.n_loads; ++i)
+      if (plan.refs[t.ref_begin + t.chain.load_ref[i]].dtype == TK_F32) return tkd::kPointwiseUnroll;
+    return tkd::kPointwiseUnroll16;
+  }
+
   int items_pointwise(const Task& t) const {
-    const int64_t per = int64_t(tkd::kThreads) * t.vec * (t.vec == 8 ? tkd::kPointwiseUnroll : 1);
+    const int64_t per = int64_t(tkd::kThreads) * t.vec * std::max(1, t.pw_unroll);
     return int(ceil_div(t.numel, per));
   }
 
@@ -1331,6 +1342,7 @@ class Planner {
     t.out = out;
     finish_refs(plan, t);
     classify_fast(plan, t);
+    t.pw_unroll = pointwise_unroll(plan, t);
     t.n_items = items_pointwise(t);
     return t;
   }

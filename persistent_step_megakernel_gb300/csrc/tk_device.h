@@ -16,6 +16,7 @@ constexpr int kThreads = 256;      // threads per block (8 warps)
 constexpr int kMaxRank = 4;
 constexpr int kVmRegs = 4;         // expression registers per element
 constexpr int kPointwiseUnroll = 4; // 8-element vectors per thread in a pointwise item
+constexpr int kPointwiseUnroll16 = 8; // the same for compiled loops over 16-bit values only
 constexpr int kHeaderUnits = 64;   // workspace header: 64 floats = 256 bytes
 constexpr int kMaxIO = 256;        // program inputs (and outputs) per launch
 
@@ -203,6 +204,7 @@ struct alignas(16) Task {
   // load slot s is read per row and copied through shared memory; bit 2 =
   // the staged path is on.  0 = operands and output accessed directly.
   int32_t epi_stage;
+  int32_t pw_unroll;         // pointwise items: vectors per thread (kPointwiseUnroll or kPointwiseUnroll16)
 };
 
 struct Stage {

@@ -138,6 +138,8 @@ typedef struct {
                                   loops of fixed shapes, else generic chains, else instructions;
                                   default), 1 no compiled loops, 2 instructions only.  All give
                                   bit-identical results; 1 and 2 exist for testing. */
+  int32_t split_k;             /* 1: split the K loop of under-filled tensor-core GEMMs over more
+                                  SMs (partial sums, then a pass that adds them; default 1) */
 } tk_options;
 
 /* What the planner decided (codegen.py `GeneratedKernel` counters). */
@@ -168,7 +170,7 @@ typedef struct {
 typedef struct {
   int32_t stage;               /* barrier-separated stage the task runs in */
   int32_t kind;                /* 0 pointwise, 1 row reduction, 2 column reduction, 3 partials sum,
-                                  4 CUDA-core GEMM, 5 tensor-core GEMM */
+                                  4 CUDA-core GEMM, 5 tensor-core GEMM, 6 split-K sum + epilogue */
   int32_t op_index;            /* index into tk_program_desc.ops; -1 for an output copy or commit */
   int32_t n_items;             /* work items (GEMM tiles, element blocks, reduction outputs x parts) */
   int32_t form;                /* expression evaluator: 0 instructions, 1 generic chain, 2 compiled loop */

@@ -52,7 +52,8 @@ class tk_options(ctypes.Structure):
                 ("fuse_pointwise", ctypes.c_int32), ("fuse_epilogues", ctypes.c_int32),
                 ("inline_input_casts", ctypes.c_int32), ("tensor_cores", ctypes.c_int32),
                 ("sm_count", ctypes.c_int32), ("profile", ctypes.c_int32),
-                ("barrier_timeout_s", ctypes.c_double), ("expr_forms", ctypes.c_int32)]
+                ("barrier_timeout_s", ctypes.c_double), ("expr_forms", ctypes.c_int32),
+                ("split_k", ctypes.c_int32)]
 
 
 class tk_plan_stats(ctypes.Structure):
@@ -259,7 +260,7 @@ def tk_plan_stats_get(handle) -> dict:
     return {name: getattr(s, name) for name, _ in tk_plan_stats._fields_}
 
 
-TASK_KINDS = ("pointwise", "reduce_row", "reduce_col", "reduce_final", "gemm_simt", "gemm_tc")
+TASK_KINDS = ("pointwise", "reduce_row", "reduce_col", "reduce_final", "gemm_simt", "gemm_tc", "splitk_final")
 EXPR_FORMS = ("instructions", "chain", "compiled")
 
 

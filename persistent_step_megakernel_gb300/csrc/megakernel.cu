@@ -1403,8 +1403,14 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])::"memory");
 }
 
-// Walk this block's tensor-core tiles of a stage in order (all roles use the
-// same sequence).  fn(task, m0, n0) returns false to stop.
+// One tensor-core work item: a tile and, for split-K, its range of k blocks.
+struct TileItem {
+  int64_t m0, n0;
+  int kb0, kb1, split;
+};
+
+// Walk this block's tensor-core items of a stage in order (all roles use the
+// same sequence).  fn(task, item) returns false to stop.
 template <typename F>
 __device__ __forceinline__ void for_my_tiles(const Ctx& c, const Stage& st, F&& fn) {
   int ti = st.task_begin, base = 0;
@@ -1414,8 +1420,14 @@ __device__ __forceinline__ void for_my_tiles(const Ctx& c, const Stage& st, F&& 
       ++ti;
     }
     const Task& t = c.tasks[ti];
-    const int item = g - base;
-    if (!fn(t, int64_t(item / t.tiles_n) * kTileM, int64_t(item % t.tiles_n) * t.tile_n)) return;
+    const int item = g - base, tile = item / t.k_splits, split = item - tile * t.k_splits;
+    TileItem it;
+    it.m0 = int64_t(tile / t.tiles_n) * kTileM;
+    it.n0 = int64_t(tile % t.tiles_n) * t.tile_n;
+    it.split = split;
+    it.kb0 = split * t.kb_split;
+    it.kb1 = min(t.k_blocks, it.kb0 + t.kb_split);
+    if (!fn(t, it)) return;
   }
 }
 
@@ -1676,6 +1688,52 @@ __device__ __noinline__ bool tc_epilogue_staged_any(const Ctx c, const Task& t, 
   }
 }
 
+// Split-K: this split's float32 accumulator, as is, to its scratch plane.
+__device__ __noinline__ void tc_epilogue_partial(const Ctx c, const Task& t, int64_t m0, int64_t n0, int split,
+                                                 uint32_t taddr) {
+  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
+  const int64_t row = m0 + q * 32 + lane, M = t.m, N = t.n;
+  float* plane = reinterpret_cast<float*>(c.ws) + t.scratch + int64_t(split) * M * N;
+#pragma unroll 1
+  for (int cc = 0; cc < t.tile_n; cc += 32) {
+    uint32_t r[32];
+    __syncwarp();
+    tmem_ld32(taddr + (uint32_t(q * 32) << 16) + uint32_t(cc), r);
+    if (row >= M) continue;
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      const int64_t col = n0 + cc + 4 * v;
+      if (col < N)
+        *reinterpret_cast<float4*>(plane + row * N + col) =
+            make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]), __uint_as_float(r[4 * v + 2]),
+                        __uint_as_float(r[4 * v + 3]));
+    }
+  }
+}
+
+// Split-K: the splits' partial accumulators summed in split order, then the
+// GEMM's epilogue (V elements per thread, flat index over [M, N]).
+template <int V>
+__device__ __noinline__ void run_splitk_final(const Ctx c, const Task& t, int item) {
+  const int64_t i0 = (int64_t(item) * kThreads + threadIdx.x) * V;
+  const int64_t numel = t.numel;
+  if (i0 >= numel) return;
+  const float* part = reinterpret_cast<const float*>(c.ws) + t.scratch;
+  float acc[V];
+#pragma unroll
+  for (int j = 0; j < V; ++j) acc[j] = 0.0f;
+  for (int s = 0; s < t.k_splits; ++s) {
+#pragma unroll
+    for (int j = 0; j < V; ++j) acc[j] = __fadd_rn(acc[j], part[int64_t(s) * numel + i0 + j]);
+  }
+  int64_t crd[kMaxRank];
+  unravel(t, i0, crd);
+  float out[V];
+  eval_expr<V>(c, t, crd, acc, out);
+  store_out<V>(c, t.out, i0, out);
+  if (t.has_side) store_side<V>(c, t, i0, out);
+}
+
 __device__ __noinline__ void tc_epilogue_tile_any(const Ctx c, const Task& t, int64_t m0, int64_t n0,
                                                   uint32_t taddr) {
   const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
@@ -1739,11 +1797,12 @@ __device__ __noinline__ uint64_t tc_producer(const Ctx c, const Stage st, const 
                                              uint32_t p_it) {
   bool ok = true;
   asm volatile("fence.proxy.async.global;" ::: "memory");
-  for_my_tiles(c, st, [&](const Task& t, int64_t m0, int64_t n0) {
+  for_my_tiles(c, st, [&](const Task& t, const TileItem& it) {
     const uint32_t bytes = uint32_t(kStageBytesA + t.tile_n * kTileK * 2);
-    const int kblocks = t.k_blocks, tile_n = t.tile_n, tma_a = t.tma_a, tma_b = t.tma_b;
+    const int tile_n = t.tile_n, tma_a = t.tma_a, tma_b = t.tma_b;
     const bool a_mn = t.a_mn_major, b_mn = t.b_mn_major;
-    for (int kb = 0; kb < kblocks; ++kb) {
+    const int64_t m0 = it.m0, n0 = it.n0;
+    for (int kb = it.kb0; kb < it.kb1; ++kb) {
       const uint32_t slot = p_it % kStages, ph = ((p_it / kStages) & 1u) ^ 1u;
       if (!mbar_wait(ts.empty + 8 * slot, ph, c.timeout_ns)) return ok = false;
       const uint32_t full = ts.full + 8 * slot;
@@ -1773,15 +1832,14 @@ __device__ __noinline__ uint64_t tc_mma(const Ctx c, const Stage st, const TcSta
   bool ok = true;
   bool first = true;
   uint32_t m_tile = *m_tile_io;
-  for_my_tiles(c, st, [&](const Task& t, int64_t, int64_t) {
+  for_my_tiles(c, st, [&](const Task& t, const TileItem& it) {
     const uint32_t acc = m_tile & 1u, ph = ((m_tile >> 1) & 1u) ^ 1u;
     if (!mbar_wait(ts.acc_empty + 8 * acc, ph, c.timeout_ns)) return ok = false;
     tc_fence_after();
     const uint32_t d_tmem = ts.tmem + acc * kMaxTileN;
-    const int kblocks = t.k_blocks;
     const uint32_t idesc = t.idesc;
     const bool a_mn = t.a_mn_major, b_mn = t.b_mn_major;
-    for (int kb = 0; kb < kblocks; ++kb) {
+    for (int kb = it.kb0; kb < it.kb1; ++kb) {
       const uint32_t slot = m_it % kStages, fph = (m_it / kStages) & 1u;
       if (!mbar_wait(ts.full + 8 * slot, fph, c.timeout_ns)) return ok = false;
       if (prof && first) prof[3] = global_ns();
@@ -1792,7 +1850,7 @@ __device__ __noinline__ uint64_t tc_mma(const Ctx c, const Stage st, const TcSta
       for (int k = 0; k < kTileK / 16; ++k) {
         const uint64_t ad = a_mn ? smem_desc(a_base + 2048 * k, 8192, 1024) : smem_desc(a_base + 32 * k, 16, 1024);
         const uint64_t bd = b_mn ? smem_desc(b_base + 2048 * k, 8192, 1024) : smem_desc(b_base + 32 * k, 16, 1024);
-        umma_f16(d_tmem, ad, bd, idesc, uint32_t(kb | k));
+        umma_f16(d_tmem, ad, bd, idesc, uint32_t((kb - it.kb0) | k));
       }
       umma_commit(ts.empty + 8 * slot);
       ++m_it;
@@ -1811,11 +1869,17 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
   bool first = true;
   const int lane = threadIdx.x & 31;
   const uint32_t stg = ts.stg + uint32_t((threadIdx.x >> 5) - 4) * ts.stg_warp_bytes;
-  for_my_tiles(c, st, [&](const Task& t, int64_t m0, int64_t n0) {
+  for_my_tiles(c, st, [&](const Task& t, const TileItem& it) {
+    const int64_t m0 = it.m0, n0 = it.n0;
     const uint32_t acc = e_tile & 1u, ph = (e_tile >> 1) & 1u;
     long long* stamp = prof && first && threadIdx.x == 128 ? prof + 5 : nullptr;
     first = false;
-    if (t.epi_stage) {
+    if (t.k_splits > 1) {
+      if (!mbar_wait(ts.acc_full + 8 * acc, ph, c.timeout_ns)) return ok = false;
+      if (stamp) *stamp = global_ns();
+      tc_fence_after();
+      tc_epilogue_partial(c, t, m0, n0, it.split, ts.tmem + acc * kMaxTileN);
+    } else if (t.epi_stage) {
       if (!tc_epilogue_staged_any(c, t, m0, n0, ts.tmem + acc * kMaxTileN, stg, ts.acc_full + 8 * acc, ph, stamp))
         return ok = false;
     } else {
@@ -1871,6 +1935,12 @@ __device__ void run_item(const Ctx& c, const Task& t, int item, float* smem) {
         run_pointwise<8>(c, t, item);
       else
         run_pointwise<1>(c, t, item);
+      break;
+    case T_SPLITK_FINAL:
+      if (t.vec == 8)
+        run_splitk_final<8>(c, t, item);
+      else
+        run_splitk_final<1>(c, t, item);
       break;
     case T_REDUCE_ROW:
       if (t.vec == 8)

@@ -1167,6 +1167,7 @@ class Planner {
     t.vec = (t.rank >= 1 && t.shape[t.rank - 1] % 8 == 0 && t.numel > 0) ? 8 : 1;
     t.tma_a = t.tma_b = -1;
     t.op_index = -1;
+    t.k_splits = 1;
     return t;
   }
 
@@ -1203,7 +1204,7 @@ class Planner {
   // rows) and go through shared memory.  -1: not eligible.
   int epi_stage_mask(const Plan& plan, const Task& t) const {
     const tkd::Chain& ch = t.chain;
-    if (t.kind != tkd::T_GEMM_TC || !ch.valid || ch.fast < tkd::FK_E_ACC ||
+    if (t.kind != tkd::T_GEMM_TC || t.k_splits > 1 || !ch.valid || ch.fast < tkd::FK_E_ACC ||
         (ch.fast > tkd::FK_E_ACC_THRESH && ch.fast != tkd::FK_E_UPDATE && ch.fast != tkd::FK_E_MOMENTUM))
       return -1;
     if (t.out.dtype == TK_F32 || t.out.base % 8 != 0 || t.n % 8 != 0) return -1;
@@ -1417,6 +1418,18 @@ class Planner {
     uint32_t ab = A.dtype == TK_BF16 ? 1u : 0u;
     t.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) |
               (uint32_t(bn >> 3) << 17) | (uint32_t(tkd::kTileM >> 4) << 24);
+    // Split-K when the tiles leave most SMs idle and each tile has a long K
+    // loop (at least 8 k blocks per split).
+    t.k_splits = 1;
+    t.kb_split = t.k_blocks;
+    if (opt_.split_k && 2 * int64_t(t.n_items) <= sms_ && t.k_blocks >= 16 && N % 8 == 0) {
+      const int splits = int(std::min<int64_t>({int64_t(t.k_blocks / 8), int64_t(sms_ / t.n_items), 8}));
+      if (splits >= 2) {
+        t.kb_split = int(ceil_div(t.k_blocks, splits));
+        t.k_splits = int(ceil_div(t.k_blocks, t.kb_split));
+        t.n_items *= t.k_splits;
+      }
+    }
     return true;
   }
 
@@ -1441,6 +1454,21 @@ class Planner {
     t.has_side = 1;
     t.side = st;
     t.out2 = out_ref(op.out.buffer_id);
+  }
+
+  // A split-K GEMM (k_splits > 1) leaves its epilogue to a second task.
+  std::vector<Task> lower_gemm_tasks(Plan& plan, const OpInfo& mm, int64_t* scratch_cursor) {
+    Task t = lower_gemm(plan, mm);
+    if (t.kind != tkd::T_GEMM_TC || t.k_splits <= 1) return {t};
+    Task f = t;
+    f.kind = tkd::T_SPLITK_FINAL;
+    f.tma_a = f.tma_b = -1;
+    f.n_items = int(ceil_div(t.numel, int64_t(tkd::kThreads) * t.vec));
+    f.scratch = t.scratch = tkd::kHeaderUnits + arena_total_ + *scratch_cursor;
+    *scratch_cursor += round_up(int64_t(t.k_splits) * t.numel, 64);
+    t.chain.fast = tkd::FK_NONE;
+    f.chain.fast = tkd::FK_NONE;
+    return {t, f};
   }
 
   Task lower_gemm(Plan& plan, const OpInfo& mm) {
@@ -1766,6 +1794,7 @@ class Planner {
       Task f;
       size_t pos;
       std::vector<Region> reads, writes;
+      bool reads_operands = false;  // the final pass reads the op's operands (epilogue chain)
     };
     std::vector<Pending> pending;
     auto barrier = [&]() {
@@ -1775,7 +1804,7 @@ class Planner {
       for (auto& p : pending) {
         stages.back().push_back(p.f);
         stage_of_[p.pos] = int(stages.size()) - 1;
-        if (p.f.post.valid) stage_reads.insert(stage_reads.end(), p.reads.begin(), p.reads.end());
+        if (p.f.post.valid || p.reads_operands) stage_reads.insert(stage_reads.end(), p.reads.begin(), p.reads.end());
         stage_writes.insert(stage_writes.end(), p.writes.begin(), p.writes.end());
       }
       pending.clear();
@@ -1788,7 +1817,7 @@ class Planner {
           for (const auto& r : writes)
             if (overlap(w, r)) return true;
         }
-        if (p.f.post.valid)
+        if (p.f.post.valid || p.reads_operands)
           for (const auto& r : p.reads)
             for (const auto& w : writes)
               if (overlap(r, w)) return true;
@@ -1831,13 +1860,23 @@ class Planner {
         while (hazard(reads, writes)) barrier();
         stages.back().push_back(ts[0]);
       } else {
-        Task t = is_mm(op.kind) ? lower_gemm(plan, op)
-                                : lower_pointwise(plan, &op, nullptr, shape_of(op.out), out_ref(op.out.buffer_id),
-                                                  op.out.dtype);
-        t.op_index = op.index;
+        std::vector<Task> ts =
+            is_mm(op.kind) ? lower_gemm_tasks(plan, op, &scratch)
+                           : std::vector<Task>{lower_pointwise(plan, &op, nullptr, shape_of(op.out),
+                                                               out_ref(op.out.buffer_id), op.out.dtype)};
+        for (auto& t : ts) t.op_index = op.index;
+        if (ts.size() == 2) {
+          // split-K: the partial products now, their sum and the epilogue with the next stage
+          if (conflicts_pending(reads, {})) barrier();
+          while (hazard(reads, {})) barrier();
+          stages.back().push_back(ts[0]);
+          stage_reads.insert(stage_reads.end(), reads.begin(), reads.end());
+          pending.push_back({ts[1], pos, reads, writes, true});
+          continue;
+        }
         if (conflicts_pending(reads, writes)) barrier();
         while (hazard(reads, writes)) barrier();
-        stages.back().push_back(t);
+        stages.back().push_back(ts[0]);
       }
       stage_of_[pos] = int(stages.size()) - 1;
       stage_reads.insert(stage_reads.end(), reads.begin(), reads.end());

@@ -204,6 +204,7 @@ void tk_options_default(tk_options* opt) {
   opt->tensor_cores = 1;
   opt->sm_count = 0;
   opt->barrier_timeout_s = 2.0;
+  opt->split_k = 1;
 }
 
 tk_status tk_program_create(const tk_program_desc* desc, const tk_options* opt_in, int device, tk_program** out) {

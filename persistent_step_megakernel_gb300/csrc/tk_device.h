@@ -153,7 +153,8 @@ enum TaskKind : int32_t {
   T_REDUCE_COL = 2,    // reduce the outer index dims; item = (column chunk, part)
   T_REDUCE_FINAL = 3,  // sum the partials of a split reduction
   T_GEMM_SIMT = 4,     // CUDA-core tiled GEMM + epilogue expression
-  T_GEMM_TC = 5        // tcgen05 GEMM + epilogue expression
+  T_GEMM_TC = 5,       // tcgen05 GEMM + epilogue expression
+  T_SPLITK_FINAL = 6   // sum of a split-K GEMM's partial accumulators + its epilogue
 };
 
 struct alignas(16) Task {
@@ -205,6 +206,12 @@ struct alignas(16) Task {
   // the staged path is on.  0 = operands and output accessed directly.
   int32_t epi_stage;
   int32_t pw_unroll;         // pointwise items: vectors per thread (kPointwiseUnroll or kPointwiseUnroll16)
+  // Split-K (under-filled tensor-core GEMMs): item = tile * k_splits + split;
+  // split s covers k blocks [s * kb_split, (s + 1) * kb_split) and writes its
+  // float32 accumulator to scratch + s * m * n; the T_SPLITK_FINAL task sums
+  // the splits in order and applies the epilogue.
+  int32_t k_splits;
+  int32_t kb_split;
 };
 
 struct Stage {

@@ -306,6 +306,30 @@ def test_general_pow_and_middle_dim_reductions():
         assert ulp_distance(gpu[3], want[3], "bfloat16").max() <= 2
 
 
+@pytest.mark.parametrize("k", [1000, 4096])
+def test_split_k_gemm_matches_oracle(k):
+    # Few tiles and a long K loop: the k blocks are split over SMs (a ragged
+    # last block for K = 1000), partial products summed in split order, then
+    # the epilogue (bias, ReLU) and a returned side value.
+    T = TensorSpec.contiguous
+    a, w, b = T("a", (64, k), "bfloat16"), T("w", (128, k), "bfloat16"), T("b", (128,), "bfloat16")
+    ops = [Operation("z", "addmm", (b, a, w.T), T("z", (64, 128), "bfloat16")),
+           Operation("r", "relu", (T("z", (64, 128), "bfloat16"),), T("r", (64, 128), "bfloat16")),
+           Operation("h", "mul", (T("r", (64, 128), "bfloat16"), 0.5), T("h", (64, 128), "bfloat16")),
+           Operation("s", "sum", (T("r", (64, 128), "bfloat16"),), T("s", (), "float32"))]
+    prog = Program([a, w, b], [T("h", (64, 128), "bfloat16"), T("s", (), "float32")], ops)
+    arrays = [S.to_storage(S.normal(S.stream_seed(11, i), int(np.prod(x.shape))), x.dtype).reshape(x.shape)
+              for i, x in enumerate(prog.inputs)]
+    split, st = run_step(prog, arrays)
+    whole, sw = run_step(prog, arrays, split_k=0)
+    kinds = [t["kind"] for t in st.tasks()]
+    assert "splitk_final" in kinds and "splitk_final" not in [t["kind"] for t in sw.tasks()]
+    want = oracle.run_program(prog, values(arrays, prog))
+    for got in (split, whole):
+        assert ulp_distance(got[0], want[0], "bfloat16").max() <= 2
+        np.testing.assert_allclose(got[1], want[1], rtol=1e-3)
+
+
 def test_barrier_timeout_is_reported_and_recoverable():
     """A barrier that can never complete gives up after its limit (no hang)."""
     cfg = S.CONFIGS["c1"]

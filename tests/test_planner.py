@@ -217,7 +217,10 @@ def test_mlp_step_tasks_take_compiled_loops(name):
     # (+ReLU) and bias-minus-target GEMM epilogues, the ReLU-mask epilogue,
     # squares and scaled sums, SGD and momentum updates.
     s = plan(S.mlp_step_program(S.CONFIGS[name], export="state"))
-    assert s["compiled_tasks"] == s["materialized_ops"] and s["chain_tasks"] == 0
+    # C3's second layer (32 tiles, K = 4096) is split over K: its partial
+    # products and their sum + epilogue evaluate the generic chain
+    split = 1 if name == "c3" else 0
+    assert s["compiled_tasks"] == s["materialized_ops"] - split and s["chain_tasks"] == 2 * split
 
 
 def test_strided_operand_falls_back_to_generic_chain():
@@ -281,3 +284,17 @@ def test_side_output_written_from_the_gemm_tile():
     assert (s["fused_epilogues"], s["materialized_ops"], s["stages"]) == (1, 3, 2)
     s = plan(prog, fuse_epilogues=0)
     assert (s["materialized_ops"], s["stages"]) == (5, 4)
+
+
+def test_under_filled_gemm_is_split_over_k():
+    prog = S.mlp_step_program(S.CONFIGS["c3"], export="state")
+    h = B.tk_program_create(prog, B.options(sm_count=152), device=-1)
+    try:
+        tasks = [B.tk_plan_task(h, i) for i in range(B.tk_plan_stats_get(h)["tasks"])]
+    finally:
+        B.tk_program_destroy(h)
+    z2 = [t for t in tasks if t["op_index"] >= 0 and prog.operations[t["op_index"]].name == "z2"]
+    assert [t["kind"] for t in z2] == ["gemm_tc", "splitk_final"]
+    assert z2[0]["n_items"] == 4 * 32 and z2[1]["stage"] == z2[0]["stage"] + 1
+    s = plan(prog, split_k=0)
+    assert s["tasks"] == len(tasks) - 1

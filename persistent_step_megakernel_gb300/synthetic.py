@@ -142,6 +142,9 @@ CONFIGS = {
                     "bfloat16", 32, (128,) * 17, 1e-3, "kaiming_uniform"),
     "c5": MLPConfig("c5", "GEMM-bound bf16 MLP step: batch 4096, 4 layers 4096->4096, ReLU, MSE, SGD lr=1e-4",
                     "bfloat16", 4096, (4096,) * 5, 1e-4, "normal002"),
+    # the online (batch-1) step on the C2 shapes
+    "c2b1": MLPConfig("c2b1", "online bf16 MLP step: batch 1, 256->512->512->128, ReLU, MSE, SGD lr=1e-3",
+                      "bfloat16", 1, (256, 512, 512, 128), 1e-3, "kaiming_uniform"),
     # the mixed-precision method of the pages' harness on the C2 shapes
     "c2m": MLPConfig("c2m", "mixed-precision MLP step: fp32 master weights, bf16 GEMMs, fp32 loss and SGD; "
                      "batch 64, 256->512->512->128", "bfloat16", 64, (256, 512, 512, 128), 1e-3,

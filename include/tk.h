@@ -170,7 +170,8 @@ typedef struct {
 typedef struct {
   int32_t stage;               /* barrier-separated stage the task runs in */
   int32_t kind;                /* 0 pointwise, 1 row reduction, 2 column reduction, 3 partials sum,
-                                  4 CUDA-core GEMM, 5 tensor-core GEMM, 6 split-K sum + epilogue */
+                                  4 CUDA-core GEMM, 5 tensor-core GEMM, 6 split-K sum + epilogue,
+                                  7 one-row GEMM (batch 1) */
   int32_t op_index;            /* index into tk_program_desc.ops; -1 for an output copy or commit */
   int32_t n_items;             /* work items (GEMM tiles, element blocks, reduction outputs x parts) */
   int32_t form;                /* expression evaluator: 0 instructions, 1 generic chain, 2 compiled loop */

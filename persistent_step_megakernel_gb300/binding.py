@@ -260,7 +260,8 @@ def tk_plan_stats_get(handle) -> dict:
     return {name: getattr(s, name) for name, _ in tk_plan_stats._fields_}
 
 
-TASK_KINDS = ("pointwise", "reduce_row", "reduce_col", "reduce_final", "gemm_simt", "gemm_tc", "splitk_final")
+TASK_KINDS = ("pointwise", "reduce_row", "reduce_col", "reduce_final", "gemm_simt", "gemm_tc", "splitk_final",
+              "gemv")
 EXPR_FORMS = ("instructions", "chain", "compiled")
 
 

@@ -1205,6 +1205,36 @@ __device__ __noinline__ void run_reduce_final(const Ctx c, const Task& t, int it
   }
 }
 
+// One-row GEMM: warp w of the item computes output n = 8 * item + w; lane l
+// sums k = 8l + 256j, 8 elements at a time, in j order; the lanes' sums are
+// added by a fixed butterfly; lane 0 applies the epilogue.
+__device__ __noinline__ void run_gemv(const Ctx c, const Task& t, int item) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t n = int64_t(item) * (kThreads / 32) + warp;
+  if (n >= t.n) return;
+  const char* pa = space_ptr(c, t.a.space, t.a.slot);
+  const char* pb = space_ptr(c, t.b.space, t.b.slot);
+  const int64_t brow = t.b.base + n * t.b.stride[1];
+  float acc = 0.0f;
+  for (int64_t k = int64_t(lane) * 8; k < t.k; k += 256) {
+    float a[8], b[8];
+    load8(pa, t.a.dtype, t.a.base + k, a);
+    load8(pb, t.b.dtype, brow + k, b);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc = fmaf(a[j], b[j], acc);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+  if (lane == 0) {
+    int64_t crd[kMaxRank] = {0, n, 0, 0};
+    float v[1];
+    const float a1[1] = {acc};
+    eval_expr<1>(c, t, crd, a1, v);
+    store_out<1>(c, t.out, n, v);
+    if (t.has_side) store_side<1>(c, t, n, v);
+  }
+}
+
 // CUDA-core GEMM tile: TM x TM outputs, 16 x 16 threads, (TM/16)^2 each;
 // float32 fmaf accumulation in k order, then the epilogue expression.
 template <int TM>
@@ -1935,6 +1965,9 @@ __device__ void run_item(const Ctx& c, const Task& t, int item, float* smem) {
         run_pointwise<8>(c, t, item);
       else
         run_pointwise<1>(c, t, item);
+      break;
+    case T_GEMV:
+      run_gemv(c, t, item);
       break;
     case T_SPLITK_FINAL:
       if (t.vec == 8)

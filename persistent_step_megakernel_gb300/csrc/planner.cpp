@@ -1495,7 +1495,14 @@ class Planner {
     t.b = operand_ref(B);
     t.a_kcontig = A.strides[1] == 1 || A.shape[0] <= 1;
     t.b_ncontig = B.strides[1] == 1 || B.shape[0] <= 1;
-    if (!try_tensor_core(plan, t, A, B)) {
+    // One row (the online, batch-1 step) with K-contiguous, 16-byte aligned
+    // operands: a warp per output, vector loads along K, a fixed-order tree sum.
+    const bool gemv = M == 1 && K % 8 == 0 && A.strides[1] == 1 && B.strides[0] == 1 &&
+                      (N <= 1 || B.strides[1] % 8 == 0) && t.a.base % 8 == 0 && t.b.base % 8 == 0;
+    if (gemv) {
+      t.kind = tkd::T_GEMV;
+      t.n_items = int(ceil_div(N, tkd::kThreads / 32));
+    } else if (!try_tensor_core(plan, t, A, B)) {
       // CUDA-core tile: the largest of 64/32/16 that still gives every SM a tile
       int tile = 16;
       for (int cand : {64, 32}) {

@@ -154,7 +154,8 @@ enum TaskKind : int32_t {
   T_REDUCE_FINAL = 3,  // sum the partials of a split reduction
   T_GEMM_SIMT = 4,     // CUDA-core tiled GEMM + epilogue expression
   T_GEMM_TC = 5,       // tcgen05 GEMM + epilogue expression
-  T_SPLITK_FINAL = 6   // sum of a split-K GEMM's partial accumulators + its epilogue
+  T_SPLITK_FINAL = 6,  // sum of a split-K GEMM's partial accumulators + its epilogue
+  T_GEMV = 7           // one-row GEMM (batch 1) with K-contiguous B: a warp per output
 };
 
 struct alignas(16) Task {

@@ -330,6 +330,25 @@ def test_split_k_gemm_matches_oracle(k):
         np.testing.assert_allclose(got[1], want[1], rtol=1e-3)
 
 
+@pytest.mark.parametrize("dtype,k", [("float16", 1000), ("bfloat16", 256), ("float32", 72)])
+def test_one_row_gemv_matches_oracle(dtype, k):
+    # batch 1: a warp per output; K not a multiple of the 256-element stride
+    T = TensorSpec.contiguous
+    a, w, b = T("a", (1, k), dtype), T("w", (40, k), dtype), T("b", (40,), dtype)
+    ops = [Operation("z", "addmm", (b, a, w.T), T("z", (1, 40), dtype)),
+           Operation("r", "relu", (T("z", (1, 40), dtype),), T("r", (1, 40), dtype))]
+    prog = Program([a, w, b], [T("r", (1, 40), dtype)], ops)
+    arrays = [S.to_storage(S.normal(S.stream_seed(13, i), int(np.prod(x.shape))), x.dtype).reshape(x.shape)
+              for i, x in enumerate(prog.inputs)]
+    got, st = run_step(prog, arrays)
+    assert [t["kind"] for t in st.tasks()] == ["gemv"]
+    want = oracle.run_program(prog, values(arrays, prog))
+    if dtype == "float32":
+        np.testing.assert_allclose(got[0], want[0], rtol=1e-5, atol=1e-5)
+    else:
+        assert ulp_distance(got[0], want[0], dtype).max() <= 2
+
+
 def test_barrier_timeout_is_reported_and_recoverable():
     """A barrier that can never complete gives up after its limit (no hang)."""
     cfg = S.CONFIGS["c1"]

@@ -1578,16 +1578,20 @@ __device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
-// Store a staged 32 x 32 chunk (16-bit values), four lanes per 64-byte row.
+// Store a staged 32 x 32 chunk (16-bit values), four lanes per 64-byte row:
+// lane l stores piece l & 3 of rows l / 4 + 8i, i = 0..3 (the swizzle of
+// those rows is the same, so their shared addresses are 512 bytes apart).
 __device__ __forceinline__ void stage_store(uint32_t buf, char* out, int64_t row0, int64_t col0, int64_t M,
                                             int64_t N) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll 1
+  const int lane = threadIdx.x & 31, lr = lane >> 2, j = lane & 3;
+  if (col0 + 8 * j >= N) return;
+  const uint32_t s0 = buf + stg_off(lr, j);
+  char* g0 = out + ((row0 + lr) * N + col0 + 8 * j) * 2;
+  const int64_t gstep = 8 * N * 2;
+#pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int p = 32 * i + lane, rr = p >> 2, j = p & 3;
-    const int64_t row = row0 + rr, col = col0 + 8 * j;
-    const uint4 val = lds128(buf + stg_off(rr, j));
-    if (row < M && col < N) *reinterpret_cast<uint4*>(out + (row * N + col) * 2) = val;
+    const uint4 val = lds128(s0 + 512 * i);
+    if (row0 + lr + 8 * i < M) *reinterpret_cast<uint4*>(g0 + i * gstep) = val;
   }
 }
 
@@ -1642,16 +1646,19 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
   // instruction cache, which matters more than loop overhead for the small
   // tiles of latency-bound steps (the first chunk of a stage otherwise waits
   // for its instructions).
+  // per-row operands of chunk ch, in the same lane pattern as stage_store
+  const int lr = lane >> 2, lj = lane & 3;
   auto prefetch = [&](int ch) {
-    const int64_t col0 = n0 + 32 * ch;
-    const uint32_t half = uint32_t(ch & 1) * kEpiBufBytes;
-#pragma unroll 1
+    if (!(st0 || st1)) return;
+    const int64_t col = n0 + 32 * ch + 8 * lj;
+    if (col >= N) return;
+    const uint32_t off = uint32_t(ch & 1) * kEpiBufBytes + stg_off(lr, lj);
+#pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int p = 32 * i + lane, r = p >> 2, j = p & 3;
-      const int64_t row = row0 + r, col = col0 + 8 * j;
-      if (row < M && col < N) {
-        if (st0) cp_async16(b0 + half + stg_off(r, j), F.p0 + row * F.rs0 + col * 2);
-        if (st1) cp_async16(b1 + half + stg_off(r, j), F.p1 + row * F.rs1 + col * 2);
+      const int64_t row = row0 + lr + 8 * i;
+      if (row < M) {
+        if (st0) cp_async16(b0 + off + 512 * i, F.p0 + row * F.rs0 + col * 2);
+        if (st1) cp_async16(b1 + off + 512 * i, F.p1 + row * F.rs1 + col * 2);
       }
     }
   };

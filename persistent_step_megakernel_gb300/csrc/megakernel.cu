@@ -1052,6 +1052,41 @@ __device__ __noinline__ float row_sum_fast(const Ctx c, const Task& t, int64_t o
   return acc;
 }
 
+// The same over 16-bit operands, streaming: eight raw 16-byte vectors per
+// thread in flight (a reduction over a tensor much larger than one block's
+// share must keep enough loads in flight to cover the memory latency).
+template <int K>
+__device__ __noinline__ float row_sum_fast16(const Ctx c, const Task& t, int64_t o, int64_t r0, int64_t r1) {
+  constexpr int W = 8;
+  constexpr int64_t step = int64_t(kThreads) * 8;
+  const Fast F = fast_params(c, t);
+  const char* p0 = F.p0 + o * t.red_inner * 2;
+  const char* p1 = FastTraits<K>::load1 ? F.p1 + o * t.red_inner * 2 : nullptr;
+  float acc = 0.0f, none[8];
+  for (int64_t r = r0 + int64_t(threadIdx.x) * 8; r < r1; r += W * step) {
+    uint4 q0[W], q1[W];
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      if (r + w * step < r1) {
+        q0[w] = *reinterpret_cast<const uint4*>(p0 + (r + w * step) * 2);
+        if constexpr (FastTraits<K>::load1) q1[w] = *reinterpret_cast<const uint4*>(p1 + (r + w * step) * 2);
+      }
+    }
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      if (r + w * step < r1) {
+        float a[8], b[8], x[8];
+        unpack8(q0[w], F.dt0, a);
+        if constexpr (FastTraits<K>::load1) unpack8(q1[w], F.dt1, b);
+        fast_apply<K>(F, a, b, none, x);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc = __fadd_rn(acc, x[j]);
+      }
+    }
+  }
+  return acc;
+}
+
 template <int V>
 __device__ __noinline__ float row_sum_vm(const Ctx c, const Task& t, int64_t o, int64_t r0, int64_t r1) {
   float acc = 0.0f;
@@ -1077,12 +1112,21 @@ __device__ __noinline__ void run_reduce_row(const Ctx c, const Task& t, int item
   bool done = false;
   if constexpr (V == 8) {
     done = true;
-#define TK_CALL(k) acc = row_sum_fast<k>(c, t, o, r0, r1)
-    switch (t.chain.fast) {
-      TK_FAST_L_CASES(TK_CALL)
-      default: done = false; break;
-    }
+    if (t.pw_unroll == kPointwiseUnroll16) {
+#define TK_CALL(k) acc = row_sum_fast16<k>(c, t, o, r0, r1)
+      switch (t.chain.fast) {
+        TK_FAST_L_CASES(TK_CALL)
+        default: done = false; break;
+      }
 #undef TK_CALL
+    } else {
+#define TK_CALL(k) acc = row_sum_fast<k>(c, t, o, r0, r1)
+      switch (t.chain.fast) {
+        TK_FAST_L_CASES(TK_CALL)
+        default: done = false; break;
+      }
+#undef TK_CALL
+    }
   }
   if (!done) acc = t.chain.valid ? row_sum_chain<V>(c, t, o, r0, r1) : row_sum_vm<V>(c, t, o, r0, r1);
   acc = block_sum(acc, red);
@@ -1153,6 +1197,52 @@ __device__ __noinline__ void run_reduce_col_fast(const Ctx c, const Task& t, int
         fast_apply<K>(F, b0, b1, none, x);
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], x[j]);
+      }
+    }
+  }
+  col_combine<8>(c, t, ch, p, acc, red, pre);
+}
+
+// Column sums over 16-bit operands, streaming: each warp keeps eight rows'
+// 16-byte vectors in flight.
+template <int K>
+__device__ __noinline__ void run_reduce_col_fast16(const Ctx c, const Task& t, int item, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int W = 8;
+  constexpr int64_t rstep = kThreads / 32;
+  const int64_t ch = item / t.parts;
+  const int p = item % t.parts;
+  const int64_t Q = t.red_inner;
+  const int64_t col0 = ch * 256 + lane * 8;
+  const int64_t r0 = int64_t(p) * t.part_len;
+  const int64_t r1 = min(t.red_outer, r0 + t.part_len);
+  const int64_t my_col = ch * 256 + threadIdx.x;
+  const float pre = t.parts == 1 && my_col < Q ? post_operand(c, t, my_col) : 0.0f;
+  const Fast F = fast_params(c, t);
+  float acc[8], none[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+  if (col0 < Q) {
+    for (int64_t r = r0 + warp; r < r1; r += W * rstep) {
+      uint4 q0[W], q1[W];
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        if (r + w * rstep < r1) {
+          q0[w] = *reinterpret_cast<const uint4*>(F.p0 + ((r + w * rstep) * Q + col0) * 2);
+          if constexpr (FastTraits<K>::load1)
+            q1[w] = *reinterpret_cast<const uint4*>(F.p1 + ((r + w * rstep) * Q + col0) * 2);
+        }
+      }
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        if (r + w * rstep < r1) {
+          float a[8], b[8], x[8];
+          unpack8(q0[w], F.dt0, a);
+          if constexpr (FastTraits<K>::load1) unpack8(q1[w], F.dt1, b);
+          fast_apply<K>(F, a, b, none, x);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], x[j]);
+        }
       }
     }
   }
@@ -1990,11 +2080,20 @@ __device__ void run_item(const Ctx& c, const Task& t, int item, float* smem) {
       break;
     case T_REDUCE_COL:
       if (t.vec == 8)
-        switch (t.chain.fast) {
-#define TK_CALL(k) run_reduce_col_fast<k>(c, t, item, smem)
-          TK_FAST_L_CASES(TK_CALL)
+        if (t.pw_unroll == kPointwiseUnroll16) {
+          switch (t.chain.fast) {
+#define TK_CALL(k) run_reduce_col_fast16<k>(c, t, item, smem)
+            TK_FAST_L_CASES(TK_CALL)
 #undef TK_CALL
-          default: run_reduce_col<8>(c, t, item, smem); break;
+            default: run_reduce_col<8>(c, t, item, smem); break;
+          }
+        } else {
+          switch (t.chain.fast) {
+#define TK_CALL(k) run_reduce_col_fast<k>(c, t, item, smem)
+            TK_FAST_L_CASES(TK_CALL)
+#undef TK_CALL
+            default: run_reduce_col<8>(c, t, item, smem); break;
+          }
         }
       else
         run_reduce_col<1>(c, t, item, smem);

@@ -1693,6 +1693,14 @@ class Planner {
     if (t.parts <= 1 && fused_it != fused_.end()) lower_post_chain(plan, t, op, fused_it->second);
     finish_refs(plan, t);
     classify_fast(plan, t);
+    // compiled sources over 16-bit operands stream with more loads in flight
+    // (pw_unroll marks them, as for pointwise tasks; the output type does not matter)
+    t.pw_unroll = tkd::kPointwiseUnroll;
+    if (t.vec == 8 && t.chain.fast >= tkd::FK_L && t.chain.fast <= tkd::FK_L_SCALE_AXPY) {
+      t.pw_unroll = tkd::kPointwiseUnroll16;
+      for (int i = 0; i < t.chain.n_loads; ++i)
+        if (plan.refs[t.ref_begin + t.chain.load_ref[i]].dtype == TK_F32) t.pw_unroll = tkd::kPointwiseUnroll;
+    }
     if (n_out == 0) t.n_items = 0;
     if (t.parts <= 1) {
       t.parts = 1;

@@ -1696,7 +1696,10 @@ class Planner {
     // compiled sources over 16-bit operands stream with more loads in flight
     // (pw_unroll marks them, as for pointwise tasks; the output type does not matter)
     t.pw_unroll = tkd::kPointwiseUnroll;
-    if (t.vec == 8 && t.chain.fast >= tkd::FK_L && t.chain.fast <= tkd::FK_L_SCALE_AXPY) {
+    // (only long parts: a short one gains nothing from deeper loads and pays
+    // for the larger loop)
+    const bool long_part = row ? t.part_len >= 16 * tkd::kThreads * 8 : t.part_len >= 128;
+    if (long_part && t.vec == 8 && t.chain.fast >= tkd::FK_L && t.chain.fast <= tkd::FK_L_SCALE_AXPY) {
       t.pw_unroll = tkd::kPointwiseUnroll16;
       for (int i = 0; i < t.chain.n_loads; ++i)
         if (plan.refs[t.ref_begin + t.chain.load_ref[i]].dtype == TK_F32) t.pw_unroll = tkd::kPointwiseUnroll;

@@ -141,12 +141,18 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def dist_setup(world: int):
+def dist_setup(world: int, backend: str = "nccl"):
+    """One process per GPU (torchrun's environment); None for a single process."""
     if world <= 1:
         return None
     import torch.distributed as dist
-    dist.init_process_group("nccl")
+    dist.init_process_group(backend)
     return dist
+
+
+def replica_value(us_per_step_max: float, world: int) -> float:
+    """Whole-job steps/s of `world` independent replicas timed by the slowest rank."""
+    return world * 1e6 / us_per_step_max
 
 
 def allmax(dist, value: float, device) -> float:
@@ -344,7 +350,7 @@ def main() -> int:
     e2e_value, h2d, d2h = time_e2e(cfg, r, min(args.steps, 500), device)
     e2e_value = allmax(dist, 1.0 / e2e_value, device)
     e2e_value = world / e2e_value
-    value = world * 1e6 / us
+    value = replica_value(us, world)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": True, "scaling": "weak",

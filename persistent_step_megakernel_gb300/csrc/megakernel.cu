@@ -1473,6 +1473,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle: start, leading and
 // stride byte offsets in 16-byte units, descriptor version 1 (bit 46),
 // layout SWIZZLE_128B (2 in bits 61-63).
@@ -1927,7 +1934,7 @@ __device__ __noinline__ uint64_t tc_producer(const Ctx c, const Stage st, const 
   for_my_tiles(c, st, [&](const Task& t, const TileItem& it) {
     const uint32_t bytes = uint32_t(kStageBytesA + t.tile_n * kTileK * 2);
     const int tile_n = t.tile_n, tma_a = t.tma_a, tma_b = t.tma_b;
-    const bool a_mn = t.a_mn_major, b_mn = t.b_mn_major;
+    const int a_mn = t.a_mn_major, b_mn = t.b_mn_major;
     const int64_t m0 = it.m0, n0 = it.n0;
     for (int kb = it.kb0; kb < it.kb1; ++kb) {
       const uint32_t slot = p_it % kStages, ph = ((p_it / kStages) & 1u) ^ 1u;
@@ -1938,12 +1945,16 @@ __device__ __noinline__ uint64_t tc_producer(const Ctx c, const Stage st, const 
       const int k0 = kb * kTileK;
       if (!a_mn) {
         tma_load_2d(a_dst, &maps[tma_a], k0, int(m0), full);
+      } else if (a_mn == 2) {
+        tma_load_3d(a_dst, &maps[tma_a], 0, k0, int(m0 >> 6), full);
       } else {
         tma_load_2d(a_dst, &maps[tma_a], int(m0), k0, full);
         tma_load_2d(a_dst + 8192, &maps[tma_a], int(m0) + 64, k0, full);
       }
       if (!b_mn) {
         tma_load_2d(b_dst, &maps[tma_b], k0, int(n0), full);
+      } else if (b_mn == 2) {
+        tma_load_3d(b_dst, &maps[tma_b], 0, k0, int(n0 >> 6), full);
       } else {
         for (int j = 0; j < tile_n / 64; ++j) tma_load_2d(b_dst + 8192 * j, &maps[tma_b], int(n0) + 64 * j, k0, full);
       }

@@ -1350,7 +1350,9 @@ class Planner {
 
   // TMA view of one GEMM operand: the contiguous dim is the box's inner dim.
   // A is [M,K], B is [K,N]; "K-major" means K is the contiguous dim.
-  bool tma_operand(const tk_tensor_spec& v, bool is_a, int box_rows, TmaOperand* out, bool* mn_major) const {
+  // *mn_major: 0 K-major, 1 MN-major in 64-wide boxes, 2 MN-major in one box
+  // of box_rows / 64 slabs (MN a multiple of 64, so no slab crosses the end).
+  bool tma_operand(const tk_tensor_spec& v, bool is_a, int box_rows, TmaOperand* out, int* mn_major) const {
     int64_t base;
     int space, slot;
     location(v.buffer_id, &space, &slot, &base);
@@ -1363,17 +1365,21 @@ class Planner {
     o.dtype = v.dtype;
     o.box_inner = tkd::kTileK;
     if (v.strides[k_dim] == 1 && v.shape[k_dim] >= 1) {
-      *mn_major = false;
+      *mn_major = 0;
       o.inner = v.shape[k_dim];
       o.outer = v.shape[mn_dim];
       o.outer_stride = v.strides[mn_dim];
       o.box_outer = box_rows;
     } else if (v.strides[mn_dim] == 1) {
-      *mn_major = true;
+      *mn_major = 1;
       o.inner = v.shape[mn_dim];
       o.outer = v.shape[k_dim];
       o.outer_stride = v.strides[k_dim];
       o.box_outer = tkd::kTileK;
+      if (box_rows > 64 && o.inner % 64 == 0) {
+        o.chunks = box_rows / 64;
+        *mn_major = 2;
+      }
     } else {
       return false;
     }
@@ -1399,7 +1405,7 @@ class Planner {
       }
     }
     TmaOperand ta, tb;
-    bool a_mn = false, b_mn = false;
+    int a_mn = 0, b_mn = 0;
     if (!tma_operand(A, true, tkd::kTileM, &ta, &a_mn) || !tma_operand(B, false, bn, &tb, &b_mn)) return false;
     t.kind = tkd::T_GEMM_TC;
     t.tile_m = tkd::kTileM;
@@ -1416,7 +1422,7 @@ class Planner {
     // instruction descriptor, kind::f16: D f32 (bits 4-5), A/B type (7-9, 10-12:
     // 0 f16, 1 bf16), A/B MN-major (15, 16), N >> 3 (17-22), M >> 4 (24-28)
     uint32_t ab = A.dtype == TK_BF16 ? 1u : 0u;
-    t.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) |
+    t.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (uint32_t(a_mn != 0) << 15) | (uint32_t(b_mn != 0) << 16) |
               (uint32_t(bn >> 3) << 17) | (uint32_t(tkd::kTileM >> 4) << 24);
     // Split-K when the tiles leave most SMs idle and each tile has a long K
     // loop (at least 8 k blocks per split).

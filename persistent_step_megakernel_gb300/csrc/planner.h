@@ -23,6 +23,10 @@ struct TmaOperand {
   int64_t inner, outer;     // extents: contiguous dim, strided dim
   int64_t outer_stride;     // elements between consecutive outer rows
   int32_t box_inner, box_outer;
+  // > 0: an MN-major operand read as one box of `chunks` 64-wide MN slabs
+  // (a 3-D view: MN within the slab, K, slab), stacked 8 KB apart in shared
+  // memory exactly as `chunks` separate 2-D boxes would be.
+  int32_t chunks;
 };
 
 struct Plan {

@@ -160,13 +160,21 @@ tk_status encode_maps(tk_program* p, const void* const* inputs, void* const* out
   for (size_t i = 0; i < ops.size(); ++i) {
     const auto& o = ops[i];
     char* addr = static_cast<char*>(const_cast<void*>(bases[i])) + o.base_elems * 2;
-    cuuint64_t dims[2] = {cuuint64_t(o.inner), cuuint64_t(o.outer)};
-    cuuint64_t strides[1] = {cuuint64_t(o.outer_stride) * 2};
-    cuuint32_t box[2] = {cuuint32_t(o.box_inner), cuuint32_t(o.box_outer)};
-    cuuint32_t estr[2] = {1, 1};
+    // 2-D: (inner, outer).  3-D (MN-major slabs): (MN within a 64-wide slab,
+    // K, slab), the slab dim stepping 128 bytes along the contiguous MN rows.
+    const bool slabs = o.chunks > 0;
+    cuuint64_t dims[3] = {cuuint64_t(o.inner), cuuint64_t(o.outer), 1};
+    cuuint64_t strides[2] = {cuuint64_t(o.outer_stride) * 2, 128};
+    cuuint32_t box[3] = {cuuint32_t(o.box_inner), cuuint32_t(o.box_outer), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (slabs) {
+      dims[0] = 64;
+      dims[2] = cuuint64_t(o.inner / 64);
+      box[2] = cuuint32_t(o.chunks);
+    }
     CUresult r = fn(&maps[i], o.dtype == TK_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                    2, addr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    slabs ? 3 : 2, addr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(TK_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string(int(r)) + ")");
   }
   p->maps.swap(maps);

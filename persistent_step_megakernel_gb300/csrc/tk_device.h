@@ -188,7 +188,7 @@ struct alignas(16) Task {
   // tcgen05 path
   int32_t tma_a, tma_b;
   uint32_t idesc;
-  int32_t a_mn_major, b_mn_major;
+  int32_t a_mn_major, b_mn_major;  // 0 K-major; 1 MN-major, 64-wide boxes; 2 MN-major, one box of slabs
   int32_t k_blocks;
   // Reductions: a pointwise chain applied to each finished output (e.g. the
   // SGD step of a bias right after its gradient's column sum).  Its start is

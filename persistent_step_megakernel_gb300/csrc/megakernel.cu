@@ -43,6 +43,15 @@ struct Ctx {
   void* const* io;  // shared-memory copy of Params::io
   long long timeout_ns;
   Prep* prep;       // shared memory: one prepared chain per warp
+  int stage;        // stage being run (for failure reports)
+  // bulk-streamed reductions (tensor-core launches): shared addresses of the
+  // slots and of their mbarriers, the slot count (0: none) and the block's
+  // running count of slots consumed, which fixes each slot's next phase
+  uint32_t bulk, bulk_bar;
+  int bulk_slots;
+  uint32_t* bulk_it;
+  uint32_t col_bar;   // column sums: the same slots, mbarriers counting every thread
+  uint32_t* col_it;
 };
 
 // ------------------------------------------------------------------ memory
@@ -1052,6 +1061,11 @@ __device__ __noinline__ float row_sum_fast(const Ctx c, const Task& t, int64_t o
   return acc;
 }
 
+template <int K>
+__device__ __noinline__ float row_sum_bulk16(const Ctx c, const Task& t, int64_t o, int64_t r0, int64_t r1);
+template <int K>
+__device__ __noinline__ void run_reduce_col_bulk16(const Ctx c, const Task& t, int item, float* red);
+
 // The same over 16-bit operands, streaming: eight raw 16-byte vectors per
 // thread in flight (a reduction over a tensor much larger than one block's
 // share must keep enough loads in flight to cover the memory latency).
@@ -1113,7 +1127,7 @@ __device__ __noinline__ void run_reduce_row(const Ctx c, const Task& t, int item
   if constexpr (V == 8) {
     done = true;
     if (t.pw_unroll == kPointwiseUnroll16) {
-#define TK_CALL(k) acc = row_sum_fast16<k>(c, t, o, r0, r1)
+#define TK_CALL(k) acc = row_sum_bulk16<k>(c, t, o, r0, r1)
       switch (t.chain.fast) {
         TK_FAST_L_CASES(TK_CALL)
         default: done = false; break;
@@ -1478,6 +1492,205 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
+}
+
+// One contiguous global -> shared bulk copy (both 16-byte aligned, size a
+// multiple of 16) completing on mbarrier bar.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// ------------------------------------------- bulk-streamed reductions
+//
+// A long reduction over 16-bit operands keeps only 32 KB per SM in flight
+// with register loads (eight 16-byte vectors per thread), far too little to
+// cover the memory latency at full bandwidth with one block per SM.  In a
+// tensor-core launch the TMA ring is idle during a stage's reductions, so
+// these variants copy the operands into up to kBulkMaxSlots slots of it with
+// bulk copies (16 KB per slot, all slots in flight) and sum from shared
+// memory.  Each thread sums exactly the elements, in exactly the order, of
+// the register-streaming variant, so the two give the same bits.
+
+__device__ __forceinline__ uint4 lds128(uint32_t a);
+
+// Slot k of the block's running slot sequence: its shared address and the
+// parity of the phase that its copy completes.
+struct BulkSlot {
+  uint32_t addr, bar, parity;
+};
+__device__ __forceinline__ BulkSlot bulk_slot(const Ctx& c, uint32_t k) {
+  const uint32_t s = k % uint32_t(c.bulk_slots);
+  return {c.bulk + s * uint32_t(kBulkSlotBytes), c.bulk_bar + 8 * s, (k / uint32_t(c.bulk_slots)) & 1u};
+}
+
+// After a wait ran out at chunk ch (known to every thread): thread 0 waits,
+// again with the time limit, for the copies still in flight (chunks ch up to
+// ch + S - 1) so that none lands after the block has moved on, and records
+// the failure.  Returns the number of chunks issued.
+__device__ __noinline__ int bulk_abandon(const Ctx c, uint32_t it0, int ch, int nch) {
+  const int issued = min(nch, ch + c.bulk_slots);
+  if (threadIdx.x == 0) {
+    for (int k = ch; k < issued; ++k) {
+      const BulkSlot b = bulk_slot(c, it0 + uint32_t(k));
+      mbar_wait(b.bar, b.parity, c.timeout_ns);
+    }
+    record_failure(c, TK_ERR_PIPELINE_TIMEOUT, c.stage);
+  }
+  __syncthreads();
+  return issued;
+}
+
+template <int K>
+__device__ __noinline__ float row_sum_bulk16(const Ctx c, const Task& t, int64_t o, int64_t r0, int64_t r1) {
+  constexpr bool L1 = FastTraits<K>::load1;
+  constexpr int64_t step = int64_t(kThreads) * 8;                         // elements per block-wide pass
+  constexpr int64_t chunk = (L1 ? kBulkSlotBytes / 2 : kBulkSlotBytes) / 2;  // elements per slot and operand
+  constexpr int passes = int(chunk / step);
+  const Fast F = fast_params(c, t);
+  const char* p0 = F.p0 + (o * t.red_inner + r0) * 2;
+  const char* p1 = L1 ? F.p1 + (o * t.red_inner + r0) * 2 : nullptr;
+  const int64_t n = r1 - r0;
+  const bool aligned = (reinterpret_cast<uintptr_t>(p0) & 15) == 0 && (!L1 || (reinterpret_cast<uintptr_t>(p1) & 15) == 0);
+  if (c.bulk_slots < 2 || n < 2 * chunk || n % 8 != 0 || !aligned) return row_sum_fast16<K>(c, t, o, r0, r1);
+  const int S = c.bulk_slots;
+  const int nch = int((n + chunk - 1) / chunk);
+  const uint32_t it0 = *c.bulk_it;
+  auto issue = [&](int ch) {
+    const BulkSlot b = bulk_slot(c, it0 + uint32_t(ch));
+    const int64_t e0 = int64_t(ch) * chunk;
+    const uint32_t bytes = uint32_t(min(chunk, n - e0) * 2);
+    mbar_expect_tx(b.bar, L1 ? 2 * bytes : bytes);
+    bulk_g2s(b.addr, p0 + e0 * 2, bytes, b.bar);
+    if constexpr (L1) bulk_g2s(b.addr + kBulkSlotBytes / 2, p1 + e0 * 2, bytes, b.bar);
+  };
+  if (threadIdx.x == 0) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    for (int ch = 0; ch < min(S, nch); ++ch) issue(ch);
+  }
+  float acc = 0.0f, none[8];
+  int done = nch;
+#pragma unroll 1
+  for (int ch = 0; ch < nch; ++ch) {
+    const BulkSlot b = bulk_slot(c, it0 + uint32_t(ch));
+    const bool ok = mbar_wait(b.bar, b.parity, c.timeout_ns);
+    const uint32_t src = b.addr + threadIdx.x * 16;
+    const int64_t e0 = int64_t(ch) * chunk + int64_t(threadIdx.x) * 8;
+#pragma unroll
+    for (int j = 0; j < passes; ++j) {
+      if (ok && e0 + j * step < n) {
+        float a[8], bb[8], x[8];
+        unpack8(lds128(src + uint32_t(j * step * 2)), F.dt0, a);
+        if constexpr (L1) unpack8(lds128(src + kBulkSlotBytes / 2 + uint32_t(j * step * 2)), F.dt1, bb);
+        fast_apply<K>(F, a, bb, none, x);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc = __fadd_rn(acc, x[q]);
+      }
+    }
+    // slot read by every thread before it is refilled; a wait that ran out
+    // anywhere ends the loop everywhere
+    if (__syncthreads_or(!ok)) {
+      done = bulk_abandon(c, it0, ch, nch);
+      break;
+    }
+    if (threadIdx.x == 0 && ch + S < nch) issue(ch + S);
+  }
+  if (threadIdx.x == 0) *c.bulk_it = it0 + uint32_t(done);
+  return acc;
+}
+
+// Column sums: a slot holds consecutive rows of the item's 256 columns (one
+// 512-byte line per row).  Rows of 512 bytes are too short for bulk copies,
+// so every thread moves its 16-byte pieces with cp.async and a per-thread
+// arrive-on on the slot's mbarrier (which counts all kThreads threads) marks
+// them done; warp w sums rows r0 + w + 8i in increasing i as in the register
+// variant.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src);
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+template <int K>
+__device__ __noinline__ void run_reduce_col_bulk16(const Ctx c, const Task& t, int item, float* red) {
+  constexpr bool L1 = FastTraits<K>::load1;
+  constexpr int rows = (L1 ? kBulkSlotBytes / 2 : kBulkSlotBytes) / 512;  // rows per slot
+  constexpr int pieces = rows * 32 / kThreads;                            // 16-byte pieces per thread
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t ch = item / t.parts;
+  const int p = item % t.parts;
+  const int64_t Q = t.red_inner;
+  const int64_t r0 = int64_t(p) * t.part_len;
+  const int64_t r1 = min(t.red_outer, r0 + t.part_len);
+  const Fast F = fast_params(c, t);
+  const bool aligned = (reinterpret_cast<uintptr_t>(F.p0) & 15) == 0 && (!L1 || (reinterpret_cast<uintptr_t>(F.p1) & 15) == 0);
+  if (c.bulk_slots < 2 || r1 - r0 < 2 * rows || Q % 8 != 0 || !aligned) {
+    run_reduce_col_fast16<K>(c, t, item, red);
+    return;
+  }
+  const int64_t col0 = ch * 256 + lane * 8;
+  const int64_t my_col = ch * 256 + threadIdx.x;
+  const float pre = t.parts == 1 && my_col < Q ? post_operand(c, t, my_col) : 0.0f;
+  const int seg = int(min(int64_t(256), Q - ch * 256) * 2);  // bytes per row
+  const int S = c.bulk_slots;
+  const int nch = int((r1 - r0 + rows - 1) / rows);
+  const uint32_t it0 = *c.col_it;
+  auto slot = [&](int i) {
+    const uint32_t k = it0 + uint32_t(i), s = k % uint32_t(S);
+    return BulkSlot{c.bulk + s * uint32_t(kBulkSlotBytes), c.col_bar + 8 * s, (k / uint32_t(S)) & 1u};
+  };
+  auto issue = [&](int i) {  // every thread
+    const BulkSlot b = slot(i);
+    const int64_t rr = r0 + int64_t(i) * rows;
+#pragma unroll
+    for (int m = 0; m < pieces; ++m) {
+      const int q = int(threadIdx.x) + kThreads * m, row = q >> 5, pc = q & 31;
+      if (rr + row < r1 && pc * 16 < seg) {
+        const int64_t off = ((rr + row) * Q + ch * 256) * 2 + pc * 16;
+        cp_async16(b.addr + uint32_t(row * 512 + pc * 16), F.p0 + off);
+        if constexpr (L1) cp_async16(b.addr + kBulkSlotBytes / 2 + uint32_t(row * 512 + pc * 16), F.p1 + off);
+      }
+    }
+    cp_async_arrive(b.bar);
+  };
+  for (int i = 0; i < min(S, nch); ++i) issue(i);
+  float acc[8], none[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+  int done = nch;
+#pragma unroll 1
+  for (int i = 0; i < nch; ++i) {
+    const BulkSlot b = slot(i);
+    const bool ok = mbar_wait(b.bar, b.parity, c.timeout_ns);
+    const int64_t rr = r0 + int64_t(i) * rows;
+    if (ok && col0 < Q) {
+      const uint32_t src = b.addr + uint32_t(lane) * 16;
+#pragma unroll
+      for (int w = 0; w < rows / 8; ++w) {
+        const int rl = warp + 8 * w;
+        if (rr + rl < r1) {
+          float a[8], bb[8], x[8];
+          unpack8(lds128(src + uint32_t(rl) * 512), F.dt0, a);
+          if constexpr (L1) unpack8(lds128(src + kBulkSlotBytes / 2 + uint32_t(rl) * 512), F.dt1, bb);
+          fast_apply<K>(F, a, bb, none, x);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], x[q]);
+        }
+      }
+    }
+    // slot read by every thread before it is refilled; a wait that ran out
+    // anywhere ends the loop everywhere, after this thread's copies landed
+    if (__syncthreads_or(!ok)) {
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      __syncthreads();
+      if (threadIdx.x == 0) record_failure(c, TK_ERR_PIPELINE_TIMEOUT, c.stage);
+      done = min(nch, i + S);
+      break;
+    }
+    if (i + S < nch) issue(i + S);
+  }
+  if (threadIdx.x == 0) *c.col_it = it0 + uint32_t(done);
+  col_combine<8>(c, t, ch, p, acc, red, pre);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle: start, leading and
@@ -2093,7 +2306,7 @@ __device__ void run_item(const Ctx& c, const Task& t, int item, float* smem) {
       if (t.vec == 8)
         if (t.pw_unroll == kPointwiseUnroll16) {
           switch (t.chain.fast) {
-#define TK_CALL(k) run_reduce_col_fast16<k>(c, t, item, smem)
+#define TK_CALL(k) run_reduce_col_bulk16<k>(c, t, item, smem)
             TK_FAST_L_CASES(TK_CALL)
 #undef TK_CALL
             default: run_reduce_col<8>(c, t, item, smem); break;
@@ -2156,6 +2369,10 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   __shared__ Stage s_stage;
   __shared__ Prep s_prep[kThreads / 32];
   __shared__ __align__(8) uint64_t s_bar[2 * kStages + 4];
+  __shared__ __align__(8) uint64_t s_bulk_bar[kBulkMaxSlots];
+  __shared__ uint32_t s_bulk_it;
+  __shared__ __align__(8) uint64_t s_col_bar[kBulkMaxSlots];
+  __shared__ uint32_t s_col_it;
   __shared__ uint32_t s_tmem;
   __shared__ int s_flag;
   extern __shared__ __align__(1024) unsigned char s_dyn[];
@@ -2188,6 +2405,12 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
         mbar_init(ts.acc_full + 8 * i, 1);
         mbar_init(ts.acc_empty + 8 * i, 4);
       }
+      for (int i = 0; i < kBulkMaxSlots; ++i) {
+        mbar_init(smem_u32(&s_bulk_bar[i]), 1);
+        mbar_init(smem_u32(&s_col_bar[i]), kThreads);
+      }
+      s_bulk_it = 0;
+      s_col_it = 0;
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -2218,6 +2441,14 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     }
   }
   Ctx c{nullptr, nullptr, nullptr, p.ws, reinterpret_cast<Header*>(p.ws), s_io, p.timeout_ns, s_prep};
+  if (tc) {
+    c.bulk = ts.ring + kBulkOffset;
+    c.bulk_bar = smem_u32(&s_bulk_bar[0]);
+    c.bulk_slots = max(0, min(kBulkMaxSlots, (kStages * p.ring_stage_bytes - kBulkOffset) / kBulkSlotBytes));
+    c.bulk_it = &s_bulk_it;
+    c.col_bar = smem_u32(&s_col_bar[0]);
+    c.col_it = &s_col_it;
+  }
   long long* prof = p.prof ? p.prof + kProfStamps * int64_t(blockIdx.x) : nullptr;
   const int64_t prof_step = kProfStamps * int64_t(gridDim.x);
   const int n_stages = prog->n_stages;
@@ -2232,6 +2463,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   }
   for (int s = 0; s < n_stages; ++s) {
     const Stage st = s_stage;
+    c.stage = s;
     if (prof && threadIdx.x == 0) prof[s * prof_step] = global_ns();
     c.tasks = st.task_end - st.task_begin <= kStageTasks ? s_tasks - st.task_begin : prog->tasks;
     c.code = st.code_hi - st.code_lo <= kStageCode ? s_code - st.code_lo : prog->code;

@@ -39,6 +39,12 @@ constexpr int kDynSmemBudget = 211 * 1024;
 // outside the tensor-core phase of a stage).
 constexpr int kWorkFloats = 2 * 16 * (64 + 4) > 8 * 256 ? 2 * 16 * (64 + 4) : 8 * 256;
 // Epilogue staging: a 32-row x 32-column chunk of 16-bit values (64-byte rows).
+// Long 16-bit reductions in a tensor-core launch stream their operands
+// through the (then idle) TMA ring with bulk copies: slots of kBulkSlotBytes
+// from kBulkOffset on (the first bytes hold the reduction scratch).
+constexpr int kBulkOffset = 16 * 1024;
+constexpr int kBulkSlotBytes = 16 * 1024;
+constexpr int kBulkMaxSlots = 12;
 constexpr int kEpiBufBytes = 32 * 64;
 constexpr int kBcastBytes = kMaxTileN * 2;   // one 16-bit row of a tile
 constexpr int kTmemCols = 2 * kMaxTileN;                // double-buffered accumulator

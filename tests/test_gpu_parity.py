@@ -330,6 +330,41 @@ def test_split_k_gemm_matches_oracle(k):
         np.testing.assert_allclose(got[1], want[1], rtol=1e-3)
 
 
+def test_long_reductions_stream_through_shared_memory():
+    # Long reductions over 16-bit operands in a tensor-core launch are
+    # bulk-copied through the idle TMA ring (one and two operands, row and
+    # column sums).  Each thread sums the same elements in the same order as
+    # the register-streaming loop that a CUDA-core launch runs, so the two
+    # agree bit for bit; both track the oracle within the summation bound.
+    T = TensorSpec.contiguous
+    R, C = 8192, 2048           # row parts of ~55 k elements, column parts of 256 rows
+    x, y = T("x", (R, C), "bfloat16"), T("y", (R, C), "bfloat16")
+    a, w = T("a", (128, 64), "bfloat16"), T("w", (128, 64), "bfloat16")
+    v = lambda n: T(n, (R, C), "bfloat16")
+    ops = [Operation("z", "mm", (a, w.T), T("z", (128, 128), "bfloat16")),
+           Operation("sq", "pow", (x, 2), v("sq")),
+           Operation("l", "mean", (v("sq"),), T("l", (), "float32")),
+           Operation("d", "sub", (x, y), v("d")),
+           Operation("cs", "sum", (v("d"),), T("cs", (C,), "bfloat16"), {"dims": (0,)}),
+           Operation("cx", "sum", (x,), T("cx", (C,), "float32"), {"dims": (0,)})]
+    outs = [T("z", (128, 128), "bfloat16"), T("l", (), "float32"), T("cs", (C,), "bfloat16"), T("cx", (C,), "float32")]
+    prog = Program([x, y, a, w], outs, ops)
+    arrays = [S.to_storage(S.normal(S.stream_seed(17, i), int(np.prod(t.shape))), t.dtype).reshape(t.shape)
+              for i, t in enumerate(prog.inputs)]
+    tc, st = run_step(prog, arrays)
+    simt, ss = run_step(prog, arrays, tensor_cores=0)
+    kinds = [t["kind"] for t in st.tasks()]
+    assert "gemm_tc" in kinds and "gemm_tc" not in [t["kind"] for t in ss.tasks()]
+    assert all(t["form"] == "compiled" for t in st.tasks() if t["kind"] in ("reduce_row", "reduce_col"))
+    for i in (1, 2, 3):
+        np.testing.assert_array_equal(tc[i], simt[i], err_msg=outs[i].buffer)
+    want = oracle.run_program(prog, values(arrays, prog))
+    xv, yv = [np.asarray(t, dtype=np.float64).reshape(R, C) for t in values(arrays, prog)[:2]]
+    check_op(ops[2], tc[1].reshape(1), np.asarray(want[1]).reshape(1), np.asarray([(xv * xv).sum() * 1.01]))
+    check_op(ops[4], tc[2], want[2], np.abs(xv - yv).sum(0) * 1.01)
+    check_op(ops[5], tc[3], want[3], np.abs(xv).sum(0))
+
+
 @pytest.mark.parametrize("dtype,k", [("float16", 1000), ("bfloat16", 256), ("float32", 72)])
 def test_one_row_gemv_matches_oracle(dtype, k):
     # batch 1: a warp per output; K not a multiple of the 256-element stride

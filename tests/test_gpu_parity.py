@@ -365,6 +365,31 @@ def test_long_reductions_stream_through_shared_memory():
     check_op(ops[5], tc[3], want[3], np.abs(xv).sum(0))
 
 
+def test_long_two_operand_row_sums_stream_through_shared_memory():
+    # Row sums of a difference (two 16-bit operands per slot) over 262144-long
+    # rows split into ~53 k-element parts: the bulk-copied form agrees bit for
+    # bit with the register loop of a CUDA-core launch and tracks the oracle.
+    T = TensorSpec.contiguous
+    R, C = 64, 262144
+    x, y = T("x", (R, C), "bfloat16"), T("y", (R, C), "bfloat16")
+    a, w = T("a", (128, 64), "bfloat16"), T("w", (128, 64), "bfloat16")
+    ops = [Operation("z", "mm", (a, w.T), T("z", (128, 128), "bfloat16")),
+           Operation("d", "sub", (x, y), T("d", (R, C), "bfloat16")),
+           Operation("rs", "sum", (T("d", (R, C), "bfloat16"),), T("rs", (R,), "float32"), {"dims": (1,)})]
+    outs = [T("z", (128, 128), "bfloat16"), T("rs", (R,), "float32")]
+    prog = Program([x, y, a, w], outs, ops)
+    arrays = [S.to_storage(S.normal(S.stream_seed(19, i), int(np.prod(t.shape))), t.dtype).reshape(t.shape)
+              for i, t in enumerate(prog.inputs)]
+    tc, st = run_step(prog, arrays)
+    simt, _ = run_step(prog, arrays, tensor_cores=0)
+    rows = [t for t in st.tasks() if t["kind"] == "reduce_row"]
+    assert rows and rows[0]["form"] == "compiled" and rows[0]["parts"] > 1
+    np.testing.assert_array_equal(tc[1], simt[1])
+    want = oracle.run_program(prog, values(arrays, prog))
+    xv, yv = [np.asarray(t, dtype=np.float64).reshape(R, C) for t in values(arrays, prog)[:2]]
+    check_op(ops[2], tc[1], want[1], np.abs(xv - yv).sum(1) * 1.01)
+
+
 @pytest.mark.parametrize("dtype,k", [("float16", 1000), ("bfloat16", 256), ("float32", 72)])
 def test_one_row_gemv_matches_oracle(dtype, k):
     # batch 1: a warp per output; K not a multiple of the 256-element stride

@@ -1,0 +1,12 @@
+// Entry point of the persistent kernel for programs with tensor-core GEMMs
+// (at most kSmallMaps TMA descriptors).
+#include "megakernel.cuh"
+#include "tk_kernel.h"
+
+namespace tkk {
+__global__ void __launch_bounds__(kThreads, 1) tk_persistent_tc_small(const __grid_constant__ ParamsTc<kSmallMaps> p) {
+  persistent_body(p.p, p.maps);
+}
+}  // namespace tkk
+
+const void* tk_kernel_fn_tc_small() { return reinterpret_cast<const void*>(&tkk::tk_persistent_tc_small); }

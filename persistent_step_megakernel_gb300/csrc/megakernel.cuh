@@ -1,4 +1,8 @@
-// The persistent training-step kernel for sm_103a (GB300).
+// The persistent training-step kernel for sm_103a (GB300): device code.
+//
+// This header holds the kernel body; kernel_plain.cu, kernel_tc_small.cu and
+// kernel_tc_large.cu each instantiate one entry point from it, so the three
+// variants compile in parallel.  launch.cu launches them.
 //
 // One cooperative launch runs a whole training step.  Every block walks the
 // device op table stage by stage; inside a stage the work items of all tasks
@@ -17,6 +21,8 @@
 // program's timeout records TK_ERR_BARRIER_TIMEOUT and the stage in the
 // workspace header, raises an abort flag and returns; blocks that see the
 // flag return too.
+#pragma once
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -24,9 +30,10 @@
 
 #include "../../include/tk.h"
 #include "tk_device.h"
-#include "tk_kernel.h"
 
 namespace tkk {
+// Internal linkage: every kernel translation unit holds its own copy.
+namespace {
 
 using namespace tkd;
 
@@ -2500,104 +2507,5 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) tk_persistent(const __grid_constant__ Params p) {
-  persistent_body(p, nullptr);
-}
-
-template <int NM>
-struct ParamsTc {
-  Params p;
-  CUtensorMap maps[NM];
-};
-
-template <int NM>
-__global__ void __launch_bounds__(kThreads, 1) tk_persistent_tc(const __grid_constant__ ParamsTc<NM> p) {
-  persistent_body(p.p, p.maps);
-}
-
-}  // namespace tkk
-
-// ------------------------------------------------------------ host side
-//
-// The tensor-core variant passes the TMA descriptors by value as
-// __grid_constant__ parameters; two capacities keep the parameter block small
-// for programs with few GEMMs.
-
-namespace {
-constexpr int kSmallMaps = 32;
-
-template <int NM>
-cudaError_t launch_tc(cudaLaunchConfig_t* cfg, const tkd::Params& params, const void* maps, int n_maps) {
-  static thread_local tkk::ParamsTc<NM> big;
-  big.p = params;
-  memcpy(big.maps, maps, size_t(n_maps) * sizeof(CUtensorMap));
-  return cudaLaunchKernelEx(cfg, tkk::tk_persistent_tc<NM>, big);
-}
 }  // namespace
-
-// Shared-memory carveout: ask for just the shared memory a launch needs so the
-// rest of the SM's unified L1/shared array stays L1 cache (spilled registers
-// and operand loads hit it).  Applied only when it changes for a kernel.
-template <typename K>
-cudaError_t set_carveout(K kernel, size_t dyn_smem, int* last) {
-  cudaFuncAttributes a;
-  cudaError_t e = cudaFuncGetAttributes(&a, kernel);
-  if (e != cudaSuccess) return e;
-  const size_t need = dyn_smem + a.sharedSizeBytes + 1024;
-  int pct = int((need * 100 + 233471) / 233472) + 1;  // of the largest carveout (228 KB)
-  pct = pct > 100 ? 100 : pct;
-  if (pct == *last) return cudaSuccess;
-  e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, pct);
-  if (e == cudaSuccess) *last = pct;
-  return e;
-}
-
-cudaError_t tk_kernel_launch(const tkd::Params& params, const void* maps, int n_maps, int grid, size_t dyn_smem,
-                             cudaStream_t stream) {
-  static int last_plain = -1, last_small = -1, last_big = -1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(tkd::kThreads);
-  cfg.dynamicSmemBytes = dyn_smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e;
-  if (!maps) {
-    e = set_carveout(tkk::tk_persistent, dyn_smem, &last_plain);
-    return e != cudaSuccess ? e : cudaLaunchKernelEx(&cfg, tkk::tk_persistent, params);
-  }
-  if (n_maps > tkd::kMaxMaps) return cudaErrorInvalidValue;
-  if (n_maps <= kSmallMaps) {
-    e = set_carveout(tkk::tk_persistent_tc<kSmallMaps>, dyn_smem, &last_small);
-    return e != cudaSuccess ? e : launch_tc<kSmallMaps>(&cfg, params, maps, n_maps);
-  }
-  e = set_carveout(tkk::tk_persistent_tc<tkd::kMaxMaps>, dyn_smem, &last_big);
-  return e != cudaSuccess ? e : launch_tc<tkd::kMaxMaps>(&cfg, params, maps, n_maps);
-}
-
-// The dynamic shared-memory limit is raised once to the largest any program
-// uses, so programs of different sizes can be launched in any order.
-cudaError_t tk_kernel_prepare(bool tc, size_t) {
-  if (!tc) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(tkk::tk_persistent_tc<kSmallMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       tkd::kDynSmemBudget);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(tkk::tk_persistent_tc<tkd::kMaxMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              tkd::kDynSmemBudget);
-}
-
-cudaError_t tk_kernel_occupancy(int* blocks_per_sm, bool tc, size_t dyn_smem) {
-  if (tc)
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, tkk::tk_persistent_tc<tkd::kMaxMaps>,
-                                                         tkd::kThreads, dyn_smem);
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, tkk::tk_persistent, tkd::kThreads, dyn_smem);
-}
-
-cudaError_t tk_kernel_attributes(cudaFuncAttributes* attr, bool tc) {
-  if (tc) return cudaFuncGetAttributes(attr, tkk::tk_persistent_tc<tkd::kMaxMaps>);
-  return cudaFuncGetAttributes(attr, tkk::tk_persistent);
-}
+}  // namespace tkk

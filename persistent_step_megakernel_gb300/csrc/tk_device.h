@@ -5,7 +5,7 @@
 // tasks into Stages; a grid barrier separates consecutive stages.  Each task
 // is cut into independent work items that blocks take round-robin.
 //
-// This header is plain data shared by planner.cpp and megakernel.cu.
+// This header is plain data shared by planner.cpp and the kernel (megakernel.cuh).
 #pragma once
 
 #include <stdint.h>

@@ -140,6 +140,9 @@ typedef struct {
                                   bit-identical results; 1 and 2 exist for testing. */
   int32_t split_k;             /* 1: split the K loop of under-filled tensor-core GEMMs over more
                                   SMs (partial sums, then a pass that adds them; default 1) */
+  int32_t tile_n;              /* N width of every tensor-core tile: 0 (default) picks 64, 128 or
+                                  256 per GEMM from its tile count and the SM count; 64, 128 or 256
+                                  forces that width (used by tests to reach each tile path) */
 } tk_options;
 
 /* What the planner decided (codegen.py `GeneratedKernel` counters). */
@@ -180,7 +183,7 @@ typedef struct {
   int32_t tile_m, tile_n;      /* GEMM tile (0 otherwise) */
   int32_t parts;               /* reduction parts (1 = not split) */
   int32_t staged_epilogue;     /* tensor-core GEMM whose epilogue moves tiles through shared memory */
-  int32_t reserved0;           /* 0 */
+  int32_t side_output;         /* GEMM that also writes a second value (a side output) from its tile */
   int64_t numel;               /* elements of the task's index space */
 } tk_task_info;
 
@@ -273,7 +276,9 @@ tk_status tk_plan_task(const tk_program* program, int32_t index, tk_task_info* i
  *   - the first call for a program's device performs set-up: it looks up the
  *     array's device address with that device current (which also makes the
  *     CUDA runtime load this library's device code there).  Make that first
- *     call before any stream capture;
+ *     call before any stream capture.  The address is kept with the device's
+ *     context; after a device reset the next call looks it up again (so make
+ *     that call outside a capture too);
  *   - every call shares the one array, which keeps the previous call's
  *     contents; each call clears the header (barrier counter, status word)
  *     with an asynchronous memset on `stream` before launching;

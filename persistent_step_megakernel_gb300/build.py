@@ -32,8 +32,26 @@ def _sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
+def _headers():
+    return (glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) +
+            [os.path.join(ROOT, "include", "tk.h")])
+
+
 def _deps():
-    return _sources() + glob.glob(os.path.join(CSRC, "*.h")) + [os.path.join(ROOT, "include", "tk.h")]
+    return _sources() + _headers()
+
+
+def _obj(src: str) -> str:
+    return os.path.join(BUILD, os.path.basename(src) + ".o")
+
+
+def _obj_stale(src: str) -> bool:
+    """An object is rebuilt when it is older than its source or any header."""
+    obj = _obj(src)
+    if not os.path.exists(obj):
+        return True
+    t = os.path.getmtime(obj)
+    return any(os.path.getmtime(p) > t for p in [src] + _headers())
 
 
 def _stale() -> bool:
@@ -43,8 +61,10 @@ def _stale() -> bool:
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src: str, verbose: bool, force: bool = True) -> str:
+    obj = _obj(src)
+    if not force and not _obj_stale(src):
+        return obj
     cmd = [nvcc(), "-std=c++17", "-O3", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include"), "-c", src, "-o", obj]
     if src.endswith(".cu"):
         cmd += ARCH + ["-lineinfo", "--fmad=false", "-Xptxas", "-v" if verbose else "-O3"]
@@ -62,7 +82,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
+        objs = list(ex.map(lambda s: _compile(s, verbose, force), srcs))
     tmp = LIB + f".{os.getpid()}.tmp"
     cmd = [nvcc(), "-shared", "-cudart", "shared"] + ARCH + ["-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)

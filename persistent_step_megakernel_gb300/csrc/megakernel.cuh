@@ -1445,6 +1445,7 @@ struct TcState {
   uint32_t slot_bytes;            // bytes per ring slot (A tile, then B tile)
   uint32_t full, empty;           // shared addresses of kStages mbarriers each
   uint32_t acc_full, acc_empty;   // 2 mbarriers each
+  uint32_t drain;                 // MMA completion after a failed wait (used once)
   uint32_t tmem;                  // TMEM base address
   uint32_t stg;                   // shared address of the epilogue staging area
   uint32_t stg_warp_bytes;        // staging bytes per epilogue warp
@@ -2147,9 +2148,16 @@ __device__ __forceinline__ void tc_epilogue_tile(const Ctx& c, const Task& t, in
 
 // Each role returns its updated ring/accumulator counter in the low 32 bits
 // and 1 << 32 if all its waits completed.
+//
+// After a wait gave up, a role still owns asynchronous work it started: TMA
+// copies into the ring (producer) and MMAs writing TMEM (MMA issuer).  Each
+// waits, again with the time limit, for that work to land before returning,
+// so that nothing arrives in shared memory or TMEM after the block has freed
+// them and exited.
 __device__ __noinline__ uint64_t tc_producer(const Ctx c, const Stage st, const CUtensorMap* maps, const TcState ts,
                                              uint32_t p_it) {
   bool ok = true;
+  const uint32_t p_it0 = p_it;
   asm volatile("fence.proxy.async.global;" ::: "memory");
   for_my_tiles(c, st, [&](const Task& t, const TileItem& it) {
     const uint32_t bytes = uint32_t(kStageBytesA + t.tile_n * kTileK * 2);
@@ -2182,6 +2190,14 @@ __device__ __noinline__ uint64_t tc_producer(const Ctx c, const Stage st, const 
     }
     return true;
   });
+  if (!ok) {
+    // the copies of the last (up to) kStages slots this stage armed: each
+    // completes its slot's current "full" phase (a slot is re-armed only
+    // after its previous phase was consumed, so that phase is still the one
+    // with this parity)
+    const uint32_t first = p_it - min(p_it - p_it0, uint32_t(kStages));
+    for (uint32_t i = first; i < p_it; ++i) mbar_wait(ts.full + 8 * (i % kStages), (i / kStages) & 1u, c.timeout_ns);
+  }
   return (uint64_t(ok) << 32) | p_it;
 }
 
@@ -2217,6 +2233,11 @@ __device__ __noinline__ uint64_t tc_mma(const Ctx c, const Stage st, const TcSta
     ++m_tile;
     return true;
   });
+  if (!ok) {
+    // every MMA this thread issued completes before the drain barrier's phase
+    umma_commit(ts.drain);
+    mbar_wait(ts.drain, 0, c.timeout_ns);
+  }
   *m_tile_io = m_tile;
   return (uint64_t(ok) << 32) | m_it;
 }
@@ -2375,7 +2396,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   __shared__ __align__(16) Ref s_refs[kStageRefs];
   __shared__ Stage s_stage;
   __shared__ Prep s_prep[kThreads / 32];
-  __shared__ __align__(8) uint64_t s_bar[2 * kStages + 4];
+  __shared__ __align__(8) uint64_t s_bar[2 * kStages + 5];
   __shared__ __align__(8) uint64_t s_bulk_bar[kBulkMaxSlots];
   __shared__ uint32_t s_bulk_it;
   __shared__ __align__(8) uint64_t s_col_bar[kBulkMaxSlots];
@@ -2403,6 +2424,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     ts.empty = smem_u32(&s_bar[kStages]);
     ts.acc_full = smem_u32(&s_bar[2 * kStages]);
     ts.acc_empty = smem_u32(&s_bar[2 * kStages + 2]);
+    ts.drain = smem_u32(&s_bar[2 * kStages + 4]);
     if (threadIdx.x == 0) {
       for (int i = 0; i < kStages; ++i) {
         mbar_init(ts.full + 8 * i, 1);
@@ -2412,6 +2434,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
         mbar_init(ts.acc_full + 8 * i, 1);
         mbar_init(ts.acc_empty + 8 * i, 4);
       }
+      mbar_init(ts.drain, 1);
       for (int i = 0; i < kBulkMaxSlots; ++i) {
         mbar_init(smem_u32(&s_bulk_bar[i]), 1);
         mbar_init(smem_u32(&s_col_bar[i]), kThreads);

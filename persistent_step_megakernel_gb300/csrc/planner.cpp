@@ -496,8 +496,9 @@ class Planner {
   }
 
   // Side outputs (a GB300 addition in the spirit of the page's side
-  // epilogues): a fused GEMM whose final value has several users also writes
-  // one of them from the same tile when that user is a one-operand pointwise
+  // epilogues): a fused GEMM whose final value is stored and read again (it
+  // has several users, or it is returned and has a user) also writes one of
+  // those users from the same tile when that user is a one-operand pointwise
   // op of the final value (e.g. the loss gradient 2/N * d next to d) and would
   // be stored anyway (a GEMM operand, a returned value or a value with several
   // users).  Not for in-place outputs.
@@ -507,7 +508,7 @@ class Planner {
       if (!is_mm(mm.kind)) continue;
       const int fin = kv.second.final_buf;
       const Buf& fb = bufs_.at(fin);
-      if (fb.users.size() < 2) continue;
+      if (fb.users.empty() || (fb.users.size() < 2 && !output_buffers_.count(fin))) continue;
       for (int u : fb.users) {
         const OpInfo& op = ops_[u];
         if (!is_pointwise(op.kind) || op.kind == TK_OP_FULL || fused_skip_.count(op.out.buffer_id)) continue;
@@ -1396,7 +1397,7 @@ class Planner {
     const int64_t M = t.m, N = t.n, K = t.k;
     if (M < 1 || N < 1 || K < 1) return false;
     if (plan.tma.size() + 2 > size_t(tkd::kMaxMaps)) return false;
-    // widest N tile that still spreads the tiles over the SMs
+    // widest N tile that still spreads the tiles over the SMs (or the forced width)
     int bn = 64;
     for (int cand : {256, 128}) {
       if (ceil_div(M, tkd::kTileM) * ceil_div(N, cand) >= (cand == 256 ? sms_ : sms_ / 2)) {
@@ -1404,6 +1405,7 @@ class Planner {
         break;
       }
     }
+    if (opt_.tile_n > 0) bn = opt_.tile_n;
     TmaOperand ta, tb;
     int a_mn = 0, b_mn = 0;
     if (!tma_operand(A, true, tkd::kTileM, &ta, &a_mn) || !tma_operand(B, false, bn, &tb, &b_mn)) return false;

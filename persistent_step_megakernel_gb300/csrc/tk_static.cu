@@ -13,6 +13,7 @@
 // The array is a file-scope static device variable, so every GPU on which this
 // library's device code is loaded holds TK_STATIC_WORKSPACE_ELEMENTS floats
 // (8 MiB) of it until the process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -34,7 +35,29 @@ namespace {
 
 constexpr int kMaxDevices = 256;
 std::mutex g_mutex;
-void* g_address[kMaxDevices] = {};  // device address of the array, per device
+// Device address of the array, per device, with the context it was looked up
+// in: a device reset (or a torn-down and recreated primary context) gives the
+// device a new context, in which the old address is meaningless.
+struct Slot {
+  CUcontext ctx = nullptr;
+  void* address = nullptr;
+};
+Slot g_slot[kMaxDevices];
+
+// cuCtxGetCurrent from the driver, through the runtime's entry-point query
+// (the library does not link the driver library directly).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<CtxGetCurrentFn>(p);
+    return static_cast<CtxGetCurrentFn>(nullptr);
+  }();
+  return fn;
+}
 
 }  // namespace
 
@@ -53,24 +76,32 @@ extern "C" tk_status tk_run_static(tk_program* program, const void* const* input
                                             std::to_string(TK_STATIC_WORKSPACE_ELEMENTS) +
                                             " (8 MiB); use tk_run with a caller-allocated workspace");
 
-  // Set-up, once per device: the host-side name of the array is not a device
-  // address, so look the address up with that device current.
+  // Set-up, once per device (and again if the device's context changed): the
+  // host-side name of the array is not a device address, so look the address
+  // up with that device current.
   void* ws = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_address[device]) {
-      int prev = -1;
-      if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
-      cudaError_t e = cudaSetDevice(device);
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    cudaError_t e = cudaSetDevice(device);
+    CUcontext ctx = nullptr;
+    CtxGetCurrentFn get = ctx_get_current();
+    if (e == cudaSuccess && (!get || get(&ctx) != CUDA_SUCCESS)) e = cudaErrorUnknown;
+    Slot& slot = g_slot[device];
+    if (e == cudaSuccess && (!slot.address || slot.ctx != ctx)) {
       void* ptr = nullptr;
-      if (e == cudaSuccess) e = cudaGetSymbolAddress(&ptr, tk_static_workspace);
-      if (prev >= 0) cudaSetDevice(prev);
-      if (e != cudaSuccess)
-        return tkapi_fail(TK_ERR_CUDA,
-                          std::string("cudaGetSymbolAddress(built-in workspace): ") + cudaGetErrorString(e));
-      g_address[device] = ptr;
+      e = cudaGetSymbolAddress(&ptr, tk_static_workspace);
+      if (e == cudaSuccess) {
+        slot.address = ptr;
+        slot.ctx = ctx;
+      }
     }
-    ws = g_address[device];
+    if (prev >= 0 && prev != device) cudaSetDevice(prev);
+    if (e != cudaSuccess)
+      return tkapi_fail(TK_ERR_CUDA,
+                        std::string("set-up of the built-in workspace (cudaGetSymbolAddress): ") + cudaGetErrorString(e));
+    ws = slot.address;
   }
 
   // The array keeps whatever the previous call left; the header (barrier

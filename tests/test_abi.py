@@ -39,7 +39,24 @@ def test_options_defaults():
     assert o.barrier_timeout_s == 2.0
 
 
-def test_struct_sizes_match_the_header():
-    assert ctypes.sizeof(B.tk_tensor_spec) == 88
-    assert ctypes.sizeof(B.tk_op) == 448
-    assert ctypes.sizeof(B.tk_options) == 48
+STRUCTS = ("tk_tensor_spec", "tk_op", "tk_program_desc", "tk_options", "tk_plan_stats", "tk_task_info")
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    # a C compiler's view of the header: size of every struct and offset of every field
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "tk.h"', "int main(void) {"]
+    for name in STRUCTS:
+        lines.append(f'  printf("{name} %zu\\n", sizeof({name}));')
+        for field, _ in getattr(B, name)._fields_:
+            lines.append(f'  printf("{name}.{field} %zu\\n", offsetof({name}, {field}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    c = dict(l.split() for l in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.splitlines())
+    for name in STRUCTS:
+        cls = getattr(B, name)
+        assert int(c[name]) == ctypes.sizeof(cls), name
+        for field, _ in cls._fields_:
+            assert int(c[f"{name}.{field}"]) == getattr(cls, field).offset, f"{name}.{field}"

@@ -21,72 +21,15 @@ from persistent_step_megakernel_gb300 import synthetic as S
 from persistent_step_megakernel_gb300.build import build
 from persistent_step_megakernel_gb300.ir import Operation, Program, TensorSpec
 from persistent_step_megakernel_gb300.runtime import TrainStep
-from tests._util import to_f64, to_torch, ulp_distance, ulp_of, values
+from tests._gpu import check_op, run_step, teacher_forced
+from tests._util import to_f64, to_torch, ulp_distance, values
 
 pytestmark = pytest.mark.gpu
-U32 = 2.0 ** -24
 
 
 @pytest.fixture(scope="module", autouse=True)
 def _built():
     build()
-
-
-def run_step(program, arrays, steps=1, **opts):
-    step = TrainStep(program, 0, **opts)
-    ins = [to_torch(a, s.dtype, "cuda") for a, s in zip(arrays, program.inputs)]
-    outs, ws = step.allocate(ins)
-    for _ in range(steps):
-        step.run(ins, outs, ws)
-    torch.cuda.synchronize()
-    status, stage = step.status(ws)
-    assert status == 0, f"device status {status} at stage {stage}"
-    return [to_f64(o) for o in outs], step
-
-
-def check_op(op, got, want, bound):
-    dt = op.output.dtype
-    got, want = np.asarray(got), np.asarray(want)
-    if op.op in ("mm", "addmm"):
-        k = op.inputs[-1].shape[0]
-    elif op.op in ("sum", "mean"):
-        src = op.inputs[0]
-        k = max(1, int(np.prod(src.shape)) // max(1, int(np.prod(op.output.shape)) if op.output.shape else 1))
-    else:
-        bad = ulp_distance(got, want, dt) != 0
-        assert not bad.any(), (op.name, got[bad][:5], want[bad][:5])
-        return 0
-    err = np.abs(got - want)
-    accum = 1.01 * k * U32 * np.asarray(bound)
-    if op.op == "mean":
-        accum = accum / max(k, 1)
-    if dt == "float32":
-        ok = (err <= 1e-5 + 1e-4 * np.abs(want)) | (err <= accum + ulp_of(want, dt))
-    else:
-        ok = (ulp_distance(got, want, dt) <= 2) | (err <= accum + ulp_of(want, dt))
-    nan_ok = np.isnan(got) & np.isnan(want)
-    ok = ok | nan_ok
-    assert ok.all(), (op.name, got[~ok][:5], want[~ok][:5], accum[~ok][:5])
-    return int(ulp_distance(got, want, dt).max()) if dt != "float32" else 0
-
-
-def teacher_forced(program, arrays, gpu_outs, sample=4096, seed=0):
-    """Every op of an all-outputs program against the oracle on GPU operands."""
-    rng = np.random.default_rng(seed)
-    o = oracle.Oracle(program)
-    for s, v in zip(program.inputs, values(arrays, program)):
-        o.set(s.buffer, v)
-    got_by_buf = {}
-    for s, v in zip(program.outputs, gpu_outs):
-        got_by_buf.setdefault(s.buffer, v)
-        o.set(s.buffer, v)
-    worst = 0
-    for i, op in enumerate(program.operations):
-        g = got_by_buf[op.output.buffer].reshape(-1)
-        idx = np.arange(g.size) if g.size <= 2 * sample else np.sort(rng.choice(g.size, sample, replace=False))
-        want, bound = o.eval_op_sampled(i, idx)
-        worst = max(worst, check_op(op, g[idx], want, bound))
-    return worst
 
 
 SMALL = {

@@ -1,20 +1,34 @@
 #!/usr/bin/env python3
 """Benchmark: one functional MLP training step = one persistent-kernel launch.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c5] [--impl ours|reference]
+                    [--stage-profile] [--launches-only]
 
-Prints ONE JSON line.  `value` is whole-job steps/s from CUDA-event device time
-of exactly K steps (an L2 flush -- a write of a buffer larger than L2 -- runs
-between timed steps, outside the events).  `e2e` repeats the metric through the
-public API with host-resident batches: each step copies x (and y) from pinned
-host memory, runs the step and reads the loss back.  With N > 1 each rank runs
-an independent replica on its own GPU (the step has no data-parallel exchange),
-times are max-reduced over ranks and `value` sums the replicas.
+Prints ONE JSON line for the headline workload (the GEMM-bound bf16 step, the
+largest of the workloads; --config picks another).  `value` is whole-job
+steps/s from the CUDA-event device time of exactly K single-step launches with
+an L2 flush (a write of a buffer larger than L2) between them, outside the
+events.  Beside it, for the headline and every other workload:
+  * back_to_back: batches of launches on one stream with the state fed back
+    (in-place updates), median of >= 5 batches;
+  * graph: the same batches captured once as a CUDA graph and replayed,
+    median of >= 5 replays (the pages time graph-captured steps);
+  * clocks: nvidia-smi samples taken while that workload's timed loops ran.
+`e2e` repeats the metric through the public API with host-resident batches:
+each step copies x (and y) from pinned host memory, runs the step and reads
+the loss back.  With N > 1 each rank runs an independent replica on its own
+GPU (the step has no data-parallel exchange), times are max-reduced over ranks
+and `value` sums the replicas.
 
 --impl reference times the CPU oracle (the method's plain restatement) on the
-host cores instead: each timed step evaluates a uniform random fraction of every
-op's outputs, sized so the run stays within a few minutes, and the throughput
-is scaled back to whole steps.
+host cores instead: each timed step evaluates a uniform random fraction of
+every op's outputs, sized so the run stays within a few minutes, and the
+throughput is scaled back to whole steps.
+
+--stage-profile prints the per-stage timing of one step (work and grid-barrier
+time per stage, from the kernel's %globaltimer stamps) instead.
+--launches-only runs W + K launches of the workload and nothing else (for
+profilers).
 """
 from __future__ import annotations
 
@@ -37,6 +51,8 @@ METRIC = "MLP train steps/sec (µs/step, device-timed) and % of roofline on 1 GB
 UNIT = "steps/s"
 L2_FLUSH_BYTES = 256 << 20           # > 129 MB L2
 KERNEL = "tk_persistent"
+HEADLINE = "c5"                      # the largest workload
+DTYPE_TAG = {"float32": "f32", "bfloat16": "bf16", "float16": "f16"}
 
 
 def peaks():
@@ -93,11 +109,12 @@ class Clocks:
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_power_cap,utilization.gpu")
 
     def __init__(self, gpu: int):
         self.gpu = gpu
         self.proc = None
+        self.lines = []
 
     def __enter__(self):
         try:
@@ -110,7 +127,6 @@ class Clocks:
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
             time.sleep(0.05)
             self.proc.terminate()
@@ -121,24 +137,35 @@ class Clocks:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        sm, mx, power, reasons, busy = [], [], [], set(), 0
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in getattr(self, "lines", []):
+        for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 7:
+            if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                util = float(parts[7])
+                clock, top = float(parts[0]), float(parts[1])
             except ValueError:
                 continue
+            if util <= 0:
+                continue                      # idle sample (before or after the loop)
+            busy += 1
+            sm.append(clock)
+            mx.append(top)
+            try:
+                power.append(float(parts[2]))
+            except ValueError:
+                pass
             for n, v in zip(names, parts[3:7]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "samples_total": len(self.lines)}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": busy, "samples_total": len(self.lines),
+                "power_w_max": max(power) if power else None}
 
 
 def dist_setup(world: int, backend: str = "nccl"):
@@ -183,45 +210,121 @@ def device_inputs(cfg, prog, device):
     return out
 
 
-def time_device(cfg, steps, warmup, device, dist, clocks_gpu=None):
-    """Mean device µs/step over exactly `steps` launches, plus status and plan stats."""
+def input_bytes(cfg) -> int:
+    prog = S.mlp_step_program(cfg, export="state")
+    size = {"float32": 4, "float16": 2, "bfloat16": 2}
+    total = 0
+    for s in prog.inputs:
+        n = 1
+        for d in s.shape:
+            n *= d
+        total += n * size[s.dtype]
+    return total
+
+
+def batch_steps_for(cfg) -> int:
+    """Steps per back-to-back batch: 100, or 20 for steps above a millisecond."""
+    return 20 if cfg.flops() > 1e11 else 100
+
+
+def setup(cfg, device, **options):
     import torch
     from persistent_step_megakernel_gb300.runtime import TrainStep
     prog = S.mlp_step_program(cfg, export="state")
-    step = TrainStep(prog, device.index)
+    step = TrainStep(prog, device.index, **options)
     ins = device_inputs(cfg, prog, device)
     outs, ws = step.allocate(ins)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
+    return {"prog": prog, "step": step, "ins": ins, "outs": outs, "ws": ws, "stream": stream,
+            "launch": step.launcher(ins, outs, ws, stream)}
+
+
+def measure(cfg, device, dist, steps, warmup, batches, batch_steps, graph=True, clocks_gpu=None):
+    """Device µs/step of the timed program three ways; the launches counted."""
+    import torch
+    ctx = setup(cfg, device)
+    launch, stream = ctx["launch"], ctx["stream"]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     for _ in range(warmup):
-        step.run(ins, outs, ws)
+        launch()
         flush.zero_()
     torch.cuda.synchronize(device)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ev = lambda: torch.cuda.Event(enable_timing=True)
     clocks = Clocks(clocks_gpu) if clocks_gpu is not None else None
+    launches = 0
     barrier(dist)
     torch.cuda.synchronize(device)
     if clocks:
         clocks.__enter__()
+    # 1. single steps, L2 flushed between them (the headline value)
+    starts, ends = [ev() for _ in range(steps)], [ev() for _ in range(steps)]
     for k in range(steps):
         starts[k].record(stream)
-        step.run(ins, outs, ws)
+        launch()
         ends[k].record(stream)
         flush.zero_()
+    launches += steps
+    torch.cuda.synchronize(device)
+    flushed = [1e3 * s.elapsed_time(e) for s, e in zip(starts, ends)]
+    # 2. back-to-back batches with the state fed back
+    b2b = []
+    for _ in range(batches):
+        flush.zero_()
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(batch_steps):
+            launch()
+        b.record(stream)
+        launches += batch_steps
+        torch.cuda.synchronize(device)
+        b2b.append(1e3 * a.elapsed_time(b) / batch_steps)
+    # 3. the batch captured as one CUDA graph, replayed
+    graph_res = None
+    if graph:
+        graph_res = {}
+        try:
+            side = torch.cuda.Stream(device)
+            side.wait_stream(stream)
+            glaunch = ctx["step"].launcher(ctx["ins"], ctx["outs"], ctx["ws"], side)
+            with torch.cuda.stream(side):
+                glaunch()
+            torch.cuda.synchronize(device)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(batch_steps):
+                    glaunch()
+            g.replay()
+            torch.cuda.synchronize(device)
+            reps = []
+            for _ in range(batches):
+                flush.zero_()
+                a, b = ev(), ev()
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+                launches += batch_steps
+                torch.cuda.synchronize(device)
+                reps.append(1e3 * a.elapsed_time(b) / batch_steps)
+            graph_res = {"us_median": statistics.median(reps), "us_samples": reps, "steps_per_replay": batch_steps}
+            del g
+        except Exception as e:  # reported, not fatal: the other timings stand
+            graph_res = {"error": f"{type(e).__name__}: {e}"[:300]}
     torch.cuda.synchronize(device)
     barrier(dist)
     if clocks:
         clocks.__exit__(None, None, None)
-    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    status = step.status(ws)
-    return {"us_mean": 1e3 * sum(ms) / len(ms), "us_median": 1e3 * statistics.median(ms),
-            "us_min": 1e3 * min(ms), "status": status, "stats": step.stats,
-            "resources": step.resource_usage(), "clocks": clocks.summary() if clocks else None,
-            "step": step, "ins": ins, "outs": outs, "ws": ws, "prog": prog}
+    status = ctx["step"].status(ctx["ws"])
+    ctx.update({
+        "status": status, "stats": ctx["step"].stats, "resources": ctx["step"].resource_usage(),
+        "clocks": clocks.summary() if clocks else None, "launches": launches,
+        "flushed": {"us_mean": statistics.mean(flushed), "us_median": statistics.median(flushed),
+                    "us_min": min(flushed), "steps": steps},
+        "back_to_back": {"us_median": statistics.median(b2b), "us_samples": b2b, "steps_per_batch": batch_steps},
+        "graph": graph_res})
+    return ctx
 
 
-def time_e2e(cfg, ctx, steps, device):
+def time_e2e(ctx, steps, device):
     """Through the public API with host batches: H2D x(,y) -> step -> D2H loss."""
     import torch
     step, ins, outs, ws, prog = ctx["step"], ctx["ins"], ctx["outs"], ctx["ws"], ctx["prog"]
@@ -232,97 +335,160 @@ def time_e2e(cfg, ctx, steps, device):
     stream = torch.cuda.current_stream(device)
     h2d = sum(host[i].numel() * host[i].element_size() for i in batch)
     d2h = loss_host.numel() * loss_host.element_size()
-    for _ in range(3):
+
+    def one():
         for i in batch:
             ins[i].copy_(host[i], non_blocking=True)
         step.run(ins, outs, ws)
         loss_host.copy_(outs[0], non_blocking=True)
         stream.synchronize()
+
+    for _ in range(3):
+        one()
     t0 = time.perf_counter()
     for _ in range(steps):
-        for i in batch:
-            ins[i].copy_(host[i], non_blocking=True)
-        step.run(ins, outs, ws)
-        loss_host.copy_(outs[0], non_blocking=True)
-        stream.synchronize()
+        one()
     dt = time.perf_counter() - t0
     return steps / dt, h2d, d2h
 
 
-def oracle_steps_per_s(cfg, seconds=10.0):
-    """The oracle as it stands, whole steps on the host cores, for ~`seconds`."""
+# ------------------------------------------------------------ the oracle
+
+def oracle_sampled(cfg, seconds: float, steps: int, warmup: int, seed: int = 0):
+    """The oracle as it stands on a bounded sample of whole steps.
+
+    Each sampled step evaluates, for every op, the same uniform random
+    fraction of its outputs (at least one output); the operand buffers are
+    primed with a constant (the timing of the oracle's loops does not depend on
+    the values), so no full step has to run first.  Each op's time is scaled
+    by its outputs / evaluated outputs, and the sum is one whole step.
+    Returns (whole steps/s, fraction, threads)."""
+    import numpy as np
     import oracle
     prog = S.mlp_step_program(cfg, export="state")
     arrays = S.mlp_inputs(cfg, prog)
-    vals = [S.storage_to_float64(a, s.dtype) for a, s in zip(arrays, prog.inputs)]
     o = oracle.Oracle(prog)
-    o.set_inputs(vals)
-    n, t0 = 0, time.perf_counter()
-    while True:
-        o.run()
-        n += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": n / dt, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
-            "sample": f"{n} whole {cfg.key} steps (all ops, all elements) in {dt:.1f} s on the host cores"}
+    o.set_inputs([S.storage_to_float64(a, s.dtype) for a, s in zip(arrays, prog.inputs)])
+    have = {s.buffer for s in prog.inputs}
+    for op in prog.operations:
+        if op.output.buffer not in have:
+            n = int(np.prod(op.output.shape)) if op.output.shape else 1
+            o.set(op.output.buffer, np.full(n, 0.5))
+            have.add(op.output.buffer)
+    rng = np.random.default_rng(seed)
+    sizes = [int(np.prod(op.output.shape)) if op.output.shape else 1 for op in prog.operations]
+
+    def sampled_step(frac):
+        """Seconds per op scaled to all of its outputs."""
+        full = []
+        for i, n in enumerate(sizes):
+            k = max(1, int(round(frac * n)))
+            idx = np.arange(n) if k >= n else np.sort(rng.choice(n, k, replace=False))
+            t0 = time.perf_counter()
+            o.eval_op_sampled(i, idx)
+            full.append((time.perf_counter() - t0) * n / min(k, n))
+        return sum(full)
+
+    # calibrate on a small sample, then aim at `seconds` of sampled work in total
+    frac = min(1.0, 64.0 / max(sizes))
+    t0 = time.perf_counter()
+    est = sampled_step(frac)
+    while time.perf_counter() - t0 < 0.2 and frac < 1.0:
+        frac = min(1.0, frac * 8)
+        t0 = time.perf_counter()
+        est = sampled_step(frac)
+    frac = min(1.0, frac * seconds / max(1, steps + warmup) / max(1e-9, time.perf_counter() - t0))
+    for _ in range(warmup):
+        sampled_step(frac)
+    whole = [sampled_step(frac) for _ in range(steps)]
+    return 1.0 / statistics.mean(whole), frac, oracle.threads()
+
+
+def cpu_baseline(cfg, seconds=15.0):
+    value, frac, threads = oracle_sampled(cfg, seconds, steps=5, warmup=1)
+    return {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"5 {cfg.key} steps, each evaluating a {frac:.3g} fraction of every op's outputs "
+                      f"(uniform random indices, ~{seconds:.0f} s on the host cores); scaled to whole steps"}
 
 
 def run_reference(args, rank, world):
     """The oracle on host cores as the reference arm (rank 0 only)."""
     if rank != 0:
         return 0
-    import numpy as np
-    import oracle
     cfg = S.CONFIGS[args.config]
-    prog = S.mlp_step_program(cfg, export="state")
-    arrays = S.mlp_inputs(cfg, prog)
-    o = oracle.Oracle(prog)
-    o.set_inputs([S.storage_to_float64(a, s.dtype) for a, s in zip(arrays, prog.inputs)])
-    t0 = time.perf_counter()
-    o.run()                                    # one whole step: all buffers exist
-    t_full = time.perf_counter() - t0
-    budget = 90.0
-    frac = min(1.0, budget / max(1e-9, (args.steps + args.warmup) * t_full))
-    rng = np.random.default_rng(0)
-    sizes = [int(np.prod(op.output.shape)) if op.output.shape else 1 for op in prog.operations]
-
-    def sampled_step():
-        for i, n in enumerate(sizes):
-            k = max(1, int(round(frac * n)))
-            idx = np.arange(n) if k >= n else rng.choice(n, k, replace=False)
-            o.eval_op_sampled(i, idx)
-
-    for _ in range(args.warmup):
-        sampled_step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        sampled_step()
-    dt = time.perf_counter() - t0
-    value = frac * args.steps / dt
+    value, frac, threads = oracle_sampled(cfg, 90.0, args.steps, args.warmup)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / value, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": {"float32": "f32", "bfloat16": "bf16",
-                                                                "float16": "f16"}[cfg.dtype],
+            "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_TAG[cfg.dtype],
             "data": "synthetic", "config": {"workload": cfg.description, "global_batch": cfg.batch * world,
                                             "dims": list(cfg.dims), "l2": "n/a (CPU)"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
-                             "sample": f"each step evaluates a {frac:.4f} fraction of every op's outputs "
-                                       f"(uniform random indices); throughput scaled to whole steps"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"each step evaluates a {frac:.3g} fraction of every op's outputs "
+                                       f"(uniform random indices, operands primed); throughput scaled to "
+                                       f"whole steps"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
 
 
+# ------------------------------------------------------------ modes
+
+def stage_profile(cfg, device, warmup=5):
+    """Per-stage work and barrier time of one step (L2 flushed before it)."""
+    import torch
+    from persistent_step_megakernel_gb300.runtime import TrainStep
+    prog = S.mlp_step_program(cfg, export="state")
+    step = TrainStep(prog, device.index, profile=1)
+    ins = device_inputs(cfg, prog, device)
+    outs, ws = step.allocate(ins)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    runs = []
+    for k in range(warmup + 3):
+        flush.zero_()
+        step.run(ins, outs, ws)
+        torch.cuda.synchronize(device)
+        if k >= warmup:
+            runs.append(step.profile(ws))
+    best = min(runs, key=lambda r: r["total_us"])
+    per_stage = {}
+    for t in step.tasks():
+        per_stage.setdefault(t["stage"], []).append(
+            f"{t['kind']}:{t['op'] or 'copy'}" + (f"[{t['m']}x{t['n']}x{t['k']}/{t['tile_n']}]" if t["m"] else ""))
+    stages = [{"stage": s, "work_us": round(w, 2), "barrier_us": round(best["barrier_us"][s], 2)
+               if s < len(best["barrier_us"]) else None, "tasks": per_stage.get(s, [])}
+              for s, w in enumerate(best["work_us"])]
+    bars = best["barrier_us"]
+    return {"workload": cfg.description, "key": cfg.key, "grid_blocks": step.stats["grid_blocks"],
+            "stages": stages, "total_us": best["total_us"], "prologue_us": best["prologue_us"],
+            "barrier_us_median": statistics.median(bars) if bars else None,
+            "barrier_us_max": max(bars) if bars else None, "status": step.status(ws)}
+
+
+def config_record(cfg, m):
+    flushed_us = m["flushed"]["us_mean"]
+    return {"us_per_step": flushed_us, "status": m["status"][0],
+            "roofline": roofline(cfg, flushed_us * 1e-6, traffic_from_profiles(cfg.key)),
+            "back_to_back_us": m["back_to_back"]["us_median"],
+            "graph_us": (m["graph"] or {}).get("us_median"),
+            "graph_error": (m["graph"] or {}).get("error"),
+            "stages": m["stats"]["stages"], "grid_barriers": m["stats"]["grid_barriers"],
+            "tensor_core_ops": m["stats"]["tensor_core_ops"],
+            "steps": m["flushed"]["steps"], "clocks": m["clocks"], "gpu_launches": m["launches"]}
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
-    ap.add_argument("--warmup", type=int, default=30)
-    ap.add_argument("--config", default="c2", choices=sorted(S.CONFIGS))
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default=HEADLINE, choices=sorted(S.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-others", action="store_true", help="skip the other configs' µs/step")
+    ap.add_argument("--batches", type=int, default=5, help="back-to-back batches and graph replays (>= 5)")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-others", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stage-profile", action="store_true", help="print per-stage timing of one step")
+    ap.add_argument("--launches-only", action="store_true", help="W + K launches and nothing else")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -343,50 +509,60 @@ def main() -> int:
     device = torch.device("cuda", local)
     cfg = S.CONFIGS[args.config]
 
-    r = time_device(cfg, args.steps, args.warmup, device, dist, clocks_gpu=local)
-    if r["status"][0] != 0:
-        raise SystemExit(f"device status {r['status']}")
-    us = allmax(dist, r["us_mean"], device)
-    e2e_value, h2d, d2h = time_e2e(cfg, r, min(args.steps, 500), device)
-    e2e_value = allmax(dist, 1.0 / e2e_value, device)
-    e2e_value = world / e2e_value
+    if args.launches_only:
+        ctx = setup(cfg, device)
+        for _ in range(args.warmup + args.steps):
+            ctx["launch"]()
+        torch.cuda.synchronize(device)
+        status = ctx["step"].status(ctx["ws"])
+        print(json.dumps({"launches": args.warmup + args.steps, "workload": cfg.key, "status": status}))
+        return 0 if status[0] == 0 else 1
+    if args.stage_profile:
+        print(json.dumps(stage_profile(cfg, device)))
+        return 0
+
+    m = measure(cfg, device, dist, args.steps, args.warmup, max(5, args.batches), batch_steps_for(cfg),
+                graph=not args.no_graph, clocks_gpu=local)
+    if m["status"][0] != 0:
+        raise SystemExit(f"device status {m['status']}")
+    us = allmax(dist, m["flushed"]["us_mean"], device)
+    e2e_value, h2d, d2h = time_e2e(m, min(args.steps, 300), device)
+    e2e_value = world / allmax(dist, 1.0 / e2e_value, device)
     value = replica_value(us, world)
+    in_mb = input_bytes(cfg) / 1e6
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": {"float32": "f32", "bfloat16": "bf16", "float16": "f16"}[cfg.dtype],
-        "data": "synthetic",
+        "vs_baseline": None, "dtype": DTYPE_TAG[cfg.dtype], "data": "synthetic",
         "config": {"workload": cfg.description, "global_batch": cfg.batch * world, "dims": list(cfg.dims),
                    "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "flushed between timed steps (256 MiB write)"},
-        "us_per_step": {"mean": us, "median": r["us_median"], "min": r["us_min"]},
+                   "l2": f"flushed between timed steps (256 MiB write); inputs {in_mb:.1f} MB"},
+        "us_per_step": {"mean": us, "median": m["flushed"]["us_median"], "min": m["flushed"]["us_min"],
+                        "back_to_back_median": m["back_to_back"]["us_median"],
+                        "graph_median": (m["graph"] or {}).get("us_median")},
+        "back_to_back": m["back_to_back"], "graph": m["graph"],
         "roofline": roofline(cfg, us * 1e-6, traffic_from_profiles(cfg.key)),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps,
+        "gpu_launches": m["launches"],
         "kernel": KERNEL,
-        "plan": {k: r["stats"][k] for k in ("stages", "grid_barriers", "grid_blocks", "fused_epilogues",
+        "plan": {k: m["stats"][k] for k in ("stages", "grid_barriers", "grid_blocks", "fused_epilogues",
                                              "inlined_ops", "tensor_core_ops", "materialized_ops")},
-        "resources": r["resources"],
-        "clocks": r["clocks"],
+        "resources": m["resources"],
+        "clocks": m["clocks"],
     }
-    line["us_per_barrier_upper_bound"] = us / max(1, r["stats"]["grid_barriers"])
-    del r
+    del m
     if not args.no_others and rank == 0:
         others = {}
         for key, c in S.CONFIGS.items():
             if key == cfg.key:
                 continue
-            k = 200 if c.flops() < 1e10 else 20
-            o = time_device(c, k, 5, device, None)
-            others[key] = {"us_per_step": o["us_mean"], "status": o["status"][0],
-                           "roofline": roofline(c, o["us_mean"] * 1e-6, traffic_from_profiles(key)),
-                           "stages": o["stats"]["stages"], "tensor_core_ops": o["stats"]["tensor_core_ops"],
-                           "steps": k, "warmup": 5}
+            k = 100 if c.flops() > 1e11 else 300
+            o = measure(c, device, None, k, 5, 5, batch_steps_for(c), graph=not args.no_graph, clocks_gpu=local)
+            others[key] = config_record(c, o)
             del o
         line["other_configs"] = others
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = oracle_steps_per_s(cfg)
+        line["cpu_baseline"] = cpu_baseline(cfg)
     if rank == 0:
         print(json.dumps(line))
     if dist is not None:

@@ -71,7 +71,7 @@ typedef enum {
   TK_OP_RELU = 5,               /* in0 < 0 ? 0 : in0 */
   TK_OP_POW = 6,                /* in0 ^ exponent (exponent: scalar in1, else attr) */
   TK_OP_THRESHOLD_BACKWARD = 7, /* in1 <= threshold ? 0 : in0 */
-  TK_OP_FULL = 8,               /* value (scalar in0, else attr) */
+  TK_OP_FULL = 8,               /* the value attribute when given, else scalar in0, else 0 */
   TK_OP_CAST = 9,               /* in0, rounded to the output dtype */
   TK_OP_MM = 10,                /* in0[m,k] @ in1[k,n]        (codegen.py emit_mm) */
   TK_OP_ADDMM = 11,             /* alpha*(in1 @ in2) + beta*in0 (bias broadcast) */
@@ -107,6 +107,9 @@ typedef struct {
   int32_t dims[TK_MAX_RANK];
   tk_tensor_spec output;
   double alpha, beta, threshold, exponent, value;
+  int32_t value_given;         /* 1: the value attribute is given; full then uses it over a scalar
+                                  operand (codegen.py point_expr: attrs value, else inputs[0], else 0) */
+  int32_t reserved;            /* 0 */
 } tk_op;
 
 /* A whole program.  inplace holds n_inplace pairs {output_slot, input_index}:

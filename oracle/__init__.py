@@ -82,10 +82,10 @@ def serialize(program) -> str:
         a = op.attrs
         dims = a.get("dims")
         dims_txt = "-1" if dims is None else " ".join([str(len(tuple(dims)))] + [str(int(d)) for d in dims])
-        lines.append("ATTR {} {} {} {} {} {} {}".format(
+        lines.append("ATTR {} {} {} {} {} {} {} {}".format(
             repr(float(a.get("alpha", 1))), repr(float(a.get("beta", 1))),
             repr(float(a.get("threshold", 0))), repr(float(a.get("exponent", 2))),
-            repr(float(a.get("value", 0))), int("exponent" in a), dims_txt))
+            repr(float(a.get("value", 0))), int("exponent" in a), int("value" in a), dims_txt))
     lines.append(f"OUTPUTS {len(program.outputs)}")
     lines += [_spec_text(s) for s in program.outputs]
     lines.append("END")

@@ -117,6 +117,7 @@ struct Op {
   Spec out;
   double alpha = 1, beta = 1, threshold = 0, exponent = 2, value = 0;
   bool has_exponent = false;
+  bool has_value = false;
   int ndims = -1;  // -1: reduce over every dim
   std::vector<int64_t> dims;
 };
@@ -203,6 +204,7 @@ Program parse(const char* text) {
     op.exponent = r.real();
     op.value = r.real();
     op.has_exponent = r.integer() != 0;
+    op.has_value = r.integer() != 0;
     op.ndims = int(r.integer());
     for (int j = 0; j < op.ndims; ++j) op.dims.push_back(r.integer());
     p.ops.push_back(op);
@@ -302,7 +304,9 @@ T pointwise(const Op& op, const T* v) {
     return std::pow(v[0], T(e));
   }
   if (k == "threshold_backward") return v[1] <= T(op.threshold) ? T(0) : v[0];
-  if (k == "full") return T(op.in.empty() ? op.value : op.in[0].value);
+  // full: the value attribute when given, else the scalar operand, else 0
+  // (page "trainkernel/codegen.py", point_expr)
+  if (k == "full") return T(op.has_value ? op.value : op.in.empty() ? 0.0 : op.in[0].value);
   if (k == "cast") return v[0];
   throw std::runtime_error("oracle: unsupported pointwise op " + k);
 }

@@ -37,7 +37,8 @@ class tk_op(ctypes.Structure):
                 ("scalar_mask", ctypes.c_uint32), ("n_dims", ctypes.c_int32), ("dims", ctypes.c_int32 * MAX_RANK),
                 ("output", tk_tensor_spec),
                 ("alpha", ctypes.c_double), ("beta", ctypes.c_double), ("threshold", ctypes.c_double),
-                ("exponent", ctypes.c_double), ("value", ctypes.c_double)]
+                ("exponent", ctypes.c_double), ("value", ctypes.c_double),
+                ("value_given", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class tk_program_desc(ctypes.Structure):
@@ -173,6 +174,7 @@ class Described:
             c.threshold = float(a.get("threshold", 0.0))
             c.exponent = float(a.get("exponent", 2.0))
             c.value = float(a.get("value", 0.0))
+            c.value_given = int("value" in a)
             dims = a.get("dims")
             c.n_dims = -1 if dims is None else len(tuple(dims))
             for j, d in enumerate(tuple(dims or ())):
@@ -226,6 +228,22 @@ def tk_run(handle, input_ptrs, output_ptrs, workspace_ptr: int, workspace_elemen
     outs = (ctypes.c_void_p * max(1, len(output_ptrs)))(*output_ptrs)
     check(lib().tk_run(handle, ins, len(input_ptrs), outs, len(output_ptrs), ctypes.c_void_p(workspace_ptr),
                        workspace_elements, ctypes.c_void_p(stream)))
+
+
+def tk_run_prepared(handle, input_ptrs, output_ptrs, workspace_ptr: int, workspace_elements: int, stream: int = 0):
+    """tk_run with its arguments marshalled once: returns a callable that
+    launches one step per call (for loops that launch the same buffers)."""
+    ins = (ctypes.c_void_p * max(1, len(input_ptrs)))(*input_ptrs)
+    outs = (ctypes.c_void_p * max(1, len(output_ptrs)))(*output_ptrs)
+    args = (handle, ins, len(input_ptrs), outs, len(output_ptrs), ctypes.c_void_p(workspace_ptr), workspace_elements,
+            ctypes.c_void_p(stream))
+    fn = lib().tk_run
+
+    def launch() -> None:
+        rc = fn(*args)
+        if rc != 0:
+            check(rc)
+    return launch
 
 
 def tk_run_status(handle, workspace_ptr: int, stream: int = 0):

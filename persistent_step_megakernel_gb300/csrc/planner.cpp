@@ -248,6 +248,14 @@ class Planner {
       }
       op.out = src.output;
       check_spec(op.out);
+      if (op.kind == TK_OP_FULL) {
+        // full's value: the attribute when given, else a scalar operand, else 0
+        // (codegen.py point_expr); kept in op.value with no operand left
+        if (op.in.size() > 1 || (op.in.size() == 1 && !op.in[0].scalar))
+          throw Error(TK_ERR_INVALID, "full takes at most one scalar value");
+        if (!src.value_given) op.value = op.in.empty() ? 0.0 : op.in[0].value;
+        op.in.clear();
+      }
       if (bufs_.count(op.out.buffer_id)) throw Error(TK_ERR_INVALID, "buffer defined twice");
       if (!relaxed_contig(op.out))
         throw Error(TK_ERR_INVALID, "materialized output must be contiguous: op " + std::to_string(i));
@@ -314,9 +322,8 @@ class Planner {
         if (op.in[0].scalar) throw Error(TK_ERR_UNSUPPORTED, "pow base must be a tensor");
         break;
       case TK_OP_FULL:
-        need(0, 1);
-        if (op.in.size() == 1 && !op.in[0].scalar) throw Error(TK_ERR_INVALID, "full takes a scalar value");
-        if (op.in.empty()) check_scalar(op.value);
+        need(0, 0);
+        check_scalar(op.value);
         break;
       case TK_OP_MM:
       case TK_OP_ADDMM: {
@@ -958,7 +965,7 @@ class Planner {
           return;
         }
         case TK_OP_FULL:
-          push(tkd::OP_CONST, r, 0, 0, rd, f32(op.in.empty() ? op.value : op.in[0].value));
+          push(tkd::OP_CONST, r, 0, 0, rd, f32(op.value));
           return;
         default:
           throw Error(TK_ERR_INVALID, "internal: not a pointwise op");
@@ -1071,7 +1078,7 @@ class Planner {
           return;
         }
         case TK_OP_FULL:
-          start_const(op.in.empty() ? op.value : op.in[0].value);
+          start_const(op.value);
           step(tkd::OP_MOV, rd, 0, 0, 0.f, 0.f);
           return;
         default:

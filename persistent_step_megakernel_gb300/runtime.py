@@ -88,6 +88,19 @@ class TrainStep:
                  workspace.data_ptr(), workspace.numel(), self._stream(stream))
         return outputs
 
+    def launcher(self, inputs, outputs, workspace, stream=None):
+        """A callable that runs one step on these buffers per call, with the
+        checks of run() done once here (the buffers must stay alive)."""
+        self.validate_inputs(inputs)
+        for j, (o, spec) in enumerate(zip(outputs, self.program.outputs)):
+            if (o.device != self.device or tuple(o.shape) != tuple(spec.shape)
+                    or o.dtype != TORCH_DTYPE[spec.dtype] or not o.is_contiguous()):
+                raise ValueError(f"tk: output {j} does not match compiled requirements")
+        if workspace.dtype != torch.float32 or not workspace.is_contiguous() or workspace.device != self.device:
+            raise ValueError("tk: workspace does not match compiled requirements")
+        return B.tk_run_prepared(self.handle, [t.data_ptr() for t in inputs], [o.data_ptr() for o in outputs],
+                                 workspace.data_ptr(), workspace.numel(), self._stream(stream))
+
     def profile(self, workspace, stream=None) -> dict:
         """Per-stage timing of the last run (program created with profile=1).
 

@@ -56,3 +56,14 @@ def test_traffic_is_taken_only_from_a_summary_of_the_same_kernel_source(peaks_di
     path.write_text("# summary\n\nsource_sha: 0000\ndram_bytes_per_launch: 1160960\n")
     assert bench.traffic_from_profiles("c2") is None          # stale counters are not reported
     assert bench.traffic_from_profiles("c4") is None          # no summary at all
+
+
+def test_sampled_oracle_rate_scales_to_whole_steps():
+    # a bounded sample of whole steps: the rate is reported per whole step
+    value, frac, threads = bench.oracle_sampled(S.CONFIGS["c1"], 0.5, steps=2, warmup=1)
+    assert value > 0 and 0 < frac <= 1 and threads >= 1
+
+
+def test_back_to_back_batches_follow_the_step_size():
+    assert bench.batch_steps_for(S.CONFIGS["c5"]) == 20
+    assert bench.batch_steps_for(S.CONFIGS["c2"]) == 100

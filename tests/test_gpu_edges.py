@@ -97,6 +97,8 @@ def pointwise_program(in_dt):
         Operation("ch", "cast", (x,), V("ch", "float16")),
         Operation("p", "pow", (x, 2), V("p", "bfloat16")),
         Operation("f", "full", (), V("f", "bfloat16"), {"value": 1.0 + 2.0 ** -8}),
+        Operation("f2", "full", (2.5,), V("f2", "float16"), {"value": 1.0 + 2.0 ** -11}),  # the attribute wins
+        Operation("f3", "full", (0.75,), V("f3", "bfloat16")),
         # chains: inlined single-use values (the loss-gradient and update shapes)
         Operation("d", "sub", (x, y), V("d", "bfloat16")),
         Operation("g", "mul", (V("d", "bfloat16"), 0.125), V("g", "bfloat16")),

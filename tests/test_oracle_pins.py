@@ -169,6 +169,47 @@ def test_sum_closed_forms_and_dims():
     assert np.isnan(got).all()
 
 
+def test_rank3_reductions_closed_forms():
+    # x[i, j, k] = 100 i + 10 j + k: every sum below has a closed form
+    A, Bd, C = 3, 4, 5
+    i, j, k = np.meshgrid(np.arange(A), np.arange(Bd), np.arange(C), indexing="ij")
+    xv = (100 * i + 10 * j + k).astype(np.float64)
+    x = T("x", (A, Bd, C), "float32")
+    tri = lambda n: n * (n - 1) // 2
+    # over the middle dim: B (100 i + k) + 10 * (0 + 1 + ... + B-1)
+    got = _run_single("sum", (x,), T("m", (A, C), "float32"), {"x": xv}, {"dims": (1,)})
+    want = np.array([[Bd * (100 * a + c) + 10 * tri(Bd) for c in range(C)] for a in range(A)])
+    np.testing.assert_array_equal(got, want)
+    got = _run_single("sum", (x,), T("m2", (A, C), "float32"), {"x": xv}, {"dims": (-2,)})
+    np.testing.assert_array_equal(got, want)
+    # over the outer and inner dims: 100 C tri(A) + 10 A C j + A tri(C)
+    got = _run_single("sum", (x,), T("o", (Bd,), "float32"), {"x": xv}, {"dims": (0, 2)})
+    want = np.array([100 * C * tri(A) + 10 * A * C * b + A * tri(C) for b in range(Bd)])
+    np.testing.assert_array_equal(got, want)
+    got = _run_single("mean", (x,), T("om", (Bd,), "float32"), {"x": xv}, {"dims": (0, -1)})
+    np.testing.assert_array_equal(got, (want.astype(np.float32) / np.float32(A * C)).astype(np.float32))
+    # over the two leading dims, and over every dim
+    got = _run_single("sum", (x,), T("l", (C,), "float32"), {"x": xv}, {"dims": (0, 1)})
+    np.testing.assert_array_equal(got, [100 * Bd * tri(A) + 10 * A * tri(Bd) + A * Bd * c for c in range(C)])
+    got = _run_single("sum", (x,), T("a", (), "float32"), {"x": xv})
+    assert got == 100 * Bd * C * tri(A) + 10 * A * C * tri(Bd) + A * Bd * tri(C)
+    # a permuted (non-contiguous) view: reducing its dim 0 is reducing the stored middle dim
+    xt = TensorSpec("x", (Bd, A, C), (C, Bd * C, 1), 0, "float32")
+    got = _run_single("sum", (xt,), T("p", (A, C), "float32"), {"x": xv}, {"dims": (0,)})
+    np.testing.assert_array_equal(got, [[Bd * (100 * a + c) + 10 * tri(Bd) for c in range(C)] for a in range(A)])
+
+
+def test_full_takes_the_value_attribute_over_an_operand():
+    # page "trainkernel/codegen.py", point_expr: attrs["value"] when present,
+    # else the first operand, else 0
+    f = _run_single("full", (2.5,), T("f", (2,), "float32"), {}, {"value": 0.75})
+    np.testing.assert_array_equal(f, [0.75, 0.75])
+    f = _run_single("full", (2.5,), T("f", (2,), "float32"), {})
+    np.testing.assert_array_equal(f, [2.5, 2.5])
+    f = _run_single("full", (), T("f", (2,), "float32"), {})
+    np.testing.assert_array_equal(f, [0.0, 0.0])
+
+
 def test_pointwise_semantics_special_cases():
     x = T("x", (6,), "float32")
     v = np.array([-1.5, -0.0, 0.0, 2.0, np.nan, 3.0])
@@ -282,6 +323,66 @@ def test_hand_computed_step_matches_exact_backprop():
     assert b2[0] - lr * sum(dz2) == Fraction(e["b2_new"][0])
 
 
+def _golden_momentum():
+    with open(os.path.join(GOLDEN, "two_layer_momentum_step.json")) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("dtype,master", [("float32", None), ("bfloat16", None), ("float16", None),
+                                          ("float64", None), ("bfloat16", "float32")])
+def test_hand_computed_momentum_step(dtype, master):
+    # the momentum wiring (v' = mu v + g, W' = W - lr v', in place) and, with a
+    # float32 master copy, the mixed-precision wiring (bf16 GEMM copies of the
+    # weights, float32 loss, gradients of the weights and updates)
+    g = _golden_momentum()
+    c = g["config"]
+    cfg = S.scaled(S.CONFIGS["c1"], batch=c["batch"], dims=tuple(c["dims"]), lr=c["lr"], momentum=c["momentum"],
+                   dtype=dtype, master=master)
+    prog = S.mlp_step_program(cfg, export="grads")
+    if master:
+        assert any(op.op == "cast" for op in prog.operations)
+        assert {s.dtype for s in prog.inputs if s.buffer.startswith(("W", "b", "v"))} == {master}
+    vals = [np.array(g["inputs"][s.buffer], dtype=np.float64) for s in prog.inputs]
+    outs = oracle.run_program(prog, vals)
+    by_name = {s.buffer: o for s, o in zip(prog.outputs, outs)}
+    assert set(g["expected"]) == set(by_name)
+    for name, want in g["expected"].items():
+        np.testing.assert_array_equal(by_name[name], np.array(want), err_msg=name)
+
+
+def test_hand_computed_momentum_step_matches_exact_momentum_sgd():
+    """The momentum fixture against textbook backprop and momentum SGD in exact rationals."""
+    g = _golden_momentum()
+    F = lambda a: [[Fraction(v) for v in r] for r in a]
+    F1 = lambda a: [Fraction(v) for v in a]
+    inp = g["inputs"]
+    x, y, W1, W2 = F(inp["x"]), F(inp["y"]), F(inp["W1"]), F(inp["W2"])
+    b1, b2 = F1(inp["b1"]), F1(inp["b2"])
+    vW1, vW2, vb1, vb2 = F(inp["vW1"]), F(inp["vW2"]), F1(inp["vb1"]), F1(inp["vb2"])
+    lr, mu, B = Fraction(g["config"]["lr"]), Fraction(g["config"]["momentum"]), len(x)
+    z1 = [[sum(W1[j][k] * x[n][k] for k in range(2)) + b1[j] for j in range(2)] for n in range(B)]
+    a1 = [[max(v, 0) for v in r] for r in z1]
+    z2 = [sum(W2[0][j] * a1[n][j] for j in range(2)) + b2[0] for n in range(B)]
+    dz2 = [2 * (z2[n] - y[n][0]) / B for n in range(B)]
+    gW2 = [sum(dz2[n] * a1[n][j] for n in range(B)) for j in range(2)]
+    dz1 = [[dz2[n] * W2[0][j] * (1 if z1[n][j] > 0 else 0) for j in range(2)] for n in range(B)]
+    gW1 = [[sum(dz1[n][j] * x[n][k] for n in range(B)) for k in range(2)] for j in range(2)]
+    gb1 = [sum(dz1[n][j] for n in range(B)) for j in range(2)]
+    gb2 = sum(dz2)
+    e = g["expected"]
+    vW1n = [[mu * vW1[j][k] + gW1[j][k] for k in range(2)] for j in range(2)]
+    vW2n = [mu * vW2[0][j] + gW2[j] for j in range(2)]
+    vb1n = [mu * vb1[j] + gb1[j] for j in range(2)]
+    vb2n = mu * vb2[0] + gb2
+    assert vW1n == F(e["vW1_new"]) and [vW2n] == F(e["vW2_new"])
+    assert vb1n == F1(e["vb1_new"]) and [vb2n] == F1(e["vb2_new"])
+    assert [[W1[j][k] - lr * vW1n[j][k] for k in range(2)] for j in range(2)] == F(e["W1_new"])
+    assert [[W2[0][j] - lr * vW2n[j] for j in range(2)]] == F(e["W2_new"])
+    assert [b1[j] - lr * vb1n[j] for j in range(2)] == F1(e["b1_new"])
+    assert [b2[0] - lr * vb2n] == F1(e["b2_new"])
+    assert sum((z2[n] - y[n][0]) ** 2 for n in range(B)) / B == Fraction(e["loss"])
+
+
 # ------------------------------------------------------ finite differences
 
 def _fd_inputs(cfg, prog, seed):
@@ -301,6 +402,8 @@ def _fd_inputs(cfg, prog, seed):
     ("c1", {}),
     ("c3", {"batch": 3, "dims": (4, 6, 4)}),
     ("c2", {"batch": 4, "dims": (5, 7, 6, 3)}),
+    ("c2m", {"batch": 4, "dims": (5, 7, 6, 3)}),                  # the cast-to-compute-copy wiring
+    ("c2m", {"batch": 3, "dims": (4, 6, 3), "momentum": 0.9}),
 ])
 def test_gradients_match_central_finite_differences(key, changes):
     cfg = S.scaled(S.CONFIGS[key], **changes)

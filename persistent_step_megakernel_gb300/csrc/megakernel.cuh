@@ -556,21 +556,39 @@ __device__ __forceinline__ void chain_compute(const Chain& ch, const float (&L)[
   }
 }
 
-// A GEMM's side output: one op on the stored (rounded) final value x, the
-// same arithmetic as the chain step it stands for.
-// (The planner only makes sides of multiplications by a constant, negations
-// and casts.)
-__device__ __forceinline__ float side_value(const ChainStep& st, float x) {
-  const float y = st.op == OP_MUL ? __fmul_rn(x, st.cval) : st.op == OP_NEG ? -x : x;
+// A side output: one op on the stored (rounded) final value x, the same
+// arithmetic as the chain step it stands for: x*c, -x, a cast, or (a loaded
+// side) x +/- a*e / e +/- a*x with e the side operand.
+__device__ __forceinline__ float side_value(const ChainStep& st, float x, float e) {
+  float y;
+  if (st.op == OP_ADD || st.op == OP_SUB) {
+    const float a = st.second ? e : x, b = st.second ? x : e;
+    const float p = __fmul_rn(st.imm, b);
+    y = st.op == OP_ADD ? __fadd_rn(a, p) : __fsub_rn(a, p);
+  } else {
+    y = st.op == OP_MUL ? __fmul_rn(x, st.cval) : st.op == OP_NEG ? -x : x;
+  }
   return round_to(y, st.round);
 }
 
 // Out of line, so that the epilogues without a side output carry no code for it.
 template <int V>
 __device__ __noinline__ void store_side(const Ctx c, const Task& t, int64_t flat, const float (&x)[V]) {
-  float y[V];
+  float e[V], y[V];
+  if (t.side.ext == EXT_LOAD1) {
+    const char* p = space_ptr(c, t.side_ld.space, t.side_ld.slot);
+    if constexpr (V == 8) {
+      load8(p, t.side_ld.dtype, t.side_ld.base + flat, e);
+    } else {
+#pragma unroll
+      for (int j = 0; j < V; ++j) e[j] = load1(p, t.side_ld.dtype, t.side_ld.base + flat + j);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < V; ++j) e[j] = 0.0f;
+  }
 #pragma unroll 1
-  for (int j = 0; j < V; ++j) y[j] = side_value(t.side, x[j]);
+  for (int j = 0; j < V; ++j) y[j] = side_value(t.side, x[j], e[j]);
   store_out<V>(c, t.out2, flat, y);
 }
 
@@ -866,6 +884,10 @@ __device__ __forceinline__ void finish_reduction(const Ctx& c, const Task& t, in
     v = reduction_post(c, t, o, v);
   }
   store1(space_ptr(c, t.out.space, t.out.slot), t.out.dtype, t.out.base + o, v);
+  if (t.has_side) {
+    const float x[1] = {round_to(v, t.out.dtype)};  // the stored value
+    store_side<1>(c, t, o, x);
+  }
 }
 
 // ------------------------------------------------------------- work items
@@ -1915,26 +1937,39 @@ __device__ __forceinline__ void stage_store(uint32_t buf, char* out, int64_t row
 
 // A GEMM's side output from a staged chunk: each lane turns its row of the
 // stored (rounded) values into the side values in place, then the chunk goes
-// to out2.  Called after the chunk's own store (a __syncwarp apart).
-__device__ __noinline__ void stage_side(const Task& t, uint32_t buf, int64_t row0, int64_t col0, int64_t M,
-                                        int64_t N, int out_dt, char* out2) {
+// to out2.  Called after the chunk's own store (a __syncwarp apart).  A
+// loaded side reads its operand's chunk from `opnd` (staged like the per-row
+// operands) and writes the side values there instead.
+__device__ __noinline__ void stage_side(const Task& t, uint32_t buf, uint32_t opnd, int64_t row0, int64_t col0,
+                                        int64_t M, int64_t N, int out_dt, char* out2) {
   const int lane = threadIdx.x & 31;
+  const bool loaded = t.side.ext == EXT_LOAD1;
+  const uint32_t dst = loaded ? opnd : buf;
   __syncwarp();
 #pragma unroll 1
   for (int v = 0; v < 4; ++v) {
-    float x[8];
+    float x[8], e[8];
     unpack8(lds128(buf + stg_off(lane, v)), out_dt, x);
-    if (t.side.op == OP_MUL) {
+    if (loaded) {
+      unpack8(lds128(opnd + stg_off(lane, v)), t.side_ld.dtype, e);
+      const bool sub = t.side.op == OP_SUB, second = t.side.second;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float a = second ? e[j] : x[j], b = second ? x[j] : e[j];
+        const float p = __fmul_rn(t.side.imm, b);
+        x[j] = sub ? __fsub_rn(a, p) : __fadd_rn(a, p);
+      }
+    } else if (t.side.op == OP_MUL) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) x[j] = __fmul_rn(x[j], t.side.cval);
     } else if (t.side.op == OP_NEG) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) x[j] = -x[j];
     }
-    sts128(buf + stg_off(lane, v), pack8(x, t.out2.dtype));  // rounds to the side's type
+    sts128(dst + stg_off(lane, v), pack8(x, t.out2.dtype));  // rounds to the side's type
   }
   __syncwarp();
-  stage_store(buf, out2, row0, col0, M, N);
+  stage_store(dst, out2, row0, col0, M, N);
 }
 
 // Returns false if the accumulator wait timed out.  An operand with one row
@@ -1958,6 +1993,10 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
   const uint32_t r0 = b1 + (st1 ? 2 * kEpiBufBytes : 0);
   const uint32_t r1 = r0 + (L0 && !st0 ? kBcastBytes : 0);
   const uint32_t only = r1 + (L1 && !st1 ? kBcastBytes : 0);
+  // the operand of a loaded side output: two chunk buffers after the rest
+  const bool sl = t.has_side && t.side.ext == EXT_LOAD1 && (mask & 8);
+  const uint32_t bs = only + (st0 || st1 ? 0 : kEpiBufBytes);
+  const char* const sp = sl ? space_ptr(c, t.side_ld.space, t.side_ld.slot) + t.side_ld.base * 2 : nullptr;
   char* const out2 = t.has_side ? space_ptr(c, t.out2.space, t.out2.slot) + t.out2.base * 2 : nullptr;
 
   // The loops below stay rolled: the code is small enough to stay in the
@@ -1967,7 +2006,7 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
   // per-row operands of chunk ch, in the same lane pattern as stage_store
   const int lr = lane >> 2, lj = lane & 3;
   auto prefetch = [&](int ch) {
-    if (!(st0 || st1)) return;
+    if (!(st0 || st1 || sl)) return;
     const int64_t col = n0 + 32 * ch + 8 * lj;
     if (col >= N) return;
     const uint32_t off = uint32_t(ch & 1) * kEpiBufBytes + stg_off(lr, lj);
@@ -1977,6 +2016,7 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
       if (row < M) {
         if (st0) cp_async16(b0 + off + 512 * i, F.p0 + row * F.rs0 + col * 2);
         if (st1) cp_async16(b1 + off + 512 * i, F.p1 + row * F.rs1 + col * 2);
+        if (sl) cp_async16(bs + off + 512 * i, sp + (row * N + col) * 2);
       }
     }
   };
@@ -2022,7 +2062,7 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
     }
     __syncwarp();
     stage_store(ob, F.out, row0, col0, M, N);
-    if (t.has_side) stage_side(t, ob, row0, col0, M, N, F.out_dt, out2);
+    if (t.has_side) stage_side(t, ob, bs + half, row0, col0, M, N, F.out_dt, out2);
     __syncwarp();
   }
   cp_async_wait<0>();

@@ -121,6 +121,10 @@ struct RegisterOverflow {
   int buffer;
 };
 
+// Raised when a decision turns out not to fit the plan (an in-place side
+// output that cannot be written directly); planning restarts without it.
+struct Replan {};
+
 float f32(double v) { return static_cast<float>(v); }
 
 class Planner {
@@ -136,6 +140,8 @@ class Planner {
       } catch (const RegisterOverflow& r) {
         if (attempt > 256) throw Error(TK_ERR_UNSUPPORTED, "expression too deep to evaluate inline");
         no_inline_.insert(r.buffer);
+      } catch (const Replan&) {
+        if (attempt > 256) throw Error(TK_ERR_UNSUPPORTED, "planning did not settle");
       }
     }
   }
@@ -149,6 +155,7 @@ class Planner {
   std::unordered_map<int, Buf> bufs_;
   std::set<int> output_buffers_;
   std::set<int> no_inline_;
+  std::set<int> no_side_;               // fused op indices that may not take a side output
 
   // per-attempt decisions
   struct Fused {
@@ -502,42 +509,83 @@ class Planner {
     }
   }
 
-  // Side outputs (a GB300 addition in the spirit of the page's side
-  // epilogues): a fused GEMM whose final value is stored and read again (it
-  // has several users, or it is returned and has a user) also writes one of
-  // those users from the same tile when that user is a one-operand pointwise
-  // op of the final value (e.g. the loss gradient 2/N * d next to d) and would
-  // be stored anyway (a GEMM operand, a returned value or a value with several
-  // users).  Not for in-place outputs.
+  // Side outputs (the page's second epilogue case, "returned pointwise
+  // descendants from the same output tile", in a restricted form): a fused
+  // GEMM or reduction whose final value is stored and read again (it has
+  // several users, or it is returned and has a user) also writes one of those
+  // users from the same tile, when that user is
+  //   * a one-operand pointwise op of the final value (x*c, -x, a cast), e.g.
+  //     the loss gradient 2/N * d next to d, that would be stored anyway (a GEMM
+  //     operand, a returned value or a value with several users); or
+  //   * an add/sub of the final value and a contiguous view of a program input
+  //     of the same shape (a "loaded" side), e.g. the momentum step
+  //     W' = W - lr*v' next to v', or W' = W - lr*gW next to a returned gW.
+  // A loaded side may be an in-place output only of the input it loads (each
+  // element is read, then overwritten by the same thread); it must then be
+  // written directly (see check_sides), or the side is dropped.  A GEMM or
+  // reduction without a chain (its own result returned, e.g. an exported
+  // weight gradient next to the weight's update) takes a side too.
   void detect_side_outputs() {
-    for (auto& kv : fused_) {
-      const OpInfo& mm = ops_[kv.first];
-      if (!is_mm(mm.kind)) continue;
-      const int fin = kv.second.final_buf;
+    for (const OpInfo& mm : ops_) {
+      if (!is_mm(mm.kind) && !is_red(mm.kind)) continue;
+      if (no_side_.count(mm.index) || (!opt_.fuse_epilogues && !fused_.count(mm.index))) continue;
+      auto fu = fused_.find(mm.index);
+      const int fin = fu != fused_.end() ? fu->second.final_buf : mm.out.buffer_id;
       const Buf& fb = bufs_.at(fin);
       if (fb.users.empty() || (fb.users.size() < 2 && !output_buffers_.count(fin))) continue;
       for (int u : fb.users) {
         const OpInfo& op = ops_[u];
         if (!is_pointwise(op.kind) || op.kind == TK_OP_FULL || fused_skip_.count(op.out.buffer_id)) continue;
-        if (op.kind != TK_OP_MUL && op.kind != TK_OP_NEG && op.kind != TK_OP_CAST) continue;
-        if (inplace_target(op.out.buffer_id) >= 0) continue;
         if (shape_of(op.out) != fb.shape || !exact_contig(op.out)) continue;
+        const bool unary = op.kind == TK_OP_MUL || op.kind == TK_OP_NEG || op.kind == TK_OP_CAST;
+        const bool axpy = op.kind == TK_OP_ADD || op.kind == TK_OP_SUB;
+        if (!unary && !axpy) continue;
+        int roots_seen = 0, loads = 0, loaded = -1;
         bool ok = true;
-        int roots_seen = 0;
         for (const auto& o : op.in) {
           if (o.scalar) continue;
-          if (o.t.buffer_id == fin && shape_of(o.t) == fb.shape && exact_contig(o.t)) ++roots_seen;
-          else ok = false;
+          if (o.t.buffer_id == fin) {
+            if (shape_of(o.t) == fb.shape && exact_contig(o.t)) ++roots_seen;
+            else ok = false;
+          } else if (axpy && bufs_.at(o.t.buffer_id).input >= 0 && shape_of(o.t) == fb.shape && exact_contig(o.t)) {
+            ++loads;
+            loaded = o.t.buffer_id;
+          } else {
+            ok = false;
+          }
         }
-        if (!ok || roots_seen != 1) continue;
+        if (!ok || roots_seen != 1 || (axpy && loads != 1) || (unary && loads != 0)) continue;
+        if (is_red(mm.kind) && !axpy) continue;  // reductions take loaded sides only
+        const int target = inplace_target(op.out.buffer_id);
+        if (target >= 0 && (!axpy || target != loaded)) continue;
         const Buf& ub = bufs_.at(op.out.buffer_id);
         const bool stored = output_buffers_.count(op.out.buffer_id) || ub.users.size() != 1 ||
                             reads_as_gemm_operand(op.out.buffer_id);
         if (!stored) continue;
-        side_[kv.first] = u;
+        if (fu == fused_.end()) {
+          if (is_red(mm.kind) && opt_.expr_forms >= 2) continue;  // a reduction's side needs its chain form
+          Fused f;
+          f.final_buf = fin;
+          fused_[mm.index] = f;
+        }
+        side_[mm.index] = u;
         fused_skip_.insert(op.out.buffer_id);
         break;
       }
+    }
+  }
+
+  // An in-place side output must be written directly into its input (the
+  // tile reads the old value at the same index just before); when the plan
+  // cannot do that, drop the side and plan again.
+  void check_sides() {
+    for (const auto& kv : side_) {
+      const int out_buf = ops_[kv.second].out.buffer_id;
+      for (const auto& io : inplace_)
+        if (outputs_[io.first].buffer_id == out_buf && !direct_.count(io.first)) {
+          no_side_.insert(kv.first);
+          throw Replan{};
+        }
     }
   }
 
@@ -611,25 +659,34 @@ class Planner {
     return -1;
   }
 
-  // A fused GEMM whose chain ends in an in-place output (e.g. a weight
-  // gradient GEMM ending in the SGD update of that weight) moves after the
-  // last scheduled op that still reads the old value (the input-gradient GEMM
-  // of the same layer), so that it can write the new value directly.  Moving
-  // it later is legal: only program outputs depend on it.
+  // A fused GEMM or reduction that writes an in-place output (its chain's
+  // final value or its side output: e.g. a weight-gradient GEMM ending in the
+  // SGD update of that weight, or writing the momentum buffer and the weight)
+  // moves after the last scheduled op that still reads an old value it
+  // overwrites (the input-gradient GEMM of the same layer), so that it can
+  // write the new values directly.  Moving it later is legal when only
+  // program outputs depend on what it writes.
   void defer_inplace_epilogues() {
     for (size_t i = 0; i < schedule_.size(); ++i) {
       const int f = schedule_[i];
-      auto fu = fused_.find(f);
-      if (fu == fused_.end() || side_.count(f)) continue;
-      const int target = inplace_target(fu->second.final_buf);
-      if (target < 0) continue;
+      if (!fused_.count(f)) continue;
+      std::set<int> targets, written;
+      for (int b : stored_buffers(f)) {
+        written.insert(b);
+        const int t = inplace_target(b);
+        if (t >= 0) targets.insert(t);
+      }
+      if (targets.empty()) continue;
       size_t last = i;
       bool blocked = false;
       for (size_t j = i + 1; j < schedule_.size(); ++j) {
         bool reads_target = false;
         for (const auto& v : reads_of(schedule_[j])) {
-          if (raw_inputs(v.buffer_id).count(target)) reads_target = true;
-          if (roots(v.buffer_id).count(fu->second.final_buf)) blocked = true;
+          const std::set<int> raw = raw_inputs(v.buffer_id);
+          for (int t : targets)
+            if (raw.count(t)) reads_target = true;
+          for (int b : roots(v.buffer_id))
+            if (written.count(b)) blocked = true;
         }
         if (blocked) break;
         if (reads_target) last = j;
@@ -653,6 +710,12 @@ class Planner {
       for (int ci : it->second.chain)
         for (const auto& o : ops_[ci].in)
           if (!o.scalar && !chain_bufs.count(o.t.buffer_id)) r.push_back(o.t);
+    }
+    auto sd = side_.find(op_index);
+    if (sd != side_.end()) {
+      const int fin = out_buffer_of(op_index);
+      for (const auto& o : ops_[sd->second].in)
+        if (!o.scalar && o.t.buffer_id != fin) r.push_back(o.t);
     }
     return r;
   }
@@ -688,7 +751,8 @@ class Planner {
       int target = inputs_[idx].buffer_id;
       int pos = -1;
       for (size_t i = 0; i < schedule_.size(); ++i)
-        if (out_buffer_of(schedule_[i]) == out.buffer_id) pos = int(i);
+        for (int b : stored_buffers(schedule_[i]))
+          if (b == out.buffer_id) pos = int(i);
       if (pos < 0 || out_count[out.buffer_id] != 1) continue;
       const bool fused_gemm = fused_.count(schedule_[pos]) > 0;
       if (!fused_gemm && !is_pointwise(ops_[schedule_[pos]].kind)) continue;
@@ -1221,6 +1285,11 @@ class Planner {
     const int last = ch.n_steps ? ch.steps[ch.n_steps - 1].round : ch.round0;
     if (last != t.out.dtype) return -1;
     int mask = 4;
+    // a loaded side's operand goes through shared memory like a per-row operand
+    if (t.has_side && t.side.ext == tkd::EXT_LOAD1) {
+      if (t.side_ld.dtype == TK_F32 || t.side_ld.base % 8 != 0) return -1;
+      mask |= 8;
+    }
     for (int s = 0; s < ch.n_loads; ++s) {
       const Ref& r = plan.refs[t.ref_begin + ch.load_ref[s]];
       if (r.dtype == TK_F32 || r.base % 8 != 0) return -1;
@@ -1239,7 +1308,7 @@ class Planner {
     if (mask < 0) return 0;
     const int rows = (mask & 1) + ((mask >> 1) & 1);
     const int bcast = t.chain.n_loads - rows;
-    return main_stage_bytes(rows, bcast);
+    return main_stage_bytes(rows, bcast) + ((mask & 8) ? 2 * tkd::kEpiBufBytes : 0);
   }
 
   static int main_stage_bytes(int rows, int bcast) {
@@ -1448,7 +1517,8 @@ class Planner {
     return true;
   }
 
-  // The side output of fused GEMM mm (if any) as one chain step on the final value.
+  // The side output of fused GEMM or reduction mm (if any) as one chain step
+  // on the final value.
   void attach_side(Task& t, const OpInfo& mm) const {
     auto it = side_.find(mm.index);
     if (it == side_.end()) return;
@@ -1457,8 +1527,23 @@ class Planner {
     tkd::ChainStep st{};
     st.round = uint8_t(op.out.dtype);
     st.ext = tkd::EXT_NONE;
-    // x*c (= c*x), -x, or a cast
-    if (op.kind == TK_OP_MUL) {
+    if (op.kind == TK_OP_ADD || op.kind == TK_OP_SUB) {
+      // a loaded side: final +/- alpha*input or input +/- alpha*final, the
+      // input read at the output's flat index from side_ld
+      const bool root_first = op.in[0].t.buffer_id == fin;
+      const tk_tensor_spec& in = op.in[root_first ? 1 : 0].t;
+      st.op = op.kind == TK_OP_ADD ? tkd::OP_ADD : tkd::OP_SUB;
+      st.imm = f32(op.alpha);
+      st.ext = tkd::EXT_LOAD1;
+      st.second = root_first ? 0 : 1;
+      Ref r{};
+      int64_t base;
+      location(in.buffer_id, &r.space, &r.slot, &base);
+      r.dtype = in.dtype;
+      r.base = base + in.offset;
+      r.vmode = tkd::VM_CONTIG;
+      t.side_ld = r;
+    } else if (op.kind == TK_OP_MUL) {  // x*c (= c*x), -x, or a cast
       const bool root_first = !op.in[0].scalar && op.in[0].t.buffer_id == fin;
       st.op = tkd::OP_MUL;
       st.ext = tkd::EXT_CONST;
@@ -1705,7 +1790,10 @@ class Planner {
       t.parts = int(ceil_div(std::max<int64_t>(n_red, 1), t.part_len));
       t.n_items = int(chunks * t.parts);
     }
-    if (t.parts <= 1 && fused_it != fused_.end()) lower_post_chain(plan, t, op, fused_it->second);
+    if (t.parts <= 1 && fused_it != fused_.end()) {
+      lower_post_chain(plan, t, op, fused_it->second);
+      attach_side(t, op);
+    }
     finish_refs(plan, t);
     classify_fast(plan, t);
     // compiled sources over 16-bit operands stream with more loads in flight
@@ -1739,6 +1827,7 @@ class Planner {
     f.ref_begin = int(plan.refs.size());
     if (fused_it != fused_.end()) {
       lower_post_chain(plan, f, op, fused_it->second);
+      attach_side(f, op);
       finish_refs(plan, f);
     }
     return {t, f};
@@ -1799,6 +1888,7 @@ class Planner {
     choose_inline();
     build_schedule();
     choose_direct_aliases();
+    check_sides();
     choose_bindings();
     // Stages first with a private slot per intermediate value, then the arena
     // reuses a slot only for a value written in a later stage than the last

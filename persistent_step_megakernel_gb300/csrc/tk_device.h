@@ -203,14 +203,20 @@ struct alignas(16) Task {
   Chain post;
   int64_t post_shape[kMaxRank];
   int32_t post_rank;
-  // GEMMs: a side output, one more pointwise op on the stored (rounded) final
-  // value, written to out2 (same shape, contiguous) from the same tile.
+  // GEMMs and reductions: a side output, one more pointwise op on the stored
+  // (rounded) final value, written to out2 (same shape, contiguous) from the
+  // same tile.  side.ext: EXT_NONE / EXT_CONST (x*c, -x, a cast), or
+  // EXT_LOAD1: an add/sub with the operand side_ld (contiguous, the output's
+  // shape) read at the output's flat index; side.second as in a chain step.
   int32_t has_side;
-  ChainStep side;            // ext is EXT_CONST or EXT_NONE
+  ChainStep side;
   Ref out2;
+  Ref side_ld;
   // Staged epilogue (compiled GEMM epilogues with 16-bit output): bit s set =
   // load slot s is read per row and copied through shared memory; bit 2 =
-  // the staged path is on.  0 = operands and output accessed directly.
+  // the staged path is on; bit 3 = the side output's operand (side_ld) is
+  // copied through shared memory too.  0 = operands and output accessed
+  // directly.
   int32_t epi_stage;
   int32_t pw_unroll;         // pointwise items: vectors per thread (kPointwiseUnroll or kPointwiseUnroll16)
   // Split-K (under-filled tensor-core GEMMs): item = tile * k_splits + split;

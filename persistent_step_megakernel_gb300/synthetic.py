@@ -106,6 +106,7 @@ class MLPConfig:
     momentum: float = 0.0  # > 0: SGD with a momentum buffer per parameter
     seed: int = 0
     master: str | None = None  # e.g. "float32": parameters kept in this type, GEMMs in dtype
+    targets: str = "normal"    # "normal": y ~ N(0, 1); "onehot": y one-hot rows of seeded class labels
 
     @property
     def layers(self) -> int:
@@ -149,6 +150,12 @@ CONFIGS = {
     "c2m": MLPConfig("c2m", "mixed-precision MLP step: fp32 master weights, bf16 GEMMs, fp32 loss and SGD; "
                      "batch 64, 256->512->512->128", "bfloat16", 64, (256, 512, 512, 128), 1e-3,
                      "kaiming_uniform", master="float32"),
+    # a linear classification head trained by least squares against one-hot
+    # targets, updated in place (the pages name the workload; these shapes are
+    # this build's own choice)
+    "lsq": MLPConfig("lsq", "one-hot least-squares classification head: bf16, batch 128, 1024 features -> "
+                     "10 classes, MSE against one-hot targets, SGD lr=1e-2, in place", "bfloat16", 128, (1024, 10),
+                     1e-2, "torch_default", targets="onehot"),
 }
 
 
@@ -263,7 +270,9 @@ def mlp_step_program(cfg: MLPConfig, export: str = "state", dtype: str | None = 
 def mlp_inputs(cfg: MLPConfig, program: Program, seed: int | None = None, dtype: str | None = None) -> list:
     """Seeded input arrays in program-input order (storage form, see to_storage).
 
-    x, y ~ N(0, 1); weights and biases per cfg.init; momentum buffers ~ N(0, 0.01^2).
+    x ~ N(0, 1); y ~ N(0, 1), or one-hot rows of class labels drawn uniformly
+    from the stream (label = floor(u * classes)); weights and biases per
+    cfg.init; momentum buffers ~ N(0, 0.01^2).
     """
     seed = cfg.seed if seed is None else seed
     arrays = []
@@ -271,7 +280,14 @@ def mlp_inputs(cfg: MLPConfig, program: Program, seed: int | None = None, dtype:
         n = int(np.prod(spec.shape)) if spec.shape else 1
         s = stream_seed(seed, idx)
         name = spec.buffer
-        if name in ("x", "y"):
+        if name == "y" and cfg.targets == "onehot":
+            classes = spec.shape[-1]
+            rows = n // classes if classes else 0
+            labels = np.minimum((uniform01(s, rows) * classes).astype(np.int64), classes - 1)
+            vals = np.zeros((rows, classes))
+            vals[np.arange(rows), labels] = 1.0
+            vals = vals.reshape(-1)
+        elif name in ("x", "y"):
             vals = normal(s, n)
         elif name.startswith("vW") or name.startswith("vb"):
             vals = normal(s, n, 0.0, 0.01)

@@ -141,8 +141,13 @@ def gemm_program(dt):
         # input gradient with the ReLU mask
         Operation("ga", "mm", (e, W), T("ga", (M, K), dt)),
         Operation("gz", "threshold_backward", (T("ga", (M, K), dt), mask), T("gz", (M, K), dt), {"threshold": 0.0}),
+        # a returned GEMM result and an update loading another input next to it
+        # (a loaded side output): u = y - 0.5 q
+        Operation("q", "mm", (a, W.T), T("q", (M, N), dt)),
+        Operation("u", "sub", (y, T("q", (M, N), dt)), T("u", (M, N), dt), {"alpha": 0.5}),
     ]
-    outs = [T("h", (M, N), dt), T("d", (M, N), dt), T("g", (M, N), dt), T("gz", (M, K), dt)]
+    outs = [T("h", (M, N), dt), T("d", (M, N), dt), T("g", (M, N), dt), T("gz", (M, K), dt), T("q", (M, N), dt),
+            T("u", (M, N), dt)]
     return Program([a, W, e, b, y, mask], outs, ops)
 
 
@@ -173,10 +178,13 @@ def test_gemm_epilogue_edge_values_bit_exact(dt, forms, bn):
     arrays = gemm_inputs(prog, dt, seed=29)
     gpu, st = run_step(prog, arrays, expr_forms=forms, tile_n=bn)
     tiles = [t for t in st.tasks() if t["kind"] == "gemm_tc"]
-    assert len(tiles) == 3 and all(t["tile_n"] == bn for t in tiles)
+    assert len(tiles) == 4 and all(t["tile_n"] == bn for t in tiles)
+    assert sum(t["side_output"] for t in tiles) == 2
     if forms == 0:
-        assert all(t["staged_epilogue"] for t in tiles)
-        assert sum(t["side_output"] for t in tiles) == 1
+        # at 256 columns the ring leaves no room to stage the loaded side's
+        # operand: that tile keeps direct accesses
+        assert all(t["staged_epilogue"] for t in tiles[:3])
+        assert tiles[3]["staged_epilogue"] == (bn < 256)
     want = oracle.run_program(prog, values(arrays, prog))
     for spec, g, w in zip(prog.outputs, gpu, want):
         assert_bit_exact(g, w, spec.dtype, (spec.buffer, dt, forms, bn))

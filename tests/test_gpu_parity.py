@@ -44,6 +44,7 @@ SMALL = {
     "c2m": S.CONFIGS["c2m"],
     "batch1_bf16": S.scaled(S.CONFIGS["c2"], batch=1),          # the online (batch-1) step
     "ragged_mixed_mom": S.scaled(S.CONFIGS["c2m"], batch=5, dims=(37, 19, 11), momentum=0.9),
+    "lsq": S.CONFIGS["lsq"],                                      # one-hot least-squares head
 }
 
 
@@ -100,7 +101,7 @@ def test_results_do_not_depend_on_grid_size(key):
 
 
 @pytest.mark.parametrize("key", ["c1", "c2", "c3s", "c4", "ragged_f32", "ragged_f16_mom", "c2m", "ragged_mixed_mom",
-                                 "batch1_bf16"])
+                                 "batch1_bf16", "lsq"])
 def test_whole_step_tracks_oracle(key):
     cfg = SMALL[key]
     prog = S.mlp_step_program(cfg, export="grads")

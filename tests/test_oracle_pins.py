@@ -404,6 +404,7 @@ def _fd_inputs(cfg, prog, seed):
     ("c2", {"batch": 4, "dims": (5, 7, 6, 3)}),
     ("c2m", {"batch": 4, "dims": (5, 7, 6, 3)}),                  # the cast-to-compute-copy wiring
     ("c2m", {"batch": 3, "dims": (4, 6, 3), "momentum": 0.9}),
+    ("lsq", {"batch": 5, "dims": (6, 3)}),                        # one-hot targets, one layer
 ])
 def test_gradients_match_central_finite_differences(key, changes):
     cfg = S.scaled(S.CONFIGS[key], **changes)
@@ -464,6 +465,27 @@ def test_relu_masks_follow_preactivation_sign():
         ga = o.get(f"ga{i}")
         np.testing.assert_array_equal(g[z > 0], ga[z > 0])
         assert (z > 0).any() and (z <= 0).any()
+
+
+def test_one_hot_least_squares_head_closed_form_at_zero_weights():
+    # logits = 0: loss = mean(onehot^2) = 1/C; g = -2/(B C) onehot, so
+    # gb[c] = -2/(B C) * count(c) and gW[c] = -2/(B C) * sum of the rows of x labelled c
+    cfg = S.scaled(S.CONFIGS["lsq"], dtype="float32", batch=12, dims=(7, 4))
+    prog = S.mlp_step_program(cfg, export="grads")
+    ins = S.mlp_inputs(cfg, prog)
+    vals = [S.storage_to_float64(a, s.dtype) for a, s in zip(ins, prog.inputs)]
+    names = [s.buffer for s in prog.inputs]
+    for p in ("W1", "b1"):
+        vals[names.index(p)] = np.zeros_like(vals[names.index(p)])
+    outs = {s.buffer: o for s, o in zip(prog.outputs, oracle.run_program(prog, vals))}
+    x, y = vals[names.index("x")], vals[names.index("y")]
+    B, C = y.shape
+    assert (y.sum(1) == 1).all() and set(np.unique(y)) == {0.0, 1.0}
+    assert outs["loss"] == np.float32(1.0 / C)
+    scale = -2.0 / (B * C)
+    np.testing.assert_allclose(outs["gb1"], scale * y.sum(0), rtol=1e-6)
+    np.testing.assert_allclose(outs["gW1"], scale * (y.T @ x), rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(outs["W1_new"], -cfg.lr * outs["gW1"], rtol=1e-6, atol=1e-9)
 
 
 def test_residual_loss_closed_form_with_zero_second_layer():

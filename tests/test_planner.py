@@ -265,9 +265,34 @@ def test_reduction_epilogue_fuses_the_bias_update():
            Operation("bn", "sub", (b, f32("gb", (8,))), f32("bn", (8,)), {"alpha": 0.5})]
     s = plan(Program([g, b], [f32("bn", (8,))], ops, {0: 1}))
     assert (s["fused_epilogues"], s["materialized_ops"], s["stages"], s["direct_state_commits"]) == (1, 1, 1, 1)
-    # a returned gradient is not fused (the chain would have to pass through it)
+    # a returned gradient is stored, and the update is written next to it as
+    # a side output of the same reduction (one op, one stage); without
+    # epilogue fusion it is a second pass behind a barrier
     s = plan(Program([g, b], [f32("bn", (8,)), f32("gb", (8,))], ops, {0: 1}))
+    assert (s["fused_epilogues"], s["materialized_ops"], s["stages"], s["direct_state_commits"]) == (1, 1, 1, 1)
+    s = plan(Program([g, b], [f32("bn", (8,)), f32("gb", (8,))], ops, {0: 1}), fuse_epilogues=0)
     assert (s["fused_epilogues"], s["materialized_ops"], s["stages"]) == (0, 2, 2)
+
+
+def test_loaded_side_outputs_write_the_momentum_step_from_the_tile():
+    # momentum: the weight-gradient GEMM writes v' = 0.9 v + gW (its chain) and
+    # W' = W - lr v' (a side output loading W); both in place, both direct,
+    # after the input-gradient GEMM that reads the old W
+    prog = S.mlp_step_program(S.CONFIGS["c3"], export="state")
+    h = B.tk_program_create(prog, B.options(sm_count=152), device=-1)
+    try:
+        st = B.tk_plan_stats_get(h)
+        tasks = [B.tk_plan_task(h, i) for i in range(st["tasks"])]
+    finally:
+        B.tk_program_destroy(h)
+    name = lambda t: prog.operations[t["op_index"]].name if t["op_index"] >= 0 else None
+    assert not any(name(t) in ("W1_new", "W2_new", "b1_new", "b2_new") for t in tasks)
+    gw = {name(t): t for t in tasks if name(t) in ("gW1", "gW2")}
+    assert all(t["side_output"] for t in gw.values())
+    ga1 = next(t for t in tasks if name(t) == "ga1")
+    assert gw["gW2"]["stage"] > ga1["stage"]
+    assert st["output_copies"] == 0 and st["direct_state_commits"] == 8
+    assert sum(t["side_output"] for t in tasks if t["kind"] in ("reduce_col", "reduce_final")) == 2
 
 
 def test_side_output_written_from_the_gemm_tile():

@@ -67,7 +67,7 @@ def test_wide_tiles_fused_bit_identical_to_unfused(key, bn):
     unfused = S.mlp_step_program(cfg, export="all")
     arrays = S.mlp_inputs(cfg, fused)
     a, sa = run_step(fused, arrays, tile_n=bn)
-    b, _ = run_step(unfused, arrays, tile_n=bn)
+    b, _ = run_step(unfused, arrays, tile_n=bn, fuse_epilogues=0)
     tiles = tc_tasks(sa)
     assert all(t["tile_n"] == bn for t in tiles)
     assert any(t["staged_epilogue"] for t in tiles)
@@ -120,7 +120,7 @@ def test_full_ffn_block_fused_bit_identical_to_unfused():
     unfused = S.mlp_step_program(cfg, export="all")
     arrays = S.mlp_inputs(cfg, fused)
     a, _ = run_step(fused, arrays)
-    b, _ = run_step(unfused, arrays)
+    b, _ = run_step(unfused, arrays, fuse_epilogues=0)
     names_b = {s.buffer: v for s, v in zip(unfused.outputs, b)}
     for s, v in zip(fused.outputs, a):
         np.testing.assert_array_equal(v, names_b[s.buffer], err_msg=s.buffer)
@@ -162,7 +162,7 @@ def test_full_gemm_bound_fused_bit_identical_to_unfused():
     unfused = S.mlp_step_program(C5_TWO, export="all")
     arrays = S.mlp_inputs(C5_TWO, fused)
     a, sa = run_on_device(fused, arrays)
-    b, _ = run_on_device(unfused, arrays)
+    b, _ = run_on_device(unfused, arrays, fuse_epilogues=0)
     tiles = tc_tasks(sa)
     assert any(t["staged_epilogue"] and t["side_output"] and t["tile_n"] == 256 for t in tiles)
     names_b = {s.buffer: v for s, v in zip(unfused.outputs, b)}

@@ -167,7 +167,7 @@ typedef struct {
   int32_t compiled_tasks;      /* tasks whose expression runs as a compiled loop of a fixed shape */
   int32_t chain_tasks;         /* tasks evaluating a generic linear chain (the rest use instructions) */
   int32_t tasks;               /* device tasks (see tk_plan_task) */
-  int32_t reserved0;           /* 0 */
+  int32_t tma_descriptors;     /* TMA descriptors a launch passes (GEMM operand tiles, epilogue chunks) */
 } tk_plan_stats;
 
 /* One device task of a plan: a scheduled op (with whatever the planner fused

@@ -63,7 +63,7 @@ class tk_plan_stats(ctypes.Structure):
         "direct_outputs", "direct_state_commits", "max_work_items", "grid_blocks", "output_copies",
         "split_reductions")] + [("workspace_elements", ctypes.c_int64), ("arena_elements", ctypes.c_int64),
         ("compiled_tasks", ctypes.c_int32), ("chain_tasks", ctypes.c_int32), ("tasks", ctypes.c_int32),
-        ("reserved0", ctypes.c_int32)]
+        ("tma_descriptors", ctypes.c_int32)]
 
 
 class tk_task_info(ctypes.Structure):

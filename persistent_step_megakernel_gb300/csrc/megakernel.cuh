@@ -1471,7 +1471,10 @@ struct TcState {
   uint32_t tmem;                  // TMEM base address
   uint32_t stg;                   // shared address of the epilogue staging area
   uint32_t stg_warp_bytes;        // staging bytes per epilogue warp
+  uint32_t epi_bar;               // 2 mbarriers per epilogue warp (staged-epilogue operand loads)
+  const CUtensorMap* maps;        // the launch's TMA descriptors
   uint32_t p_it, m_it, m_tile, e_tile;
+  uint32_t e_ld;                  // this epilogue warp's staged chunk loads so far
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -1918,40 +1921,19 @@ __device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
-// Store a staged 32 x 32 chunk (16-bit values), four lanes per 64-byte row:
-// lane l stores piece l & 3 of rows l / 4 + 8i, i = 0..3 (the swizzle of
-// those rows is the same, so their shared addresses are 512 bytes apart).
-__device__ __forceinline__ void stage_store(uint32_t buf, char* out, int64_t row0, int64_t col0, int64_t M,
-                                            int64_t N) {
-  const int lane = threadIdx.x & 31, lr = lane >> 2, j = lane & 3;
-  if (col0 + 8 * j >= N) return;
-  const uint32_t s0 = buf + stg_off(lr, j);
-  char* g0 = out + ((row0 + lr) * N + col0 + 8 * j) * 2;
-  const int64_t gstep = 8 * N * 2;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 val = lds128(s0 + 512 * i);
-    if (row0 + lr + 8 * i < M) *reinterpret_cast<uint4*>(g0 + i * gstep) = val;
-  }
-}
-
 // A GEMM's side output from a staged chunk: each lane turns its row of the
-// stored (rounded) values into the side values in place, then the chunk goes
-// to out2.  Called after the chunk's own store (a __syncwarp apart).  A
-// loaded side reads its operand's chunk from `opnd` (staged like the per-row
-// operands) and writes the side values there instead.
-__device__ __noinline__ void stage_side(const Task& t, uint32_t buf, uint32_t opnd, int64_t row0, int64_t col0,
-                                        int64_t M, int64_t N, int out_dt, char* out2) {
+// stored (rounded) values in `buf` into the side values and writes them to
+// `dst` (buf itself, or for a loaded side the buffer holding its operand,
+// read from there).  The caller stores dst.
+__device__ __noinline__ void stage_side(const Task& t, uint32_t buf, uint32_t dst, int out_dt) {
   const int lane = threadIdx.x & 31;
   const bool loaded = t.side.ext == EXT_LOAD1;
-  const uint32_t dst = loaded ? opnd : buf;
-  __syncwarp();
 #pragma unroll 1
   for (int v = 0; v < 4; ++v) {
     float x[8], e[8];
     unpack8(lds128(buf + stg_off(lane, v)), out_dt, x);
     if (loaded) {
-      unpack8(lds128(opnd + stg_off(lane, v)), t.side_ld.dtype, e);
+      unpack8(lds128(dst + stg_off(lane, v)), t.side_ld.dtype, e);
       const bool sub = t.side.op == OP_SUB, second = t.side.second;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -1968,118 +1950,168 @@ __device__ __noinline__ void stage_side(const Task& t, uint32_t buf, uint32_t op
     }
     sts128(dst + stg_off(lane, v), pack8(x, t.out2.dtype));  // rounds to the side's type
   }
-  __syncwarp();
-  stage_store(dst, out2, row0, col0, M, N);
 }
 
-// Returns false if the accumulator wait timed out.  An operand with one row
-// for all tile rows (a bias) is staged once per tile: its tile_n values.
+// TMA store of a staged 32 x 32 chunk (64-byte swizzle) at (col, row) of the
+// tensor behind `map`; rows and columns beyond the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// every committed bulk store of this thread has finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// every committed bulk store of this thread has completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Returns false if a wait timed out.  Per-row operands (the target, the ReLU
+// mask input, the parameter being updated, a loaded side's operand) arrive as
+// 32 x 32 TMA boxes into two buffer halves per operand, one chunk ahead, on
+// this warp's two mbarriers (*eld counts the chunk loads the warp has made:
+// it selects the half and the phase parity).  Each lane then turns its row of
+// the chunk into outputs in shared memory (in place in the first per-row
+// operand's half, else in the `only` buffer), and lane 0 stores the chunk with
+// a TMA store; a side output follows the same way.  A buffer is refilled only
+// after the stores reading it have finished reading.  An operand with one row
+// for all tile rows (a bias) is copied once per tile by cp.async: its tile_n
+// values.
 template <int K>
 __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int64_t m0, int64_t n0, uint32_t taddr,
-                                                uint32_t stg, uint32_t acc_bar, uint32_t phase, long long* stamp) {
+                                                uint32_t stg, uint32_t acc_bar, uint32_t phase, long long* stamp,
+                                                const CUtensorMap* maps, uint32_t ebar, uint32_t* eld) {
   const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
-  const int64_t row0 = m0 + q * 32;
-  const int64_t M = t.m, N = t.n;
+  const int row0 = int(m0) + q * 32;
   const int nch = t.tile_n / 32;
   const int mask = t.epi_stage;
   constexpr bool L0 = FastTraits<K>::load0, L1 = FastTraits<K>::load1;
   const bool st0 = L0 && (mask & 1), st1 = L1 && (mask & 2);
-  const Fast F = fast_params(c, t);
-  // per warp: two chunk buffers per per-row slot (slot 0's first), then one
-  // kBcastBytes row per one-row slot, then (only without per-row slots) the
-  // output buffer; the output otherwise reuses the first per-row slot's
-  // current buffer
-  const uint32_t b0 = stg, b1 = b0 + (st0 ? 2 * kEpiBufBytes : 0);
-  const uint32_t r0 = b1 + (st1 ? 2 * kEpiBufBytes : 0);
-  const uint32_t r1 = r0 + (L0 && !st0 ? kBcastBytes : 0);
-  const uint32_t only = r1 + (L1 && !st1 ? kBcastBytes : 0);
-  // the operand of a loaded side output: two chunk buffers after the rest
   const bool sl = t.has_side && t.side.ext == EXT_LOAD1 && (mask & 8);
+  const Fast F = fast_params(c, t);
+  // per warp, every piece a multiple of 512 bytes (the 64-byte swizzle's
+  // alignment): two halves per per-row operand, the output buffer when there
+  // is no per-row operand, two halves for a loaded side's operand, then one
+  // kBcastBytes row per one-row operand
+  const uint32_t b0 = stg, b1 = b0 + (st0 ? 2 * kEpiBufBytes : 0);
+  const uint32_t only = b1 + (st1 ? 2 * kEpiBufBytes : 0);
   const uint32_t bs = only + (st0 || st1 ? 0 : kEpiBufBytes);
-  const char* const sp = sl ? space_ptr(c, t.side_ld.space, t.side_ld.slot) + t.side_ld.base * 2 : nullptr;
-  char* const out2 = t.has_side ? space_ptr(c, t.out2.space, t.out2.slot) + t.out2.base * 2 : nullptr;
+  const uint32_t r0 = bs + (sl ? 2 * kEpiBufBytes : 0);
+  const uint32_t r1 = r0 + (L0 && !st0 ? kBcastBytes : 0);
+  const bool loads = st0 || st1 || sl;
+  const uint32_t ld_bytes = uint32_t(int(st0) + int(st1) + int(sl)) * kEpiBufBytes;
+  const uint32_t it = *eld;
+  const int64_t col_base = n0;
 
-  // The loops below stay rolled: the code is small enough to stay in the
-  // instruction cache, which matters more than loop overhead for the small
-  // tiles of latency-bound steps (the first chunk of a stage otherwise waits
-  // for its instructions).
-  // per-row operands of chunk ch, in the same lane pattern as stage_store
-  const int lr = lane >> 2, lj = lane & 3;
-  auto prefetch = [&](int ch) {
-    if (!(st0 || st1 || sl)) return;
-    const int64_t col = n0 + 32 * ch + 8 * lj;
-    if (col >= N) return;
-    const uint32_t off = uint32_t(ch & 1) * kEpiBufBytes + stg_off(lr, lj);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t row = row0 + lr + 8 * i;
-      if (row < M) {
-        if (st0) cp_async16(b0 + off + 512 * i, F.p0 + row * F.rs0 + col * 2);
-        if (st1) cp_async16(b1 + off + 512 * i, F.p1 + row * F.rs1 + col * 2);
-        if (sl) cp_async16(bs + off + 512 * i, sp + (row * N + col) * 2);
-      }
-    }
+  auto load = [&](int ch) {  // lane 0
+    const uint32_t k = it + uint32_t(ch), h = k & 1u, bar = ebar + 8 * h, off = h * kEpiBufBytes;
+    const int x = int(col_base) + 32 * ch;
+    mbar_expect_tx(bar, ld_bytes);
+    if (st0) tma_load_2d(b0 + off, &maps[t.tma_ld0], x, row0, bar);
+    if (st1) tma_load_2d(b1 + off, &maps[t.tma_ld1], x, row0, bar);
+    if (sl) tma_load_2d(bs + off, &maps[t.tma_sd], x, row0, bar);
   };
 
-  // one-row operands: 8 values per lane, with chunk 0
+  // one-row operands: 8 values per lane, once per tile
   {
     const int64_t col = n0 + 8 * lane;
-    if (8 * lane < t.tile_n && col < N) {
+    if (8 * lane < t.tile_n && col < t.n) {
       if (L0 && !st0) cp_async16(r0 + 16 * lane, F.p0 + col * 2);
       if (L1 && !st1) cp_async16(r1 + 16 * lane, F.p1 + col * 2);
     }
   }
-  prefetch(0);
   cp_async_commit();
-  if (!mbar_wait(acc_bar, phase, c.timeout_ns)) {
-    cp_async_wait<0>();
-    return false;
+  int issued = 0;  // chunk loads issued (lane 0)
+  if (loads && lane == 0) {
+    bulk_wait_read();  // the previous tile's stores are done with the buffers
+    load(0);
+    issued = 1;
   }
-  if (stamp) *stamp = global_ns();
+  bool ok = mbar_wait(acc_bar, phase, c.timeout_ns);
+  if (ok && stamp) *stamp = global_ns();
   tc_fence_after();
+  cp_async_wait<0>();
+  __syncwarp();
   const uint32_t tlane = taddr + (uint32_t(q * 32) << 16);
+  int ch = 0;
 #pragma unroll 1
-  for (int ch = 0; ch < nch; ++ch) {
-    if (ch + 1 < nch) prefetch(ch + 1);
-    cp_async_commit();
-    cp_async_wait<1>();
+  for (; ok && ch < nch; ++ch) {
+    const uint32_t k = it + uint32_t(ch), h = k & 1u, half = h * kEpiBufBytes;
+    const int col0 = int(col_base) + 32 * ch;
+    if (lane == 0) {
+      // the output buffer (without per-row operands) and the half the next
+      // load fills were last read by chunk ch - 1's stores
+      const bool more = loads && ch + 1 < nch;
+      if (more || !(st0 || st1)) bulk_wait_read();
+      if (more) {
+        load(ch + 1);
+        issued = ch + 2;
+      }
+    }
+    if (loads && !mbar_wait(ebar + 8 * h, (k >> 1) & 1u, c.timeout_ns)) {
+      ok = false;
+      break;
+    }
     __syncwarp();
-    const int64_t col0 = n0 + 32 * ch;
-    const uint32_t half = uint32_t(ch & 1) * kEpiBufBytes;
     const uint32_t ob = st0 ? b0 + half : (st1 ? b1 + half : only);
+    uint32_t rv[32];
+    tmem_ld32(tlane + uint32_t(32 * ch), rv);
     // one 8-wide vector at a time: this thread's row, read and written in place
-#pragma unroll 1
+#pragma unroll
     for (int v = 0; v < 4; ++v) {
-      uint32_t rv[8];
-      tmem_ld8(tlane + uint32_t(32 * ch + 8 * v), rv);
       float l0[8], l1[8], a8[8], x[8];
       if constexpr (L0) unpack8(lds128(st0 ? b0 + half + stg_off(lane, v) : r0 + 64 * ch + 16 * v), F.dt0, l0);
       if constexpr (L1) unpack8(lds128(st1 ? b1 + half + stg_off(lane, v) : r1 + 64 * ch + 16 * v), F.dt1, l1);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) a8[j] = __uint_as_float(rv[j]);
+      for (int j = 0; j < 8; ++j) a8[j] = __uint_as_float(rv[8 * v + j]);
       fast_apply<K, false>(F, l0, l1, a8, x);
       sts128(ob + stg_off(lane, v), pack8(x, F.out_dt));
     }
+    fence_async_smem();
     __syncwarp();
-    stage_store(ob, F.out, row0, col0, M, N);
-    if (t.has_side) stage_side(t, ob, bs + half, row0, col0, M, N, F.out_dt, out2);
-    __syncwarp();
+    if (lane == 0) tma_store_2d(&maps[t.tma_out], ob, col0, row0);
+    if (t.has_side) {
+      if (!sl) {  // the side values replace the outputs in ob once the store has read them
+        if (lane == 0) {
+          bulk_commit();
+          bulk_wait_read();
+        }
+        __syncwarp();
+      }
+      const uint32_t dst = sl ? bs + half : ob;
+      stage_side(t, ob, dst, F.out_dt);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) tma_store_2d(&maps[t.tma_out2], dst, col0, row0);
+    }
+    if (lane == 0) bulk_commit();
   }
-  cp_async_wait<0>();
-  return true;
+  if (!ok && lane == 0) {
+    // a wait gave up: the loads already issued land, and the stores already
+    // issued finish, before the block moves on
+    for (int j = ch; j < issued; ++j) {
+      const uint32_t k = it + uint32_t(j);
+      mbar_wait(ebar + 8 * (k & 1u), (k >> 1) & 1u, c.timeout_ns);
+    }
+    bulk_wait_all();
+  }
+  __syncwarp();
+  *eld = it + (loads ? uint32_t(nch) : 0u);
+  return ok;
 }
 
 __device__ __noinline__ bool tc_epilogue_staged_any(const Ctx c, const Task& t, int64_t m0, int64_t n0,
                                                     uint32_t taddr, uint32_t stg, uint32_t acc_bar, uint32_t phase,
-                                                    long long* stamp) {
+                                                    long long* stamp, const CUtensorMap* maps, uint32_t ebar,
+                                                    uint32_t* eld) {
   switch (t.chain.fast) {
-    case FK_E_ACC: return tc_epilogue_staged<FK_E_ACC>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp);
-    case FK_E_BIAS: return tc_epilogue_staged<FK_E_BIAS>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp);
-    case FK_E_BIAS_RELU: return tc_epilogue_staged<FK_E_BIAS_RELU>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp);
-    case FK_E_BIAS_AXPY: return tc_epilogue_staged<FK_E_BIAS_AXPY>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp);
-    case FK_E_ACC_THRESH: return tc_epilogue_staged<FK_E_ACC_THRESH>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp);
-    case FK_E_MOMENTUM: return tc_epilogue_staged<FK_E_MOMENTUM>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp);
-    default: return tc_epilogue_staged<FK_E_UPDATE>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp);
+    case FK_E_ACC: return tc_epilogue_staged<FK_E_ACC>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
+    case FK_E_BIAS: return tc_epilogue_staged<FK_E_BIAS>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
+    case FK_E_BIAS_RELU: return tc_epilogue_staged<FK_E_BIAS_RELU>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
+    case FK_E_BIAS_AXPY: return tc_epilogue_staged<FK_E_BIAS_AXPY>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
+    case FK_E_ACC_THRESH: return tc_epilogue_staged<FK_E_ACC_THRESH>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
+    case FK_E_MOMENTUM: return tc_epilogue_staged<FK_E_MOMENTUM>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
+    default: return tc_epilogue_staged<FK_E_UPDATE>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
   }
 }
 
@@ -2283,11 +2315,12 @@ __device__ __noinline__ uint64_t tc_mma(const Ctx c, const Stage st, const TcSta
 }
 
 __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const TcState ts, uint32_t e_tile,
-                                             long long* prof) {
+                                             long long* prof, uint32_t* e_ld) {
   bool ok = true;
   bool first = true;
   const int lane = threadIdx.x & 31;
-  const uint32_t stg = ts.stg + uint32_t((threadIdx.x >> 5) - 4) * ts.stg_warp_bytes;
+  const uint32_t ew = uint32_t(threadIdx.x >> 5) - 4;
+  const uint32_t stg = ts.stg + ew * ts.stg_warp_bytes, ebar = ts.epi_bar + 16 * ew;
   for_my_tiles(c, st, [&](const Task& t, const TileItem& it) {
     const int64_t m0 = it.m0, n0 = it.n0;
     const uint32_t acc = e_tile & 1u, ph = (e_tile >> 1) & 1u;
@@ -2299,7 +2332,8 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
       tc_fence_after();
       tc_epilogue_partial(c, t, m0, n0, it.split, ts.tmem + acc * kMaxTileN);
     } else if (t.epi_stage) {
-      if (!tc_epilogue_staged_any(c, t, m0, n0, ts.tmem + acc * kMaxTileN, stg, ts.acc_full + 8 * acc, ph, stamp))
+      if (!tc_epilogue_staged_any(c, t, m0, n0, ts.tmem + acc * kMaxTileN, stg, ts.acc_full + 8 * acc, ph, stamp,
+                                  ts.maps, ebar, e_ld))
         return ok = false;
     } else {
       if (!mbar_wait(ts.acc_full + 8 * acc, ph, c.timeout_ns)) return ok = false;
@@ -2313,6 +2347,9 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
     ++e_tile;
     return true;
   });
+  // the stage's TMA stores complete before the block reaches the grid barrier
+  if (lane == 0) bulk_wait_all();
+  __syncwarp();
   return (uint64_t(ok) << 32) | e_tile;
 }
 
@@ -2334,8 +2371,10 @@ __device__ bool run_tc_phase(const Ctx& c, const Stage& st, const CUtensorMap* m
     ok = (r >> 32) != 0;
     if (prof) prof[4] = global_ns();
   } else if (warp >= 4) {
-    const uint64_t r = tc_epilogue(c, st, ts, ts.e_tile, prof);
+    uint32_t e_ld = ts.e_ld;
+    const uint64_t r = tc_epilogue(c, st, ts, ts.e_tile, prof, &e_ld);
     ts.e_tile = uint32_t(r);
+    ts.e_ld = e_ld;
     ok = (r >> 32) != 0;
     if (prof && threadIdx.x == 128) prof[6] = global_ns();
   }
@@ -2437,6 +2476,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   __shared__ Stage s_stage;
   __shared__ Prep s_prep[kThreads / 32];
   __shared__ __align__(8) uint64_t s_bar[2 * kStages + 5];
+  __shared__ __align__(8) uint64_t s_epi_bar[8];
   __shared__ __align__(8) uint64_t s_bulk_bar[kBulkMaxSlots];
   __shared__ uint32_t s_bulk_it;
   __shared__ __align__(8) uint64_t s_col_bar[kBulkMaxSlots];
@@ -2465,6 +2505,8 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     ts.acc_full = smem_u32(&s_bar[2 * kStages]);
     ts.acc_empty = smem_u32(&s_bar[2 * kStages + 2]);
     ts.drain = smem_u32(&s_bar[2 * kStages + 4]);
+    ts.epi_bar = smem_u32(&s_epi_bar[0]);
+    ts.maps = maps;
     if (threadIdx.x == 0) {
       for (int i = 0; i < kStages; ++i) {
         mbar_init(ts.full + 8 * i, 1);
@@ -2475,6 +2517,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
         mbar_init(ts.acc_empty + 8 * i, 4);
       }
       mbar_init(ts.drain, 1);
+      for (int i = 0; i < 8; ++i) mbar_init(ts.epi_bar + 8 * i, 1);
       for (int i = 0; i < kBulkMaxSlots; ++i) {
         mbar_init(smem_u32(&s_bulk_bar[i]), 1);
         mbar_init(smem_u32(&s_col_bar[i]), kThreads);

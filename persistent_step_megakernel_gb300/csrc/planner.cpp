@@ -1238,6 +1238,7 @@ class Planner {
     if (t.numel >= (int64_t(1) << 31)) throw Error(TK_ERR_UNSUPPORTED, "tensors of 2^31 or more elements");
     t.vec = (t.rank >= 1 && t.shape[t.rank - 1] % 8 == 0 && t.numel > 0) ? 8 : 1;
     t.tma_a = t.tma_b = -1;
+    t.tma_out = t.tma_out2 = t.tma_ld0 = t.tma_ld1 = t.tma_sd = -1;
     t.op_index = -1;
     t.k_splits = 1;
     return t;
@@ -1468,11 +1469,65 @@ class Planner {
     return true;
   }
 
+  // Index of TMA descriptor o in the plan, shared with an equal one.
+  static int map_index(Plan& plan, const TmaOperand& o) {
+    for (size_t i = 0; i < plan.tma.size(); ++i)
+      if (plan.tma[i] == o) return int(i);
+    plan.tma.push_back(o);
+    return int(plan.tma.size()) - 1;
+  }
+
+  // A 32 x 32 epilogue-chunk descriptor over an [m, n] view with row stride
+  // `row` (elements) at ref r's location.
+  static TmaOperand chunk_map(const Ref& r, int64_t m, int64_t n, int64_t row) {
+    TmaOperand o{};
+    o.space = r.space;
+    o.slot = r.slot;
+    o.base_elems = r.base;
+    o.dtype = r.dtype;
+    o.inner = n;
+    o.outer = m;
+    o.outer_stride = row;
+    o.box_inner = 32;
+    o.box_outer = 32;
+    o.swizzle = 1;
+    return o;
+  }
+
+  // Descriptors for a staged epilogue (false, and nothing added, when they do
+  // not fit the descriptor budget).
+  bool epilogue_maps(Plan& plan, Task& t, int mask) const {
+    std::vector<TmaOperand> want;
+    auto add = [&](const Ref& r, int64_t row) {
+      want.push_back(chunk_map(r, t.m, t.n, row));
+      return int(want.size()) - 1;
+    };
+    int out = add(t.out, t.n), out2 = -1, ld0 = -1, ld1 = -1, sd = -1;
+    if (t.has_side) out2 = add(t.out2, t.n);
+    if (mask & 1) ld0 = add(plan.refs[t.ref_begin + t.chain.load_ref[0]], plan.refs[t.ref_begin + t.chain.load_ref[0]].stride[0]);
+    if (mask & 2) ld1 = add(plan.refs[t.ref_begin + t.chain.load_ref[1]], plan.refs[t.ref_begin + t.chain.load_ref[1]].stride[0]);
+    if (mask & 8) sd = add(t.side_ld, t.n);
+    size_t extra = 0;
+    for (const auto& o : want) {
+      bool have = false;
+      for (const auto& p : plan.tma) have = have || p == o;
+      extra += have ? 0 : 1;
+    }
+    if (plan.tma.size() + extra > size_t(tkd::kMaxMaps)) return false;
+    auto idx = [&](int i) { return i < 0 ? -1 : map_index(plan, want[size_t(i)]); };
+    t.tma_out = idx(out);
+    t.tma_out2 = idx(out2);
+    t.tma_ld0 = idx(ld0);
+    t.tma_ld1 = idx(ld1);
+    t.tma_sd = idx(sd);
+    return true;
+  }
+
   bool try_tensor_core(Plan& plan, Task& t, const tk_tensor_spec& A, const tk_tensor_spec& B) const {
     if (!opt_.tensor_cores || A.dtype != B.dtype || (A.dtype != TK_BF16 && A.dtype != TK_F16)) return false;
     const int64_t M = t.m, N = t.n, K = t.k;
     if (M < 1 || N < 1 || K < 1) return false;
-    if (plan.tma.size() + 2 > size_t(tkd::kMaxMaps)) return false;
+    if (plan.tma.size() + 2 > size_t(tkd::kMaxMaps)) return false;  // (a bound: equal maps are shared)
     // widest N tile that still spreads the tiles over the SMs (or the forced width)
     int bn = 64;
     for (int cand : {256, 128}) {
@@ -1493,10 +1548,8 @@ class Planner {
     t.n_items = int(ceil_div(M, tkd::kTileM) * t.tiles_n);
     t.a_mn_major = a_mn;
     t.b_mn_major = b_mn;
-    t.tma_a = int(plan.tma.size());
-    plan.tma.push_back(ta);
-    t.tma_b = int(plan.tma.size());
-    plan.tma.push_back(tb);
+    t.tma_a = map_index(plan, ta);
+    t.tma_b = map_index(plan, tb);
     // instruction descriptor, kind::f16: D f32 (bits 4-5), A/B type (7-9, 10-12:
     // 0 f16, 1 bf16), A/B MN-major (15, 16), N >> 3 (17-22), M >> 4 (24-28)
     uint32_t ab = A.dtype == TK_BF16 ? 1u : 0u;
@@ -2094,10 +2147,13 @@ class Planner {
     const size_t ring = 1024 + size_t(tkd::kStages) * plan.ring_stage_bytes;
     for (auto& t : plan.tasks) {
       t.epi_stage = 0;
+      t.tma_out = t.tma_out2 = t.tma_ld0 = t.tma_ld1 = t.tma_sd = -1;
       const int need = epi_stage_plan(plan, t);
       if (need > 0 && ring + 4 * size_t(std::max(need, plan.epi_warp_bytes)) <= size_t(tkd::kDynSmemBudget)) {
+        const int mask = epi_stage_mask(plan, t);
+        if (!epilogue_maps(plan, t, mask)) continue;
         plan.epi_warp_bytes = std::max(plan.epi_warp_bytes, need);
-        t.epi_stage = epi_stage_mask(plan, t);
+        t.epi_stage = mask;
       }
     }
     plan.smem_bytes = plan.uses_tc ? ring + 4 * size_t(plan.epi_warp_bytes) : 1024 + size_t(tkd::kWorkFloats) * 4;
@@ -2120,6 +2176,7 @@ class Planner {
     st.workspace_elements = plan.workspace_units;
     st.arena_elements = arena_total_;
     st.tasks = int(plan.tasks.size());
+    st.tma_descriptors = int(plan.tma.size());
     for (const auto& t : plan.tasks) {
       if (t.chain.valid && t.chain.fast != tkd::FK_NONE) ++st.compiled_tasks;
       else if (t.chain.valid) ++st.chain_tasks;

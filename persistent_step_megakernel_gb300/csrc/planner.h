@@ -27,6 +27,16 @@ struct TmaOperand {
   // (a 3-D view: MN within the slab, K, slab), stacked 8 KB apart in shared
   // memory exactly as `chunks` separate 2-D boxes would be.
   int32_t chunks;
+  // Shared-memory layout: 0 = 128-byte swizzle (GEMM operand tiles), 1 =
+  // 64-byte swizzle (32 x 32 epilogue chunks: loads of per-row operands and
+  // stores of the outputs).
+  int32_t swizzle;
+
+  bool operator==(const TmaOperand& o) const {
+    return space == o.space && slot == o.slot && base_elems == o.base_elems && dtype == o.dtype && inner == o.inner &&
+           outer == o.outer && outer_stride == o.outer_stride && box_inner == o.box_inner &&
+           box_outer == o.box_outer && chunks == o.chunks && swizzle == o.swizzle;
+  }
 };
 
 struct Plan {

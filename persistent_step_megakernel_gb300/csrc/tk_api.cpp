@@ -172,9 +172,12 @@ tk_status encode_maps(tk_program* p, const void* const* inputs, void* const* out
       dims[2] = cuuint64_t(o.inner / 64);
       box[2] = cuuint32_t(o.chunks);
     }
+    // GEMM operand tiles: 128-byte swizzle (the MMA descriptors' layout);
+    // epilogue chunks (32 x 64 bytes): 64-byte swizzle (the staging layout)
+    const CUtensorMapSwizzle sw = o.swizzle == 1 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
     CUresult r = fn(&maps[i], o.dtype == TK_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                    slabs ? 3 : 2, addr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    slabs ? 3 : 2, addr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(TK_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string(int(r)) + ")");
   }
   p->maps.swap(maps);

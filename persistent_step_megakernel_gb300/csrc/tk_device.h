@@ -218,6 +218,10 @@ struct alignas(16) Task {
   // copied through shared memory too.  0 = operands and output accessed
   // directly.
   int32_t epi_stage;
+  // TMA descriptors of a staged epilogue's 32 x 32 chunks (64-byte swizzle,
+  // the staging layout): the output, the side output, the per-row operands
+  // of load slots 0 and 1 and the loaded side's operand (-1: none).
+  int32_t tma_out, tma_out2, tma_ld0, tma_ld1, tma_sd;
   int32_t pw_unroll;         // pointwise items: vectors per thread (kPointwiseUnroll or kPointwiseUnroll16)
   // Split-K (under-filled tensor-core GEMMs): item = tile * k_splits + split;
   // split s covers k blocks [s * kb_split, (s + 1) * kb_split) and writes its

@@ -137,35 +137,37 @@ class Clocks:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, power, reasons, busy = [], [], [], set(), 0
+        """Median SM clock over the samples taken while the GPU was busy (all
+        samples when none reported utilisation), the maximum, and every
+        throttle reason seen."""
+        parsed = []
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
                 continue
             try:
-                util = float(parts[7])
                 clock, top = float(parts[0]), float(parts[1])
             except ValueError:
                 continue
-            if util <= 0:
-                continue                      # idle sample (before or after the loop)
-            busy += 1
-            sm.append(clock)
-            mx.append(top)
             try:
-                power.append(float(parts[2]))
+                util = float(parts[7])
             except ValueError:
-                pass
-            for n, v in zip(names, parts[3:7]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "samples_total": len(self.lines)}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": busy, "samples_total": len(self.lines),
-                "power_w_max": max(power) if power else None}
+                util = 0.0
+            try:
+                power = float(parts[2])
+            except ValueError:
+                power = None
+            active = {n for n, v in zip(names, parts[3:7]) if v.lower().startswith("active")}
+            parsed.append((clock, top, util, power, active))
+        if not parsed:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "samples_busy": 0}
+        busy = [p for p in parsed if p[2] > 0]
+        use = busy or parsed
+        powers = [p[3] for p in use if p[3] is not None]
+        return {"sm_mhz": statistics.median(p[0] for p in use), "sm_max_mhz": max(p[1] for p in use),
+                "reasons": sorted(set().union(*(p[4] for p in parsed))), "samples": len(parsed),
+                "samples_busy": len(busy), "power_w_max": max(powers) if powers else None}
 
 
 def dist_setup(world: int, backend: str = "nccl"):

@@ -67,3 +67,15 @@ def test_sampled_oracle_rate_scales_to_whole_steps():
 def test_back_to_back_batches_follow_the_step_size():
     assert bench.batch_steps_for(S.CONFIGS["c5"]) == 20
     assert bench.batch_steps_for(S.CONFIGS["c2"]) == 100
+
+
+def test_clock_summary_uses_busy_samples_and_keeps_every_reason():
+    c = bench.Clocks(0)
+    c.lines = ["2070, 2070, 500.1, Not Active, Not Active, Not Active, Active, 95",
+               "1900, 2070, 300.0, Not Active, Not Active, Not Active, Not Active, 0",
+               "2055, 2070, 640.0, Not Active, Not Active, Not Active, Not Active, 90"]
+    s = c.summary()
+    assert s["sm_mhz"] == 2062.5 and s["sm_max_mhz"] == 2070 and s["samples"] == 3 and s["samples_busy"] == 2
+    assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 640.0
+    c.lines = ["1900, 2070, 300.0, Not Active, Not Active, Not Active, Not Active, 0"]
+    assert c.summary()["sm_mhz"] == 1900                     # no busy sample: all samples

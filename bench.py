@@ -436,7 +436,8 @@ def run_reference(args, rank, world):
 # ------------------------------------------------------------ modes
 
 def stage_profile(cfg, device, warmup=5):
-    """Per-stage work and barrier time of one step (L2 flushed before it)."""
+    """Per-stage work and barrier time of one step, with the L2 flushed before
+    the step and warm (back to back), from the kernel's %globaltimer stamps."""
     import torch
     from persistent_step_megakernel_gb300.runtime import TrainStep
     prog = S.mlp_step_program(cfg, export="state")
@@ -444,26 +445,47 @@ def stage_profile(cfg, device, warmup=5):
     ins = device_inputs(cfg, prog, device)
     outs, ws = step.allocate(ins)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
-    runs = []
-    for k in range(warmup + 3):
-        flush.zero_()
-        step.run(ins, outs, ws)
-        torch.cuda.synchronize(device)
-        if k >= warmup:
-            runs.append(step.profile(ws))
-    best = min(runs, key=lambda r: r["total_us"])
     per_stage = {}
     for t in step.tasks():
         per_stage.setdefault(t["stage"], []).append(
             f"{t['kind']}:{t['op'] or 'copy'}" + (f"[{t['m']}x{t['n']}x{t['k']}/{t['tile_n']}]" if t["m"] else ""))
-    stages = [{"stage": s, "work_us": round(w, 2), "barrier_us": round(best["barrier_us"][s], 2)
-               if s < len(best["barrier_us"]) else None, "tasks": per_stage.get(s, [])}
-              for s, w in enumerate(best["work_us"])]
-    bars = best["barrier_us"]
+
+    def timeline(best, s):
+        """Median over the blocks with tensor-core tiles in stage s of the
+        time from the stage's start to: the producer done, the first operand
+        tile landed, the MMA issue done, the first accumulator ready, the
+        epilogue done, the barrier arrival (µs)."""
+        rows = [r for r in best["stamps"][s] if r[3] > 0 and r[0] > 0]
+        if not rows:
+            return None
+        med = lambda i: round(statistics.median((r[i] - r[0]) / 1e3 for r in rows), 2)
+        return {"blocks": len(rows), "producer_done": med(2), "first_tile": med(3), "mma_done": med(4),
+                "first_acc": med(5), "epilogue_done": med(6), "arrive": med(1)}
+
+    def run(flushed):
+        runs = []
+        for k in range(warmup + 3):
+            if flushed:
+                flush.zero_()
+            step.run(ins, outs, ws)
+            if flushed or k >= warmup:
+                torch.cuda.synchronize(device)
+            if k >= warmup:
+                runs.append(step.profile(ws))
+        best = min(runs, key=lambda r: r["total_us"])
+        bars = best["barrier_us"]
+        stages = [{"stage": s, "work_us": round(w, 2),
+                   "barrier_us": round(bars[s], 2) if s < len(bars) else None,
+                   "tasks": per_stage.get(s, []), "tc_timeline": timeline(best, s)}
+                  for s, w in enumerate(best["work_us"])]
+        return {"stages": stages, "total_us": best["total_us"], "prologue_us": best["prologue_us"],
+                "barrier_us_median": statistics.median(bars) if bars else None,
+                "barrier_us_max": max(bars) if bars else None}
+
+    flushed = run(True)
+    warm = run(False)
     return {"workload": cfg.description, "key": cfg.key, "grid_blocks": step.stats["grid_blocks"],
-            "stages": stages, "total_us": best["total_us"], "prologue_us": best["prologue_us"],
-            "barrier_us_median": statistics.median(bars) if bars else None,
-            "barrier_us_max": max(bars) if bars else None, "status": step.status(ws)}
+            "flushed": flushed, "warm": warm, "status": step.status(ws)}
 
 
 def config_record(cfg, m):

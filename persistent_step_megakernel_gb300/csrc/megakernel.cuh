@@ -1962,6 +1962,10 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // every committed bulk store of this thread has finished reading shared memory
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... all but the most recently committed group
+__device__ __forceinline__ void bulk_wait_read_but_last() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 // every committed bulk store of this thread has completed
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -1990,12 +1994,12 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
   const bool sl = t.has_side && t.side.ext == EXT_LOAD1 && (mask & 8);
   const Fast F = fast_params(c, t);
   // per warp, every piece a multiple of 512 bytes (the 64-byte swizzle's
-  // alignment): two halves per per-row operand, the output buffer when there
+  // alignment): two halves per per-row operand, two output halves when there
   // is no per-row operand, two halves for a loaded side's operand, then one
   // kBcastBytes row per one-row operand
   const uint32_t b0 = stg, b1 = b0 + (st0 ? 2 * kEpiBufBytes : 0);
   const uint32_t only = b1 + (st1 ? 2 * kEpiBufBytes : 0);
-  const uint32_t bs = only + (st0 || st1 ? 0 : kEpiBufBytes);
+  const uint32_t bs = only + (st0 || st1 ? 0 : 2 * kEpiBufBytes);
   const uint32_t r0 = bs + (sl ? 2 * kEpiBufBytes : 0);
   const uint32_t r1 = r0 + (L0 && !st0 ? kBcastBytes : 0);
   const bool loads = st0 || st1 || sl;
@@ -2039,10 +2043,12 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
     const uint32_t k = it + uint32_t(ch), h = k & 1u, half = h * kEpiBufBytes;
     const int col0 = int(col_base) + 32 * ch;
     if (lane == 0) {
-      // the output buffer (without per-row operands) and the half the next
-      // load fills were last read by chunk ch - 1's stores
+      // the half the next load fills was last read by chunk ch - 1's stores;
+      // without per-row operands the output half this chunk fills was last
+      // read by chunk ch - 2's stores (chunk ch - 1's last group may still run)
       const bool more = loads && ch + 1 < nch;
-      if (more || !(st0 || st1)) bulk_wait_read();
+      if (more) bulk_wait_read();
+      else if (!(st0 || st1)) bulk_wait_read_but_last();
       if (more) {
         load(ch + 1);
         issued = ch + 2;
@@ -2053,7 +2059,7 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
       break;
     }
     __syncwarp();
-    const uint32_t ob = st0 ? b0 + half : (st1 ? b1 + half : only);
+    const uint32_t ob = st0 ? b0 + half : (st1 ? b1 + half : only + (uint32_t(ch & 1) * kEpiBufBytes));
     uint32_t rv[32];
     tmem_ld32(tlane + uint32_t(32 * ch), rv);
     // one 8-wide vector at a time: this thread's row, read and written in place

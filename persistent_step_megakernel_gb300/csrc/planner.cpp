@@ -1313,7 +1313,7 @@ class Planner {
   }
 
   static int main_stage_bytes(int rows, int bcast) {
-    return (rows ? 2 * rows : 1) * tkd::kEpiBufBytes + bcast * tkd::kBcastBytes;
+    return 2 * (rows ? rows : 1) * tkd::kEpiBufBytes + bcast * tkd::kBcastBytes;
   }
 
   // Recognise the chain shapes the kernel runs as compiled loops (FastKind).

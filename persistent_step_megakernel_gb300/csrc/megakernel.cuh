@@ -1475,6 +1475,9 @@ struct TcState {
   const CUtensorMap* maps;        // the launch's TMA descriptors
   uint32_t p_it, m_it, m_tile, e_tile;
   uint32_t e_ld;                  // this epilogue warp's staged chunk loads so far
+  float* sk_slots;                // stream-K partial slots (sk_slot_floats each, one per block)
+  unsigned* sk_flags;             // stream-K flags (one per block)
+  int sk_slot_floats;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -1776,16 +1779,52 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])::"memory");
 }
 
-// One tensor-core work item: a tile and, for split-K, its range of k blocks.
+// One tensor-core work item: a tile and, for split-K or stream-K, its range
+// of k blocks.  sk: 0 a whole tile (or a split-K part), 1 a stream-K tile's
+// first k blocks (this block finishes the tile), 2 a stream-K tile's later k
+// blocks (this block leaves their partial sum to the finisher).
 struct TileItem {
   int64_t m0, n0;
-  int kb0, kb1, split;
+  int kb0, kb1, split, sk;
 };
+
+// Stream-K: this block's range of the stage's k-block units (see
+// tkd::Stage), cut at tile boundaries.
+template <typename F>
+__device__ __forceinline__ void for_my_segments(const Ctx& c, const Stage& st, F&& fn) {
+  const int64_t U = st.sk_units, G = gridDim.x, b = blockIdx.x;
+  int64_t u = b * U / G;
+  const int64_t u1 = (b + 1) * U / G;
+  int64_t off = 0;
+  for (int ti = st.task_begin; ti < st.task_end && u < u1; ++ti) {
+    const Task& t = c.tasks[ti];
+    if (t.kind != T_GEMM_TC) break;
+    const int64_t kb = t.k_blocks, units = int64_t(t.n_items) * kb;
+    while (u < u1 && u < off + units) {
+      const int64_t rel = u - off;
+      const int tile = int(rel / kb);
+      TileItem it;
+      it.kb0 = int(rel - int64_t(tile) * kb);
+      it.kb1 = int(min(kb, int64_t(it.kb0) + (u1 - u)));
+      it.m0 = int64_t(tile / t.tiles_n) * kTileM;
+      it.n0 = int64_t(tile % t.tiles_n) * t.tile_n;
+      it.split = 0;
+      it.sk = it.kb0 > 0 ? 2 : (it.kb1 < kb ? 1 : 0);
+      if (!fn(t, it)) return;
+      u += it.kb1 - it.kb0;
+    }
+    off += units;
+  }
+}
 
 // Walk this block's tensor-core items of a stage in order (all roles use the
 // same sequence).  fn(task, item) returns false to stop.
 template <typename F>
 __device__ __forceinline__ void for_my_tiles(const Ctx& c, const Stage& st, F&& fn) {
+  if (st.sk) {
+    for_my_segments(c, st, fn);
+    return;
+  }
   int ti = st.task_begin, base = 0;
   for (int g = blockIdx.x; g < st.n_tc_items; g += gridDim.x) {
     while (g >= base + c.tasks[ti].n_items) {
@@ -1798,6 +1837,7 @@ __device__ __forceinline__ void for_my_tiles(const Ctx& c, const Stage& st, F&& 
     it.m0 = int64_t(tile / t.tiles_n) * kTileM;
     it.n0 = int64_t(tile % t.tiles_n) * t.tile_n;
     it.split = split;
+    it.sk = 0;
     it.kb0 = split * t.kb_split;
     it.kb1 = min(t.k_blocks, it.kb0 + t.kb_split);
     if (!fn(t, it)) return;
@@ -1984,7 +2024,8 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 template <int K>
 __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int64_t m0, int64_t n0, uint32_t taddr,
                                                 uint32_t stg, uint32_t acc_bar, uint32_t phase, long long* stamp,
-                                                const CUtensorMap* maps, uint32_t ebar, uint32_t* eld) {
+                                                const CUtensorMap* maps, uint32_t ebar, uint32_t* eld,
+                                                const float* part) {
   const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
   const int row0 = int(m0) + q * 32;
   const int nch = t.tile_n / 32;
@@ -2062,6 +2103,17 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
     const uint32_t ob = st0 ? b0 + half : (st1 ? b1 + half : only + (uint32_t(ch & 1) * kEpiBufBytes));
     uint32_t rv[32];
     tmem_ld32(tlane + uint32_t(32 * ch), rv);
+    if (part) {  // stream-K: the fp32 partial sum of the tile's later k blocks
+      const float4* pp = reinterpret_cast<const float4*>(part + (q * 32 + lane) * t.tile_n + 32 * ch);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 w = __ldcg(pp + j);  // written by another SM: read at L2
+        rv[4 * j] = __float_as_uint(__fadd_rn(__uint_as_float(rv[4 * j]), w.x));
+        rv[4 * j + 1] = __float_as_uint(__fadd_rn(__uint_as_float(rv[4 * j + 1]), w.y));
+        rv[4 * j + 2] = __float_as_uint(__fadd_rn(__uint_as_float(rv[4 * j + 2]), w.z));
+        rv[4 * j + 3] = __float_as_uint(__fadd_rn(__uint_as_float(rv[4 * j + 3]), w.w));
+      }
+    }
     // one 8-wide vector at a time: this thread's row, read and written in place
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
@@ -2109,15 +2161,15 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
 __device__ __noinline__ bool tc_epilogue_staged_any(const Ctx c, const Task& t, int64_t m0, int64_t n0,
                                                     uint32_t taddr, uint32_t stg, uint32_t acc_bar, uint32_t phase,
                                                     long long* stamp, const CUtensorMap* maps, uint32_t ebar,
-                                                    uint32_t* eld) {
+                                                    uint32_t* eld, const float* part) {
   switch (t.chain.fast) {
-    case FK_E_ACC: return tc_epilogue_staged<FK_E_ACC>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
-    case FK_E_BIAS: return tc_epilogue_staged<FK_E_BIAS>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
-    case FK_E_BIAS_RELU: return tc_epilogue_staged<FK_E_BIAS_RELU>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
-    case FK_E_BIAS_AXPY: return tc_epilogue_staged<FK_E_BIAS_AXPY>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
-    case FK_E_ACC_THRESH: return tc_epilogue_staged<FK_E_ACC_THRESH>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
-    case FK_E_MOMENTUM: return tc_epilogue_staged<FK_E_MOMENTUM>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
-    default: return tc_epilogue_staged<FK_E_UPDATE>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
+    case FK_E_ACC: return tc_epilogue_staged<FK_E_ACC>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part);
+    case FK_E_BIAS: return tc_epilogue_staged<FK_E_BIAS>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part);
+    case FK_E_BIAS_RELU: return tc_epilogue_staged<FK_E_BIAS_RELU>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part);
+    case FK_E_BIAS_AXPY: return tc_epilogue_staged<FK_E_BIAS_AXPY>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part);
+    case FK_E_ACC_THRESH: return tc_epilogue_staged<FK_E_ACC_THRESH>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part);
+    case FK_E_MOMENTUM: return tc_epilogue_staged<FK_E_MOMENTUM>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part);
+    default: return tc_epilogue_staged<FK_E_UPDATE>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part);
   }
 }
 
@@ -2320,6 +2372,71 @@ __device__ __noinline__ uint64_t tc_mma(const Ctx c, const Stage st, const TcSta
   return (uint64_t(ok) << 32) | m_it;
 }
 
+// Stream-K hand-off between the block that computes a tile's later k blocks
+// (writer: its 4 epilogue warps each store their 32 rows of the fp32 partial
+// sum, then add 1 to the block's flag) and the block that finishes the tile
+// (each of its 4 epilogue warps waits for the flag to reach 4, adds the
+// partial rows it owns, then adds 1; the fourth to finish sets the flag back
+// to 0 for the next stage).
+__device__ __noinline__ void sk_write_partial(const Task& t, uint32_t taddr, float* slot, unsigned* flag) {
+  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
+  float* row = slot + (q * 32 + lane) * t.tile_n;
+#pragma unroll 1
+  for (int cc = 0; cc < t.tile_n; cc += 32) {
+    uint32_t r[32];
+    __syncwarp();
+    tmem_ld32(taddr + (uint32_t(q * 32) << 16) + uint32_t(cc), r);
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+      *reinterpret_cast<float4*>(row + cc + 4 * v) = make_float4(
+          __uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]), __uint_as_float(r[4 * v + 2]),
+          __uint_as_float(r[4 * v + 3]));
+  }
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) atomicAdd(flag, 1u);
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait (lane 0 polls) for a writer's 4 warps; false if it timed out
+// or another block gave up.
+__device__ __noinline__ bool sk_wait_partial(const Ctx c, const unsigned* flag) {
+  const int lane = threadIdx.x & 31;
+  int ok = 1;
+  if (lane == 0) {
+    unsigned spins = 0;
+    long long t0 = 0;
+    while (ld_acquire(flag) < 4u) {
+      if ((++spins & 31u) == 0u) {
+        if (*reinterpret_cast<volatile int*>(&c.hdr->abort)) {
+          ok = 0;
+          break;
+        }
+        const long long now = global_ns();
+        if (t0 == 0) t0 = now;
+        if (now - t0 > c.timeout_ns) {
+          record_failure(c, TK_ERR_PIPELINE_TIMEOUT, c.stage);
+          ok = 0;
+          break;
+        }
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)ld_acquire(flag);  // every lane's later reads of the slot see the writer's stores
+  return ok != 0;
+}
+
+__device__ __forceinline__ void sk_release_partial(unsigned* flag) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0 && atomicAdd(flag, 1u) == 7u) atomicExch(flag, 0u);
+}
+
 __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const TcState ts, uint32_t e_tile,
                                              long long* prof, uint32_t* e_ld) {
   bool ok = true;
@@ -2337,10 +2454,26 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
       if (stamp) *stamp = global_ns();
       tc_fence_after();
       tc_epilogue_partial(c, t, m0, n0, it.split, ts.tmem + acc * kMaxTileN);
+    } else if (it.sk == 2) {
+      // stream-K: this block's first segment, the later k blocks of a tile
+      // another block finishes: the partial sum goes to this block's slot
+      if (!mbar_wait(ts.acc_full + 8 * acc, ph, c.timeout_ns)) return ok = false;
+      if (stamp) *stamp = global_ns();
+      tc_fence_after();
+      sk_write_partial(t, ts.tmem + acc * kMaxTileN, ts.sk_slots + int64_t(blockIdx.x) * ts.sk_slot_floats,
+                       ts.sk_flags + blockIdx.x);
     } else if (t.epi_stage) {
+      // a stream-K tile's first k blocks: wait for the next block's partial sum
+      const float* part = nullptr;
+      unsigned* flag = ts.sk_flags + blockIdx.x + 1;
+      if (it.sk == 1) {
+        if (!sk_wait_partial(c, flag)) return ok = false;
+        part = ts.sk_slots + int64_t(blockIdx.x + 1) * ts.sk_slot_floats;
+      }
       if (!tc_epilogue_staged_any(c, t, m0, n0, ts.tmem + acc * kMaxTileN, stg, ts.acc_full + 8 * acc, ph, stamp,
-                                  ts.maps, ebar, e_ld))
+                                  ts.maps, ebar, e_ld, part))
         return ok = false;
+      if (part) sk_release_partial(flag);
     } else {
       if (!mbar_wait(ts.acc_full + 8 * acc, ph, c.timeout_ns)) return ok = false;
       if (stamp) *stamp = global_ns();
@@ -2513,6 +2646,9 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     ts.drain = smem_u32(&s_bar[2 * kStages + 4]);
     ts.epi_bar = smem_u32(&s_epi_bar[0]);
     ts.maps = maps;
+    ts.sk_slots = reinterpret_cast<float*>(p.ws) + prog->sk_slot_base;
+    ts.sk_flags = reinterpret_cast<unsigned*>(p.ws) + prog->sk_flag_base;
+    ts.sk_slot_floats = prog->sk_slot_floats;
     if (threadIdx.x == 0) {
       for (int i = 0; i < kStages; ++i) {
         mbar_init(ts.full + 8 * i, 1);

@@ -1886,6 +1886,52 @@ class Planner {
     return {t, f};
   }
 
+  // The grid tk_run launches, at most (occupancy can only lower it).
+  int64_t grid_bound(int64_t max_items) const {
+    int64_t g = int64_t(sms_) * std::max(1, opt_.blocks_per_sm);
+    g = std::min(g, std::max<int64_t>(max_items, 1));
+    if (opt_.max_blocks > 0) g = std::min<int64_t>(g, opt_.max_blocks);
+    return std::max<int64_t>(g, 1);
+  }
+
+  // Stream-K stages (see tkd::Stage): tensor-core tiles with long K loops
+  // (16 k blocks or more) whose count leaves the last wave at most 97 % full,
+  // every task of the stage on the staged epilogue (it adds the partial sums)
+  // and every block's range at least one whole tile long; and nothing else in
+  // the stage (other work already fills the blocks a partial last wave leaves
+  // idle).  The workspace gets one fp32 slot of a 128 x widest-tile partial
+  // sum and one flag per block.
+  void plan_stream_k(Plan& plan, int max_bn) const {
+    if (!opt_.stream_k) return;
+    const int64_t grid = grid_bound(plan.max_items);
+    bool any = false;
+    for (auto& S : plan.stages) {
+      if (S.n_tc_items <= grid || S.n_items != S.n_tc_items) continue;
+      int64_t units = 0, kb_max = 0;
+      bool ok = true;
+      for (int i = S.task_begin; i < S.task_end; ++i) {
+        const Task& t = plan.tasks[size_t(i)];
+        if (t.kind != tkd::T_GEMM_TC) break;
+        if (t.k_splits != 1 || !t.epi_stage) ok = false;
+        units += int64_t(t.n_items) * t.k_blocks;
+        kb_max = std::max<int64_t>(kb_max, t.k_blocks);
+      }
+      const int64_t waves = ceil_div(S.n_tc_items, grid);
+      const double fill = double(S.n_tc_items) / double(waves * grid);
+      if (!ok || kb_max < 16 || units / grid < kb_max || fill > 0.97) continue;
+      S.sk = 1;
+      S.sk_units = units;
+      any = true;
+    }
+    if (!any) return;
+    plan.sk_slot_floats = tkd::kTileM * max_bn;
+    plan.sk_slots = int32_t(grid);
+    plan.sk_slot_base = plan.workspace_units;
+    plan.workspace_units += round_up(grid * plan.sk_slot_floats, 64);
+    plan.sk_flag_base = plan.workspace_units;
+    plan.workspace_units += round_up(grid, 64);
+  }
+
   // The chain after reduction r, evaluated per finished output of task t.
   void lower_post_chain(Plan& plan, Task& t, const OpInfo& r, const Fused& fu) {
     const Shape out_shape = shape_of(r.out);
@@ -2157,6 +2203,7 @@ class Planner {
       }
     }
     plan.smem_bytes = plan.uses_tc ? ring + 4 * size_t(plan.epi_warp_bytes) : 1024 + size_t(tkd::kWorkFloats) * 4;
+    plan_stream_k(plan, max_bn);
     for (const auto& s : inputs_) plan.input_bytes.push_back(extent_of(s) * esize(s.dtype));
     for (const auto& s : outputs_) plan.output_bytes.push_back(numel(s) * esize(s.dtype));
     for (const auto& kv : inplace_) plan.inplace.push_back({kv.first, kv.second});

@@ -1471,10 +1471,10 @@ struct TcState {
   uint32_t tmem;                  // TMEM base address
   uint32_t stg;                   // shared address of the epilogue staging area
   uint32_t stg_warp_bytes;        // staging bytes per epilogue warp
-  uint32_t epi_bar;               // 2 mbarriers per epilogue warp (staged-epilogue operand loads)
+  uint32_t epi_bar;               // kEpiMaxBufs mbarriers per epilogue warp (staged-epilogue operand loads)
   const CUtensorMap* maps;        // the launch's TMA descriptors
   uint32_t p_it, m_it, m_tile, e_tile;
-  uint32_t e_ld;                  // this epilogue warp's staged chunk loads so far
+  uint32_t e_ld;                  // this epilogue warp's phase parity bit per staged-load mbarrier
   float* sk_slots;                // stream-K partial slots (sk_slot_floats each, one per block)
   unsigned* sk_flags;             // stream-K flags (one per block)
   int sk_slot_floats;
@@ -2012,9 +2012,9 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 
 // Returns false if a wait timed out.  Per-row operands (the target, the ReLU
 // mask input, the parameter being updated, a loaded side's operand) arrive as
-// 32 x 32 TMA boxes into two buffer halves per operand, one chunk ahead, on
-// this warp's two mbarriers (*eld counts the chunk loads the warp has made:
-// it selects the half and the phase parity).  Each lane then turns its row of
+// 32 x 32 TMA boxes into t.epi_nbuf buffers per operand, up to nbuf - 1
+// chunks ahead, chunk ch in buffer ch % nbuf on this warp's mbarrier of that
+// index (*eld holds the warp's phase parity bit per mbarrier).  Each lane then turns its row of
 // the chunk into outputs in shared memory (in place in the first per-row
 // operand's half, else in the `only` buffer), and lane 0 stores the chunk with
 // a TMA store; a side output follows the same way.  A buffer is refilled only
@@ -2034,22 +2034,24 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
   const bool st0 = L0 && (mask & 1), st1 = L1 && (mask & 2);
   const bool sl = t.has_side && t.side.ext == EXT_LOAD1 && (mask & 8);
   const Fast F = fast_params(c, t);
+  const int nb = t.epi_nbuf;
   // per warp, every piece a multiple of 512 bytes (the 64-byte swizzle's
-  // alignment): two halves per per-row operand, two output halves when there
-  // is no per-row operand, two halves for a loaded side's operand, then one
+  // alignment): nb buffers per per-row operand, two output halves when there
+  // is no per-row operand, nb buffers for a loaded side's operand, then one
   // kBcastBytes row per one-row operand
-  const uint32_t b0 = stg, b1 = b0 + (st0 ? 2 * kEpiBufBytes : 0);
-  const uint32_t only = b1 + (st1 ? 2 * kEpiBufBytes : 0);
+  const uint32_t nbb = uint32_t(nb) * kEpiBufBytes;
+  const uint32_t b0 = stg, b1 = b0 + (st0 ? nbb : 0);
+  const uint32_t only = b1 + (st1 ? nbb : 0);
   const uint32_t bs = only + (st0 || st1 ? 0 : 2 * kEpiBufBytes);
-  const uint32_t r0 = bs + (sl ? 2 * kEpiBufBytes : 0);
+  const uint32_t r0 = bs + (sl ? nbb : 0);
   const uint32_t r1 = r0 + (L0 && !st0 ? kBcastBytes : 0);
   const bool loads = st0 || st1 || sl;
   const uint32_t ld_bytes = uint32_t(int(st0) + int(st1) + int(sl)) * kEpiBufBytes;
-  const uint32_t it = *eld;
+  uint32_t ph = *eld;
   const int64_t col_base = n0;
 
   auto load = [&](int ch) {  // lane 0
-    const uint32_t k = it + uint32_t(ch), h = k & 1u, bar = ebar + 8 * h, off = h * kEpiBufBytes;
+    const uint32_t j = uint32_t(ch % nb), bar = ebar + 8 * j, off = j * kEpiBufBytes;
     const int x = int(col_base) + 32 * ch;
     mbar_expect_tx(bar, ld_bytes);
     if (st0) tma_load_2d(b0 + off, &maps[t.tma_ld0], x, row0, bar);
@@ -2069,8 +2071,8 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
   int issued = 0;  // chunk loads issued (lane 0)
   if (loads && lane == 0) {
     bulk_wait_read();  // the previous tile's stores are done with the buffers
-    load(0);
-    issued = 1;
+    issued = min(nb - 1, nch);
+    for (int j = 0; j < issued; ++j) load(j);
   }
   bool ok = mbar_wait(acc_bar, phase, c.timeout_ns);
   if (ok && stamp) *stamp = global_ns();
@@ -2081,23 +2083,28 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
   int ch = 0;
 #pragma unroll 1
   for (; ok && ch < nch; ++ch) {
-    const uint32_t k = it + uint32_t(ch), h = k & 1u, half = h * kEpiBufBytes;
+    const uint32_t j = uint32_t(ch % nb), half = j * kEpiBufBytes;
     const int col0 = int(col_base) + 32 * ch;
     if (lane == 0) {
-      // the half the next load fills was last read by chunk ch - 1's stores;
-      // without per-row operands the output half this chunk fills was last
-      // read by chunk ch - 2's stores (chunk ch - 1's last group may still run)
-      const bool more = loads && ch + 1 < nch;
+      // the buffer the next load fills was last read by chunk ch - 1's
+      // stores; without per-row operands the output half this chunk fills was
+      // last read by chunk ch - 2's stores (chunk ch - 1's last group may still
+      // run)
+      const int nxt = ch + nb - 1;
+      const bool more = loads && nxt < nch;
       if (more) bulk_wait_read();
       else if (!(st0 || st1)) bulk_wait_read_but_last();
       if (more) {
-        load(ch + 1);
-        issued = ch + 2;
+        load(nxt);
+        issued = nxt + 1;
       }
     }
-    if (loads && !mbar_wait(ebar + 8 * h, (k >> 1) & 1u, c.timeout_ns)) {
-      ok = false;
-      break;
+    if (loads) {
+      if (!mbar_wait(ebar + 8 * j, (ph >> j) & 1u, c.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      ph ^= 1u << j;
     }
     __syncwarp();
     const uint32_t ob = st0 ? b0 + half : (st1 ? b1 + half : only + (uint32_t(ch & 1) * kEpiBufBytes));
@@ -2147,14 +2154,15 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
   if (!ok && lane == 0) {
     // a wait gave up: the loads already issued land, and the stores already
     // issued finish, before the block moves on
-    for (int j = ch; j < issued; ++j) {
-      const uint32_t k = it + uint32_t(j);
-      mbar_wait(ebar + 8 * (k & 1u), (k >> 1) & 1u, c.timeout_ns);
+    for (int k = ch; k < issued; ++k) {
+      const uint32_t j = uint32_t(k % nb);
+      mbar_wait(ebar + 8 * j, (ph >> j) & 1u, c.timeout_ns);
+      ph ^= 1u << j;
     }
     bulk_wait_all();
   }
   __syncwarp();
-  *eld = it + (loads ? uint32_t(nch) : 0u);
+  *eld = ph;
   return ok;
 }
 
@@ -2443,7 +2451,7 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
   bool first = true;
   const int lane = threadIdx.x & 31;
   const uint32_t ew = uint32_t(threadIdx.x >> 5) - 4;
-  const uint32_t stg = ts.stg + ew * ts.stg_warp_bytes, ebar = ts.epi_bar + 16 * ew;
+  const uint32_t stg = ts.stg + ew * ts.stg_warp_bytes, ebar = ts.epi_bar + 8 * kEpiMaxBufs * ew;
   for_my_tiles(c, st, [&](const Task& t, const TileItem& it) {
     const int64_t m0 = it.m0, n0 = it.n0;
     const uint32_t acc = e_tile & 1u, ph = (e_tile >> 1) & 1u;
@@ -2615,7 +2623,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   __shared__ Stage s_stage;
   __shared__ Prep s_prep[kThreads / 32];
   __shared__ __align__(8) uint64_t s_bar[2 * kStages + 5];
-  __shared__ __align__(8) uint64_t s_epi_bar[8];
+  __shared__ __align__(8) uint64_t s_epi_bar[4 * kEpiMaxBufs];
   __shared__ __align__(8) uint64_t s_bulk_bar[kBulkMaxSlots];
   __shared__ uint32_t s_bulk_it;
   __shared__ __align__(8) uint64_t s_col_bar[kBulkMaxSlots];
@@ -2659,7 +2667,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
         mbar_init(ts.acc_empty + 8 * i, 4);
       }
       mbar_init(ts.drain, 1);
-      for (int i = 0; i < 8; ++i) mbar_init(ts.epi_bar + 8 * i, 1);
+      for (int i = 0; i < 4 * kEpiMaxBufs; ++i) mbar_init(ts.epi_bar + 8 * i, 1);
       for (int i = 0; i < kBulkMaxSlots; ++i) {
         mbar_init(smem_u32(&s_bulk_bar[i]), 1);
         mbar_init(smem_u32(&s_col_bar[i]), kThreads);

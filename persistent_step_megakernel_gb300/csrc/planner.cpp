@@ -1304,16 +1304,21 @@ class Planner {
   // Staging bytes per epilogue warp: two chunk buffers per per-row operand
   // (the output reuses the current one, else has its own buffer) and one
   // tile row per one-row operand.
-  int epi_stage_plan(const Plan& plan, const Task& t) const {
+  // With nbuf chunk buffers per per-row operand (the prefetch runs nbuf - 1
+  // chunks ahead).
+  int epi_stage_plan(const Plan& plan, const Task& t, int nbuf) const {
     const int mask = epi_stage_mask(plan, t);
     if (mask < 0) return 0;
-    const int rows = (mask & 1) + ((mask >> 1) & 1);
-    const int bcast = t.chain.n_loads - rows;
-    return main_stage_bytes(rows, bcast) + ((mask & 8) ? 2 * tkd::kEpiBufBytes : 0);
+    const int rows = (mask & 1) + ((mask >> 1) & 1) + ((mask >> 3) & 1);
+    const int bcast = t.chain.n_loads - (mask & 1) - ((mask >> 1) & 1);
+    return stage_bytes(rows, (mask & 3) != 0, bcast, nbuf);
   }
 
-  static int main_stage_bytes(int rows, int bcast) {
-    return 2 * (rows ? rows : 1) * tkd::kEpiBufBytes + bcast * tkd::kBcastBytes;
+  // Staging bytes per epilogue warp: nbuf buffers per per-row operand
+  // (the output reuses the current one of the first, else it has two halves
+  // of its own) and one tile row per one-row operand.
+  static int stage_bytes(int rows, bool output_in_place, int bcast, int nbuf) {
+    return (nbuf * rows + (output_in_place ? 0 : 2)) * tkd::kEpiBufBytes + bcast * tkd::kBcastBytes;
   }
 
   // Recognise the chain shapes the kernel runs as compiled loops (FastKind).
@@ -2191,15 +2196,22 @@ class Planner {
     // SM's unified L1/shared memory to the L1 cache.
     plan.ring_stage_bytes = tkd::kStageBytesA + max_bn * tkd::kTileK * 2;
     const size_t ring = 1024 + size_t(tkd::kStages) * plan.ring_stage_bytes;
+    // Staged epilogues: the deepest operand prefetch (up to 4 buffers, at most
+    // one per 32-column chunk of the tile) that fits beside the ring.
     for (auto& t : plan.tasks) {
       t.epi_stage = 0;
+      t.epi_nbuf = 2;
       t.tma_out = t.tma_out2 = t.tma_ld0 = t.tma_ld1 = t.tma_sd = -1;
-      const int need = epi_stage_plan(plan, t);
-      if (need > 0 && ring + 4 * size_t(std::max(need, plan.epi_warp_bytes)) <= size_t(tkd::kDynSmemBudget)) {
+      if (epi_stage_plan(plan, t, 2) <= 0) continue;
+      for (int nbuf = std::min(tkd::kEpiMaxBufs, std::max(2, t.tile_n / 32)); nbuf >= 2; --nbuf) {
+        const int need = epi_stage_plan(plan, t, nbuf);
+        if (ring + 4 * size_t(std::max(need, plan.epi_warp_bytes)) > size_t(tkd::kDynSmemBudget)) continue;
         const int mask = epi_stage_mask(plan, t);
-        if (!epilogue_maps(plan, t, mask)) continue;
+        if (!epilogue_maps(plan, t, mask)) break;
         plan.epi_warp_bytes = std::max(plan.epi_warp_bytes, need);
         t.epi_stage = mask;
+        t.epi_nbuf = nbuf;
+        break;
       }
     }
     plan.smem_bytes = plan.uses_tc ? ring + 4 * size_t(plan.epi_warp_bytes) : 1024 + size_t(tkd::kWorkFloats) * 4;

@@ -46,6 +46,7 @@ constexpr int kBulkOffset = 16 * 1024;
 constexpr int kBulkSlotBytes = 16 * 1024;
 constexpr int kBulkMaxSlots = 12;
 constexpr int kEpiBufBytes = 32 * 64;
+constexpr int kEpiMaxBufs = 4;   // chunk buffers per per-row operand of a staged epilogue, at most
 constexpr int kBcastBytes = kMaxTileN * 2;   // one 16-bit row of a tile
 constexpr int kTmemCols = 2 * kMaxTileN;                // double-buffered accumulator
 constexpr int kMaxMaps = 192;                           // TMA descriptors per launch
@@ -218,6 +219,7 @@ struct alignas(16) Task {
   // copied through shared memory too.  0 = operands and output accessed
   // directly.
   int32_t epi_stage;
+  int32_t epi_nbuf;          // chunk buffers per per-row operand (2..kEpiMaxBufs)
   // TMA descriptors of a staged epilogue's 32 x 32 chunks (64-byte swizzle,
   // the staging layout): the output, the side output, the per-row operands
   // of load slots 0 and 1 and the loaded side's operand (-1: none).

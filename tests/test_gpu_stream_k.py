@@ -13,7 +13,7 @@ from persistent_step_megakernel_gb300 import synthetic as S
 from persistent_step_megakernel_gb300.build import build
 from persistent_step_megakernel_gb300.ir import Operation, Program, TensorSpec
 from tests._gpu import run_step, teacher_forced
-from tests._util import ulp_distance
+from tests._util import ulp_distance, ulp_of, values
 
 pytestmark = pytest.mark.gpu
 T = TensorSpec.contiguous
@@ -57,10 +57,14 @@ def test_stream_k_gemm_matches_oracle_and_whole_tiles(grid):
     whole, sw = run_step(prog, arrays, tile_n=128, max_blocks=grid, split_k=0, stream_k=0)
     assert not sk_tasks(sw)
     # the first GEMM's output differs only by its float32 summation order: each
-    # is within 2 ulp of the exact value (teacher-forced below), so the two may
-    # differ by a few ulp where a sum rounds near a tie
+    # is within the float32 summation bound K 2^-24 sum|a w| (plus the final
+    # rounding) of the exact value, so the two are within twice that; sums
+    # that nearly cancel may differ by many ulp of their small value
+    av, wv, bv = (np.abs(v) for v in values(arrays, prog)[:3])
+    bound = 2 * 1.01 * 1024 * 2.0 ** -24 * (av @ wv.T + bv) + 2 * ulp_of(whole[0], "bfloat16")
+    assert (np.abs(sk[0] - whole[0]) <= bound).all()
     u = ulp_distance(sk[0], whole[0], "bfloat16")
-    assert (u <= 2).mean() >= 0.999 and u.max() <= 8, u.max()
+    assert (u <= 2).mean() >= 0.999
     all_prog = Program(prog.inputs, [T("z", (1024, 1024), "bfloat16")] + list(prog.outputs), prog.operations)
     outs, sa = run_step(all_prog, arrays, tile_n=128, max_blocks=grid, split_k=0)
     assert sk_tasks(sa)

@@ -92,5 +92,11 @@ def test_stream_k_in_the_gemm_bound_step():
     # through the layers into the gradients' cancelling column sums, so this
     # is the end-to-end tracking bound (per-op parity is checked above)
     for slot in state.inplace:
-        u = ulp_distance(a[slot], b[slot], "bfloat16")
-        assert (u <= 2).mean() >= 0.99 and u.max() <= 64, (state.outputs[slot].buffer, (u <= 2).mean(), u.max())
+        name = state.outputs[slot].buffer
+        if name.startswith("W"):
+            u = ulp_distance(a[slot], b[slot], "bfloat16")
+            assert (u <= 2).mean() >= 0.99 and u.max() <= 64, (name, (u <= 2).mean(), u.max())
+        else:
+            # the biases start at 0 and move by lr times a cancelling column
+            # sum: compare on the scale of the update, not in ulps
+            assert np.abs(a[slot] - b[slot]).max() <= 0.02 * np.abs(b[slot]).max(), name

@@ -816,15 +816,10 @@ __device__ __forceinline__ bool barrier_wait(const Ctx& c, unsigned target, int 
   return true;
 }
 
-// Last block out resets the counters for the next run (the barrier count and
-// the dynamic stages' item counters).  Thread 0 only.
-__device__ __forceinline__ void kernel_exit(const Ctx& c, const Program* prog) {
+// Last block out resets the counters for the next run.  Thread 0 only.
+__device__ __forceinline__ void kernel_exit(const Ctx& c) {
   Header* h = c.hdr;
   if (atom_add_acq_rel(&h->exits, 1u) + 1u == gridDim.x) {
-    if (prog->dyn_base >= 0) {
-      unsigned* ctr = reinterpret_cast<unsigned*>(c.ws) + prog->dyn_base;
-      for (int s = 0; s < prog->n_stages; ++s) atomicExch(ctr + s, 0u);
-    }
     atomicExch(&h->count, 0u);
     atomicExch(&h->exits, 0u);
   }
@@ -2635,7 +2630,6 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   __shared__ uint32_t s_col_it;
   __shared__ uint32_t s_tmem;
   __shared__ int s_flag;
-  __shared__ int s_next_item;
   extern __shared__ __align__(1024) unsigned char s_dyn[];
   const bool tc = maps != nullptr;
   // scratch for reductions and CUDA-core GEMMs at the start of the dynamic
@@ -2740,32 +2734,13 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     if (tc && st.n_tc_items > 0 && !run_tc_phase(c, st, maps, ts, s, &s_flag, prof ? prof + s * prof_step : nullptr))
       break;
     int ti = st.task_begin, base = 0;
-    auto item = [&](int g) {
+    for (int g = blockIdx.x; g < st.n_items; g += gridDim.x) {
+      if (g < st.n_tc_items) continue;  // handled by the tensor-core phase
       while (ti < st.task_end && g >= base + c.tasks[ti].n_items) {
         base += c.tasks[ti].n_items;
         ++ti;
       }
       run_item(c, c.tasks[ti], g - base, s_work);
-    };
-    if (st.dyn) {
-      // the stage's other items in the order blocks ask for them: thread 0
-      // asks for the next index while the block runs the current item
-      unsigned* ctr = reinterpret_cast<unsigned*>(c.ws) + prog->dyn_base + s;
-      if (threadIdx.x == 0) s_next_item = int(atomicAdd(ctr, 1u));
-      __syncthreads();
-      int k = s_next_item;
-      while (st.n_tc_items + k < st.n_items) {
-        __syncthreads();  // every thread has read s_next_item
-        unsigned nxt = 0;
-        if (threadIdx.x == 0) nxt = atomicAdd(ctr, 1u);
-        item(st.n_tc_items + k);
-        if (threadIdx.x == 0) s_next_item = int(nxt);
-        __syncthreads();
-        k = s_next_item;
-      }
-    } else {
-      for (int g = blockIdx.x; g < st.n_items; g += gridDim.x)
-        if (g >= st.n_tc_items) item(g);  // tiles: the tensor-core phase
     }
     asm volatile("fence.proxy.async.global;" ::: "memory");
     __syncthreads();
@@ -2778,7 +2753,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     if (!s_flag) break;
   }
   __syncthreads();
-  if (threadIdx.x == 0) kernel_exit(c, prog);
+  if (threadIdx.x == 0) kernel_exit(c);
   if (tc) {
     tc_fence_before();
     __syncthreads();

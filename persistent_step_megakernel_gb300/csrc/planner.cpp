@@ -2216,17 +2216,6 @@ class Planner {
     }
     plan.smem_bytes = plan.uses_tc ? ring + 4 * size_t(plan.epi_warp_bytes) : 1024 + size_t(tkd::kWorkFloats) * 4;
     plan_stream_k(plan, max_bn);
-    // Dynamic hand-out of the other items of a stage whose tensor-core tiles
-    // leave some blocks with fewer tiles than others.
-    const int64_t grid = grid_bound(plan.max_items);
-    for (auto& S : plan.stages) {
-      S.dyn = !S.sk && S.n_tc_items > 0 && S.n_items > S.n_tc_items && S.n_tc_items % grid != 0;
-      if (S.dyn && plan.dyn_base < 0) plan.dyn_base = 0;
-    }
-    if (plan.dyn_base == 0) {
-      plan.dyn_base = plan.workspace_units;
-      plan.workspace_units += round_up(int64_t(plan.stages.size()), 64);
-    }
     for (const auto& s : inputs_) plan.input_bytes.push_back(extent_of(s) * esize(s.dtype));
     for (const auto& s : outputs_) plan.output_bytes.push_back(numel(s) * esize(s.dtype));
     for (const auto& kv : inplace_) plan.inplace.push_back({kv.first, kv.second});

@@ -53,8 +53,6 @@ struct Plan {
   // stream-K partial slots and flags (see tkd::Stage); sk_slots == 0: none
   int64_t sk_slot_base = 0, sk_flag_base = 0;
   int32_t sk_slot_floats = 0, sk_slots = 0;
-  // per-stage counters of dynamic stages (see tkd::Stage::dyn); -1: none
-  int64_t dyn_base = -1;
   int epi_warp_bytes = 0;    // epilogue staging per epilogue warp
   bool uses_tc = false;
   tk_plan_stats stats{};

@@ -114,7 +114,6 @@ tk_status upload(tk_program* p) {
   prog.sk_flag_base = pl.sk_flag_base;
   prog.sk_slot_floats = pl.sk_slot_floats;
   prog.sk_slots = pl.sk_slots;
-  prog.dyn_base = pl.dyn_base;
   prog.prefetch = reinterpret_cast<const tkd::Prefetch*>(base + off_pf);
   std::memcpy(host.data() + off_prog, &prog, sizeof(prog));
   if (!pf.empty()) std::memcpy(host.data() + off_pf, pf.data(), pf.size() * sizeof(tkd::Prefetch));
@@ -330,10 +329,6 @@ tk_status tk_workspace_init(const tk_program* p, float* ws, size_t n, void* stre
   if (p->plan.sk_slots > 0) {  // stream-K flags
     e = cudaMemsetAsync(ws + p->plan.sk_flag_base, 0, size_t(p->plan.sk_slots) * 4, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(stream-K flags)");
-  }
-  if (p->plan.dyn_base >= 0) {  // item counters of dynamic stages
-    e = cudaMemsetAsync(ws + p->plan.dyn_base, 0, p->plan.stages.size() * 4, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(stage counters)");
   }
   return TK_OK;
 }

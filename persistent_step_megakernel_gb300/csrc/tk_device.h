@@ -248,10 +248,7 @@ struct Stage {
   int32_t n_tc_items;
   int32_t code_lo, code_hi;  // instructions the stage's tasks use
   int32_t ref_lo, ref_hi;    // operand refs the stage's tasks use
-  int32_t sk;                // stream-K for the tensor-core tiles
-  // 1: the stage's other items go to whichever block asks next (a counter in
-  // the workspace), so blocks with fewer tensor-core tiles take more of them
-  int32_t dyn;
+  int32_t sk, sk_pad;        // stream-K for the tensor-core tiles
   int64_t sk_units;          // U: k-block units of the stage's tensor-core tiles
 };
 
@@ -287,9 +284,6 @@ struct Program {
   // after every stage)
   int64_t sk_slot_base, sk_flag_base;
   int32_t sk_slot_floats, sk_slots;
-  // per-stage item counters of dynamic stages (float offset; one int per
-  // stage; zeroed by workspace initialisation and by the last block to leave)
-  int64_t dyn_base;
 };
 
 // Workspace header (offset 0, 256 bytes).  `count` only grows during a run

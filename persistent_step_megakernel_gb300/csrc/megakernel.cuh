@@ -1471,7 +1471,9 @@ struct TcState {
   uint32_t tmem;                  // TMEM base address
   uint32_t stg;                   // shared address of the epilogue staging area
   uint32_t stg_warp_bytes;        // staging bytes per epilogue warp
-  uint32_t epi_bar;               // kEpiMaxBufs mbarriers per epilogue warp (staged-epilogue operand loads)
+  uint32_t epi_bar;               // kEpiMaxBufs mbarriers per warp (staged-epilogue operand loads)
+  uint32_t join;                  // 4 mbarriers: helper warp q done with its chunks of the last tile
+  uint32_t join_n;                // tiles shared with a helper warp so far (the join barriers' parity)
   const CUtensorMap* maps;        // the launch's TMA descriptors
   uint32_t p_it, m_it, m_tile, e_tile;
   uint32_t e_ld;                  // this epilogue warp's phase parity bit per staged-load mbarrier
@@ -1992,6 +1994,15 @@ __device__ __noinline__ void stage_side(const Task& t, uint32_t buf, uint32_t ds
   }
 }
 
+// Stream-K partial-sum slot layout (float4 units): the piece (lane quarter q,
+// 32-column chunk cc, 4-column vector v) of lane l is at
+// ((q * chunks + cc) * 8 + v) * 32 + l, so each warp access covers 512
+// contiguous bytes; the finisher's lanes read their own rows back with the
+// same mapping.
+__device__ __forceinline__ int sk_piece(int q, int chunks, int cc, int v, int lane) {
+  return ((q * chunks + cc) * 8 + v) * 32 + lane;
+}
+
 // TMA store of a staged 32 x 32 chunk (64-byte swizzle) at (col, row) of the
 // tensor behind `map`; rows and columns beyond the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
@@ -2025,10 +2036,12 @@ template <int K>
 __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int64_t m0, int64_t n0, uint32_t taddr,
                                                 uint32_t stg, uint32_t acc_bar, uint32_t phase, long long* stamp,
                                                 const CUtensorMap* maps, uint32_t ebar, uint32_t* eld,
-                                                const float* part) {
+                                                const float* part, int c0, int c1) {
   const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
   const int row0 = int(m0) + q * 32;
-  const int nch = t.tile_n / 32;
+  // chunks [c0, c1) of the tile's tile_n / 32 (a warp sharing the tile with
+  // another takes part of them); buffer and mbarrier j = (ch - c0) % nbuf
+  const int nch = c1;
   const int mask = t.epi_stage;
   constexpr bool L0 = FastTraits<K>::load0, L1 = FastTraits<K>::load1;
   const bool st0 = L0 && (mask & 1), st1 = L1 && (mask & 2);
@@ -2051,7 +2064,7 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
   const int64_t col_base = n0;
 
   auto load = [&](int ch) {  // lane 0
-    const uint32_t j = uint32_t(ch % nb), bar = ebar + 8 * j, off = j * kEpiBufBytes;
+    const uint32_t j = uint32_t((ch - c0) % nb), bar = ebar + 8 * j, off = j * kEpiBufBytes;
     const int x = int(col_base) + 32 * ch;
     mbar_expect_tx(bar, ld_bytes);
     if (st0) tma_load_2d(b0 + off, &maps[t.tma_ld0], x, row0, bar);
@@ -2071,8 +2084,8 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
   int issued = 0;  // chunk loads issued (lane 0)
   if (loads && lane == 0) {
     bulk_wait_read();  // the previous tile's stores are done with the buffers
-    issued = min(nb - 1, nch);
-    for (int j = 0; j < issued; ++j) load(j);
+    issued = min(c0 + nb - 1, nch);
+    for (int j = c0; j < issued; ++j) load(j);
   }
   bool ok = mbar_wait(acc_bar, phase, c.timeout_ns);
   if (ok && stamp) *stamp = global_ns();
@@ -2080,10 +2093,10 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
   cp_async_wait<0>();
   __syncwarp();
   const uint32_t tlane = taddr + (uint32_t(q * 32) << 16);
-  int ch = 0;
+  int ch = c0;
 #pragma unroll 1
   for (; ok && ch < nch; ++ch) {
-    const uint32_t j = uint32_t(ch % nb), half = j * kEpiBufBytes;
+    const uint32_t j = uint32_t((ch - c0) % nb), half = j * kEpiBufBytes;
     const int col0 = int(col_base) + 32 * ch;
     if (lane == 0) {
       // the buffer the next load fills was last read by chunk ch - 1's
@@ -2107,14 +2120,14 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
       ph ^= 1u << j;
     }
     __syncwarp();
-    const uint32_t ob = st0 ? b0 + half : (st1 ? b1 + half : only + (uint32_t(ch & 1) * kEpiBufBytes));
+    const uint32_t ob = st0 ? b0 + half : (st1 ? b1 + half : only + (uint32_t((ch - c0) & 1) * kEpiBufBytes));
     uint32_t rv[32];
     tmem_ld32(tlane + uint32_t(32 * ch), rv);
     if (part) {  // stream-K: the fp32 partial sum of the tile's later k blocks
-      const float4* pp = reinterpret_cast<const float4*>(part + (q * 32 + lane) * t.tile_n + 32 * ch);
+      const float4* pp = reinterpret_cast<const float4*>(part);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float4 w = __ldcg(pp + j);  // written by another SM: read at L2
+        const float4 w = __ldcg(pp + sk_piece(q, t.tile_n / 32, ch, j, lane));  // another SM's: read at L2
         rv[4 * j] = __float_as_uint(__fadd_rn(__uint_as_float(rv[4 * j]), w.x));
         rv[4 * j + 1] = __float_as_uint(__fadd_rn(__uint_as_float(rv[4 * j + 1]), w.y));
         rv[4 * j + 2] = __float_as_uint(__fadd_rn(__uint_as_float(rv[4 * j + 2]), w.z));
@@ -2155,7 +2168,7 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
     // a wait gave up: the loads already issued land, and the stores already
     // issued finish, before the block moves on
     for (int k = ch; k < issued; ++k) {
-      const uint32_t j = uint32_t(k % nb);
+      const uint32_t j = uint32_t((k - c0) % nb);
       mbar_wait(ebar + 8 * j, (ph >> j) & 1u, c.timeout_ns);
       ph ^= 1u << j;
     }
@@ -2169,15 +2182,15 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
 __device__ __noinline__ bool tc_epilogue_staged_any(const Ctx c, const Task& t, int64_t m0, int64_t n0,
                                                     uint32_t taddr, uint32_t stg, uint32_t acc_bar, uint32_t phase,
                                                     long long* stamp, const CUtensorMap* maps, uint32_t ebar,
-                                                    uint32_t* eld, const float* part) {
+                                                    uint32_t* eld, const float* part, int c0, int c1) {
   switch (t.chain.fast) {
-    case FK_E_ACC: return tc_epilogue_staged<FK_E_ACC>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part);
-    case FK_E_BIAS: return tc_epilogue_staged<FK_E_BIAS>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part);
-    case FK_E_BIAS_RELU: return tc_epilogue_staged<FK_E_BIAS_RELU>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part);
-    case FK_E_BIAS_AXPY: return tc_epilogue_staged<FK_E_BIAS_AXPY>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part);
-    case FK_E_ACC_THRESH: return tc_epilogue_staged<FK_E_ACC_THRESH>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part);
-    case FK_E_MOMENTUM: return tc_epilogue_staged<FK_E_MOMENTUM>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part);
-    default: return tc_epilogue_staged<FK_E_UPDATE>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part);
+    case FK_E_ACC: return tc_epilogue_staged<FK_E_ACC>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part, c0, c1);
+    case FK_E_BIAS: return tc_epilogue_staged<FK_E_BIAS>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part, c0, c1);
+    case FK_E_BIAS_RELU: return tc_epilogue_staged<FK_E_BIAS_RELU>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part, c0, c1);
+    case FK_E_BIAS_AXPY: return tc_epilogue_staged<FK_E_BIAS_AXPY>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part, c0, c1);
+    case FK_E_ACC_THRESH: return tc_epilogue_staged<FK_E_ACC_THRESH>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part, c0, c1);
+    case FK_E_MOMENTUM: return tc_epilogue_staged<FK_E_MOMENTUM>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part, c0, c1);
+    default: return tc_epilogue_staged<FK_E_UPDATE>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part, c0, c1);
   }
 }
 
@@ -2387,18 +2400,17 @@ __device__ __noinline__ uint64_t tc_mma(const Ctx c, const Stage st, const TcSta
 // partial rows it owns, then adds 1; the fourth to finish sets the flag back
 // to 0 for the next stage).
 __device__ __noinline__ void sk_write_partial(const Task& t, uint32_t taddr, float* slot, unsigned* flag) {
-  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
-  float* row = slot + (q * 32 + lane) * t.tile_n;
+  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3, chunks = t.tile_n / 32;
+  float4* s4 = reinterpret_cast<float4*>(slot);
 #pragma unroll 1
-  for (int cc = 0; cc < t.tile_n; cc += 32) {
+  for (int cc = 0; cc < chunks; ++cc) {
     uint32_t r[32];
     __syncwarp();
-    tmem_ld32(taddr + (uint32_t(q * 32) << 16) + uint32_t(cc), r);
+    tmem_ld32(taddr + (uint32_t(q * 32) << 16) + uint32_t(32 * cc), r);
 #pragma unroll
     for (int v = 0; v < 8; ++v)
-      *reinterpret_cast<float4*>(row + cc + 4 * v) = make_float4(
-          __uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]), __uint_as_float(r[4 * v + 2]),
-          __uint_as_float(r[4 * v + 3]));
+      s4[sk_piece(q, chunks, cc, v, lane)] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                                         __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
   }
   __threadfence();
   __syncwarp();
@@ -2445,14 +2457,37 @@ __device__ __forceinline__ void sk_release_partial(unsigned* flag) {
   if ((threadIdx.x & 31) == 0 && atomicAdd(flag, 1u) == 7u) atomicExch(flag, 0u);
 }
 
+// The block's last tile of a stage is shared with warps 0-3 (idle once the
+// producer and the MMA issuer are done; warp q reads TMEM lane quarter q like
+// epilogue warp 4 + q): chunks [0, nch/2) here, the rest in
+// tc_epilogue_assist.  Only staged epilogues of whole (non-stream-K-writer,
+// non-split-K) tiles, and only when the helpers' staging fits in a quarter of
+// the then idle TMA ring.
+__device__ __forceinline__ bool assisted(const Task& t, const TileItem& it, const TcState& ts) {
+  return t.epi_stage && t.k_splits == 1 && it.sk != 2 && t.tile_n >= 64 &&
+         ts.stg_warp_bytes <= uint32_t(kStages) * ts.slot_bytes / 4;
+}
+
+__device__ __forceinline__ int count_my_tiles(const Ctx& c, const Stage& st) {
+  int n = 0;
+  for_my_tiles(c, st, [&](const Task&, const TileItem&) {
+    ++n;
+    return true;
+  });
+  return n;
+}
+
 __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const TcState ts, uint32_t e_tile,
-                                             long long* prof, uint32_t* e_ld) {
+                                             long long* prof, uint32_t* e_ld, uint32_t* join_n) {
   bool ok = true;
   bool first = true;
   const int lane = threadIdx.x & 31;
   const uint32_t ew = uint32_t(threadIdx.x >> 5) - 4;
-  const uint32_t stg = ts.stg + ew * ts.stg_warp_bytes, ebar = ts.epi_bar + 8 * kEpiMaxBufs * ew;
+  const uint32_t stg = ts.stg + ew * ts.stg_warp_bytes, ebar = ts.epi_bar + 8 * kEpiMaxBufs * (4 + ew);
+  const int n_tiles = count_my_tiles(c, st);
+  int idx = 0;
   for_my_tiles(c, st, [&](const Task& t, const TileItem& it) {
+    const bool shared_tile = ++idx == n_tiles && assisted(t, it, ts);
     const int64_t m0 = it.m0, n0 = it.n0;
     const uint32_t acc = e_tile & 1u, ph = (e_tile >> 1) & 1u;
     long long* stamp = prof && first && threadIdx.x == 128 ? prof + 5 : nullptr;
@@ -2478,9 +2513,14 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
         if (!sk_wait_partial(c, flag)) return ok = false;
         part = ts.sk_slots + int64_t(blockIdx.x + 1) * ts.sk_slot_floats;
       }
+      const int nch = t.tile_n / 32;
       if (!tc_epilogue_staged_any(c, t, m0, n0, ts.tmem + acc * kMaxTileN, stg, ts.acc_full + 8 * acc, ph, stamp,
-                                  ts.maps, ebar, e_ld, part))
+                                  ts.maps, ebar, e_ld, part, 0, shared_tile ? nch / 2 : nch))
         return ok = false;
+      if (shared_tile) {  // the helper warp's half of the chunks is done too
+        if (!mbar_wait(ts.join + 8 * ew, *join_n & 1u, c.timeout_ns)) return ok = false;
+        ++*join_n;
+      }
       if (part) sk_release_partial(flag);
     } else {
       if (!mbar_wait(ts.acc_full + 8 * acc, ph, c.timeout_ns)) return ok = false;
@@ -2498,6 +2538,45 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
   if (lane == 0) bulk_wait_all();
   __syncwarp();
   return (uint64_t(ok) << 32) | e_tile;
+}
+
+// Warps 0-3: the second half of the chunks of the block's last tile (see
+// assisted), staged in quarter q of the idle TMA ring, then an arrival on
+// join barrier q for epilogue warp 4 + q.  Returns the tile counter advanced
+// by the stage's tiles (these warps follow the epilogue's sequence) and 1 << 32
+// if every wait completed.
+__device__ __noinline__ uint64_t tc_epilogue_assist(const Ctx c, const Stage st, const TcState ts, uint32_t e_tile,
+                                                    uint32_t* e_ld, uint32_t* join_n) {
+  const int lane = threadIdx.x & 31, q = threadIdx.x >> 5;
+  const int n_tiles = count_my_tiles(c, st);
+  if (n_tiles == 0) return (uint64_t(1) << 32) | e_tile;
+  bool ok = true;
+  int idx = 0;
+  for_my_tiles(c, st, [&](const Task& t, const TileItem& it) {
+    if (++idx < n_tiles) return true;
+    if (!assisted(t, it, ts)) return false;
+    const uint32_t k = e_tile + uint32_t(n_tiles - 1), acc = k & 1u, ph = (k >> 1) & 1u;
+    // the tile's MMAs are done (they have read every ring slot) before this
+    // warp writes its staging area in the ring
+    if (!mbar_wait(ts.acc_full + 8 * acc, ph, c.timeout_ns)) return ok = false;
+    const float* part = nullptr;
+    if (it.sk == 1) {  // a stream-K tile's first k blocks: the next block's partial sum
+      if (!sk_wait_partial(c, ts.sk_flags + blockIdx.x + 1)) return ok = false;
+      part = ts.sk_slots + int64_t(blockIdx.x + 1) * ts.sk_slot_floats;
+    }
+    const uint32_t stg = ts.ring + uint32_t(q) * (uint32_t(kStages) * ts.slot_bytes / 4);
+    const uint32_t ebar = ts.epi_bar + 8 * kEpiMaxBufs * q;
+    const int nch = t.tile_n / 32;
+    ok = tc_epilogue_staged_any(c, t, it.m0, it.n0, ts.tmem + acc * kMaxTileN, stg, ts.acc_full + 8 * acc, ph,
+                                nullptr, ts.maps, ebar, e_ld, part, nch / 2, nch);
+    tc_fence_before();
+    if (lane == 0) bulk_wait_all();  // the ring is reused after the phase
+    __syncwarp();
+    if (lane == 0) mbar_arrive(ts.join + 8 * q);
+    ++*join_n;
+    return false;
+  });
+  return (uint64_t(ok) << 32) | (e_tile + uint32_t(n_tiles));
 }
 
 // Run this block's tensor-core tiles of one stage; false after a wait timed out.
@@ -2518,12 +2597,24 @@ __device__ bool run_tc_phase(const Ctx& c, const Stage& st, const CUtensorMap* m
     ok = (r >> 32) != 0;
     if (prof) prof[4] = global_ns();
   } else if (warp >= 4) {
-    uint32_t e_ld = ts.e_ld;
-    const uint64_t r = tc_epilogue(c, st, ts, ts.e_tile, prof, &e_ld);
+    uint32_t e_ld = ts.e_ld, join_n = ts.join_n;
+    const uint64_t r = tc_epilogue(c, st, ts, ts.e_tile, prof, &e_ld, &join_n);
     ts.e_tile = uint32_t(r);
     ts.e_ld = e_ld;
+    ts.join_n = join_n;
     ok = (r >> 32) != 0;
     if (prof && threadIdx.x == 128) prof[6] = global_ns();
+  }
+  if (warp < 4) {
+    // warps 0-3 (the producer and MMA lanes once their loops are done) take
+    // half of the block's last tile's epilogue
+    __syncwarp();
+    uint32_t e_ld = ts.e_ld, join_n = ts.join_n;
+    const uint64_t r = tc_epilogue_assist(c, st, ts, ts.e_tile, &e_ld, &join_n);
+    ts.e_tile = uint32_t(r);
+    ts.e_ld = e_ld;
+    ts.join_n = join_n;
+    ok = ok && (r >> 32) != 0;
   }
   if (!ok) record_failure(c, TK_ERR_PIPELINE_TIMEOUT, stage);
   if (threadIdx.x == 0) *s_flag = 1;
@@ -2623,7 +2714,8 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   __shared__ Stage s_stage;
   __shared__ Prep s_prep[kThreads / 32];
   __shared__ __align__(8) uint64_t s_bar[2 * kStages + 5];
-  __shared__ __align__(8) uint64_t s_epi_bar[4 * kEpiMaxBufs];
+  __shared__ __align__(8) uint64_t s_epi_bar[8 * kEpiMaxBufs];
+  __shared__ __align__(8) uint64_t s_join_bar[4];
   __shared__ __align__(8) uint64_t s_bulk_bar[kBulkMaxSlots];
   __shared__ uint32_t s_bulk_it;
   __shared__ __align__(8) uint64_t s_col_bar[kBulkMaxSlots];
@@ -2653,6 +2745,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     ts.acc_empty = smem_u32(&s_bar[2 * kStages + 2]);
     ts.drain = smem_u32(&s_bar[2 * kStages + 4]);
     ts.epi_bar = smem_u32(&s_epi_bar[0]);
+    ts.join = smem_u32(&s_join_bar[0]);
     ts.maps = maps;
     ts.sk_slots = reinterpret_cast<float*>(p.ws) + prog->sk_slot_base;
     ts.sk_flags = reinterpret_cast<unsigned*>(p.ws) + prog->sk_flag_base;
@@ -2667,7 +2760,8 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
         mbar_init(ts.acc_empty + 8 * i, 4);
       }
       mbar_init(ts.drain, 1);
-      for (int i = 0; i < 4 * kEpiMaxBufs; ++i) mbar_init(ts.epi_bar + 8 * i, 1);
+      for (int i = 0; i < 8 * kEpiMaxBufs; ++i) mbar_init(ts.epi_bar + 8 * i, 1);
+      for (int i = 0; i < 4; ++i) mbar_init(ts.join + 8 * i, 1);
       for (int i = 0; i < kBulkMaxSlots; ++i) {
         mbar_init(smem_u32(&s_bulk_bar[i]), 1);
         mbar_init(smem_u32(&s_col_bar[i]), kThreads);

@@ -1473,6 +1473,7 @@ struct TcState {
   uint32_t stg_warp_bytes;        // staging bytes per epilogue warp
   uint32_t epi_bar;               // kEpiMaxBufs mbarriers per warp (staged-epilogue operand loads)
   uint32_t join;                  // 4 mbarriers: helper warp q done with its chunks of the last tile
+  uint32_t go;                    // 4 mbarriers: the last tile's accumulator is ready (epilogue warp 4 + q)
   uint32_t join_n;                // tiles shared with a helper warp so far (the join barriers' parity)
   const CUtensorMap* maps;        // the launch's TMA descriptors
   uint32_t p_it, m_it, m_tile, e_tile;
@@ -2514,6 +2515,15 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
         part = ts.sk_slots + int64_t(blockIdx.x + 1) * ts.sk_slot_floats;
       }
       const int nch = t.tile_n / 32;
+      if (shared_tile) {
+        // the helper warp may touch the tile (and its staging in the ring)
+        // only once the tile's MMAs are done; this warp waits for the
+        // accumulator in tile order (an mbarrier parity wait must not run
+        // ahead by more than one phase), then lets the helper go
+        if (!mbar_wait(ts.acc_full + 8 * acc, ph, c.timeout_ns)) return ok = false;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ts.go + 8 * ew);
+      }
       if (!tc_epilogue_staged_any(c, t, m0, n0, ts.tmem + acc * kMaxTileN, stg, ts.acc_full + 8 * acc, ph, stamp,
                                   ts.maps, ebar, e_ld, part, 0, shared_tile ? nch / 2 : nch))
         return ok = false;
@@ -2556,9 +2566,10 @@ __device__ __noinline__ uint64_t tc_epilogue_assist(const Ctx c, const Stage st,
     if (++idx < n_tiles) return true;
     if (!assisted(t, it, ts)) return false;
     const uint32_t k = e_tile + uint32_t(n_tiles - 1), acc = k & 1u, ph = (k >> 1) & 1u;
-    // the tile's MMAs are done (they have read every ring slot) before this
-    // warp writes its staging area in the ring
-    if (!mbar_wait(ts.acc_full + 8 * acc, ph, c.timeout_ns)) return ok = false;
+    // epilogue warp 4 + q has seen the tile's accumulator ready (its MMAs, the
+    // last readers of the ring, are done) before this warp writes its staging
+    // area in the ring
+    if (!mbar_wait(ts.go + 8 * q, *join_n & 1u, c.timeout_ns)) return ok = false;
     const float* part = nullptr;
     if (it.sk == 1) {  // a stream-K tile's first k blocks: the next block's partial sum
       if (!sk_wait_partial(c, ts.sk_flags + blockIdx.x + 1)) return ok = false;
@@ -2715,7 +2726,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   __shared__ Prep s_prep[kThreads / 32];
   __shared__ __align__(8) uint64_t s_bar[2 * kStages + 5];
   __shared__ __align__(8) uint64_t s_epi_bar[8 * kEpiMaxBufs];
-  __shared__ __align__(8) uint64_t s_join_bar[4];
+  __shared__ __align__(8) uint64_t s_join_bar[8];
   __shared__ __align__(8) uint64_t s_bulk_bar[kBulkMaxSlots];
   __shared__ uint32_t s_bulk_it;
   __shared__ __align__(8) uint64_t s_col_bar[kBulkMaxSlots];
@@ -2746,6 +2757,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     ts.drain = smem_u32(&s_bar[2 * kStages + 4]);
     ts.epi_bar = smem_u32(&s_epi_bar[0]);
     ts.join = smem_u32(&s_join_bar[0]);
+    ts.go = smem_u32(&s_join_bar[4]);
     ts.maps = maps;
     ts.sk_slots = reinterpret_cast<float*>(p.ws) + prog->sk_slot_base;
     ts.sk_flags = reinterpret_cast<unsigned*>(p.ws) + prog->sk_flag_base;
@@ -2761,7 +2773,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
       }
       mbar_init(ts.drain, 1);
       for (int i = 0; i < 8 * kEpiMaxBufs; ++i) mbar_init(ts.epi_bar + 8 * i, 1);
-      for (int i = 0; i < 4; ++i) mbar_init(ts.join + 8 * i, 1);
+      for (int i = 0; i < 8; ++i) mbar_init(ts.join + 8 * i, 1);  // join, then go
       for (int i = 0; i < kBulkMaxSlots; ++i) {
         mbar_init(smem_u32(&s_bulk_bar[i]), 1);
         mbar_init(smem_u32(&s_col_bar[i]), kThreads);

@@ -146,11 +146,6 @@ typedef struct {
   int32_t tile_n;              /* N width of every tensor-core tile: 0 (default) picks 64, 128 or
                                   256 per GEMM from its tile count and the SM count; 64, 128 or 256
                                   forces that width (used by tests to reach each tile path) */
-  int32_t stream_k;            /* 1 (default): a stage of long tensor-core GEMMs whose tiles leave the
-                                  last wave partly idle deals equal ranges of k blocks to the blocks
-                                  (a tile cut in two is finished by adding an fp32 partial sum); the
-                                  cut points follow the grid size, so such GEMMs round in a
-                                  grid-dependent order.  0: whole tiles only */
 } tk_options;
 
 /* What the planner decided (codegen.py `GeneratedKernel` counters). */
@@ -192,8 +187,6 @@ typedef struct {
   int32_t parts;               /* reduction parts (1 = not split) */
   int32_t staged_epilogue;     /* tensor-core GEMM whose epilogue moves tiles through shared memory */
   int32_t side_output;         /* GEMM that also writes a second value (a side output) from its tile */
-  int32_t stream_k;            /* tensor-core GEMM in a stream-K stage (see tk_options.stream_k) */
-  int32_t reserved0;           /* 0 */
   int64_t numel;               /* elements of the task's index space */
 } tk_task_info;
 
@@ -217,10 +210,10 @@ void tk_program_destroy(tk_program* program);
  * only: the caller allocates (runtime.py `allocate`). */
 tk_status tk_allocate(const tk_program* program, size_t* workspace_elements);
 
-/* Zero the workspace header (barrier counter and status word, and the
- * stream-K flags of a program that has any) on `stream`.  Required once for
- * each new workspace and again after a run whose device status was not TK_OK;
- * every successful run leaves them ready for the next one. */
+/* Zero the workspace header (barrier counter and status word) on `stream`.
+ * Required once for each new workspace and again after a run whose device
+ * status was not TK_OK; every successful run leaves the header ready for the
+ * next one. */
 tk_status tk_workspace_init(const tk_program* program, float* workspace, size_t workspace_elements,
                             void* stream);
 

@@ -54,7 +54,7 @@ class tk_options(ctypes.Structure):
                 ("inline_input_casts", ctypes.c_int32), ("tensor_cores", ctypes.c_int32),
                 ("sm_count", ctypes.c_int32), ("profile", ctypes.c_int32),
                 ("barrier_timeout_s", ctypes.c_double), ("expr_forms", ctypes.c_int32),
-                ("split_k", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("stream_k", ctypes.c_int32)]
+                ("split_k", ctypes.c_int32), ("tile_n", ctypes.c_int32)]
 
 
 class tk_plan_stats(ctypes.Structure):
@@ -69,7 +69,7 @@ class tk_plan_stats(ctypes.Structure):
 class tk_task_info(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "stage", "kind", "op_index", "n_items", "form", "compiled_shape", "m", "n", "k", "tile_m", "tile_n",
-        "parts", "staged_epilogue", "side_output", "stream_k", "reserved0")] + [("numel", ctypes.c_int64)]
+        "parts", "staged_epilogue", "side_output")] + [("numel", ctypes.c_int64)]
 
 
 # (name, restype, argtypes) for every entry point of include/tk.h

@@ -1471,16 +1471,10 @@ struct TcState {
   uint32_t tmem;                  // TMEM base address
   uint32_t stg;                   // shared address of the epilogue staging area
   uint32_t stg_warp_bytes;        // staging bytes per epilogue warp
-  uint32_t epi_bar;               // kEpiMaxBufs mbarriers per warp (staged-epilogue operand loads)
-  uint32_t join;                  // 4 mbarriers: helper warp q done with its chunks of the last tile
-  uint32_t go;                    // 4 mbarriers: the last tile's accumulator is ready (epilogue warp 4 + q)
-  uint32_t join_n;                // tiles shared with a helper warp so far (the join barriers' parity)
+  uint32_t epi_bar;               // 2 mbarriers per epilogue warp (staged-epilogue operand loads)
   const CUtensorMap* maps;        // the launch's TMA descriptors
   uint32_t p_it, m_it, m_tile, e_tile;
-  uint32_t e_ld;                  // this epilogue warp's phase parity bit per staged-load mbarrier
-  float* sk_slots;                // stream-K partial slots (sk_slot_floats each, one per block)
-  unsigned* sk_flags;             // stream-K flags (one per block)
-  int sk_slot_floats;
+  uint32_t e_ld;                  // this epilogue warp's staged chunk loads so far
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -1782,52 +1776,16 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])::"memory");
 }
 
-// One tensor-core work item: a tile and, for split-K or stream-K, its range
-// of k blocks.  sk: 0 a whole tile (or a split-K part), 1 a stream-K tile's
-// first k blocks (this block finishes the tile), 2 a stream-K tile's later k
-// blocks (this block leaves their partial sum to the finisher).
+// One tensor-core work item: a tile and, for split-K, its range of k blocks.
 struct TileItem {
   int64_t m0, n0;
-  int kb0, kb1, split, sk;
+  int kb0, kb1, split;
 };
-
-// Stream-K: this block's range of the stage's k-block units (see
-// tkd::Stage), cut at tile boundaries.
-template <typename F>
-__device__ __forceinline__ void for_my_segments(const Ctx& c, const Stage& st, F&& fn) {
-  const int64_t U = st.sk_units, G = gridDim.x, b = blockIdx.x;
-  int64_t u = b * U / G;
-  const int64_t u1 = (b + 1) * U / G;
-  int64_t off = 0;
-  for (int ti = st.task_begin; ti < st.task_end && u < u1; ++ti) {
-    const Task& t = c.tasks[ti];
-    if (t.kind != T_GEMM_TC) break;
-    const int64_t kb = t.k_blocks, units = int64_t(t.n_items) * kb;
-    while (u < u1 && u < off + units) {
-      const int64_t rel = u - off;
-      const int tile = int(rel / kb);
-      TileItem it;
-      it.kb0 = int(rel - int64_t(tile) * kb);
-      it.kb1 = int(min(kb, int64_t(it.kb0) + (u1 - u)));
-      it.m0 = int64_t(tile / t.tiles_n) * kTileM;
-      it.n0 = int64_t(tile % t.tiles_n) * t.tile_n;
-      it.split = 0;
-      it.sk = it.kb0 > 0 ? 2 : (it.kb1 < kb ? 1 : 0);
-      if (!fn(t, it)) return;
-      u += it.kb1 - it.kb0;
-    }
-    off += units;
-  }
-}
 
 // Walk this block's tensor-core items of a stage in order (all roles use the
 // same sequence).  fn(task, item) returns false to stop.
 template <typename F>
 __device__ __forceinline__ void for_my_tiles(const Ctx& c, const Stage& st, F&& fn) {
-  if (st.sk) {
-    for_my_segments(c, st, fn);
-    return;
-  }
   int ti = st.task_begin, base = 0;
   for (int g = blockIdx.x; g < st.n_tc_items; g += gridDim.x) {
     while (g >= base + c.tasks[ti].n_items) {
@@ -1840,7 +1798,6 @@ __device__ __forceinline__ void for_my_tiles(const Ctx& c, const Stage& st, F&& 
     it.m0 = int64_t(tile / t.tiles_n) * kTileM;
     it.n0 = int64_t(tile % t.tiles_n) * t.tile_n;
     it.split = split;
-    it.sk = 0;
     it.kb0 = split * t.kb_split;
     it.kb1 = min(t.k_blocks, it.kb0 + t.kb_split);
     if (!fn(t, it)) return;
@@ -1995,15 +1952,6 @@ __device__ __noinline__ void stage_side(const Task& t, uint32_t buf, uint32_t ds
   }
 }
 
-// Stream-K partial-sum slot layout (float4 units): the piece (lane quarter q,
-// 32-column chunk cc, 4-column vector v) of lane l is at
-// ((q * chunks + cc) * 8 + v) * 32 + l, so each warp access covers 512
-// contiguous bytes; the finisher's lanes read their own rows back with the
-// same mapping.
-__device__ __forceinline__ int sk_piece(int q, int chunks, int cc, int v, int lane) {
-  return ((q * chunks + cc) * 8 + v) * 32 + lane;
-}
-
 // TMA store of a staged 32 x 32 chunk (64-byte swizzle) at (col, row) of the
 // tensor behind `map`; rows and columns beyond the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
@@ -2024,9 +1972,9 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 
 // Returns false if a wait timed out.  Per-row operands (the target, the ReLU
 // mask input, the parameter being updated, a loaded side's operand) arrive as
-// 32 x 32 TMA boxes into t.epi_nbuf buffers per operand, up to nbuf - 1
-// chunks ahead, chunk ch in buffer ch % nbuf on this warp's mbarrier of that
-// index (*eld holds the warp's phase parity bit per mbarrier).  Each lane then turns its row of
+// 32 x 32 TMA boxes into two buffer halves per operand, one chunk ahead, on
+// this warp's two mbarriers (*eld counts the chunk loads the warp has made:
+// it selects the half and the phase parity).  Each lane then turns its row of
 // the chunk into outputs in shared memory (in place in the first per-row
 // operand's half, else in the `only` buffer), and lane 0 stores the chunk with
 // a TMA store; a side output follows the same way.  A buffer is refilled only
@@ -2036,36 +1984,31 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 template <int K>
 __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int64_t m0, int64_t n0, uint32_t taddr,
                                                 uint32_t stg, uint32_t acc_bar, uint32_t phase, long long* stamp,
-                                                const CUtensorMap* maps, uint32_t ebar, uint32_t* eld,
-                                                const float* part, int c0, int c1) {
+                                                const CUtensorMap* maps, uint32_t ebar, uint32_t* eld) {
   const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
   const int row0 = int(m0) + q * 32;
-  // chunks [c0, c1) of the tile's tile_n / 32 (a warp sharing the tile with
-  // another takes part of them); buffer and mbarrier j = (ch - c0) % nbuf
-  const int nch = c1;
+  const int nch = t.tile_n / 32;
   const int mask = t.epi_stage;
   constexpr bool L0 = FastTraits<K>::load0, L1 = FastTraits<K>::load1;
   const bool st0 = L0 && (mask & 1), st1 = L1 && (mask & 2);
   const bool sl = t.has_side && t.side.ext == EXT_LOAD1 && (mask & 8);
   const Fast F = fast_params(c, t);
-  const int nb = t.epi_nbuf;
   // per warp, every piece a multiple of 512 bytes (the 64-byte swizzle's
-  // alignment): nb buffers per per-row operand, two output halves when there
-  // is no per-row operand, nb buffers for a loaded side's operand, then one
+  // alignment): two halves per per-row operand, two output halves when there
+  // is no per-row operand, two halves for a loaded side's operand, then one
   // kBcastBytes row per one-row operand
-  const uint32_t nbb = uint32_t(nb) * kEpiBufBytes;
-  const uint32_t b0 = stg, b1 = b0 + (st0 ? nbb : 0);
-  const uint32_t only = b1 + (st1 ? nbb : 0);
+  const uint32_t b0 = stg, b1 = b0 + (st0 ? 2 * kEpiBufBytes : 0);
+  const uint32_t only = b1 + (st1 ? 2 * kEpiBufBytes : 0);
   const uint32_t bs = only + (st0 || st1 ? 0 : 2 * kEpiBufBytes);
-  const uint32_t r0 = bs + (sl ? nbb : 0);
+  const uint32_t r0 = bs + (sl ? 2 * kEpiBufBytes : 0);
   const uint32_t r1 = r0 + (L0 && !st0 ? kBcastBytes : 0);
   const bool loads = st0 || st1 || sl;
   const uint32_t ld_bytes = uint32_t(int(st0) + int(st1) + int(sl)) * kEpiBufBytes;
-  uint32_t ph = *eld;
+  const uint32_t it = *eld;
   const int64_t col_base = n0;
 
   auto load = [&](int ch) {  // lane 0
-    const uint32_t j = uint32_t((ch - c0) % nb), bar = ebar + 8 * j, off = j * kEpiBufBytes;
+    const uint32_t k = it + uint32_t(ch), h = k & 1u, bar = ebar + 8 * h, off = h * kEpiBufBytes;
     const int x = int(col_base) + 32 * ch;
     mbar_expect_tx(bar, ld_bytes);
     if (st0) tma_load_2d(b0 + off, &maps[t.tma_ld0], x, row0, bar);
@@ -2085,8 +2028,8 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
   int issued = 0;  // chunk loads issued (lane 0)
   if (loads && lane == 0) {
     bulk_wait_read();  // the previous tile's stores are done with the buffers
-    issued = min(c0 + nb - 1, nch);
-    for (int j = c0; j < issued; ++j) load(j);
+    load(0);
+    issued = 1;
   }
   bool ok = mbar_wait(acc_bar, phase, c.timeout_ns);
   if (ok && stamp) *stamp = global_ns();
@@ -2094,47 +2037,31 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
   cp_async_wait<0>();
   __syncwarp();
   const uint32_t tlane = taddr + (uint32_t(q * 32) << 16);
-  int ch = c0;
+  int ch = 0;
 #pragma unroll 1
   for (; ok && ch < nch; ++ch) {
-    const uint32_t j = uint32_t((ch - c0) % nb), half = j * kEpiBufBytes;
+    const uint32_t k = it + uint32_t(ch), h = k & 1u, half = h * kEpiBufBytes;
     const int col0 = int(col_base) + 32 * ch;
     if (lane == 0) {
-      // the buffer the next load fills was last read by chunk ch - 1's
-      // stores; without per-row operands the output half this chunk fills was
-      // last read by chunk ch - 2's stores (chunk ch - 1's last group may still
-      // run)
-      const int nxt = ch + nb - 1;
-      const bool more = loads && nxt < nch;
+      // the half the next load fills was last read by chunk ch - 1's stores;
+      // without per-row operands the output half this chunk fills was last
+      // read by chunk ch - 2's stores (chunk ch - 1's last group may still run)
+      const bool more = loads && ch + 1 < nch;
       if (more) bulk_wait_read();
       else if (!(st0 || st1)) bulk_wait_read_but_last();
       if (more) {
-        load(nxt);
-        issued = nxt + 1;
+        load(ch + 1);
+        issued = ch + 2;
       }
     }
-    if (loads) {
-      if (!mbar_wait(ebar + 8 * j, (ph >> j) & 1u, c.timeout_ns)) {
-        ok = false;
-        break;
-      }
-      ph ^= 1u << j;
+    if (loads && !mbar_wait(ebar + 8 * h, (k >> 1) & 1u, c.timeout_ns)) {
+      ok = false;
+      break;
     }
     __syncwarp();
-    const uint32_t ob = st0 ? b0 + half : (st1 ? b1 + half : only + (uint32_t((ch - c0) & 1) * kEpiBufBytes));
+    const uint32_t ob = st0 ? b0 + half : (st1 ? b1 + half : only + (uint32_t(ch & 1) * kEpiBufBytes));
     uint32_t rv[32];
     tmem_ld32(tlane + uint32_t(32 * ch), rv);
-    if (part) {  // stream-K: the fp32 partial sum of the tile's later k blocks
-      const float4* pp = reinterpret_cast<const float4*>(part);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float4 w = __ldcg(pp + sk_piece(q, t.tile_n / 32, ch, j, lane));  // another SM's: read at L2
-        rv[4 * j] = __float_as_uint(__fadd_rn(__uint_as_float(rv[4 * j]), w.x));
-        rv[4 * j + 1] = __float_as_uint(__fadd_rn(__uint_as_float(rv[4 * j + 1]), w.y));
-        rv[4 * j + 2] = __float_as_uint(__fadd_rn(__uint_as_float(rv[4 * j + 2]), w.z));
-        rv[4 * j + 3] = __float_as_uint(__fadd_rn(__uint_as_float(rv[4 * j + 3]), w.w));
-      }
-    }
     // one 8-wide vector at a time: this thread's row, read and written in place
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
@@ -2168,30 +2095,29 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
   if (!ok && lane == 0) {
     // a wait gave up: the loads already issued land, and the stores already
     // issued finish, before the block moves on
-    for (int k = ch; k < issued; ++k) {
-      const uint32_t j = uint32_t((k - c0) % nb);
-      mbar_wait(ebar + 8 * j, (ph >> j) & 1u, c.timeout_ns);
-      ph ^= 1u << j;
+    for (int j = ch; j < issued; ++j) {
+      const uint32_t k = it + uint32_t(j);
+      mbar_wait(ebar + 8 * (k & 1u), (k >> 1) & 1u, c.timeout_ns);
     }
     bulk_wait_all();
   }
   __syncwarp();
-  *eld = ph;
+  *eld = it + (loads ? uint32_t(nch) : 0u);
   return ok;
 }
 
 __device__ __noinline__ bool tc_epilogue_staged_any(const Ctx c, const Task& t, int64_t m0, int64_t n0,
                                                     uint32_t taddr, uint32_t stg, uint32_t acc_bar, uint32_t phase,
                                                     long long* stamp, const CUtensorMap* maps, uint32_t ebar,
-                                                    uint32_t* eld, const float* part, int c0, int c1) {
+                                                    uint32_t* eld) {
   switch (t.chain.fast) {
-    case FK_E_ACC: return tc_epilogue_staged<FK_E_ACC>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part, c0, c1);
-    case FK_E_BIAS: return tc_epilogue_staged<FK_E_BIAS>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part, c0, c1);
-    case FK_E_BIAS_RELU: return tc_epilogue_staged<FK_E_BIAS_RELU>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part, c0, c1);
-    case FK_E_BIAS_AXPY: return tc_epilogue_staged<FK_E_BIAS_AXPY>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part, c0, c1);
-    case FK_E_ACC_THRESH: return tc_epilogue_staged<FK_E_ACC_THRESH>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part, c0, c1);
-    case FK_E_MOMENTUM: return tc_epilogue_staged<FK_E_MOMENTUM>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part, c0, c1);
-    default: return tc_epilogue_staged<FK_E_UPDATE>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld, part, c0, c1);
+    case FK_E_ACC: return tc_epilogue_staged<FK_E_ACC>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
+    case FK_E_BIAS: return tc_epilogue_staged<FK_E_BIAS>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
+    case FK_E_BIAS_RELU: return tc_epilogue_staged<FK_E_BIAS_RELU>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
+    case FK_E_BIAS_AXPY: return tc_epilogue_staged<FK_E_BIAS_AXPY>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
+    case FK_E_ACC_THRESH: return tc_epilogue_staged<FK_E_ACC_THRESH>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
+    case FK_E_MOMENTUM: return tc_epilogue_staged<FK_E_MOMENTUM>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
+    default: return tc_epilogue_staged<FK_E_UPDATE>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
   }
 }
 
@@ -2394,101 +2320,14 @@ __device__ __noinline__ uint64_t tc_mma(const Ctx c, const Stage st, const TcSta
   return (uint64_t(ok) << 32) | m_it;
 }
 
-// Stream-K hand-off between the block that computes a tile's later k blocks
-// (writer: its 4 epilogue warps each store their 32 rows of the fp32 partial
-// sum, then add 1 to the block's flag) and the block that finishes the tile
-// (each of its 4 epilogue warps waits for the flag to reach 4, adds the
-// partial rows it owns, then adds 1; the fourth to finish sets the flag back
-// to 0 for the next stage).
-__device__ __noinline__ void sk_write_partial(const Task& t, uint32_t taddr, float* slot, unsigned* flag) {
-  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3, chunks = t.tile_n / 32;
-  float4* s4 = reinterpret_cast<float4*>(slot);
-#pragma unroll 1
-  for (int cc = 0; cc < chunks; ++cc) {
-    uint32_t r[32];
-    __syncwarp();
-    tmem_ld32(taddr + (uint32_t(q * 32) << 16) + uint32_t(32 * cc), r);
-#pragma unroll
-    for (int v = 0; v < 8; ++v)
-      s4[sk_piece(q, chunks, cc, v, lane)] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                                         __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-  }
-  __threadfence();
-  __syncwarp();
-  if (lane == 0) atomicAdd(flag, 1u);
-}
-
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Bounded wait (lane 0 polls) for a writer's 4 warps; false if it timed out
-// or another block gave up.
-__device__ __noinline__ bool sk_wait_partial(const Ctx c, const unsigned* flag) {
-  const int lane = threadIdx.x & 31;
-  int ok = 1;
-  if (lane == 0) {
-    unsigned spins = 0;
-    long long t0 = 0;
-    while (ld_acquire(flag) < 4u) {
-      if ((++spins & 31u) == 0u) {
-        if (*reinterpret_cast<volatile int*>(&c.hdr->abort)) {
-          ok = 0;
-          break;
-        }
-        const long long now = global_ns();
-        if (t0 == 0) t0 = now;
-        if (now - t0 > c.timeout_ns) {
-          record_failure(c, TK_ERR_PIPELINE_TIMEOUT, c.stage);
-          ok = 0;
-          break;
-        }
-      }
-    }
-  }
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok) (void)ld_acquire(flag);  // every lane's later reads of the slot see the writer's stores
-  return ok != 0;
-}
-
-__device__ __forceinline__ void sk_release_partial(unsigned* flag) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0 && atomicAdd(flag, 1u) == 7u) atomicExch(flag, 0u);
-}
-
-// The block's last tile of a stage is shared with warps 0-3 (idle once the
-// producer and the MMA issuer are done; warp q reads TMEM lane quarter q like
-// epilogue warp 4 + q): chunks [0, nch/2) here, the rest in
-// tc_epilogue_assist.  Only staged epilogues of whole (non-stream-K-writer,
-// non-split-K) tiles, and only when the helpers' staging fits in a quarter of
-// the then idle TMA ring.
-__device__ __forceinline__ bool assisted(const Task& t, const TileItem& it, const TcState& ts) {
-  return t.epi_stage && t.k_splits == 1 && it.sk != 2 && t.tile_n >= 64 &&
-         ts.stg_warp_bytes <= uint32_t(kStages) * ts.slot_bytes / 4;
-}
-
-__device__ __forceinline__ int count_my_tiles(const Ctx& c, const Stage& st) {
-  int n = 0;
-  for_my_tiles(c, st, [&](const Task&, const TileItem&) {
-    ++n;
-    return true;
-  });
-  return n;
-}
-
 __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const TcState ts, uint32_t e_tile,
-                                             long long* prof, uint32_t* e_ld, uint32_t* join_n) {
+                                             long long* prof, uint32_t* e_ld) {
   bool ok = true;
   bool first = true;
   const int lane = threadIdx.x & 31;
   const uint32_t ew = uint32_t(threadIdx.x >> 5) - 4;
-  const uint32_t stg = ts.stg + ew * ts.stg_warp_bytes, ebar = ts.epi_bar + 8 * kEpiMaxBufs * (4 + ew);
-  const int n_tiles = count_my_tiles(c, st);
-  int idx = 0;
+  const uint32_t stg = ts.stg + ew * ts.stg_warp_bytes, ebar = ts.epi_bar + 16 * ew;
   for_my_tiles(c, st, [&](const Task& t, const TileItem& it) {
-    const bool shared_tile = ++idx == n_tiles && assisted(t, it, ts);
     const int64_t m0 = it.m0, n0 = it.n0;
     const uint32_t acc = e_tile & 1u, ph = (e_tile >> 1) & 1u;
     long long* stamp = prof && first && threadIdx.x == 128 ? prof + 5 : nullptr;
@@ -2498,40 +2337,10 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
       if (stamp) *stamp = global_ns();
       tc_fence_after();
       tc_epilogue_partial(c, t, m0, n0, it.split, ts.tmem + acc * kMaxTileN);
-    } else if (it.sk == 2) {
-      // stream-K: this block's first segment, the later k blocks of a tile
-      // another block finishes: the partial sum goes to this block's slot
-      if (!mbar_wait(ts.acc_full + 8 * acc, ph, c.timeout_ns)) return ok = false;
-      if (stamp) *stamp = global_ns();
-      tc_fence_after();
-      sk_write_partial(t, ts.tmem + acc * kMaxTileN, ts.sk_slots + int64_t(blockIdx.x) * ts.sk_slot_floats,
-                       ts.sk_flags + blockIdx.x);
     } else if (t.epi_stage) {
-      // a stream-K tile's first k blocks: wait for the next block's partial sum
-      const float* part = nullptr;
-      unsigned* flag = ts.sk_flags + blockIdx.x + 1;
-      if (it.sk == 1) {
-        if (!sk_wait_partial(c, flag)) return ok = false;
-        part = ts.sk_slots + int64_t(blockIdx.x + 1) * ts.sk_slot_floats;
-      }
-      const int nch = t.tile_n / 32;
-      if (shared_tile) {
-        // the helper warp may touch the tile (and its staging in the ring)
-        // only once the tile's MMAs are done; this warp waits for the
-        // accumulator in tile order (an mbarrier parity wait must not run
-        // ahead by more than one phase), then lets the helper go
-        if (!mbar_wait(ts.acc_full + 8 * acc, ph, c.timeout_ns)) return ok = false;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(ts.go + 8 * ew);
-      }
       if (!tc_epilogue_staged_any(c, t, m0, n0, ts.tmem + acc * kMaxTileN, stg, ts.acc_full + 8 * acc, ph, stamp,
-                                  ts.maps, ebar, e_ld, part, 0, shared_tile ? nch / 2 : nch))
+                                  ts.maps, ebar, e_ld))
         return ok = false;
-      if (shared_tile) {  // the helper warp's half of the chunks is done too
-        if (!mbar_wait(ts.join + 8 * ew, *join_n & 1u, c.timeout_ns)) return ok = false;
-        ++*join_n;
-      }
-      if (part) sk_release_partial(flag);
     } else {
       if (!mbar_wait(ts.acc_full + 8 * acc, ph, c.timeout_ns)) return ok = false;
       if (stamp) *stamp = global_ns();
@@ -2548,46 +2357,6 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
   if (lane == 0) bulk_wait_all();
   __syncwarp();
   return (uint64_t(ok) << 32) | e_tile;
-}
-
-// Warps 0-3: the second half of the chunks of the block's last tile (see
-// assisted), staged in quarter q of the idle TMA ring, then an arrival on
-// join barrier q for epilogue warp 4 + q.  Returns the tile counter advanced
-// by the stage's tiles (these warps follow the epilogue's sequence) and 1 << 32
-// if every wait completed.
-__device__ __noinline__ uint64_t tc_epilogue_assist(const Ctx c, const Stage st, const TcState ts, uint32_t e_tile,
-                                                    uint32_t* e_ld, uint32_t* join_n) {
-  const int lane = threadIdx.x & 31, q = threadIdx.x >> 5;
-  const int n_tiles = count_my_tiles(c, st);
-  if (n_tiles == 0) return (uint64_t(1) << 32) | e_tile;
-  bool ok = true;
-  int idx = 0;
-  for_my_tiles(c, st, [&](const Task& t, const TileItem& it) {
-    if (++idx < n_tiles) return true;
-    if (!assisted(t, it, ts)) return false;
-    const uint32_t k = e_tile + uint32_t(n_tiles - 1), acc = k & 1u, ph = (k >> 1) & 1u;
-    // epilogue warp 4 + q has seen the tile's accumulator ready (its MMAs, the
-    // last readers of the ring, are done) before this warp writes its staging
-    // area in the ring
-    if (!mbar_wait(ts.go + 8 * q, *join_n & 1u, c.timeout_ns)) return ok = false;
-    const float* part = nullptr;
-    if (it.sk == 1) {  // a stream-K tile's first k blocks: the next block's partial sum
-      if (!sk_wait_partial(c, ts.sk_flags + blockIdx.x + 1)) return ok = false;
-      part = ts.sk_slots + int64_t(blockIdx.x + 1) * ts.sk_slot_floats;
-    }
-    const uint32_t stg = ts.ring + uint32_t(q) * (uint32_t(kStages) * ts.slot_bytes / 4);
-    const uint32_t ebar = ts.epi_bar + 8 * kEpiMaxBufs * q;
-    const int nch = t.tile_n / 32;
-    ok = tc_epilogue_staged_any(c, t, it.m0, it.n0, ts.tmem + acc * kMaxTileN, stg, ts.acc_full + 8 * acc, ph,
-                                nullptr, ts.maps, ebar, e_ld, part, nch / 2, nch);
-    tc_fence_before();
-    if (lane == 0) bulk_wait_all();  // the ring is reused after the phase
-    __syncwarp();
-    if (lane == 0) mbar_arrive(ts.join + 8 * q);
-    ++*join_n;
-    return false;
-  });
-  return (uint64_t(ok) << 32) | (e_tile + uint32_t(n_tiles));
 }
 
 // Run this block's tensor-core tiles of one stage; false after a wait timed out.
@@ -2608,24 +2377,12 @@ __device__ bool run_tc_phase(const Ctx& c, const Stage& st, const CUtensorMap* m
     ok = (r >> 32) != 0;
     if (prof) prof[4] = global_ns();
   } else if (warp >= 4) {
-    uint32_t e_ld = ts.e_ld, join_n = ts.join_n;
-    const uint64_t r = tc_epilogue(c, st, ts, ts.e_tile, prof, &e_ld, &join_n);
+    uint32_t e_ld = ts.e_ld;
+    const uint64_t r = tc_epilogue(c, st, ts, ts.e_tile, prof, &e_ld);
     ts.e_tile = uint32_t(r);
     ts.e_ld = e_ld;
-    ts.join_n = join_n;
     ok = (r >> 32) != 0;
     if (prof && threadIdx.x == 128) prof[6] = global_ns();
-  }
-  if (warp < 4) {
-    // warps 0-3 (the producer and MMA lanes once their loops are done) take
-    // half of the block's last tile's epilogue
-    __syncwarp();
-    uint32_t e_ld = ts.e_ld, join_n = ts.join_n;
-    const uint64_t r = tc_epilogue_assist(c, st, ts, ts.e_tile, &e_ld, &join_n);
-    ts.e_tile = uint32_t(r);
-    ts.e_ld = e_ld;
-    ts.join_n = join_n;
-    ok = ok && (r >> 32) != 0;
   }
   if (!ok) record_failure(c, TK_ERR_PIPELINE_TIMEOUT, stage);
   if (threadIdx.x == 0) *s_flag = 1;
@@ -2725,8 +2482,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   __shared__ Stage s_stage;
   __shared__ Prep s_prep[kThreads / 32];
   __shared__ __align__(8) uint64_t s_bar[2 * kStages + 5];
-  __shared__ __align__(8) uint64_t s_epi_bar[8 * kEpiMaxBufs];
-  __shared__ __align__(8) uint64_t s_join_bar[8];
+  __shared__ __align__(8) uint64_t s_epi_bar[8];
   __shared__ __align__(8) uint64_t s_bulk_bar[kBulkMaxSlots];
   __shared__ uint32_t s_bulk_it;
   __shared__ __align__(8) uint64_t s_col_bar[kBulkMaxSlots];
@@ -2756,12 +2512,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     ts.acc_empty = smem_u32(&s_bar[2 * kStages + 2]);
     ts.drain = smem_u32(&s_bar[2 * kStages + 4]);
     ts.epi_bar = smem_u32(&s_epi_bar[0]);
-    ts.join = smem_u32(&s_join_bar[0]);
-    ts.go = smem_u32(&s_join_bar[4]);
     ts.maps = maps;
-    ts.sk_slots = reinterpret_cast<float*>(p.ws) + prog->sk_slot_base;
-    ts.sk_flags = reinterpret_cast<unsigned*>(p.ws) + prog->sk_flag_base;
-    ts.sk_slot_floats = prog->sk_slot_floats;
     if (threadIdx.x == 0) {
       for (int i = 0; i < kStages; ++i) {
         mbar_init(ts.full + 8 * i, 1);
@@ -2772,8 +2523,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
         mbar_init(ts.acc_empty + 8 * i, 4);
       }
       mbar_init(ts.drain, 1);
-      for (int i = 0; i < 8 * kEpiMaxBufs; ++i) mbar_init(ts.epi_bar + 8 * i, 1);
-      for (int i = 0; i < 8; ++i) mbar_init(ts.join + 8 * i, 1);  // join, then go
+      for (int i = 0; i < 8; ++i) mbar_init(ts.epi_bar + 8 * i, 1);
       for (int i = 0; i < kBulkMaxSlots; ++i) {
         mbar_init(smem_u32(&s_bulk_bar[i]), 1);
         mbar_init(smem_u32(&s_col_bar[i]), kThreads);

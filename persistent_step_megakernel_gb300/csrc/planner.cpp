@@ -1304,21 +1304,16 @@ class Planner {
   // Staging bytes per epilogue warp: two chunk buffers per per-row operand
   // (the output reuses the current one, else has its own buffer) and one
   // tile row per one-row operand.
-  // With nbuf chunk buffers per per-row operand (the prefetch runs nbuf - 1
-  // chunks ahead).
-  int epi_stage_plan(const Plan& plan, const Task& t, int nbuf) const {
+  int epi_stage_plan(const Plan& plan, const Task& t) const {
     const int mask = epi_stage_mask(plan, t);
     if (mask < 0) return 0;
-    const int rows = (mask & 1) + ((mask >> 1) & 1) + ((mask >> 3) & 1);
-    const int bcast = t.chain.n_loads - (mask & 1) - ((mask >> 1) & 1);
-    return stage_bytes(rows, (mask & 3) != 0, bcast, nbuf);
+    const int rows = (mask & 1) + ((mask >> 1) & 1);
+    const int bcast = t.chain.n_loads - rows;
+    return main_stage_bytes(rows, bcast) + ((mask & 8) ? 2 * tkd::kEpiBufBytes : 0);
   }
 
-  // Staging bytes per epilogue warp: nbuf buffers per per-row operand
-  // (the output reuses the current one of the first, else it has two halves
-  // of its own) and one tile row per one-row operand.
-  static int stage_bytes(int rows, bool output_in_place, int bcast, int nbuf) {
-    return (nbuf * rows + (output_in_place ? 0 : 2)) * tkd::kEpiBufBytes + bcast * tkd::kBcastBytes;
+  static int main_stage_bytes(int rows, int bcast) {
+    return 2 * (rows ? rows : 1) * tkd::kEpiBufBytes + bcast * tkd::kBcastBytes;
   }
 
   // Recognise the chain shapes the kernel runs as compiled loops (FastKind).
@@ -1891,52 +1886,6 @@ class Planner {
     return {t, f};
   }
 
-  // The grid tk_run launches, at most (occupancy can only lower it).
-  int64_t grid_bound(int64_t max_items) const {
-    int64_t g = int64_t(sms_) * std::max(1, opt_.blocks_per_sm);
-    g = std::min(g, std::max<int64_t>(max_items, 1));
-    if (opt_.max_blocks > 0) g = std::min<int64_t>(g, opt_.max_blocks);
-    return std::max<int64_t>(g, 1);
-  }
-
-  // Stream-K stages (see tkd::Stage): tensor-core tiles with long K loops
-  // (16 k blocks or more) whose count leaves the last wave at most 97 % full,
-  // every task of the stage on the staged epilogue (it adds the partial sums)
-  // and every block's range at least one whole tile long; and nothing else in
-  // the stage (other work already fills the blocks a partial last wave leaves
-  // idle).  The workspace gets one fp32 slot of a 128 x widest-tile partial
-  // sum and one flag per block.
-  void plan_stream_k(Plan& plan, int max_bn) const {
-    if (!opt_.stream_k) return;
-    const int64_t grid = grid_bound(plan.max_items);
-    bool any = false;
-    for (auto& S : plan.stages) {
-      if (S.n_tc_items <= grid || S.n_items != S.n_tc_items) continue;
-      int64_t units = 0, kb_max = 0;
-      bool ok = true;
-      for (int i = S.task_begin; i < S.task_end; ++i) {
-        const Task& t = plan.tasks[size_t(i)];
-        if (t.kind != tkd::T_GEMM_TC) break;
-        if (t.k_splits != 1 || !t.epi_stage) ok = false;
-        units += int64_t(t.n_items) * t.k_blocks;
-        kb_max = std::max<int64_t>(kb_max, t.k_blocks);
-      }
-      const int64_t waves = ceil_div(S.n_tc_items, grid);
-      const double fill = double(S.n_tc_items) / double(waves * grid);
-      if (!ok || kb_max < 16 || units / grid < kb_max || fill > 0.97) continue;
-      S.sk = 1;
-      S.sk_units = units;
-      any = true;
-    }
-    if (!any) return;
-    plan.sk_slot_floats = tkd::kTileM * max_bn;
-    plan.sk_slots = int32_t(grid);
-    plan.sk_slot_base = plan.workspace_units;
-    plan.workspace_units += round_up(grid * plan.sk_slot_floats, 64);
-    plan.sk_flag_base = plan.workspace_units;
-    plan.workspace_units += round_up(grid, 64);
-  }
-
   // The chain after reduction r, evaluated per finished output of task t.
   void lower_post_chain(Plan& plan, Task& t, const OpInfo& r, const Fused& fu) {
     const Shape out_shape = shape_of(r.out);
@@ -2196,26 +2145,18 @@ class Planner {
     // SM's unified L1/shared memory to the L1 cache.
     plan.ring_stage_bytes = tkd::kStageBytesA + max_bn * tkd::kTileK * 2;
     const size_t ring = 1024 + size_t(tkd::kStages) * plan.ring_stage_bytes;
-    // Staged epilogues: the deepest operand prefetch (up to 4 buffers, at most
-    // one per 32-column chunk of the tile) that fits beside the ring.
     for (auto& t : plan.tasks) {
       t.epi_stage = 0;
-      t.epi_nbuf = 2;
       t.tma_out = t.tma_out2 = t.tma_ld0 = t.tma_ld1 = t.tma_sd = -1;
-      if (epi_stage_plan(plan, t, 2) <= 0) continue;
-      for (int nbuf = std::min(tkd::kEpiMaxBufs, std::max(2, t.tile_n / 32)); nbuf >= 2; --nbuf) {
-        const int need = epi_stage_plan(plan, t, nbuf);
-        if (ring + 4 * size_t(std::max(need, plan.epi_warp_bytes)) > size_t(tkd::kDynSmemBudget)) continue;
+      const int need = epi_stage_plan(plan, t);
+      if (need > 0 && ring + 4 * size_t(std::max(need, plan.epi_warp_bytes)) <= size_t(tkd::kDynSmemBudget)) {
         const int mask = epi_stage_mask(plan, t);
-        if (!epilogue_maps(plan, t, mask)) break;
+        if (!epilogue_maps(plan, t, mask)) continue;
         plan.epi_warp_bytes = std::max(plan.epi_warp_bytes, need);
         t.epi_stage = mask;
-        t.epi_nbuf = nbuf;
-        break;
       }
     }
     plan.smem_bytes = plan.uses_tc ? ring + 4 * size_t(plan.epi_warp_bytes) : 1024 + size_t(tkd::kWorkFloats) * 4;
-    plan_stream_k(plan, max_bn);
     for (const auto& s : inputs_) plan.input_bytes.push_back(extent_of(s) * esize(s.dtype));
     for (const auto& s : outputs_) plan.output_bytes.push_back(numel(s) * esize(s.dtype));
     for (const auto& kv : inplace_) plan.inplace.push_back({kv.first, kv.second});

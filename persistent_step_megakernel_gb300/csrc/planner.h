@@ -50,9 +50,6 @@ struct Plan {
   int32_t max_items = 1;
   size_t smem_bytes = 0;
   int ring_stage_bytes = 0;  // TMA ring slot size for the widest tensor-core tile
-  // stream-K partial slots and flags (see tkd::Stage); sk_slots == 0: none
-  int64_t sk_slot_base = 0, sk_flag_base = 0;
-  int32_t sk_slot_floats = 0, sk_slots = 0;
   int epi_warp_bytes = 0;    // epilogue staging per epilogue warp
   bool uses_tc = false;
   tk_plan_stats stats{};

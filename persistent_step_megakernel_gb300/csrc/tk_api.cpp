@@ -110,10 +110,6 @@ tk_status upload(tk_program* p) {
   prog.code = reinterpret_cast<const tkd::Instr*>(base + off_code);
   prog.refs = reinterpret_cast<const tkd::Ref*>(base + off_refs);
   prog.n_prefetch = int32_t(pf.size());
-  prog.sk_slot_base = pl.sk_slot_base;
-  prog.sk_flag_base = pl.sk_flag_base;
-  prog.sk_slot_floats = pl.sk_slot_floats;
-  prog.sk_slots = pl.sk_slots;
   prog.prefetch = reinterpret_cast<const tkd::Prefetch*>(base + off_pf);
   std::memcpy(host.data() + off_prog, &prog, sizeof(prog));
   if (!pf.empty()) std::memcpy(host.data() + off_pf, pf.data(), pf.size() * sizeof(tkd::Prefetch));
@@ -220,7 +216,6 @@ void tk_options_default(tk_options* opt) {
   opt->sm_count = 0;
   opt->barrier_timeout_s = 2.0;
   opt->split_k = 1;
-  opt->stream_k = 1;
 }
 
 tk_status tk_program_create(const tk_program_desc* desc, const tk_options* opt_in, int device, tk_program** out) {
@@ -326,10 +321,6 @@ tk_status tk_workspace_init(const tk_program* p, float* ws, size_t n, void* stre
   DeviceGuard g(p->device);
   cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(tkd::Header), static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace header)");
-  if (p->plan.sk_slots > 0) {  // stream-K flags
-    e = cudaMemsetAsync(ws + p->plan.sk_flag_base, 0, size_t(p->plan.sk_slots) * 4, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(stream-K flags)");
-  }
   return TK_OK;
 }
 
@@ -479,8 +470,6 @@ tk_status tk_plan_task(const tk_program* p, int32_t index, tk_task_info* info) {
   r.parts = t.parts > 0 ? t.parts : 1;
   r.staged_epilogue = t.epi_stage != 0;
   r.side_output = t.has_side != 0;
-  r.stream_k = t.kind == tkd::T_GEMM_TC && t.stage >= 0 && size_t(t.stage) < p->plan.stages.size() &&
-               p->plan.stages[size_t(t.stage)].sk != 0;
   r.numel = t.numel;
   *info = r;
   return TK_OK;

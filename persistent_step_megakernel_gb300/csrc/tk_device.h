@@ -46,7 +46,6 @@ constexpr int kBulkOffset = 16 * 1024;
 constexpr int kBulkSlotBytes = 16 * 1024;
 constexpr int kBulkMaxSlots = 12;
 constexpr int kEpiBufBytes = 32 * 64;
-constexpr int kEpiMaxBufs = 4;   // chunk buffers per per-row operand of a staged epilogue, at most
 constexpr int kBcastBytes = kMaxTileN * 2;   // one 16-bit row of a tile
 constexpr int kTmemCols = 2 * kMaxTileN;                // double-buffered accumulator
 constexpr int kMaxMaps = 192;                           // TMA descriptors per launch
@@ -219,7 +218,6 @@ struct alignas(16) Task {
   // copied through shared memory too.  0 = operands and output accessed
   // directly.
   int32_t epi_stage;
-  int32_t epi_nbuf;          // chunk buffers per per-row operand (2..kEpiMaxBufs)
   // TMA descriptors of a staged epilogue's 32 x 32 chunks (64-byte swizzle,
   // the staging layout): the output, the side output, the per-row operands
   // of load slots 0 and 1 and the loaded side's operand (-1: none).
@@ -233,23 +231,12 @@ struct alignas(16) Task {
   int32_t kb_split;
 };
 
-// Stream-K (sk = 1): the stage's tensor-core work is cut into k-block units
-// (tiles x k blocks of every tensor-core task, in task order) and block b
-// takes units [b U / G, (b + 1) U / G) of the U units over a grid of G blocks,
-// instead of whole tiles round-robin, so that no block idles in a last,
-// partly filled wave.  A tile cut in two is finished by the block holding its
-// first k blocks (its last segment), after adding the fp32 partial sum of the
-// rest, which the next block computed as its first segment and left in its
-// workspace slot behind a flag.  Every block's range holds at least the
-// longest tile's k blocks, so a tile has at most these two parts.
 struct Stage {
   int32_t task_begin, task_end;
   int32_t n_items;           // all items of the stage (tensor-core tiles first)
   int32_t n_tc_items;
   int32_t code_lo, code_hi;  // instructions the stage's tasks use
   int32_t ref_lo, ref_hi;    // operand refs the stage's tasks use
-  int32_t sk, sk_pad;        // stream-K for the tensor-core tiles
-  int64_t sk_units;          // U: k-block units of the stage's tensor-core tiles
 };
 
 // A stage whose descriptors fit these bounds is copied into shared memory
@@ -278,12 +265,6 @@ struct Program {
   const Ref* refs;
   int32_t n_prefetch, pad;
   const Prefetch* prefetch;
-  // stream-K: one partial slot of sk_slot_floats floats per block (float
-  // offset sk_slot_base in the workspace) and one flag per block (float
-  // offset sk_flag_base; zeroed by workspace initialisation, and back to zero
-  // after every stage)
-  int64_t sk_slot_base, sk_flag_base;
-  int32_t sk_slot_floats, sk_slots;
 };
 
 // Workspace header (offset 0, 256 bytes).  `count` only grows during a run

@@ -70,8 +70,8 @@ def test_fused_plan_bit_identical_to_unfused(key):
     fused = S.mlp_step_program(cfg, export="grads")
     unfused = S.mlp_step_program(cfg, export="all")
     arrays = S.mlp_inputs(cfg, fused)
-    a, sa = run_step(fused, arrays, stream_k=0)
-    b, sb = run_step(unfused, arrays, fuse_epilogues=0, stream_k=0)
+    a, sa = run_step(fused, arrays)
+    b, sb = run_step(unfused, arrays, fuse_epilogues=0)
     assert sa.stats["fused_epilogues"] > 0 and sb.stats["fused_epilogues"] == 0
     names_b = {s.buffer: v for s, v in zip(unfused.outputs, b)}
     for s, v in zip(fused.outputs, a):
@@ -85,9 +85,9 @@ def test_expression_forms_bit_identical(key):
     cfg = SMALL[key]
     prog = S.mlp_step_program(cfg, export="grads")
     arrays = S.mlp_inputs(cfg, prog)
-    ref, s0 = run_step(prog, arrays, expr_forms=0, stream_k=0)
+    ref, s0 = run_step(prog, arrays, expr_forms=0)
     for forms in (1, 2):
-        got, st = run_step(prog, arrays, expr_forms=forms, stream_k=0)
+        got, st = run_step(prog, arrays, expr_forms=forms)
         assert st.stats["compiled_tasks"] == 0
         for spec, x, y in zip(prog.outputs, ref, got):
             np.testing.assert_array_equal(x, y, err_msg=f"{spec.buffer} forms={forms}")
@@ -154,8 +154,8 @@ def test_state_program_fused_matches_unfused_over_steps(key):
     cfg = SMALL[key]
     prog = S.mlp_step_program(cfg, export="state")
     arrays = S.mlp_inputs(cfg, prog)
-    fused, sf = run_step(prog, arrays, steps=2, stream_k=0)
-    plain, sp = run_step(prog, arrays, steps=2, fuse_epilogues=0, fuse_pointwise=0, stream_k=0)
+    fused, sf = run_step(prog, arrays, steps=2)
+    plain, sp = run_step(prog, arrays, steps=2, fuse_epilogues=0, fuse_pointwise=0)
     assert sf.stats["stages"] <= sp.stats["stages"]
     for spec, x, y in zip(prog.outputs, fused, plain):
         np.testing.assert_array_equal(x, y, err_msg=spec.buffer)

@@ -66,8 +66,8 @@ def test_wide_tiles_fused_bit_identical_to_unfused(key, bn):
     fused = S.mlp_step_program(cfg, export="grads")
     unfused = S.mlp_step_program(cfg, export="all")
     arrays = S.mlp_inputs(cfg, fused)
-    a, sa = run_step(fused, arrays, tile_n=bn, stream_k=0)
-    b, _ = run_step(unfused, arrays, tile_n=bn, fuse_epilogues=0, stream_k=0)
+    a, sa = run_step(fused, arrays, tile_n=bn)
+    b, _ = run_step(unfused, arrays, tile_n=bn, fuse_epilogues=0)
     tiles = tc_tasks(sa)
     assert all(t["tile_n"] == bn for t in tiles)
     assert any(t["staged_epilogue"] for t in tiles)
@@ -84,8 +84,8 @@ def test_wide_tiles_state_program_fused_matches_unfused_over_steps(key, bn):
     cfg = WIDE[key]
     prog = S.mlp_step_program(cfg, export="state")
     arrays = S.mlp_inputs(cfg, prog)
-    fused, _ = run_step(prog, arrays, steps=2, tile_n=bn, stream_k=0)
-    plain, _ = run_step(prog, arrays, steps=2, tile_n=bn, fuse_epilogues=0, fuse_pointwise=0, stream_k=0)
+    fused, _ = run_step(prog, arrays, steps=2, tile_n=bn)
+    plain, _ = run_step(prog, arrays, steps=2, tile_n=bn, fuse_epilogues=0, fuse_pointwise=0)
     for spec, x, y in zip(prog.outputs, fused, plain):
         np.testing.assert_array_equal(x, y, err_msg=spec.buffer)
 
@@ -119,8 +119,8 @@ def test_full_ffn_block_fused_bit_identical_to_unfused():
     fused = S.mlp_step_program(cfg, export="grads")
     unfused = S.mlp_step_program(cfg, export="all")
     arrays = S.mlp_inputs(cfg, fused)
-    a, _ = run_step(fused, arrays, stream_k=0)
-    b, _ = run_step(unfused, arrays, fuse_epilogues=0, stream_k=0)
+    a, _ = run_step(fused, arrays)
+    b, _ = run_step(unfused, arrays, fuse_epilogues=0)
     names_b = {s.buffer: v for s, v in zip(unfused.outputs, b)}
     for s, v in zip(fused.outputs, a):
         np.testing.assert_array_equal(v, names_b[s.buffer], err_msg=s.buffer)
@@ -129,12 +129,11 @@ def test_full_ffn_block_fused_bit_identical_to_unfused():
 @pytest.mark.parametrize("key", ["c3", "c5"])
 def test_full_timed_program_fused_matches_unfused_over_steps(key):
     # the program the benchmark times, against its plan with no fusion at all
-    # (whole tiles in both: stream-K cut points depend on the stage layout)
     cfg = S.CONFIGS[key]
     prog = S.mlp_step_program(cfg, export="state")
     arrays = S.mlp_inputs(cfg, prog)
-    fused, sf = run_on_device(prog, arrays, steps=2, stream_k=0)
-    plain, sp = run_on_device(prog, arrays, steps=2, fuse_epilogues=0, fuse_pointwise=0, stream_k=0)
+    fused, sf = run_on_device(prog, arrays, steps=2)
+    plain, sp = run_on_device(prog, arrays, steps=2, fuse_epilogues=0, fuse_pointwise=0)
     widths = {t["tile_n"] for t in tc_tasks(sf)}
     assert widths == {t["tile_n"] for t in tc_tasks(sp)}
     if key == "c5":
@@ -162,8 +161,8 @@ def test_full_gemm_bound_fused_bit_identical_to_unfused():
     fused = S.mlp_step_program(C5_TWO, export="grads")
     unfused = S.mlp_step_program(C5_TWO, export="all")
     arrays = S.mlp_inputs(C5_TWO, fused)
-    a, sa = run_on_device(fused, arrays, stream_k=0)
-    b, _ = run_on_device(unfused, arrays, fuse_epilogues=0, stream_k=0)
+    a, sa = run_on_device(fused, arrays)
+    b, _ = run_on_device(unfused, arrays, fuse_epilogues=0)
     tiles = tc_tasks(sa)
     assert any(t["staged_epilogue"] and t["side_output"] and t["tile_n"] == 256 for t in tiles)
     names_b = {s.buffer: v for s, v in zip(unfused.outputs, b)}

@@ -454,13 +454,14 @@ def stage_profile(cfg, device, warmup=5):
         """Median over the blocks with tensor-core tiles in stage s of the
         time from the stage's start to: the producer done, the first operand
         tile landed, the MMA issue done, the first accumulator ready, the
-        epilogue done, the barrier arrival (µs)."""
+        epilogue's last store issued, the epilogue done (its stores complete),
+        the barrier arrival (µs)."""
         rows = [r for r in best["stamps"][s] if r[3] > 0 and r[0] > 0]
         if not rows:
             return None
         med = lambda i: round(statistics.median((r[i] - r[0]) / 1e3 for r in rows), 2)
         return {"blocks": len(rows), "producer_done": med(2), "first_tile": med(3), "mma_done": med(4),
-                "first_acc": med(5), "epilogue_done": med(6), "arrive": med(1)}
+                "first_acc": med(5), "stores_issued": med(8), "epilogue_done": med(6), "arrive": med(1)}
 
     def run(flushed):
         runs = []

@@ -143,9 +143,14 @@ typedef struct {
                                   bit-identical results; 1 and 2 exist for testing. */
   int32_t split_k;             /* 1: split the K loop of under-filled tensor-core GEMMs over more
                                   SMs (partial sums, then a pass that adds them; default 1) */
-  int32_t tile_n;              /* N width of every tensor-core tile: 0 (default) picks 64, 128 or
-                                  256 per GEMM from its tile count and the SM count; 64, 128 or 256
-                                  forces that width (used by tests to reach each tile path) */
+  int32_t tile_n;              /* N width of every tensor-core tile: 0 (default) picks 64, 128,
+                                  224 or 256 per GEMM from its tile count and the SM count; 64,
+                                  128, 224 or 256 forces that width (224 only where the B operand
+                                  is K-major, else 256; used by tests to reach each tile path) */
+  int32_t epi_stage_bytes;     /* cap on the shared-memory staging bytes of each epilogue warp
+                                  (0, default: what the SM has left beside the operand ring).
+                                  Smaller caps give shallower staging rings; results are
+                                  identical (used by tests to reach each staging layout) */
 } tk_options;
 
 /* What the planner decided (codegen.py `GeneratedKernel` counters). */
@@ -187,6 +192,8 @@ typedef struct {
   int32_t parts;               /* reduction parts (1 = not split) */
   int32_t staged_epilogue;     /* tensor-core GEMM whose epilogue moves tiles through shared memory */
   int32_t side_output;         /* GEMM that also writes a second value (a side output) from its tile */
+  int32_t staged_depth;        /* staged epilogue: 32-column chunks in flight per epilogue warp
+                                  (2, 4 or 8; +16 when a side output has buffers of its own); 0 */
   int64_t numel;               /* elements of the task's index space */
 } tk_task_info;
 
@@ -241,13 +248,14 @@ tk_status tk_run_status(const tk_program* program, const float* workspace, void*
 tk_status tk_resource_usage(const tk_program* program, int64_t out[4]);
 
 /* Per-stage timing of the last run of a program created with profile = 1.
- * Synchronises `stream`, then copies stages * grid_blocks groups of 8
- * %globaltimer stamps (ns) into stamps[(s*grid+b)*8 + i]: i = 0 block b starts
+ * Synchronises `stream`, then copies stages * grid_blocks groups of 9
+ * %globaltimer stamps (ns) into stamps[(s*grid+b)*9 + i]: i = 0 block b starts
  * stage s, 1 it reaches the barrier after it, 2 its TMA producer is done,
  * 3 its first operand tile has landed, 4 its MMA issue is done, 5 its first
- * accumulator is ready, 6 its epilogue is done (2-6 are 0 when the block has
- * no tensor-core tile in that stage), 7 kernel entry (stage 0 only).
- * n_stamps must be >= 8 * stages * grid_blocks (see tk_plan_stats). */
+ * accumulator is ready, 6 its epilogue is done (its stores complete), 8 its
+ * epilogue has issued its last store (2-6 and 8 are 0 when the block has no
+ * tensor-core tile in that stage), 7 kernel entry (stage 0 only).
+ * n_stamps must be >= 9 * stages * grid_blocks (see tk_plan_stats). */
 tk_status tk_profile_read(const tk_program* program, const float* workspace, void* stream, int64_t* stamps,
                           size_t n_stamps);
 

@@ -54,7 +54,8 @@ class tk_options(ctypes.Structure):
                 ("inline_input_casts", ctypes.c_int32), ("tensor_cores", ctypes.c_int32),
                 ("sm_count", ctypes.c_int32), ("profile", ctypes.c_int32),
                 ("barrier_timeout_s", ctypes.c_double), ("expr_forms", ctypes.c_int32),
-                ("split_k", ctypes.c_int32), ("tile_n", ctypes.c_int32)]
+                ("split_k", ctypes.c_int32), ("tile_n", ctypes.c_int32),
+                ("epi_stage_bytes", ctypes.c_int32)]
 
 
 class tk_plan_stats(ctypes.Structure):
@@ -69,7 +70,7 @@ class tk_plan_stats(ctypes.Structure):
 class tk_task_info(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "stage", "kind", "op_index", "n_items", "form", "compiled_shape", "m", "n", "k", "tile_m", "tile_n",
-        "parts", "staged_epilogue", "side_output")] + [("numel", ctypes.c_int64)]
+        "parts", "staged_epilogue", "side_output", "staged_depth")] + [("numel", ctypes.c_int64)]
 
 
 # (name, restype, argtypes) for every entry point of include/tk.h
@@ -260,11 +261,11 @@ def tk_resource_usage(handle) -> dict:
                      "resident_blocks_per_sm"), list(out)))
 
 
-PROFILE_STAMPS = 8
+PROFILE_STAMPS = 9
 
 
 def tk_profile_read(handle, workspace_ptr: int, stages: int, grid: int, stream: int = 0):
-    """Stamps as a list [stage][block] of 8-tuples (see tk_profile_read in tk.h)."""
+    """Stamps as a list [stage][block] of 9-tuples (see tk_profile_read in tk.h)."""
     n = PROFILE_STAMPS * stages * grid
     buf = (ctypes.c_int64 * n)()
     check(lib().tk_profile_read(handle, ctypes.c_void_p(workspace_ptr), ctypes.c_void_p(stream), buf, n))

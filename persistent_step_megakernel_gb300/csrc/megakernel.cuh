@@ -1462,6 +1462,15 @@ __device__ __noinline__ void run_gemm_simt(const Ctx c, const Task& t, int item,
 // role's registers for the whole kernel, so every stage continues the same
 // phase sequence.
 
+// An epilogue warp's staging ring: the task whose layout it currently holds,
+// the chunks staged through it since that task began (chunk k uses buffer
+// k % depth of each region) and the phase of each buffer's load mbarrier.
+struct EpiRing {
+  int32_t task;
+  uint32_t k;
+  uint32_t phases;
+};
+
 struct TcState {
   uint32_t ring;                  // shared address of the 1024-aligned ring
   uint32_t slot_bytes;            // bytes per ring slot (A tile, then B tile)
@@ -1471,10 +1480,10 @@ struct TcState {
   uint32_t tmem;                  // TMEM base address
   uint32_t stg;                   // shared address of the epilogue staging area
   uint32_t stg_warp_bytes;        // staging bytes per epilogue warp
-  uint32_t epi_bar;               // 2 mbarriers per epilogue warp (staged-epilogue operand loads)
+  uint32_t epi_bar;               // kEpiMaxDepth mbarriers per epilogue warp (staged-epilogue operand loads)
   const CUtensorMap* maps;        // the launch's TMA descriptors
   uint32_t p_it, m_it, m_tile, e_tile;
-  uint32_t e_ld;                  // this epilogue warp's staged chunk loads so far
+  EpiRing er;                      // this epilogue warp's staging ring
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -1923,17 +1932,19 @@ __device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
 
 // A GEMM's side output from a staged chunk: each lane turns its row of the
 // stored (rounded) values in `buf` into the side values and writes them to
-// `dst` (buf itself, or for a loaded side the buffer holding its operand,
-// read from there).  The caller stores dst.
-__device__ __noinline__ void stage_side(const Task& t, uint32_t buf, uint32_t dst, int out_dt) {
+// `dst` (buf itself, a buffer of its own, or for a loaded side the buffer
+// holding its operand, read from there).  Every value is of the 16-bit type
+// DT.  The caller stores dst.
+template <int DT>
+__device__ __forceinline__ void stage_side(const Task& t, uint32_t buf, uint32_t dst) {
   const int lane = threadIdx.x & 31;
   const bool loaded = t.side.ext == EXT_LOAD1;
-#pragma unroll 1
+#pragma unroll
   for (int v = 0; v < 4; ++v) {
     float x[8], e[8];
-    unpack8(lds128(buf + stg_off(lane, v)), out_dt, x);
+    unpack8(lds128(buf + stg_off(lane, v)), DT, x);
     if (loaded) {
-      unpack8(lds128(dst + stg_off(lane, v)), t.side_ld.dtype, e);
+      unpack8(lds128(dst + stg_off(lane, v)), DT, e);
       const bool sub = t.side.op == OP_SUB, second = t.side.second;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -1948,7 +1959,7 @@ __device__ __noinline__ void stage_side(const Task& t, uint32_t buf, uint32_t ds
 #pragma unroll
       for (int j = 0; j < 8; ++j) x[j] = -x[j];
     }
-    sts128(dst + stg_off(lane, v), pack8(x, t.out2.dtype));  // rounds to the side's type
+    sts128(dst + stg_off(lane, v), pack8(x, DT));  // rounds to the side's type
   }
 }
 
@@ -1962,54 +1973,94 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // every committed bulk store of this thread has finished reading shared memory
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// ... all but the most recently committed group
-__device__ __forceinline__ void bulk_wait_read_but_last() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
 // every committed bulk store of this thread has completed
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// Returns false if a wait timed out.  Per-row operands (the target, the ReLU
-// mask input, the parameter being updated, a loaded side's operand) arrive as
-// 32 x 32 TMA boxes into two buffer halves per operand, one chunk ahead, on
-// this warp's two mbarriers (*eld counts the chunk loads the warp has made:
-// it selects the half and the phase parity).  Each lane then turns its row of
-// the chunk into outputs in shared memory (in place in the first per-row
-// operand's half, else in the `only` buffer), and lane 0 stores the chunk with
-// a TMA store; a side output follows the same way.  A buffer is refilled only
-// after the stores reading it have finished reading.  An operand with one row
-// for all tile rows (a bias) is copied once per tile by cp.async: its tile_n
-// values.
-template <int K>
-__device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int64_t m0, int64_t n0, uint32_t taddr,
-                                                uint32_t stg, uint32_t acc_bar, uint32_t phase, long long* stamp,
-                                                const CUtensorMap* maps, uint32_t ebar, uint32_t* eld) {
+// Lane 0: every bulk store group this thread committed, except the `n` most
+// recent ones, has finished reading shared memory (n above 7 waits as for 7).
+__device__ __forceinline__ void bulk_wait_read_n(uint32_t n) {
+  switch (n) {
+    case 0: asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.bulk.wait_group.read 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.bulk.wait_group.read 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.bulk.wait_group.read 6;" ::: "memory"); break;
+    default: asm volatile("cp.async.bulk.wait_group.read 7;" ::: "memory"); break;
+  }
+}
+
+// Returns false if a wait timed out.  The tile's 32-column chunks move through
+// this warp's staging ring of D = t.epi_depth buffers per region: per-row
+// operands (the target, the ReLU mask input, the parameter being updated, a
+// loaded side's operand) arrive as 32 x 32 TMA boxes on the buffer's mbarrier,
+// up to D - 1 chunks ahead (D - 2 from D = 4 on, so that a refill never waits
+// for the stores of the chunk just finished); each lane turns its row of the
+// chunk into outputs in shared memory (in place in the first per-row operand's
+// buffer, else in the chunk's output buffer), and lane 0 stores the chunk with
+// a TMA store, a side output the same way (from its own buffer, from the
+// loaded side's buffer, or in place once the output's store has read it).
+// Lane 0 commits one bulk group per chunk, so a buffer last used by ring chunk
+// j is free once all but the groups of the chunks after j have been read.  An
+// operand with one row for all tile rows (a bias) is copied once per tile by
+// cp.async: its tile_n values.
+template <int K, int DT>
+__device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int task_id, int64_t m0, int64_t n0,
+                                                uint32_t taddr, uint32_t stg, uint32_t acc_bar, uint32_t phase,
+                                                long long* stamp, const CUtensorMap* maps, uint32_t ebar,
+                                                EpiRing* er) {
   const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
   const int row0 = int(m0) + q * 32;
-  const int nch = t.tile_n / 32;
+  // 32-column chunks holding columns of the output (a 224-wide tile at the
+  // right edge may hold only a few)
+  const uint32_t nch = uint32_t((min(int64_t(t.tile_n), int64_t(t.n) - n0) + 31) / 32);
   const int mask = t.epi_stage;
+  const uint32_t D = uint32_t(t.epi_depth), dmask = D - 1;  // 2, 4 or 8
   constexpr bool L0 = FastTraits<K>::load0, L1 = FastTraits<K>::load1;
   const bool st0 = L0 && (mask & 1), st1 = L1 && (mask & 2);
   const bool sl = t.has_side && t.side.ext == EXT_LOAD1 && (mask & 8);
-  const Fast F = fast_params(c, t);
-  // per warp, every piece a multiple of 512 bytes (the 64-byte swizzle's
-  // alignment): two halves per per-row operand, two output halves when there
-  // is no per-row operand, two halves for a loaded side's operand, then one
-  // kBcastBytes row per one-row operand
-  const uint32_t b0 = stg, b1 = b0 + (st0 ? 2 * kEpiBufBytes : 0);
-  const uint32_t only = b1 + (st1 ? 2 * kEpiBufBytes : 0);
-  const uint32_t bs = only + (st0 || st1 ? 0 : 2 * kEpiBufBytes);
-  const uint32_t r0 = bs + (sl ? 2 * kEpiBufBytes : 0);
+  const bool su = t.has_side && !sl && (mask & 16);
+  // every operand, rounding and output is of type DT: the conversions are
+  // compiled for it, with no branch on a type read at run time
+  Fast F = fast_params(c, t);
+  F.dt0 = F.dt1 = F.out_dt = DT;
+  F.r0 = F.r1 = F.r2 = F.er = DT;
+  // per warp, regions of D buffers (each a multiple of 512 bytes, the 64-byte
+  // swizzle's alignment): per-row operand 0, per-row operand 1, the outputs
+  // when there is no per-row operand, a loaded side's operand, a unary side's
+  // values; then one kBcastBytes row per one-row operand
+  const uint32_t reg = D * kEpiBufBytes;
+  const uint32_t b0 = stg, b1 = b0 + (st0 ? reg : 0);
+  const uint32_t only = b1 + (st1 ? reg : 0);
+  const uint32_t bs = only + (st0 || st1 ? 0 : reg);
+  const uint32_t bu = bs + (sl ? reg : 0);
+  const uint32_t r0 = bu + (su ? reg : 0);
   const uint32_t r1 = r0 + (L0 && !st0 ? kBcastBytes : 0);
   const bool loads = st0 || st1 || sl;
+  const bool own_out = !(st0 || st1) || su;  // buffers written without a load first
   const uint32_t ld_bytes = uint32_t(int(st0) + int(st1) + int(sl)) * kEpiBufBytes;
-  const uint32_t it = *eld;
-  const int64_t col_base = n0;
-
-  auto load = [&](int ch) {  // lane 0
-    const uint32_t k = it + uint32_t(ch), h = k & 1u, bar = ebar + 8 * h, off = h * kEpiBufBytes;
-    const int x = int(col_base) + 32 * ch;
+  if (er->task != task_id) {
+    // the staging area takes this task's layout: every earlier store has
+    // finished reading it first
+    if (lane == 0) bulk_wait_read();
+    er->task = task_id;
+    er->k = 0;
+  }
+  const uint32_t k = er->k;
+  const uint32_t lag = D >= 4 ? 2u : 1u;
+  // lane 0: before chunk j's buffers are refilled or rewritten, the stores of
+  // ring chunk k + j - D (their last user) have read them; ring chunks before
+  // `done` have committed their groups
+  auto free_bufs = [&](uint32_t j, uint32_t done) {
+    const uint32_t kk = k + j;
+    if (kk >= D) bulk_wait_read_n(done - 1u - (kk - D));
+  };
+  auto load = [&](uint32_t j, uint32_t done) {  // lane 0
+    free_bufs(j, done);
+    const uint32_t b = (k + j) & dmask, bar = ebar + 8 * b, off = b * kEpiBufBytes;
+    const int x = int(n0) + 32 * int(j);
     mbar_expect_tx(bar, ld_bytes);
     if (st0) tma_load_2d(b0 + off, &maps[t.tma_ld0], x, row0, bar);
     if (st1) tma_load_2d(b1 + off, &maps[t.tma_ld1], x, row0, bar);
@@ -2025,49 +2076,43 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
     }
   }
   cp_async_commit();
-  int issued = 0;  // chunk loads issued (lane 0)
-  if (loads && lane == 0) {
-    bulk_wait_read();  // the previous tile's stores are done with the buffers
-    load(0);
-    issued = 1;
-  }
+  uint32_t issued = 0;  // chunk loads issued (lane 0)
+  if (loads && lane == 0)
+    for (; issued < nch && issued + lag <= D; ++issued) load(issued, k);
   bool ok = mbar_wait(acc_bar, phase, c.timeout_ns);
   if (ok && stamp) *stamp = global_ns();
   tc_fence_after();
   cp_async_wait<0>();
   __syncwarp();
+  uint32_t phases = er->phases;
   const uint32_t tlane = taddr + (uint32_t(q * 32) << 16);
-  int ch = 0;
+  uint32_t ch = 0;
 #pragma unroll 1
   for (; ok && ch < nch; ++ch) {
-    const uint32_t k = it + uint32_t(ch), h = k & 1u, half = h * kEpiBufBytes;
-    const int col0 = int(col_base) + 32 * ch;
+    const uint32_t kk = k + ch, b = kk & dmask, off = b * kEpiBufBytes;
+    const int col0 = int(n0) + 32 * int(ch);
     if (lane == 0) {
-      // the half the next load fills was last read by chunk ch - 1's stores;
-      // without per-row operands the output half this chunk fills was last
-      // read by chunk ch - 2's stores (chunk ch - 1's last group may still run)
-      const bool more = loads && ch + 1 < nch;
-      if (more) bulk_wait_read();
-      else if (!(st0 || st1)) bulk_wait_read_but_last();
-      if (more) {
-        load(ch + 1);
-        issued = ch + 2;
-      }
+      if (loads)
+        for (; issued < nch && issued + lag <= ch + D; ++issued) load(issued, kk);
+      if (own_out) free_bufs(ch, kk);
     }
-    if (loads && !mbar_wait(ebar + 8 * h, (k >> 1) & 1u, c.timeout_ns)) {
-      ok = false;
-      break;
+    if (loads) {
+      if (!mbar_wait(ebar + 8 * b, (phases >> b) & 1u, c.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      phases ^= 1u << b;
     }
     __syncwarp();
-    const uint32_t ob = st0 ? b0 + half : (st1 ? b1 + half : only + (uint32_t(ch & 1) * kEpiBufBytes));
+    const uint32_t ob = st0 ? b0 + off : (st1 ? b1 + off : only + off);
     uint32_t rv[32];
-    tmem_ld32(tlane + uint32_t(32 * ch), rv);
+    tmem_ld32(tlane + 32 * ch, rv);
     // one 8-wide vector at a time: this thread's row, read and written in place
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
       float l0[8], l1[8], a8[8], x[8];
-      if constexpr (L0) unpack8(lds128(st0 ? b0 + half + stg_off(lane, v) : r0 + 64 * ch + 16 * v), F.dt0, l0);
-      if constexpr (L1) unpack8(lds128(st1 ? b1 + half + stg_off(lane, v) : r1 + 64 * ch + 16 * v), F.dt1, l1);
+      if constexpr (L0) unpack8(lds128(st0 ? b0 + off + stg_off(lane, v) : r0 + 64 * ch + 16 * v), F.dt0, l0);
+      if constexpr (L1) unpack8(lds128(st1 ? b1 + off + stg_off(lane, v) : r1 + 64 * ch + 16 * v), F.dt1, l1);
 #pragma unroll
       for (int j = 0; j < 8; ++j) a8[j] = __uint_as_float(rv[8 * v + j]);
       fast_apply<K, false>(F, l0, l1, a8, x);
@@ -2077,15 +2122,16 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
     __syncwarp();
     if (lane == 0) tma_store_2d(&maps[t.tma_out], ob, col0, row0);
     if (t.has_side) {
-      if (!sl) {  // the side values replace the outputs in ob once the store has read them
+      uint32_t dst = sl ? bs + off : bu + off;
+      if (!sl && !su) {  // in place: the side values replace the outputs once their store has read them
         if (lane == 0) {
           bulk_commit();
           bulk_wait_read();
         }
         __syncwarp();
+        dst = ob;
       }
-      const uint32_t dst = sl ? bs + half : ob;
-      stage_side(t, ob, dst, F.out_dt);
+      stage_side<DT>(t, ob, dst);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) tma_store_2d(&maps[t.tma_out2], dst, col0, row0);
@@ -2095,30 +2141,39 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int6
   if (!ok && lane == 0) {
     // a wait gave up: the loads already issued land, and the stores already
     // issued finish, before the block moves on
-    for (int j = ch; j < issued; ++j) {
-      const uint32_t k = it + uint32_t(j);
-      mbar_wait(ebar + 8 * (k & 1u), (k >> 1) & 1u, c.timeout_ns);
+    for (uint32_t j = ch; j < issued; ++j) {
+      const uint32_t b = (k + j) & dmask;
+      mbar_wait(ebar + 8 * b, (phases >> b) & 1u, c.timeout_ns);
+      phases ^= 1u << b;
     }
     bulk_wait_all();
   }
   __syncwarp();
-  *eld = it + (loads ? uint32_t(nch) : 0u);
+  er->k = k + nch;
+  er->phases = phases;
   return ok;
 }
 
-__device__ __noinline__ bool tc_epilogue_staged_any(const Ctx c, const Task& t, int64_t m0, int64_t n0,
+__device__ __noinline__ bool tc_epilogue_staged_any(const Ctx c, const Task& t, int task_id, int64_t m0, int64_t n0,
                                                     uint32_t taddr, uint32_t stg, uint32_t acc_bar, uint32_t phase,
                                                     long long* stamp, const CUtensorMap* maps, uint32_t ebar,
-                                                    uint32_t* eld) {
-  switch (t.chain.fast) {
-    case FK_E_ACC: return tc_epilogue_staged<FK_E_ACC>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
-    case FK_E_BIAS: return tc_epilogue_staged<FK_E_BIAS>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
-    case FK_E_BIAS_RELU: return tc_epilogue_staged<FK_E_BIAS_RELU>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
-    case FK_E_BIAS_AXPY: return tc_epilogue_staged<FK_E_BIAS_AXPY>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
-    case FK_E_ACC_THRESH: return tc_epilogue_staged<FK_E_ACC_THRESH>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
-    case FK_E_MOMENTUM: return tc_epilogue_staged<FK_E_MOMENTUM>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
-    default: return tc_epilogue_staged<FK_E_UPDATE>(c, t, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, eld);
+                                                    EpiRing* er) {
+#define TK_STAGED(KIND, DT) \
+  tc_epilogue_staged<KIND, DT>(c, t, task_id, m0, n0, taddr, stg, acc_bar, phase, stamp, maps, ebar, er)
+#define TK_STAGED_KINDS(DT)                                       \
+  switch (t.chain.fast) {                                         \
+    case FK_E_ACC: return TK_STAGED(FK_E_ACC, DT);                \
+    case FK_E_BIAS: return TK_STAGED(FK_E_BIAS, DT);              \
+    case FK_E_BIAS_RELU: return TK_STAGED(FK_E_BIAS_RELU, DT);    \
+    case FK_E_BIAS_AXPY: return TK_STAGED(FK_E_BIAS_AXPY, DT);    \
+    case FK_E_ACC_THRESH: return TK_STAGED(FK_E_ACC_THRESH, DT);  \
+    case FK_E_MOMENTUM: return TK_STAGED(FK_E_MOMENTUM, DT);      \
+    default: return TK_STAGED(FK_E_UPDATE, DT);                   \
   }
+  if (t.epi_dtype == TK_BF16) TK_STAGED_KINDS(TK_BF16)
+  TK_STAGED_KINDS(TK_F16)
+#undef TK_STAGED_KINDS
+#undef TK_STAGED
 }
 
 // Split-K: this split's float32 accumulator, as is, to its scratch plane.
@@ -2321,12 +2376,12 @@ __device__ __noinline__ uint64_t tc_mma(const Ctx c, const Stage st, const TcSta
 }
 
 __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const TcState ts, uint32_t e_tile,
-                                             long long* prof, uint32_t* e_ld) {
+                                             long long* prof, EpiRing* er) {
   bool ok = true;
   bool first = true;
   const int lane = threadIdx.x & 31;
   const uint32_t ew = uint32_t(threadIdx.x >> 5) - 4;
-  const uint32_t stg = ts.stg + ew * ts.stg_warp_bytes, ebar = ts.epi_bar + 16 * ew;
+  const uint32_t stg = ts.stg + ew * ts.stg_warp_bytes, ebar = ts.epi_bar + 8 * kEpiMaxDepth * ew;
   for_my_tiles(c, st, [&](const Task& t, const TileItem& it) {
     const int64_t m0 = it.m0, n0 = it.n0;
     const uint32_t acc = e_tile & 1u, ph = (e_tile >> 1) & 1u;
@@ -2338,8 +2393,8 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
       tc_fence_after();
       tc_epilogue_partial(c, t, m0, n0, it.split, ts.tmem + acc * kMaxTileN);
     } else if (t.epi_stage) {
-      if (!tc_epilogue_staged_any(c, t, m0, n0, ts.tmem + acc * kMaxTileN, stg, ts.acc_full + 8 * acc, ph, stamp,
-                                  ts.maps, ebar, e_ld))
+      if (!tc_epilogue_staged_any(c, t, int(&t - c.tasks), m0, n0, ts.tmem + acc * kMaxTileN, stg,
+                                  ts.acc_full + 8 * acc, ph, stamp, ts.maps, ebar, er))
         return ok = false;
     } else {
       if (!mbar_wait(ts.acc_full + 8 * acc, ph, c.timeout_ns)) return ok = false;
@@ -2354,6 +2409,7 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
     return true;
   });
   // the stage's TMA stores complete before the block reaches the grid barrier
+  if (prof && threadIdx.x == 128) prof[8] = global_ns();
   if (lane == 0) bulk_wait_all();
   __syncwarp();
   return (uint64_t(ok) << 32) | e_tile;
@@ -2377,10 +2433,10 @@ __device__ bool run_tc_phase(const Ctx& c, const Stage& st, const CUtensorMap* m
     ok = (r >> 32) != 0;
     if (prof) prof[4] = global_ns();
   } else if (warp >= 4) {
-    uint32_t e_ld = ts.e_ld;
-    const uint64_t r = tc_epilogue(c, st, ts, ts.e_tile, prof, &e_ld);
+    EpiRing er = ts.er;
+    const uint64_t r = tc_epilogue(c, st, ts, ts.e_tile, prof, &er);
     ts.e_tile = uint32_t(r);
-    ts.e_ld = e_ld;
+    ts.er = er;
     ok = (r >> 32) != 0;
     if (prof && threadIdx.x == 128) prof[6] = global_ns();
   }
@@ -2482,7 +2538,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   __shared__ Stage s_stage;
   __shared__ Prep s_prep[kThreads / 32];
   __shared__ __align__(8) uint64_t s_bar[2 * kStages + 5];
-  __shared__ __align__(8) uint64_t s_epi_bar[8];
+  __shared__ __align__(8) uint64_t s_epi_bar[4 * kEpiMaxDepth];
   __shared__ __align__(8) uint64_t s_bulk_bar[kBulkMaxSlots];
   __shared__ uint32_t s_bulk_it;
   __shared__ __align__(8) uint64_t s_col_bar[kBulkMaxSlots];
@@ -2513,6 +2569,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     ts.drain = smem_u32(&s_bar[2 * kStages + 4]);
     ts.epi_bar = smem_u32(&s_epi_bar[0]);
     ts.maps = maps;
+    ts.er.task = -1;
     if (threadIdx.x == 0) {
       for (int i = 0; i < kStages; ++i) {
         mbar_init(ts.full + 8 * i, 1);
@@ -2523,7 +2580,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
         mbar_init(ts.acc_empty + 8 * i, 4);
       }
       mbar_init(ts.drain, 1);
-      for (int i = 0; i < 8; ++i) mbar_init(ts.epi_bar + 8 * i, 1);
+      for (int i = 0; i < 4 * kEpiMaxDepth; ++i) mbar_init(ts.epi_bar + 8 * i, 1);
       for (int i = 0; i < kBulkMaxSlots; ++i) {
         mbar_init(smem_u32(&s_bulk_bar[i]), 1);
         mbar_init(smem_u32(&s_col_bar[i]), kThreads);

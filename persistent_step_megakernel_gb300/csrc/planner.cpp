@@ -1298,22 +1298,63 @@ class Planner {
       if ((r.stride[0] * 2) % 16 != 0) return -1;
       mask |= 1 << s;
     }
+    if (epi_uniform_dtype(plan, t) == 0) return -1;
     return mask;
   }
 
-  // Staging bytes per epilogue warp: two chunk buffers per per-row operand
-  // (the output reuses the current one, else has its own buffer) and one
-  // tile row per one-row operand.
-  int epi_stage_plan(const Plan& plan, const Task& t) const {
-    const int mask = epi_stage_mask(plan, t);
-    if (mask < 0) return 0;
-    const int rows = (mask & 1) + ((mask >> 1) & 1);
-    const int bcast = t.chain.n_loads - rows;
-    return main_stage_bytes(rows, bcast) + ((mask & 8) ? 2 * tkd::kEpiBufBytes : 0);
+  // The one 16-bit type of every operand, rounding and output of a GEMM
+  // epilogue (with its side output), or 0 if they mix types.  The staged
+  // epilogue is compiled per type, so that its conversions carry no
+  // branches on a type read at run time.
+  static int epi_uniform_dtype(const Plan& plan, const Task& t) {
+    const tkd::Chain& ch = t.chain;
+    const int dt = t.out.dtype;
+    if (dt != TK_BF16 && dt != TK_F16) return 0;
+    bool same = ch.round0 == dt;
+    for (int i = 0; i < ch.n_steps; ++i) {
+      same = same && ch.steps[i].round == dt;
+      if (ch.steps[i].ext_mul) same = same && ch.steps[i].ext_round == dt;
+    }
+    for (int s = 0; s < ch.n_loads; ++s) same = same && plan.refs[t.ref_begin + ch.load_ref[s]].dtype == dt;
+    if (t.has_side) {
+      same = same && t.out2.dtype == dt && t.side.round == dt;
+      if (t.side.ext == tkd::EXT_LOAD1) same = same && t.side_ld.dtype == dt;
+    }
+    return same ? dt : 0;
   }
 
-  static int main_stage_bytes(int rows, int bcast) {
-    return 2 * (rows ? rows : 1) * tkd::kEpiBufBytes + bcast * tkd::kBcastBytes;
+  // Staging bytes per epilogue warp at a ring depth of `depth` chunks: per
+  // chunk one buffer per per-row operand (the output is written in place into
+  // the first, else it has its own buffer), one for a loaded side's operand and
+  // one for a unary side output when `side_buf`; then one tile row per one-row
+  // operand.
+  static int epi_stage_bytes(const Task& t, int mask, int depth, bool side_buf) {
+    const int rows = (mask & 1) + ((mask >> 1) & 1);
+    const int bcast = t.chain.n_loads - rows;
+    const int bufs = (rows ? rows : 1) + ((mask & 8) ? 1 : 0) + (side_buf ? 1 : 0);
+    return depth * bufs * tkd::kEpiBufBytes + bcast * tkd::kBcastBytes;
+  }
+
+  // Ring depth (chunks staged at once: 2, 4 or 8, at most the tile's chunks)
+  // and whether a unary side output gets buffers of its own, for the staging
+  // bytes `avail` an epilogue warp may use: the deepest ring first, side
+  // buffers before depth (without them every chunk waits for its output's
+  // store to leave shared memory).  Returns the bytes used, 0 if nothing fits.
+  static int epi_stage_fit(const Task& t, int mask, int avail, int* depth, bool* side_buf) {
+    const bool unary_side = t.has_side && !(mask & 8);
+    const int nch = t.tile_n / 32;
+    int top = tkd::kEpiMaxDepth;
+    while (top > nch) top /= 2;
+    for (int sb = unary_side ? 1 : 0; sb >= 0; --sb)
+      for (int d = top; d >= 2; d /= 2) {
+        const int need = epi_stage_bytes(t, mask, d, sb != 0);
+        if (need <= avail) {
+          *depth = d;
+          *side_buf = sb != 0;
+          return need;
+        }
+      }
+    return 0;
   }
 
   // Recognise the chain shapes the kernel runs as compiled loops (FastKind).
@@ -1539,7 +1580,21 @@ class Planner {
     if (opt_.tile_n > 0) bn = opt_.tile_n;
     TmaOperand ta, tb;
     int a_mn = 0, b_mn = 0;
-    if (!tma_operand(A, true, tkd::kTileM, &ta, &a_mn) || !tma_operand(B, false, bn, &tb, &b_mn)) return false;
+    if (!tma_operand(A, true, tkd::kTileM, &ta, &a_mn) || !tma_operand(B, false, bn == 224 ? 256 : bn, &tb, &b_mn))
+      return false;
+    // A K-major B tile may also be 224 wide (seven 32-column chunks; MN-major
+    // B tiles load whole 64-wide slabs).  Where the 256-wide tiles leave a
+    // partial last wave on the SMs, take 224 if it makes the waves times the
+    // bytes each k block stages (A tile + B tile) smaller: 4096 x 4096 outputs
+    // take 512 tiles = 3.4 waves at 256, 608 = 4 waves at 224.
+    if (opt_.tile_n == 0 && bn == 256 && b_mn == 0) {
+      auto cost = [&](int w) {
+        return ceil_div(ceil_div(M, tkd::kTileM) * ceil_div(N, w), sms_) * (tkd::kStageBytesA + w * tkd::kTileK * 2);
+      };
+      if (cost(224) < cost(256)) bn = 224;
+    }
+    if (bn == 224 && b_mn != 0) bn = 256;
+    if (bn == 224 && !tma_operand(B, false, bn, &tb, &b_mn)) return false;
     t.kind = tkd::T_GEMM_TC;
     t.tile_m = tkd::kTileM;
     t.tile_n = bn;
@@ -2145,16 +2200,23 @@ class Planner {
     // SM's unified L1/shared memory to the L1 cache.
     plan.ring_stage_bytes = tkd::kStageBytesA + max_bn * tkd::kTileK * 2;
     const size_t ring = 1024 + size_t(tkd::kStages) * plan.ring_stage_bytes;
+    // every staged task may use the staging bytes left beside the ring
+    const int avail = ring < size_t(tkd::kDynSmemBudget) ? int((size_t(tkd::kDynSmemBudget) - ring) / 4) : 0;
     for (auto& t : plan.tasks) {
       t.epi_stage = 0;
+      t.epi_depth = 0;
+      t.epi_dtype = 0;
       t.tma_out = t.tma_out2 = t.tma_ld0 = t.tma_ld1 = t.tma_sd = -1;
-      const int need = epi_stage_plan(plan, t);
-      if (need > 0 && ring + 4 * size_t(std::max(need, plan.epi_warp_bytes)) <= size_t(tkd::kDynSmemBudget)) {
-        const int mask = epi_stage_mask(plan, t);
-        if (!epilogue_maps(plan, t, mask)) continue;
-        plan.epi_warp_bytes = std::max(plan.epi_warp_bytes, need);
-        t.epi_stage = mask;
-      }
+      int mask = epi_stage_mask(plan, t), depth = 0;
+      bool side_buf = false;
+      if (mask < 0) continue;
+      const int need = epi_stage_fit(t, mask, opt_.epi_stage_bytes > 0 ? std::min(avail, opt_.epi_stage_bytes) : avail,
+                                     &depth, &side_buf);
+      if (need == 0 || !epilogue_maps(plan, t, mask)) continue;
+      plan.epi_warp_bytes = std::max(plan.epi_warp_bytes, need);
+      t.epi_stage = mask | (side_buf ? 16 : 0);
+      t.epi_depth = depth;
+      t.epi_dtype = epi_uniform_dtype(plan, t);
     }
     plan.smem_bytes = plan.uses_tc ? ring + 4 * size_t(plan.epi_warp_bytes) : 1024 + size_t(tkd::kWorkFloats) * 4;
     for (const auto& s : inputs_) plan.input_bytes.push_back(extent_of(s) * esize(s.dtype));

@@ -230,8 +230,9 @@ tk_status tk_program_create(const tk_program_desc* desc, const tk_options* opt_i
   if (!(opt.barrier_timeout_s > 0.0) || opt.barrier_timeout_s > 3600.0)
     return fail(TK_ERR_INVALID, "barrier_timeout_s must be in (0, 3600]");
   if (opt.sm_count < 0) return fail(TK_ERR_INVALID, "sm_count must be >= 0");
-  if (opt.tile_n != 0 && opt.tile_n != 64 && opt.tile_n != 128 && opt.tile_n != 256)
-    return fail(TK_ERR_INVALID, "tile_n must be 0, 64, 128 or 256");
+  if (opt.tile_n != 0 && opt.tile_n != 64 && opt.tile_n != 128 && opt.tile_n != 224 && opt.tile_n != 256)
+    return fail(TK_ERR_INVALID, "tile_n must be 0, 64, 128, 224 or 256");
+  if (opt.epi_stage_bytes < 0) return fail(TK_ERR_INVALID, "epi_stage_bytes must be >= 0");
 
   int sms = opt.sm_count > 0 ? opt.sm_count : 152;
   if (device >= 0) {
@@ -470,6 +471,7 @@ tk_status tk_plan_task(const tk_program* p, int32_t index, tk_task_info* info) {
   r.parts = t.parts > 0 ? t.parts : 1;
   r.staged_epilogue = t.epi_stage != 0;
   r.side_output = t.has_side != 0;
+  r.staged_depth = t.epi_stage ? t.epi_depth + ((t.epi_stage & 16) ? 16 : 0) : 0;
   r.numel = t.numel;
   *info = r;
   return TK_OK;

@@ -46,6 +46,7 @@ constexpr int kBulkOffset = 16 * 1024;
 constexpr int kBulkSlotBytes = 16 * 1024;
 constexpr int kBulkMaxSlots = 12;
 constexpr int kEpiBufBytes = 32 * 64;
+constexpr int kEpiMaxDepth = 8;                         // chunk buffers (and mbarriers) per epilogue warp
 constexpr int kBcastBytes = kMaxTileN * 2;   // one 16-bit row of a tile
 constexpr int kTmemCols = 2 * kMaxTileN;                // double-buffered accumulator
 constexpr int kMaxMaps = 192;                           // TMA descriptors per launch
@@ -215,9 +216,14 @@ struct alignas(16) Task {
   // Staged epilogue (compiled GEMM epilogues with 16-bit output): bit s set =
   // load slot s is read per row and copied through shared memory; bit 2 =
   // the staged path is on; bit 3 = the side output's operand (side_ld) is
-  // copied through shared memory too.  0 = operands and output accessed
-  // directly.
+  // copied through shared memory too; bit 4 = a unary side output has chunk
+  // buffers of its own.  0 = operands and output accessed directly.
+  // epi_depth: chunk buffers per operand in each epilogue warp's ring
+  // (2, 4 or 8; at most the tile's 32-column chunks); epi_dtype: the one
+  // 16-bit type of all the staged epilogue's operands, roundings and outputs.
   int32_t epi_stage;
+  int32_t epi_depth;
+  int32_t epi_dtype;
   // TMA descriptors of a staged epilogue's 32 x 32 chunks (64-byte swizzle,
   // the staging layout): the output, the side output, the per-row operands
   // of load slots 0 and 1 and the loaded side's operand (-1: none).
@@ -283,8 +289,9 @@ struct Header {
 // Kernel arguments: io[i] is input i, io[kMaxIO + j] is output j.
 // Profile stamps per (stage, block): 0 stage begin, 1 barrier arrival,
 // 2 producer done, 3 first operand tile ready, 4 MMA issue done, 5 first
-// accumulator ready, 6 epilogue done, 7 kernel entry (stage 0 only).
-constexpr int kProfStamps = 8;
+// accumulator ready, 6 epilogue done, 7 kernel entry (stage 0 only), 8 the
+// epilogue's last store issued.
+constexpr int kProfStamps = 9;
 
 struct Params {
   const Program* prog;

@@ -43,7 +43,16 @@ def tc_tasks(step):
     return [t for t in step.tasks() if t["kind"] == "gemm_tc"]
 
 
-@pytest.mark.parametrize("bn", [128, 256])
+def widths_ok(tiles, bn):
+    # forcing 224 gives 224-wide tiles where B is K-major (the forward GEMMs)
+    # and 256 elsewhere (the backward GEMMs read B along its rows)
+    if bn != 224:
+        return all(t["tile_n"] == bn for t in tiles)
+    fwd = [t for t in tiles if t["op"].startswith("z")]
+    return fwd and all(t["tile_n"] == 224 for t in fwd) and all(t["tile_n"] in (224, 256) for t in tiles)
+
+
+@pytest.mark.parametrize("bn", [128, 224, 256])
 @pytest.mark.parametrize("key", list(WIDE))
 def test_wide_tiles_each_op_matches_oracle_teacher_forced(key, bn):
     cfg = WIDE[key]
@@ -51,13 +60,13 @@ def test_wide_tiles_each_op_matches_oracle_teacher_forced(key, bn):
     arrays = S.mlp_inputs(cfg, prog)
     outs, step = run_step(prog, arrays, tile_n=bn)
     tiles = tc_tasks(step)
-    assert tiles and all(t["tile_n"] == bn for t in tiles)
+    assert tiles and widths_ok(tiles, bn)
     report = []
     teacher_forced(prog, arrays, outs, report=report)
     assert any(op.startswith("gW") for op, _, _ in report)
 
 
-@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("bn", [128, 224, 256])
 @pytest.mark.parametrize("key", list(WIDE))
 def test_wide_tiles_fused_bit_identical_to_unfused(key, bn):
     # the fused plan runs the staged epilogue (with the loss gradient as a
@@ -69,7 +78,7 @@ def test_wide_tiles_fused_bit_identical_to_unfused(key, bn):
     a, sa = run_step(fused, arrays, tile_n=bn)
     b, _ = run_step(unfused, arrays, tile_n=bn, fuse_epilogues=0)
     tiles = tc_tasks(sa)
-    assert all(t["tile_n"] == bn for t in tiles)
+    assert widths_ok(tiles, bn)
     assert any(t["staged_epilogue"] for t in tiles)
     if cfg.loss == "mse":
         assert any(t["staged_epilogue"] and t["side_output"] for t in tiles)
@@ -78,7 +87,7 @@ def test_wide_tiles_fused_bit_identical_to_unfused(key, bn):
         np.testing.assert_array_equal(v, names_b[s.buffer], err_msg=s.buffer)
 
 
-@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("bn", [128, 224, 256])
 @pytest.mark.parametrize("key", list(WIDE))
 def test_wide_tiles_state_program_fused_matches_unfused_over_steps(key, bn):
     cfg = WIDE[key]
@@ -88,6 +97,28 @@ def test_wide_tiles_state_program_fused_matches_unfused_over_steps(key, bn):
     plain, _ = run_step(prog, arrays, steps=2, tile_n=bn, fuse_epilogues=0, fuse_pointwise=0)
     for spec, x, y in zip(prog.outputs, fused, plain):
         np.testing.assert_array_equal(x, y, err_msg=spec.buffer)
+
+
+@pytest.mark.parametrize("key", ["wide_f16_mom", "wide_bf16"])
+def test_staging_ring_depths_bit_identical(key):
+    # the deepest staging rings (all chunks of a momentum tile in flight, the
+    # loss gradient in buffers of its own) against depth 2 with the side values
+    # written in place, over two steps of the timed program and the grads one
+    cfg = WIDE[key]
+    for export, steps in (("state", 2), ("grads", 1)):
+        prog = S.mlp_step_program(cfg, export=export)
+        arrays = S.mlp_inputs(cfg, prog)
+        deep, sd = run_step(prog, arrays, steps=steps, tile_n=128)
+        flat, sf = run_step(prog, arrays, steps=steps, tile_n=128, epi_stage_bytes=8192)
+        deep_d = [t["staged_depth"] for t in tc_tasks(sd)]
+        flat_d = [t["staged_depth"] for t in tc_tasks(sf)]
+        assert all(f & 15 <= d & 15 for d, f in zip(deep_d, flat_d))
+        assert any(f & 15 < d & 15 for d, f in zip(deep_d, flat_d)), (deep_d, flat_d)
+        # with the cap, staged side outputs (the momentum step's W', the loss
+        # gradient) run at depth 2, the unary one in place
+        assert all(t["staged_depth"] in (0, 2) for t in tc_tasks(sf) if t["side_output"])
+        for spec, x, y in zip(prog.outputs, deep, flat):
+            np.testing.assert_array_equal(x, y, err_msg=(export, spec.buffer))
 
 
 # ------------------------------------------------------------ full sizes
@@ -134,18 +165,21 @@ def test_full_timed_program_fused_matches_unfused_over_steps(key):
     arrays = S.mlp_inputs(cfg, prog)
     fused, sf = run_on_device(prog, arrays, steps=2)
     plain, sp = run_on_device(prog, arrays, steps=2, fuse_epilogues=0, fuse_pointwise=0)
-    widths = {t["tile_n"] for t in tc_tasks(sf)}
-    assert widths == {t["tile_n"] for t in tc_tasks(sp)}
+    widths = {t["op"]: t["tile_n"] for t in tc_tasks(sf)}
+    assert widths == {t["op"]: t["tile_n"] for t in tc_tasks(sp)}
     if key == "c5":
-        assert widths == {256}
+        # forward GEMMs 4 full waves of 224-wide tiles, backward 256-wide
+        assert {t["tile_n"] for t in tc_tasks(sf) if t["op"].startswith("z")} == {224}
+        assert {t["tile_n"] for t in tc_tasks(sf) if not t["op"].startswith("z")} == {256}
     for spec, x, y in zip(prog.outputs, fused, plain):
         assert torch.equal(x, y), spec.buffer
 
 
 # Two layers of the GEMM-bound step: every GEMM has the full 4096 x 4096 x 4096
-# shape and the planner's 128 x 256 tiles (forward with ReLU, the output layer
-# with the MSE epilogue and its side output, weight and input gradients with
-# the ReLU mask, the fused SGD updates).
+# shape and the planner's tiles (128 x 224 forward: 19 column tiles, the last
+# with 64 live columns; 128 x 256 backward): forward with ReLU, the output
+# layer with the MSE epilogue and its side output, weight and input gradients
+# with the ReLU mask, the fused SGD updates.
 C5_TWO = S.scaled(S.CONFIGS["c5"], dims=(4096, 4096, 4096))
 
 
@@ -153,7 +187,7 @@ def test_full_gemm_bound_each_op_matches_oracle_teacher_forced():
     prog = S.mlp_step_program(C5_TWO, export="all")
     arrays = S.mlp_inputs(C5_TWO, prog)
     outs, step = run_step(prog, arrays)
-    assert {t["tile_n"] for t in tc_tasks(step)} == {256}
+    assert {t["tile_n"] for t in tc_tasks(step)} == {224, 256}
     teacher_forced(prog, arrays, outs, sample=2048)
 
 
@@ -164,7 +198,7 @@ def test_full_gemm_bound_fused_bit_identical_to_unfused():
     a, sa = run_on_device(fused, arrays)
     b, _ = run_on_device(unfused, arrays, fuse_epilogues=0)
     tiles = tc_tasks(sa)
-    assert any(t["staged_epilogue"] and t["side_output"] and t["tile_n"] == 256 for t in tiles)
+    assert any(t["staged_epilogue"] and t["side_output"] and t["tile_n"] == 224 for t in tiles)
     names_b = {s.buffer: v for s, v in zip(unfused.outputs, b)}
     for s, v in zip(fused.outputs, a):
         assert torch.equal(v, names_b[s.buffer]), s.buffer

@@ -259,6 +259,37 @@ def test_tensor_core_epilogues_are_staged(name):
     assert tc and direct == []
 
 
+def _tc_tasks(prog, **opts):
+    h = B.tk_program_create(prog, B.options(sm_count=152, **opts), device=-1)
+    try:
+        tasks = [B.tk_plan_task(h, i) for i in range(B.tk_plan_stats_get(h)["tasks"])]
+    finally:
+        B.tk_program_destroy(h)
+    return {prog.operations[t["op_index"]].name: t for t in tasks if t["kind"] == "gemm_tc"}
+
+
+def test_staging_ring_depth_follows_the_shared_memory_left():
+    # C3's momentum GEMMs (128-wide tiles, a 128 KB ring): v and W of all four
+    # 32-column chunks of a tile fit at once (depth 4); C2's output layer gets
+    # buffers of its own for the loss gradient (depth 2 + 16); C5's 192 KB ring
+    # leaves room for depth 2 only, with the side values written in place
+    c3 = _tc_tasks(S.mlp_step_program(S.CONFIGS["c3"], export="state"))
+    assert c3["gW1"]["staged_depth"] == c3["gW2"]["staged_depth"] == 4
+    assert c3["z1"]["staged_depth"] == 2                     # 64-wide tiles: two chunks
+    c2 = _tc_tasks(S.mlp_step_program(S.CONFIGS["c2"], export="state"))
+    assert c2["z3"]["side_output"] and c2["z3"]["staged_depth"] == 2 + 16
+    c5 = _tc_tasks(S.mlp_step_program(S.CONFIGS["c5"], export="state"))
+    assert {t["staged_depth"] for t in c5.values()} == {2}
+    # a cap on the staging bytes of each epilogue warp gives shallower rings
+    capped = _tc_tasks(S.mlp_step_program(S.CONFIGS["c3"], export="state"), epi_stage_bytes=8192)
+    assert capped["gW1"]["staged_depth"] == 2
+    capped = _tc_tasks(S.mlp_step_program(S.CONFIGS["c2"], export="state"), epi_stage_bytes=8192)
+    assert capped["z3"]["staged_depth"] == 2
+    assert not _tc_tasks(S.mlp_step_program(S.CONFIGS["c2"], export="state"), epi_stage_bytes=1024)["z3"]["staged_epilogue"]
+    with pytest.raises(B.TkError):
+        plan(S.mlp_step_program(S.CONFIGS["c2"], export="state"), epi_stage_bytes=-1)
+
+
 def test_reduction_epilogue_fuses_the_bias_update():
     g, b = f32("g", (16, 8)), f32("b", (8,))
     ops = [Operation("gb", "sum", (g,), f32("gb", (8,)), {"dims": (0,)}),

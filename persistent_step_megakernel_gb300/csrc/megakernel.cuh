@@ -2646,14 +2646,27 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     c.refs = st.ref_hi - st.ref_lo <= kStageRefs ? s_refs - st.ref_lo : prog->refs;
     if (tc && st.n_tc_items > 0 && !run_tc_phase(c, st, maps, ts, s, &s_flag, prof ? prof + s * prof_step : nullptr))
       break;
-    int ti = st.task_begin, base = 0;
-    for (int g = blockIdx.x; g < st.n_items; g += gridDim.x) {
-      if (g < st.n_tc_items) continue;  // handled by the tensor-core phase
-      while (ti < st.task_end && g >= base + c.tasks[ti].n_items) {
-        base += c.tasks[ti].n_items;
-        ++ti;
+    // the stage's other items after its tiles: blocks with one tile fewer
+    // than the busiest (r = tiles mod grid of them have one more) first take
+    // up to light_items each, the rest go round-robin from block r on
+    {
+      const int G = gridDim.x, b = blockIdx.x, T = st.n_tc_items, n_rest = st.n_items - T;
+      const int r = T % G, n_light = r ? G - r : 0;
+      const int extra = min(n_rest, n_light * st.light_items);
+      // this block's first-round items j = b - r + k * n_light (k < n1), then
+      // j = extra + (b - r) mod G + k' * G
+      const int n1 = b >= r && extra > b - r ? (extra - (b - r) + n_light - 1) / n_light : 0;
+      int ti = st.task_begin, base = 0;
+      for (int k = 0;; ++k) {
+        const int j = k < n1 ? b - r + k * n_light : extra + (b - r + G) % G + (k - n1) * G;
+        if (j >= n_rest) break;
+        const int g = T + j;
+        while (ti < st.task_end && g >= base + c.tasks[ti].n_items) {
+          base += c.tasks[ti].n_items;
+          ++ti;
+        }
+        run_item(c, c.tasks[ti], g - base, s_work);
       }
-      run_item(c, c.tasks[ti], g - base, s_work);
     }
     asm volatile("fence.proxy.async.global;" ::: "memory");
     __syncthreads();

@@ -1302,6 +1302,35 @@ class Planner {
     return mask;
   }
 
+  // How many of a stage's other items (reductions, pointwise, split-K sums)
+  // one tensor-core tile is worth, from rough per-SM costs: a tile ~0.4 us
+  // per 64-deep k block (its operand ring is latency-bound) plus ~2 us of
+  // epilogue; an item ~1 us plus its bytes at ~25 GB/s.  Blocks with one
+  // tile fewer than the busiest ones take that many items each first, so
+  // that the stage's items fill the wave's last partial round of tiles
+  // (stages whose tiles loop over at least 15 k blocks).
+  static int light_items(const Plan& plan, const Stage& S) {
+    if (S.n_tc_items == 0 || S.n_items == S.n_tc_items) return 0;
+    double tile_us = 0.0, item_us = 0.0;
+    int64_t items = 0;
+    for (int i = S.task_begin; i < int(plan.tasks.size()); ++i) {
+      const Task& t = plan.tasks[i];
+      if (t.kind == tkd::T_GEMM_TC) {
+        tile_us = std::max(tile_us, 2.0 + 0.4 * t.kb_split);
+      } else if (t.n_items > 0) {
+        const bool red = t.kind == tkd::T_REDUCE_ROW || t.kind == tkd::T_REDUCE_COL || t.kind == tkd::T_REDUCE_FINAL;
+        const double elems = double(t.numel) / double(t.n_items);
+        const double bytes = elems * 2.0 * (red ? std::max(1, t.chain.n_loads) : 1 + t.chain.n_loads);
+        item_us += double(t.n_items) * (1.0 + bytes / 25e3);
+        items += t.n_items;
+      }
+    }
+    // short tiles (a few k blocks) finish within an item or two of each
+    // other: plain round-robin balances those stages better
+    if (items == 0 || item_us <= 0.0 || tile_us < 8.0) return 0;
+    return int(std::min(64.0, std::floor(tile_us / (item_us / double(items)))));
+  }
+
   // The one 16-bit type of every operand, rounding and output of a GEMM
   // epilogue (with its side output), or 0 if they mix types.  The staged
   // epilogue is compiled per type, so that its conversions carry no
@@ -2184,6 +2213,7 @@ class Planner {
         plan.tasks.push_back(t);
       }
       S.task_end = int(plan.tasks.size());
+      S.light_items = light_items(plan, S);
       if (S.code_lo > S.code_hi) S.code_lo = S.code_hi = 0;
       if (S.ref_lo > S.ref_hi) S.ref_lo = S.ref_hi = 0;
       plan.stages.push_back(S);

@@ -243,6 +243,12 @@ struct Stage {
   int32_t n_tc_items;
   int32_t code_lo, code_hi;  // instructions the stage's tasks use
   int32_t ref_lo, ref_hi;    // operand refs the stage's tasks use
+  // Other items a block with one tensor-core tile fewer than the busiest
+  // blocks takes before the rest are dealt round-robin over all blocks (the
+  // planner's estimate of one tile's time in items of the stage; 0: plain
+  // round-robin after the tiles).
+  int32_t light_items;
+  int32_t pad;
 };
 
 // A stage whose descriptors fit these bounds is copied into shared memory

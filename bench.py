@@ -229,11 +229,15 @@ def batch_steps_for(cfg) -> int:
     return 20 if cfg.flops() > 1e11 else 100
 
 
+# Planner options of every program the bench builds (set from the command line).
+OPTIONS = {}
+
+
 def setup(cfg, device, **options):
     import torch
     from persistent_step_megakernel_gb300.runtime import TrainStep
     prog = S.mlp_step_program(cfg, export="state")
-    step = TrainStep(prog, device.index, **options)
+    step = TrainStep(prog, device.index, **{**OPTIONS, **options})
     ins = device_inputs(cfg, prog, device)
     outs, ws = step.allocate(ins)
     stream = torch.cuda.current_stream(device)
@@ -441,7 +445,7 @@ def stage_profile(cfg, device, warmup=5):
     import torch
     from persistent_step_megakernel_gb300.runtime import TrainStep
     prog = S.mlp_step_program(cfg, export="state")
-    step = TrainStep(prog, device.index, profile=1)
+    step = TrainStep(prog, device.index, profile=1, **OPTIONS)
     ins = device_inputs(cfg, prog, device)
     outs, ws = step.allocate(ins)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
@@ -514,7 +518,11 @@ def main() -> int:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--stage-profile", action="store_true", help="print per-stage timing of one step")
     ap.add_argument("--launches-only", action="store_true", help="W + K launches and nothing else")
+    ap.add_argument("--cta-pairs", type=int, choices=[0, 1], default=None,
+                    help="run the tensor-core GEMMs on pairs of SMs (1) or one SM per tile (0); default: the planner's")
     args = ap.parse_args()
+    if args.cta_pairs is not None:
+        OPTIONS["cta_pairs"] = args.cta_pairs
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

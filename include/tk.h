@@ -57,7 +57,9 @@ typedef enum {
   TK_ERR_CUDA = 5,             /* a CUDA runtime call failed */
   TK_ERR_DEVICE = 6,           /* no usable device (or a plan-only program was run) */
   TK_ERR_BARRIER_TIMEOUT = 7,  /* device status: a grid barrier wait ran out */
-  TK_ERR_PIPELINE_TIMEOUT = 8  /* device status: a tensor-core pipeline wait ran out */
+  TK_ERR_PIPELINE_TIMEOUT = 8, /* device status: a tensor-core pipeline wait ran out */
+  TK_ERR_PAIR_TMEM = 9         /* device status: the two blocks of a pair-tile launch were given
+                                  different tensor-memory addresses (no tile was run) */
 } tk_status;
 
 typedef enum { TK_F32 = 0, TK_F16 = 1, TK_BF16 = 2 } tk_dtype;
@@ -151,6 +153,11 @@ typedef struct {
                                   (0, default: what the SM has left beside the operand ring).
                                   Smaller caps give shallower staging rings; results are
                                   identical (used by tests to reach each staging layout) */
+  int32_t cta_pairs;           /* 1: every tensor-core GEMM runs on pairs of SMs: 256-row tiles,
+                                  one cluster of two blocks per tile, each block staging its 128
+                                  rows of A and half of B's columns, cta_group::2 MMAs (programs
+                                  with no tensor-core GEMM ignore it); 0 (default): one SM per
+                                  128-row tile */
 } tk_options;
 
 /* What the planner decided (codegen.py `GeneratedKernel` counters). */
@@ -173,6 +180,7 @@ typedef struct {
   int32_t chain_tasks;         /* tasks evaluating a generic linear chain (the rest use instructions) */
   int32_t tasks;               /* device tasks (see tk_plan_task) */
   int32_t tma_descriptors;     /* TMA descriptors a launch passes (GEMM operand tiles, epilogue chunks) */
+  int32_t cta_pairs;           /* 1: a pair-tile launch (clusters of two blocks; see tk_options) */
 } tk_plan_stats;
 
 /* One device task of a plan: a scheduled op (with whatever the planner fused

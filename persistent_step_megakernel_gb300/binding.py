@@ -22,7 +22,8 @@ DTYPE = {"float32": 0, "float16": 1, "bfloat16": 2}
 OP_KIND = {"add": 0, "sub": 1, "mul": 2, "div": 3, "neg": 4, "relu": 5, "pow": 6,
            "threshold_backward": 7, "full": 8, "cast": 9, "mm": 10, "addmm": 11, "sum": 12, "mean": 13}
 STATUS = {0: "TK_OK", 1: "TK_ERR_INVALID", 2: "TK_ERR_UNSUPPORTED", 3: "TK_ERR_WORKSPACE", 4: "TK_ERR_ALIAS",
-          5: "TK_ERR_CUDA", 6: "TK_ERR_DEVICE", 7: "TK_ERR_BARRIER_TIMEOUT", 8: "TK_ERR_PIPELINE_TIMEOUT"}
+          5: "TK_ERR_CUDA", 6: "TK_ERR_DEVICE", 7: "TK_ERR_BARRIER_TIMEOUT", 8: "TK_ERR_PIPELINE_TIMEOUT",
+          9: "TK_ERR_PAIR_TMEM"}
 
 
 class tk_tensor_spec(ctypes.Structure):
@@ -55,7 +56,7 @@ class tk_options(ctypes.Structure):
                 ("sm_count", ctypes.c_int32), ("profile", ctypes.c_int32),
                 ("barrier_timeout_s", ctypes.c_double), ("expr_forms", ctypes.c_int32),
                 ("split_k", ctypes.c_int32), ("tile_n", ctypes.c_int32),
-                ("epi_stage_bytes", ctypes.c_int32)]
+                ("epi_stage_bytes", ctypes.c_int32), ("cta_pairs", ctypes.c_int32)]
 
 
 class tk_plan_stats(ctypes.Structure):
@@ -64,7 +65,7 @@ class tk_plan_stats(ctypes.Structure):
         "direct_outputs", "direct_state_commits", "max_work_items", "grid_blocks", "output_copies",
         "split_reductions")] + [("workspace_elements", ctypes.c_int64), ("arena_elements", ctypes.c_int64),
         ("compiled_tasks", ctypes.c_int32), ("chain_tasks", ctypes.c_int32), ("tasks", ctypes.c_int32),
-        ("tma_descriptors", ctypes.c_int32)]
+        ("tma_descriptors", ctypes.c_int32), ("cta_pairs", ctypes.c_int32)]
 
 
 class tk_task_info(ctypes.Structure):

@@ -11,10 +11,13 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-enum Variant { V_PLAIN = 0, V_TC_SMALL = 1, V_TC_LARGE = 2, V_COUNT = 3 };
+enum Variant { V_PLAIN = 0, V_TC_SMALL = 1, V_TC_LARGE = 2, V_TC_PAIR = 3, V_COUNT = 4 };
 
 const void* kernel_of(int v) {
-  return v == V_PLAIN ? tk_kernel_fn_plain() : v == V_TC_SMALL ? tk_kernel_fn_tc_small() : tk_kernel_fn_tc_large();
+  return v == V_PLAIN      ? tk_kernel_fn_plain()
+         : v == V_TC_SMALL ? tk_kernel_fn_tc_small()
+         : v == V_TC_LARGE ? tk_kernel_fn_tc_large()
+                           : tk_kernel_fn_tc_pair();
 }
 
 // Per device and variant: the kernel's static shared memory (read once) and
@@ -67,18 +70,23 @@ cudaError_t launch_tc(const cudaLaunchConfig_t* cfg, const void* fn, const tkd::
 }  // namespace
 
 cudaError_t tk_kernel_launch(const tkd::Params& params, const void* maps, int n_maps, int grid, size_t dyn_smem,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, bool pair) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(tkd::kThreads);
   cfg.dynamicSmemBytes = dyn_smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const int v = !maps ? V_PLAIN : n_maps <= tkd::kSmallMaps ? V_TC_SMALL : V_TC_LARGE;
+  cfg.numAttrs = pair ? 2 : 1;
+  if (pair && (!maps || grid % 2)) return cudaErrorInvalidValue;
+  const int v = !maps ? V_PLAIN : pair ? V_TC_PAIR : n_maps <= tkd::kSmallMaps ? V_TC_SMALL : V_TC_LARGE;
   if (maps && n_maps > tkd::kMaxMaps) return cudaErrorInvalidValue;
   cudaError_t e = set_carveout(v, dyn_smem);
   if (e != cudaSuccess) return e;
@@ -91,16 +99,34 @@ cudaError_t tk_kernel_launch(const tkd::Params& params, const void* maps, int n_
   return launch_tc<tkd::kMaxMaps>(&cfg, kernel_of(v), params, maps, n_maps);
 }
 
+cudaError_t tk_kernel_pair_clusters(int* clusters, size_t dyn_smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(tkd::kThreads);
+  cfg.dynamicSmemBytes = dyn_smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = set_carveout(V_TC_PAIR, dyn_smem);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveClusters(clusters, kernel_of(V_TC_PAIR), &cfg);
+}
+
 // The dynamic shared-memory limit is raised to the largest any program uses,
 // so programs of different sizes can be launched in any order.  Called for
 // every program, with the program's device current.
 cudaError_t tk_kernel_prepare(bool tc, size_t) {
   if (!tc) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kernel_of(V_TC_SMALL), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       tkd::kDynSmemBudget);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(kernel_of(V_TC_LARGE), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              tkd::kDynSmemBudget);
+  for (int v : {V_TC_SMALL, V_TC_LARGE, V_TC_PAIR}) {
+    cudaError_t e = cudaFuncSetAttribute(kernel_of(v), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         tkd::kDynSmemBudget);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t tk_kernel_occupancy(int* blocks_per_sm, bool tc, size_t dyn_smem) {
@@ -108,6 +134,6 @@ cudaError_t tk_kernel_occupancy(int* blocks_per_sm, bool tc, size_t dyn_smem) {
                                                        tkd::kThreads, dyn_smem);
 }
 
-cudaError_t tk_kernel_attributes(cudaFuncAttributes* attr, bool tc) {
-  return cudaFuncGetAttributes(attr, kernel_of(tc ? V_TC_LARGE : V_PLAIN));
+cudaError_t tk_kernel_attributes(cudaFuncAttributes* attr, bool tc, bool pair) {
+  return cudaFuncGetAttributes(attr, kernel_of(!tc ? V_PLAIN : pair ? V_TC_PAIR : V_TC_LARGE));
 }

@@ -1478,6 +1478,7 @@ struct TcState {
   uint32_t acc_full, acc_empty;   // 2 mbarriers each
   uint32_t drain;                 // MMA completion after a failed wait (used once)
   uint32_t tmem;                  // TMEM base address
+  uint32_t acc_cols;              // TMEM columns per accumulator buffer (half the allocation)
   uint32_t stg;                   // shared address of the epilogue staging area
   uint32_t stg_warp_bytes;        // staging bytes per epilogue warp
   uint32_t epi_bar;               // kEpiMaxDepth mbarriers per epilogue warp (staged-epilogue operand loads)
@@ -1534,6 +1535,84 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
+}
+
+// ------------------------------------------------- pairs of SMs (clusters of 2)
+//
+// A pair-tile launch runs in clusters of two blocks on two SMs.  The even
+// block of a pair (its leader) issues the pair's MMAs (cta_group::2): A rows
+// 0-127 of a 256-row tile come from the leader's shared memory and rows
+// 128-255 from the peer's, at the same offset; B's columns are split in halves
+// the same way; each block's TMEM holds the accumulator rows of its half.
+
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The shared::cluster address of `addr` (a shared::cta address of this block)
+// in block `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier of another block of the cluster (cluster-scope release).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// All threads of both blocks of the pair meet (cluster-scope release/acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// TMA loads into this block's shared memory whose completion is counted on an
+// mbarrier of either block of the pair (cluster_bar: a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(cluster_bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                                 uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(cluster_bar)
+      : "memory");
+}
+
+// Bounded wait with cluster-scope acquire (for phases completed by arrivals
+// from the other block of the pair).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, long long timeout_ns) {
+  for (int i = 0; i < 256; ++i)
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+  const long long t0 = global_ns();
+  while (!mbar_try_wait_cluster(bar, parity))
+    if (global_ns() - t0 > timeout_ns) return false;
+  return true;
 }
 
 // One contiguous global -> shared bulk copy (both 16-byte aligned, size a
@@ -1755,6 +1834,25 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// The pair forms (every tcgen05 operation of a pair-tile launch uses
+// cta_group::2): one MMA over both blocks' operands, and commits that arrive
+// on the mbarrier at offset `bar` in the blocks of `mask` or in this block.
+__device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_pair_mc(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+               ::"r"(bar), "h"(mask)
+               : "memory");
+}
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -1792,11 +1890,14 @@ struct TileItem {
 };
 
 // Walk this block's tensor-core items of a stage in order (all roles use the
-// same sequence).  fn(task, item) returns false to stop.
-template <typename F>
+// same sequence; in a pair-tile launch both blocks of a pair walk the pair's
+// 256-row tiles, m0 being the tile's first row).  fn(task, item) returns
+// false to stop.
+template <bool PAIR, typename F>
 __device__ __forceinline__ void for_my_tiles(const Ctx& c, const Stage& st, F&& fn) {
   int ti = st.task_begin, base = 0;
-  for (int g = blockIdx.x; g < st.n_tc_items; g += gridDim.x) {
+  const int g0 = PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x), step = PAIR ? int(gridDim.x >> 1) : int(gridDim.x);
+  for (int g = g0; g < st.n_tc_items; g += step) {
     while (g >= base + c.tasks[ti].n_items) {
       base += c.tasks[ti].n_items;
       ++ti;
@@ -1804,7 +1905,7 @@ __device__ __forceinline__ void for_my_tiles(const Ctx& c, const Stage& st, F&& 
     const Task& t = c.tasks[ti];
     const int item = g - base, tile = item / t.k_splits, split = item - tile * t.k_splits;
     TileItem it;
-    it.m0 = int64_t(tile / t.tiles_n) * kTileM;
+    it.m0 = int64_t(tile / t.tiles_n) * (PAIR ? 2 * kTileM : kTileM);
     it.n0 = int64_t(tile % t.tiles_n) * t.tile_n;
     it.split = split;
     it.kb0 = split * t.kb_split;
@@ -2287,67 +2388,104 @@ __device__ __forceinline__ void tc_epilogue_tile(const Ctx& c, const Task& t, in
 // waits, again with the time limit, for that work to land before returning,
 // so that nothing arrives in shared memory or TMEM after the block has freed
 // them and exited.
+template <bool PAIR>
 __device__ __noinline__ uint64_t tc_producer(const Ctx c, const Stage st, const CUtensorMap* maps, const TcState ts,
                                              uint32_t p_it) {
+  constexpr uint32_t NS = PAIR ? kPairStages : kStages;
   bool ok = true;
   const uint32_t p_it0 = p_it;
+  // pair: this block loads its 128 rows of A and its half of B's columns;
+  // both blocks' copies complete on the leader's "full" mbarrier
+  const uint32_t rank = PAIR ? cluster_rank() & 1u : 0u;
+  const uint32_t leader = PAIR ? cluster_rank() & ~1u : 0u;
   asm volatile("fence.proxy.async.global;" ::: "memory");
-  for_my_tiles(c, st, [&](const Task& t, const TileItem& it) {
-    const uint32_t bytes = uint32_t(kStageBytesA + t.tile_n * kTileK * 2);
-    const int tile_n = t.tile_n, tma_a = t.tma_a, tma_b = t.tma_b;
+  for_my_tiles<PAIR>(c, st, [&](const Task& t, const TileItem& it) {
+    const int half = PAIR ? t.tile_n / 2 : t.tile_n;  // B columns this block loads
+    const uint32_t bytes = uint32_t(kStageBytesA + half * kTileK * 2);
+    const int tma_a = t.tma_a, tma_b = t.tma_b;
     const int a_mn = t.a_mn_major, b_mn = t.b_mn_major;
-    const int64_t m0 = it.m0, n0 = it.n0;
+    const int64_t m0 = it.m0 + int64_t(rank) * kTileM, n0 = it.n0 + int64_t(rank) * half;
     for (int kb = it.kb0; kb < it.kb1; ++kb) {
-      const uint32_t slot = p_it % kStages, ph = ((p_it / kStages) & 1u) ^ 1u;
+      const uint32_t slot = p_it % NS, ph = ((p_it / NS) & 1u) ^ 1u;
       if (!mbar_wait(ts.empty + 8 * slot, ph, c.timeout_ns)) return ok = false;
       const uint32_t full = ts.full + 8 * slot;
-      mbar_expect_tx(full, bytes);
       const uint32_t a_dst = ts.ring + slot * ts.slot_bytes, b_dst = a_dst + kStageBytesA;
       const int k0 = kb * kTileK;
-      if (!a_mn) {
-        tma_load_2d(a_dst, &maps[tma_a], k0, int(m0), full);
-      } else if (a_mn == 2) {
-        tma_load_3d(a_dst, &maps[tma_a], 0, k0, int(m0 >> 6), full);
+      if constexpr (PAIR) {
+        if (rank == 0) mbar_expect_tx(full, 2 * bytes);  // the leader counts both blocks' bytes
+        const uint32_t bar = cluster_addr(full, leader);
+        if (!a_mn) {
+          tma_load_2d_pair(a_dst, &maps[tma_a], k0, int(m0), bar);
+        } else if (a_mn == 2) {
+          tma_load_3d_pair(a_dst, &maps[tma_a], 0, k0, int(m0 >> 6), bar);
+        } else {
+          tma_load_2d_pair(a_dst, &maps[tma_a], int(m0), k0, bar);
+          tma_load_2d_pair(a_dst + 8192, &maps[tma_a], int(m0) + 64, k0, bar);
+        }
+        if (!b_mn) {
+          tma_load_2d_pair(b_dst, &maps[tma_b], k0, int(n0), bar);
+        } else if (b_mn == 2) {
+          tma_load_3d_pair(b_dst, &maps[tma_b], 0, k0, int(n0 >> 6), bar);
+        } else {
+          for (int j = 0; j < half / 64; ++j) tma_load_2d_pair(b_dst + 8192 * j, &maps[tma_b], int(n0) + 64 * j, k0, bar);
+        }
       } else {
-        tma_load_2d(a_dst, &maps[tma_a], int(m0), k0, full);
-        tma_load_2d(a_dst + 8192, &maps[tma_a], int(m0) + 64, k0, full);
-      }
-      if (!b_mn) {
-        tma_load_2d(b_dst, &maps[tma_b], k0, int(n0), full);
-      } else if (b_mn == 2) {
-        tma_load_3d(b_dst, &maps[tma_b], 0, k0, int(n0 >> 6), full);
-      } else {
-        for (int j = 0; j < tile_n / 64; ++j) tma_load_2d(b_dst + 8192 * j, &maps[tma_b], int(n0) + 64 * j, k0, full);
+        mbar_expect_tx(full, bytes);
+        if (!a_mn) {
+          tma_load_2d(a_dst, &maps[tma_a], k0, int(m0), full);
+        } else if (a_mn == 2) {
+          tma_load_3d(a_dst, &maps[tma_a], 0, k0, int(m0 >> 6), full);
+        } else {
+          tma_load_2d(a_dst, &maps[tma_a], int(m0), k0, full);
+          tma_load_2d(a_dst + 8192, &maps[tma_a], int(m0) + 64, k0, full);
+        }
+        if (!b_mn) {
+          tma_load_2d(b_dst, &maps[tma_b], k0, int(n0), full);
+        } else if (b_mn == 2) {
+          tma_load_3d(b_dst, &maps[tma_b], 0, k0, int(n0 >> 6), full);
+        } else {
+          for (int j = 0; j < half / 64; ++j) tma_load_2d(b_dst + 8192 * j, &maps[tma_b], int(n0) + 64 * j, k0, full);
+        }
       }
       ++p_it;
     }
     return true;
   });
-  if (!ok) {
-    // the copies of the last (up to) kStages slots this stage armed: each
+  if (!ok && rank == 0) {
+    // the copies of the last (up to) NS slots this stage armed: each
     // completes its slot's current "full" phase (a slot is re-armed only
     // after its previous phase was consumed, so that phase is still the one
-    // with this parity)
-    const uint32_t first = p_it - min(p_it - p_it0, uint32_t(kStages));
-    for (uint32_t i = first; i < p_it; ++i) mbar_wait(ts.full + 8 * (i % kStages), (i / kStages) & 1u, c.timeout_ns);
+    // with this parity; in a pair the leader's phases count the peer's
+    // copies too)
+    const uint32_t first = p_it - min(p_it - p_it0, NS);
+    for (uint32_t i = first; i < p_it; ++i) mbar_wait(ts.full + 8 * (i % NS), (i / NS) & 1u, c.timeout_ns);
   }
   return (uint64_t(ok) << 32) | p_it;
 }
 
+template <bool PAIR>
 __device__ __noinline__ uint64_t tc_mma(const Ctx c, const Stage st, const TcState ts, uint32_t m_it,
                                         uint32_t* m_tile_io, long long* prof) {
+  constexpr uint32_t NS = PAIR ? kPairStages : kStages;
+  // pair: the leader issues the pair's MMAs; its commits arrive on the
+  // "empty" and accumulator mbarriers of both blocks
+  if (PAIR && (cluster_rank() & 1u)) return uint64_t(1) << 32 | m_it;
+  const uint16_t pair_mask = PAIR ? uint16_t(3u << (cluster_rank() & ~1u)) : uint16_t(0);
   bool ok = true;
   bool first = true;
   uint32_t m_tile = *m_tile_io;
-  for_my_tiles(c, st, [&](const Task& t, const TileItem& it) {
+  for_my_tiles<PAIR>(c, st, [&](const Task& t, const TileItem& it) {
     const uint32_t acc = m_tile & 1u, ph = ((m_tile >> 1) & 1u) ^ 1u;
-    if (!mbar_wait(ts.acc_empty + 8 * acc, ph, c.timeout_ns)) return ok = false;
+    // pair: the epilogue warps of both blocks release the accumulator
+    const bool freed = PAIR ? mbar_wait_cluster(ts.acc_empty + 8 * acc, ph, c.timeout_ns)
+                            : mbar_wait(ts.acc_empty + 8 * acc, ph, c.timeout_ns);
+    if (!freed) return ok = false;
     tc_fence_after();
-    const uint32_t d_tmem = ts.tmem + acc * kMaxTileN;
+    const uint32_t d_tmem = ts.tmem + acc * ts.acc_cols;
     const uint32_t idesc = t.idesc;
     const bool a_mn = t.a_mn_major, b_mn = t.b_mn_major;
     for (int kb = it.kb0; kb < it.kb1; ++kb) {
-      const uint32_t slot = m_it % kStages, fph = (m_it / kStages) & 1u;
+      const uint32_t slot = m_it % NS, fph = (m_it / NS) & 1u;
       if (!mbar_wait(ts.full + 8 * slot, fph, c.timeout_ns)) return ok = false;
       if (prof && first) prof[3] = global_ns();
       first = false;
@@ -2357,24 +2495,37 @@ __device__ __noinline__ uint64_t tc_mma(const Ctx c, const Stage st, const TcSta
       for (int k = 0; k < kTileK / 16; ++k) {
         const uint64_t ad = a_mn ? smem_desc(a_base + 2048 * k, 8192, 1024) : smem_desc(a_base + 32 * k, 16, 1024);
         const uint64_t bd = b_mn ? smem_desc(b_base + 2048 * k, 8192, 1024) : smem_desc(b_base + 32 * k, 16, 1024);
-        umma_f16(d_tmem, ad, bd, idesc, uint32_t((kb - it.kb0) | k));
+        if constexpr (PAIR)
+          umma_f16_pair(d_tmem, ad, bd, idesc, uint32_t((kb - it.kb0) | k));
+        else
+          umma_f16(d_tmem, ad, bd, idesc, uint32_t((kb - it.kb0) | k));
       }
-      umma_commit(ts.empty + 8 * slot);
+      if constexpr (PAIR)
+        umma_commit_pair_mc(ts.empty + 8 * slot, pair_mask);
+      else
+        umma_commit(ts.empty + 8 * slot);
       ++m_it;
     }
-    umma_commit(ts.acc_full + 8 * acc);
+    if constexpr (PAIR)
+      umma_commit_pair_mc(ts.acc_full + 8 * acc, pair_mask);
+    else
+      umma_commit(ts.acc_full + 8 * acc);
     ++m_tile;
     return true;
   });
   if (!ok) {
     // every MMA this thread issued completes before the drain barrier's phase
-    umma_commit(ts.drain);
+    if constexpr (PAIR)
+      umma_commit_pair(ts.drain);
+    else
+      umma_commit(ts.drain);
     mbar_wait(ts.drain, 0, c.timeout_ns);
   }
   *m_tile_io = m_tile;
   return (uint64_t(ok) << 32) | m_it;
 }
 
+template <bool PAIR>
 __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const TcState ts, uint32_t e_tile,
                                              long long* prof, EpiRing* er) {
   bool ok = true;
@@ -2382,8 +2533,12 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
   const int lane = threadIdx.x & 31;
   const uint32_t ew = uint32_t(threadIdx.x >> 5) - 4;
   const uint32_t stg = ts.stg + ew * ts.stg_warp_bytes, ebar = ts.epi_bar + 8 * kEpiMaxDepth * ew;
-  for_my_tiles(c, st, [&](const Task& t, const TileItem& it) {
-    const int64_t m0 = it.m0, n0 = it.n0;
+  // pair: this block's accumulator rows are the tile's half `rank`; the
+  // accumulator is released on the leader's mbarrier
+  const uint32_t rank = PAIR ? cluster_rank() & 1u : 0u;
+  const uint32_t acc_empty_leader = PAIR ? cluster_addr(ts.acc_empty, cluster_rank() & ~1u) : 0u;
+  for_my_tiles<PAIR>(c, st, [&](const Task& t, const TileItem& it) {
+    const int64_t m0 = it.m0 + int64_t(rank) * kTileM, n0 = it.n0;
     const uint32_t acc = e_tile & 1u, ph = (e_tile >> 1) & 1u;
     long long* stamp = prof && first && threadIdx.x == 128 ? prof + 5 : nullptr;
     first = false;
@@ -2391,20 +2546,25 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
       if (!mbar_wait(ts.acc_full + 8 * acc, ph, c.timeout_ns)) return ok = false;
       if (stamp) *stamp = global_ns();
       tc_fence_after();
-      tc_epilogue_partial(c, t, m0, n0, it.split, ts.tmem + acc * kMaxTileN);
+      tc_epilogue_partial(c, t, m0, n0, it.split, ts.tmem + acc * ts.acc_cols);
     } else if (t.epi_stage) {
-      if (!tc_epilogue_staged_any(c, t, int(&t - c.tasks), m0, n0, ts.tmem + acc * kMaxTileN, stg,
+      if (!tc_epilogue_staged_any(c, t, int(&t - c.tasks), m0, n0, ts.tmem + acc * ts.acc_cols, stg,
                                   ts.acc_full + 8 * acc, ph, stamp, ts.maps, ebar, er))
         return ok = false;
     } else {
       if (!mbar_wait(ts.acc_full + 8 * acc, ph, c.timeout_ns)) return ok = false;
       if (stamp) *stamp = global_ns();
       tc_fence_after();
-      tc_epilogue_tile(c, t, m0, n0, ts.tmem + acc * kMaxTileN);
+      tc_epilogue_tile(c, t, m0, n0, ts.tmem + acc * ts.acc_cols);
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(ts.acc_empty + 8 * acc);
+    if (lane == 0) {
+      if constexpr (PAIR)
+        mbar_arrive_cluster(acc_empty_leader + 8 * acc);
+      else
+        mbar_arrive(ts.acc_empty + 8 * acc);
+    }
     ++e_tile;
     return true;
   });
@@ -2416,25 +2576,26 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
 }
 
 // Run this block's tensor-core tiles of one stage; false after a wait timed out.
+template <bool PAIR>
 __device__ bool run_tc_phase(const Ctx& c, const Stage& st, const CUtensorMap* maps, TcState& ts, int stage,
                              int* s_flag, long long* prof) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   bool ok = true;
   if (warp == 0 && lane == 0) {
-    const uint64_t r = tc_producer(c, st, maps, ts, ts.p_it);
+    const uint64_t r = tc_producer<PAIR>(c, st, maps, ts, ts.p_it);
     ts.p_it = uint32_t(r);
     ok = (r >> 32) != 0;
     if (prof) prof[2] = global_ns();
   } else if (warp == 1 && lane == 0) {
     uint32_t m_tile = ts.m_tile;
-    const uint64_t r = tc_mma(c, st, ts, ts.m_it, &m_tile, prof);
+    const uint64_t r = tc_mma<PAIR>(c, st, ts, ts.m_it, &m_tile, prof);
     ts.m_it = uint32_t(r);
     ts.m_tile = m_tile;
     ok = (r >> 32) != 0;
     if (prof) prof[4] = global_ns();
   } else if (warp >= 4) {
     EpiRing er = ts.er;
-    const uint64_t r = tc_epilogue(c, st, ts, ts.e_tile, prof, &er);
+    const uint64_t r = tc_epilogue<PAIR>(c, st, ts, ts.e_tile, prof, &er);
     ts.e_tile = uint32_t(r);
     ts.er = er;
     ok = (r >> 32) != 0;
@@ -2530,14 +2691,18 @@ __device__ __forceinline__ void stage_in(const Program* prog, int s, Stage* s_st
     copy_words(s_refs, prog->refs + st.ref_lo, (st.ref_hi - st.ref_lo) * int(sizeof(Ref)), tid, n);
 }
 
+// PAIR: a pair-tile launch (clusters of two blocks; every tensor-core GEMM on
+// 256-row tiles of cta_group::2 MMAs, kPairStages ring slots).
+template <bool PAIR>
 __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorMap* maps) {
+  constexpr int NS = PAIR ? kPairStages : kStages;
   __shared__ void* s_io[2 * kMaxIO];
   __shared__ Task s_tasks[kStageTasks];
   __shared__ __align__(16) Instr s_code[kStageCode];
   __shared__ __align__(16) Ref s_refs[kStageRefs];
   __shared__ Stage s_stage;
   __shared__ Prep s_prep[kThreads / 32];
-  __shared__ __align__(8) uint64_t s_bar[2 * kStages + 5];
+  __shared__ __align__(8) uint64_t s_bar[2 * NS + 5];
   __shared__ __align__(8) uint64_t s_epi_bar[4 * kEpiMaxDepth];
   __shared__ __align__(8) uint64_t s_bulk_bar[kBulkMaxSlots];
   __shared__ uint32_t s_bulk_it;
@@ -2547,6 +2712,9 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   __shared__ int s_flag;
   extern __shared__ __align__(1024) unsigned char s_dyn[];
   const bool tc = maps != nullptr;
+  // pair: the launch must have formed clusters of two (else no cluster or
+  // pair operation runs and the kernel reports TK_ERR_PAIR_TMEM)
+  const bool paired = PAIR && cluster_size() == 2;
   // scratch for reductions and CUDA-core GEMMs at the start of the dynamic
   // region; in a tensor-core launch it overlays the (then idle) ring
   float* s_work = reinterpret_cast<float*>(s_dyn + ((1024u - (smem_u32(s_dyn) & 1023u)) & 1023u));
@@ -2560,24 +2728,24 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   if (tc) {
     ts.ring = (smem_u32(s_dyn) + 1023u) & ~1023u;
     ts.slot_bytes = uint32_t(p.ring_stage_bytes);
-    ts.stg = ts.ring + uint32_t(kStages) * ts.slot_bytes;
+    ts.stg = ts.ring + uint32_t(NS) * ts.slot_bytes;
     ts.stg_warp_bytes = uint32_t(p.epi_warp_bytes);
     ts.full = smem_u32(&s_bar[0]);
-    ts.empty = smem_u32(&s_bar[kStages]);
-    ts.acc_full = smem_u32(&s_bar[2 * kStages]);
-    ts.acc_empty = smem_u32(&s_bar[2 * kStages + 2]);
-    ts.drain = smem_u32(&s_bar[2 * kStages + 4]);
+    ts.empty = smem_u32(&s_bar[NS]);
+    ts.acc_full = smem_u32(&s_bar[2 * NS]);
+    ts.acc_empty = smem_u32(&s_bar[2 * NS + 2]);
+    ts.drain = smem_u32(&s_bar[2 * NS + 4]);
     ts.epi_bar = smem_u32(&s_epi_bar[0]);
     ts.maps = maps;
     ts.er.task = -1;
     if (threadIdx.x == 0) {
-      for (int i = 0; i < kStages; ++i) {
+      for (int i = 0; i < NS; ++i) {
         mbar_init(ts.full + 8 * i, 1);
         mbar_init(ts.empty + 8 * i, 1);
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(ts.acc_full + 8 * i, 1);
-        mbar_init(ts.acc_empty + 8 * i, 4);
+        mbar_init(ts.acc_empty + 8 * i, PAIR ? 8 : 4);  // pair: both blocks' epilogue warps (leader's copy)
       }
       mbar_init(ts.drain, 1);
       for (int i = 0; i < 4 * kEpiMaxDepth; ++i) mbar_init(ts.epi_bar + 8 * i, 1);
@@ -2593,17 +2761,39 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     if (threadIdx.x == 0)
       for (int i = 0; i < p.n_maps; ++i)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps[i])) : "memory");
-    if (warp == 1) {
-      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                   "r"(kTmemCols));
-      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    if (warp == 1 && (!PAIR || paired)) {
+      // pair: one warp of each block of the pair allocates, together
+      if constexpr (PAIR) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(p.tmem_cols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+      } else {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(p.tmem_cols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+      }
     }
     tc_fence_before();
   }
   __syncthreads();
+  // pair: neither block signals the other's mbarriers before both have
+  // initialised them
+  if (paired) cluster_sync();
+  bool pair_ok = !PAIR || paired;
   if (tc) {
     tc_fence_after();
     ts.tmem = s_tmem;
+    ts.acc_cols = uint32_t(p.tmem_cols) / 2;
+    // pair: an MMA of the pair writes the same TMEM columns in both blocks,
+    // so both must have been given the same address
+    if (paired) {
+      uint32_t other;
+      asm volatile("ld.shared::cluster.u32 %0, [%1];"
+                   : "=r"(other)
+                   : "r"(cluster_addr(smem_u32(&s_tmem), cluster_rank() ^ 1u))
+                   : "memory");
+      pair_ok = other == ts.tmem;
+    }
   }
   if (warp == 2) {
     // L2 prefetch of the op table and the inputs, spread over blocks and lanes
@@ -2620,14 +2810,15 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   if (tc) {
     c.bulk = ts.ring + kBulkOffset;
     c.bulk_bar = smem_u32(&s_bulk_bar[0]);
-    c.bulk_slots = max(0, min(kBulkMaxSlots, (kStages * p.ring_stage_bytes - kBulkOffset) / kBulkSlotBytes));
+    c.bulk_slots = max(0, min(kBulkMaxSlots, (NS * p.ring_stage_bytes - kBulkOffset) / kBulkSlotBytes));
     c.bulk_it = &s_bulk_it;
     c.col_bar = smem_u32(&s_col_bar[0]);
     c.col_it = &s_col_it;
   }
   long long* prof = p.prof ? p.prof + kProfStamps * int64_t(blockIdx.x) : nullptr;
   const int64_t prof_step = kProfStamps * int64_t(gridDim.x);
-  const int n_stages = prog->n_stages;
+  if (!pair_ok && threadIdx.x == 0) record_failure(c, TK_ERR_PAIR_TMEM, 0);
+  const int n_stages = pair_ok ? prog->n_stages : 0;
   if (prof) {
     // stamps a stage may leave unwritten read as 0
     if (threadIdx.x == 0) {
@@ -2644,7 +2835,8 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     c.tasks = st.task_end - st.task_begin <= kStageTasks ? s_tasks - st.task_begin : prog->tasks;
     c.code = st.code_hi - st.code_lo <= kStageCode ? s_code - st.code_lo : prog->code;
     c.refs = st.ref_hi - st.ref_lo <= kStageRefs ? s_refs - st.ref_lo : prog->refs;
-    if (tc && st.n_tc_items > 0 && !run_tc_phase(c, st, maps, ts, s, &s_flag, prof ? prof + s * prof_step : nullptr))
+    if (tc && st.n_tc_items > 0 &&
+        !run_tc_phase<PAIR>(c, st, maps, ts, s, &s_flag, prof ? prof + s * prof_step : nullptr))
       break;
     // the stage's other items after its tiles: blocks with one tile fewer
     // than the busiest (r = tiles mod grid of them have one more) first take
@@ -2683,9 +2875,16 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   if (tc) {
     tc_fence_before();
     __syncthreads();
+    // pair: no block leaves while the other may still signal its mbarriers;
+    // both free the TMEM together
+    if (paired) cluster_sync();
     tc_fence_after();
-    if (warp == 1)
-      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(ts.tmem), "r"(kTmemCols));
+    if (warp == 1 && (!PAIR || paired)) {
+      if constexpr (PAIR)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(ts.tmem), "r"(p.tmem_cols));
+      else
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(ts.tmem), "r"(p.tmem_cols));
+    }
   }
 }
 

@@ -129,7 +129,8 @@ float f32(double v) { return static_cast<float>(v); }
 
 class Planner {
  public:
-  Planner(const tk_program_desc& d, const tk_options& o, int sms) : opt_(o), sms_(std::max(sms, 1)) {
+  Planner(const tk_program_desc& d, const tk_options& o, int sms)
+      : opt_(o), sms_(std::max(sms, 1)), pair_(o.cta_pairs != 0 && sms >= 2) {
     read_desc(d);
   }
 
@@ -149,6 +150,7 @@ class Planner {
  private:
   tk_options opt_;
   int sms_;
+  bool pair_;  // pair tiles: every tensor-core GEMM on 256-row tiles of a pair of SMs
   std::vector<OpInfo> ops_;
   std::vector<tk_tensor_spec> inputs_, outputs_;
   std::map<int, int> inplace_;  // output slot -> input index
@@ -1598,18 +1600,23 @@ class Planner {
     const int64_t M = t.m, N = t.n, K = t.k;
     if (M < 1 || N < 1 || K < 1) return false;
     if (plan.tma.size() + 2 > size_t(tkd::kMaxMaps)) return false;  // (a bound: equal maps are shared)
-    // widest N tile that still spreads the tiles over the SMs (or the forced width)
-    int bn = 64;
+    // widest N tile that still spreads the tiles over the SMs (or the forced
+    // width); a pair-tile launch deals 256-row tiles to pairs of SMs
+    const int64_t tm = pair_ ? 2 * tkd::kTileM : tkd::kTileM, units = pair_ ? sms_ / 2 : sms_;
+    int bn = pair_ ? 128 : 64;
     for (int cand : {256, 128}) {
-      if (ceil_div(M, tkd::kTileM) * ceil_div(N, cand) >= (cand == 256 ? sms_ : sms_ / 2)) {
+      if (ceil_div(M, tm) * ceil_div(N, cand) >= (cand == 256 ? units : units / 2)) {
         bn = cand;
         break;
       }
     }
-    if (opt_.tile_n > 0) bn = opt_.tile_n;
+    if (opt_.tile_n > 0) bn = pair_ ? std::max(opt_.tile_n, 128) : opt_.tile_n;
+    // each block of a pair stages half of B's columns
+    const int bdiv = pair_ ? 2 : 1;
     TmaOperand ta, tb;
     int a_mn = 0, b_mn = 0;
-    if (!tma_operand(A, true, tkd::kTileM, &ta, &a_mn) || !tma_operand(B, false, bn == 224 ? 256 : bn, &tb, &b_mn))
+    if (!tma_operand(A, true, tkd::kTileM, &ta, &a_mn) ||
+        !tma_operand(B, false, (bn == 224 ? 256 : bn) / bdiv, &tb, &b_mn))
       return false;
     // A K-major B tile may also be 224 wide (seven 32-column chunks; MN-major
     // B tiles load whole 64-wide slabs).  Where the 256-wide tiles leave a
@@ -1618,18 +1625,18 @@ class Planner {
     // take 512 tiles = 3.4 waves at 256, 608 = 4 waves at 224.
     if (opt_.tile_n == 0 && bn == 256 && b_mn == 0) {
       auto cost = [&](int w) {
-        return ceil_div(ceil_div(M, tkd::kTileM) * ceil_div(N, w), sms_) * (tkd::kStageBytesA + w * tkd::kTileK * 2);
+        return ceil_div(ceil_div(M, tm) * ceil_div(N, w), units) * (tkd::kStageBytesA + w / bdiv * tkd::kTileK * 2);
       };
       if (cost(224) < cost(256)) bn = 224;
     }
     if (bn == 224 && b_mn != 0) bn = 256;
-    if (bn == 224 && !tma_operand(B, false, bn, &tb, &b_mn)) return false;
+    if (bn == 224 && !tma_operand(B, false, bn / bdiv, &tb, &b_mn)) return false;
     t.kind = tkd::T_GEMM_TC;
-    t.tile_m = tkd::kTileM;
+    t.tile_m = int(tm);
     t.tile_n = bn;
     t.tiles_n = int(ceil_div(N, bn));
     t.k_blocks = int(ceil_div(K, tkd::kTileK));
-    t.n_items = int(ceil_div(M, tkd::kTileM) * t.tiles_n);
+    t.n_items = int(ceil_div(M, tm) * t.tiles_n);
     t.a_mn_major = a_mn;
     t.b_mn_major = b_mn;
     t.tma_a = map_index(plan, ta);
@@ -1638,12 +1645,12 @@ class Planner {
     // 0 f16, 1 bf16), A/B MN-major (15, 16), N >> 3 (17-22), M >> 4 (24-28)
     uint32_t ab = A.dtype == TK_BF16 ? 1u : 0u;
     t.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (uint32_t(a_mn != 0) << 15) | (uint32_t(b_mn != 0) << 16) |
-              (uint32_t(bn >> 3) << 17) | (uint32_t(tkd::kTileM >> 4) << 24);
+              (uint32_t(bn >> 3) << 17) | (uint32_t(tm >> 4) << 24);
     // Split-K when the tiles leave most SMs idle and each tile has a long K
     // loop (at least 8 k blocks per split).
     t.k_splits = 1;
     t.kb_split = t.k_blocks;
-    if (opt_.split_k && 2 * int64_t(t.n_items) <= sms_ && t.k_blocks >= 16 && N % 8 == 0) {
+    if (opt_.split_k && !pair_ && 2 * int64_t(t.n_items) <= sms_ && t.k_blocks >= 16 && N % 8 == 0) {
       const int splits = int(std::min<int64_t>({int64_t(t.k_blocks / 8), int64_t(sms_ / t.n_items), 8}));
       if (splits >= 2) {
         t.kb_split = int(ceil_div(t.k_blocks, splits));
@@ -2228,8 +2235,12 @@ class Planner {
       if (t.kind == tkd::T_GEMM_TC) max_bn = std::max(max_bn, t.tile_n);
     // Ring slots sized for the widest tile: smaller rings leave more of the
     // SM's unified L1/shared memory to the L1 cache.
-    plan.ring_stage_bytes = tkd::kStageBytesA + max_bn * tkd::kTileK * 2;
-    const size_t ring = 1024 + size_t(tkd::kStages) * plan.ring_stage_bytes;
+    // (a pair-tile launch stages half of each B tile per block)
+    plan.pair = pair_ && tc_ops > 0;
+    plan.tmem_cols = 32;
+    while (plan.tmem_cols < 2 * max_bn) plan.tmem_cols *= 2;
+    plan.ring_stage_bytes = tkd::kStageBytesA + (plan.pair ? max_bn / 2 : max_bn) * tkd::kTileK * 2;
+    const size_t ring = 1024 + size_t(plan.pair ? tkd::kPairStages : tkd::kStages) * plan.ring_stage_bytes;
     // every staged task may use the staging bytes left beside the ring
     const int avail = ring < size_t(tkd::kDynSmemBudget) ? int((size_t(tkd::kDynSmemBudget) - ring) / 4) : 0;
     for (auto& t : plan.tasks) {
@@ -2258,6 +2269,7 @@ class Planner {
     st.inlined_ops = int(inline_.size());
     st.fused_epilogues = int(fused_.size());
     st.tensor_core_ops = tc_ops;
+    st.cta_pairs = plan.pair ? 1 : 0;
     st.stages = int(plan.stages.size());
     st.grid_barriers = st.stages - 1;
     st.direct_outputs = int(binding_.size());

@@ -233,6 +233,7 @@ tk_status tk_program_create(const tk_program_desc* desc, const tk_options* opt_i
   if (opt.tile_n != 0 && opt.tile_n != 64 && opt.tile_n != 128 && opt.tile_n != 224 && opt.tile_n != 256)
     return fail(TK_ERR_INVALID, "tile_n must be 0, 64, 128, 224 or 256");
   if (opt.epi_stage_bytes < 0) return fail(TK_ERR_INVALID, "epi_stage_bytes must be >= 0");
+  if (opt.cta_pairs != 0 && opt.cta_pairs != 1) return fail(TK_ERR_INVALID, "cta_pairs must be 0 or 1");
 
   int sms = opt.sm_count > 0 ? opt.sm_count : 152;
   if (device >= 0) {
@@ -287,6 +288,23 @@ tk_status tk_program_create(const tk_program_desc* desc, const tk_options* opt_i
   int64_t grid = int64_t(sms) * std::min(occupancy, opt.blocks_per_sm);
   grid = std::min<int64_t>(grid, p->plan.max_items);
   if (opt.max_blocks > 0) grid = std::min<int64_t>(grid, opt.max_blocks);
+  if (p->plan.pair) {
+    // one block per SM in clusters of two: an even grid of resident clusters
+    int clusters = int(sms / 2);
+    if (device >= 0) {
+      DeviceGuard g(device);
+      cudaError_t e = tk_kernel_pair_clusters(&clusters, p->dyn_smem);
+      if (e != cudaSuccess) {
+        tk_program_destroy(p);
+        return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+      }
+    }
+    grid = std::min<int64_t>({int64_t(sms), grid + (grid & 1), 2 * int64_t(clusters)}) & ~int64_t(1);
+    if (grid < 2) {
+      tk_program_destroy(p);
+      return fail(TK_ERR_DEVICE, "no two-block cluster fits on the device");
+    }
+  }
   p->grid = int(std::max<int64_t>(grid, 1));
   p->plan.stats.grid_blocks = p->grid;
   if (opt.profile) {
@@ -379,6 +397,7 @@ tk_status tk_run(tk_program* p, const void* const* inputs, int32_t n_inputs, voi
   prm.timeout_ns = static_cast<long long>(p->opt.barrier_timeout_s * 1e9);
   prm.prof = p->prof_offset >= 0 ? reinterpret_cast<long long*>(ws + p->prof_offset) : nullptr;
   prm.ring_stage_bytes = pl.ring_stage_bytes;
+  prm.tmem_cols = pl.tmem_cols;
   prm.epi_warp_bytes = pl.epi_warp_bytes;
   prm.n_in = n_inputs;
   prm.n_out = n_outputs;
@@ -393,7 +412,7 @@ tk_status tk_run(tk_program* p, const void* const* inputs, int32_t n_inputs, voi
     prm.n_maps = int(p->maps.size());
   }
   cudaError_t e = tk_kernel_launch(prm, maps, int(p->maps.size()), p->grid, p->dyn_smem,
-                                   static_cast<cudaStream_t>(stream));
+                                   static_cast<cudaStream_t>(stream), p->plan.pair);
   if (e != cudaSuccess) return cuda_fail(e, "cooperative launch");
   return TK_OK;
 }
@@ -417,7 +436,7 @@ tk_status tk_resource_usage(const tk_program* p, int64_t out[4]) {
   if (p->device < 0) return fail(TK_ERR_DEVICE, "plan-only program (created with device -1)");
   DeviceGuard g(p->device);
   cudaFuncAttributes a;
-  cudaError_t e = tk_kernel_attributes(&a, p->plan.uses_tc);
+  cudaError_t e = tk_kernel_attributes(&a, p->plan.uses_tc, p->plan.pair);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes");
   int occ = 0;
   e = tk_kernel_occupancy(&occ, p->plan.uses_tc, p->dyn_smem);

@@ -27,6 +27,10 @@ constexpr int kTileM = 128;
 constexpr int kTileK = 64;
 constexpr int kMaxTileN = 256;
 constexpr int kStages = 4;
+// Pair-tile launches (clusters of two blocks, 256-row tiles of cta_group::2
+// MMAs) stage half of B per block: 16 KB of A + 16 KB of B per slot at
+// 256-wide tiles, so six slots fit where four did.
+constexpr int kPairStages = 6;
 constexpr int kStageBytesA = kTileM * kTileK * 2;       // 16 KB
 constexpr int kStageBytesB = kMaxTileN * kTileK * 2;    // 32 KB
 // Dynamic shared memory of a tensor-core launch: 1 KB alignment slack, the
@@ -48,7 +52,7 @@ constexpr int kBulkMaxSlots = 12;
 constexpr int kEpiBufBytes = 32 * 64;
 constexpr int kEpiMaxDepth = 8;                         // chunk buffers (and mbarriers) per epilogue warp
 constexpr int kBcastBytes = kMaxTileN * 2;   // one 16-bit row of a tile
-constexpr int kTmemCols = 2 * kMaxTileN;                // double-buffered accumulator
+constexpr int kTmemCols = 2 * kMaxTileN;                // double-buffered accumulator (at most)
 constexpr int kMaxMaps = 192;                           // TMA descriptors per launch
 
 // Where a referenced tensor lives.
@@ -306,6 +310,7 @@ struct Params {
   long long* prof;      // optional stamps, [stage][block][kProfStamps]
   int n_in, n_out, n_maps;
   int ring_stage_bytes; // bytes per TMA ring slot (A tile + widest B tile)
+  int tmem_cols;        // TMEM columns allocated: two accumulators of the widest tile (a power of 2)
   int epi_warp_bytes;   // staging bytes per epilogue warp (after the ring)
   void* io[2 * kMaxIO];
 };

@@ -187,6 +187,10 @@ def test_rejects_malformed_programs():
     _err(Program([x], [f32("p", (4, 8))], [Operation("p", "pow", (x, x), f32("p", (4, 8)))]), "exponent")
     _err(Program([x], [f32("a", (4, 8))], [Operation("a", "neg", (x,), f32("a", (4, 8)))]), "blocks_per_sm",
          blocks_per_sm=9)
+    neg = Program([x], [f32("a", (4, 8))], [Operation("a", "neg", (x,), f32("a", (4, 8)))])
+    _err(neg, "tile_n", tile_n=192)
+    _err(neg, "cta_pairs", cta_pairs=2)
+    _err(neg, "epi_stage_bytes", epi_stage_bytes=-4)
 
 
 def test_rejects_bad_inplace_mappings():
@@ -354,3 +358,38 @@ def test_under_filled_gemm_is_split_over_k():
     assert z2[0]["n_items"] == 4 * 32 and z2[1]["stage"] == z2[0]["stage"] + 1
     s = plan(prog, split_k=0)
     assert s["tasks"] == len(tasks) - 1
+
+
+def test_pair_tiles_plan_256_row_tiles_without_split_k():
+    # cta_pairs: every tensor-core GEMM on 256-row tiles dealt to pairs of
+    # SMs, 128-wide at least (each block stages half of B's columns), no
+    # split-K; the C5 forward GEMMs still take 224 columns (16 x 19 = 304 pair
+    # tiles = 4 waves of 76 pairs), the backward ones (MN-major B) 256
+    c5 = S.mlp_step_program(S.CONFIGS["c5"], export="state")
+    st = plan(c5, cta_pairs=1)
+    assert st["cta_pairs"] == 1
+    tasks = _tc_tasks(c5, cta_pairs=1)
+    assert all(t["tile_m"] == 256 for t in tasks.values())
+    assert (tasks["z1"]["tile_n"], tasks["z1"]["n_items"]) == (224, 304)
+    assert (tasks["gW1"]["tile_n"], tasks["gW1"]["n_items"]) == (256, 256)
+    c3 = S.mlp_step_program(S.CONFIGS["c3"], export="state")
+    assert plan(c3)["split_reductions"] >= 1
+    single = _tc_tasks(c3)
+    paired = _tc_tasks(c3, cta_pairs=1)
+    assert single["z2"]["n_items"] == 128                  # 32 tiles x 4 k splits
+    assert paired["z2"]["n_items"] == 8 and paired["z2"]["tile_n"] == 128
+    assert plan(c3, cta_pairs=0)["cta_pairs"] == 0
+    # a program without tensor-core GEMMs ignores the option
+    assert plan(S.mlp_step_program(S.CONFIGS["c1"], export="state"), cta_pairs=1)["cta_pairs"] == 0
+
+
+def test_forward_gemms_take_224_wide_tiles_where_they_fill_whole_waves():
+    c5 = _tc_tasks(S.mlp_step_program(S.CONFIGS["c5"], export="state"))
+    assert {n: t["tile_n"] for n, t in c5.items() if n.startswith("z")} == {f"z{i}": 224 for i in range(1, 5)}
+    assert c5["z1"]["n_items"] == 608 == 4 * 152
+    # MN-major B (the input-gradient and weight-gradient GEMMs) stays at 256
+    assert {t["tile_n"] for n, t in c5.items() if not n.startswith("z")} == {256}
+    # forced: 224 where B is K-major, 256 elsewhere
+    forced = _tc_tasks(S.mlp_step_program(S.CONFIGS["c2"], export="state"), tile_n=224)
+    assert {t["tile_n"] for n, t in forced.items() if n.startswith("z")} == {224}
+    assert {t["tile_n"] for n, t in forced.items() if not n.startswith("z")} == {256}

@@ -518,8 +518,9 @@ def main() -> int:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--stage-profile", action="store_true", help="print per-stage timing of one step")
     ap.add_argument("--launches-only", action="store_true", help="W + K launches and nothing else")
-    ap.add_argument("--cta-pairs", type=int, choices=[0, 1], default=None,
-                    help="run the tensor-core GEMMs on pairs of SMs (1) or one SM per tile (0); default: the planner's")
+    ap.add_argument("--cta-pairs", type=int, choices=[0, 1, 2], default=None,
+                    help="tensor-core GEMMs on pairs of SMs (1: cta_group::2 MMAs, 2: B shared by multicast) "
+                         "or one SM per tile (0); default: the planner's")
     args = ap.parse_args()
     if args.cta_pairs is not None:
         OPTIONS["cta_pairs"] = args.cta_pairs

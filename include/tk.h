@@ -153,11 +153,12 @@ typedef struct {
                                   (0, default: what the SM has left beside the operand ring).
                                   Smaller caps give shallower staging rings; results are
                                   identical (used by tests to reach each staging layout) */
-  int32_t cta_pairs;           /* 1: every tensor-core GEMM runs on pairs of SMs: 256-row tiles,
-                                  one cluster of two blocks per tile, each block staging its 128
-                                  rows of A and half of B's columns, cta_group::2 MMAs (programs
-                                  with no tensor-core GEMM ignore it); 0 (default): one SM per
-                                  128-row tile */
+  int32_t cta_pairs;           /* every tensor-core GEMM on pairs of SMs: 256-row tiles, one
+                                  cluster of two blocks per tile, each block loading its 128 rows
+                                  of A and half of B's columns; 1: cta_group::2 MMAs over both
+                                  blocks' shared memory; 2: each block runs its own 128-row MMAs,
+                                  the B halves multicast to both blocks.  Programs with no
+                                  tensor-core GEMM ignore it; 0 (default): one SM per 128-row tile */
 } tk_options;
 
 /* What the planner decided (codegen.py `GeneratedKernel` counters). */
@@ -180,7 +181,7 @@ typedef struct {
   int32_t chain_tasks;         /* tasks evaluating a generic linear chain (the rest use instructions) */
   int32_t tasks;               /* device tasks (see tk_plan_task) */
   int32_t tma_descriptors;     /* TMA descriptors a launch passes (GEMM operand tiles, epilogue chunks) */
-  int32_t cta_pairs;           /* 1: a pair-tile launch (clusters of two blocks; see tk_options) */
+  int32_t cta_pairs;           /* 1 or 2: a pair-tile launch (clusters of two blocks; see tk_options) */
 } tk_plan_stats;
 
 /* One device task of a plan: a scheduled op (with whatever the planner fused

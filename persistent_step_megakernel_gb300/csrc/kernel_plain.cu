@@ -4,7 +4,7 @@
 
 namespace tkk {
 __global__ void __launch_bounds__(kThreads, 1) tk_persistent(const __grid_constant__ Params p) {
-  persistent_body<false>(p, nullptr);
+  persistent_body<0>(p, nullptr);
 }
 }  // namespace tkk
 

@@ -5,7 +5,7 @@
 
 namespace tkk {
 __global__ void __launch_bounds__(kThreads, 1) tk_persistent_tc_large(const __grid_constant__ ParamsTc<kMaxMaps> p) {
-  persistent_body<false>(p.p, p.maps);
+  persistent_body<0>(p.p, p.maps);
 }
 }  // namespace tkk
 

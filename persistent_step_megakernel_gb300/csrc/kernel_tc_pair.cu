@@ -6,7 +6,7 @@
 
 namespace tkk {
 __global__ void __launch_bounds__(kThreads, 1) tk_persistent_tc_pair(const __grid_constant__ ParamsTc<kMaxMaps> p) {
-  persistent_body<true>(p.p, p.maps);
+  persistent_body<1>(p.p, p.maps);
 }
 }  // namespace tkk
 

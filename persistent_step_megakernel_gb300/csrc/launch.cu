@@ -11,14 +11,17 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-enum Variant { V_PLAIN = 0, V_TC_SMALL = 1, V_TC_LARGE = 2, V_TC_PAIR = 3, V_COUNT = 4 };
+enum Variant { V_PLAIN = 0, V_TC_SMALL = 1, V_TC_LARGE = 2, V_TC_PAIR = 3, V_TC_MCAST = 4, V_COUNT = 5 };
 
 const void* kernel_of(int v) {
   return v == V_PLAIN      ? tk_kernel_fn_plain()
          : v == V_TC_SMALL ? tk_kernel_fn_tc_small()
          : v == V_TC_LARGE ? tk_kernel_fn_tc_large()
-                           : tk_kernel_fn_tc_pair();
+         : v == V_TC_PAIR  ? tk_kernel_fn_tc_pair()
+                           : tk_kernel_fn_tc_mcast();
 }
+
+int pair_variant(int pair) { return pair == 1 ? V_TC_PAIR : V_TC_MCAST; }
 
 // Per device and variant: the kernel's static shared memory (read once) and
 // the shared-memory carveout last applied.  Function attributes belong to a
@@ -70,7 +73,7 @@ cudaError_t launch_tc(const cudaLaunchConfig_t* cfg, const void* fn, const tkd::
 }  // namespace
 
 cudaError_t tk_kernel_launch(const tkd::Params& params, const void* maps, int n_maps, int grid, size_t dyn_smem,
-                             cudaStream_t stream, bool pair) {
+                             cudaStream_t stream, int pair) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(tkd::kThreads);
@@ -86,7 +89,7 @@ cudaError_t tk_kernel_launch(const tkd::Params& params, const void* maps, int n_
   cfg.attrs = attr;
   cfg.numAttrs = pair ? 2 : 1;
   if (pair && (!maps || grid % 2)) return cudaErrorInvalidValue;
-  const int v = !maps ? V_PLAIN : pair ? V_TC_PAIR : n_maps <= tkd::kSmallMaps ? V_TC_SMALL : V_TC_LARGE;
+  const int v = !maps ? V_PLAIN : pair ? pair_variant(pair) : n_maps <= tkd::kSmallMaps ? V_TC_SMALL : V_TC_LARGE;
   if (maps && n_maps > tkd::kMaxMaps) return cudaErrorInvalidValue;
   cudaError_t e = set_carveout(v, dyn_smem);
   if (e != cudaSuccess) return e;
@@ -99,7 +102,7 @@ cudaError_t tk_kernel_launch(const tkd::Params& params, const void* maps, int n_
   return launch_tc<tkd::kMaxMaps>(&cfg, kernel_of(v), params, maps, n_maps);
 }
 
-cudaError_t tk_kernel_pair_clusters(int* clusters, size_t dyn_smem) {
+cudaError_t tk_kernel_pair_clusters(int* clusters, size_t dyn_smem, int pair) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);
   cfg.blockDim = dim3(tkd::kThreads);
@@ -111,9 +114,9 @@ cudaError_t tk_kernel_pair_clusters(int* clusters, size_t dyn_smem) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = set_carveout(V_TC_PAIR, dyn_smem);
+  cudaError_t e = set_carveout(pair_variant(pair), dyn_smem);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveClusters(clusters, kernel_of(V_TC_PAIR), &cfg);
+  return cudaOccupancyMaxActiveClusters(clusters, kernel_of(pair_variant(pair)), &cfg);
 }
 
 // The dynamic shared-memory limit is raised to the largest any program uses,
@@ -121,7 +124,7 @@ cudaError_t tk_kernel_pair_clusters(int* clusters, size_t dyn_smem) {
 // every program, with the program's device current.
 cudaError_t tk_kernel_prepare(bool tc, size_t) {
   if (!tc) return cudaSuccess;
-  for (int v : {V_TC_SMALL, V_TC_LARGE, V_TC_PAIR}) {
+  for (int v : {V_TC_SMALL, V_TC_LARGE, V_TC_PAIR, V_TC_MCAST}) {
     cudaError_t e = cudaFuncSetAttribute(kernel_of(v), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          tkd::kDynSmemBudget);
     if (e != cudaSuccess) return e;
@@ -134,6 +137,6 @@ cudaError_t tk_kernel_occupancy(int* blocks_per_sm, bool tc, size_t dyn_smem) {
                                                        tkd::kThreads, dyn_smem);
 }
 
-cudaError_t tk_kernel_attributes(cudaFuncAttributes* attr, bool tc, bool pair) {
-  return cudaFuncGetAttributes(attr, kernel_of(!tc ? V_PLAIN : pair ? V_TC_PAIR : V_TC_LARGE));
+cudaError_t tk_kernel_attributes(cudaFuncAttributes* attr, bool tc, int pair) {
+  return cudaFuncGetAttributes(attr, kernel_of(!tc ? V_PLAIN : pair ? pair_variant(pair) : V_TC_LARGE));
 }

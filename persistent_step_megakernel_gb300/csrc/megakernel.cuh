@@ -1594,6 +1594,25 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// TMA loads of a box into this block's and the other pair block's shared
+// memory (same offset), completing on the mbarrier at `bar`'s offset in each.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                               uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(mask)
+      : "memory");
+}
+
 // Bounded wait with cluster-scope acquire (for phases completed by arrivals
 // from the other block of the pair).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
@@ -1846,6 +1865,13 @@ __device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t adesc, u
 }
 __device__ __forceinline__ void umma_commit_pair_mc(uint32_t bar, uint16_t mask) {
   asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+               ::"r"(bar), "h"(mask)
+               : "memory");
+}
+// A single block's commit arriving on the mbarrier at `bar`'s offset in the
+// blocks of `mask` (a shared-B pair: both blocks' MMAs free a ring slot).
+__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
                ::"r"(bar), "h"(mask)
                : "memory");
 }
@@ -2388,20 +2414,27 @@ __device__ __forceinline__ void tc_epilogue_tile(const Ctx& c, const Task& t, in
 // waits, again with the time limit, for that work to land before returning,
 // so that nothing arrives in shared memory or TMEM after the block has freed
 // them and exited.
-template <bool PAIR>
+// PM: 0 one block per tile; 1 a pair of blocks per 256-row tile with
+// cta_group::2 MMAs; 2 a pair per 256-row tile, each block its own 128-row
+// MMAs, B's halves multicast to both blocks.
+template <int PM>
 __device__ __noinline__ uint64_t tc_producer(const Ctx c, const Stage st, const CUtensorMap* maps, const TcState ts,
                                              uint32_t p_it) {
+  constexpr bool PAIR = PM == 1, MC = PM == 2, CL = PM != 0;
   constexpr uint32_t NS = PAIR ? kPairStages : kStages;
   bool ok = true;
   const uint32_t p_it0 = p_it;
-  // pair: this block loads its 128 rows of A and its half of B's columns;
-  // both blocks' copies complete on the leader's "full" mbarrier
-  const uint32_t rank = PAIR ? cluster_rank() & 1u : 0u;
-  const uint32_t leader = PAIR ? cluster_rank() & ~1u : 0u;
+  // pairs: this block loads its 128 rows of A and its half of B's columns;
+  // PM 1: both blocks' copies complete on the leader's "full" mbarrier;
+  // PM 2: the B half goes to both blocks, each counting the whole tile
+  const uint32_t rank = CL ? cluster_rank() & 1u : 0u;
+  const uint32_t leader = CL ? cluster_rank() & ~1u : 0u;
+  const uint16_t mask = uint16_t(3u << leader);
   asm volatile("fence.proxy.async.global;" ::: "memory");
-  for_my_tiles<PAIR>(c, st, [&](const Task& t, const TileItem& it) {
-    const int half = PAIR ? t.tile_n / 2 : t.tile_n;  // B columns this block loads
+  for_my_tiles<CL>(c, st, [&](const Task& t, const TileItem& it) {
+    const int half = CL ? t.tile_n / 2 : t.tile_n;  // B columns this block loads
     const uint32_t bytes = uint32_t(kStageBytesA + half * kTileK * 2);
+    const uint32_t tile_bytes = uint32_t(kStageBytesA + t.tile_n * kTileK * 2);
     const int tma_a = t.tma_a, tma_b = t.tma_b;
     const int a_mn = t.a_mn_major, b_mn = t.b_mn_major;
     const int64_t m0 = it.m0 + int64_t(rank) * kTileM, n0 = it.n0 + int64_t(rank) * half;
@@ -2429,6 +2462,24 @@ __device__ __noinline__ uint64_t tc_producer(const Ctx c, const Stage st, const 
         } else {
           for (int j = 0; j < half / 64; ++j) tma_load_2d_pair(b_dst + 8192 * j, &maps[tma_b], int(n0) + 64 * j, k0, bar);
         }
+      } else if constexpr (MC) {
+        mbar_expect_tx(full, tile_bytes);  // own A, both B halves
+        if (!a_mn) {
+          tma_load_2d(a_dst, &maps[tma_a], k0, int(m0), full);
+        } else if (a_mn == 2) {
+          tma_load_3d(a_dst, &maps[tma_a], 0, k0, int(m0 >> 6), full);
+        } else {
+          tma_load_2d(a_dst, &maps[tma_a], int(m0), k0, full);
+          tma_load_2d(a_dst + 8192, &maps[tma_a], int(m0) + 64, k0, full);
+        }
+        const uint32_t bh = b_dst + rank * uint32_t(half) * kTileK * 2;  // this block's half of the tile
+        if (!b_mn) {
+          tma_load_2d_mc(bh, &maps[tma_b], k0, int(n0), full, mask);
+        } else if (b_mn == 2) {
+          tma_load_3d_mc(bh, &maps[tma_b], 0, k0, int(n0 >> 6), full, mask);
+        } else {
+          for (int j = 0; j < half / 64; ++j) tma_load_2d_mc(bh + 8192 * j, &maps[tma_b], int(n0) + 64 * j, k0, full, mask);
+        }
       } else {
         mbar_expect_tx(full, bytes);
         if (!a_mn) {
@@ -2451,7 +2502,7 @@ __device__ __noinline__ uint64_t tc_producer(const Ctx c, const Stage st, const 
     }
     return true;
   });
-  if (!ok && rank == 0) {
+  if (!ok && (!PAIR || rank == 0)) {
     // the copies of the last (up to) NS slots this stage armed: each
     // completes its slot's current "full" phase (a slot is re-armed only
     // after its previous phase was consumed, so that phase is still the one
@@ -2463,18 +2514,20 @@ __device__ __noinline__ uint64_t tc_producer(const Ctx c, const Stage st, const 
   return (uint64_t(ok) << 32) | p_it;
 }
 
-template <bool PAIR>
+template <int PM>
 __device__ __noinline__ uint64_t tc_mma(const Ctx c, const Stage st, const TcState ts, uint32_t m_it,
                                         uint32_t* m_tile_io, long long* prof) {
+  constexpr bool PAIR = PM == 1, MC = PM == 2, CL = PM != 0;
   constexpr uint32_t NS = PAIR ? kPairStages : kStages;
   // pair: the leader issues the pair's MMAs; its commits arrive on the
   // "empty" and accumulator mbarriers of both blocks
   if (PAIR && (cluster_rank() & 1u)) return uint64_t(1) << 32 | m_it;
-  const uint16_t pair_mask = PAIR ? uint16_t(3u << (cluster_rank() & ~1u)) : uint16_t(0);
+  // (shared B: a slot is free once both blocks' MMAs have read it)
+  const uint16_t pair_mask = CL ? uint16_t(3u << (cluster_rank() & ~1u)) : uint16_t(0);
   bool ok = true;
   bool first = true;
   uint32_t m_tile = *m_tile_io;
-  for_my_tiles<PAIR>(c, st, [&](const Task& t, const TileItem& it) {
+  for_my_tiles<CL>(c, st, [&](const Task& t, const TileItem& it) {
     const uint32_t acc = m_tile & 1u, ph = ((m_tile >> 1) & 1u) ^ 1u;
     // pair: the epilogue warps of both blocks release the accumulator
     const bool freed = PAIR ? mbar_wait_cluster(ts.acc_empty + 8 * acc, ph, c.timeout_ns)
@@ -2502,6 +2555,8 @@ __device__ __noinline__ uint64_t tc_mma(const Ctx c, const Stage st, const TcSta
       }
       if constexpr (PAIR)
         umma_commit_pair_mc(ts.empty + 8 * slot, pair_mask);
+      else if constexpr (MC)
+        umma_commit_mc(ts.empty + 8 * slot, pair_mask);
       else
         umma_commit(ts.empty + 8 * slot);
       ++m_it;
@@ -2525,9 +2580,10 @@ __device__ __noinline__ uint64_t tc_mma(const Ctx c, const Stage st, const TcSta
   return (uint64_t(ok) << 32) | m_it;
 }
 
-template <bool PAIR>
+template <int PM>
 __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const TcState ts, uint32_t e_tile,
                                              long long* prof, EpiRing* er) {
+  constexpr bool PAIR = PM == 1, CL = PM != 0;
   bool ok = true;
   bool first = true;
   const int lane = threadIdx.x & 31;
@@ -2535,9 +2591,9 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
   const uint32_t stg = ts.stg + ew * ts.stg_warp_bytes, ebar = ts.epi_bar + 8 * kEpiMaxDepth * ew;
   // pair: this block's accumulator rows are the tile's half `rank`; the
   // accumulator is released on the leader's mbarrier
-  const uint32_t rank = PAIR ? cluster_rank() & 1u : 0u;
+  const uint32_t rank = CL ? cluster_rank() & 1u : 0u;
   const uint32_t acc_empty_leader = PAIR ? cluster_addr(ts.acc_empty, cluster_rank() & ~1u) : 0u;
-  for_my_tiles<PAIR>(c, st, [&](const Task& t, const TileItem& it) {
+  for_my_tiles<CL>(c, st, [&](const Task& t, const TileItem& it) {
     const int64_t m0 = it.m0 + int64_t(rank) * kTileM, n0 = it.n0;
     const uint32_t acc = e_tile & 1u, ph = (e_tile >> 1) & 1u;
     long long* stamp = prof && first && threadIdx.x == 128 ? prof + 5 : nullptr;
@@ -2576,26 +2632,26 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
 }
 
 // Run this block's tensor-core tiles of one stage; false after a wait timed out.
-template <bool PAIR>
+template <int PM>
 __device__ bool run_tc_phase(const Ctx& c, const Stage& st, const CUtensorMap* maps, TcState& ts, int stage,
                              int* s_flag, long long* prof) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   bool ok = true;
   if (warp == 0 && lane == 0) {
-    const uint64_t r = tc_producer<PAIR>(c, st, maps, ts, ts.p_it);
+    const uint64_t r = tc_producer<PM>(c, st, maps, ts, ts.p_it);
     ts.p_it = uint32_t(r);
     ok = (r >> 32) != 0;
     if (prof) prof[2] = global_ns();
   } else if (warp == 1 && lane == 0) {
     uint32_t m_tile = ts.m_tile;
-    const uint64_t r = tc_mma<PAIR>(c, st, ts, ts.m_it, &m_tile, prof);
+    const uint64_t r = tc_mma<PM>(c, st, ts, ts.m_it, &m_tile, prof);
     ts.m_it = uint32_t(r);
     ts.m_tile = m_tile;
     ok = (r >> 32) != 0;
     if (prof) prof[4] = global_ns();
   } else if (warp >= 4) {
     EpiRing er = ts.er;
-    const uint64_t r = tc_epilogue<PAIR>(c, st, ts, ts.e_tile, prof, &er);
+    const uint64_t r = tc_epilogue<PM>(c, st, ts, ts.e_tile, prof, &er);
     ts.e_tile = uint32_t(r);
     ts.er = er;
     ok = (r >> 32) != 0;
@@ -2691,10 +2747,12 @@ __device__ __forceinline__ void stage_in(const Program* prog, int s, Stage* s_st
     copy_words(s_refs, prog->refs + st.ref_lo, (st.ref_hi - st.ref_lo) * int(sizeof(Ref)), tid, n);
 }
 
-// PAIR: a pair-tile launch (clusters of two blocks; every tensor-core GEMM on
-// 256-row tiles of cta_group::2 MMAs, kPairStages ring slots).
-template <bool PAIR>
+// PM: 0 one block per tile; a pair-tile launch (clusters of two blocks, every
+// tensor-core GEMM on 256-row tiles) with 1 cta_group::2 MMAs and kPairStages
+// ring slots, or 2 each block's own MMAs on B tiles shared by multicast.
+template <int PM>
 __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorMap* maps) {
+  constexpr bool PAIR = PM == 1, MC = PM == 2;
   constexpr int NS = PAIR ? kPairStages : kStages;
   __shared__ void* s_io[2 * kMaxIO];
   __shared__ Task s_tasks[kStageTasks];
@@ -2714,7 +2772,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   const bool tc = maps != nullptr;
   // pair: the launch must have formed clusters of two (else no cluster or
   // pair operation runs and the kernel reports TK_ERR_PAIR_TMEM)
-  const bool paired = PAIR && cluster_size() == 2;
+  const bool paired = PM != 0 && cluster_size() == 2;
   // scratch for reductions and CUDA-core GEMMs at the start of the dynamic
   // region; in a tensor-core launch it overlays the (then idle) ring
   float* s_work = reinterpret_cast<float*>(s_dyn + ((1024u - (smem_u32(s_dyn) & 1023u)) & 1023u));
@@ -2741,7 +2799,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     if (threadIdx.x == 0) {
       for (int i = 0; i < NS; ++i) {
         mbar_init(ts.full + 8 * i, 1);
-        mbar_init(ts.empty + 8 * i, 1);
+        mbar_init(ts.empty + 8 * i, MC ? 2 : 1);  // shared B: both blocks' MMAs free a slot
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(ts.acc_full + 8 * i, 1);
@@ -2761,7 +2819,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     if (threadIdx.x == 0)
       for (int i = 0; i < p.n_maps; ++i)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps[i])) : "memory");
-    if (warp == 1 && (!PAIR || paired)) {
+    if (warp == 1 && (PM == 0 || paired)) {
       // pair: one warp of each block of the pair allocates, together
       if constexpr (PAIR) {
         asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
@@ -2779,14 +2837,14 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
   // pair: neither block signals the other's mbarriers before both have
   // initialised them
   if (paired) cluster_sync();
-  bool pair_ok = !PAIR || paired;
+  bool pair_ok = PM == 0 || paired;
   if (tc) {
     tc_fence_after();
     ts.tmem = s_tmem;
     ts.acc_cols = uint32_t(p.tmem_cols) / 2;
     // pair: an MMA of the pair writes the same TMEM columns in both blocks,
     // so both must have been given the same address
-    if (paired) {
+    if (PAIR && paired) {
       uint32_t other;
       asm volatile("ld.shared::cluster.u32 %0, [%1];"
                    : "=r"(other)
@@ -2836,14 +2894,15 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     c.code = st.code_hi - st.code_lo <= kStageCode ? s_code - st.code_lo : prog->code;
     c.refs = st.ref_hi - st.ref_lo <= kStageRefs ? s_refs - st.ref_lo : prog->refs;
     if (tc && st.n_tc_items > 0 &&
-        !run_tc_phase<PAIR>(c, st, maps, ts, s, &s_flag, prof ? prof + s * prof_step : nullptr))
+        !run_tc_phase<PM>(c, st, maps, ts, s, &s_flag, prof ? prof + s * prof_step : nullptr))
       break;
     // the stage's other items after its tiles: blocks with one tile fewer
-    // than the busiest (r = tiles mod grid of them have one more) first take
+    // than the busiest (the first r blocks have one more: r = tiles mod grid,
+    // or twice tiles mod pairs when tiles go to pairs of blocks) first take
     // up to light_items each, the rest go round-robin from block r on
     {
       const int G = gridDim.x, b = blockIdx.x, T = st.n_tc_items, n_rest = st.n_items - T;
-      const int r = T % G, n_light = r ? G - r : 0;
+      const int r = PM ? 2 * (T % (G / 2)) : T % G, n_light = r ? G - r : 0;
       const int extra = min(n_rest, n_light * st.light_items);
       // this block's first-round items j = b - r + k * n_light (k < n1), then
       // j = extra + (b - r) mod G + k' * G
@@ -2879,7 +2938,7 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
     // both free the TMEM together
     if (paired) cluster_sync();
     tc_fence_after();
-    if (warp == 1 && (!PAIR || paired)) {
+    if (warp == 1 && (PM == 0 || paired)) {
       if constexpr (PAIR)
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(ts.tmem), "r"(p.tmem_cols));
       else

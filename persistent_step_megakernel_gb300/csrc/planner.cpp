@@ -130,7 +130,7 @@ float f32(double v) { return static_cast<float>(v); }
 class Planner {
  public:
   Planner(const tk_program_desc& d, const tk_options& o, int sms)
-      : opt_(o), sms_(std::max(sms, 1)), pair_(o.cta_pairs != 0 && sms >= 2) {
+      : opt_(o), sms_(std::max(sms, 1)), pair_(sms >= 2 ? o.cta_pairs : 0) {
     read_desc(d);
   }
 
@@ -150,7 +150,9 @@ class Planner {
  private:
   tk_options opt_;
   int sms_;
-  bool pair_;  // pair tiles: every tensor-core GEMM on 256-row tiles of a pair of SMs
+  // pair tiles: every tensor-core GEMM on 256-row tiles of a pair of SMs;
+  // 1: cta_group::2 MMAs, 2: each SM its 128 rows, B shared by TMA multicast
+  int pair_;
   std::vector<OpInfo> ops_;
   std::vector<tk_tensor_spec> inputs_, outputs_;
   std::map<int, int> inplace_;  // output slot -> input index
@@ -1612,7 +1614,7 @@ class Planner {
     }
     if (opt_.tile_n > 0) bn = pair_ ? std::max(opt_.tile_n, 128) : opt_.tile_n;
     // each block of a pair stages half of B's columns
-    const int bdiv = pair_ ? 2 : 1;
+    const int bdiv = pair_ ? 2 : 1;  // each block loads half of B's columns
     TmaOperand ta, tb;
     int a_mn = 0, b_mn = 0;
     if (!tma_operand(A, true, tkd::kTileM, &ta, &a_mn) ||
@@ -1644,8 +1646,10 @@ class Planner {
     // instruction descriptor, kind::f16: D f32 (bits 4-5), A/B type (7-9, 10-12:
     // 0 f16, 1 bf16), A/B MN-major (15, 16), N >> 3 (17-22), M >> 4 (24-28)
     uint32_t ab = A.dtype == TK_BF16 ? 1u : 0u;
+    // (a shared-B pair's blocks each run their own 128-row MMAs)
+    const int64_t mma_m = pair_ == 1 ? tm : tkd::kTileM;
     t.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (uint32_t(a_mn != 0) << 15) | (uint32_t(b_mn != 0) << 16) |
-              (uint32_t(bn >> 3) << 17) | (uint32_t(tm >> 4) << 24);
+              (uint32_t(bn >> 3) << 17) | (uint32_t(mma_m >> 4) << 24);
     // Split-K when the tiles leave most SMs idle and each tile has a long K
     // loop (at least 8 k blocks per split).
     t.k_splits = 1;
@@ -2236,11 +2240,12 @@ class Planner {
     // Ring slots sized for the widest tile: smaller rings leave more of the
     // SM's unified L1/shared memory to the L1 cache.
     // (a pair-tile launch stages half of each B tile per block)
-    plan.pair = pair_ && tc_ops > 0;
+    plan.pair = tc_ops > 0 ? pair_ : 0;
     plan.tmem_cols = 32;
     while (plan.tmem_cols < 2 * max_bn) plan.tmem_cols *= 2;
-    plan.ring_stage_bytes = tkd::kStageBytesA + (plan.pair ? max_bn / 2 : max_bn) * tkd::kTileK * 2;
-    const size_t ring = 1024 + size_t(plan.pair ? tkd::kPairStages : tkd::kStages) * plan.ring_stage_bytes;
+    // (a shared-B pair keeps whole B tiles: each block's half arrives by multicast)
+    plan.ring_stage_bytes = tkd::kStageBytesA + (plan.pair == 1 ? max_bn / 2 : max_bn) * tkd::kTileK * 2;
+    const size_t ring = 1024 + size_t(plan.pair == 1 ? tkd::kPairStages : tkd::kStages) * plan.ring_stage_bytes;
     // every staged task may use the staging bytes left beside the ring
     const int avail = ring < size_t(tkd::kDynSmemBudget) ? int((size_t(tkd::kDynSmemBudget) - ring) / 4) : 0;
     for (auto& t : plan.tasks) {
@@ -2269,7 +2274,7 @@ class Planner {
     st.inlined_ops = int(inline_.size());
     st.fused_epilogues = int(fused_.size());
     st.tensor_core_ops = tc_ops;
-    st.cta_pairs = plan.pair ? 1 : 0;
+    st.cta_pairs = plan.pair;
     st.stages = int(plan.stages.size());
     st.grid_barriers = st.stages - 1;
     st.direct_outputs = int(binding_.size());

@@ -52,7 +52,7 @@ struct Plan {
   int ring_stage_bytes = 0;  // TMA ring slot size for the widest tensor-core tile
   int epi_warp_bytes = 0;    // epilogue staging per epilogue warp
   bool uses_tc = false;
-  bool pair = false;         // pair-tile launch (clusters of two blocks, cta_group::2 MMAs)
+  int pair = 0;              // pair-tile launch (clusters of two blocks): 1 cta_group::2 MMAs, 2 shared B
   int tmem_cols = 0;         // TMEM columns: two accumulators of the widest tile, a power of 2 >= 32
   tk_plan_stats stats{};
   // what tk_run checks

@@ -233,7 +233,7 @@ tk_status tk_program_create(const tk_program_desc* desc, const tk_options* opt_i
   if (opt.tile_n != 0 && opt.tile_n != 64 && opt.tile_n != 128 && opt.tile_n != 224 && opt.tile_n != 256)
     return fail(TK_ERR_INVALID, "tile_n must be 0, 64, 128, 224 or 256");
   if (opt.epi_stage_bytes < 0) return fail(TK_ERR_INVALID, "epi_stage_bytes must be >= 0");
-  if (opt.cta_pairs != 0 && opt.cta_pairs != 1) return fail(TK_ERR_INVALID, "cta_pairs must be 0 or 1");
+  if (opt.cta_pairs < 0 || opt.cta_pairs > 2) return fail(TK_ERR_INVALID, "cta_pairs must be 0, 1 or 2");
 
   int sms = opt.sm_count > 0 ? opt.sm_count : 152;
   if (device >= 0) {
@@ -293,7 +293,7 @@ tk_status tk_program_create(const tk_program_desc* desc, const tk_options* opt_i
     int clusters = int(sms / 2);
     if (device >= 0) {
       DeviceGuard g(device);
-      cudaError_t e = tk_kernel_pair_clusters(&clusters, p->dyn_smem);
+      cudaError_t e = tk_kernel_pair_clusters(&clusters, p->dyn_smem, p->plan.pair);
       if (e != cudaSuccess) {
         tk_program_destroy(p);
         return cuda_fail(e, "cudaOccupancyMaxActiveClusters");

@@ -189,7 +189,7 @@ def test_rejects_malformed_programs():
          blocks_per_sm=9)
     neg = Program([x], [f32("a", (4, 8))], [Operation("a", "neg", (x,), f32("a", (4, 8)))])
     _err(neg, "tile_n", tile_n=192)
-    _err(neg, "cta_pairs", cta_pairs=2)
+    _err(neg, "cta_pairs", cta_pairs=3)
     _err(neg, "epi_stage_bytes", epi_stage_bytes=-4)
 
 

@@ -159,6 +159,11 @@ typedef struct {
                                   blocks' shared memory; 2: each block runs its own 128-row MMAs,
                                   the B halves multicast to both blocks.  Programs with no
                                   tensor-core GEMM ignore it; 0 (default): one SM per 128-row tile */
+  int32_t overlap_reductions;  /* 1 (default): a stage's compiled row and column reductions of
+                                  16-bit operands run on the warps the tensor-core tiles leave idle,
+                                  while the tiles run, where the planner estimates they fit in the
+                                  tiles' time; 2: every such reduction (tests); 0: after the tiles.
+                                  Results are identical */
 } tk_options;
 
 /* What the planner decided (codegen.py `GeneratedKernel` counters). */
@@ -203,6 +208,7 @@ typedef struct {
   int32_t side_output;         /* GEMM that also writes a second value (a side output) from its tile */
   int32_t staged_depth;        /* staged epilogue: 32-column chunks in flight per epilogue warp
                                   (2, 4 or 8; +16 when a side output has buffers of its own); 0 */
+  int32_t beside_tiles;        /* reduction run while the stage's tensor-core tiles run */
   int64_t numel;               /* elements of the task's index space */
 } tk_task_info;
 

@@ -56,7 +56,8 @@ class tk_options(ctypes.Structure):
                 ("sm_count", ctypes.c_int32), ("profile", ctypes.c_int32),
                 ("barrier_timeout_s", ctypes.c_double), ("expr_forms", ctypes.c_int32),
                 ("split_k", ctypes.c_int32), ("tile_n", ctypes.c_int32),
-                ("epi_stage_bytes", ctypes.c_int32), ("cta_pairs", ctypes.c_int32)]
+                ("epi_stage_bytes", ctypes.c_int32), ("cta_pairs", ctypes.c_int32),
+                ("overlap_reductions", ctypes.c_int32)]
 
 
 class tk_plan_stats(ctypes.Structure):
@@ -71,7 +72,7 @@ class tk_plan_stats(ctypes.Structure):
 class tk_task_info(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "stage", "kind", "op_index", "n_items", "form", "compiled_shape", "m", "n", "k", "tile_m", "tile_n",
-        "parts", "staged_epilogue", "side_output", "staged_depth")] + [("numel", ctypes.c_int64)]
+        "parts", "staged_epilogue", "side_output", "staged_depth", "beside_tiles")] + [("numel", ctypes.c_int64)]
 
 
 # (name, restype, argtypes) for every entry point of include/tk.h

@@ -2631,6 +2631,167 @@ __device__ __noinline__ uint64_t tc_epilogue(const Ctx c, const Stage st, const 
   return (uint64_t(ok) << 32) | e_tile;
 }
 
+// ------------------------------------ reductions beside the tensor-core tiles
+//
+// During a stage's tensor-core phase warps 2 and 3 have no role.  Reductions
+// the planner marks `bg` run there instead of after the tiles: one warp per
+// work item, emulating the eight warps of the 256-thread routines so that
+// every output gets exactly the same additions in exactly the same order
+// (per virtual thread the same elements in sequence; the same butterfly per
+// virtual warp; the warps' totals added in warp order), hence the same bits.
+
+// Row reduction item (output o, part p): virtual thread vt = 32 w + lane sums
+// elements r0 + 8 vt + k * 2048 (k = 0, 1, ...), eight at a time in order.
+template <int K, int DT>
+__device__ __forceinline__ void bg_row_item(const Ctx& c, const Task& t, int item) {
+  constexpr int64_t step = int64_t(kThreads) * 8;
+  constexpr int VW = kThreads / 32;  // virtual warps
+  const int lane = threadIdx.x & 31;
+  const int64_t o = item / t.parts;
+  const int p = item % t.parts;
+  const int64_t r0 = int64_t(p) * t.part_len;
+  const int64_t r1 = min(t.red_inner, r0 + t.part_len);
+  const float pre = lane == 0 && t.parts == 1 ? post_operand(c, t, o) : 0.0f;
+  const Fast F = fast_params(c, t);
+  const int64_t row0 = o * t.red_inner;
+  float acc[VW], none[8];
+#pragma unroll
+  for (int w = 0; w < VW; ++w) acc[w] = 0.0f;
+  // all eight virtual warps' vectors in flight at a time
+  for (int64_t base = r0; base < r1; base += step) {
+#pragma unroll
+    for (int h = 0; h < VW; h += 8) {
+      uint4 qa[8], qb[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t r = base + int64_t(32 * (h + u) + lane) * 8;
+        if (r < r1) {
+          qa[u] = *reinterpret_cast<const uint4*>(F.p0 + (row0 + r) * 2);
+          if constexpr (FastTraits<K>::load1) qb[u] = *reinterpret_cast<const uint4*>(F.p1 + (row0 + r) * 2);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t r = base + int64_t(32 * (h + u) + lane) * 8;
+        if (r < r1) {
+          float a[8], b[8], x[8];
+          unpack8(qa[u], DT, a);
+          if constexpr (FastTraits<K>::load1) unpack8(qb[u], DT, b);
+          fast_apply<K>(F, a, b, none, x);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[h + u] = __fadd_rn(acc[h + u], x[j]);
+        }
+      }
+    }
+  }
+  float s = 0.0f;
+#pragma unroll
+  for (int w = 0; w < VW; ++w) {
+    float v = acc[w];
+#pragma unroll
+    for (int d = 16; d; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+    s += v;
+  }
+  if (lane == 0) {
+    if (t.parts == 1)
+      finish_reduction(c, t, o, s, pre);
+    else
+      reinterpret_cast<float*>(c.ws)[t.scratch + o * t.parts + p] = s;
+  }
+}
+
+// Column reduction item (256-column chunk, part p): virtual warp w sums rows
+// r0 + w + 8 i (i = 0, 1, ...) of the lane's eight columns; then the eight
+// virtual warps' sums are added in warp order.
+template <int K, int DT>
+__device__ __forceinline__ void bg_col_item(const Ctx& c, const Task& t, int item) {
+  constexpr int VW = kThreads / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t ch = item / t.parts;
+  const int p = item % t.parts;
+  const int64_t Q = t.red_inner;
+  const int64_t col0 = ch * 256 + lane * 8;
+  const int64_t r0 = int64_t(p) * t.part_len;
+  const int64_t r1 = min(t.red_outer, r0 + t.part_len);
+  const Fast F = fast_params(c, t);
+  float acc[VW][8], none[8];
+#pragma unroll
+  for (int w = 0; w < VW; ++w)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[w][j] = 0.0f;
+  if (col0 < Q) {
+    // four rows' vectors in flight at a time
+    for (int64_t i0 = r0; i0 < r1; i0 += VW) {
+#pragma unroll
+      for (int h = 0; h < VW; h += 4) {
+        uint4 qa[4], qb[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (i0 + h + u < r1) {
+            qa[u] = *reinterpret_cast<const uint4*>(F.p0 + ((i0 + h + u) * Q + col0) * 2);
+            if constexpr (FastTraits<K>::load1) qb[u] = *reinterpret_cast<const uint4*>(F.p1 + ((i0 + h + u) * Q + col0) * 2);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (i0 + h + u < r1) {
+            float a[8], b[8], x[8];
+            unpack8(qa[u], DT, a);
+            if constexpr (FastTraits<K>::load1) unpack8(qb[u], DT, b);
+            fast_apply<K>(F, a, b, none, x);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[h + u][j] = __fadd_rn(acc[h + u][j], x[j]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float s = 0.0f;
+#pragma unroll
+    for (int w = 0; w < VW; ++w) s = __fadd_rn(s, acc[w][j]);
+    const int64_t col = col0 + j;
+    if (col < Q) {
+      if (t.parts == 1)
+        finish_reduction(c, t, col, s, post_operand(c, t, col));
+      else
+        reinterpret_cast<float*>(c.ws)[t.scratch + col * t.parts + p] = s;
+    }
+  }
+}
+
+// The kinds run beside the tiles: sums of a 16-bit operand (FK_L, a bias
+// gradient) and of its squares (FK_L_SQUARE, a squared-error loss), all
+// operand of the type t.bg says (the planner marks only those).
+__device__ __noinline__ void bg_item(const Ctx& c, const Task& t, int item) {
+  const bool row = t.kind == T_REDUCE_ROW, bf = t.bg == TK_BF16;
+  if (t.chain.fast == FK_L) {
+    if (row)
+      bf ? bg_row_item<FK_L, TK_BF16>(c, t, item) : bg_row_item<FK_L, TK_F16>(c, t, item);
+    else
+      bf ? bg_col_item<FK_L, TK_BF16>(c, t, item) : bg_col_item<FK_L, TK_F16>(c, t, item);
+  } else {
+    if (row)
+      bf ? bg_row_item<FK_L_SQUARE, TK_BF16>(c, t, item) : bg_row_item<FK_L_SQUARE, TK_F16>(c, t, item);
+    else
+      bf ? bg_col_item<FK_L_SQUARE, TK_BF16>(c, t, item) : bg_col_item<FK_L_SQUARE, TK_F16>(c, t, item);
+  }
+}
+
+// Warp 2 or 3: this block's `bg` items of the stage (item g of a bg task goes
+// to block g mod grid; the block's items alternate between the two warps).
+__device__ __noinline__ void run_bg_items(const Ctx& c, const Stage& st) {
+  const int w = (threadIdx.x >> 5) - 2;
+  int k = 0;
+  for (int ti = st.task_begin; ti < st.task_end; ++ti) {
+    const Task& t = c.tasks[ti];
+    if (!t.bg) continue;
+    for (int g = blockIdx.x; g < t.n_items; g += gridDim.x, ++k)
+      if ((k & 1) == w) bg_item(c, t, g);
+  }
+}
+
 // Run this block's tensor-core tiles of one stage; false after a wait timed out.
 template <int PM>
 __device__ bool run_tc_phase(const Ctx& c, const Stage& st, const CUtensorMap* maps, TcState& ts, int stage,
@@ -2649,6 +2810,8 @@ __device__ bool run_tc_phase(const Ctx& c, const Stage& st, const CUtensorMap* m
     ts.m_tile = m_tile;
     ok = (r >> 32) != 0;
     if (prof) prof[4] = global_ns();
+  } else if (warp == 2 || warp == 3) {
+    if (st.has_bg) run_bg_items(c, st);
   } else if (warp >= 4) {
     EpiRing er = ts.er;
     const uint64_t r = tc_epilogue<PM>(c, st, ts, ts.e_tile, prof, &er);
@@ -2916,7 +3079,8 @@ __device__ __forceinline__ void persistent_body(const Params& p, const CUtensorM
           base += c.tasks[ti].n_items;
           ++ti;
         }
-        run_item(c, c.tasks[ti], g - base, s_work);
+        // (a bg task ran beside the tiles; without tiles it runs here)
+        if (!(c.tasks[ti].bg && st.n_tc_items > 0 && tc)) run_item(c, c.tasks[ti], g - base, s_work);
       }
     }
     asm volatile("fence.proxy.async.global;" ::: "memory");

@@ -216,6 +216,7 @@ void tk_options_default(tk_options* opt) {
   opt->sm_count = 0;
   opt->barrier_timeout_s = 2.0;
   opt->split_k = 1;
+  opt->overlap_reductions = 1;
 }
 
 tk_status tk_program_create(const tk_program_desc* desc, const tk_options* opt_in, int device, tk_program** out) {
@@ -234,6 +235,8 @@ tk_status tk_program_create(const tk_program_desc* desc, const tk_options* opt_i
     return fail(TK_ERR_INVALID, "tile_n must be 0, 64, 128, 224 or 256");
   if (opt.epi_stage_bytes < 0) return fail(TK_ERR_INVALID, "epi_stage_bytes must be >= 0");
   if (opt.cta_pairs < 0 || opt.cta_pairs > 2) return fail(TK_ERR_INVALID, "cta_pairs must be 0, 1 or 2");
+  if (opt.overlap_reductions < 0 || opt.overlap_reductions > 2)
+    return fail(TK_ERR_INVALID, "overlap_reductions must be 0, 1 or 2");
 
   int sms = opt.sm_count > 0 ? opt.sm_count : 152;
   if (device >= 0) {
@@ -491,6 +494,7 @@ tk_status tk_plan_task(const tk_program* p, int32_t index, tk_task_info* info) {
   r.staged_epilogue = t.epi_stage != 0;
   r.side_output = t.has_side != 0;
   r.staged_depth = t.epi_stage ? t.epi_depth + ((t.epi_stage & 16) ? 16 : 0) : 0;
+  r.beside_tiles = t.bg != 0;
   r.numel = t.numel;
   *info = r;
   return TK_OK;

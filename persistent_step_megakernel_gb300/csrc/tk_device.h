@@ -239,6 +239,10 @@ struct alignas(16) Task {
   // the splits in order and applies the epilogue.
   int32_t k_splits;
   int32_t kb_split;
+  // A reduction run by warps 2 and 3 while the stage's tensor-core tiles run
+  // (same additions in the same order as after the tiles): the 16-bit type
+  // of its operand (TK_BF16 or TK_F16); 0: after the tiles.
+  int32_t bg;
 };
 
 struct Stage {
@@ -252,7 +256,7 @@ struct Stage {
   // planner's estimate of one tile's time in items of the stage; 0: plain
   // round-robin after the tiles).
   int32_t light_items;
-  int32_t pad;
+  int32_t has_bg;            // some task runs beside the tiles (Task::bg)
 };
 
 // A stage whose descriptors fit these bounds is copied into shared memory

@@ -393,3 +393,22 @@ def test_forward_gemms_take_224_wide_tiles_where_they_fill_whole_waves():
     forced = _tc_tasks(S.mlp_step_program(S.CONFIGS["c2"], export="state"), tile_n=224)
     assert {t["tile_n"] for n, t in forced.items() if n.startswith("z")} == {224}
     assert {t["tile_n"] for n, t in forced.items() if not n.startswith("z")} == {256}
+
+
+def test_reductions_run_beside_long_tiles_where_they_fit():
+    # C5: the loss and the four bias gradients run on warps 2-3 beside the
+    # 4096^3 GEMM tiles; C2's short tiles keep theirs after the tiles unless
+    # forced; option 0 keeps every reduction after the tiles
+    def beside(name, **opts):
+        prog = S.mlp_step_program(S.CONFIGS[name], export="state")
+        h = B.tk_program_create(prog, B.options(sm_count=152, **opts), device=-1)
+        try:
+            tasks = [B.tk_plan_task(h, i) for i in range(B.tk_plan_stats_get(h)["tasks"])]
+        finally:
+            B.tk_program_destroy(h)
+        return sorted(prog.operations[t["op_index"]].name for t in tasks if t["beside_tiles"])
+    assert beside("c5") == ["gb1", "gb2", "gb3", "gb4", "loss"]
+    assert beside("c5", overlap_reductions=0) == []
+    assert beside("c2") == []
+    assert beside("c2", overlap_reductions=2) == ["gb1", "gb2", "gb3", "loss"]
+    assert beside("c1", overlap_reductions=2) == []          # no tensor-core stage

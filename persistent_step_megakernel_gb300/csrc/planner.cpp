@@ -2226,18 +2226,19 @@ class Planner {
       S.task_end = int(plan.tasks.size());
       // a stage's compiled row and column reductions run on warps 2 and 3
       // while its tensor-core tiles run (the same additions in the same
-      // order), as long as they fit in the tiles' time: one warp streams an
-      // item at ~4 GB/s (+2 us), a block's tiles take ~0.4 us per 64-deep k
-      // block each (+2 us); only beside long tiles (15 or more k blocks)
+      // order), as long as they fit in 90 % of the tiles' time: one warp
+      // streams an item at ~2 GB/s (+1 us), a block's tiles take ~0.4 us per
+      // 64-deep k block each (+4 us of epilogue); only beside long tiles (15
+      // or more k blocks)
       if (S.n_tc_items > 0 && opt_.overlap_reductions) {
         double tile_us = 0.0;
         for (int i = S.task_begin; i < S.task_end; ++i)
-          if (plan.tasks[i].kind == tkd::T_GEMM_TC) tile_us = std::max(tile_us, 2.0 + 0.4 * plan.tasks[i].kb_split);
+          if (plan.tasks[i].kind == tkd::T_GEMM_TC) tile_us = std::max(tile_us, 4.0 + 0.4 * plan.tasks[i].kb_split);
         const double units = pair_ ? sms_ / 2 : sms_;
         const double tiles_us = std::ceil(S.n_tc_items / units) * tile_us;
         // (2 runs every eligible reduction beside the tiles: for tests)
         const bool force = opt_.overlap_reductions == 2;
-        double bg_us = tile_us < 8.0 && !force ? 1e30 : 0.0;
+        double bg_us = tile_us < 10.0 && !force ? 1e30 : 0.0;
         for (int i = S.task_begin; i < S.task_end; ++i) {
           Task& t = plan.tasks[i];
           if ((t.kind == tkd::T_REDUCE_ROW || t.kind == tkd::T_REDUCE_COL) && t.vec == 8 &&
@@ -2245,9 +2246,9 @@ class Planner {
               t.n_items > 0) {
             // (a 16-bit operand: the kernel compiles these per type)
             const int dt = plan.refs[t.ref_begin + t.chain.load_ref[0]].dtype;
-            const double item_us = 2.0 + double(t.numel) / double(t.n_items) * 2.0 / 4e3;
+            const double item_us = 1.0 + double(t.numel) / double(t.n_items) * 2.0 / 2e3;
             const double us = std::ceil(t.n_items / (2.0 * sms_)) * item_us;
-            if ((dt == TK_BF16 || dt == TK_F16) && (force || bg_us + us <= 0.8 * tiles_us)) {
+            if ((dt == TK_BF16 || dt == TK_F16) && (force || bg_us + us <= 0.9 * tiles_us)) {
               t.bg = dt;
               S.has_bg = 1;
               bg_us += us;

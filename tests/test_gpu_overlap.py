@@ -54,6 +54,6 @@ def test_full_gemm_bound_step_reductions_beside_tiles_bit_identical():
     arrays = S.mlp_inputs(cfg, prog)
     beside, sb = run_on_device(prog, arrays, steps=2)      # the default plan
     after, _ = run_on_device(prog, arrays, steps=2, overlap_reductions=0)
-    assert sum(t["beside_tiles"] for t in sb.tasks()) == 5
+    assert sum(t["beside_tiles"] for t in sb.tasks()) == 4
     for spec, x, y in zip(prog.outputs, beside, after):
         assert torch.equal(x, y), spec.buffer

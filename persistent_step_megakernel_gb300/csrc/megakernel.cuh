@@ -2168,6 +2168,14 @@ __device__ __noinline__ bool tc_epilogue_staged(const Ctx c, const Task& t, int 
   const bool loads = st0 || st1 || sl;
   const bool own_out = !(st0 || st1) || su;  // buffers written without a load first
   const uint32_t ld_bytes = uint32_t(int(st0) + int(st1) + int(sl)) * kEpiBufBytes;
+  if (row0 >= t.m) {
+    // no output row in this warp's lane quarter (a short GEMM): nothing to
+    // load, compute or store; the accumulator is still waited for, so that
+    // this warp's release of it follows the MMAs that wrote it
+    const bool ok = mbar_wait(acc_bar, phase, c.timeout_ns);
+    if (ok && stamp) *stamp = global_ns();
+    return ok;
+  }
   if (er->task != task_id) {
     // the staging area takes this task's layout: every earlier store has
     // finished reading it first

@@ -209,6 +209,8 @@ typedef struct {
   int32_t staged_depth;        /* staged epilogue: 32-column chunks in flight per epilogue warp
                                   (2, 4 or 8; +16 when a side output has buffers of its own); 0 */
   int32_t beside_tiles;        /* reduction run while the stage's tensor-core tiles run */
+  int32_t folded;              /* partials sum run in the stage of its partials, by the warp that
+                                  adds a 256-column chunk's last part (n_items 0) */
   int64_t numel;               /* elements of the task's index space */
 } tk_task_info;
 

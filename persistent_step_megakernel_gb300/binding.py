@@ -72,7 +72,7 @@ class tk_plan_stats(ctypes.Structure):
 class tk_task_info(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "stage", "kind", "op_index", "n_items", "form", "compiled_shape", "m", "n", "k", "tile_m", "tile_n",
-        "parts", "staged_epilogue", "side_output", "staged_depth", "beside_tiles")] + [("numel", ctypes.c_int64)]
+        "parts", "staged_epilogue", "side_output", "staged_depth", "beside_tiles", "folded")] + [("numel", ctypes.c_int64)]
 
 
 # (name, restype, argtypes) for every entry point of include/tk.h

@@ -816,10 +816,13 @@ __device__ __forceinline__ bool barrier_wait(const Ctx& c, unsigned target, int 
   return true;
 }
 
-// Last block out resets the counters for the next run.  Thread 0 only.
+// Last block out resets the counters for the next run (also the folded
+// finals' part counts, which a run that gave up may have left behind).
+// Thread 0 only.
 __device__ __forceinline__ void kernel_exit(const Ctx& c) {
   Header* h = c.hdr;
   if (atom_add_acq_rel(&h->exits, 1u) + 1u == gridDim.x) {
+    for (int i = 0; i < kFoldCounters; ++i) h->fold[i] = 0u;
     atomicExch(&h->count, 0u);
     atomicExch(&h->exits, 0u);
   }
@@ -2772,6 +2775,7 @@ __device__ __forceinline__ void bg_col_item(const Ctx& c, const Task& t, int ite
 // The kinds run beside the tiles: sums of a 16-bit operand (FK_L, a bias
 // gradient) and of its squares (FK_L_SQUARE, a squared-error loss), all
 // operand of the type t.bg says (the planner marks only those).
+__device__ __noinline__ void fold_arrive(const Ctx c, const Task& t, int item);
 __device__ __noinline__ void bg_item(const Ctx& c, const Task& t, int item) {
   const bool row = t.kind == T_REDUCE_ROW, bf = t.bg == TK_BF16;
   if (t.chain.fast == FK_L) {
@@ -2784,6 +2788,43 @@ __device__ __noinline__ void bg_item(const Ctx& c, const Task& t, int item) {
       bf ? bg_row_item<FK_L_SQUARE, TK_BF16>(c, t, item) : bg_row_item<FK_L_SQUARE, TK_F16>(c, t, item);
     else
       bf ? bg_col_item<FK_L_SQUARE, TK_BF16>(c, t, item) : bg_col_item<FK_L_SQUARE, TK_F16>(c, t, item);
+  }
+  if (t.fold) fold_arrive(c, t, item);
+}
+
+// A folded final pass (Task::fold): after a warp has written part p of
+// 256-column chunk ch, it counts the part; the warp that counts the chunk's
+// last part sums the chunk's parts and applies the final's chain, output by
+// output with the same additions in the same order as the final pass's
+// threads (lane l takes outputs 256 ch + 32 v + l, v = 0..7).  The parts are
+// read from L2: other blocks wrote them, each before a release of its count.
+__device__ __noinline__ void fold_arrive(const Ctx c, const Task& t, int item) {
+  const int lane = threadIdx.x & 31;
+  const int ch = item / t.parts;
+  __threadfence();
+  __syncwarp();
+  unsigned last = 0;
+  if (lane == 0) last = atom_add_acq_rel(&c.hdr->fold[t.fold_ctr + ch], 1u) + 1u == unsigned(t.parts);
+  last = __shfl_sync(0xffffffffu, last, 0);
+  __syncwarp();
+  if (!last) return;
+  const Task& f = c.tasks[t.fold - 1];
+  const float* part = reinterpret_cast<const float*>(c.ws) + f.scratch;
+  for (int v = 0; v < kThreads / 32; ++v) {
+    const int64_t o = int64_t(ch) * kThreads + v * 32 + lane;
+    if (o >= f.red_outer) break;
+    const float pre = post_operand(c, f, o);
+    const float* q = part + o * f.parts;
+    float acc = 0.0f;
+    for (int q0 = 0; q0 < f.parts; q0 += 8) {
+      float x[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) x[u] = q0 + u < f.parts ? __ldcg(q + q0 + u) : 0.0f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (q0 + u < f.parts) acc = __fadd_rn(acc, x[u]);
+    }
+    finish_reduction(c, f, o, acc, pre);
   }
 }
 

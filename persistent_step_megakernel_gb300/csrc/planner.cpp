@@ -2050,9 +2050,14 @@ class Planner {
   }
 
   std::vector<int> stage_of_;  // stage of each schedule position (last stage for split reductions)
+  // split reductions (by partials scratch offset) whose final pass could run
+  // in the stage of their partial sums: its writes (and reads) conflict with
+  // no other task of that stage
+  std::set<int64_t> fold_ok_;
 
   Plan lower_and_stage() {
     stage_of_.assign(schedule_.size(), 0);
+    fold_ok_.clear();
     Plan plan;
     std::vector<std::vector<Task>> stages(1);
     std::vector<Region> stage_reads, stage_writes;
@@ -2121,6 +2126,11 @@ class Planner {
           ++split;
           if (conflicts_pending(reads, {})) barrier();
           while (hazard(reads, {})) barrier();
+          // (tasks placed in this stage later never conflict with a pending
+          // final pass: they would start the next stage first)
+          if (ts[1].kind == tkd::T_REDUCE_FINAL && !ts[1].final_block &&
+              !hazard(ts[1].post.valid ? reads : std::vector<Region>{}, writes))
+            fold_ok_.insert(ts[1].scratch);
           stages.back().push_back(ts[0]);
           stage_reads.insert(stage_reads.end(), reads.begin(), reads.end());
           // the final pass also reads a reduction epilogue's operands
@@ -2198,7 +2208,11 @@ class Planner {
 
     // Flatten: tensor-core tasks first inside each stage.
     int tc_ops = 0;
-    for (auto& st : stages) {
+    int fold_used = 0;
+    std::vector<bool> emptied(stages.size(), false);
+    for (size_t si = 0; si < stages.size(); ++si) {
+      auto& st = stages[si];
+      if (emptied[si] && st.empty()) continue;  // its final passes all ran in the stage before
       std::stable_sort(st.begin(), st.end(), [](const Task& a, const Task& b) {
         return (a.kind == tkd::T_GEMM_TC) > (b.kind == tkd::T_GEMM_TC);
       });
@@ -2253,6 +2267,40 @@ class Planner {
               S.has_bg = 1;
               bg_us += us;
             }
+          }
+        }
+      }
+      // a split column reduction beside the tiles takes its final pass along
+      // (Task::fold): the warp adding a chunk's last part finishes the chunk,
+      // so the final's own stage (and barrier) can go when nothing else is in it
+      if (S.has_bg && si + 1 < stages.size()) {
+        for (int i = S.task_begin; i < S.task_end; ++i) {
+          const Task t = plan.tasks[i];
+          if (!t.bg || t.kind != tkd::T_REDUCE_COL || t.parts <= 1 || !fold_ok_.count(t.scratch)) continue;
+          auto& next = stages[si + 1];
+          auto it = std::find_if(next.begin(), next.end(), [&](const Task& f) {
+            return f.kind == tkd::T_REDUCE_FINAL && f.scratch == t.scratch && !f.final_block;
+          });
+          const int chunks = t.n_items / t.parts;
+          if (it == next.end() || it->n_items != chunks || fold_used + chunks > tkd::kFoldCounters) continue;
+          Task f = *it;
+          next.erase(it);
+          emptied[si + 1] = true;
+          f.stage = int(plan.stages.size());
+          f.folded = 1;
+          f.n_items = 0;  // run by the part items' warps only
+          plan.tasks.push_back(f);
+          plan.tasks[i].fold = int(plan.tasks.size());
+          plan.tasks[i].fold_ctr = fold_used;
+          fold_used += chunks;
+          S.task_end = int(plan.tasks.size());
+          if (f.code_len) {
+            S.code_lo = std::min(S.code_lo, f.code_begin);
+            S.code_hi = std::max(S.code_hi, f.code_begin + f.code_len);
+          }
+          if (f.n_refs) {
+            S.ref_lo = std::min(S.ref_lo, f.ref_begin);
+            S.ref_hi = std::max(S.ref_hi, f.ref_begin + f.n_refs);
           }
         }
       }

@@ -495,6 +495,7 @@ tk_status tk_plan_task(const tk_program* p, int32_t index, tk_task_info* info) {
   r.side_output = t.has_side != 0;
   r.staged_depth = t.epi_stage ? t.epi_depth + ((t.epi_stage & 16) ? 16 : 0) : 0;
   r.beside_tiles = t.bg != 0;
+  r.folded = t.folded != 0;
   r.numel = t.numel;
   *info = r;
   return TK_OK;

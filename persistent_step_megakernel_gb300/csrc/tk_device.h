@@ -243,6 +243,14 @@ struct alignas(16) Task {
   // (same additions in the same order as after the tiles): the 16-bit type
   // of its operand (TK_BF16 or TK_F16); 0: after the tiles.
   int32_t bg;
+  // A split column reduction run beside the tiles whose final pass runs in
+  // the same stage: fold = 1 + the index of that T_REDUCE_FINAL task (which
+  // has folded = 1 and no items of its own), 0: none.  The warp that adds
+  // the last part of a 256-column chunk (counter fold_ctr + chunk of the
+  // workspace header) sums the chunk's parts and applies the final's chain.
+  int32_t fold;
+  int32_t fold_ctr;
+  int32_t folded;
 };
 
 struct Stage {
@@ -297,8 +305,13 @@ struct Header {
   int status;           // 0, or the tk_status of the first failure
   int stage;            // stage of the first failure
   int abort;            // nonzero once any block gives up
-  int pad[59];
+  // parts added so far per 256-column chunk of the split reductions whose
+  // final pass is folded into their own stage (Task::fold_ctr); zero between
+  // runs (the last block to leave clears them)
+  unsigned int fold[59];
 };
+constexpr int kFoldCounters = 59;
+static_assert(sizeof(Header) == kHeaderUnits * 4, "the workspace header is kHeaderUnits floats");
 
 // Kernel arguments: io[i] is input i, io[kMaxIO + j] is output j.
 // Profile stamps per (stage, block): 0 stage begin, 1 barrier arrival,

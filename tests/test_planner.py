@@ -412,3 +412,35 @@ def test_reductions_run_beside_long_tiles_where_they_fit():
     assert beside("c2") == []
     assert beside("c2", overlap_reductions=2) == ["gb1", "gb2", "gb3", "loss"]
     assert beside("c1", overlap_reductions=2) == []          # no tensor-core stage
+
+
+def test_split_bias_gradient_finals_fold_into_their_partials_stage():
+    # C5: gb1..gb3 are split column sums beside the tiles; each one's final
+    # pass (the sum of its 19 parts and the SGD update of the bias) is run by
+    # the warp that adds a 256-column chunk's last part, in the same stage, so
+    # the stage that held only gb1's final pass goes; the loss (one output,
+    # a block-wide final) and gb4 (after the tiles) keep their final passes
+    def plan(**opts):
+        prog = S.mlp_step_program(S.CONFIGS["c5"], export="state")
+        h = B.tk_program_create(prog, B.options(sm_count=152, **opts), device=-1)
+        try:
+            stats = B.tk_plan_stats_get(h)
+            tasks = [B.tk_plan_task(h, i) for i in range(stats["tasks"])]
+        finally:
+            B.tk_program_destroy(h)
+        for t in tasks:
+            t["op"] = prog.operations[t["op_index"]].name
+        return stats, tasks
+    stats, tasks = plan()
+    assert stats["stages"] == 8 and stats["grid_barriers"] == 7
+    folded = {t["op"]: t for t in tasks if t["folded"]}
+    assert sorted(folded) == ["gb1", "gb2", "gb3"]
+    for name, f in folded.items():
+        (part,) = [t for t in tasks if t["op"] == name and t["kind"] == "reduce_col"]
+        assert f["kind"] == "reduce_final" and f["n_items"] == 0 and f["stage"] == part["stage"] and part["beside_tiles"]
+        assert part["n_items"] == 16 * part["parts"]
+    finals = sorted(t["op"] for t in tasks if t["kind"] == "reduce_final" and not t["folded"])
+    assert finals == ["gb4", "loss"]
+    # with every reduction after the tiles nothing folds
+    stats0, tasks0 = plan(overlap_reductions=0)
+    assert stats0["stages"] == 9 and not any(t["folded"] for t in tasks0)

@@ -57,3 +57,18 @@ def test_full_gemm_bound_step_reductions_beside_tiles_bit_identical():
     assert sum(t["beside_tiles"] for t in sb.tasks()) == 4
     for spec, x, y in zip(prog.outputs, beside, after):
         assert torch.equal(x, y), spec.buffer
+
+
+def test_every_reduction_beside_the_tiles_with_folded_finals_bit_identical():
+    # forced: gb4 beside the tiles too; the finals of gb4, gb3 and gb2 fold
+    # into their partials' stages (48 of the 59 chunk counters), gb1's does
+    # not fit and keeps a stage of its own
+    cfg = S.CONFIGS["c5"]
+    prog = S.mlp_step_program(cfg, export="state")
+    arrays = S.mlp_inputs(cfg, prog)
+    forced, sf = run_on_device(prog, arrays, steps=3, overlap_reductions=2)
+    after, _ = run_on_device(prog, arrays, steps=3, overlap_reductions=0)
+    folded = sorted(prog.operations[t["op_index"]].name for t in sf.tasks() if t["folded"])
+    assert folded == ["gb2", "gb3", "gb4"]
+    for spec, x, y in zip(prog.outputs, forced, after):
+        assert torch.equal(x, y), spec.buffer

@@ -444,3 +444,8 @@ def test_split_bias_gradient_finals_fold_into_their_partials_stage():
     # with every reduction after the tiles nothing folds
     stats0, tasks0 = plan(overlap_reductions=0)
     assert stats0["stages"] == 9 and not any(t["folded"] for t in tasks0)
+    # with every reduction beside the tiles gb4 folds too, and gb1's 16
+    # chunks no longer fit the 59 counters: it keeps its own final stage
+    stats2, tasks2 = plan(overlap_reductions=2)
+    assert sorted(t["op"] for t in tasks2 if t["folded"]) == ["gb2", "gb3", "gb4"]
+    assert stats2["stages"] == 9

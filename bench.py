@@ -14,8 +14,9 @@ events.  Beside it, for the headline and every other workload:
   * graph: the same batches captured once as a CUDA graph and replayed,
     median of >= 5 replays (the pages time graph-captured steps);
   * clocks: nvidia-smi samples taken while that workload's timed loops ran.
-`e2e` repeats the metric through the public API with host-resident batches:
-each step copies x (and y) from pinned host memory, runs the step and reads
+`e2e` repeats the metric through the public API with host-resident batches
+(tk_run_host): each step copies x (and y) from pinned host memory, overlapped
+with the previous step on the library's copy stream, runs the step and reads
 the loss back.  With N > 1 each rank runs an independent replica on its own
 GPU (the step has no data-parallel exchange), times are max-reduced over ranks
 and `value` sums the replicas.
@@ -331,29 +332,30 @@ def measure(cfg, device, dist, steps, warmup, batches, batch_steps, graph=True, 
 
 
 def time_e2e(ctx, steps, device):
-    """Through the public API with host batches: H2D x(,y) -> step -> D2H loss."""
+    """Through the public API with host batches (tk_run_host): every step
+    copies its x (and y) from page-locked host memory, on the library's copy
+    stream while the previous step computes, runs the step and copies its
+    loss back to host memory; the timed region ends when the last loss is on
+    the host.  The batches alternate between two host copies."""
     import torch
     step, ins, outs, ws, prog = ctx["step"], ctx["ins"], ctx["outs"], ctx["ws"], ctx["prog"]
     names = [s.buffer for s in prog.inputs]
     batch = [names.index("x")] + ([names.index("y")] if "y" in names else [])
-    host = {i: ins[i].cpu().pin_memory() for i in batch}
-    loss_host = torch.empty_like(outs[0], device="cpu").pin_memory()
+    host = [[ins[i].cpu().pin_memory() for i in batch] for _ in range(2)]
+    alt = [torch.empty_like(ins[i]) for i in batch]
+    loss_host = torch.empty((steps,) + tuple(outs[0].shape), dtype=outs[0].dtype).pin_memory()
     stream = torch.cuda.current_stream(device)
-    h2d = sum(host[i].numel() * host[i].element_size() for i in batch)
-    d2h = loss_host.numel() * loss_host.element_size()
+    h2d = sum(t.numel() * t.element_size() for t in host[0])
+    d2h = outs[0].numel() * outs[0].element_size()
 
-    def one():
-        for i in batch:
-            ins[i].copy_(host[i], non_blocking=True)
-        step.run(ins, outs, ws)
-        loss_host.copy_(outs[0], non_blocking=True)
+    def run(n):
+        step.run_host(ins, outs, ws, batch, alt, [host[s & 1] for s in range(n)], [0],
+                      [[loss_host[s]] for s in range(n)], stream=stream)
         stream.synchronize()
 
-    for _ in range(3):
-        one()
+    run(3)
     t0 = time.perf_counter()
-    for _ in range(steps):
-        one()
+    run(steps)
     dt = time.perf_counter() - t0
     return steps / dt, h2d, d2h
 

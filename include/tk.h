@@ -321,6 +321,48 @@ tk_status tk_plan_task(const tk_program* program, int32_t index, tk_task_info* i
 tk_status tk_run_static(tk_program* program, const void* const* inputs, int32_t n_inputs,
                         void* const* outputs, int32_t n_outputs, void* stream);
 
+/* ---- Steps fed from host memory ------------------------------------------
+ * The pages time steps on batches already resident on the GPU; a training
+ * loop fed by a host-side loader also moves each batch to the device.  This
+ * entry point keeps that copy off the critical path.
+ *
+ * tk_run_host enqueues n_steps steps, each exactly like tk_run, where the
+ * batch inputs of step s are copied from host memory first and chosen outputs
+ * of step s are copied to host memory after it.  The host-to-device copies run
+ * on a second stream the program owns, into two device buffers per batch
+ * input used alternately (step s reads buffer s mod 2), so the copy of step
+ * s+1's batch overlaps step s; step s waits for its own copy, and the copy
+ * into a buffer waits for the step that last read it.
+ *
+ *   batch[b], b < n_batch: the index of the b-th batch input.  A batch input
+ *     is not the target of an in-place output.  Its two device buffers are
+ *     inputs[batch[b]] (even steps) and batch_alt[b] (odd steps): each holds
+ *     the input's bytes (its tk_run extent), is 16-byte aligned and overlaps
+ *     no other buffer of the call.
+ *   host_batches[s * n_batch + b]: host address of step s's value of batch
+ *     input b, the same bytes as the device buffer.  Page-locked memory lets
+ *     the copy overlap the previous step; pageable memory also works, without
+ *     the overlap.
+ *   results[r], r < n_results: an output index; after step s the output's
+ *     bytes are copied to host_results[s * n_results + r] (on `stream`).
+ *   Every other argument as tk_run; in-place outputs carry the state from
+ *   step to step.
+ *
+ * Ownership: the caller owns every buffer; the program owns the copy stream
+ * and its events (released by tk_program_destroy).  Asynchronous on `stream`:
+ * the call returns once everything is enqueued, and the host buffers must
+ * stay valid and host_batches unchanged until `stream` has completed.  The
+ * copies into the first buffer wait for the work enqueued on `stream` before
+ * the call.  Errors found on the host (counts, NULL or misaligned pointers,
+ * aliasing, a batch input that is an in-place target) return before anything
+ * is enqueued; a CUDA error part-way returns TK_ERR_CUDA with earlier steps
+ * enqueued. */
+tk_status tk_run_host(tk_program* program, int32_t n_steps, const void* const* inputs, int32_t n_inputs,
+                      void* const* outputs, int32_t n_outputs, const int32_t* batch, int32_t n_batch,
+                      void* const* batch_alt, const void* const* host_batches, const int32_t* results,
+                      int32_t n_results, void* const* host_results, float* workspace,
+                      size_t workspace_elements, void* stream);
+
 /* Message of the last failing call on this thread ("" if none). */
 const char* tk_last_error(void);
 

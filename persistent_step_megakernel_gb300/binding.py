@@ -95,6 +95,11 @@ SIGNATURES = [
     ("tk_plan_task", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(tk_task_info)]),
     ("tk_run_static", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32,
                                      ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32, ctypes.c_void_p]),
+    ("tk_run_host", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32,
+                                   ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
+                                   ctypes.c_int32, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p),
+                                   ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, ctypes.POINTER(ctypes.c_void_p),
+                                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     ("tk_last_error", ctypes.c_char_p, []),
 ]
 
@@ -306,6 +311,24 @@ def tk_run_static(handle, input_ptrs, output_ptrs, stream: int = 0) -> None:
     ins = (ctypes.c_void_p * max(1, len(input_ptrs)))(*input_ptrs)
     outs = (ctypes.c_void_p * max(1, len(output_ptrs)))(*output_ptrs)
     check(lib().tk_run_static(handle, ins, len(input_ptrs), outs, len(output_ptrs), ctypes.c_void_p(stream)))
+
+
+def tk_run_host(handle, n_steps: int, input_ptrs, output_ptrs, batch, batch_alt_ptrs, host_batch_ptrs,
+                results, host_result_ptrs, workspace_ptr: int, workspace_elements: int, stream: int = 0) -> None:
+    """n_steps steps fed from host memory (tk_run_host in include/tk.h):
+    host_batch_ptrs[s * len(batch) + b] is step s's host copy of input
+    batch[b], host_result_ptrs[s * len(results) + r] receives output
+    results[r] after step s."""
+    P = ctypes.c_void_p
+    ins = (P * max(1, len(input_ptrs)))(*input_ptrs)
+    outs = (P * max(1, len(output_ptrs)))(*output_ptrs)
+    bt = (ctypes.c_int32 * max(1, len(batch)))(*batch)
+    alt = (P * max(1, len(batch_alt_ptrs)))(*batch_alt_ptrs)
+    hb = (P * max(1, len(host_batch_ptrs)))(*host_batch_ptrs)
+    rs = (ctypes.c_int32 * max(1, len(results)))(*results)
+    hr = (P * max(1, len(host_result_ptrs)))(*host_result_ptrs)
+    check(lib().tk_run_host(handle, n_steps, ins, len(input_ptrs), outs, len(output_ptrs), bt, len(batch), alt, hb,
+                            rs, len(results), hr, P(workspace_ptr), workspace_elements, P(stream)))
 
 
 def tk_last_error() -> str:

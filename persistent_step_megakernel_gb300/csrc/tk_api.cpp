@@ -32,9 +32,14 @@ struct tk_program {
   size_t dyn_smem = 0;
   void* d_table = nullptr;
   const tkd::Program* d_prog = nullptr;
-  // TMA descriptors of the last run and the base pointers they encode
-  std::vector<CUtensorMap> maps;
-  std::vector<const void*> map_bases;
+  // TMA descriptors of the last run and the base pointers they encode, and
+  // the set before it (host-fed steps alternate between two batch buffers)
+  std::vector<CUtensorMap> maps, maps_prev;
+  std::vector<const void*> map_bases, map_bases_prev;
+  // tk_run_host: the stream of the batch copies; events: copy into buffer k
+  // done (0, 1), step reading buffer k done (2, 3), entry (4)
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
   // optional per-stage stamps at the end of the workspace (float units)
   int64_t prof_offset = -1;
 };
@@ -154,6 +159,11 @@ tk_status encode_maps(tk_program* p, const void* const* inputs, void* const* out
     bases[i] = o.space == tkd::SP_IN ? inputs[o.slot] : o.space == tkd::SP_OUT ? outputs[o.slot] : ws;
   }
   if (bases == p->map_bases && p->maps.size() == ops.size()) return TK_OK;
+  if (bases == p->map_bases_prev && p->maps_prev.size() == ops.size()) {
+    p->maps.swap(p->maps_prev);
+    p->map_bases.swap(p->map_bases_prev);
+    return TK_OK;
+  }
   EncodeTiledFn fn = encoder();
   if (!fn) return fail(TK_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   std::vector<CUtensorMap> maps(ops.size());
@@ -180,6 +190,8 @@ tk_status encode_maps(tk_program* p, const void* const* inputs, void* const* out
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(TK_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string(int(r)) + ")");
   }
+  p->maps_prev.swap(p->maps);
+  p->map_bases_prev.swap(p->map_bases);
   p->maps.swap(maps);
   p->map_bases.swap(bases);
   return TK_OK;
@@ -322,9 +334,12 @@ tk_status tk_program_create(const tk_program_desc* desc, const tk_options* opt_i
 
 void tk_program_destroy(tk_program* p) {
   if (!p) return;
-  if (p->d_table) {
+  if (p->d_table || p->copy_stream) {
     DeviceGuard g(p->device);
-    cudaFree(p->d_table);
+    if (p->d_table) cudaFree(p->d_table);
+    for (cudaEvent_t e : p->ev)
+      if (e) cudaEventDestroy(e);
+    if (p->copy_stream) cudaStreamDestroy(p->copy_stream);
   }
   delete p;
 }
@@ -346,8 +361,11 @@ tk_status tk_workspace_init(const tk_program* p, float* ws, size_t n, void* stre
   return TK_OK;
 }
 
-tk_status tk_run(tk_program* p, const void* const* inputs, int32_t n_inputs, void* const* outputs, int32_t n_outputs,
-                 float* ws, size_t ws_elems, void* stream) {
+namespace {
+
+// Host-side checks of one step's buffers (tk_run's error contract).
+tk_status check_run(const tk_program* p, const void* const* inputs, int32_t n_inputs, void* const* outputs,
+                    int32_t n_outputs, const float* ws, size_t ws_elems) {
   if (!p) return fail(TK_ERR_INVALID, "program must not be NULL");
   if (p->device < 0) return fail(TK_ERR_DEVICE, "plan-only program (created with device -1)");
   const tkp::Plan& pl = p->plan;
@@ -393,7 +411,13 @@ tk_status tk_run(tk_program* p, const void* const* inputs, int32_t n_inputs, voi
       if (overlaps(written[a], range_of(inputs[i], pl.input_bytes[i])))
         return fail(TK_ERR_ALIAS, "execution buffers must not alias inputs or each other");
   }
+  return TK_OK;
+}
 
+// Launch one checked step on `stream`.
+tk_status launch_run(tk_program* p, const void* const* inputs, int32_t n_inputs, void* const* outputs,
+                     int32_t n_outputs, float* ws, void* stream) {
+  const tkp::Plan& pl = p->plan;
   tkd::Params prm{};
   prm.prog = p->d_prog;
   prm.ws = reinterpret_cast<char*>(ws);
@@ -417,6 +441,119 @@ tk_status tk_run(tk_program* p, const void* const* inputs, int32_t n_inputs, voi
   cudaError_t e = tk_kernel_launch(prm, maps, int(p->maps.size()), p->grid, p->dyn_smem,
                                    static_cast<cudaStream_t>(stream), p->plan.pair);
   if (e != cudaSuccess) return cuda_fail(e, "cooperative launch");
+  return TK_OK;
+}
+
+}  // namespace
+
+tk_status tk_run(tk_program* p, const void* const* inputs, int32_t n_inputs, void* const* outputs, int32_t n_outputs,
+                 float* ws, size_t ws_elems, void* stream) {
+  tk_status s = check_run(p, inputs, n_inputs, outputs, n_outputs, ws, ws_elems);
+  if (s != TK_OK) return s;
+  return launch_run(p, inputs, n_inputs, outputs, n_outputs, ws, stream);
+}
+
+tk_status tk_run_host(tk_program* p, int32_t n_steps, const void* const* inputs, int32_t n_inputs,
+                      void* const* outputs, int32_t n_outputs, const int32_t* batch, int32_t n_batch,
+                      void* const* batch_alt, const void* const* host_batches, const int32_t* results,
+                      int32_t n_results, void* const* host_results, float* ws, size_t ws_elems, void* stream) {
+  tk_status st = check_run(p, inputs, n_inputs, outputs, n_outputs, ws, ws_elems);
+  if (st != TK_OK) return st;
+  const tkp::Plan& pl = p->plan;
+  if (n_steps < 0 || n_batch < 0 || n_results < 0) return fail(TK_ERR_INVALID, "negative count");
+  if (n_batch > n_inputs) return fail(TK_ERR_INVALID, "more batch inputs than inputs");
+  if ((n_batch && (!batch || !batch_alt)) || (n_steps && n_batch && !host_batches) ||
+      (n_results && !results) || (n_steps && n_results && !host_results))
+    return fail(TK_ERR_INVALID, "NULL array");
+  std::vector<const void*> odd(inputs, inputs + n_inputs);
+  std::vector<Range> alt;
+  for (int b = 0; b < n_batch; ++b) {
+    const int i = batch[b];
+    if (i < 0 || i >= n_inputs) return fail(TK_ERR_INVALID, "batch index " + std::to_string(i) + " out of range");
+    for (int c = 0; c < b; ++c)
+      if (batch[c] == i) return fail(TK_ERR_INVALID, "batch input " + std::to_string(i) + " listed twice");
+    for (const auto& kv : pl.inplace)
+      if (kv.second == i) return fail(TK_ERR_INVALID, "batch input " + std::to_string(i) + " is an in-place target");
+    if (pl.input_bytes[i] > 0 && !batch_alt[b]) return fail(TK_ERR_INVALID, "batch_alt buffer is NULL");
+    if (reinterpret_cast<uintptr_t>(batch_alt[b]) % 16) return fail(TK_ERR_INVALID, "batch_alt pointers must be 16-byte aligned");
+    for (int s = 0; s < n_steps; ++s)
+      if (pl.input_bytes[i] > 0 && !host_batches[size_t(s) * n_batch + b])
+        return fail(TK_ERR_INVALID, "host batch of step " + std::to_string(s) + " is NULL");
+    odd[i] = batch_alt[b];
+    alt.push_back(range_of(batch_alt[b], pl.input_bytes[i]));
+  }
+  // the odd steps' buffers pass the same checks, and no second buffer overlaps
+  // a buffer of the even steps
+  st = check_run(p, odd.data(), n_inputs, outputs, n_outputs, ws, ws_elems);
+  if (st != TK_OK) return st;
+  for (const Range& r : alt)
+    for (int i = 0; i < n_inputs; ++i)
+      if (overlaps(r, range_of(inputs[i], pl.input_bytes[i])))
+        return fail(TK_ERR_ALIAS, "batch_alt buffers must not overlap another buffer");
+  for (int r = 0; r < n_results; ++r) {
+    if (results[r] < 0 || results[r] >= n_outputs) return fail(TK_ERR_INVALID, "result index out of range");
+    for (int s = 0; s < n_steps; ++s)
+      if (pl.output_bytes[results[r]] > 0 && !host_results[size_t(s) * n_results + r])
+        return fail(TK_ERR_INVALID, "host result of step " + std::to_string(s) + " is NULL");
+  }
+  if (n_steps == 0) return TK_OK;
+
+  DeviceGuard g(p->device);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (n_batch && !p->copy_stream) {
+    e = cudaStreamCreateWithFlags(&p->copy_stream, cudaStreamNonBlocking);
+    for (int k = 0; k < 5 && e == cudaSuccess; ++k) e = cudaEventCreateWithFlags(&p->ev[k], cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "creating the batch copy stream");
+  }
+  const cudaStream_t xs = p->copy_stream;
+  auto copy_batch = [&](int s) -> cudaError_t {
+    const int k = s & 1;
+    cudaError_t r = cudaSuccess;
+    // buffer k was last read by step s - 2
+    if (s >= 2) r = cudaStreamWaitEvent(xs, p->ev[2 + k], 0);
+    for (int b = 0; b < n_batch && r == cudaSuccess; ++b) {
+      const int i = batch[b];
+      if (pl.input_bytes[i] == 0) continue;
+      void* dst = const_cast<void*>(k ? odd[i] : inputs[i]);
+      r = cudaMemcpyAsync(dst, host_batches[size_t(s) * n_batch + b], size_t(pl.input_bytes[i]),
+                          cudaMemcpyHostToDevice, xs);
+    }
+    if (r == cudaSuccess) r = cudaEventRecord(p->ev[k], xs);
+    return r;
+  };
+  if (n_batch) {
+    // the first copies wait for the work already on `stream` (which may read
+    // either buffer)
+    e = cudaEventRecord(p->ev[4], cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(xs, p->ev[4], 0);
+    if (e == cudaSuccess) e = copy_batch(0);
+    if (e != cudaSuccess) return cuda_fail(e, "enqueueing the first batch copy");
+  }
+  for (int s = 0; s < n_steps; ++s) {
+    const int k = s & 1;
+    if (n_batch) {
+      if (s + 1 < n_steps) {
+        e = copy_batch(s + 1);
+        if (e != cudaSuccess) return cuda_fail(e, "enqueueing a batch copy");
+      }
+      e = cudaStreamWaitEvent(cs, p->ev[k], 0);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
+    }
+    st = launch_run(p, k ? odd.data() : inputs, n_inputs, outputs, n_outputs, ws, stream);
+    if (st != TK_OK) return st;
+    if (n_batch) {
+      e = cudaEventRecord(p->ev[2 + k], cs);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    }
+    for (int r = 0; r < n_results; ++r) {
+      const int j = results[r];
+      if (pl.output_bytes[j] == 0) continue;
+      e = cudaMemcpyAsync(host_results[size_t(s) * n_results + r], outputs[j], size_t(pl.output_bytes[j]),
+                          cudaMemcpyDeviceToHost, cs);
+      if (e != cudaSuccess) return cuda_fail(e, "enqueueing a result copy");
+    }
+  }
   return TK_OK;
 }
 

@@ -88,6 +88,43 @@ class TrainStep:
                  workspace.data_ptr(), workspace.numel(), self._stream(stream))
         return outputs
 
+    def run_host(self, inputs, outputs, workspace, batch, batch_alt, host_batches, results=(), host_results=(),
+                 stream=None):
+        """len(host_batches) steps fed from host memory: step s copies
+        host_batches[s][b] (a host tensor, page-locked for overlap) into the
+        device input named by batch[b] (an input index), alternating with
+        batch_alt[b] (a second device buffer like it), and copies output
+        results[r] to host_results[s][r] after the step.  The copy of step
+        s+1's batch overlaps step s (tk_run_host).  Asynchronous on `stream`:
+        every host tensor must stay alive until it completes."""
+        self.validate_inputs(inputs)
+        for j, (o, spec) in enumerate(zip(outputs, self.program.outputs)):
+            if (o.device != self.device or tuple(o.shape) != tuple(spec.shape)
+                    or o.dtype != TORCH_DTYPE[spec.dtype] or not o.is_contiguous()):
+                raise ValueError(f"tk: output {j} does not match compiled requirements")
+        if workspace.dtype != torch.float32 or not workspace.is_contiguous() or workspace.device != self.device:
+            raise ValueError("tk: workspace does not match compiled requirements")
+        batch, results = list(batch), list(results)
+        for b, i in enumerate(batch):
+            ref = inputs[i]
+            for t, where in [(batch_alt[b], ref.device)] + [(hb[b], torch.device("cpu")) for hb in host_batches]:
+                if (t.device != where or t.dtype != ref.dtype or tuple(t.shape) != tuple(ref.shape)
+                        or not t.is_contiguous()):
+                    raise ValueError(f"tk: batch buffer of input {i} does not match it")
+        for s, hr in enumerate(host_results):
+            for r, j in enumerate(results):
+                o = outputs[j]
+                if hr[r].device.type != "cpu" or hr[r].dtype != o.dtype or hr[r].numel() != o.numel():
+                    raise ValueError(f"tk: host result of output {j} at step {s} does not match it")
+        n_steps = len(host_batches) if batch else len(host_results)
+        if results and len(host_results) != n_steps:
+            raise ValueError("tk: one host result list per step")
+        B.tk_run_host(self.handle, n_steps, [t.data_ptr() for t in inputs], [o.data_ptr() for o in outputs], batch,
+                      [t.data_ptr() for t in batch_alt], [t.data_ptr() for hb in host_batches for t in hb], results,
+                      [t.data_ptr() for hr in host_results for t in hr], workspace.data_ptr(), workspace.numel(),
+                      self._stream(stream))
+        return outputs
+
     def launcher(self, inputs, outputs, workspace, stream=None):
         """A callable that runs one step on these buffers per call, with the
         checks of run() done once here (the buffers must stay alive)."""

@@ -35,7 +35,7 @@ def batches(prog, arrays, n, seed):
     return idx, out
 
 
-@pytest.mark.parametrize("key,n", [("c2", 5), ("c3", 4), ("c4", 3)])
+@pytest.mark.parametrize("key,n", [("c2", 5), ("c3", 4), ("c4", 3), ("c5", 3)])
 def test_host_fed_steps_bit_identical_to_steps_one_by_one(key, n):
     cfg = S.CONFIGS[key]
     prog = S.mlp_step_program(cfg, export="state")

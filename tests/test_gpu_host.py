@@ -116,3 +116,30 @@ def test_host_fed_steps_reject_bad_calls_before_enqueueing():
     assert step.status(ws)[0] == 0
     for a, t, s in zip(arrays, ins, prog.inputs):
         assert torch.equal(t, to_torch(a, s.dtype, "cuda")), s.buffer
+
+
+def test_host_fed_steps_without_batch_inputs_only_read_results_back():
+    # no batch input: the steps run on the resident inputs and only the loss
+    # of every step comes back; zero steps enqueue nothing
+    cfg = S.CONFIGS["c2"]
+    prog = S.mlp_step_program(cfg, export="state")
+    arrays = S.mlp_inputs(cfg, prog)
+    step = TrainStep(prog, 0)
+    ins = [to_torch(a, s.dtype, "cuda") for a, s in zip(arrays, prog.inputs)]
+    outs, ws = step.allocate(ins)
+    want = []
+    for _ in range(3):
+        step.run(ins, outs, ws)
+        want.append(outs[0].cpu())
+    step2 = TrainStep(prog, 0)
+    ins2 = [to_torch(a, s.dtype, "cuda") for a, s in zip(arrays, prog.inputs)]
+    outs2, ws2 = step2.allocate(ins2)
+    loss_host = torch.empty((3,) + tuple(outs2[0].shape), dtype=outs2[0].dtype).pin_memory()
+    step2.run_host(ins2, outs2, ws2, [], [], [], [0], [[loss_host[s]] for s in range(3)])
+    step2.run_host(ins2, outs2, ws2, [], [], [], [], [])
+    torch.cuda.synchronize()
+    assert step2.status(ws2)[0] == 0
+    for s in range(3):
+        assert torch.equal(loss_host[s], want[s]), s
+    for spec, x, y in zip(prog.outputs, outs2, outs):
+        assert torch.equal(x, y), spec.buffer
